@@ -1,0 +1,359 @@
+"""Python binding of libfmad.so, the GB300 flow-matching action decoder.
+
+Argument marshalling only: every step of the decoder runs in the library's CUDA
+kernels. PyTorch supplies device memory and streams. The functions keep the C
+names (include/fmad.h); they take torch tensors (or raw integer pointers) and
+raise FmError on a non-zero status. Loading fails loudly when the compiled
+library is missing: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "FmError", "lib", "load", "FmConfig", "make_config", "workspace_size", "policy_create",
+    "policy_destroy", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
+    "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status",
+    "kernel_count", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
+    "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "Policy", "DeviceWeights",
+    "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "COND_TIME", "COND_GIVEN",
+    "ABI_VERSION", "STATUS",
+]
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfmad.so")
+
+ABI_VERSION = 1
+FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
+FLAG_USE_GRAPH, FLAG_USE_PDL = 1, 2
+COND_TIME, COND_GIVEN = 0, 1
+STATUS = {0: "FM_OK", 1: "FM_ERR_INVALID_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_ALIGN",
+          4: "FM_ERR_WORKSPACE", 5: "FM_ERR_CUDA", 6: "FM_ERR_STATE_MISMATCH",
+          7: "FM_ERR_DEVICE", 8: "FM_ERR_UNSUPPORTED"}
+EXPORTS = [
+    "fm_status_string", "fm_last_error", "fm_workspace_size", "policy_create", "policy_destroy",
+    "fm_set_act_scales", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
+    "fm_state_size", "snapshot_state", "restore_state", "fm_device_status", "fm_test_kernel_count",
+    "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight", "fm_test_skinny_gemm",
+    "fm_test_consumer", "fm_test_layer",
+]
+
+
+class FmError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class FmConfig(ctypes.Structure):
+    _fields_ = [("abi_version", ctypes.c_int),
+                ("L", ctypes.c_int), ("S", ctypes.c_int), ("M", ctypes.c_int), ("d", ctypes.c_int),
+                ("H", ctypes.c_int), ("Hkv", ctypes.c_int), ("Dh", ctypes.c_int), ("F", ctypes.c_int),
+                ("P", ctypes.c_int), ("A", ctypes.c_int),
+                ("weight_fmt", ctypes.c_int), ("act_fmt", ctypes.c_int), ("cond_mode", ctypes.c_int),
+                ("rms_eps", ctypes.c_float), ("ksplit", ctypes.c_int * 4), ("flags", ctypes.c_uint)]
+
+
+class FmLayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_qkv", "w_o", "w_gu", "w_d", "gamma1", "gamma2", "w_mod", "b_mod")]
+
+
+class FmWeights(ctypes.Structure):
+    _fields_ = [("layers", ctypes.POINTER(FmLayerWeights))] + [
+        (n, ctypes.c_void_p) for n in
+        ("w_in", "b_in", "w_out", "b_out", "gamma_f", "w_mod_f", "b_mod_f", "conds")]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree libfmad.so (build it with __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "fm_status_string": (ctypes.c_char_p, [i]),
+        "fm_last_error": (ctypes.c_char_p, [vp]),
+        "fm_workspace_size": (i, [ctypes.POINTER(FmConfig), ctypes.POINTER(sz)]),
+        "policy_create": (i, [ctypes.POINTER(FmConfig), ctypes.POINTER(FmWeights), vp, vp, sz, vp,
+                              ctypes.POINTER(vp)]),
+        "policy_destroy": (i, [vp]),
+        "fm_set_act_scales": (i, [vp, vp, vp]),
+        "set_prefix_kv": (i, [vp, vp, vp, vp]),
+        "refresh_prefix": (i, [vp, i, i, vp, vp, vp]),
+        "decode_actions": (i, [vp, vp, vp, vp]),
+        "decode_actions_host": (i, [vp, vp, vp, vp]),
+        "fm_state_size": (i, [vp, ctypes.POINTER(sz)]),
+        "snapshot_state": (i, [vp, vp, sz, i, vp]),
+        "restore_state": (i, [vp, vp, sz, i, vp]),
+        "fm_device_status": (i, [vp, vp, ctypes.POINTER(i)]),
+        "fm_test_kernel_count": (i, [vp, ctypes.POINTER(i), ctypes.POINTER(i)]),
+        "fm_test_quant_e4m3": (i, [vp, ctypes.c_int64, ctypes.c_float, vp, vp]),
+        "fm_packed_weight_bytes": (i, [i, i, i, ctypes.POINTER(sz)]),
+        "fm_pack_weight": (i, [vp, vp, i, i, i, vp, vp, vp]),
+        "fm_test_skinny_gemm": (i, [vp, i, i, vp, i, i, i, i, vp, vp]),
+        "fm_test_consumer": (i, [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, i, vp]),
+        "fm_test_layer": (i, [vp, vp, i, i, vp, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str, policy=None):
+    if status != 0:
+        detail = load().fm_last_error(policy).decode(errors="replace")
+        raise FmError(status, where, detail)
+
+
+def make_config(cfg, flags: int = FLAG_USE_GRAPH | FLAG_USE_PDL, ksplit=(0, 0, 0, 0)) -> FmConfig:
+    """fm_config from an fm_synth.Config-like object."""
+    fmts = {"bf16": FMT_BF16, "fp8": FMT_FP8, "nvfp4": FMT_NVFP4}
+    c = FmConfig()
+    c.abi_version = ABI_VERSION
+    for k in ("L", "S", "M", "d", "H", "Hkv", "Dh", "F", "P", "A"):
+        setattr(c, k, int(getattr(cfg, k)))
+    c.weight_fmt = fmts[cfg.weight_fmt]
+    c.act_fmt = fmts[cfg.act_fmt]
+    c.cond_mode = COND_GIVEN if cfg.cond == "given" else COND_TIME
+    c.rms_eps = float(cfg.eps)
+    for i, s in enumerate(ksplit):
+        c.ksplit[i] = int(s)
+    c.flags = int(flags)
+    return c
+
+
+def workspace_size(cfg: FmConfig) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "fm_workspace_size")
+    return n.value
+
+
+def policy_create(cfg: FmConfig, weights: FmWeights, act_scales, workspace, ws_bytes: int, stream=None) -> int:
+    """act_scales: host float32 numpy array [L][4] (or None for BF16 activations)."""
+    import numpy as np
+    out = ctypes.c_void_p()
+    sc = None
+    if act_scales is not None:
+        act_scales = np.ascontiguousarray(act_scales, dtype=np.float32)
+        sc = act_scales.ctypes.data
+    _check(load().policy_create(ctypes.byref(cfg), ctypes.byref(weights), sc, _ptr(workspace), ws_bytes,
+                                _stream(stream), ctypes.byref(out)), "policy_create")
+    return out.value
+
+
+def policy_destroy(p: int):
+    _check(load().policy_destroy(p), "policy_destroy")
+
+
+def fm_set_act_scales(p: int, act_scales, stream=None):
+    import numpy as np
+    a = np.ascontiguousarray(act_scales, dtype=np.float32)
+    _check(load().fm_set_act_scales(p, a.ctypes.data, _stream(stream)), "fm_set_act_scales", p)
+
+
+def set_prefix_kv(p: int, k, v, stream=None):
+    _check(load().set_prefix_kv(p, _ptr(k), _ptr(v), _stream(stream)), "set_prefix_kv", p)
+
+
+def refresh_prefix(p: int, tok_begin: int, tok_end: int, k, v, stream=None):
+    _check(load().refresh_prefix(p, tok_begin, tok_end, _ptr(k), _ptr(v), _stream(stream)), "refresh_prefix", p)
+
+
+def decode_actions(p: int, noise, actions, stream=None):
+    _check(load().decode_actions(p, _ptr(noise), _ptr(actions), _stream(stream)), "decode_actions", p)
+
+
+def decode_actions_host(p: int, noise_host, actions_host, stream=None):
+    """noise_host / actions_host: pinned (or pageable) CPU float32 tensors."""
+    _check(load().decode_actions_host(p, _ptr(noise_host), _ptr(actions_host), _stream(stream)),
+           "decode_actions_host", p)
+
+
+def state_size(p: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_state_size(p, ctypes.byref(n)), "fm_state_size", p)
+    return n.value
+
+
+def snapshot_state(p: int, dst, nbytes: int, dst_on_device: bool, stream=None):
+    _check(load().snapshot_state(p, _ptr(dst), nbytes, int(dst_on_device), _stream(stream)), "snapshot_state", p)
+
+
+def restore_state(p: int, src, nbytes: int, src_on_device: bool, stream=None) -> int:
+    """Returns the status (FM_ERR_STATE_MISMATCH = 6 is an expected outcome, not raised)."""
+    st = load().restore_state(p, _ptr(src), nbytes, int(src_on_device), _stream(stream))
+    if st not in (0, 6):
+        _check(st, "restore_state", p)
+    return st
+
+
+def device_status(p: int, stream=None) -> int:
+    w = ctypes.c_int()
+    st = load().fm_device_status(p, _stream(stream), ctypes.byref(w))
+    if st not in (0, 7):
+        _check(st, "fm_device_status", p)
+    return w.value
+
+
+def kernel_count(p: int):
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(load().fm_test_kernel_count(p, ctypes.byref(a), ctypes.byref(b)), "fm_test_kernel_count", p)
+    return a.value, b.value
+
+
+def fm_test_quant_e4m3(x, scale: float, codes, stream=None):
+    _check(load().fm_test_quant_e4m3(_ptr(x), x.numel(), float(scale), _ptr(codes), _stream(stream)),
+           "fm_test_quant_e4m3")
+
+
+def fm_packed_weight_bytes(N: int, K: int, fmt: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_packed_weight_bytes(N, K, fmt, ctypes.byref(n)), "fm_packed_weight_bytes")
+    return n.value
+
+
+def fm_pack_weight(w, gamma, N: int, K: int, fmt: int, packed, scale_out, stream=None):
+    _check(load().fm_pack_weight(_ptr(w), _ptr(gamma), N, K, fmt, _ptr(packed), _ptr(scale_out),
+                                 _stream(stream)), "fm_pack_weight")
+
+
+def fm_test_skinny_gemm(a, M: int, K: int, w_packed, N: int, fmt: int, s: int, cluster_reduce: int,
+                        partials, stream=None):
+    _check(load().fm_test_skinny_gemm(_ptr(a), M, K, _ptr(w_packed), N, fmt, s, cluster_reduce,
+                                      _ptr(partials), _stream(stream)), "fm_test_skinny_gemm")
+
+
+def fm_test_consumer(partials, nparts: int, M: int, N: int, s_a, s_w, bias, x, gate, scale, shift,
+                     eps: float, s_q, q, act_fmt: int, stream=None):
+    _check(load().fm_test_consumer(_ptr(partials), nparts, M, N, _ptr(s_a), _ptr(s_w), _ptr(bias), _ptr(x),
+                                   _ptr(gate), _ptr(scale), _ptr(shift), float(eps), _ptr(s_q), _ptr(q),
+                                   act_fmt, _stream(stream)), "fm_test_consumer")
+
+
+def fm_test_layer(p: int, x_in, layer: int, step: int, x_out, q_out, stream=None):
+    _check(load().fm_test_layer(p, _ptr(x_in), layer, step, _ptr(x_out), _ptr(q_out), _stream(stream)),
+           "fm_test_layer", p)
+
+
+# ---------------------------------------------------------------- convenience owner
+
+class DeviceWeights:
+    """Device copies of a policy's raw parameters and the fm_weights struct pointing at them.
+
+    layers: list of per-layer dicts of numpy arrays ([out][in] fp32 GEMM weights,
+    gamma1/2, w_mod (bf16 values), b_mod); final: dict with w_in, b_in, w_out, b_out,
+    gamma_f, w_mod_f, b_mod_f; conds: [S][d] for cond == "given" workloads.
+    """
+
+    def __init__(self, cfg, layers, final, conds=None, device="cuda"):
+        import torch
+        self.device = torch.device(device)
+        to = lambda a, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(a)).to(self.device, dt)
+        bf = lambda a: to(a, torch.bfloat16)
+        self.tensors = []
+        self._lw = (FmLayerWeights * cfg.L)()
+        for l, d in enumerate(layers):
+            t = {k: to(d[k]) for k in ("w_qkv", "w_o", "w_gu", "w_d", "gamma1", "gamma2", "b_mod")}
+            t["w_mod"] = bf(d["w_mod"])
+            self.tensors.append(t)
+            for k in ("w_qkv", "w_o", "w_gu", "w_d", "gamma1", "gamma2", "w_mod", "b_mod"):
+                setattr(self._lw[l], k, t[k].data_ptr())
+        fin = {k: bf(final[k]) for k in ("w_in", "w_out", "w_mod_f")}
+        fin.update({k: to(final[k]) for k in ("b_in", "b_out", "gamma_f", "b_mod_f")})
+        if conds is not None:
+            fin["conds"] = to(conds)
+        self.tensors.append(fin)
+        w = FmWeights()
+        w.layers = self._lw
+        for k in ("w_in", "b_in", "w_out", "b_out", "gamma_f", "w_mod_f", "b_mod_f"):
+            setattr(w, k, fin[k].data_ptr())
+        w.conds = fin["conds"].data_ptr() if conds is not None else None
+        self.struct = w
+
+
+class Policy:
+    """Owns a policy's workspace and handle (and, optionally, its raw device weights).
+
+    weights: a DeviceWeights, or (layers, final) numpy dicts as DeviceWeights takes
+    them; the raw copies made here are released after create.
+    """
+
+    def __init__(self, cfg, layers=None, final=None, act_scales=None, conds=None,
+                 flags: int = FLAG_USE_GRAPH | FLAG_USE_PDL, ksplit=(0, 0, 0, 0), device="cuda",
+                 weights: "DeviceWeights | None" = None):
+        import torch
+        self.torch = torch
+        self.cfg = cfg
+        self.fmcfg = make_config(cfg, flags, ksplit)
+        self.device = torch.device(device)
+        own = weights is None
+        if own:
+            weights = DeviceWeights(cfg, layers, final, conds, device)
+        self.ws_bytes = workspace_size(self.fmcfg)
+        self.workspace = torch.empty(self.ws_bytes + 1024, dtype=torch.uint8, device=self.device)
+        off = (-self.workspace.data_ptr()) % 1024
+        self.ws_ptr = self.workspace.data_ptr() + off
+        self.handle = policy_create(self.fmcfg, weights.struct, act_scales, self.ws_ptr, self.ws_bytes)
+        if own:
+            del weights
+            torch.cuda.empty_cache()
+
+    def set_prefix_kv(self, k, v, stream=None):
+        set_prefix_kv(self.handle, k, v, stream)
+
+    def refresh_prefix(self, b, e, k, v, stream=None):
+        refresh_prefix(self.handle, b, e, k, v, stream)
+
+    def decode(self, noise, actions=None, stream=None):
+        if actions is None:
+            actions = self.torch.empty_like(noise)
+        decode_actions(self.handle, noise, actions, stream)
+        return actions
+
+    def close(self):
+        if getattr(self, "handle", None):
+            policy_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

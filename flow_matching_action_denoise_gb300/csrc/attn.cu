@@ -1,0 +1,359 @@
+// Attention of the action chunk over [persistent prefix KV cache; the chunk's own KV].
+//
+// The prefix cache holds the observation- and instruction-dependent keys and
+// values; it persists across decisions and is refreshed only when the
+// observation changes (news article "FlashRT-PAI", section "It optimises the
+// relay": reuse instruction-dependent results, refresh image-dependent ones).
+// Queries, keys and values of the chunk come from the merged QKV GEMM (blog post,
+// "CUDA Graph vs graph simplification": three projections sharing one input
+// become one wider GEMM); this kernel's prologue reduces its partial planes,
+// dequantises with fp32(s_a * s_w) and rounds to bf16.
+//
+// Layout of the work: the G = H/Hkv query heads that share a KV head are stacked
+// into rows r = h_local * M + m, so one K/V tile serves all of them. A CTA owns
+// 64 stacked rows (4 warps x 16) and one contiguous slice of the keys; the
+// slices of one row tile form a thread-block cluster. Each warp runs QK^T and PV
+// on bf16 tensor cores (m16n8k16, fp32 accumulate) with an online softmax over
+// 64-key chunks; the unnormalised partial (O, running max, running sum) of each
+// CTA is combined across the cluster through distributed shared memory in fixed
+// slice order, normalised, and quantised with the static output scale.
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fm {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kRows = 64;        // stacked query rows per CTA
+constexpr int kDh = 128;         // head dim
+constexpr int kLds = kDh + 8;    // bf16 elements per shared row (272 B: conflict-free ldmatrix)
+constexpr int kChunk = 64;       // keys per online-softmax chunk
+constexpr int kMaxSplit = 8;     // portable cluster size
+
+struct KParams {
+  const float* y;
+  int nparts, ldy;
+  const float* sa;
+  const float* sw;
+  const __nv_bfloat16* kpre;
+  const __nv_bfloat16* vpre;
+  void* out;
+  const float* s_out;
+  int out_fp8;
+  int M, P, H, Hkv, G, kc, nsplit;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Sum of the partial planes of one 4-column group, times the dequant scale.
+__device__ __forceinline__ float4 reduce_parts4(const float* __restrict__ y, int nparts, size_t plane, size_t off,
+                                                float ds) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < nparts; ++p) {
+    const float4 v = *reinterpret_cast<const float4*>(y + p * plane + off);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  return make_float4(acc.x * ds, acc.y * ds, acc.z * ds, acc.w * ds);
+}
+
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+__global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem);
+  __nv_bfloat16* sK = sQ + kRows * kLds;
+  __nv_bfloat16* sV = sK + p.kc * kLds;
+  float* sML = reinterpret_cast<float*>(sV + p.kc * kLds);   // [64][2]: running max (log2 units), sum
+  float* sO = reinterpret_cast<float*>(sK);                   // [64][128] fp32, aliases K/V after compute
+
+  const int split = blockIdx.x;
+  const int qt = blockIdx.y;
+  const int g = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int nkeys = p.P + p.M;
+  const int t0 = split * p.kc;
+  const int nvalid = min(p.kc, nkeys - t0);
+  const size_t plane = static_cast<size_t>(p.M) * p.ldy;
+
+  pdl_trigger();
+
+  // ---- prefix keys/values of this slice (written before this graph ran)
+  for (int idx = tid; idx < p.kc * 16; idx += kThreads) {
+    const int i = idx >> 4, c = idx & 15;
+    const int t = t0 + i;
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+    if (t < p.P) {
+      const size_t off = (static_cast<size_t>(t) * p.Hkv + g) * kDh + c * 8;
+      kv = *reinterpret_cast<const uint4*>(p.kpre + off);
+      vv = *reinterpret_cast<const uint4*>(p.vpre + off);
+    }
+    if (t < p.P || t >= nkeys) {
+      *reinterpret_cast<uint4*>(sK + i * kLds + c * 8) = kv;
+      *reinterpret_cast<uint4*>(sV + i * kLds + c * 8) = vv;
+    }
+  }
+  const float ds = __fmul_rn(*p.sa, *p.sw);
+  pdl_wait();
+
+  // ---- the chunk's own keys/values (rows P..P+M-1 of the key axis)
+  const int c_lo = max(t0, p.P), c_hi = min(t0 + p.kc, nkeys);
+  for (int idx = tid; idx < (c_hi > c_lo ? (c_hi - c_lo) : 0) * 32; idx += kThreads) {
+    const int t = c_lo + (idx >> 5), e4 = idx & 31;
+    const int m = t - p.P, i = t - t0;
+    const size_t base = static_cast<size_t>(m) * p.ldy;
+    const float4 kf = reduce_parts4(p.y, p.nparts, plane, base + (p.H + g) * kDh + e4 * 4, ds);
+    const float4 vf = reduce_parts4(p.y, p.nparts, plane, base + (p.H + p.Hkv + g) * kDh + e4 * 4, ds);
+    store_bf16x4(sK + i * kLds + e4 * 4, kf);
+    store_bf16x4(sV + i * kLds + e4 * 4, vf);
+  }
+  // ---- stacked query rows
+  for (int idx = tid; idx < kRows * 32; idx += kThreads) {
+    const int r = idx >> 5, e4 = idx & 31;
+    const int R = qt * kRows + r;
+    float4 qf = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (R < p.G * p.M) {
+      const int hl = R / p.M, m = R % p.M;
+      const int h = g * p.G + hl;
+      qf = reduce_parts4(p.y, p.nparts, plane, static_cast<size_t>(m) * p.ldy + h * kDh + e4 * 4, ds);
+    }
+    store_bf16x4(sQ + r * kLds + e4 * 4, qf);
+  }
+  __syncthreads();
+
+  // ---- per-warp flash attention over this slice
+  const int warp = tid >> 5, lane = tid & 31;
+  const int r0 = warp * 16;
+  uint32_t qf[8][4];
+  {
+    const uint32_t qbase = smem_u32(sQ + (r0 + (lane & 15)) * kLds + (lane >> 4) * 8);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) ldsm_x4(qbase + ks * 32, qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+  }
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY};
+  float lrow[2] = {0.f, 0.f};
+  const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh));   // log2(e) / sqrt(Dh)
+  const int nchunks = (nvalid + kChunk - 1) / kChunk;
+  const int mat = lane >> 3;
+
+  for (int ch = 0; ch < nchunks; ++ch) {
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      const int key = ch * kChunk + np * 16 + (lane & 7) + (mat >> 1) * 8;
+      const uint32_t kbase = smem_u32(sK + key * kLds + (mat & 1) * 8);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + ks * 32, b0, b1, b2, b3);
+        mma_bf16(s[2 * np], qf[ks], b0, b1);
+        mma_bf16(s[2 * np + 1], qf[ks], b2, b3);
+      }
+    }
+    // scale, mask, online softmax
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = ch * kChunk + nt * 8 + (lane & 3) * 2 + (e & 1);
+        s[nt][e] = key < nvalid ? s[nt][e] * kscale : -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+      }
+    }
+    float corr[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+      const float mnew = fmaxf(mrow[hr], mx[hr]);
+      corr[hr] = exp2f(mrow[hr] - mnew);
+      mrow[hr] = mnew;
+      lrow[hr] *= corr[hr];
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pe = exp2f(s[nt][e] - mrow[e >> 1]);
+        s[nt][e] = pe;
+        lrow[e >> 1] += pe;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= corr[0];
+      o[i][1] *= corr[0];
+      o[i][2] *= corr[1];
+      o[i][3] *= corr[1];
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t a[4];
+      a[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+      a[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+      a[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      a[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      const int key = ch * kChunk + kk * 16 + (lane & 7) + (mat & 1) * 8;
+      const uint32_t vbase = smem_u32(sV + key * kLds + (mat >> 1) * 8);
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + dp * 32, b0, b1, b2, b3);
+        mma_bf16(o[2 * dp], a, b0, b1);
+        mma_bf16(o[2 * dp + 1], a, b2, b3);
+      }
+    }
+  }
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
+    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
+  }
+
+  // ---- partial result of this slice into shared memory (over the K/V tiles)
+  __syncthreads();
+  {
+    const int rlo = r0 + (lane >> 2), rhi = rlo + 8;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<float2*>(sO + rlo * kDh + col) = make_float2(o[nt][0], o[nt][1]);
+      *reinterpret_cast<float2*>(sO + rhi * kDh + col) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if ((lane & 3) == 0) {
+      sML[rlo * 2] = mrow[0];
+      sML[rlo * 2 + 1] = lrow[0];
+      sML[rhi * 2] = mrow[1];
+      sML[rhi * 2 + 1] = lrow[1];
+    }
+  }
+
+  // ---- combine the slices of this row tile across the cluster, fixed slice order
+  cluster_sync_all();
+  {
+    const int rank = static_cast<int>(cluster_rank());
+    const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
+    const int e = tid;   // head-dim column
+    const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
+    const uint32_t o_local = smem_u32(sO);
+    const uint32_t ml_local = smem_u32(sML);
+    for (int r = rank * rows_per; r < min(kRows, (rank + 1) * rows_per); ++r) {
+      const int R = qt * kRows + r;
+      if (R >= p.G * p.M) break;
+      float mq[kMaxSplit], lq[kMaxSplit];
+      float mstar = -INFINITY;
+      for (int q = 0; q < p.nsplit; ++q) {
+        mq[q] = ld_dsmem_f32(map_dsmem(ml_local + r * 8, q));
+        lq[q] = ld_dsmem_f32(map_dsmem(ml_local + r * 8 + 4, q));
+        mstar = fmaxf(mstar, mq[q]);
+      }
+      float lsum = 0.f, acc = 0.f;
+      for (int q = 0; q < p.nsplit; ++q) {
+        const float w = exp2f(mq[q] - mstar);
+        lsum += w * lq[q];
+        acc += w * ld_dsmem_f32(map_dsmem(o_local + (r * kDh + e) * 4, q));
+      }
+      const float val = acc / lsum;
+      const int hl = R / p.M, m = R % p.M;
+      const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e;
+      if (p.out_fp8) {
+        static_cast<uint8_t*>(p.out)[oidx] =
+            static_cast<uint8_t>(__nv_cvt_float_to_fp8(val * rs, __NV_SATFINITE, __NV_E4M3));
+      } else {
+        static_cast<__nv_bfloat16*>(p.out)[oidx] = __float2bfloat16_rn(val);
+      }
+    }
+  }
+  cluster_sync_all();   // peers may still be reading this CTA's partial
+}
+
+}  // namespace
+
+void attn_plan(int M, int P, int* kc, int* nsplit) {
+  const int keys = P + M;
+  int ns = (keys + kChunk - 1) / kChunk;
+  if (ns > kMaxSplit) ns = kMaxSplit;
+  int per = (keys + ns - 1) / ns;
+  per = (per + kChunk - 1) / kChunk * kChunk;
+  *kc = per;
+  *nsplit = (keys + per - 1) / per;
+}
+
+size_t attn_smem_bytes(int kc) {
+  return 128 + static_cast<size_t>(kRows) * kLds * 2 + 2 * static_cast<size_t>(kc) * kLds * 2 + kRows * 2 * 4;
+}
+
+cudaError_t attn_configure() {
+  return cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
+  KParams p;
+  p.y = a.yqkv;
+  p.nparts = a.nparts;
+  p.ldy = (a.H + 2 * a.Hkv) * kDh;
+  p.sa = a.sa;
+  p.sw = a.sw;
+  p.kpre = a.kpre;
+  p.vpre = a.vpre;
+  p.out = a.out;
+  p.s_out = a.s_out;
+  p.out_fp8 = a.out_fp8;
+  p.M = a.M;
+  p.P = a.P;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = a.H / a.Hkv;
+  p.kc = a.kc;
+  p.nsplit = a.nsplit;
+  const int rows = p.G * p.M;
+  const dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>((rows + kRows - 1) / kRows),
+                  static_cast<unsigned>(a.Hkv));
+  LaunchOpts lo = o;
+  lo.cluster = dim3(static_cast<unsigned>(a.nsplit), 1, 1);
+  return launch(attn_kernel, grid, dim3(kThreads), attn_smem_bytes(a.kc), lo, p);
+}
+
+}  // namespace fm

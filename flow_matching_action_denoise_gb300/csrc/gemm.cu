@@ -1,0 +1,427 @@
+// Skinny GEMM with K-split on tcgen05 tensor cores, and weight packing.
+//
+// Computes partial[j][m][n] = sum_{k in slice j} A[m][k] * W[n][k] for an action
+// chunk of M <= 256 rows (blog post "Embodied inference acceleration", section
+// "Small-M GEMM": C = sum_j A_j W_j over s K slices, FP32 partial sums reduced
+// before the consumer's own transform).
+//
+// GB300 mapping ("swap-AB"): the weight tile is the MMA's A operand (M = 128 rows
+// of W, i.e. 128 output columns n), the activations are the MMA's B operand
+// (N = M rounded up to 16), so the tiny row count costs nothing in tensor-core
+// shape and the weights - the only large operand - stream through TMA in
+// 16 KB boxes (128 rows x 128 bytes of K) into a multi-stage shared-memory ring.
+// One elected thread issues the TMA loads, another issues tcgen05.mma into a
+// TMEM accumulator; four warps read TMEM back. CTAs (n-tile, slice j) of
+// consecutive slices form a thread-block cluster of size cs that sums its
+// partials in fixed slice order through distributed shared memory, so only
+// s/cs partial planes go to global memory (deterministic, no atomics).
+// Weight loads are issued before the programmatic-dependent-launch wait: they do
+// not depend on the previous kernel, so they overlap its tail.
+
+#include <cudaTypedefs.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fm {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTileN = 128;                      // weight rows per CTA (MMA M)
+constexpr int kBlockBytes = 128;                 // K bytes per pipeline block (one swizzle row)
+constexpr int kMaxStages = 8;
+constexpr int kWTileBytes = kTileN * kBlockBytes;   // 16 KB
+constexpr size_t kStageCap = 196 * 1024;         // shared-memory budget for the ring
+constexpr size_t kCtrlBytes = 256;
+
+struct KParams {
+  float* out;
+  int M, N;
+  int nkb_total, nkb_cta;
+  int n_pad, stages, cs;
+  int* err;
+};
+
+__host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
+  uint32_t p = lo;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                               const __grid_constant__ CUtensorMap tmA,
+                                                               const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
+  __shared__ int s_abort;
+  __shared__ int s_issued;
+
+  const int stages = p.stages;
+  const uint32_t a_tile_bytes = static_cast<uint32_t>(p.n_pad) * kBlockBytes;
+  uint8_t* w_tiles = smem;
+  uint8_t* a_tiles = smem + static_cast<size_t>(stages) * kWTileBytes;
+  const size_t main_bytes = static_cast<size_t>(stages) * (kWTileBytes + a_tile_bytes);
+  const size_t red_bytes = p.cs > 1 ? static_cast<size_t>(p.n_pad) * kTileN * sizeof(float) : 0;
+  uint8_t* ctrl = smem + align_up(main_bytes > red_bytes ? main_bytes : red_bytes, 1024);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* done = empty + kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nt = blockIdx.x;
+  const int j = blockIdx.y;
+  const uint32_t ncols = pow2_at_least(static_cast<uint32_t>(p.n_pad), 32);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_issued = 0;
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Dependents may start only once this CTA holds its TMEM: a later GEMM's CTAs that
+  // wait for this grid must never be able to take the columns this CTA still needs.
+  pdl_trigger();
+
+  const int a_elems_per_block = kFp8 ? kBlockBytes : kBlockBytes / 2;
+  const int kb0 = j * p.nkb_cta;
+
+  if (threadIdx.x == 0) {
+    // ---------------- TMA producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_a = l2_policy_evict_last();
+    const int wrow0 = (nt * p.nkb_total + kb0) * kTileN;
+    const uint32_t tx = kWTileBytes + a_tile_bytes;
+    for (int i = 0; i < stages; ++i) {
+      mbar_arrive_expect_tx(&full[i], tx);
+      tma_load_2d(w_tiles + static_cast<size_t>(i) * kWTileBytes, &tmW, &full[i], 0, wrow0 + i * kTileN, pol_w);
+    }
+    pdl_wait();   // activations are written by the previous kernel
+    for (int i = 0; i < stages; ++i)
+      tma_load_2d(a_tiles + static_cast<size_t>(i) * a_tile_bytes, &tmA, &full[i], (kb0 + i) * a_elems_per_block,
+                  0, pol_a);
+    int issued = stages;
+    for (int kb = stages; kb < p.nkb_cta; ++kb) {
+      const int slot = kb % stages;
+      const uint32_t use = static_cast<uint32_t>(kb / stages);
+      if (!mbar_wait(&empty[slot], (use - 1) & 1)) {
+        atomicOr(p.err, kErrPipelineTimeout);
+        s_abort = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[slot], tx);
+      tma_load_2d(w_tiles + static_cast<size_t>(slot) * kWTileBytes, &tmW, &full[slot], 0, wrow0 + kb * kTileN,
+                  pol_w);
+      tma_load_2d(a_tiles + static_cast<size_t>(slot) * a_tile_bytes, &tmA, &full[slot],
+                  (kb0 + kb) * a_elems_per_block, 0, pol_a);
+      ++issued;
+    }
+    s_issued = issued;
+  } else if (threadIdx.x == 32) {
+    // ---------------- MMA issuer
+    const uint32_t idesc = make_idesc(kFp8, kTileN, static_cast<uint32_t>(p.n_pad));
+    for (int kb = 0; kb < p.nkb_cta; ++kb) {
+      const int slot = kb % stages;
+      const uint32_t use = static_cast<uint32_t>(kb / stages);
+      if (!mbar_wait(&full[slot], use & 1)) {
+        atomicOr(p.err, kErrPipelineTimeout);
+        s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t wa = smem_u32(w_tiles + static_cast<size_t>(slot) * kWTileBytes);
+      const uint32_t aa = smem_u32(a_tiles + static_cast<size_t>(slot) * a_tile_bytes);
+#pragma unroll
+      for (int k = 0; k < kBlockBytes / 32; ++k) {
+        tc_mma<kFp8>(tmem, sw128_kmajor_desc(wa + k * 32), sw128_kmajor_desc(aa + k * 32), idesc,
+                     (kb > 0 || k > 0) ? 1u : 0u);
+      }
+      tc_commit(&empty[slot]);
+    }
+    tc_commit(done);
+  }
+
+  // ---------------- epilogue: TMEM -> registers -> global (or cluster reduction)
+  pdl_wait();
+  if (!mbar_wait(done, 0)) {
+    atomicOr(p.err, kErrPipelineTimeout);
+    s_abort = 1;
+  }
+  tc_fence_after();
+  __syncthreads();
+  const bool abort = s_abort != 0;
+  const int n_local = warp * 32 + lane;   // TMEM lane == weight row within the tile
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  float* red = reinterpret_cast<float*>(smem);   // [n_pad][128], reuses the drained ring
+  const size_t ncol = static_cast<size_t>(nt) * kTileN + n_local;
+  __syncwarp();   // tcgen05.ld is warp-collective
+  for (int c = 0; c < p.n_pad; c += 16) {
+    float v[16];
+    tmem_ld16(t_row + static_cast<uint32_t>(c), v);
+    if (p.cs == 1) {
+      if (!abort) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int m = c + i;
+          if (m < p.M) p.out[(static_cast<size_t>(j) * p.M + m) * p.N + ncol] = v[i];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) red[(c + i) * kTileN + n_local] = v[i];
+    }
+  }
+  if (p.cs > 1) {
+    cluster_sync_all();
+    const int rank = static_cast<int>(cluster_rank());
+    const int part = j / p.cs;
+    const int rows_per = (p.M + p.cs - 1) / p.cs;
+    const int m_lo = rank * rows_per;
+    const int m_hi = min(p.M, m_lo + rows_per);
+    if (!abort) {
+      for (int m = m_lo; m < m_hi; ++m) {
+        const uint32_t local = smem_u32(&red[m * kTileN + n_local]);
+        float acc = 0.f;
+        for (int q = 0; q < p.cs; ++q) acc += ld_dsmem_f32(map_dsmem(local, static_cast<uint32_t>(q)));
+        p.out[(static_cast<size_t>(part) * p.M + m) * p.N + ncol] = acc;
+      }
+    }
+    cluster_sync_all();   // keep this CTA's shared memory alive until every peer has read it
+  }
+
+  // On an abandoned pipeline, let copies already in flight land before the CTA exits.
+  if (abort && threadIdx.x == 0) {
+    const int issued = s_issued;
+    for (int slot = 0; slot < stages && slot < issued; ++slot) {
+      const uint32_t last_use = static_cast<uint32_t>((issued - 1 - slot) / stages);
+      mbar_wait(&full[slot], last_use & 1, 100000000ull);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+// ---------------------------------------------------------------- packing kernels
+
+__global__ void amax_fold_kernel(const float* __restrict__ w, const float* __restrict__ gamma, int N, int K,
+                                 unsigned* __restrict__ amax) {
+  const size_t total = static_cast<size_t>(N) * K;
+  float m = 0.f;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float g = gamma ? gamma[i % K] : 1.0f;
+    m = fmaxf(m, fabsf(__fmul_rn(w[i], g)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax, __float_as_uint(m));   // non-negative floats order as uints
+}
+
+__global__ void scale_from_amax_kernel(const unsigned* __restrict__ amax, float* __restrict__ scale) {
+  const float a = __uint_as_float(*amax);
+  *scale = a > 0.f ? a / 448.0f : 1.0f;
+}
+
+__global__ void set_one_kernel(float* p) { *p = 1.0f; }
+
+// FP8: one thread writes 16 bytes (16 codes) of a [128][128]-byte tile.
+__global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __restrict__ gamma, int N, int K,
+                                const float* __restrict__ scale, uint8_t* __restrict__ out) {
+  const size_t chunks = static_cast<size_t>(N) * K / 16;
+  const size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  if (c >= chunks) return;
+  const float rs = 1.0f / *scale;
+  const size_t o = c * 16;
+  const int nkb = K / 128;
+  const size_t tile = o / kWTileBytes;
+  const int within = static_cast<int>(o % kWTileBytes);
+  const int r = within / 128, cb = within % 128;
+  const int ntile = static_cast<int>(tile / nkb), kb = static_cast<int>(tile % nkb);
+  const size_t n = static_cast<size_t>(ntile) * 128 + r;
+  const int k0 = kb * 128 + cb;
+  alignas(16) uint8_t codes[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float g = gamma ? gamma[k0 + i] : 1.0f;
+    const float v = __fmul_rn(__fmul_rn(w[n * K + k0 + i], g), rs);
+    codes[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+  }
+  *reinterpret_cast<uint4*>(out + o) = *reinterpret_cast<const uint4*>(codes);
+}
+
+// BF16: one thread writes 16 bytes (8 values) of a [128][64]-element tile.
+__global__ void pack_bf16_kernel(const float* __restrict__ w, const float* __restrict__ gamma, int N, int K,
+                                 __nv_bfloat16* __restrict__ out) {
+  const size_t chunks = static_cast<size_t>(N) * K / 8;
+  const size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  if (c >= chunks) return;
+  const size_t e = c * 8;   // element offset in the packed buffer
+  const int nkb = K / 64;
+  const size_t tile = e / (128 * 64);
+  const int within = static_cast<int>(e % (128 * 64));
+  const int r = within / 64, ce = within % 64;
+  const int ntile = static_cast<int>(tile / nkb), kb = static_cast<int>(tile % nkb);
+  const size_t n = static_cast<size_t>(ntile) * 128 + r;
+  const int k0 = kb * 64 + ce;
+  alignas(16) __nv_bfloat16 vals[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float g = gamma ? gamma[k0 + i] : 1.0f;
+    vals[i] = __float2bfloat16_rn(__fmul_rn(w[n * K + k0 + i], g));
+  }
+  *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(vals);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_outer) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16) return false;
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * static_cast<cuuint64_t>(elem_bytes)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
+  if (M < 1 || M > 256 || N <= 0 || K <= 0 || N % 128 || K % 128) return FM_ERR_SHAPE;
+  const int eb = fp8 ? 1 : 2;
+  const int nkb_total = K * eb / kBlockBytes;
+  if (s < 1 || nkb_total % s) return FM_ERR_SHAPE;
+  if (cs < 1 || cs > 8 || (cs & (cs - 1)) || s % cs) return FM_ERR_SHAPE;
+  g->M = M;
+  g->N = N;
+  g->K = K;
+  g->fp8 = fp8;
+  g->s = s;
+  g->cs = cs;
+  g->n_pad = (M + 15) / 16 * 16;
+  g->nkb_total = nkb_total;
+  g->nkb_cta = nkb_total / s;
+  const size_t stage_bytes = kWTileBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;
+  int st = static_cast<int>(kStageCap / stage_bytes);
+  st = std::min(st, kMaxStages);
+  st = std::min(st, g->nkb_cta);
+  g->stages = std::max(st, 1);
+  const size_t main_bytes = g->stages * stage_bytes;
+  const size_t red_bytes = cs > 1 ? static_cast<size_t>(g->n_pad) * kTileN * sizeof(float) : 0;
+  g->smem = 1024 + align_up(std::max(main_bytes, red_bytes), 1024) + kCtrlBytes;
+  return FM_OK;
+}
+
+bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g) {
+  const int eb = g.fp8 ? 1 : 2;
+  return make_tmap_2d(map, a, eb, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), kBlockBytes / eb,
+                      static_cast<uint32_t>(g.n_pad));
+}
+
+bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g) {
+  const int eb = g.fp8 ? 1 : 2;
+  const uint64_t rows = static_cast<uint64_t>(g.N / kTileN) * g.nkb_total * kTileN;
+  return make_tmap_2d(map, packed, eb, kBlockBytes / eb, rows, kBlockBytes / eb, kTileN);
+}
+
+cudaError_t gemm_configure() {
+  cudaError_t e = cudaFuncSetAttribute(skinny_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       227 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(skinny_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
+                        const LaunchOpts& o) {
+  KParams p;
+  p.out = out;
+  p.M = g.M;
+  p.N = g.N;
+  p.nkb_total = g.nkb_total;
+  p.nkb_cta = g.nkb_cta;
+  p.n_pad = g.n_pad;
+  p.stages = g.stages;
+  p.cs = g.cs;
+  p.err = err;
+  LaunchOpts lo = o;
+  lo.cluster = dim3(1, static_cast<unsigned>(g.cs), 1);
+  const dim3 grid(static_cast<unsigned>(g.N / kTileN), static_cast<unsigned>(g.s), 1);
+  if (g.fp8) return launch(skinny_gemm_kernel<true>, grid, dim3(kThreads), g.smem, lo, tmW, tmA, p);
+  return launch(skinny_gemm_kernel<false>, grid, dim3(kThreads), g.smem, lo, tmW, tmA, p);
+}
+
+size_t packed_weight_bytes(int N, int K, int fmt) {
+  if (fmt == FM_FMT_FP8) return static_cast<size_t>(N) * K;
+  if (fmt == FM_FMT_BF16) return static_cast<size_t>(N) * K * 2;
+  return 0;
+}
+
+cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
+                        unsigned* amax_scratch, cudaStream_t st) {
+  const int threads = 256;
+  if (fmt == FM_FMT_FP8) {
+    cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    amax_fold_kernel<<<1184, threads, 0, st>>>(w, gamma, N, K, amax_scratch);
+    scale_from_amax_kernel<<<1, 1, 0, st>>>(amax_scratch, scale_out);
+    const size_t chunks = static_cast<size_t>(N) * K / 16;
+    pack_fp8_kernel<<<static_cast<unsigned>((chunks + threads - 1) / threads), threads, 0, st>>>(
+        w, gamma, N, K, scale_out, static_cast<uint8_t*>(packed));
+    return cudaGetLastError();
+  }
+  if (fmt == FM_FMT_BF16) {
+    set_one_kernel<<<1, 1, 0, st>>>(scale_out);
+    const size_t chunks = static_cast<size_t>(N) * K / 8;
+    pack_bf16_kernel<<<static_cast<unsigned>((chunks + threads - 1) / threads), threads, 0, st>>>(
+        w, gamma, N, K, static_cast<__nv_bfloat16*>(packed));
+    return cudaGetLastError();
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fm

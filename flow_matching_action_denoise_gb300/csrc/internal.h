@@ -1,0 +1,160 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "fmad.h"
+
+namespace fm {
+
+// Error-word bits set by kernels that abandon a bounded wait.
+constexpr int kErrPipelineTimeout = 1;
+
+// ---------------------------------------------------------------- launching
+struct LaunchOpts {
+  cudaStream_t stream = nullptr;
+  bool pdl = false;      // Programmatic Dependent Launch attribute
+  dim3 cluster{1, 1, 1};
+};
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchOpts& o,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = o.stream;
+  cudaLaunchAttribute attrs[2];
+  unsigned n = 0;
+  if (o.pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (o.cluster.x * o.cluster.y * o.cluster.z > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = o.cluster.x;
+    attrs[n].val.clusterDim.y = o.cluster.y;
+    attrs[n].val.clusterDim.z = o.cluster.z;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------- tensor maps
+// 2-D tensor map over a row-major [outer][inner] array of 1- or 2-byte elements,
+// 128-byte swizzle, zero fill out of bounds. Returns false on failure.
+bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_outer);
+
+// ---------------------------------------------------------------- skinny GEMM
+struct GemmShape {
+  int M, N, K;
+  int fp8;        // 1: E4M3 operands, 0: BF16 operands
+  int s;          // K-split
+  int cs;         // cluster size reducing consecutive slices (divides s)
+  int n_pad;      // MMA N (M rounded up to 16)
+  int nkb_total;  // 128-byte K blocks
+  int nkb_cta;    // K blocks per CTA
+  int stages;     // pipeline stages in shared memory
+  size_t smem;    // dynamic shared memory bytes
+};
+// Fills the derived fields; returns FM_OK or FM_ERR_SHAPE.
+int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g);
+// Activation tensor map: A [M][K], box = 128 bytes x n_pad rows.
+bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
+// Weight tensor map over the packed tiles of a [N][K] weight.
+bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g);
+cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
+                        const LaunchOpts& o);
+cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
+
+// Packing
+size_t packed_weight_bytes(int N, int K, int fmt);
+cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
+                        unsigned* amax_scratch, cudaStream_t st);
+
+// ---------------------------------------------------------------- row kernels
+struct RowArgs {
+  int M, N;
+  // residual update from GEMM partials: x += gate * (sum_p parts[p] * fp32(sa*sw) + bias)
+  const float* parts;
+  int nparts;
+  const float* sa;
+  const float* sw;
+  const float* bias;
+  const float* gate;
+  float* x;
+  const float* x_src;   // if non-null, x is first loaded from here (single-layer entry)
+  // Euler tail: a += dt * (AdaRMSNorm_f(x) * gamma_f . w_out^T + b_out)
+  int do_tail;
+  const float* scale_f;
+  const float* shift_f;
+  const float* gamma_f;
+  const __nv_bfloat16* w_out;
+  const float* b_out;
+  float* a;
+  int A;
+  float dt;
+  // head: x = a . w_in^T + b_in
+  int do_head;
+  const __nv_bfloat16* w_in;
+  const float* b_in;
+  // AdaRMSNorm + quantise into q
+  int do_quant;
+  const float* scale;
+  const float* shift;
+  const float* sq;
+  void* q;
+  int q_fp8;
+  float eps;
+};
+cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o);
+
+struct GegluArgs {
+  int M, F;
+  const float* parts;   // [nparts][M][2F]
+  int nparts;
+  const float* sa;
+  const float* sw;
+  const float* sq;
+  void* q;   // [M][F]
+  int q_fp8;
+};
+cudaError_t geglu_launch(const GegluArgs& g, const LaunchOpts& o);
+
+struct AttnArgs {
+  const float* yqkv;   // [nparts][M][(H+2Hkv)*Dh]
+  int nparts;
+  const float* sa;
+  const float* sw;
+  const __nv_bfloat16* kpre;   // [P][Hkv][Dh] of this layer
+  const __nv_bfloat16* vpre;
+  void* out;                   // [M][H*Dh] codes
+  const float* s_out;
+  int out_fp8;
+  int M, P, H, Hkv;
+  int kc;       // keys per split (multiple of 64)
+  int nsplit;   // splits = cluster size (<= 8)
+};
+void attn_plan(int M, int P, int* kc, int* nsplit);
+size_t attn_smem_bytes(int kc);
+cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
+cudaError_t attn_configure();
+
+// ---------------------------------------------------------------- create-time kernels
+cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, cudaStream_t st);
+cudaError_t modtable_launch(const double* conds, int S, int d, const __nv_bfloat16* w_mod, const float* b_mod,
+                            int nout, float* out, size_t out_step_stride, cudaStream_t st);
+cudaError_t quant_e4m3_launch(const float* x, int64_t n, float scale, uint8_t* codes, cudaStream_t st);
+cudaError_t scale_mul_launch(const float* a, const float* b, float* out, int n, cudaStream_t st);
+
+}  // namespace fm

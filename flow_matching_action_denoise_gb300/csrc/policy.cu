@@ -1,0 +1,914 @@
+// Policy object and C ABI of libfmad.so.
+//
+// A policy owns the plan of one decision - (L layers x 8 kernels) x S steps plus
+// one step-head kernel - recorded once as a CUDA graph whose kernel nodes carry
+// Programmatic Dependent Launch edges (news article "FlashRT-PAI", section "It
+// optimises the relay": launch overlap; blog post "Embodied inference
+// acceleration", section "CUDA Graph vs graph simplification": replay with the
+// same parameters and addresses, new inputs written into agreed buffers).
+// The caller's workspace is carved into named persistent buffers (the execution
+// contract): packed weights and their scales, the static activation scales, the
+// modulation table, the prefix KV cache, the noise/action buffer and the
+// activation ping buffers. The execution-state capsule (snapshot / restore) is
+// an in-process copy of the per-session regions, bound to the plan hash and the
+// workspace address.
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using fm::LaunchOpts;
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+constexpr uint64_t kCapsuleMagic = 0x3153504143444d46ull;   // "FMDCAPS1"
+
+thread_local std::string g_last_error;
+
+}  // namespace
+
+// Device error word of the standalone building-block entry points (the policy
+// keeps its own in its workspace).
+__device__ int fm_standalone_err;
+
+namespace {
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t total = 0;
+  std::vector<size_t> wpk;   // [L*4] packed weights
+  size_t wscale, ascale, mod, modf, w_in, b_in, w_out, b_out, gamma_f, kcache, vcache, a, x, q, o, q2, mc;
+  size_t y[4];
+  size_t err, amax, conds;
+  size_t kv_bytes, a_bytes, scale_bytes;
+  size_t take(size_t bytes) {
+    const size_t off = total;
+    total = align_up(total + std::max<size_t>(bytes, 1));
+    return off;
+  }
+};
+
+struct Derived {
+  int nqkv;
+  int act_bytes;
+  int fp8;
+  fm::GemmShape gs[4];
+  int gN[4], gK[4];
+  int attn_kc, attn_nsplit;
+};
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      n = 148;
+  }
+  return n;
+}
+
+int auto_split(int tiles, int nkb) {
+  const int target = num_sms() * 3 / 4;
+  for (int s = 1; s <= nkb; ++s)
+    if (nkb % s == 0 && tiles * s >= target) return s;
+  return nkb;
+}
+
+int cluster_for(int s) {
+  int c = 8;
+  while (c > 1 && s % c) c >>= 1;
+  return c;
+}
+
+int validate(const fm_config* c, std::string* why) {
+  if (!c) {
+    *why = "config is NULL";
+    return FM_ERR_INVALID_ARG;
+  }
+  if (c->abi_version != FM_ABI_VERSION) {
+    *why = "abi_version mismatch";
+    return FM_ERR_INVALID_ARG;
+  }
+  const bool fmt_ok = (c->weight_fmt == FM_FMT_FP8 && c->act_fmt == FM_FMT_FP8) ||
+                      (c->weight_fmt == FM_FMT_BF16 && c->act_fmt == FM_FMT_BF16) ||
+                      (c->weight_fmt == FM_FMT_NVFP4 && c->act_fmt == FM_FMT_FP8);
+  if (!fmt_ok) {
+    *why = "unsupported weight/activation format pair";
+    return FM_ERR_INVALID_ARG;
+  }
+  if (c->weight_fmt == FM_FMT_NVFP4) {
+    *why = "NVFP4 weights are not implemented in this build";
+    return FM_ERR_UNSUPPORTED;
+  }
+  if (c->cond_mode != FM_COND_TIME && c->cond_mode != FM_COND_GIVEN) {
+    *why = "bad cond_mode";
+    return FM_ERR_INVALID_ARG;
+  }
+  if (c->L < 1 || c->S < 1 || c->M < 1 || c->M > 256 || c->A < 1 || c->A > 32 || c->P < 0 || c->Dh != 128 ||
+      c->H < 1 || c->Hkv < 1 || c->H % c->Hkv || c->d % 128 || c->d <= 0 || c->F % 128 || c->F <= 0 ||
+      c->d > 12288) {
+    *why = "shape precondition violated (d, F multiples of 128, d <= 12288, Dh == 128, H % Hkv == 0, "
+           "1 <= M <= 256, 1 <= A <= 32)";
+    return FM_ERR_SHAPE;
+  }
+  if (!(c->rms_eps > 0.f)) {
+    *why = "rms_eps must be positive";
+    return FM_ERR_INVALID_ARG;
+  }
+  return FM_OK;
+}
+
+int derive(const fm_config* c, Derived* dv, std::string* why) {
+  dv->nqkv = (c->H + 2 * c->Hkv) * c->Dh;
+  dv->fp8 = c->act_fmt == FM_FMT_FP8;
+  dv->act_bytes = dv->fp8 ? 1 : 2;
+  const int N[4] = {dv->nqkv, c->d, 2 * c->F, c->d};
+  const int K[4] = {c->d, c->H * c->Dh, c->d, c->F};
+  for (int g = 0; g < 4; ++g) {
+    dv->gN[g] = N[g];
+    dv->gK[g] = K[g];
+    const int nkb = K[g] * dv->act_bytes / 128;
+    const int s = c->ksplit[g] > 0 ? c->ksplit[g] : auto_split(N[g] / 128, nkb);
+    const int st = fm::gemm_plan(c->M, N[g], K[g], dv->fp8, s, cluster_for(s), &dv->gs[g]);
+    if (st != FM_OK) {
+      char buf[160];
+      snprintf(buf, sizeof buf, "GEMM %d: split %d does not divide %d K-blocks (N=%d, K=%d)", g, s, nkb, N[g], K[g]);
+      *why = buf;
+      return st;
+    }
+  }
+  fm::attn_plan(c->M, c->P, &dv->attn_kc, &dv->attn_nsplit);
+  return FM_OK;
+}
+
+Layout make_layout(const fm_config* c, const Derived& dv) {
+  Layout ly;
+  const int L = c->L, d = c->d, S = c->S, M = c->M;
+  const int wfmt = c->weight_fmt;
+  ly.wpk.resize(static_cast<size_t>(L) * 4);
+  for (int l = 0; l < L; ++l)
+    for (int g = 0; g < 4; ++g) ly.wpk[l * 4 + g] = ly.take(fm::packed_weight_bytes(dv.gN[g], dv.gK[g], wfmt));
+  ly.scale_bytes = static_cast<size_t>(L) * 4 * sizeof(float);
+  ly.wscale = ly.take(ly.scale_bytes);
+  ly.ascale = ly.take(ly.scale_bytes);
+  ly.mod = ly.take(static_cast<size_t>(S) * L * 6 * d * sizeof(float));
+  ly.modf = ly.take(static_cast<size_t>(S) * 2 * d * sizeof(float));
+  ly.w_in = ly.take(static_cast<size_t>(d) * c->A * 2);
+  ly.b_in = ly.take(static_cast<size_t>(d) * 4);
+  ly.w_out = ly.take(static_cast<size_t>(d) * c->A * 2);
+  ly.b_out = ly.take(static_cast<size_t>(c->A) * 4);
+  ly.gamma_f = ly.take(static_cast<size_t>(d) * 4);
+  ly.kv_bytes = static_cast<size_t>(L) * c->P * c->Hkv * c->Dh * 2;
+  ly.kcache = ly.take(ly.kv_bytes);
+  ly.vcache = ly.take(ly.kv_bytes);
+  ly.a_bytes = static_cast<size_t>(M) * c->A * 4;
+  ly.a = ly.take(ly.a_bytes);
+  ly.x = ly.take(static_cast<size_t>(M) * d * 4);
+  ly.q = ly.take(static_cast<size_t>(M) * d * dv.act_bytes);
+  ly.o = ly.take(static_cast<size_t>(M) * c->H * c->Dh * dv.act_bytes);
+  ly.q2 = ly.take(static_cast<size_t>(M) * d * dv.act_bytes);
+  ly.mc = ly.take(static_cast<size_t>(M) * c->F * dv.act_bytes);
+  for (int g = 0; g < 4; ++g)
+    ly.y[g] = ly.take(static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4);
+  ly.err = ly.take(64);
+  ly.amax = ly.take(64);
+  ly.conds = ly.take(static_cast<size_t>(S) * d * sizeof(double));
+  return ly;
+}
+
+uint64_t fnv(uint64_t h, const void* p, size_t n) {
+  const unsigned char* b = static_cast<const unsigned char*>(p);
+  for (size_t i = 0; i < n; ++i) {
+    h ^= b[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+struct CapsuleHeader {
+  uint64_t magic;
+  uint32_t abi, header_bytes;
+  uint64_t plan_hash;
+  uint64_t ws_base;
+  uint64_t kv_bytes, a_bytes, scale_bytes;
+  int32_t L, P, Hkv, Dh, M, A;
+  uint64_t decisions;
+  uint8_t pad[256 - 8 - 8 - 8 - 8 - 24 - 24 - 8];
+};
+static_assert(sizeof(CapsuleHeader) == 256, "capsule header is 256 bytes");
+
+}  // namespace
+
+struct fm_policy {
+  fm_config cfg;
+  Derived dv;
+  Layout ly;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  std::vector<CUtensorMap> tmW;   // [L*4]
+  CUtensorMap tmA[4];
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  uint64_t plan_hash = 0;
+  uint64_t decisions = 0;
+  std::string err;
+  CapsuleHeader hdr;   // staging for device-side snapshots (must outlive the async copy)
+
+  template <typename T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+  float* mod(int k, int l, int i) const {
+    return at<float>(ly.mod) + ((static_cast<size_t>(k) * cfg.L + l) * 6 + i) * cfg.d;
+  }
+  float* modf(int k, int i) const { return at<float>(ly.modf) + (static_cast<size_t>(k) * 2 + i) * cfg.d; }
+  float* wscale(int l, int g) const { return at<float>(ly.wscale) + l * 4 + g; }
+  float* ascale(int l, int i) const { return at<float>(ly.ascale) + l * 4 + i; }
+  int* errw() const { return at<int>(ly.err); }
+};
+
+namespace {
+
+int fail(fm_policy* p, int status, const std::string& why) {
+  if (p)
+    p->err = why;
+  else
+    g_last_error = why;
+  return status;
+}
+
+int cuda_fail(fm_policy* p, cudaError_t e, const char* where) {
+  std::string s = std::string(where) + ": " + cudaGetErrorString(e);
+  return fail(p, FM_ERR_CUDA, s);
+}
+
+#define FM_CUDA(p, call)                                       \
+  do {                                                         \
+    cudaError_t e_ = (call);                                   \
+    if (e_ != cudaSuccess) return cuda_fail((p), e_, #call);   \
+  } while (0)
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+// ---------------------------------------------------------------- the plan
+// Kernels of layer l at step k. tail: -1 = next layer's norm (layer (l+1) mod L),
+// otherwise the last layer of a decision step (Euler tail; head of step tail
+// if tail < S).
+cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const LaunchOpts& o) {
+  const fm_config& c = p->cfg;
+  const Derived& dv = p->dv;
+  cudaError_t e;
+  int* err = p->errw();
+  float* y[4];
+  for (int g = 0; g < 4; ++g) y[g] = p->at<float>(p->ly.y[g]);
+  const int fp8 = dv.fp8;
+
+  e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], y[0], err, o);
+  if (e != cudaSuccess) return e;
+
+  fm::AttnArgs at;
+  at.yqkv = y[0];
+  at.nparts = dv.gs[0].s / dv.gs[0].cs;
+  at.sa = p->ascale(l, FM_SITE_ATTN_IN);
+  at.sw = p->wscale(l, 0);
+  const size_t kv_layer = static_cast<size_t>(c.P) * c.Hkv * c.Dh;
+  at.kpre = p->at<__nv_bfloat16>(p->ly.kcache) + l * kv_layer;
+  at.vpre = p->at<__nv_bfloat16>(p->ly.vcache) + l * kv_layer;
+  at.out = p->at<void>(p->ly.o);
+  at.s_out = p->ascale(l, FM_SITE_ATTN_OUT);
+  at.out_fp8 = fp8;
+  at.M = c.M;
+  at.P = c.P;
+  at.H = c.H;
+  at.Hkv = c.Hkv;
+  at.kc = dv.attn_kc;
+  at.nsplit = dv.attn_nsplit;
+  e = fm::attn_launch(at, o);
+  if (e != cudaSuccess) return e;
+
+  e = fm::gemm_launch(p->tmW[l * 4 + 1], p->tmA[1], dv.gs[1], y[1], err, o);
+  if (e != cudaSuccess) return e;
+
+  fm::RowArgs r1 = {};
+  r1.M = c.M;
+  r1.N = c.d;
+  r1.parts = y[1];
+  r1.nparts = dv.gs[1].s / dv.gs[1].cs;
+  r1.sa = p->ascale(l, FM_SITE_ATTN_OUT);
+  r1.sw = p->wscale(l, 1);
+  r1.gate = p->mod(k, l, 2);
+  r1.x = p->at<float>(p->ly.x);
+  r1.do_quant = 1;
+  r1.scale = p->mod(k, l, 3);
+  r1.shift = p->mod(k, l, 4);
+  r1.sq = p->ascale(l, FM_SITE_MLP_IN);
+  r1.q = p->at<void>(p->ly.q2);
+  r1.q_fp8 = fp8;
+  r1.eps = c.rms_eps;
+  e = fm::row_launch(r1, o);
+  if (e != cudaSuccess) return e;
+
+  e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], y[2], err, o);
+  if (e != cudaSuccess) return e;
+
+  fm::GegluArgs gg;
+  gg.M = c.M;
+  gg.F = c.F;
+  gg.parts = y[2];
+  gg.nparts = dv.gs[2].s / dv.gs[2].cs;
+  gg.sa = p->ascale(l, FM_SITE_MLP_IN);
+  gg.sw = p->wscale(l, 2);
+  gg.sq = p->ascale(l, FM_SITE_GEGLU);
+  gg.q = p->at<void>(p->ly.mc);
+  gg.q_fp8 = fp8;
+  e = fm::geglu_launch(gg, o);
+  if (e != cudaSuccess) return e;
+
+  e = fm::gemm_launch(p->tmW[l * 4 + 3], p->tmA[3], dv.gs[3], y[3], err, o);
+  if (e != cudaSuccess) return e;
+
+  fm::RowArgs r2 = {};
+  r2.M = c.M;
+  r2.N = c.d;
+  r2.parts = y[3];
+  r2.nparts = dv.gs[3].s / dv.gs[3].cs;
+  r2.sa = p->ascale(l, FM_SITE_GEGLU);
+  r2.sw = p->wscale(l, 3);
+  r2.gate = p->mod(k, l, 5);
+  r2.x = p->at<float>(p->ly.x);
+  r2.eps = c.rms_eps;
+  r2.q = p->at<void>(p->ly.q);
+  r2.q_fp8 = fp8;
+  if (!step_end) {
+    const int ln = (l + 1) % c.L;
+    r2.do_quant = 1;
+    r2.scale = p->mod(k, ln, 0);
+    r2.shift = p->mod(k, ln, 1);
+    r2.sq = p->ascale(ln, FM_SITE_ATTN_IN);
+  } else {
+    r2.do_tail = 1;
+    r2.scale_f = p->modf(k, 0);
+    r2.shift_f = p->modf(k, 1);
+    r2.gamma_f = p->at<float>(p->ly.gamma_f);
+    r2.w_out = p->at<__nv_bfloat16>(p->ly.w_out);
+    r2.b_out = p->at<float>(p->ly.b_out);
+    r2.a = p->at<float>(p->ly.a);
+    r2.A = c.A;
+    r2.dt = -1.0f / static_cast<float>(c.S);
+    if (k + 1 < c.S) {
+      r2.do_head = 1;
+      r2.w_in = p->at<__nv_bfloat16>(p->ly.w_in);
+      r2.b_in = p->at<float>(p->ly.b_in);
+      r2.do_quant = 1;
+      r2.scale = p->mod(k + 1, 0, 0);
+      r2.shift = p->mod(k + 1, 0, 1);
+      r2.sq = p->ascale(0, FM_SITE_ATTN_IN);
+    }
+  }
+  return fm::row_launch(r2, o);
+}
+
+cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
+  const fm_config& c = p->cfg;
+  fm::RowArgs r = {};
+  r.M = c.M;
+  r.N = c.d;
+  r.x = p->at<float>(p->ly.x);
+  r.a = p->at<float>(p->ly.a);
+  r.A = c.A;
+  r.do_head = 1;
+  r.w_in = p->at<__nv_bfloat16>(p->ly.w_in);
+  r.b_in = p->at<float>(p->ly.b_in);
+  r.do_quant = 1;
+  r.scale = p->mod(0, 0, 0);
+  r.shift = p->mod(0, 0, 1);
+  r.sq = p->ascale(0, FM_SITE_ATTN_IN);
+  r.q = p->at<void>(p->ly.q);
+  r.q_fp8 = p->dv.fp8;
+  r.eps = c.rms_eps;
+  return fm::row_launch(r, o);
+}
+
+cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st) {
+  LaunchOpts o;
+  o.stream = st;
+  o.pdl = (p->cfg.flags & FM_FLAG_USE_PDL) != 0;
+  cudaError_t e = enqueue_head(p, o);
+  if (e != cudaSuccess) return e;
+  for (int k = 0; k < p->cfg.S; ++k)
+    for (int l = 0; l < p->cfg.L; ++l) {
+      e = enqueue_layer(p, l, k, l == p->cfg.L - 1, o);
+      if (e != cudaSuccess) return e;
+    }
+  return cudaGetLastError();
+}
+
+int build_graph(fm_policy* p) {
+  FM_CUDA(p, cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking));
+  FM_CUDA(p, cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeThreadLocal));
+  cudaError_t e = enqueue_decision(p, p->cap_stream);
+  cudaGraph_t g = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(p->cap_stream, &g);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return cuda_fail(p, e, "capturing the decision");
+  }
+  if (e2 != cudaSuccess) return cuda_fail(p, e2, "cudaStreamEndCapture");
+  p->graph = g;
+  FM_CUDA(p, cudaGraphInstantiate(&p->exec, p->graph, 0));
+  return FM_OK;
+}
+
+void release(fm_policy* p) {
+  if (!p) return;
+  if (p->exec) cudaGraphExecDestroy(p->exec);
+  if (p->graph) cudaGraphDestroy(p->graph);
+  if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
+  delete p;
+}
+
+int check_ptrs(const fm_weights* w, int L, bool given, std::string* why) {
+  if (!w || !w->layers || !w->w_in || !w->b_in || !w->w_out || !w->b_out || !w->gamma_f || !w->w_mod_f ||
+      !w->b_mod_f || (given && !w->conds)) {
+    *why = "a weight pointer is NULL";
+    return FM_ERR_INVALID_ARG;
+  }
+  for (int l = 0; l < L; ++l) {
+    const fm_layer_weights& lw = w->layers[l];
+    const void* ptrs[8] = {lw.w_qkv, lw.w_o, lw.w_gu, lw.w_d, lw.gamma1, lw.gamma2, lw.w_mod, lw.b_mod};
+    for (const void* q : ptrs) {
+      if (!q) {
+        *why = "a layer weight pointer is NULL";
+        return FM_ERR_INVALID_ARG;
+      }
+      if (!aligned16(q)) {
+        *why = "a layer weight pointer is not 16-byte aligned";
+        return FM_ERR_ALIGN;
+      }
+    }
+  }
+  const void* ptrs[7] = {w->w_in, w->b_in, w->w_out, w->b_out, w->gamma_f, w->w_mod_f, w->b_mod_f};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) {
+      *why = "a weight pointer is not 16-byte aligned";
+      return FM_ERR_ALIGN;
+    }
+  return FM_OK;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+extern "C" {
+
+const char* fm_status_string(int s) {
+  switch (s) {
+    case FM_OK: return "FM_OK";
+    case FM_ERR_INVALID_ARG: return "FM_ERR_INVALID_ARG";
+    case FM_ERR_SHAPE: return "FM_ERR_SHAPE";
+    case FM_ERR_ALIGN: return "FM_ERR_ALIGN";
+    case FM_ERR_WORKSPACE: return "FM_ERR_WORKSPACE";
+    case FM_ERR_CUDA: return "FM_ERR_CUDA";
+    case FM_ERR_STATE_MISMATCH: return "FM_ERR_STATE_MISMATCH";
+    case FM_ERR_DEVICE: return "FM_ERR_DEVICE";
+    case FM_ERR_UNSUPPORTED: return "FM_ERR_UNSUPPORTED";
+    default: return "FM_ERR_UNKNOWN";
+  }
+}
+
+const char* fm_last_error(const fm_policy* p) { return p ? p->err.c_str() : g_last_error.c_str(); }
+
+int fm_workspace_size(const fm_config* cfg, size_t* bytes) {
+  std::string why;
+  int st = validate(cfg, &why);
+  if (st != FM_OK) return fail(nullptr, st, why);
+  if (!bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "bytes is NULL");
+  Derived dv;
+  st = derive(cfg, &dv, &why);
+  if (st != FM_OK) return fail(nullptr, st, why);
+  *bytes = make_layout(cfg, dv).total;
+  return FM_OK;
+}
+
+int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_scales, void* workspace,
+                  size_t ws_bytes, void* stream, fm_policy** out) {
+  if (!out) return fail(nullptr, FM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  int st = validate(cfg, &why);
+  if (st != FM_OK) return fail(nullptr, st, why);
+  st = check_ptrs(w, cfg->L, cfg->cond_mode == FM_COND_GIVEN, &why);
+  if (st != FM_OK) return fail(nullptr, st, why);
+  if (cfg->act_fmt == FM_FMT_FP8 && !act_scales)
+    return fail(nullptr, FM_ERR_INVALID_ARG, "FP8 activations need an activation-scale table");
+  if (!workspace) return fail(nullptr, FM_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return fail(nullptr, FM_ERR_ALIGN, "workspace not 1024-aligned");
+
+  fm_policy* p = new (std::nothrow) fm_policy();
+  if (!p) return fail(nullptr, FM_ERR_INVALID_ARG, "out of host memory");
+  p->cfg = *cfg;
+  st = derive(cfg, &p->dv, &why);
+  if (st != FM_OK) {
+    release(p);
+    return fail(nullptr, st, why);
+  }
+  p->ly = make_layout(cfg, p->dv);
+  if (ws_bytes < p->ly.total) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "workspace has %zu bytes, needs %zu", ws_bytes, p->ly.total);
+    release(p);
+    return fail(nullptr, FM_ERR_WORKSPACE, buf);
+  }
+  p->ws = static_cast<uint8_t*>(workspace);
+  p->ws_bytes = ws_bytes;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const fm_config& c = p->cfg;
+  const Derived& dv = p->dv;
+
+  auto bail = [&](int code, const std::string& msg) {
+    release(p);
+    return fail(nullptr, code, msg);
+  };
+  auto cu = [&](cudaError_t e, const char* where) -> bool {
+    if (e == cudaSuccess) return true;
+    why = std::string(where) + ": " + cudaGetErrorString(e);
+    return false;
+  };
+
+  if (!cu(fm::gemm_configure(), "gemm_configure") || !cu(fm::attn_configure(), "attn_configure"))
+    return bail(FM_ERR_CUDA, why);
+
+  // weights: fold gamma, quantise, tile
+  unsigned* amax = p->at<unsigned>(p->ly.amax);
+  for (int l = 0; l < c.L; ++l) {
+    const fm_layer_weights& lw = w->layers[l];
+    const float* src[4] = {lw.w_qkv, lw.w_o, lw.w_gu, lw.w_d};
+    const float* gam[4] = {lw.gamma1, nullptr, lw.gamma2, nullptr};
+    for (int g = 0; g < 4; ++g) {
+      if (!cu(fm::pack_weight(src[g], gam[g], dv.gN[g], dv.gK[g], c.weight_fmt, p->at<void>(p->ly.wpk[l * 4 + g]),
+                              p->wscale(l, g), amax, s),
+              "pack_weight"))
+        return bail(FM_ERR_CUDA, why);
+    }
+  }
+  // modulation table (the t-schedule is fixed: per-create state)
+  double* conds = p->at<double>(p->ly.conds);
+  if (!cu(fm::cond_embed_launch(conds, c.S, c.d, c.cond_mode == FM_COND_GIVEN ? w->conds : nullptr, s),
+          "cond_embed"))
+    return bail(FM_ERR_CUDA, why);
+  for (int l = 0; l < c.L; ++l) {
+    const fm_layer_weights& lw = w->layers[l];
+    if (!cu(fm::modtable_launch(conds, c.S, c.d, reinterpret_cast<const __nv_bfloat16*>(lw.w_mod), lw.b_mod, 6 * c.d,
+                                p->mod(0, l, 0), static_cast<size_t>(c.L) * 6 * c.d, s),
+            "modtable"))
+      return bail(FM_ERR_CUDA, why);
+  }
+  if (!cu(fm::modtable_launch(conds, c.S, c.d, reinterpret_cast<const __nv_bfloat16*>(w->w_mod_f), w->b_mod_f,
+                              2 * c.d, p->modf(0, 0), static_cast<size_t>(2) * c.d, s),
+          "modtable_final"))
+    return bail(FM_ERR_CUDA, why);
+  // in/out projections
+  const size_t da = static_cast<size_t>(c.d) * c.A;
+  if (!cu(cudaMemcpyAsync(p->at<void>(p->ly.w_in), w->w_in, da * 2, cudaMemcpyDeviceToDevice, s), "copy w_in") ||
+      !cu(cudaMemcpyAsync(p->at<void>(p->ly.w_out), w->w_out, da * 2, cudaMemcpyDeviceToDevice, s), "copy w_out") ||
+      !cu(cudaMemcpyAsync(p->at<void>(p->ly.b_in), w->b_in, c.d * 4, cudaMemcpyDeviceToDevice, s), "copy b_in") ||
+      !cu(cudaMemcpyAsync(p->at<void>(p->ly.b_out), w->b_out, c.A * 4, cudaMemcpyDeviceToDevice, s), "copy b_out") ||
+      !cu(cudaMemcpyAsync(p->at<void>(p->ly.gamma_f), w->gamma_f, c.d * 4, cudaMemcpyDeviceToDevice, s),
+          "copy gamma_f"))
+    return bail(FM_ERR_CUDA, why);
+  // activation scales (BF16 activations: 1)
+  std::vector<float> sc(static_cast<size_t>(c.L) * 4, 1.0f);
+  if (dv.fp8) std::copy(act_scales, act_scales + sc.size(), sc.begin());
+  if (!cu(cudaMemcpyAsync(p->at<void>(p->ly.ascale), sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, s),
+          "copy act scales") ||
+      !cu(cudaMemsetAsync(p->at<void>(p->ly.kcache), 0, p->ly.kv_bytes, s), "zero kcache") ||
+      !cu(cudaMemsetAsync(p->at<void>(p->ly.vcache), 0, p->ly.kv_bytes, s), "zero vcache") ||
+      !cu(cudaMemsetAsync(p->at<void>(p->ly.a), 0, p->ly.a_bytes, s), "zero a") ||
+      !cu(cudaMemsetAsync(p->errw(), 0, 64, s), "zero err"))
+    return bail(FM_ERR_CUDA, why);
+  if (!cu(cudaStreamSynchronize(s), "create sync")) return bail(FM_ERR_CUDA, why);
+
+  // tensor maps (fixed addresses, recorded into the graph by value)
+  p->tmW.resize(static_cast<size_t>(c.L) * 4);
+  for (int l = 0; l < c.L; ++l)
+    for (int g = 0; g < 4; ++g)
+      if (!fm::gemm_tmap_weight(&p->tmW[l * 4 + g], p->at<void>(p->ly.wpk[l * 4 + g]), dv.gs[g]))
+        return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed");
+  const size_t act_off[4] = {p->ly.q, p->ly.o, p->ly.q2, p->ly.mc};
+  for (int g = 0; g < 4; ++g)
+    if (!fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.gs[g]))
+      return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
+
+  uint64_t h = 1469598103934665603ull;
+  h = fnv(h, &c, sizeof c);
+  const uintptr_t base = reinterpret_cast<uintptr_t>(p->ws);
+  h = fnv(h, &base, sizeof base);
+  for (int g = 0; g < 4; ++g) h = fnv(h, &dv.gs[g], sizeof(fm::GemmShape));
+  h = fnv(h, &dv.attn_kc, sizeof(int));
+  p->plan_hash = h;
+
+  if (c.flags & FM_FLAG_USE_GRAPH) {
+    st = build_graph(p);
+    if (st != FM_OK) {
+      why = p->err;
+      return bail(st, why);
+    }
+  }
+  *out = p;
+  return FM_OK;
+}
+
+int policy_destroy(fm_policy* p) {
+  if (!p) return fail(nullptr, FM_ERR_INVALID_ARG, "policy is NULL");
+  release(p);
+  return FM_OK;
+}
+
+int fm_set_act_scales(fm_policy* p, const float* act_scales, void* stream) {
+  if (!p || !act_scales) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  if (!p->dv.fp8) return FM_OK;
+  FM_CUDA(p, cudaMemcpyAsync(p->at<void>(p->ly.ascale), act_scales, p->ly.scale_bytes, cudaMemcpyHostToDevice,
+                             static_cast<cudaStream_t>(stream)));
+  return cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) == cudaSuccess ? FM_OK
+                                                                                 : fail(p, FM_ERR_CUDA, "sync");
+}
+
+int set_prefix_kv(fm_policy* p, const uint16_t* k, const uint16_t* v, void* stream) {
+  if (!p || !k || !v) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  if (p->cfg.P == 0) return FM_OK;
+  return refresh_prefix(p, 0, p->cfg.P, k, v, stream);
+}
+
+int refresh_prefix(fm_policy* p, int tok_begin, int tok_end, const uint16_t* k, const uint16_t* v, void* stream) {
+  if (!p || !k || !v) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  const fm_config& c = p->cfg;
+  if (tok_begin < 0 || tok_end > c.P || tok_begin >= tok_end) return fail(p, FM_ERR_SHAPE, "bad token range");
+  const size_t row = static_cast<size_t>(c.Hkv) * c.Dh * 2;
+  const size_t rows = static_cast<size_t>(tok_end - tok_begin);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* src[2] = {k, v};
+  const size_t dst_off[2] = {p->ly.kcache, p->ly.vcache};
+  for (int i = 0; i < 2; ++i) {
+    uint8_t* dst = p->at<uint8_t>(dst_off[i]) + tok_begin * row;
+    FM_CUDA(p, cudaMemcpy2DAsync(dst, static_cast<size_t>(c.P) * row, src[i], rows * row, rows * row, c.L,
+                                 cudaMemcpyDeviceToDevice, s));
+  }
+  return FM_OK;
+}
+
+int decode_actions(fm_policy* p, const float* noise, float* actions, void* stream) {
+  if (!p || !actions) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->at<float>(p->ly.a);
+  if (noise && noise != a) FM_CUDA(p, cudaMemcpyAsync(a, noise, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  if (p->exec) {
+    FM_CUDA(p, cudaGraphLaunch(p->exec, s));
+  } else {
+    FM_CUDA(p, enqueue_decision(p, s));
+  }
+  if (actions != a) FM_CUDA(p, cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  ++p->decisions;
+  return FM_OK;
+}
+
+int decode_actions_host(fm_policy* p, const float* noise_host, float* actions_host, void* stream) {
+  if (!p || !actions_host) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->at<float>(p->ly.a);
+  if (noise_host) FM_CUDA(p, cudaMemcpyAsync(a, noise_host, p->ly.a_bytes, cudaMemcpyHostToDevice, s));
+  const int st = decode_actions(p, nullptr, a, stream);
+  if (st != FM_OK) return st;
+  FM_CUDA(p, cudaMemcpyAsync(actions_host, a, p->ly.a_bytes, cudaMemcpyDeviceToHost, s));
+  FM_CUDA(p, cudaStreamSynchronize(s));
+  return FM_OK;
+}
+
+int fm_state_size(const fm_policy* p, size_t* bytes) {
+  if (!p || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  *bytes = sizeof(CapsuleHeader) + 2 * p->ly.kv_bytes + p->ly.a_bytes + p->ly.scale_bytes;
+  return FM_OK;
+}
+
+int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, void* stream) {
+  if (!p || !dst) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  size_t need = 0;
+  fm_state_size(p, &need);
+  if (bytes < need) return fail(p, FM_ERR_WORKSPACE, "capsule buffer too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CapsuleHeader& h = p->hdr;
+  std::memset(&h, 0, sizeof h);
+  h.magic = kCapsuleMagic;
+  h.abi = FM_ABI_VERSION;
+  h.header_bytes = sizeof h;
+  h.plan_hash = p->plan_hash;
+  h.ws_base = reinterpret_cast<uintptr_t>(p->ws);
+  h.kv_bytes = p->ly.kv_bytes;
+  h.a_bytes = p->ly.a_bytes;
+  h.scale_bytes = p->ly.scale_bytes;
+  h.L = p->cfg.L;
+  h.P = p->cfg.P;
+  h.Hkv = p->cfg.Hkv;
+  h.Dh = p->cfg.Dh;
+  h.M = p->cfg.M;
+  h.A = p->cfg.A;
+  h.decisions = p->decisions;
+  uint8_t* d = static_cast<uint8_t*>(dst);
+  const cudaMemcpyKind k = dst_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost;
+  if (dst_on_device) {
+    FM_CUDA(p, cudaMemcpyAsync(d, &h, sizeof h, cudaMemcpyHostToDevice, s));
+    FM_CUDA(p, cudaStreamSynchronize(s));   // the staging header is reused by the next snapshot
+  } else {
+    std::memcpy(d, &h, sizeof h);
+  }
+  size_t off = sizeof h;
+  const size_t regions[4][2] = {{p->ly.kcache, p->ly.kv_bytes},
+                                {p->ly.vcache, p->ly.kv_bytes},
+                                {p->ly.a, p->ly.a_bytes},
+                                {p->ly.ascale, p->ly.scale_bytes}};
+  for (const auto& r : regions) {
+    if (r[1]) FM_CUDA(p, cudaMemcpyAsync(d + off, p->at<void>(r[0]), r[1], k, s));
+    off += r[1];
+  }
+  if (!dst_on_device) FM_CUDA(p, cudaStreamSynchronize(s));
+  return FM_OK;
+}
+
+int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream) {
+  if (!p || !src) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  size_t need = 0;
+  fm_state_size(p, &need);
+  if (bytes < need) return fail(p, FM_ERR_STATE_MISMATCH, "capsule too small for this policy");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CapsuleHeader h;
+  if (src_on_device) {
+    FM_CUDA(p, cudaMemcpyAsync(&h, src, sizeof h, cudaMemcpyDeviceToHost, s));
+    FM_CUDA(p, cudaStreamSynchronize(s));
+  } else {
+    std::memcpy(&h, src, sizeof h);
+  }
+  if (h.magic != kCapsuleMagic || h.abi != FM_ABI_VERSION || h.header_bytes != sizeof h)
+    return fail(p, FM_ERR_STATE_MISMATCH, "not a capsule of this library version");
+  if (h.plan_hash != p->plan_hash) return fail(p, FM_ERR_STATE_MISMATCH, "capsule was made by another plan");
+  if (h.ws_base != reinterpret_cast<uintptr_t>(p->ws))
+    return fail(p, FM_ERR_STATE_MISMATCH, "capsule is bound to another workspace address");
+  if (h.kv_bytes != p->ly.kv_bytes || h.a_bytes != p->ly.a_bytes || h.scale_bytes != p->ly.scale_bytes ||
+      h.L != p->cfg.L || h.P != p->cfg.P || h.M != p->cfg.M || h.A != p->cfg.A)
+    return fail(p, FM_ERR_STATE_MISMATCH, "capsule shapes differ");
+  const uint8_t* sp = static_cast<const uint8_t*>(src);
+  const cudaMemcpyKind k = src_on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+  size_t off = sizeof h;
+  const size_t regions[4][2] = {{p->ly.kcache, p->ly.kv_bytes},
+                                {p->ly.vcache, p->ly.kv_bytes},
+                                {p->ly.a, p->ly.a_bytes},
+                                {p->ly.ascale, p->ly.scale_bytes}};
+  for (const auto& r : regions) {
+    if (r[1]) FM_CUDA(p, cudaMemcpyAsync(p->at<void>(r[0]), sp + off, r[1], k, s));
+    off += r[1];
+  }
+  if (!src_on_device) FM_CUDA(p, cudaStreamSynchronize(s));
+  p->decisions = h.decisions;
+  return FM_OK;
+}
+
+int fm_device_status(fm_policy* p, void* stream, int* word) {
+  if (!p || !word) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int w = 0;
+  FM_CUDA(p, cudaMemcpyAsync(&w, p->errw(), sizeof w, cudaMemcpyDeviceToHost, s));
+  FM_CUDA(p, cudaMemsetAsync(p->errw(), 0, sizeof w, s));
+  FM_CUDA(p, cudaStreamSynchronize(s));
+  *word = w;
+  return w ? fail(p, FM_ERR_DEVICE, "a kernel abandoned a bounded wait") : FM_OK;
+}
+
+int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) {
+  if (!p || !per_layer || !per_decision) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  *per_layer = 8;
+  *per_decision = 1 + p->cfg.S * p->cfg.L * 8;
+  return FM_OK;
+}
+
+int fm_test_quant_e4m3(const float* x, int64_t n, float scale, uint8_t* codes, void* stream) {
+  if (!x || !codes || n < 0) return fail(nullptr, FM_ERR_INVALID_ARG, "bad argument");
+  if (!(scale > 0.f)) return fail(nullptr, FM_ERR_INVALID_ARG, "scale must be positive");
+  const cudaError_t e = fm::quant_e4m3_launch(x, n, scale, codes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "quant_e4m3");
+}
+
+int fm_packed_weight_bytes(int N, int K, int fmt, size_t* bytes) {
+  if (!bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "bytes is NULL");
+  if (N <= 0 || K <= 0 || N % 128 || K % 128) return fail(nullptr, FM_ERR_SHAPE, "N, K must be multiples of 128");
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
+  *bytes = fm::packed_weight_bytes(N, K, fmt);
+  return FM_OK;
+}
+
+int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
+                   void* stream) {
+  if (!w || !packed || !scale_out) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  if (N <= 0 || K <= 0 || N % 128 || K % 128) return fail(nullptr, FM_ERR_SHAPE, "N, K must be multiples of 128");
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
+  if (reinterpret_cast<uintptr_t>(packed) % kAlign) return fail(nullptr, FM_ERR_ALIGN, "packed not 1024-aligned");
+  // The caller's 4-byte scale slot doubles as the amax accumulator: the amax kernel
+  // fills it, then one thread reads it and overwrites it with the scale.
+  const cudaError_t e = fm::pack_weight(w, gamma, N, K, fmt, packed, scale_out,
+                                        reinterpret_cast<unsigned*>(scale_out), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "pack_weight");
+}
+
+int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s, int cluster_reduce,
+                        float* partials, void* stream) {
+  if (!a || !w_packed || !partials) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
+  if (!aligned16(a) || reinterpret_cast<uintptr_t>(w_packed) % kAlign)
+    return fail(nullptr, FM_ERR_ALIGN, "a must be 16-byte and w_packed 1024-byte aligned");
+  fm::GemmShape g;
+  const int st = fm::gemm_plan(M, N, K, fmt == FM_FMT_FP8, s, cluster_reduce, &g);
+  if (st != FM_OK) return fail(nullptr, st, "GEMM shape/split precondition violated");
+  CUtensorMap tw, ta;
+  if (!fm::gemm_tmap_weight(&tw, w_packed, g) || !fm::gemm_tmap_act(&ta, a, g))
+    return fail(nullptr, FM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  cudaError_t e = fm::gemm_configure();
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "gemm_configure");
+  int* err_word = nullptr;   // looked up per call: the address is per device
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err_word), fm_standalone_err);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
+  LaunchOpts o;
+  o.stream = static_cast<cudaStream_t>(stream);
+  e = fm::gemm_launch(tw, ta, g, partials, err_word, o);
+  return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "skinny_gemm launch");
+}
+
+int fm_test_consumer(const float* partials, int nparts, int M, int N, const float* s_a, const float* s_w,
+                     const float* bias, float* x, const float* gate, const float* scale, const float* shift, float eps,
+                     const float* s_q, void* q, int act_fmt, void* stream) {
+  if (!partials || !s_a || !s_w || !x || !gate || !scale || !shift || !s_q || !q)
+    return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  if (nparts < 1 || M < 1 || N < 4 || N % 4 || N > 16384) return fail(nullptr, FM_ERR_SHAPE, "bad shape");
+  if (act_fmt != FM_FMT_FP8 && act_fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_INVALID_ARG, "act_fmt");
+  const void* ptrs[7] = {partials, x, gate, scale, shift, q, bias ? bias : partials};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return fail(nullptr, FM_ERR_ALIGN, "pointers must be 16-byte aligned");
+  fm::RowArgs r = {};
+  r.M = M;
+  r.N = N;
+  r.parts = partials;
+  r.nparts = nparts;
+  r.sa = s_a;
+  r.sw = s_w;
+  r.bias = bias;
+  r.gate = gate;
+  r.x = x;
+  r.do_quant = 1;
+  r.scale = scale;
+  r.shift = shift;
+  r.sq = s_q;
+  r.q = q;
+  r.q_fp8 = act_fmt == FM_FMT_FP8;
+  r.eps = eps;
+  LaunchOpts o;
+  o.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = fm::row_launch(r, o);
+  return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "consumer launch");
+}
+
+int fm_test_layer(fm_policy* p, const float* x_in, int layer, int step, float* x_out, void* q_out, void* stream) {
+  if (!p || !x_in || !x_out || !q_out) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  if (layer < 0 || layer >= p->cfg.L || step < 0 || step >= p->cfg.S) return fail(p, FM_ERR_SHAPE, "bad layer/step");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchOpts o;
+  o.stream = s;
+  o.pdl = (p->cfg.flags & FM_FLAG_USE_PDL) != 0;
+  fm::RowArgs r = {};
+  r.M = p->cfg.M;
+  r.N = p->cfg.d;
+  r.x = p->at<float>(p->ly.x);
+  r.x_src = x_in;
+  r.do_quant = 1;
+  r.scale = p->mod(step, layer, 0);
+  r.shift = p->mod(step, layer, 1);
+  r.sq = p->ascale(layer, FM_SITE_ATTN_IN);
+  r.q = p->at<void>(p->ly.q);
+  r.q_fp8 = p->dv.fp8;
+  r.eps = p->cfg.rms_eps;
+  FM_CUDA(p, fm::row_launch(r, o));
+  FM_CUDA(p, enqueue_layer(p, layer, step, false, o));
+  const size_t xb = static_cast<size_t>(p->cfg.M) * p->cfg.d * 4;
+  FM_CUDA(p, cudaMemcpyAsync(x_out, p->at<void>(p->ly.x), xb, cudaMemcpyDeviceToDevice, s));
+  FM_CUDA(p, cudaMemcpyAsync(q_out, p->at<void>(p->ly.q), static_cast<size_t>(p->cfg.M) * p->cfg.d * p->dv.act_bytes,
+                             cudaMemcpyDeviceToDevice, s));
+  return FM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,317 @@
+// Row-wise fused kernels of the decoder, one CTA per action-chunk row.
+//
+// row_kernel: the consumer of a K-split GEMM (blog post "Embodied inference
+// acceleration", section "Static quantisation": gated residual + AdaRMSNorm +
+// FP8 convert fused, with the next layer's condition parameters, emitting exactly
+// the operand the next GEMM reads). It sums the partial planes in fixed order,
+// dequantises with fp32(s_a * s_w), applies the gated residual
+// x <- x + gate * y, then (optionally) the flow-matching step boundary
+// (final AdaRMSNorm * gamma_f, output projection, Euler update of the action
+// chunk, input projection of the next step) and finally
+// q = Q(x / sqrt(mean(x^2) + eps) * (1 + scale) + shift) (blog post, "CUDA
+// Graph vs graph simplification": the input-dependent RMS stays, gamma is folded
+// into the next GEMM's weights). The row statistic uses warp shuffles and one
+// shared-memory exchange.
+//
+// geglu_kernel: consumer of the gate|up GEMM: m = gelu_tanh(g) * u, quantised.
+// Create-time kernels: timestep embedding and the per-step modulation table.
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fm {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kMaxA = 32;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();   // protect red[] from a previous use
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+__device__ __forceinline__ uint8_t e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ void store_q4(void* q, size_t idx, float4 h, int fp8, float rs) {
+  if (fp8) {
+    uchar4 c;
+    c.x = e4m3(h.x * rs);
+    c.y = e4m3(h.y * rs);
+    c.z = e4m3(h.z * rs);
+    c.w = e4m3(h.w * rs);
+    *reinterpret_cast<uchar4*>(static_cast<uint8_t*>(q) + idx) = c;
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(h.x, h.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(h.z, h.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(q) + idx) = u;
+  }
+}
+
+__global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
+  extern __shared__ float xs[];   // the row, N floats
+  __shared__ float red[kRowThreads / 32];
+  __shared__ float sa_vec[kMaxA];
+  __shared__ float vred[kRowThreads / 32][kMaxA];
+
+  const int m = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int N = r.N;
+  const int n4 = N / 4;
+  pdl_trigger();
+  const float ds = r.parts ? __fmul_rn(*r.sa, *r.sw) : 0.f;
+  pdl_wait();
+
+  float* xrow = r.x + static_cast<size_t>(m) * N;
+  const float* xin = r.x_src ? r.x_src + static_cast<size_t>(m) * N : xrow;
+  const size_t plane = static_cast<size_t>(r.M) * N;
+
+  // ---- residual update (skipped when the step head recomputes x from the actions)
+  float ss = 0.f;
+  const bool load_x = r.parts || r.x_src || !r.do_head;
+  for (int c = tid; load_x && c < n4; c += kRowThreads) {
+    float4 x = *reinterpret_cast<const float4*>(xin + c * 4);
+    if (r.parts) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p = 0; p < r.nparts; ++p) {
+        const float4 v = *reinterpret_cast<const float4*>(r.parts + p * plane + static_cast<size_t>(m) * N + c * 4);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r.bias) b = *reinterpret_cast<const float4*>(r.bias + c * 4);
+      const float4 gt = *reinterpret_cast<const float4*>(r.gate + c * 4);
+      x.x = fmaf(gt.x, fmaf(acc.x, ds, b.x), x.x);
+      x.y = fmaf(gt.y, fmaf(acc.y, ds, b.y), x.y);
+      x.z = fmaf(gt.z, fmaf(acc.z, ds, b.z), x.z);
+      x.w = fmaf(gt.w, fmaf(acc.w, ds, b.w), x.w);
+    }
+    *reinterpret_cast<float4*>(xs + c * 4) = x;
+    if (!r.do_head && (r.parts || r.x_src)) *reinterpret_cast<float4*>(xrow + c * 4) = x;
+    ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+  }
+
+  // ---- Euler step tail: a <- a + dt * (AdaRMSNorm_f(x) * gamma_f . w_out^T + b_out)
+  if (r.do_tail) {
+    const float rr = rsqrtf(block_sum(ss, red) / N + r.eps);
+    float acc[kMaxA];
+#pragma unroll
+    for (int a = 0; a < kMaxA; ++a) acc[a] = 0.f;
+    for (int c = tid; c < n4; c += kRowThreads) {
+      const float4 x = *reinterpret_cast<const float4*>(xs + c * 4);
+      const float4 sc = *reinterpret_cast<const float4*>(r.scale_f + c * 4);
+      const float4 sh = *reinterpret_cast<const float4*>(r.shift_f + c * 4);
+      const float4 gf = *reinterpret_cast<const float4*>(r.gamma_f + c * 4);
+      float hf[4];
+      hf[0] = fmaf(x.x * rr, 1.f + sc.x, sh.x) * gf.x;
+      hf[1] = fmaf(x.y * rr, 1.f + sc.y, sh.y) * gf.y;
+      hf[2] = fmaf(x.z * rr, 1.f + sc.z, sh.z) * gf.z;
+      hf[3] = fmaf(x.w * rr, 1.f + sc.w, sh.w) * gf.w;
+#pragma unroll
+      for (int a = 0; a < kMaxA; ++a) {
+        if (a < r.A) {
+          const uint2 wv = *reinterpret_cast<const uint2*>(r.w_out + static_cast<size_t>(a) * N + c * 4);
+          const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wv.x);
+          const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wv.y);
+          acc[a] = fmaf(hf[0], __low2float(w01), acc[a]);
+          acc[a] = fmaf(hf[1], __high2float(w01), acc[a]);
+          acc[a] = fmaf(hf[2], __low2float(w23), acc[a]);
+          acc[a] = fmaf(hf[3], __high2float(w23), acc[a]);
+        }
+      }
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+    for (int a = 0; a < kMaxA; ++a) {
+      float v = acc[a];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) vred[warp][a] = v;
+    }
+    __syncthreads();
+    if (tid < r.A) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRowThreads / 32; ++w) v += vred[w][tid];
+      float* arow = r.a + static_cast<size_t>(m) * r.A;
+      const float anew = fmaf(r.dt, v + r.b_out[tid], arow[tid]);
+      arow[tid] = anew;
+      sa_vec[tid] = anew;
+    }
+    __syncthreads();
+  } else if (r.do_head) {
+    if (tid < r.A) sa_vec[tid] = r.a[static_cast<size_t>(m) * r.A + tid];
+    __syncthreads();
+  }
+
+  // ---- step head: x = a . w_in^T + b_in
+  if (r.do_head) {
+    ss = 0.f;
+    for (int c = tid; c < n4; c += kRowThreads) {
+      float xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = c * 4 + i;
+        const __nv_bfloat16* wrow = r.w_in + static_cast<size_t>(n) * r.A;
+        float acc = 0.f;
+        for (int a = 0; a < r.A; ++a) acc = fmaf(sa_vec[a], __bfloat162float(wrow[a]), acc);
+        xv[i] = acc + r.b_in[n];
+      }
+      const float4 x = make_float4(xv[0], xv[1], xv[2], xv[3]);
+      *reinterpret_cast<float4*>(xs + c * 4) = x;
+      *reinterpret_cast<float4*>(xrow + c * 4) = x;
+      ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+    }
+  }
+
+  // ---- AdaRMSNorm + static-scale quantisation into the next GEMM's operand
+  if (r.do_quant) {
+    const float rr = rsqrtf(block_sum(ss, red) / N + r.eps);
+    const float rs = r.q_fp8 ? 1.0f / *r.sq : 1.0f;
+    for (int c = tid; c < n4; c += kRowThreads) {
+      const float4 x = *reinterpret_cast<const float4*>(xs + c * 4);
+      const float4 sc = *reinterpret_cast<const float4*>(r.scale + c * 4);
+      const float4 sh = *reinterpret_cast<const float4*>(r.shift + c * 4);
+      float4 h;
+      h.x = fmaf(x.x * rr, 1.f + sc.x, sh.x);
+      h.y = fmaf(x.y * rr, 1.f + sc.y, sh.y);
+      h.z = fmaf(x.z * rr, 1.f + sc.z, sh.z);
+      h.w = fmaf(x.w * rr, 1.f + sc.w, sh.w);
+      store_q4(r.q, static_cast<size_t>(m) * N + c * 4, h, r.q_fp8, rs);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRowThreads) geglu_kernel(const GegluArgs g) {
+  const int m = blockIdx.x;
+  const int c = blockIdx.y * kRowThreads + threadIdx.x;   // 4-column group
+  pdl_trigger();
+  const float ds = __fmul_rn(*g.sa, *g.sw);
+  const float rs = g.q_fp8 ? 1.0f / *g.sq : 1.0f;
+  pdl_wait();
+  if (c * 4 >= g.F) return;
+  const size_t plane = static_cast<size_t>(g.M) * 2 * g.F;
+  const size_t row = static_cast<size_t>(m) * 2 * g.F;
+  float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), ua = ga;
+  for (int p = 0; p < g.nparts; ++p) {
+    const float4 gv = *reinterpret_cast<const float4*>(g.parts + p * plane + row + c * 4);
+    const float4 uv = *reinterpret_cast<const float4*>(g.parts + p * plane + row + g.F + c * 4);
+    ga.x += gv.x;
+    ga.y += gv.y;
+    ga.z += gv.z;
+    ga.w += gv.w;
+    ua.x += uv.x;
+    ua.y += uv.y;
+    ua.z += uv.z;
+    ua.w += uv.w;
+  }
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+  float gg[4] = {ga.x * ds, ga.y * ds, ga.z * ds, ga.w * ds};
+  float uu[4] = {ua.x * ds, ua.y * ds, ua.z * ds, ua.w * ds};
+  float hv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float x = gg[i];
+    hv[i] = 0.5f * x * (1.f + tanhf(k0 * fmaf(k1 * x, x * x, x))) * uu[i];
+  }
+  store_q4(g.q, static_cast<size_t>(m) * g.F + c * 4, make_float4(hv[0], hv[1], hv[2], hv[3]), g.q_fp8, rs);
+}
+
+// ---------------------------------------------------------------- create-time kernels
+
+// cond[k][i]: the given vector, or the sinusoidal embedding of t_k = 1 - k/S
+// ([sin(2 pi t / p_i), cos(2 pi t / p_i)], p_i geometric from 4e-3 to 4), in double.
+__global__ void cond_embed_kernel(double* conds, int S, int d, const float* given) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= S * d) return;
+  if (given) {
+    conds[idx] = static_cast<double>(given[idx]);
+    return;
+  }
+  const int k = idx / d, i = idx % d, half = d / 2;
+  const int f = i < half ? i : i - half;
+  const double t = 1.0 - static_cast<double>(k) / S;
+  const double period = 4e-3 * pow(4.0 / 4e-3, static_cast<double>(f) / (half - 1));
+  const double arg = 2.0 * 3.14159265358979323846 * t / period;
+  conds[idx] = i < half ? sin(arg) : cos(arg);
+}
+
+// out[k * step_stride + j] = fp32(sum_i cond[k][i] * w[j][i] + b[j]); one warp per output j.
+__global__ void modtable_kernel(const double* __restrict__ conds, int S, int d, const __nv_bfloat16* __restrict__ w,
+                                const float* __restrict__ b, int nout, float* __restrict__ out, size_t step_stride) {
+  const int j = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= nout) return;
+  const __nv_bfloat16* wr = w + static_cast<size_t>(j) * d;
+  for (int k = 0; k < S; ++k) {
+    const double* c = conds + static_cast<size_t>(k) * d;
+    double acc = 0.0;
+    for (int i = lane; i < d; i += 32) acc += c[i] * static_cast<double>(__bfloat162float(wr[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) out[k * step_stride + j] = static_cast<float>(acc + static_cast<double>(b[j]));
+  }
+}
+
+__global__ void quant_e4m3_kernel(const float* __restrict__ x, int64_t n, float scale, uint8_t* __restrict__ codes) {
+  const float rs = 1.0f / scale;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    codes[i] = e4m3(x[i] * rs);
+}
+
+}  // namespace
+
+cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
+  const size_t smem = static_cast<size_t>(r.N) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch(row_kernel, dim3(static_cast<unsigned>(r.M)), dim3(kRowThreads), smem, o, r);
+}
+
+cudaError_t geglu_launch(const GegluArgs& g, const LaunchOpts& o) {
+  const unsigned gy = static_cast<unsigned>((g.F / 4 + kRowThreads - 1) / kRowThreads);
+  return launch(geglu_kernel, dim3(static_cast<unsigned>(g.M), gy), dim3(kRowThreads), 0, o, g);
+}
+
+cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, cudaStream_t st) {
+  const int n = S * d;
+  cond_embed_kernel<<<(n + 255) / 256, 256, 0, st>>>(conds, S, d, given);
+  return cudaGetLastError();
+}
+
+cudaError_t modtable_launch(const double* conds, int S, int d, const __nv_bfloat16* w_mod, const float* b_mod,
+                            int nout, float* out, size_t out_step_stride, cudaStream_t st) {
+  const int warps = 8;
+  modtable_kernel<<<(nout + warps - 1) / warps, warps * 32, 0, st>>>(conds, S, d, w_mod, b_mod, nout, out,
+                                                                     out_step_stride);
+  return cudaGetLastError();
+}
+
+cudaError_t quant_e4m3_launch(const float* x, int64_t n, float scale, uint8_t* codes, cudaStream_t st) {
+  quant_e4m3_kernel<<<1184, 256, 0, st>>>(x, n, scale, codes);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

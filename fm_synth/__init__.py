@@ -172,7 +172,7 @@ def default_act_scales(cfg: Config) -> np.ndarray:
     2 = pre-MLP norm output, 3 = GeGLU output. Used where no calibrated table is
     supplied; the values are plain constants sized for the distributions above.
     """
-    base = np.array([8.0, 2.0, 8.0, 4.0], np.float32) / np.float32(448.0)
+    base = np.array([24.0, 1.0, 24.0, 16.0], np.float32) / np.float32(448.0)
     return np.tile(base, (cfg.L, 1)).astype(np.float32)
 
 

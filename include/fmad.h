@@ -1,0 +1,268 @@
+/*
+ * fmad.h - C ABI of the GB300 flow-matching action decoder (libfmad.so).
+ *
+ * The library runs the single-batch flow-matching action-decoder loop of a
+ * vision-language-action policy (FlashRT-PAI pages): L transformer layers x S
+ * Euler denoise steps over an M-row action chunk. Each layer is
+ *   AdaRMSNorm (x / sqrt(mean(x^2) + eps) * (1 + scale) + shift, fixed gamma
+ *     folded into the next GEMM's weights W' = diag(gamma) W)
+ *   -> static-scale quantise -> QKV GEMM (split along K)
+ *   -> attention of the chunk over [persistent prefix KV cache; chunk KV]
+ *   -> O GEMM -> gated residual + AdaRMSNorm + quantise
+ *   -> gate|up GEMM -> GeGLU + quantise -> down GEMM
+ *   -> gated residual + the next layer's AdaRMSNorm + quantise.
+ * Sources: blog post "Embodied inference acceleration: first ask how old the
+ * observation is" (sections "CUDA Graph vs graph simplification": RMSNorm,
+ * gamma fold, QKV merge, CUDA Graph replay; "Static quantisation": static
+ * activation scales, fused gated residual + AdaRMSNorm + FP8 convert, next
+ * layer's condition parameters; "Small-M GEMM": K-split with FP32 partials
+ * reduced before the consumer's transform); news article "FlashRT-PAI"
+ * (section "It optimises the relay": launch overlap with Programmatic
+ * Dependent Launch, the execution contract of named persistent buffers with
+ * reuse of instruction-dependent state and selective refresh of
+ * image-dependent state, and execution-state capsules that snapshot and
+ * restore in-process state bound to the plan and device addresses).
+ *
+ * Conventions for every entry point:
+ *   - Returns int status (fm_status). No exceptions, aborts or device traps.
+ *   - The caller owns ALL device memory, including the workspace; the library
+ *     never allocates or frees device memory. Pointers documented "device"
+ *     must be device pointers on the current CUDA device; "host" pointers are
+ *     ordinary host memory (pinned recommended for async copies).
+ *   - Work is stream-ordered on the given cudaStream_t (passed as void*; NULL
+ *     means the legacy default stream) and asynchronous unless noted.
+ *   - A policy is used from one stream at a time.
+ *   - Matrices are row-major; "[R][C]" means R rows of C contiguous elements.
+ *   - fp8 means OCP E4M3 (E4M3FN: max 448, no infinities), one byte per code;
+ *     bf16 tensors are passed as uint16_t bit patterns.
+ */
+#ifndef FMAD_H
+#define FMAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FM_ABI_VERSION 1
+
+typedef enum fm_status {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1,     /* NULL pointer, bad enum, bad ABI version */
+  FM_ERR_SHAPE = 2,           /* a size violates a documented precondition */
+  FM_ERR_ALIGN = 3,           /* a pointer is not 16-byte (workspace: 1024-byte) aligned */
+  FM_ERR_WORKSPACE = 4,       /* workspace smaller than fm_workspace_size() */
+  FM_ERR_CUDA = 5,            /* a CUDA runtime call failed; see fm_last_error() */
+  FM_ERR_STATE_MISMATCH = 6,  /* capsule from another plan, policy or address */
+  FM_ERR_DEVICE = 7,          /* a kernel gave up a bounded wait and set the error word */
+  FM_ERR_UNSUPPORTED = 8      /* valid request this build does not implement */
+} fm_status;
+
+typedef enum fm_format {
+  FM_FMT_BF16 = 0,   /* bf16 operands, no quantisation */
+  FM_FMT_FP8 = 1,    /* E4M3 codes with a static per-tensor scale */
+  FM_FMT_NVFP4 = 2   /* weights only: E2M1 + E4M3 scale per 16 along K + fp32 tensor scale */
+} fm_format;
+
+enum {
+  FM_FLAG_USE_GRAPH = 1u,  /* replay the whole decision as one CUDA graph */
+  FM_FLAG_USE_PDL = 2u     /* launch every kernel with Programmatic Dependent Launch */
+};
+
+enum {
+  FM_COND_TIME = 0,   /* cond of step k = sinusoidal embedding of t_k = 1 - k/S */
+  FM_COND_GIVEN = 1   /* cond of step k = caller-supplied vector (fm_weights.conds) */
+};
+
+/* Activation quant points per layer, the column index of the [L][4] scale table. */
+enum {
+  FM_SITE_ATTN_IN = 0,   /* pre-attention AdaRMSNorm output (QKV GEMM input) */
+  FM_SITE_ATTN_OUT = 1,  /* attention output (O GEMM input) */
+  FM_SITE_MLP_IN = 2,    /* pre-MLP AdaRMSNorm output (gate|up GEMM input) */
+  FM_SITE_GEGLU = 3      /* GeGLU output (down GEMM input) */
+};
+
+/* Policy shape and options. Preconditions (FM_ERR_SHAPE otherwise):
+ *   d, F and H*Dh multiples of 128; Dh == 128; H a multiple of Hkv;
+ *   1 <= M <= 256; 1 <= A <= 256; P >= 0; L, S >= 1;
+ *   ksplit[i] (0 = automatic) divides the GEMM's K/128-byte block count.
+ * act_fmt must be FP8 or BF16; weight_fmt FP8 requires act_fmt FP8, BF16
+ * requires BF16, NVFP4 requires FP8. */
+typedef struct fm_config {
+  int abi_version;     /* must be FM_ABI_VERSION */
+  int L, S, M, d, H, Hkv, Dh, F, P, A;
+  int weight_fmt;      /* fm_format */
+  int act_fmt;         /* fm_format (FP8 or BF16) */
+  int cond_mode;       /* FM_COND_TIME or FM_COND_GIVEN */
+  float rms_eps;       /* AdaRMSNorm epsilon */
+  int ksplit[4];       /* K-split of the QKV, O, gate|up and down GEMMs; 0 = auto */
+  unsigned flags;      /* FM_FLAG_* */
+} fm_config;
+
+/* One layer's raw parameters (device pointers, read only during policy_create).
+ * GEMM weights are fp32 in [out][in] layout (y = x W^T):
+ *   w_qkv [(H+2Hkv)*Dh][d] (rows: Q heads, then K heads, then V heads),
+ *   w_o [d][H*Dh], w_gu [2F][d] (rows 0..F-1 gate, F..2F-1 up), w_d [d][F].
+ * gamma1 [d] folds into w_qkv's columns, gamma2 [d] into w_gu's columns.
+ * w_mod bf16 [6d][d], b_mod fp32 [6d]: modulation = cond . w_mod^T + b_mod,
+ * split as [scale1, shift1, gate1, scale2, shift2, gate2]. */
+typedef struct fm_layer_weights {
+  const float* w_qkv;
+  const float* w_o;
+  const float* w_gu;
+  const float* w_d;
+  const float* gamma1;
+  const float* gamma2;
+  const uint16_t* w_mod;
+  const float* b_mod;
+} fm_layer_weights;
+
+/* Whole-policy parameters. `layers` is a HOST array of L entries whose fields
+ * are device pointers; everything else is a device pointer.
+ *   w_in bf16 [d][A], b_in fp32 [d]      : x = a . w_in^T + b_in
+ *   w_out bf16 [A][d], b_out fp32 [A]    : v = h_f . w_out^T + b_out
+ *   gamma_f fp32 [d]                     : h_f = AdaRMSNorm_f(x) * gamma_f
+ *   w_mod_f bf16 [2d][d], b_mod_f [2d]   : [scale_f, shift_f] of the final norm
+ *   conds fp32 [S][d] when cond_mode == FM_COND_GIVEN, else NULL. */
+typedef struct fm_weights {
+  const fm_layer_weights* layers;
+  const uint16_t* w_in;
+  const float* b_in;
+  const uint16_t* w_out;
+  const float* b_out;
+  const float* gamma_f;
+  const uint16_t* w_mod_f;
+  const float* b_mod_f;
+  const float* conds;
+} fm_weights;
+
+typedef struct fm_policy fm_policy;   /* opaque; owned by the library */
+
+/* Human-readable name of a status code (static string). */
+const char* fm_status_string(int status);
+
+/* Detail of the last failure on this policy (or of the last policy-free call
+ * on this thread when p is NULL). Valid until the next call. */
+const char* fm_last_error(const fm_policy* p);
+
+/* Bytes of device workspace a policy with this config needs (host call). */
+int fm_workspace_size(const fm_config* cfg, size_t* bytes);
+
+/* Build a policy in a caller-owned workspace (device, 1024-byte aligned,
+ * >= fm_workspace_size bytes). Folds gamma into the GEMM weights, computes each
+ * weight's static scale (amax/448 for FP8; amax/(448*6) tensor scale plus E4M3
+ * block scales for NVFP4), quantises and re-tiles the weights into
+ * K-major 128-byte swizzled tiles, precomputes the per-step modulation table
+ * (the t-schedule is fixed, so modulation is per-create state), copies the
+ * in/out projections, stores the static activation scales (host [L][4] fp32,
+ * columns FM_SITE_*; ignored for BF16 activations and may then be NULL) and,
+ * with FM_FLAG_USE_GRAPH, captures the whole decision as one CUDA graph.
+ * Synchronises `stream` before returning. The prefix cache starts zeroed.
+ * On failure nothing is leaked and *out is NULL. */
+int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_scales,
+                  void* workspace, size_t ws_bytes, void* stream, fm_policy** out);
+
+/* Release the host-side policy (graph, plan). Does not touch the workspace.
+ * The caller must not destroy a policy with work in flight on its stream. */
+int policy_destroy(fm_policy* p);
+
+/* Replace the static activation scales (host [L][4] fp32). Stream-ordered copy
+ * into the policy's scale buffer; the captured graph reads them from there. */
+int fm_set_act_scales(fm_policy* p, const float* act_scales, void* stream);
+
+/* Overwrite the whole prefix KV cache: k, v device bf16 [L][P][Hkv][Dh]. */
+int set_prefix_kv(fm_policy* p, const uint16_t* k, const uint16_t* v, void* stream);
+
+/* Overwrite rows [tok_begin, tok_end) of every layer's prefix K and V (the
+ * image-dependent part after a new observation); other rows persist.
+ * k, v: device bf16 [L][tok_end - tok_begin][Hkv][Dh]. 0 <= begin < end <= P. */
+int refresh_prefix(fm_policy* p, int tok_begin, int tok_end, const uint16_t* k,
+                   const uint16_t* v, void* stream);
+
+/* One decision: S Euler steps from the noise (t = 1) to the action chunk (t = 0).
+ * noise: device fp32 [M][A], or NULL to start from the policy's noise/action
+ * buffer as it stands (e.g. after restore_state). actions: device fp32 [M][A]
+ * (may equal noise). Asynchronous. */
+int decode_actions(fm_policy* p, const float* noise, float* actions, void* stream);
+
+/* Same as decode_actions with HOST buffers (pinned recommended): copies the
+ * noise in, decodes, copies the actions out, then synchronises the stream. */
+int decode_actions_host(fm_policy* p, const float* noise_host, float* actions_host, void* stream);
+
+/* Bytes of an execution-state capsule (header + prefix K/V + noise/action
+ * buffer + activation scales + counters). */
+int fm_state_size(const fm_policy* p, size_t* bytes);
+
+/* Copy the policy's persistent state into dst (host if dst_on_device == 0, else
+ * device), stream-ordered; host copies synchronise the stream. */
+int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, void* stream);
+
+/* Restore a capsule made by snapshot_state of THIS policy (same plan hash,
+ * workspace address and shapes); otherwise FM_ERR_STATE_MISMATCH and nothing is
+ * written. Capsules are in-process only, bound to the plan and device addresses. */
+int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream);
+
+/* Synchronise `stream`, read and clear the device error word. Returns FM_OK, or
+ * FM_ERR_DEVICE with *word = the bits a kernel set when it abandoned a bounded
+ * wait (1 = TMA/MMA pipeline wait expired). */
+int fm_device_status(fm_policy* p, void* stream, int* word);
+
+/* Kernel launches per decoder layer and per decision of the captured plan. */
+int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
+
+/* ---------------------------------------------------------------------------
+ * Building blocks, exported for tests and standalone use (same conventions).
+ * ------------------------------------------------------------------------- */
+
+/* Static-scale E4M3 quantisation: codes[i] = E4M3_RNE_satfinite(x[i] * (1/scale)),
+ * the reciprocal rounded to fp32. x device fp32 [n], codes device uint8 [n]. */
+int fm_test_quant_e4m3(const float* x, int64_t n, float scale, uint8_t* codes, void* stream);
+
+/* Bytes of a packed weight [N][K] in format fmt (N, K multiples of 128). */
+int fm_packed_weight_bytes(int N, int K, int fmt, size_t* bytes);
+
+/* Fold gamma (device fp32 [K] or NULL), quantise and tile a weight w (device fp32
+ * [N][K]) into `packed` (device, 1024-byte aligned, fm_packed_weight_bytes).
+ * scale_out (device fp32 [1]) receives the tensor scale (1.0 for BF16).
+ * FP8 tile layout: tile (n/128, k/128) is 128 rows x 128 bytes, rows n, bytes k,
+ * tiles ordered n-tile-major then k-block; each tile is stored as TMA writes it
+ * with 128-byte swizzle undone, i.e. plain [128][128] bytes (BF16: [128][64]). */
+int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt,
+                   void* packed, float* scale_out, void* stream);
+
+/* Skinny GEMM with K-split on tcgen05 tensor cores (blog post, "Small-M GEMM"):
+ * partials[j][m][n] = sum_{k in slice j} A[m][k] * Wcodes[n][k] for the s equal
+ * contiguous K slices (fp32, unscaled). A: device [M][K], fp8 codes (fmt FP8)
+ * or bf16 (fmt BF16), 16-byte aligned; w_packed from fm_pack_weight.
+ * cluster_reduce = c (1, 2, 4 or 8, dividing s): the c CTAs of consecutive
+ * slices sum their partials in fixed order through distributed shared memory,
+ * so partials holds s/c slices [s/c][M][N]. 1 <= M <= 256; N, K multiples of
+ * 128; s divides K/128 (FP8) or K/64 (BF16). */
+int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt,
+                        int s, int cluster_reduce, float* partials, void* stream);
+
+/* Fused consumer (blog post, "Static quantisation"): with y = (sum_j
+ * partials[j]) * fp32(s_a * s_w) + bias,  x <- x + gate * y,
+ * q = Q(AdaRMSNorm(x; scale, shift), s_q) where Q is E4M3 with the fp32
+ * reciprocal of s_q (act_fmt FP8) or bf16 rounding (BF16). partials device fp32
+ * [nparts][M][N]; bias/gate/scale/shift device fp32 [N] (bias may be NULL);
+ * x device fp32 [M][N] in/out; s_a, s_w, s_q device fp32 [1]; q device [M][N]. */
+int fm_test_consumer(const float* partials, int nparts, int M, int N, const float* s_a,
+                     const float* s_w, const float* bias, float* x, const float* gate,
+                     const float* scale, const float* shift, float eps, const float* s_q,
+                     void* q, int act_fmt, void* stream);
+
+/* One decoder layer of a policy on a given residual input, launched exactly as
+ * decode_actions launches it: q = Q(AdaRMSNorm_l(x_in)), the layer, then the
+ * next layer's ((layer+1) mod L) pre-attention norm + quantise.
+ * x_in, x_out device fp32 [M][d]; q_out device [M][d] codes (fp8 or bf16). */
+int fm_test_layer(fm_policy* p, const float* x_in, int layer, int step, float* x_out,
+                  void* q_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FMAD_H */

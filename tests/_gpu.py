@@ -1,0 +1,65 @@
+"""Helpers shared by the GPU tests: device buffers, tile layouts, tolerances."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import flow_matching_action_denoise_gb300 as fmad
+from oracle import codecs as C
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    fmad.load()   # raises if the compiled library is missing: no fallback
+    return torch.device("cuda:0")
+
+
+def dev(a, device, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+def aligned_empty(nbytes, device, align=1024):
+    """A uint8 device buffer whose returned pointer is `align`-aligned (buffer, ptr)."""
+    buf = torch.empty(nbytes + align, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % align
+    return buf, buf.data_ptr() + off
+
+
+def tile_codes(codes, elems_per_row_block):
+    """[N][K] -> the packed tile order [N/128][K/e][128][e] (e = 128 fp8 or 64 bf16)."""
+    n, k = codes.shape
+    e = elems_per_row_block
+    return codes.reshape(n // 128, 128, k // e, e).transpose(0, 2, 1, 3).copy()
+
+
+def untile_codes(packed, n, k, e):
+    return packed.reshape(n // 128, k // e, 128, e).transpose(0, 2, 1, 3).reshape(n, k)
+
+
+def e4m3_values_of_bytes(b):
+    return C.e4m3_decode_code(np.asarray(b, np.uint8))
+
+
+def bf16_values_of_bits(bits):
+    return C.bf16_decode_bits(np.asarray(bits).view(np.uint16))
+
+
+def code_step_distance(a_codes, b_codes):
+    """Distance in representable E4M3 steps between codes (sign-magnitude order)."""
+    def ordinal(c):
+        c = np.asarray(c, np.int64)
+        mag = c & 0x7F
+        return np.where(c & 0x80, -mag, mag)
+    return np.abs(ordinal(a_codes) - ordinal(b_codes))
+
+
+def load_scales(name):
+    path = os.path.join(GOLDEN, f"act_scales_{name}.txt")
+    return np.loadtxt(path, dtype=np.float32, ndmin=2)

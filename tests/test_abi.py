@@ -1,0 +1,91 @@
+"""The C-ABI library loads and exports every entry point include/fmad.h declares,
+and host-side validation returns the documented status codes (no GPU needed:
+nothing here launches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fm_synth
+import flow_matching_action_denoise_gb300 as fmad
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fmad.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\([^;{]*\)\s*;", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fmad.LIB_PATH):
+        from flow_matching_action_denoise_gb300 import build
+        build.build()
+    return fmad.load()
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ["policy_create", "set_prefix_kv", "refresh_prefix", "decode_actions",
+                     "snapshot_state", "restore_state", "policy_destroy"]:
+        assert required in names
+    assert sorted(names) == sorted(fmad.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in fmad.STATUS.items():
+        assert lib.fm_status_string(code).decode() == name
+
+
+def test_workspace_size_and_validation(lib):
+    cfg = fmad.make_config(fm_synth.config("expert_fp8_m50"))
+    n = fmad.workspace_size(cfg)
+    # packed FP8 weights alone are 18 x 14.94 MB
+    assert n > 18 * 14_942_208
+    bad = fmad.make_config(fm_synth.config("expert_fp8_m50"))
+    bad.M = 300
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(bad)
+    assert e.value.status == 2
+    bad = fmad.make_config(fm_synth.config("expert_fp8_m50"))
+    bad.abi_version = 99
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(bad)
+    assert e.value.status == 1
+    bad = fmad.make_config(fm_synth.config("expert_fp8_m50"), ksplit=(3, 0, 0, 0))
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(bad)
+    assert e.value.status == 2
+
+
+def test_policy_create_rejects_bad_arguments_without_touching_the_gpu(lib):
+    cfg = fmad.make_config(fm_synth.config("expert_fp8_m50"))
+    out = ctypes.c_void_p()
+    w = fmad.FmWeights()
+    # NULL weights
+    st = lib.policy_create(ctypes.byref(cfg), ctypes.byref(w), None, 1024, 1 << 30, None, ctypes.byref(out))
+    assert st == 1 and out.value is None
+    assert b"NULL" in lib.fm_last_error(None)
+
+
+def test_policy_free_exports_validate(lib):
+    n = ctypes.c_size_t()
+    assert lib.fm_packed_weight_bytes(1280, 1024, fmad.FMT_FP8, ctypes.byref(n)) == 0
+    assert n.value == 1280 * 1024
+    assert lib.fm_packed_weight_bytes(1280, 1000, fmad.FMT_FP8, ctypes.byref(n)) == 2
+    assert lib.fm_packed_weight_bytes(1280, 1024, fmad.FMT_BF16, ctypes.byref(n)) == 0
+    assert n.value == 1280 * 1024 * 2
+    # GEMM: split must divide the K-block count; pointers are checked before any launch
+    assert lib.fm_test_skinny_gemm(None, 10, 1024, None, 1024, fmad.FMT_FP8, 8, 8, None, None) == 1
+    assert lib.fm_test_skinny_gemm(1024, 10, 1024, 1024, 1024, fmad.FMT_FP8, 3, 1, 1024, None) == 2
+    assert lib.fm_test_skinny_gemm(1024, 300, 1024, 1024, 1024, fmad.FMT_FP8, 1, 1, 1024, None) == 2
+    assert lib.fm_test_skinny_gemm(1032, 10, 1024, 1024, 1024, fmad.FMT_FP8, 1, 1, 1024, None) == 3
+    assert lib.fm_test_quant_e4m3(1024, 16, ctypes.c_float(0.0), 1024, None) == 1
