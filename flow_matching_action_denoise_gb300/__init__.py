@@ -18,7 +18,7 @@ __all__ = [
     "policy_destroy", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
     "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status",
     "kernel_count", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
-    "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "Policy", "DeviceWeights",
+    "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "named_buffer", "Policy", "DeviceWeights",
     "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "COND_TIME", "COND_GIVEN",
     "ABI_VERSION", "STATUS",
 ]
@@ -38,7 +38,7 @@ EXPORTS = [
     "fm_set_act_scales", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
     "fm_state_size", "snapshot_state", "restore_state", "fm_device_status", "fm_test_kernel_count",
     "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight", "fm_test_skinny_gemm",
-    "fm_test_consumer", "fm_test_layer",
+    "fm_test_consumer", "fm_test_layer", "fm_named_buffer",
 ]
 
 
@@ -104,6 +104,7 @@ def load() -> ctypes.CDLL:
         "fm_test_skinny_gemm": (i, [vp, i, i, vp, i, i, i, i, vp, vp]),
         "fm_test_consumer": (i, [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, i, vp]),
         "fm_test_layer": (i, [vp, vp, i, i, vp, vp, vp]),
+        "fm_named_buffer": (i, [vp, ctypes.c_char_p, ctypes.POINTER(vp), ctypes.POINTER(sz)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -232,6 +233,13 @@ def device_status(p: int, stream=None) -> int:
     return w.value
 
 
+def named_buffer(p: int, name: str):
+    """(device pointer, bytes) of a policy's named persistent buffer."""
+    ptr, n = ctypes.c_void_p(), ctypes.c_size_t()
+    _check(load().fm_named_buffer(p, name.encode(), ctypes.byref(ptr), ctypes.byref(n)), "fm_named_buffer")
+    return ptr.value, n.value
+
+
 def kernel_count(p: int):
     a, b = ctypes.c_int(), ctypes.c_int()
     _check(load().fm_test_kernel_count(p, ctypes.byref(a), ctypes.byref(b)), "fm_test_kernel_count", p)
@@ -340,6 +348,20 @@ class Policy:
 
     def refresh_prefix(self, b, e, k, v, stream=None):
         refresh_prefix(self.handle, b, e, k, v, stream)
+
+    def buffer(self, name: str, dtype=None, shape=None):
+        """Zero-copy torch view of a named persistent buffer inside the workspace."""
+        ptr, n = named_buffer(self.handle, name)
+        off = ptr - self.workspace.data_ptr()
+        view = self.workspace[off:off + n]
+        if dtype is not None:
+            view = view.view(dtype)
+        if shape is not None:
+            count = 1
+            for s_ in shape:
+                count *= s_
+            view = view[:count].view(*shape)
+        return view
 
     def decode(self, noise, actions=None, stream=None):
         if actions is None:

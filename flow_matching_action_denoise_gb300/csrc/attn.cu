@@ -13,10 +13,11 @@
 // into rows r = h_local * M + m, so one K/V tile serves all of them. A CTA owns
 // 64 stacked rows (4 warps x 16) and one contiguous slice of the keys; the
 // slices of one row tile form a thread-block cluster. Each warp runs QK^T and PV
-// on bf16 tensor cores (m16n8k16, fp32 accumulate) with an online softmax over
-// 64-key chunks; the unnormalised partial (O, running max, running sum) of each
-// CTA is combined across the cluster through distributed shared memory in fixed
-// slice order, normalised, and quantised with the static output scale.
+// on bf16 tensor cores (m16n8k16, fp32 accumulate). The softmax statistics (row
+// max and sum) are exchanged across the cluster through distributed shared
+// memory, so the probabilities are normalised before they are rounded to bf16;
+// the slices' shares of O are summed across the cluster in fixed slice order and
+// quantised with the static output scale.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -99,7 +100,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem);
   __nv_bfloat16* sK = sQ + kRows * kLds;
   __nv_bfloat16* sV = sK + p.kc * kLds;
-  float* sML = reinterpret_cast<float*>(sV + p.kc * kLds);   // [64][2]: running max (log2 units), sum
+  float* sML = reinterpret_cast<float*>(sV + p.kc * kLds);   // [64][2]: slice max (log2 units), slice sum
+  float* sStat = sML + kRows * 2;                             // [64][2]: global max, global sum
   float* sO = reinterpret_cast<float*>(sK);                   // [64][128] fp32, aliases K/V after compute
 
   const int split = blockIdx.x;
@@ -156,7 +158,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   }
   __syncthreads();
 
-  // ---- per-warp flash attention over this slice
+  // ---- per-warp attention over this slice, two passes over the keys:
+  // pass 1 finds the row max and the row sum of exp over the slice; the cluster
+  // exchanges them so every CTA holds the global max M and sum L of each row;
+  // pass 2 forms the normalised probabilities P = exp(s - M) / L, rounds them to
+  // bf16 for the tensor-core PV product, and accumulates this slice's share of O.
+  // The rounding points are thus those of softmax-then-bf16, independent of how
+  // the keys are split across CTAs.
   const int warp = tid >> 5, lane = tid & 31;
   const int r0 = warp * 16;
   uint32_t qf[8][4];
@@ -165,17 +173,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) ldsm_x4(qbase + ks * 32, qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
   }
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY};
-  float lrow[2] = {0.f, 0.f};
   const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh));   // log2(e) / sqrt(Dh)
   const int nchunks = (nvalid + kChunk - 1) / kChunk;
   const int mat = lane >> 3;
 
-  for (int ch = 0; ch < nchunks; ++ch) {
-    float s[8][4];
+  // S = Q K^T for one 64-key chunk, scaled to log2 units, masked past nvalid.
+  auto scores = [&](int ch, float (&s)[8][4]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
 #pragma unroll
@@ -190,44 +193,88 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
         mma_bf16(s[2 * np + 1], qf[ks], b2, b3);
       }
     }
-    // scale, mask, online softmax
-    float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = ch * kChunk + nt * 8 + (lane & 3) * 2 + (e & 1);
         s[nt][e] = key < nvalid ? s[nt][e] * kscale : -INFINITY;
-        mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
       }
     }
-    float corr[2];
+  };
+
+  // ---- pass 1: row max and sum of exp over this slice
+  float mrow[2] = {-INFINITY, -INFINITY};
+  float lrow[2] = {0.f, 0.f};
+  for (int ch = 0; ch < nchunks; ++ch) {
+    float s[8][4];
+    scores(ch, s);
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+    }
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
       mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
       const float mnew = fmaxf(mrow[hr], mx[hr]);
-      corr[hr] = exp2f(mrow[hr] - mnew);
+      lrow[hr] *= exp2f(mrow[hr] - mnew);
       mrow[hr] = mnew;
-      lrow[hr] *= corr[hr];
     }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pe = exp2f(s[nt][e] - mrow[e >> 1]);
-        s[nt][e] = pe;
-        lrow[e >> 1] += pe;
-      }
+      for (int e = 0; e < 4; ++e) lrow[e >> 1] += exp2f(s[nt][e] - mrow[e >> 1]);
     }
+  }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= corr[0];
-      o[i][1] *= corr[0];
-      o[i][2] *= corr[1];
-      o[i][3] *= corr[1];
+  for (int hr = 0; hr < 2; ++hr) {
+    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
+    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
+  }
+  {
+    const int rlo = r0 + (lane >> 2), rhi = rlo + 8;
+    if ((lane & 3) == 0) {
+      sML[rlo * 2] = mrow[0];
+      sML[rlo * 2 + 1] = lrow[0];
+      sML[rhi * 2] = mrow[1];
+      sML[rhi * 2 + 1] = lrow[1];
     }
-    // O += P V
+  }
+  // ---- exchange the slice statistics across the cluster: global max and sum per row
+  cluster_sync_all();
+  if (tid < kRows) {
+    const uint32_t ml_local = smem_u32(sML + tid * 2);
+    float mq[kMaxSplit], lq[kMaxSplit];
+    float mstar = -INFINITY;
+    for (int q = 0; q < p.nsplit; ++q) {
+      mq[q] = ld_dsmem_f32(map_dsmem(ml_local, q));
+      lq[q] = ld_dsmem_f32(map_dsmem(ml_local + 4, q));
+      mstar = fmaxf(mstar, mq[q]);
+    }
+    float lsum = 0.f;
+    for (int q = 0; q < p.nsplit; ++q) lsum += lq[q] * exp2f(mq[q] - mstar);
+    sStat[tid * 2] = mstar;
+    sStat[tid * 2 + 1] = lsum;
+  }
+  __syncthreads();
+  const float gmax[2] = {sStat[(r0 + (lane >> 2)) * 2], sStat[(r0 + (lane >> 2) + 8) * 2]};
+  const float gsum[2] = {sStat[(r0 + (lane >> 2)) * 2 + 1], sStat[(r0 + (lane >> 2) + 8) * 2 + 1]};
+
+  // ---- pass 2: O_slice = bf16(exp(s - M) / L) V
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    float s[8][4];
+    scores(ch, s);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = exp2f(s[nt][e] - gmax[e >> 1]) / gsum[e >> 1];
+    }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t a[4];
@@ -246,13 +293,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
     }
   }
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
-    lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
-  }
 
-  // ---- partial result of this slice into shared memory (over the K/V tiles)
+  // ---- this slice's share of O into shared memory (over the K/V tiles)
   __syncthreads();
   {
     const int rlo = r0 + (lane >> 2), rhi = rlo + 8;
@@ -262,15 +304,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       *reinterpret_cast<float2*>(sO + rlo * kDh + col) = make_float2(o[nt][0], o[nt][1]);
       *reinterpret_cast<float2*>(sO + rhi * kDh + col) = make_float2(o[nt][2], o[nt][3]);
     }
-    if ((lane & 3) == 0) {
-      sML[rlo * 2] = mrow[0];
-      sML[rlo * 2 + 1] = lrow[0];
-      sML[rhi * 2] = mrow[1];
-      sML[rhi * 2 + 1] = lrow[1];
-    }
   }
 
-  // ---- combine the slices of this row tile across the cluster, fixed slice order
+  // ---- sum the slices' shares across the cluster in fixed slice order, quantise
   cluster_sync_all();
   {
     const int rank = static_cast<int>(cluster_rank());
@@ -278,35 +314,22 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     const int e = tid;   // head-dim column
     const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
     const uint32_t o_local = smem_u32(sO);
-    const uint32_t ml_local = smem_u32(sML);
     for (int r = rank * rows_per; r < min(kRows, (rank + 1) * rows_per); ++r) {
       const int R = qt * kRows + r;
       if (R >= p.G * p.M) break;
-      float mq[kMaxSplit], lq[kMaxSplit];
-      float mstar = -INFINITY;
-      for (int q = 0; q < p.nsplit; ++q) {
-        mq[q] = ld_dsmem_f32(map_dsmem(ml_local + r * 8, q));
-        lq[q] = ld_dsmem_f32(map_dsmem(ml_local + r * 8 + 4, q));
-        mstar = fmaxf(mstar, mq[q]);
-      }
-      float lsum = 0.f, acc = 0.f;
-      for (int q = 0; q < p.nsplit; ++q) {
-        const float w = exp2f(mq[q] - mstar);
-        lsum += w * lq[q];
-        acc += w * ld_dsmem_f32(map_dsmem(o_local + (r * kDh + e) * 4, q));
-      }
-      const float val = acc / lsum;
+      float acc = 0.f;
+      for (int q = 0; q < p.nsplit; ++q) acc += ld_dsmem_f32(map_dsmem(o_local + (r * kDh + e) * 4, q));
       const int hl = R / p.M, m = R % p.M;
       const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e;
       if (p.out_fp8) {
         static_cast<uint8_t*>(p.out)[oidx] =
-            static_cast<uint8_t>(__nv_cvt_float_to_fp8(val * rs, __NV_SATFINITE, __NV_E4M3));
+            static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc * rs, __NV_SATFINITE, __NV_E4M3));
       } else {
-        static_cast<__nv_bfloat16*>(p.out)[oidx] = __float2bfloat16_rn(val);
+        static_cast<__nv_bfloat16*>(p.out)[oidx] = __float2bfloat16_rn(acc);
       }
     }
   }
-  cluster_sync_all();   // peers may still be reading this CTA's partial
+  cluster_sync_all();   // peers may still be reading this CTA's share
 }
 
 }  // namespace
@@ -322,12 +345,10 @@ void attn_plan(int M, int P, int* kc, int* nsplit) {
 }
 
 size_t attn_smem_bytes(int kc) {
-  return 128 + static_cast<size_t>(kRows) * kLds * 2 + 2 * static_cast<size_t>(kc) * kLds * 2 + kRows * 2 * 4;
+  return 128 + static_cast<size_t>(kRows) * kLds * 2 + 2 * static_cast<size_t>(kc) * kLds * 2 + 2 * kRows * 2 * 4;
 }
 
-cudaError_t attn_configure() {
-  return cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-}
+cudaError_t attn_configure() { return allow_max_dynamic_smem(reinterpret_cast<const void*>(attn_kernel)); }
 
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   KParams p;

@@ -369,11 +369,22 @@ bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g) 
   return make_tmap_2d(map, packed, eb, kBlockBytes / eb, rows, kBlockBytes / eb, kTileN);
 }
 
-cudaError_t gemm_configure() {
-  cudaError_t e = cudaFuncSetAttribute(skinny_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       227 * 1024);
+cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(skinny_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+  if (granted) *granted = static_cast<size_t>(dyn);
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+}
+
+cudaError_t gemm_configure() {
+  cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(skinny_gemm_kernel<true>));
+  if (e != cudaSuccess) return e;
+  return allow_max_dynamic_smem(reinterpret_cast<const void*>(skinny_gemm_kernel<false>));
 }
 
 cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,

@@ -49,6 +49,10 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Largest dynamic shared memory `kernel` may request on the current device (the
+// opt-in per-block maximum minus the kernel's static shared memory); sets it.
+cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted = nullptr);
+
 // ---------------------------------------------------------------- tensor maps
 // 2-D tensor map over a row-major [outer][inner] array of 1- or 2-byte elements,
 // 128-byte swizzle, zero fill out of bounds. Returns false on failure.

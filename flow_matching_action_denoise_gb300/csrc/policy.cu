@@ -792,6 +792,44 @@ int fm_device_status(fm_policy* p, void* stream, int* word) {
   return w ? fail(p, FM_ERR_DEVICE, "a kernel abandoned a bounded wait") : FM_OK;
 }
 
+int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* bytes) {
+  if (!p || !name || !ptr || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  const fm_config& c = p->cfg;
+  const Derived& dv = p->dv;
+  const Layout& ly = p->ly;
+  const size_t M = c.M, ab = dv.act_bytes;
+  auto ypart = [&](int g) { return static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4; };
+  struct Entry {
+    const char* n;
+    size_t off, bytes;
+  } table[] = {
+      {"prefix_k", ly.kcache, ly.kv_bytes},
+      {"prefix_v", ly.vcache, ly.kv_bytes},
+      {"actions", ly.a, ly.a_bytes},
+      {"x", ly.x, M * c.d * 4},
+      {"q", ly.q, M * c.d * ab},
+      {"q2", ly.q2, M * c.d * ab},
+      {"attn_out", ly.o, M * c.H * c.Dh * ab},
+      {"geglu_out", ly.mc, M * c.F * ab},
+      {"y_qkv", ly.y[0], ypart(0)},
+      {"y_o", ly.y[1], ypart(1)},
+      {"y_gu", ly.y[2], ypart(2)},
+      {"y_d", ly.y[3], ypart(3)},
+      {"act_scales", ly.ascale, ly.scale_bytes},
+      {"weight_scales", ly.wscale, ly.scale_bytes},
+      {"mod", ly.mod, static_cast<size_t>(c.S) * c.L * 6 * c.d * 4},
+      {"mod_final", ly.modf, static_cast<size_t>(c.S) * 2 * c.d * 4},
+  };
+  for (const Entry& e : table) {
+    if (std::strcmp(e.n, name) == 0) {
+      *ptr = p->ws + e.off;
+      *bytes = e.bytes;
+      return FM_OK;
+    }
+  }
+  return fail(nullptr, FM_ERR_INVALID_ARG, std::string("unknown buffer name: ") + name);
+}
+
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) {
   if (!p || !per_layer || !per_decision) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
   *per_layer = 8;

@@ -283,8 +283,7 @@ __global__ void quant_e4m3_kernel(const float* __restrict__ x, int64_t n, float 
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
   const size_t smem = static_cast<size_t>(r.N) * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(row_kernel));
     if (e != cudaSuccess) return e;
   }
   return launch(row_kernel, dim3(static_cast<unsigned>(r.M)), dim3(kRowThreads), smem, o, r);

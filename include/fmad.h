@@ -209,6 +209,20 @@ int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device
  * wait (1 = TMA/MMA pipeline wait expired). */
 int fm_device_status(fm_policy* p, void* stream, int* word);
 
+/* Address and size of one of the policy's named persistent buffers (the
+ * execution contract's named buffers), for inspection and for zero-copy input:
+ *   "prefix_k", "prefix_v"  bf16 [L][P][Hkv][Dh]
+ *   "actions"               fp32 [M][A] noise/action state
+ *   "x"                     fp32 [M][d] residual stream
+ *   "q", "q2"               codes [M][d] (pre-attention / pre-MLP GEMM operand)
+ *   "attn_out"              codes [M][H*Dh]
+ *   "geglu_out"             codes [M][F]
+ *   "y_qkv", "y_o", "y_gu", "y_d"  fp32 [parts][M][N] GEMM partial planes
+ *   "act_scales", "weight_scales"  fp32 [L][4]
+ *   "mod"                   fp32 [S][L][6][d]; "mod_final" fp32 [S][2][d]
+ * Codes are one byte (FP8 activations) or bf16. FM_ERR_INVALID_ARG for an unknown name. */
+int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* bytes);
+
 /* Kernel launches per decoder layer and per decision of the captured plan. */
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
 
