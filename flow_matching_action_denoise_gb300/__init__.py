@@ -38,7 +38,7 @@ EXPORTS = [
     "fm_set_act_scales", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
     "fm_state_size", "snapshot_state", "restore_state", "fm_device_status", "fm_test_kernel_count",
     "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight", "fm_test_skinny_gemm",
-    "fm_test_consumer", "fm_test_layer", "fm_named_buffer",
+    "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
 ]
 
 
@@ -105,6 +105,8 @@ def load() -> ctypes.CDLL:
         "fm_test_consumer": (i, [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, i, vp]),
         "fm_test_layer": (i, [vp, vp, i, i, vp, vp, vp]),
         "fm_named_buffer": (i, [vp, ctypes.c_char_p, ctypes.POINTER(vp), ctypes.POINTER(sz)]),
+        "fm_trace_size": (i, [vp, ctypes.POINTER(sz)]),
+        "fm_decode_trace": (i, [vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -238,6 +240,17 @@ def named_buffer(p: int, name: str):
     ptr, n = ctypes.c_void_p(), ctypes.c_size_t()
     _check(load().fm_named_buffer(p, name.encode(), ctypes.byref(ptr), ctypes.byref(n)), "fm_named_buffer")
     return ptr.value, n.value
+
+
+def trace_size(p: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_trace_size(p, ctypes.byref(n)), "fm_trace_size", p)
+    return n.value
+
+
+def decode_trace(p: int, noise, actions, trace, nbytes: int, stream=None):
+    _check(load().fm_decode_trace(p, _ptr(noise), _ptr(actions), _ptr(trace), nbytes, _stream(stream)),
+           "fm_decode_trace", p)
 
 
 def kernel_count(p: int):

@@ -261,21 +261,51 @@ int cuda_fail(fm_policy* p, cudaError_t e, const char* where) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
+// ---------------------------------------------------------------- tracing
+// Optional recorder: after a kernel, copy the buffer it wrote into the trace.
+struct Trace {
+  uint8_t* base = nullptr;
+  size_t off = 0;
+  cudaStream_t st = nullptr;
+  cudaError_t rec(const void* src, size_t bytes) {
+    if (!base) return cudaSuccess;
+    const cudaError_t e = cudaMemcpyAsync(base + off, src, bytes, cudaMemcpyDeviceToDevice, st);
+    off += bytes;
+    return e;
+  }
+};
+
 // ---------------------------------------------------------------- the plan
 // Kernels of layer l at step k. tail: -1 = next layer's norm (layer (l+1) mod L),
 // otherwise the last layer of a decision step (Euler tail; head of step tail
 // if tail < S).
-cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const LaunchOpts& o) {
+cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const LaunchOpts& o, Trace* tr = nullptr) {
   const fm_config& c = p->cfg;
   const Derived& dv = p->dv;
   cudaError_t e;
   int* err = p->errw();
   float* y[4];
-  for (int g = 0; g < 4; ++g) y[g] = p->at<float>(p->ly.y[g]);
+  size_t ybytes[4];
+  for (int g = 0; g < 4; ++g) {
+    y[g] = p->at<float>(p->ly.y[g]);
+    ybytes[g] = static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * c.M * dv.gN[g] * 4;
+  }
   const int fp8 = dv.fp8;
+  const size_t xbytes = static_cast<size_t>(c.M) * c.d * 4;
+  const size_t ab = dv.act_bytes;
+  Trace none;
+  Trace& t = tr ? *tr : none;
+#define FM_REC(ptr, bytes)                 \
+  do {                                     \
+    e = t.rec((ptr), (bytes));             \
+    if (e != cudaSuccess) return e;        \
+  } while (0)
+  FM_REC(p->at<void>(p->ly.x), xbytes);
+  FM_REC(p->at<void>(p->ly.q), static_cast<size_t>(c.M) * c.d * ab);
 
   e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], y[0], err, o);
   if (e != cudaSuccess) return e;
+  FM_REC(y[0], ybytes[0]);
 
   fm::AttnArgs at;
   at.yqkv = y[0];
@@ -296,9 +326,11 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   at.nsplit = dv.attn_nsplit;
   e = fm::attn_launch(at, o);
   if (e != cudaSuccess) return e;
+  FM_REC(p->at<void>(p->ly.o), static_cast<size_t>(c.M) * c.H * c.Dh * ab);
 
   e = fm::gemm_launch(p->tmW[l * 4 + 1], p->tmA[1], dv.gs[1], y[1], err, o);
   if (e != cudaSuccess) return e;
+  FM_REC(y[1], ybytes[1]);
 
   fm::RowArgs r1 = {};
   r1.M = c.M;
@@ -318,9 +350,12 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   r1.eps = c.rms_eps;
   e = fm::row_launch(r1, o);
   if (e != cudaSuccess) return e;
+  FM_REC(p->at<void>(p->ly.x), xbytes);
+  FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
 
   e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], y[2], err, o);
   if (e != cudaSuccess) return e;
+  FM_REC(y[2], ybytes[2]);
 
   fm::GegluArgs gg;
   gg.M = c.M;
@@ -334,9 +369,11 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   gg.q_fp8 = fp8;
   e = fm::geglu_launch(gg, o);
   if (e != cudaSuccess) return e;
+  FM_REC(p->at<void>(p->ly.mc), static_cast<size_t>(c.M) * c.F * ab);
 
   e = fm::gemm_launch(p->tmW[l * 4 + 3], p->tmA[3], dv.gs[3], y[3], err, o);
   if (e != cudaSuccess) return e;
+  FM_REC(y[3], ybytes[3]);
 
   fm::RowArgs r2 = {};
   r2.M = c.M;
@@ -376,7 +413,21 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
       r2.sq = p->ascale(0, FM_SITE_ATTN_IN);
     }
   }
-  return fm::row_launch(r2, o);
+  e = fm::row_launch(r2, o);
+  if (e != cudaSuccess) return e;
+  FM_REC(p->at<void>(p->ly.x), xbytes);
+  FM_REC(p->at<void>(p->ly.a), p->ly.a_bytes);
+#undef FM_REC
+  return cudaSuccess;
+}
+
+size_t trace_record_bytes(const fm_policy* p) {
+  const fm_config& c = p->cfg;
+  const Derived& dv = p->dv;
+  const size_t M = c.M, ab = dv.act_bytes;
+  size_t n = 3 * M * c.d * 4 + M * c.d * ab * 2 + M * c.H * c.Dh * ab + M * c.F * ab + p->ly.a_bytes;
+  for (int g = 0; g < 4; ++g) n += static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4;
+  return n;
 }
 
 cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
@@ -400,7 +451,7 @@ cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
   return fm::row_launch(r, o);
 }
 
-cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st) {
+cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st, Trace* tr = nullptr) {
   LaunchOpts o;
   o.stream = st;
   o.pdl = (p->cfg.flags & FM_FLAG_USE_PDL) != 0;
@@ -408,7 +459,7 @@ cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   for (int k = 0; k < p->cfg.S; ++k)
     for (int l = 0; l < p->cfg.L; ++l) {
-      e = enqueue_layer(p, l, k, l == p->cfg.L - 1, o);
+      e = enqueue_layer(p, l, k, l == p->cfg.L - 1, o, tr);
       if (e != cudaSuccess) return e;
     }
   return cudaGetLastError();
@@ -828,6 +879,30 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
     }
   }
   return fail(nullptr, FM_ERR_INVALID_ARG, std::string("unknown buffer name: ") + name);
+}
+
+int fm_trace_size(const fm_policy* p, size_t* bytes) {
+  if (!p || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  *bytes = trace_record_bytes(p) * p->cfg.S * p->cfg.L;
+  return FM_OK;
+}
+
+int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trace, size_t bytes, void* stream) {
+  if (!p || !actions || !trace) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  size_t need = 0;
+  fm_trace_size(p, &need);
+  if (bytes < need) return fail(p, FM_ERR_WORKSPACE, "trace buffer too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->at<float>(p->ly.a);
+  if (noise && noise != a) FM_CUDA(p, cudaMemcpyAsync(a, noise, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  Trace tr;
+  tr.base = static_cast<uint8_t*>(trace);
+  tr.st = s;
+  FM_CUDA(p, enqueue_decision(p, s, &tr));
+  if (actions != a) FM_CUDA(p, cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  FM_CUDA(p, cudaStreamSynchronize(s));
+  if (tr.off != need) return fail(p, FM_ERR_INVALID_ARG, "internal: trace size mismatch");
+  return FM_OK;
 }
 
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) {

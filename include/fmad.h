@@ -223,6 +223,31 @@ int fm_device_status(fm_policy* p, void* stream, int* word);
  * Codes are one byte (FP8 activations) or bf16. FM_ERR_INVALID_ARG for an unknown name. */
 int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* bytes);
 
+/* Bytes of one decision trace (see fm_decode_trace). */
+int fm_trace_size(const fm_policy* p, size_t* bytes);
+
+/* Run one decision with the same kernels and launch configuration as
+ * decode_actions, launched one by one (no graph), and record after the kernels
+ * of every layer-step a copy of the buffers they wrote into `trace` (device,
+ * >= fm_trace_size bytes), for stage-by-stage verification. Records are ordered
+ * step-major then layer; each record holds, contiguously in this order:
+ *   x_in fp32 [M][d]          residual stream entering the layer
+ *   q codes [M][d]            pre-attention operand
+ *   y_qkv fp32 [P0][M][Nqkv]  QKV partial planes (P0 = fm_named_buffer size / (M*Nqkv*4))
+ *   attn_out codes [M][H*Dh]
+ *   y_o fp32 [P1][M][d]
+ *   x_mid fp32 [M][d]         after the attention gated residual
+ *   q2 codes [M][d]
+ *   y_gu fp32 [P2][M][2F]
+ *   geglu_out codes [M][F]
+ *   y_d fp32 [P3][M][d]
+ *   x_out fp32 [M][d]         after the MLP gated residual; for the last layer of
+ *                             a step that is not the last, the next step's x
+ *                             (after the Euler update and input projection)
+ *   actions fp32 [M][A]       the noise/action state after this layer-step
+ * Codes are one byte (FP8) or bf16 (BF16 activations). Synchronous. */
+int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trace, size_t bytes, void* stream);
+
 /* Kernel launches per decoder layer and per decision of the captured plan. */
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
 

@@ -63,3 +63,43 @@ def code_step_distance(a_codes, b_codes):
 def load_scales(name):
     path = os.path.join(GOLDEN, f"act_scales_{name}.txt")
     return np.loadtxt(path, dtype=np.float32, ndmin=2)
+
+
+def parse_trace(raw, cfg, pol):
+    """Split an fm_decode_trace buffer into records[k][l] of numpy arrays; codes are
+    returned as decoded values (E4M3 codes without their scale, or bf16 values)."""
+    M, d = cfg.M, cfg.d
+    fp8 = cfg.act_fmt == "fp8"
+    ab = 1 if fp8 else 2
+
+    def parts(name, n):
+        _, nbytes = fmad.named_buffer(pol.handle, name)
+        return nbytes // (M * n * 4)
+
+    layout = [("x_in", "f", (M, d)), ("q", "c", (M, d)),
+              ("y_qkv", "f", (parts("y_qkv", cfg.n_qkv), M, cfg.n_qkv)),
+              ("attn_out", "c", (M, cfg.H * cfg.Dh)), ("y_o", "f", (parts("y_o", d), M, d)),
+              ("x_mid", "f", (M, d)), ("q2", "c", (M, d)),
+              ("y_gu", "f", (parts("y_gu", 2 * cfg.F), M, 2 * cfg.F)), ("geglu_out", "c", (M, cfg.F)),
+              ("y_d", "f", (parts("y_d", d), M, d)), ("x_out", "f", (M, d)), ("actions", "f", (M, cfg.A))]
+    off = 0
+    recs = []
+    for k in range(cfg.S):
+        row = []
+        for l in range(cfg.L):
+            r = {}
+            for name, kind, shape in layout:
+                n = int(np.prod(shape))
+                nb = n * (4 if kind == "f" else ab)
+                chunk = raw[off:off + nb]
+                off += nb
+                if kind == "f":
+                    r[name] = chunk.view(np.float32).reshape(shape).astype(np.float64)
+                elif fp8:
+                    r[name] = C.e4m3_decode_code(chunk).reshape(shape)
+                else:
+                    r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
+            row.append(r)
+        recs.append(row)
+    assert off == raw.size, (off, raw.size)
+    return recs
