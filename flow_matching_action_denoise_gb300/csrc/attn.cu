@@ -6,8 +6,8 @@
 // relay": reuse instruction-dependent results, refresh image-dependent ones).
 // Queries, keys and values of the chunk come from the merged QKV GEMM (blog post,
 // "CUDA Graph vs graph simplification": three projections sharing one input
-// become one wider GEMM); this kernel's prologue reduces its partial planes,
-// dequantises with fp32(s_a * s_w) and rounds to bf16.
+// become one wider GEMM), whose epilogue already dequantised them and rounded
+// them to bf16, so this kernel only copies rows into shared memory.
 //
 // Layout of the work: the G = H/Hkv query heads that share a KV head are stacked
 // into rows r = h_local * M + m, so one K/V tile serves all of them. A CTA owns
@@ -37,10 +37,8 @@ constexpr int kChunk = 64;       // keys per online-softmax chunk
 constexpr int kMaxSplit = 8;     // portable cluster size
 
 struct KParams {
-  const float* y;
-  int nparts, ldy;
-  const float* sa;
-  const float* sw;
+  const __nv_bfloat16* qkv;   // [M][ldq]
+  int ldq;
   const __nv_bfloat16* kpre;
   const __nv_bfloat16* vpre;
   void* out;
@@ -71,19 +69,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Sum of the partial planes of one 4-column group, times the dequant scale.
-__device__ __forceinline__ float4 reduce_parts4(const float* __restrict__ y, int nparts, size_t plane, size_t off,
-                                                float ds) {
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = 0; p < nparts; ++p) {
-    const float4 v = *reinterpret_cast<const float4*>(y + p * plane + off);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  return make_float4(acc.x * ds, acc.y * ds, acc.z * ds, acc.w * ds);
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
   __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
@@ -111,51 +101,46 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int nkeys = p.P + p.M;
   const int t0 = split * p.kc;
   const int nvalid = min(p.kc, nkeys - t0);
-  const size_t plane = static_cast<size_t>(p.M) * p.ldy;
 
   pdl_trigger();
 
-  // ---- prefix keys/values of this slice (written before this graph ran)
+  // ---- prefix keys/values of this slice (written before this graph ran): 16-byte
+  // asynchronous copies, all in flight together; rows past the last key are zeroed.
   for (int idx = tid; idx < p.kc * 16; idx += kThreads) {
     const int i = idx >> 4, c = idx & 15;
     const int t = t0 + i;
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
     if (t < p.P) {
       const size_t off = (static_cast<size_t>(t) * p.Hkv + g) * kDh + c * 8;
-      kv = *reinterpret_cast<const uint4*>(p.kpre + off);
-      vv = *reinterpret_cast<const uint4*>(p.vpre + off);
-    }
-    if (t < p.P || t >= nkeys) {
-      *reinterpret_cast<uint4*>(sK + i * kLds + c * 8) = kv;
-      *reinterpret_cast<uint4*>(sV + i * kLds + c * 8) = vv;
+      cp_async16(sK + i * kLds + c * 8, p.kpre + off);
+      cp_async16(sV + i * kLds + c * 8, p.vpre + off);
+    } else if (t >= nkeys) {
+      *reinterpret_cast<uint4*>(sK + i * kLds + c * 8) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sV + i * kLds + c * 8) = make_uint4(0, 0, 0, 0);
     }
   }
-  const float ds = __fmul_rn(*p.sa, *p.sw);
-  pdl_wait();
+  pdl_wait();   // Q, K, V of the chunk are written by the QKV GEMM
 
-  // ---- the chunk's own keys/values (rows P..P+M-1 of the key axis)
-  const int c_lo = max(t0, p.P), c_hi = min(t0 + p.kc, nkeys);
-  for (int idx = tid; idx < (c_hi > c_lo ? (c_hi - c_lo) : 0) * 32; idx += kThreads) {
-    const int t = c_lo + (idx >> 5), e4 = idx & 31;
-    const int m = t - p.P, i = t - t0;
-    const size_t base = static_cast<size_t>(m) * p.ldy;
-    const float4 kf = reduce_parts4(p.y, p.nparts, plane, base + (p.H + g) * kDh + e4 * 4, ds);
-    const float4 vf = reduce_parts4(p.y, p.nparts, plane, base + (p.H + p.Hkv + g) * kDh + e4 * 4, ds);
-    store_bf16x4(sK + i * kLds + e4 * 4, kf);
-    store_bf16x4(sV + i * kLds + e4 * 4, vf);
-  }
-  // ---- stacked query rows
-  for (int idx = tid; idx < kRows * 32; idx += kThreads) {
-    const int r = idx >> 5, e4 = idx & 31;
+  // ---- stacked query rows and the chunk's own keys/values (key rows P..P+M-1):
+  // bf16 rows of the QKV GEMM's dequantised output, copied asynchronously.
+  for (int idx = tid; idx < kRows * 16; idx += kThreads) {
+    const int r = idx >> 4, c = idx & 15;
     const int R = qt * kRows + r;
-    float4 qf = make_float4(0.f, 0.f, 0.f, 0.f);
     if (R < p.G * p.M) {
       const int hl = R / p.M, m = R % p.M;
-      const int h = g * p.G + hl;
-      qf = reduce_parts4(p.y, p.nparts, plane, static_cast<size_t>(m) * p.ldy + h * kDh + e4 * 4, ds);
+      cp_async16(sQ + r * kLds + c * 8, p.qkv + static_cast<size_t>(m) * p.ldq + (g * p.G + hl) * kDh + c * 8);
+    } else {
+      *reinterpret_cast<uint4*>(sQ + r * kLds + c * 8) = make_uint4(0, 0, 0, 0);
     }
-    store_bf16x4(sQ + r * kLds + e4 * 4, qf);
   }
+  const int c_lo = max(t0, p.P), c_hi = min(t0 + p.kc, nkeys);
+  for (int idx = tid; idx < (c_hi > c_lo ? (c_hi - c_lo) : 0) * 16; idx += kThreads) {
+    const int t = c_lo + (idx >> 4), c = idx & 15;
+    const __nv_bfloat16* row = p.qkv + static_cast<size_t>(t - p.P) * p.ldq;
+    cp_async16(sK + (t - t0) * kLds + c * 8, row + (p.H + g) * kDh + c * 8);
+    cp_async16(sV + (t - t0) * kLds + c * 8, row + (p.H + p.Hkv + g) * kDh + c * 8);
+  }
+  cp_async_commit();
+  cp_async_wait_all();
   __syncthreads();
 
   // ---- per-warp attention over this slice, two passes over the keys:
@@ -248,14 +233,22 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   if (tid < kRows) {
     const uint32_t ml_local = smem_u32(sML + tid * 2);
     float mq[kMaxSplit], lq[kMaxSplit];
-    float mstar = -INFINITY;
-    for (int q = 0; q < p.nsplit; ++q) {
-      mq[q] = ld_dsmem_f32(map_dsmem(ml_local, q));
-      lq[q] = ld_dsmem_f32(map_dsmem(ml_local + 4, q));
-      mstar = fmaxf(mstar, mq[q]);
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q) {
+      if (q < p.nsplit) {
+        const uint32_t a = map_dsmem(ml_local, static_cast<uint32_t>(q));
+        mq[q] = ld_dsmem_f32(a);
+        lq[q] = ld_dsmem_f32(a + 4);
+      }
     }
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q)
+      if (q < p.nsplit) mstar = fmaxf(mstar, mq[q]);
     float lsum = 0.f;
-    for (int q = 0; q < p.nsplit; ++q) lsum += lq[q] * exp2f(mq[q] - mstar);
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q)
+      if (q < p.nsplit) lsum += lq[q] * exp2f(mq[q] - mstar);
     sStat[tid * 2] = mstar;
     sStat[tid * 2 + 1] = lsum;
   }
@@ -306,26 +299,49 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     }
   }
 
-  // ---- sum the slices' shares across the cluster in fixed slice order, quantise
+  // ---- sum the slices' shares across the cluster in fixed slice order, quantise.
+  // A thread owns 4 adjacent head-dim columns of one row (32 threads per row,
+  // 4 rows in flight per CTA) and issues the loads of all slices before summing.
   cluster_sync_all();
   {
     const int rank = static_cast<int>(cluster_rank());
     const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
-    const int e = tid;   // head-dim column
+    const int e4 = lane * 4;
     const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
     const uint32_t o_local = smem_u32(sO);
-    for (int r = rank * rows_per; r < min(kRows, (rank + 1) * rows_per); ++r) {
+    uint32_t peer[kMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q) peer[q] = q < p.nsplit ? map_dsmem(o_local, static_cast<uint32_t>(q)) : 0u;
+    const int r_end = min(kRows, (rank + 1) * rows_per);
+    for (int r = rank * rows_per + warp; r < r_end; r += kThreads / 32) {
       const int R = qt * kRows + r;
       if (R >= p.G * p.M) break;
-      float acc = 0.f;
-      for (int q = 0; q < p.nsplit; ++q) acc += ld_dsmem_f32(map_dsmem(o_local + (r * kDh + e) * 4, q));
+      const uint32_t off = static_cast<uint32_t>((r * kDh + e4) * 4);
+      float4 v[kMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q)
+        if (q < p.nsplit) v[q] = ld_dsmem_f32x4(peer[q] + off);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q) {
+        if (q < p.nsplit) {
+          acc.x += v[q].x;
+          acc.y += v[q].y;
+          acc.z += v[q].z;
+          acc.w += v[q].w;
+        }
+      }
       const int hl = R / p.M, m = R % p.M;
-      const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e;
+      const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e4;
       if (p.out_fp8) {
-        static_cast<uint8_t*>(p.out)[oidx] =
-            static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc * rs, __NV_SATFINITE, __NV_E4M3));
+        uchar4 c;
+        c.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.x * rs, __NV_SATFINITE, __NV_E4M3));
+        c.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.y * rs, __NV_SATFINITE, __NV_E4M3));
+        c.z = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.z * rs, __NV_SATFINITE, __NV_E4M3));
+        c.w = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.w * rs, __NV_SATFINITE, __NV_E4M3));
+        *reinterpret_cast<uchar4*>(static_cast<uint8_t*>(p.out) + oidx) = c;
       } else {
-        static_cast<__nv_bfloat16*>(p.out)[oidx] = __float2bfloat16_rn(acc);
+        store_bf16x4(static_cast<__nv_bfloat16*>(p.out) + oidx, acc);
       }
     }
   }
@@ -352,11 +368,8 @@ cudaError_t attn_configure() { return allow_max_dynamic_smem(reinterpret_cast<co
 
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   KParams p;
-  p.y = a.yqkv;
-  p.nparts = a.nparts;
-  p.ldy = (a.H + 2 * a.Hkv) * kDh;
-  p.sa = a.sa;
-  p.sw = a.sw;
+  p.qkv = a.qkv;
+  p.ldq = (a.H + 2 * a.Hkv) * kDh;
   p.kpre = a.kpre;
   p.vpre = a.vpre;
   p.out = a.out;

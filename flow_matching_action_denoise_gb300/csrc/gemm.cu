@@ -39,7 +39,10 @@ constexpr size_t kStageCap = 196 * 1024;         // shared-memory budget for the
 constexpr size_t kCtrlBytes = 256;
 
 struct KParams {
-  float* out;
+  float* out;               // fp32 partial planes [s/cs][M][N], or
+  __nv_bfloat16* out_bf16;  // when non-null (cs == s): bf16(sum * fp32(sa * sw)) [M][N]
+  const float* sa;
+  const float* sw;
   int M, N;
   int nkb_total, nkb_cta;
   int n_pad, stages, cs;
@@ -54,7 +57,7 @@ __host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-template <bool kFp8>
+template <bool kFp8, int kCs>
 __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                const __grid_constant__ CUtensorMap tmA,
                                                                const KParams p) {
@@ -68,8 +71,10 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   uint8_t* w_tiles = smem;
   uint8_t* a_tiles = smem + static_cast<size_t>(stages) * kWTileBytes;
   const size_t main_bytes = static_cast<size_t>(stages) * (kWTileBytes + a_tile_bytes);
-  const size_t red_bytes = p.cs > 1 ? static_cast<size_t>(p.n_pad) * kTileN * sizeof(float) : 0;
-  uint8_t* ctrl = smem + align_up(main_bytes > red_bytes ? main_bytes : red_bytes, 1024);
+  const int rows_per = (p.M + kCs - 1) / kCs;   // output rows each cluster rank finalises
+  float* recv = reinterpret_cast<float*>(smem + align_up(main_bytes, 1024));   // [kCs][rows_per][128]
+  uint8_t* ctrl = reinterpret_cast<uint8_t*>(recv) +
+                  align_up(static_cast<size_t>(kCs) * rows_per * kTileN * sizeof(float), 1024);
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
@@ -101,7 +106,9 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (kCs > 1) cluster_arrive_relaxed();   // paired with the wait before the first remote store
   const uint32_t tmem = *tmem_slot;
+  const float ds = p.out_bf16 ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
   // Dependents may start only once this CTA holds its TMEM: a later GEMM's CTAs that
   // wait for this grid must never be able to take the columns this CTA still needs.
   pdl_trigger();
@@ -164,7 +171,12 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     tc_commit(done);
   }
 
-  // ---------------- epilogue: TMEM -> registers -> global (or cluster reduction)
+  // ---------------- epilogue. Output row m belongs to cluster rank m mod cs, as its
+  // local row m / cs. Each CTA pushes its fp32 partial of every row into the
+  // owner's receive buffer (slot = its own rank) with remote shared-memory
+  // stores; after one cluster barrier each owner sums its rows over the cs slots
+  // in slice order and writes them with 16-byte stores. With cs == 1 the push is
+  // a local shared-memory store.
   pdl_wait();
   if (!mbar_wait(done, 0)) {
     atomicOr(p.err, kErrPipelineTimeout);
@@ -175,41 +187,61 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const bool abort = s_abort != 0;
   const int n_local = warp * 32 + lane;   // TMEM lane == weight row within the tile
   const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  float* red = reinterpret_cast<float*>(smem);   // [n_pad][128], reuses the drained ring
-  const size_t ncol = static_cast<size_t>(nt) * kTileN + n_local;
-  __syncwarp();   // tcgen05.ld is warp-collective
+  const int rank = kCs > 1 ? static_cast<int>(cluster_rank()) : 0;
+  const uint32_t recv_base = smem_u32(recv);
+  uint32_t peer[kCs];
+#pragma unroll
+  for (int q = 0; q < kCs; ++q)
+    peer[q] = (kCs > 1 ? map_dsmem(recv_base, static_cast<uint32_t>(q)) : recv_base) +
+              static_cast<uint32_t>((rank * rows_per * kTileN + n_local) * 4);
+  if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
+  __syncwarp();                  // tcgen05.ld is warp-collective
   for (int c = 0; c < p.n_pad; c += 16) {
     float v[16];
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
-    if (p.cs == 1) {
-      if (!abort) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int m = c + i;
-          if (m < p.M) p.out[(static_cast<size_t>(j) * p.M + m) * p.N + ncol] = v[i];
-        }
+    for (int i = 0; i < 16; ++i) {
+      if (c + i < p.M) {
+        // owner (c + i) % kCs == i % kCs since kCs divides 16; local row (c + i) / kCs
+        const uint32_t addr = peer[i % kCs] + static_cast<uint32_t>(((c + i) / kCs) * kTileN * 4);
+        if (kCs > 1)
+          st_dsmem_f32(addr, v[i]);
+        else
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v[i]) : "memory");
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) red[(c + i) * kTileN + n_local] = v[i];
     }
   }
-  if (p.cs > 1) {
-    cluster_sync_all();
-    const int rank = static_cast<int>(cluster_rank());
-    const int part = j / p.cs;
-    const int rows_per = (p.M + p.cs - 1) / p.cs;
-    const int m_lo = rank * rows_per;
-    const int m_hi = min(p.M, m_lo + rows_per);
-    if (!abort) {
-      for (int m = m_lo; m < m_hi; ++m) {
-        const uint32_t local = smem_u32(&red[m * kTileN + n_local]);
-        float acc = 0.f;
-        for (int q = 0; q < p.cs; ++q) acc += ld_dsmem_f32(map_dsmem(local, static_cast<uint32_t>(q)));
-        p.out[(static_cast<size_t>(part) * p.M + m) * p.N + ncol] = acc;
+  if (kCs > 1)
+    cluster_sync_all();   // all pushes into this CTA's receive buffer have landed
+  else
+    __syncthreads();
+  if (!abort) {
+    const int part = j / kCs;
+    const int c4 = lane * 4;
+    const size_t col = static_cast<size_t>(nt) * kTileN + c4;
+    for (int lr = warp; lr < rows_per; lr += kThreads / 32) {
+      const int m = lr * kCs + rank;
+      if (m >= p.M) break;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kCs; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kTileN + c4);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      if (p.out_bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * ds, acc.y * ds);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * ds, acc.w * ds);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p.out_bf16 + static_cast<size_t>(m) * p.N + col) = u;
+      } else {
+        *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(part) * p.M + m) * p.N + col) = acc;
       }
     }
-    cluster_sync_all();   // keep this CTA's shared memory alive until every peer has read it
   }
 
   // On an abandoned pipeline, let copies already in flight land before the CTA exits.
@@ -347,13 +379,15 @@ int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
   g->nkb_total = nkb_total;
   g->nkb_cta = nkb_total / s;
   const size_t stage_bytes = kWTileBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;
-  int st = static_cast<int>(kStageCap / stage_bytes);
+  const int rows_per = (M + cs - 1) / cs;
+  const size_t recv_bytes = align_up(static_cast<size_t>(cs) * rows_per * kTileN * sizeof(float), 1024);
+  if (recv_bytes + stage_bytes > kStageCap) return FM_ERR_SHAPE;
+  int st = static_cast<int>((kStageCap - recv_bytes) / stage_bytes);
   st = std::min(st, kMaxStages);
   st = std::min(st, g->nkb_cta);
   g->stages = std::max(st, 1);
   const size_t main_bytes = g->stages * stage_bytes;
-  const size_t red_bytes = cs > 1 ? static_cast<size_t>(g->n_pad) * kTileN * sizeof(float) : 0;
-  g->smem = 1024 + align_up(std::max(main_bytes, red_bytes), 1024) + kCtrlBytes;
+  g->smem = 1024 + align_up(main_bytes, 1024) + recv_bytes + kCtrlBytes;
   return FM_OK;
 }
 
@@ -382,15 +416,29 @@ cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted) {
 }
 
 cudaError_t gemm_configure() {
-  cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(skinny_gemm_kernel<true>));
-  if (e != cudaSuccess) return e;
-  return allow_max_dynamic_smem(reinterpret_cast<const void*>(skinny_gemm_kernel<false>));
+  const void* ks[8] = {reinterpret_cast<const void*>(skinny_gemm_kernel<true, 1>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 4>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 8>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 1>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 4>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 8>)};
+  for (const void* k : ks) {
+    const cudaError_t e = allow_max_dynamic_smem(k);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
-                        const LaunchOpts& o) {
+                        const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw) {
+  if (out_bf16 && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
   KParams p;
   p.out = out;
+  p.out_bf16 = out_bf16;
+  p.sa = sa;
+  p.sw = sw;
   p.M = g.M;
   p.N = g.N;
   p.nkb_total = g.nkb_total;
@@ -402,8 +450,18 @@ cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const Ge
   LaunchOpts lo = o;
   lo.cluster = dim3(1, static_cast<unsigned>(g.cs), 1);
   const dim3 grid(static_cast<unsigned>(g.N / kTileN), static_cast<unsigned>(g.s), 1);
-  if (g.fp8) return launch(skinny_gemm_kernel<true>, grid, dim3(kThreads), g.smem, lo, tmW, tmA, p);
-  return launch(skinny_gemm_kernel<false>, grid, dim3(kThreads), g.smem, lo, tmW, tmA, p);
+  const dim3 blk(kThreads);
+  switch (g.cs * 2 + (g.fp8 ? 1 : 0)) {
+    case 3: return launch(skinny_gemm_kernel<true, 1>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 5: return launch(skinny_gemm_kernel<true, 2>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 9: return launch(skinny_gemm_kernel<true, 4>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 17: return launch(skinny_gemm_kernel<true, 8>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 2: return launch(skinny_gemm_kernel<false, 1>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 4: return launch(skinny_gemm_kernel<false, 2>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 8: return launch(skinny_gemm_kernel<false, 4>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 16: return launch(skinny_gemm_kernel<false, 8>, grid, blk, g.smem, lo, tmW, tmA, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 size_t packed_weight_bytes(int N, int K, int fmt) {

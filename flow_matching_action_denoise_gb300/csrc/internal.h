@@ -77,8 +77,11 @@ int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g);
 bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
 // Weight tensor map over the packed tiles of a [N][K] weight.
 bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g);
+// out: fp32 partial planes [s/cs][M][N]; or, with out_bf16 (requires cs == s), the
+// dequantised product bf16(sum * fp32(*sa * *sw)) as [M][N].
 cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
-                        const LaunchOpts& o);
+                        const LaunchOpts& o, __nv_bfloat16* out_bf16 = nullptr, const float* sa = nullptr,
+                        const float* sw = nullptr);
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
 // Packing
@@ -136,10 +139,7 @@ struct GegluArgs {
 cudaError_t geglu_launch(const GegluArgs& g, const LaunchOpts& o);
 
 struct AttnArgs {
-  const float* yqkv;   // [nparts][M][(H+2Hkv)*Dh]
-  int nparts;
-  const float* sa;
-  const float* sw;
+  const __nv_bfloat16* qkv;    // [M][(H+2Hkv)*Dh] dequantised Q | K | V
   const __nv_bfloat16* kpre;   // [P][Hkv][Dh] of this layer
   const __nv_bfloat16* vpre;
   void* out;                   // [M][H*Dh] codes

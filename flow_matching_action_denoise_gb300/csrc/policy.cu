@@ -138,7 +138,13 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
     dv->gN[g] = N[g];
     dv->gK[g] = K[g];
     const int nkb = K[g] * dv->act_bytes / 128;
-    const int s = c->ksplit[g] > 0 ? c->ksplit[g] : auto_split(N[g] / 128, nkb);
+    int s = c->ksplit[g] > 0 ? c->ksplit[g] : auto_split(N[g] / 128, nkb);
+    if (g == 0 && c->ksplit[0] <= 0)   // the QKV GEMM reduces all its slices in one cluster
+      while (s > 8 || (s & (s - 1)) || nkb % s) --s;
+    if (g == 0 && (s > 8 || (s & (s - 1)))) {
+      *why = "the QKV K-split must be 1, 2, 4 or 8 (its slices are reduced within one cluster)";
+      return FM_ERR_SHAPE;
+    }
     const int st = fm::gemm_plan(c->M, N[g], K[g], dv->fp8, s, cluster_for(s), &dv->gs[g]);
     if (st != FM_OK) {
       char buf[160];
@@ -179,7 +185,8 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.q2 = ly.take(static_cast<size_t>(M) * d * dv.act_bytes);
   ly.mc = ly.take(static_cast<size_t>(M) * c->F * dv.act_bytes);
   for (int g = 0; g < 4; ++g)
-    ly.y[g] = ly.take(static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4);
+    ly.y[g] = ly.take(g == 0 ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
+                             : static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4);
   ly.err = ly.take(64);
   ly.amax = ly.take(64);
   ly.conds = ly.take(static_cast<size_t>(S) * d * sizeof(double));
@@ -288,7 +295,8 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   size_t ybytes[4];
   for (int g = 0; g < 4; ++g) {
     y[g] = p->at<float>(p->ly.y[g]);
-    ybytes[g] = static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * c.M * dv.gN[g] * 4;
+    ybytes[g] = g == 0 ? static_cast<size_t>(c.M) * dv.gN[0] * 2
+                       : static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * c.M * dv.gN[g] * 4;
   }
   const int fp8 = dv.fp8;
   const size_t xbytes = static_cast<size_t>(c.M) * c.d * 4;
@@ -303,15 +311,14 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   FM_REC(p->at<void>(p->ly.x), xbytes);
   FM_REC(p->at<void>(p->ly.q), static_cast<size_t>(c.M) * c.d * ab);
 
-  e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], y[0], err, o);
+  // QKV: the epilogue dequantises and rounds to bf16, the operand attention reads
+  e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], nullptr, err, o,
+                      reinterpret_cast<__nv_bfloat16*>(y[0]), p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0));
   if (e != cudaSuccess) return e;
   FM_REC(y[0], ybytes[0]);
 
   fm::AttnArgs at;
-  at.yqkv = y[0];
-  at.nparts = dv.gs[0].s / dv.gs[0].cs;
-  at.sa = p->ascale(l, FM_SITE_ATTN_IN);
-  at.sw = p->wscale(l, 0);
+  at.qkv = reinterpret_cast<const __nv_bfloat16*>(y[0]);
   const size_t kv_layer = static_cast<size_t>(c.P) * c.Hkv * c.Dh;
   at.kpre = p->at<__nv_bfloat16>(p->ly.kcache) + l * kv_layer;
   at.vpre = p->at<__nv_bfloat16>(p->ly.vcache) + l * kv_layer;
@@ -426,7 +433,8 @@ size_t trace_record_bytes(const fm_policy* p) {
   const Derived& dv = p->dv;
   const size_t M = c.M, ab = dv.act_bytes;
   size_t n = 3 * M * c.d * 4 + M * c.d * ab * 2 + M * c.H * c.Dh * ab + M * c.F * ab + p->ly.a_bytes;
-  for (int g = 0; g < 4; ++g) n += static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4;
+  n += M * dv.gN[0] * 2;
+  for (int g = 1; g < 4; ++g) n += static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4;
   return n;
 }
 
@@ -862,7 +870,7 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
       {"q2", ly.q2, M * c.d * ab},
       {"attn_out", ly.o, M * c.H * c.Dh * ab},
       {"geglu_out", ly.mc, M * c.F * ab},
-      {"y_qkv", ly.y[0], ypart(0)},
+      {"y_qkv", ly.y[0], M * dv.gN[0] * 2},
       {"y_o", ly.y[1], ypart(1)},
       {"y_gu", ly.y[2], ypart(2)},
       {"y_d", ly.y[3], ypart(3)},

@@ -75,7 +75,23 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   const int N = r.N;
   const int n4 = N / 4;
   pdl_trigger();
+  // Per-create constants (scales, modulation rows) do not depend on the previous
+  // kernel: fetch them before waiting for it.
   const float ds = r.parts ? __fmul_rn(*r.sa, *r.sw) : 0.f;
+  const float rs_q = (r.do_quant && r.q_fp8) ? 1.0f / *r.sq : 1.0f;
+  constexpr int kPre = 2;   // column groups per thread kept in registers (N <= 2048)
+  float4 gate_v[kPre], scale_v[kPre], shift_v[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int c = tid + u * kRowThreads;
+    if (c < n4) {
+      if (r.gate) gate_v[u] = *reinterpret_cast<const float4*>(r.gate + c * 4);
+      if (r.do_quant) {
+        scale_v[u] = *reinterpret_cast<const float4*>(r.scale + c * 4);
+        shift_v[u] = *reinterpret_cast<const float4*>(r.shift + c * 4);
+      }
+    }
+  }
   pdl_wait();
 
   float* xrow = r.x + static_cast<size_t>(m) * N;
@@ -98,7 +114,8 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
       }
       float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
       if (r.bias) b = *reinterpret_cast<const float4*>(r.bias + c * 4);
-      const float4 gt = *reinterpret_cast<const float4*>(r.gate + c * 4);
+      const int u = (c - tid) / kRowThreads;
+      const float4 gt = u < kPre ? gate_v[u] : *reinterpret_cast<const float4*>(r.gate + c * 4);
       x.x = fmaf(gt.x, fmaf(acc.x, ds, b.x), x.x);
       x.y = fmaf(gt.y, fmaf(acc.y, ds, b.y), x.y);
       x.z = fmaf(gt.z, fmaf(acc.z, ds, b.z), x.z);
@@ -185,11 +202,12 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   // ---- AdaRMSNorm + static-scale quantisation into the next GEMM's operand
   if (r.do_quant) {
     const float rr = rsqrtf(block_sum(ss, red) / N + r.eps);
-    const float rs = r.q_fp8 ? 1.0f / *r.sq : 1.0f;
+    const float rs = rs_q;
     for (int c = tid; c < n4; c += kRowThreads) {
       const float4 x = *reinterpret_cast<const float4*>(xs + c * 4);
-      const float4 sc = *reinterpret_cast<const float4*>(r.scale + c * 4);
-      const float4 sh = *reinterpret_cast<const float4*>(r.shift + c * 4);
+      const int u = (c - tid) / kRowThreads;
+      const float4 sc = u < kPre ? scale_v[u] : *reinterpret_cast<const float4*>(r.scale + c * 4);
+      const float4 sh = u < kPre ? shift_v[u] : *reinterpret_cast<const float4*>(r.shift + c * 4);
       float4 h;
       h.x = fmaf(x.x * rr, 1.f + sc.x, sh.x);
       h.y = fmaf(x.y * rr, 1.f + sc.y, sh.y);

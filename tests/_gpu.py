@@ -77,7 +77,7 @@ def parse_trace(raw, cfg, pol):
         return nbytes // (M * n * 4)
 
     layout = [("x_in", "f", (M, d)), ("q", "c", (M, d)),
-              ("y_qkv", "f", (parts("y_qkv", cfg.n_qkv), M, cfg.n_qkv)),
+              ("y_qkv", "b", (M, cfg.n_qkv)),
               ("attn_out", "c", (M, cfg.H * cfg.Dh)), ("y_o", "f", (parts("y_o", d), M, d)),
               ("x_mid", "f", (M, d)), ("q2", "c", (M, d)),
               ("y_gu", "f", (parts("y_gu", 2 * cfg.F), M, 2 * cfg.F)), ("geglu_out", "c", (M, cfg.F)),
@@ -90,10 +90,12 @@ def parse_trace(raw, cfg, pol):
             r = {}
             for name, kind, shape in layout:
                 n = int(np.prod(shape))
-                nb = n * (4 if kind == "f" else ab)
+                nb = n * (4 if kind == "f" else 2 if kind == "b" else ab)
                 chunk = raw[off:off + nb]
                 off += nb
-                if kind == "f":
+                if kind == "b":
+                    r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
+                elif kind == "f":
                     r[name] = chunk.view(np.float32).reshape(shape).astype(np.float64)
                 elif fp8:
                     r[name] = C.e4m3_decode_code(chunk).reshape(shape)

@@ -177,16 +177,16 @@ def test_decision_fp8_every_stage_vs_oracle(expert):
             where = f"step {k} layer {l}"
             _check_codes(r["q"], O.quant_codes(O.ada_norm(r["x_in"], sc1, sh1, cfg.eps), sc[l, 0], "fp8"),
                          where + " pre-attention quantise")
-            yq = r["y_qkv"].sum(0)
-            _check_close(yq, r["q"] @ W["qkv"].codes.T, where + " QKV GEMM")
-            # the attention stage's input: bf16 of the fp32 dequantised sum, as the kernel forms it
-            acc = np.zeros(r["y_qkv"].shape[1:], np.float32)
-            for plane in r["y_qkv"]:
-                acc = acc + plane.astype(np.float32)
-            qkv = (acc * (np.float32(sc[l, 0]) * np.float32(W["qkv"].scale))).astype(np.float64)
-            Q = C.bf16(qkv[:, :H * Dh])
-            Kc = C.bf16(qkv[:, H * Dh:(H + cfg.Hkv) * Dh])
-            Vc = C.bf16(qkv[:, (H + cfg.Hkv) * Dh:])
+            # QKV: the GEMM epilogue emits bf16(sum * fp32(s_a * s_w)); within one bf16
+            # rounding of the exact dequantised product
+            qkv = r["y_qkv"]
+            exact = (r["q"] @ W["qkv"].codes.T) * np.float64(np.float32(sc[l, 0]) * np.float32(W["qkv"].scale))
+            assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-5 * np.sqrt(np.mean(exact ** 2))), \
+                where + " QKV GEMM"
+            # the attention stage's input is exactly the recorded bf16 Q | K | V
+            Q = qkv[:, :H * Dh]
+            Kc = qkv[:, H * Dh:(H + cfg.Hkv) * Dh]
+            Vc = qkv[:, (H + cfg.Hkv) * Dh:]
             Oref = O.attention(Q, Kc, Vc, kp[l], vp[l], H, cfg.Hkv, Dh)
             # attention rounds its probabilities to bf16: a near-tie probability rounding
             # either way moves a row of O by up to 2^-9 * P * |V|, so its allowance is 2^-7 * RMS
