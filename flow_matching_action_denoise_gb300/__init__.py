@@ -39,6 +39,7 @@ EXPORTS = [
     "fm_state_size", "snapshot_state", "restore_state", "fm_device_status", "fm_test_kernel_count",
     "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight", "fm_test_skinny_gemm",
     "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
+    "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer",
 ]
 
 
@@ -106,7 +107,9 @@ def load() -> ctypes.CDLL:
         "fm_test_layer": (i, [vp, vp, i, i, vp, vp, vp]),
         "fm_named_buffer": (i, [vp, ctypes.c_char_p, ctypes.POINTER(vp), ctypes.POINTER(sz)]),
         "fm_trace_size": (i, [vp, ctypes.POINTER(sz)]),
-        "fm_decode_trace": (i, [vp, vp, vp, vp, sz, vp]),
+        "fm_gemm_consumer_scratch_bytes": (i, [i, i, i, i, i, ctypes.POINTER(sz)]),
+        "fm_gemm_consumer": (i, [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz,
+                                 vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -286,6 +289,19 @@ def fm_test_consumer(partials, nparts: int, M: int, N: int, s_a, s_w, bias, x, g
     _check(load().fm_test_consumer(_ptr(partials), nparts, M, N, _ptr(s_a), _ptr(s_w), _ptr(bias), _ptr(x),
                                    _ptr(gate), _ptr(scale), _ptr(shift), float(eps), _ptr(s_q), _ptr(q),
                                    act_fmt, _stream(stream)), "fm_test_consumer")
+
+
+def gemm_consumer_scratch_bytes(M: int, N: int, K: int, fmt: int, s: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_gemm_consumer_scratch_bytes(M, N, K, fmt, s, ctypes.byref(n)), "fm_gemm_consumer_scratch_bytes")
+    return n.value
+
+
+def fm_gemm_consumer(a, M: int, K: int, w_packed, N: int, fmt: int, s: int, s_a, s_w, bias, x, gate, scale,
+                     shift, eps: float, s_q, q, scratch, scratch_bytes: int, stream=None):
+    _check(load().fm_gemm_consumer(_ptr(a), M, K, _ptr(w_packed), N, fmt, s, _ptr(s_a), _ptr(s_w), _ptr(bias),
+                                   _ptr(x), _ptr(gate), _ptr(scale), _ptr(shift), float(eps), _ptr(s_q), _ptr(q),
+                                   _ptr(scratch), scratch_bytes, _stream(stream)), "fm_gemm_consumer")
 
 
 def fm_test_layer(p: int, x_in, layer: int, step: int, x_out, q_out, stream=None):

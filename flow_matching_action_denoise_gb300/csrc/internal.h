@@ -154,6 +154,33 @@ size_t attn_smem_bytes(int kc);
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
 cudaError_t attn_configure();
 
+// ---------------------------------------------------------------- standalone GEMM + consumer
+struct GemmConsumerArgs {
+  const void* a;   // [M][K] fp8 codes or bf16
+  int M, K, N, fmt, s;
+  const void* w_packed;
+  const float* s_a;
+  const float* s_w;
+  const float* bias;   // may be null
+  float* x;            // [M][N] in/out
+  const float* gate;
+  const float* scale;
+  const float* shift;
+  float eps;
+  const float* s_q;
+  void* q;             // [M][N] codes
+};
+// Bytes of fp32 split-K partial planes the pair needs; FM_OK or a status.
+int gemm_consumer_scratch_bytes(int M, int N, int K, int fmt, int s, size_t* bytes, const char** why);
+// Validate, plan and launch the skinny GEMM into `scratch` (fp32 partial planes)
+// and the fused consumer reading them. Returns FM_OK or a status; *why on failure.
+int gemm_consumer_run(const GemmConsumerArgs& g, float* scratch, size_t scratch_bytes, int* err_word,
+                      cudaStream_t st, const char** why);
+
+// Record `why` as the thread's last policy-free error (what fm_last_error(NULL)
+// reports) and return `status`.
+int record_error(int status, const char* why);
+
 // ---------------------------------------------------------------- create-time kernels
 cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, cudaStream_t st);
 cudaError_t modtable_launch(const double* conds, int S, int d, const __nv_bfloat16* w_mod, const float* b_mod,

@@ -528,6 +528,91 @@ int check_ptrs(const fm_weights* w, int L, bool given, std::string* why) {
 
 }  // namespace
 
+namespace fm {
+
+int record_error(int status, const char* why) { return fail(nullptr, status, why); }
+
+int gemm_consumer_scratch_bytes(int M, int N, int K, int fmt, int s, size_t* bytes, const char** why) {
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) {
+    *why = "fmt must be FM_FMT_FP8 or FM_FMT_BF16";
+    return FM_ERR_INVALID_ARG;
+  }
+  GemmShape g;
+  if (gemm_plan(M, N, K, fmt == FM_FMT_FP8, s, cluster_for(s), &g) != FM_OK || N > 16384) {
+    *why = "shape: 1 <= M <= 256, N and K multiples of 128, N <= 16384, s dividing the K-block count";
+    return FM_ERR_SHAPE;
+  }
+  *bytes = static_cast<size_t>(g.s / g.cs) * M * N * sizeof(float);
+  return FM_OK;
+}
+
+int gemm_consumer_run(const GemmConsumerArgs& a, float* scratch, size_t scratch_bytes, int* err_word,
+                      cudaStream_t st, const char** why) {
+  if (!a.a || !a.w_packed || !a.s_a || !a.s_w || !a.x || !a.gate || !a.scale || !a.shift || !a.s_q || !a.q ||
+      !scratch) {
+    *why = "NULL argument";
+    return FM_ERR_INVALID_ARG;
+  }
+  size_t need = 0;
+  const int st0 = gemm_consumer_scratch_bytes(a.M, a.N, a.K, a.fmt, a.s, &need, why);
+  if (st0 != FM_OK) return st0;
+  if (scratch_bytes < need) {
+    *why = "scratch smaller than the split-K partial planes need";
+    return FM_ERR_WORKSPACE;
+  }
+  const void* ptrs[8] = {a.a, a.x, a.gate, a.scale, a.shift, a.q, scratch, a.bias ? a.bias : a.x};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) {
+      *why = "pointers must be 16-byte aligned";
+      return FM_ERR_ALIGN;
+    }
+  if (reinterpret_cast<uintptr_t>(a.w_packed) % kAlign) {
+    *why = "w_packed must be 1024-byte aligned";
+    return FM_ERR_ALIGN;
+  }
+  GemmShape g;
+  gemm_plan(a.M, a.N, a.K, a.fmt == FM_FMT_FP8, a.s, cluster_for(a.s), &g);
+  CUtensorMap tw, ta;
+  if (!gemm_tmap_weight(&tw, a.w_packed, g) || !gemm_tmap_act(&ta, a.a, g)) {
+    *why = "cuTensorMapEncodeTiled failed";
+    return FM_ERR_CUDA;
+  }
+  if (gemm_configure() != cudaSuccess) {
+    *why = "configuring the GEMM kernels failed";
+    return FM_ERR_CUDA;
+  }
+  LaunchOpts o;
+  o.stream = st;
+  if (gemm_launch(tw, ta, g, scratch, err_word, o) != cudaSuccess) {
+    *why = "GEMM launch failed";
+    return FM_ERR_CUDA;
+  }
+  RowArgs r = {};
+  r.M = a.M;
+  r.N = a.N;
+  r.parts = scratch;
+  r.nparts = g.s / g.cs;
+  r.sa = a.s_a;
+  r.sw = a.s_w;
+  r.bias = a.bias;
+  r.gate = a.gate;
+  r.x = a.x;
+  r.do_quant = 1;
+  r.scale = a.scale;
+  r.shift = a.shift;
+  r.sq = a.s_q;
+  r.q = a.q;
+  r.q_fp8 = a.fmt == FM_FMT_FP8;
+  r.eps = a.eps;
+  if (row_launch(r, o) != cudaSuccess) {
+    *why = "consumer launch failed";
+    return FM_ERR_CUDA;
+  }
+  return FM_OK;
+}
+
+}  // namespace fm
+
 // ==================================================================== C ABI
 extern "C" {
 
@@ -969,6 +1054,27 @@ int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N
   o.stream = static_cast<cudaStream_t>(stream);
   e = fm::gemm_launch(tw, ta, g, partials, err_word, o);
   return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "skinny_gemm launch");
+}
+
+int fm_gemm_consumer_scratch_bytes(int M, int N, int K, int fmt, int s, size_t* bytes) {
+  if (!bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "bytes is NULL");
+  const char* why = "";
+  const int st = fm::gemm_consumer_scratch_bytes(M, N, K, fmt, s, bytes, &why);
+  return st == FM_OK ? FM_OK : fail(nullptr, st, why);
+}
+
+int fm_gemm_consumer(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s, const float* s_a,
+                     const float* s_w, const float* bias, float* x, const float* gate, const float* scale,
+                     const float* shift, float eps, const float* s_q, void* q, void* scratch, size_t scratch_bytes,
+                     void* stream) {
+  int* err_word = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err_word), fm_standalone_err);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
+  const fm::GemmConsumerArgs g{a, M, K, N, fmt, s, w_packed, s_a, s_w, bias, x, gate, scale, shift, eps, s_q, q};
+  const char* why = "";
+  const int st = fm::gemm_consumer_run(g, static_cast<float*>(scratch), scratch_bytes, err_word,
+                                       static_cast<cudaStream_t>(stream), &why);
+  return st == FM_OK ? FM_OK : fail(nullptr, st, why);
 }
 
 int fm_test_consumer(const float* partials, int nparts, int M, int N, const float* s_a, const float* s_w,

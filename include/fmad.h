@@ -282,6 +282,24 @@ int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt,
 int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt,
                         int s, int cluster_reduce, float* partials, void* stream);
 
+/* Bytes of scratch fm_gemm_consumer needs for its fp32 split-K partial planes. */
+int fm_gemm_consumer_scratch_bytes(int M, int N, int K, int fmt, int s, size_t* bytes);
+
+/* Skinny GEMM + fused consumer in one call (blog post, "Small-M GEMM": K-split
+ * with FP32 partials reduced by the consumer, which applies its own transform;
+ * section "Static quantisation": bias + gated residual + AdaRMSNorm + static
+ * quantise): y = (A Wcodes^T) * fp32(s_a * s_w) + bias, x <- x + gate * y,
+ * q = Q(AdaRMSNorm(x; scale, shift), s_q). The s K-slices' partials go through
+ * `scratch` (device, 16-byte aligned, >= fm_gemm_consumer_scratch_bytes; its
+ * contents on entry do not matter). A, w_packed, fmt and s as in
+ * fm_test_skinny_gemm (N <= 16384); bias (may be NULL), gate, scale, shift
+ * device fp32 [N]; x device fp32 [M][N] in/out; s_a, s_w, s_q device fp32 [1];
+ * q device [M][N] codes (E4M3 bytes for FP8, bf16 for BF16). */
+int fm_gemm_consumer(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s, const float* s_a,
+                     const float* s_w, const float* bias, float* x, const float* gate, const float* scale,
+                     const float* shift, float eps, const float* s_q, void* q, void* scratch, size_t scratch_bytes,
+                     void* stream);
+
 /* Fused consumer (blog post, "Static quantisation"): with y = (sum_j
  * partials[j]) * fp32(s_a * s_w) + bias,  x <- x + gate * y,
  * q = Q(AdaRMSNorm(x; scale, shift), s_q) where Q is E4M3 with the fp32

@@ -181,3 +181,70 @@ def test_consumer_vs_oracle(device, M, N, nparts):
     dist = code_step_distance(qg, qr)
     assert np.max(dist) <= 1
     assert np.mean(dist > 0) <= 1e-3
+
+
+# ---------------------------------------------------------------- GEMM + fused consumer in one call
+
+def gemm_consumer_case(device, M, K, N, fmt, seed=2):
+    """Inputs for fm_gemm_consumer on the device and the oracle's expected outputs."""
+    case = fm_synth.gemm_case(M, K, N, seed=seed)
+    act = "fp8" if fmt == fmad.FMT_FP8 else "bf16"
+    if act == "fp8":
+        s_a = float(np.float32(np.max(np.abs(case["a"])) / np.float32(448)))
+        a_codes = O.quant_codes(case["a"], s_a, "fp8")
+        a_dev = dev(C.e4m3_encode_code(a_codes), device)
+    else:
+        s_a = 1.0
+        a_codes = C.bf16(case["a"])
+        a_dev = dev(a_codes.astype(np.float32), device, torch.bfloat16)
+    pw = O.prep_weight(case["w"], None, act)
+    y, x_ref, _ = O.gemm_consumer(a_codes, s_a, pw, case["bias"], case["x"], case["gate"], case["scale"],
+                                  case["shift"], 1.0, 1e-6, act)
+    h = O.ada_norm(x_ref, case["scale"], case["shift"], 1e-6)
+    s_q = float(np.float32(np.max(np.abs(h)) / np.float32(448))) if act == "fp8" else 1.0
+    q_ref = O.quant_codes(h, s_q, act)
+    nbytes = fmad.fm_packed_weight_bytes(N, K, fmt)
+    wbuf, wptr = aligned_empty(nbytes, device)
+    w_scale = torch.empty(1, dtype=torch.float32, device=device)
+    fmad.fm_pack_weight(dev(case["w"], device), None, N, K, fmt, wptr, w_scale)
+    f32 = lambda v: dev(np.asarray(v, np.float32), device)
+    inputs = dict(a=a_dev, w=(wbuf, wptr), s_a=f32([s_a]), s_w=w_scale, bias=f32(case["bias"]),
+                  x0=f32(case["x"]), gate=f32(case["gate"]), scale=f32(case["scale"]), shift=f32(case["shift"]),
+                  s_q=f32([s_q]))
+    return inputs, x_ref, q_ref
+
+
+def run_gemm_consumer(device, inp, M, K, N, fmt, s, entry="scratch"):
+    x = inp["x0"].clone()
+    q = torch.empty((M, N), dtype=torch.uint8 if fmt == fmad.FMT_FP8 else torch.bfloat16, device=device)
+    args = (inp["a"], M, K, inp["w"][1], N, fmt, s, inp["s_a"], inp["s_w"], inp["bias"], x, inp["gate"],
+            inp["scale"], inp["shift"], 1e-6, inp["s_q"], q)
+    if entry == "scratch":
+        nbytes = fmad.gemm_consumer_scratch_bytes(M, N, K, fmt, s)
+        scratch = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=device)
+        fmad.fm_gemm_consumer(*args, scratch, nbytes)
+    else:
+        fmad.fm_gemm_consumer_noalloc(*args)
+    torch.cuda.synchronize()
+    return x.cpu().numpy().astype(np.float64), q
+
+
+def check_gemm_consumer_outputs(x, q, x_ref, q_ref, fmt):
+    assert np.max(np.abs(x - x_ref)) <= 1e-5 * np.sqrt(np.mean(x_ref ** 2))
+    if fmt == fmad.FMT_FP8:
+        dist = code_step_distance(q.cpu().numpy(), C.e4m3_encode_code(q_ref))
+        assert np.max(dist) <= 1 and np.mean(dist > 0) <= 1e-3
+    else:
+        # a near-tie input may round to the neighbouring bf16 value: one step is at most
+        # 2^-7 of the value
+        qv = q.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(qv - q_ref) <= 2.0 ** -7 * np.abs(q_ref) + 1e-6 * np.sqrt(np.mean(q_ref ** 2)))
+
+
+@pytest.mark.parametrize("M,K,N,s,fmt", [(1, 1024, 1024, 1, fmad.FMT_FP8), (10, 2048, 4096, 4, fmad.FMT_FP8),
+                                         (50, 4096, 1024, 16, fmad.FMT_FP8), (63, 1024, 16384, 2, fmad.FMT_FP8),
+                                         (63, 1024, 4096, 2, fmad.FMT_BF16)])
+def test_gemm_consumer_vs_oracle(device, M, K, N, s, fmt):
+    inp, x_ref, q_ref = gemm_consumer_case(device, M, K, N, fmt)
+    x, q = run_gemm_consumer(device, inp, M, K, N, fmt, s)
+    check_gemm_consumer_outputs(x, q, x_ref, q_ref, fmt)
