@@ -39,7 +39,7 @@ EXPORTS = [
     "fm_state_size", "snapshot_state", "restore_state", "fm_device_status", "fm_test_kernel_count",
     "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight", "fm_test_skinny_gemm",
     "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
-    "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer",
+    "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer", "fm_gemm_consumer_noalloc",
 ]
 
 
@@ -110,6 +110,9 @@ def load() -> ctypes.CDLL:
         "fm_gemm_consumer_scratch_bytes": (i, [i, i, i, i, i, ctypes.POINTER(sz)]),
         "fm_gemm_consumer": (i, [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz,
                                  vp]),
+        "fm_gemm_consumer_noalloc": (i, [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                         vp]),
+        "fm_decode_trace": (i, [vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -302,6 +305,15 @@ def fm_gemm_consumer(a, M: int, K: int, w_packed, N: int, fmt: int, s: int, s_a,
     _check(load().fm_gemm_consumer(_ptr(a), M, K, _ptr(w_packed), N, fmt, s, _ptr(s_a), _ptr(s_w), _ptr(bias),
                                    _ptr(x), _ptr(gate), _ptr(scale), _ptr(shift), float(eps), _ptr(s_q), _ptr(q),
                                    _ptr(scratch), scratch_bytes, _stream(stream)), "fm_gemm_consumer")
+
+
+def fm_gemm_consumer_noalloc(a, M: int, K: int, w_packed, N: int, fmt: int, s: int, s_a, s_w, bias, x, gate,
+                             scale, shift, eps: float, s_q, q, stream=None):
+    """fm_gemm_consumer without a scratch argument, for callers that cannot allocate
+    device memory: the library's built-in 8 MiB device array holds the partials."""
+    _check(load().fm_gemm_consumer_noalloc(_ptr(a), M, K, _ptr(w_packed), N, fmt, s, _ptr(s_a), _ptr(s_w),
+                                           _ptr(bias), _ptr(x), _ptr(gate), _ptr(scale), _ptr(shift), float(eps),
+                                           _ptr(s_q), _ptr(q), _stream(stream)), "fm_gemm_consumer_noalloc")
 
 
 def fm_test_layer(p: int, x_in, layer: int, step: int, x_out, q_out, stream=None):

@@ -300,6 +300,19 @@ int fm_gemm_consumer(const void* a, int M, int K, const void* w_packed, int N, i
                      const float* shift, float eps, const float* s_q, void* q, void* scratch, size_t scratch_bytes,
                      void* stream);
 
+/* fm_gemm_consumer for callers that cannot allocate device memory (no
+ * counterpart in the paper). Same arguments and results, minus the scratch
+ * buffer: the split-K partials go to an 8 MiB array built into the library's
+ * device image, so this call allocates nothing. Shapes whose partials need more
+ * (s/cluster x M x N x 4 bytes > 8 MiB) return FM_ERR_WORKSPACE. The first call
+ * on each device looks the array's address up (make it before any stream
+ * capture); every GPU that loads the library keeps the array until exit; calls
+ * that overlap on the GPU share the array and race. */
+int fm_gemm_consumer_noalloc(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s,
+                             const float* s_a, const float* s_w, const float* bias, float* x, const float* gate,
+                             const float* scale, const float* shift, float eps, const float* s_q, void* q,
+                             void* stream);
+
 /* Fused consumer (blog post, "Static quantisation"): with y = (sum_j
  * partials[j]) * fp32(s_a * s_w) + bias,  x <- x + gate * y,
  * q = Q(AdaRMSNorm(x; scale, shift), s_q) where Q is E4M3 with the fp32

@@ -1,0 +1,55 @@
+"""fm_gemm_consumer_noalloc: the skinny GEMM + fused consumer for callers that cannot
+allocate device memory (code under an allocator that must not be re-entered, a
+control loop that forbids allocation after start-up, a host framework that hands
+the library only its inputs and outputs). It keeps the split-K partials in an
+array built into the library instead of caller scratch. Two calls in a row (the
+shared array still holds the previous call's data) must match fm_gemm_consumer,
+the entry point with caller scratch, within the same tolerances as its own test.
+
+This file is collected last so that a run stopping at its first failure has
+already run every other test.
+"""
+import pytest
+import torch
+
+import flow_matching_action_denoise_gb300 as fmad
+
+from _gpu import require_gpu
+from test_gpu_kernels import check_gemm_consumer_outputs, gemm_consumer_case, run_gemm_consumer
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(x_na, q_na, x_ref_gpu, q_ref_gpu, fmt):
+    """The allocation-free call against the scratch-taking call on the same inputs."""
+    import numpy as np
+    assert np.max(np.abs(x_na - x_ref_gpu)) <= 1e-5 * np.sqrt(np.mean(x_ref_gpu ** 2))
+    if fmt == fmad.FMT_FP8:
+        from _gpu import code_step_distance
+        dist = code_step_distance(q_na.cpu().numpy(), q_ref_gpu.cpu().numpy())
+        assert np.max(dist) <= 1 and np.mean(dist > 0) <= 1e-3
+    else:
+        a, b = q_na.float().cpu().numpy(), q_ref_gpu.float().cpu().numpy()
+        assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.abs(b) + 1e-6 * np.sqrt(np.mean(b ** 2)))
+
+
+def test_noalloc_matches_scratch_entry_on_consecutive_calls():
+    device = require_gpu()
+    cases = [(50, 1024, 8192, 2, fmad.FMT_FP8), (10, 4096, 1024, 16, fmad.FMT_FP8),
+             (63, 1024, 4096, 2, fmad.FMT_BF16), (50, 1024, 8192, 2, fmad.FMT_FP8)]
+    for i, (M, K, N, s, fmt) in enumerate(cases):
+        inp, x_oracle, q_oracle = gemm_consumer_case(device, M, K, N, fmt, seed=20 + i)
+        x_ref, q_ref = run_gemm_consumer(device, inp, M, K, N, fmt, s, entry="scratch")
+        x_na, q_na = run_gemm_consumer(device, inp, M, K, N, fmt, s, entry="noalloc")
+        _compare(x_na, q_na, x_ref, q_ref, fmt)
+        check_gemm_consumer_outputs(x_na, q_na, x_oracle, q_oracle, fmt)
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    device = require_gpu()
+    M, K, N, s = 256, 1024, 16384, 1   # 256 x 16384 x 4 bytes = 16 MiB of partials
+    assert fmad.gemm_consumer_scratch_bytes(M, N, K, fmad.FMT_FP8, s) > (8 << 20)
+    x = torch.zeros((M, N), dtype=torch.float32, device=device)
+    with pytest.raises(fmad.FmError) as e:
+        fmad.fm_gemm_consumer_noalloc(x, M, K, x, N, fmad.FMT_FP8, s, x, x, None, x, x, x, x, 1e-6, x, x)
+    assert e.value.status == 4 and "8 MiB" in str(e.value)
