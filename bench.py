@@ -124,11 +124,21 @@ def run_ours(args, rank, world, local_rank):
     weights = fmad.DeviceWeights(cfg, layers, final, device=device)
     del layers
     pol = fmad.Policy(cfg, act_scales=scales, weights=weights, device=device)
+    # launch-mode variants of the same policy (same kernels): graph without PDL, no graph
+    variants = {}
+    if not args.no_variants:
+        variants = {"graph_no_pdl": fmad.Policy(cfg, act_scales=scales, weights=weights, device=device,
+                                                flags=fmad.FLAG_USE_GRAPH),
+                    "eager_pdl": fmad.Policy(cfg, act_scales=scales, weights=weights, device=device,
+                                             flags=fmad.FLAG_USE_PDL)}
     del weights
     torch.cuda.empty_cache()
     kp, vp = fm_synth.prefix_kv(cfg)
-    pol.set_prefix_kv(torch.from_numpy(kp).to(device, torch.bfloat16),
-                      torch.from_numpy(vp).to(device, torch.bfloat16))
+    k_dev = torch.from_numpy(kp).to(device, torch.bfloat16)
+    v_dev = torch.from_numpy(vp).to(device, torch.bfloat16)
+    pol.set_prefix_kv(k_dev, v_dev)
+    for vpol in variants.values():
+        vpol.set_prefix_kv(k_dev, v_dev)
     noise = torch.from_numpy(fm_synth.noise(cfg, 0)).to(device)
     actions = torch.empty_like(noise)
     stream = torch.cuda.current_stream(device)
@@ -173,6 +183,21 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- dominant kernel timed alone: the gate|up skinny GEMM, rotating weight copies
     gemm = time_dominant_gemm(cfg, pol, device, stream)
+
+    # ---- launch-mode variants (PDL off, graph off), same kernels and inputs
+    variant_ms = {}
+    for name, vpol in variants.items():
+        for _ in range(args.warmup):
+            vpol.decode(noise, actions)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            vpol.decode(noise, actions)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        variant_ms[name] = round(e0.elapsed_time(e1) / args.steps, 4)
+        vpol.close()
 
     # ---- max over ranks
     if world > 1:
@@ -219,6 +244,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": gemm,
         "gpu_launches": int(per_decision * args.steps),
         "kernels_per_layer": per_layer,
+        "launch_variants_ms": variant_ms,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
@@ -332,6 +358,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
