@@ -301,8 +301,25 @@ def time_dominant_gemm(cfg, pol, device, stream):
                       f"split {s}, cluster {cs})",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind_note(kind),
-            "traffic": None, "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
+            "traffic": profiled_traffic(), "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
             "timing": "back-to-back launches, rotating weights over > 2x L2, CUDA events"}
+
+
+def profiled_traffic(name="skinny_gemm_gu_m50.md"):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    only while the kernel source is the one that was profiled (else None)."""
+    import hashlib
+    import re
+    try:
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        src = open(os.path.join(ROOT, "flow_matching_action_denoise_gb300", "csrc", "gemm.cu"), "rb").read()
+    except OSError:
+        return None
+    sha = re.search(r"sha256 prefix: ([0-9a-f]+)", text)
+    traffic = re.search(r"traffic_bytes_per_launch: (\d+)", text)
+    if not sha or not traffic or hashlib.sha256(src).hexdigest()[:len(sha.group(1))] != sha.group(1):
+        return None
+    return int(traffic.group(1))
 
 
 def peak_kind_note(kind):
@@ -351,6 +368,27 @@ def run_reference(args, rank, world):
             "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case():
+    """Small ncu target: a 1-layer, 1-step policy of the bench workload (about 18 MiB
+    on the device); the second decision runs inside a cudaProfilerStart/Stop range
+    (ncu --profile-from-start off)."""
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    cfg = fm_synth.config(WORKLOAD, L=1, S=1)
+    pol = fmad.Policy(cfg, [fm_synth.layer_weights(cfg, 0)], fm_synth.final_weights(cfg),
+                      act_scales=fm_synth.default_act_scales(cfg))
+    kp, vp = fm_synth.prefix_kv(cfg)
+    pol.set_prefix_kv(torch.from_numpy(kp).cuda().to(torch.bfloat16), torch.from_numpy(vp).cuda().to(torch.bfloat16))
+    noise = torch.from_numpy(fm_synth.noise(cfg, 0)).cuda()
+    pol.decode(noise)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    pol.decode(noise)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    pol.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,7 +397,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run only the small 1-layer, 1-step case for ncu (profiler range on its 2nd decision)")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case()
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
