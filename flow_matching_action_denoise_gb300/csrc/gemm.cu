@@ -41,6 +41,9 @@ constexpr size_t kCtrlBytes = 256;
 struct KParams {
   float* out;               // fp32 partial planes [s/cs][M][N], or
   __nv_bfloat16* out_bf16;  // when non-null (cs == s): bf16(sum * fp32(sa * sw)) [M][N]
+  void* out_geglu;          // when non-null (cs == s, gate|up interleaved): Q(gelu(g) u) [M][N/2]
+  int geglu_fp8;
+  const float* sq;          // static scale of the GeGLU output
   const float* sa;
   const float* sw;
   int M, N;
@@ -108,7 +111,8 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   tc_fence_after();
   if (kCs > 1) cluster_arrive_relaxed();   // paired with the wait before the first remote store
   const uint32_t tmem = *tmem_slot;
-  const float ds = p.out_bf16 ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
+  const float ds = (p.out_bf16 || p.out_geglu) ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
+  const float rs_geglu = (p.out_geglu && p.geglu_fp8) ? 1.0f / *p.sq : 1.0f;
   // Dependents may start only once this CTA holds its TMEM: a later GEMM's CTAs that
   // wait for this grid must never be able to take the columns this CTA still needs.
   pdl_trigger();
@@ -231,7 +235,41 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
         acc.z += v.z;
         acc.w += v.w;
       }
-      if (p.out_bf16) {
+      if (p.out_geglu) {
+        // lanes 0-15 hold gate columns 4L..4L+3 of this tile's 64 GeGLU columns, lanes
+        // 16-31 the matching up columns: m = gelu_tanh(g) * u, quantised
+        float4 up;
+        up.x = __shfl_xor_sync(0xffffffffu, acc.x, 16);
+        up.y = __shfl_xor_sync(0xffffffffu, acc.y, 16);
+        up.z = __shfl_xor_sync(0xffffffffu, acc.z, 16);
+        up.w = __shfl_xor_sync(0xffffffffu, acc.w, 16);
+        if (lane < 16) {
+          const float gv[4] = {acc.x * ds, acc.y * ds, acc.z * ds, acc.w * ds};
+          const float uv[4] = {up.x * ds, up.y * ds, up.z * ds, up.w * ds};
+          float mv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x = gv[e];
+            mv[e] = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * uv[e];
+          }
+          const size_t fidx = static_cast<size_t>(m) * (p.N / 2) + static_cast<size_t>(nt) * 64 + c4;
+          if (p.geglu_fp8) {
+            uchar4 c;
+            c.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[0] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
+            c.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[1] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
+            c.z = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[2] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
+            c.w = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[3] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
+            *reinterpret_cast<uchar4*>(static_cast<uint8_t*>(p.out_geglu) + fidx) = c;
+          } else {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(mv[0], mv[1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(mv[2], mv[3]);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t*>(&lo);
+            u.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out_geglu) + fidx) = u;
+          }
+        }
+      } else if (p.out_bf16) {
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * ds, acc.y * ds);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * ds, acc.w * ds);
         uint2 u;
@@ -285,8 +323,17 @@ __global__ void scale_from_amax_kernel(const unsigned* __restrict__ amax, float*
 __global__ void set_one_kernel(float* p) { *p = 1.0f; }
 
 // FP8: one thread writes 16 bytes (16 codes) of a [128][128]-byte tile.
+// Packed row n of a gate|up weight with interleave: tile t = n / 128 holds gate rows
+// 64t..64t+63 then the matching up rows F+64t..F+64t+63 (F = N/2), so one output tile
+// carries both halves of 64 GeGLU columns.
+__device__ __forceinline__ size_t source_row(size_t n, int N, int interleave) {
+  if (!interleave) return n;
+  const size_t t = n / 128, r = n % 128;
+  return r < 64 ? t * 64 + r : static_cast<size_t>(N / 2) + t * 64 + (r - 64);
+}
+
 __global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __restrict__ gamma, int N, int K,
-                                const float* __restrict__ scale, uint8_t* __restrict__ out) {
+                                const float* __restrict__ scale, uint8_t* __restrict__ out, int interleave) {
   const size_t chunks = static_cast<size_t>(N) * K / 16;
   const size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
   if (c >= chunks) return;
@@ -297,7 +344,7 @@ __global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __rest
   const int within = static_cast<int>(o % kWTileBytes);
   const int r = within / 128, cb = within % 128;
   const int ntile = static_cast<int>(tile / nkb), kb = static_cast<int>(tile % nkb);
-  const size_t n = static_cast<size_t>(ntile) * 128 + r;
+  const size_t n = source_row(static_cast<size_t>(ntile) * 128 + r, N, interleave);
   const int k0 = kb * 128 + cb;
   alignas(16) uint8_t codes[16];
 #pragma unroll
@@ -311,7 +358,7 @@ __global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __rest
 
 // BF16: one thread writes 16 bytes (8 values) of a [128][64]-element tile.
 __global__ void pack_bf16_kernel(const float* __restrict__ w, const float* __restrict__ gamma, int N, int K,
-                                 __nv_bfloat16* __restrict__ out) {
+                                 __nv_bfloat16* __restrict__ out, int interleave) {
   const size_t chunks = static_cast<size_t>(N) * K / 8;
   const size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
   if (c >= chunks) return;
@@ -321,7 +368,7 @@ __global__ void pack_bf16_kernel(const float* __restrict__ w, const float* __res
   const int within = static_cast<int>(e % (128 * 64));
   const int r = within / 64, ce = within % 64;
   const int ntile = static_cast<int>(tile / nkb), kb = static_cast<int>(tile % nkb);
-  const size_t n = static_cast<size_t>(ntile) * 128 + r;
+  const size_t n = source_row(static_cast<size_t>(ntile) * 128 + r, N, interleave);
   const int k0 = kb * 64 + ce;
   alignas(16) __nv_bfloat16 vals[8];
 #pragma unroll
@@ -432,11 +479,16 @@ cudaError_t gemm_configure() {
 }
 
 cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
-                        const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw) {
-  if (out_bf16 && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
+                        const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw,
+                        void* out_geglu, int geglu_fp8, const float* sq) {
+  if ((out_bf16 || out_geglu) && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
+  if (out_geglu && (!sq || g.N % 128)) return cudaErrorInvalidValue;
   KParams p;
   p.out = out;
   p.out_bf16 = out_bf16;
+  p.out_geglu = out_geglu;
+  p.geglu_fp8 = geglu_fp8;
+  p.sq = sq;
   p.sa = sa;
   p.sw = sw;
   p.M = g.M;
@@ -471,7 +523,7 @@ size_t packed_weight_bytes(int N, int K, int fmt) {
 }
 
 cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
-                        unsigned* amax_scratch, cudaStream_t st) {
+                        unsigned* amax_scratch, cudaStream_t st, int geglu_interleave) {
   const int threads = 256;
   if (fmt == FM_FMT_FP8) {
     cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), st);
@@ -480,14 +532,14 @@ cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fm
     scale_from_amax_kernel<<<1, 1, 0, st>>>(amax_scratch, scale_out);
     const size_t chunks = static_cast<size_t>(N) * K / 16;
     pack_fp8_kernel<<<static_cast<unsigned>((chunks + threads - 1) / threads), threads, 0, st>>>(
-        w, gamma, N, K, scale_out, static_cast<uint8_t*>(packed));
+        w, gamma, N, K, scale_out, static_cast<uint8_t*>(packed), geglu_interleave);
     return cudaGetLastError();
   }
   if (fmt == FM_FMT_BF16) {
     set_one_kernel<<<1, 1, 0, st>>>(scale_out);
     const size_t chunks = static_cast<size_t>(N) * K / 8;
     pack_bf16_kernel<<<static_cast<unsigned>((chunks + threads - 1) / threads), threads, 0, st>>>(
-        w, gamma, N, K, static_cast<__nv_bfloat16*>(packed));
+        w, gamma, N, K, static_cast<__nv_bfloat16*>(packed), geglu_interleave);
     return cudaGetLastError();
   }
   return cudaErrorInvalidValue;

@@ -79,15 +79,20 @@ bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
 bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g);
 // out: fp32 partial planes [s/cs][M][N]; or, with out_bf16 (requires cs == s), the
 // dequantised product bf16(sum * fp32(*sa * *sw)) as [M][N].
+// out_geglu (requires cs == s and a gate|up weight packed with interleave): the
+// epilogue applies m = gelu_tanh(g) * u to the dequantised sums and writes Q(m, *sq)
+// as [M][N/2] codes (E4M3 bytes if geglu_fp8, else bf16).
 cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16 = nullptr, const float* sa = nullptr,
-                        const float* sw = nullptr);
+                        const float* sw = nullptr, void* out_geglu = nullptr, int geglu_fp8 = 0,
+                        const float* sq = nullptr);
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
 // Packing
 size_t packed_weight_bytes(int N, int K, int fmt);
+// geglu_interleave: pack a gate|up weight [2F][K] so tile t holds gate rows 64t.. and up rows F+64t..
 cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
-                        unsigned* amax_scratch, cudaStream_t st);
+                        unsigned* amax_scratch, cudaStream_t st, int geglu_interleave = 0);
 
 // ---------------------------------------------------------------- row kernels
 struct RowArgs {
@@ -126,17 +131,7 @@ struct RowArgs {
 };
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o);
 
-struct GegluArgs {
-  int M, F;
-  const float* parts;   // [nparts][M][2F]
-  int nparts;
-  const float* sa;
-  const float* sw;
-  const float* sq;
-  void* q;   // [M][F]
-  int q_fp8;
-};
-cudaError_t geglu_launch(const GegluArgs& g, const LaunchOpts& o);
+
 
 struct AttnArgs {
   const __nv_bfloat16* qkv;    // [M][(H+2Hkv)*Dh] dequantised Q | K | V

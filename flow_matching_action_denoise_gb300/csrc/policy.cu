@@ -1,6 +1,6 @@
 // Policy object and C ABI of libfmad.so.
 //
-// A policy owns the plan of one decision - (L layers x 8 kernels) x S steps plus
+// A policy owns the plan of one decision - (L layers x 7 kernels) x S steps plus
 // one step-head kernel - recorded once as a CUDA graph whose kernel nodes carry
 // Programmatic Dependent Launch edges (news article "FlashRT-PAI", section "It
 // optimises the relay": launch overlap; blog post "Embodied inference
@@ -139,10 +139,13 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
     dv->gK[g] = K[g];
     const int nkb = K[g] * dv->act_bytes / 128;
     int s = c->ksplit[g] > 0 ? c->ksplit[g] : auto_split(N[g] / 128, nkb);
-    if (g == 0 && c->ksplit[0] <= 0)   // the QKV GEMM reduces all its slices in one cluster
+    // The QKV and gate|up GEMMs reduce all their K-slices inside one cluster (their
+    // epilogues emit bf16 Q|K|V and the GeGLU output), so their split is 1, 2, 4 or 8.
+    const bool whole_cluster = g == 0 || g == 2;
+    if (whole_cluster && c->ksplit[g] <= 0)
       while (s > 8 || (s & (s - 1)) || nkb % s) --s;
-    if (g == 0 && (s > 8 || (s & (s - 1)))) {
-      *why = "the QKV K-split must be 1, 2, 4 or 8 (its slices are reduced within one cluster)";
+    if (whole_cluster && (s > 8 || (s & (s - 1)))) {
+      *why = "the QKV and gate|up K-splits must be 1, 2, 4 or 8 (their slices are reduced within one cluster)";
       return FM_ERR_SHAPE;
     }
     const int st = fm::gemm_plan(c->M, N[g], K[g], dv->fp8, s, cluster_for(s), &dv->gs[g]);
@@ -185,7 +188,8 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.q2 = ly.take(static_cast<size_t>(M) * d * dv.act_bytes);
   ly.mc = ly.take(static_cast<size_t>(M) * c->F * dv.act_bytes);
   for (int g = 0; g < 4; ++g)
-    ly.y[g] = ly.take(g == 0 ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
+    ly.y[g] = ly.take(g == 2 ? 0 :   // the gate|up GEMM writes the GeGLU output directly
+                      g == 0 ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
                              : static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4);
   ly.err = ly.take(64);
   ly.amax = ly.take(64);
@@ -360,21 +364,9 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   FM_REC(p->at<void>(p->ly.x), xbytes);
   FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
 
-  e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], y[2], err, o);
-  if (e != cudaSuccess) return e;
-  FM_REC(y[2], ybytes[2]);
-
-  fm::GegluArgs gg;
-  gg.M = c.M;
-  gg.F = c.F;
-  gg.parts = y[2];
-  gg.nparts = dv.gs[2].s / dv.gs[2].cs;
-  gg.sa = p->ascale(l, FM_SITE_MLP_IN);
-  gg.sw = p->wscale(l, 2);
-  gg.sq = p->ascale(l, FM_SITE_GEGLU);
-  gg.q = p->at<void>(p->ly.mc);
-  gg.q_fp8 = fp8;
-  e = fm::geglu_launch(gg, o);
+  // gate|up: the epilogue applies GeGLU and quantises, writing the down GEMM's operand
+  e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], nullptr, err, o, nullptr, p->ascale(l, FM_SITE_MLP_IN),
+                      p->wscale(l, 2), p->at<void>(p->ly.mc), fp8, p->ascale(l, FM_SITE_GEGLU));
   if (e != cudaSuccess) return e;
   FM_REC(p->at<void>(p->ly.mc), static_cast<size_t>(c.M) * c.F * ab);
 
@@ -434,7 +426,7 @@ size_t trace_record_bytes(const fm_policy* p) {
   const size_t M = c.M, ab = dv.act_bytes;
   size_t n = 3 * M * c.d * 4 + M * c.d * ab * 2 + M * c.H * c.Dh * ab + M * c.F * ab + p->ly.a_bytes;
   n += M * dv.gN[0] * 2;
-  for (int g = 1; g < 4; ++g) n += static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4;
+  for (int g = 1; g < 4; g += 2) n += static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4;
   return n;
 }
 
@@ -701,7 +693,7 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
     const float* gam[4] = {lw.gamma1, nullptr, lw.gamma2, nullptr};
     for (int g = 0; g < 4; ++g) {
       if (!cu(fm::pack_weight(src[g], gam[g], dv.gN[g], dv.gK[g], c.weight_fmt, p->at<void>(p->ly.wpk[l * 4 + g]),
-                              p->wscale(l, g), amax, s),
+                              p->wscale(l, g), amax, s, g == 2),
               "pack_weight"))
         return bail(FM_ERR_CUDA, why);
     }
@@ -957,7 +949,6 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
       {"geglu_out", ly.mc, M * c.F * ab},
       {"y_qkv", ly.y[0], M * dv.gN[0] * 2},
       {"y_o", ly.y[1], ypart(1)},
-      {"y_gu", ly.y[2], ypart(2)},
       {"y_d", ly.y[3], ypart(3)},
       {"act_scales", ly.ascale, ly.scale_bytes},
       {"weight_scales", ly.wscale, ly.scale_bytes},
@@ -1000,8 +991,8 @@ int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trac
 
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) {
   if (!p || !per_layer || !per_decision) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
-  *per_layer = 8;
-  *per_decision = 1 + p->cfg.S * p->cfg.L * 8;
+  *per_layer = 7;
+  *per_decision = 1 + p->cfg.S * p->cfg.L * 7;
   return FM_OK;
 }
 

@@ -13,7 +13,6 @@
 // into the next GEMM's weights). The row statistic uses warp shuffles and one
 // shared-memory exchange.
 //
-// geglu_kernel: consumer of the gate|up GEMM: m = gelu_tanh(g) * u, quantised.
 // Create-time kernels: timestep embedding and the per-step modulation table.
 
 #include <cuda_bf16.h>
@@ -218,41 +217,6 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   }
 }
 
-__global__ void __launch_bounds__(kRowThreads) geglu_kernel(const GegluArgs g) {
-  const int m = blockIdx.x;
-  const int c = blockIdx.y * kRowThreads + threadIdx.x;   // 4-column group
-  pdl_trigger();
-  const float ds = __fmul_rn(*g.sa, *g.sw);
-  const float rs = g.q_fp8 ? 1.0f / *g.sq : 1.0f;
-  pdl_wait();
-  if (c * 4 >= g.F) return;
-  const size_t plane = static_cast<size_t>(g.M) * 2 * g.F;
-  const size_t row = static_cast<size_t>(m) * 2 * g.F;
-  float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), ua = ga;
-  for (int p = 0; p < g.nparts; ++p) {
-    const float4 gv = *reinterpret_cast<const float4*>(g.parts + p * plane + row + c * 4);
-    const float4 uv = *reinterpret_cast<const float4*>(g.parts + p * plane + row + g.F + c * 4);
-    ga.x += gv.x;
-    ga.y += gv.y;
-    ga.z += gv.z;
-    ga.w += gv.w;
-    ua.x += uv.x;
-    ua.y += uv.y;
-    ua.z += uv.z;
-    ua.w += uv.w;
-  }
-  const float k0 = 0.7978845608028654f, k1 = 0.044715f;
-  float gg[4] = {ga.x * ds, ga.y * ds, ga.z * ds, ga.w * ds};
-  float uu[4] = {ua.x * ds, ua.y * ds, ua.z * ds, ua.w * ds};
-  float hv[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float x = gg[i];
-    hv[i] = 0.5f * x * (1.f + tanhf(k0 * fmaf(k1 * x, x * x, x))) * uu[i];
-  }
-  store_q4(g.q, static_cast<size_t>(m) * g.F + c * 4, make_float4(hv[0], hv[1], hv[2], hv[3]), g.q_fp8, rs);
-}
-
 // ---------------------------------------------------------------- create-time kernels
 
 // cond[k][i]: the given vector, or the sinusoidal embedding of t_k = 1 - k/S
@@ -305,11 +269,6 @@ cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
     if (e != cudaSuccess) return e;
   }
   return launch(row_kernel, dim3(static_cast<unsigned>(r.M)), dim3(kRowThreads), smem, o, r);
-}
-
-cudaError_t geglu_launch(const GegluArgs& g, const LaunchOpts& o) {
-  const unsigned gy = static_cast<unsigned>((g.F / 4 + kRowThreads - 1) / kRowThreads);
-  return launch(geglu_kernel, dim3(static_cast<unsigned>(g.M), gy), dim3(kRowThreads), 0, o, g);
 }
 
 cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, cudaStream_t st) {

@@ -217,7 +217,8 @@ int fm_device_status(fm_policy* p, void* stream, int* word);
  *   "q", "q2"               codes [M][d] (pre-attention / pre-MLP GEMM operand)
  *   "attn_out"              codes [M][H*Dh]
  *   "geglu_out"             codes [M][F]
- *   "y_qkv", "y_o", "y_gu", "y_d"  fp32 [parts][M][N] GEMM partial planes
+ *   "y_qkv"                 bf16 [M][(H+2Hkv)*Dh] dequantised Q | K | V
+ *   "y_o", "y_d"            fp32 [parts][M][N] GEMM partial planes
  *   "act_scales", "weight_scales"  fp32 [L][4]
  *   "mod"                   fp32 [S][L][6][d]; "mod_final" fp32 [S][2][d]
  * Codes are one byte (FP8 activations) or bf16. FM_ERR_INVALID_ARG for an unknown name. */
@@ -233,13 +234,12 @@ int fm_trace_size(const fm_policy* p, size_t* bytes);
  * step-major then layer; each record holds, contiguously in this order:
  *   x_in fp32 [M][d]          residual stream entering the layer
  *   q codes [M][d]            pre-attention operand
- *   y_qkv fp32 [P0][M][Nqkv]  QKV partial planes (P0 = fm_named_buffer size / (M*Nqkv*4))
+ *   y_qkv bf16 [M][Nqkv]      dequantised Q | K | V (the QKV GEMM's output)
  *   attn_out codes [M][H*Dh]
- *   y_o fp32 [P1][M][d]
+ *   y_o fp32 [P1][M][d]       O partial planes (P1 = fm_named_buffer size / (M*d*4))
  *   x_mid fp32 [M][d]         after the attention gated residual
  *   q2 codes [M][d]
- *   y_gu fp32 [P2][M][2F]
- *   geglu_out codes [M][F]
+ *   geglu_out codes [M][F]    the gate|up GEMM's output (GeGLU applied in its epilogue)
  *   y_d fp32 [P3][M][d]
  *   x_out fp32 [M][d]         after the MLP gated residual; for the last layer of
  *                             a step that is not the last, the next step's x

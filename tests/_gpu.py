@@ -80,7 +80,7 @@ def parse_trace(raw, cfg, pol):
               ("y_qkv", "b", (M, cfg.n_qkv)),
               ("attn_out", "c", (M, cfg.H * cfg.Dh)), ("y_o", "f", (parts("y_o", d), M, d)),
               ("x_mid", "f", (M, d)), ("q2", "c", (M, d)),
-              ("y_gu", "f", (parts("y_gu", 2 * cfg.F), M, 2 * cfg.F)), ("geglu_out", "c", (M, cfg.F)),
+              ("geglu_out", "c", (M, cfg.F)),
               ("y_d", "f", (parts("y_d", d), M, d)), ("x_out", "f", (M, d)), ("actions", "f", (M, cfg.A))]
     off = 0
     recs = []
