@@ -134,20 +134,26 @@ cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o);
 
 
 struct AttnArgs {
-  const __nv_bfloat16* qkv;    // [M][(H+2Hkv)*Dh] dequantised Q | K | V
-  const __nv_bfloat16* kpre;   // [P][Hkv][Dh] of this layer
-  const __nv_bfloat16* vpre;
-  void* out;                   // [M][H*Dh] codes
+  const __nv_bfloat16* qkv;     // [M][(H+2Hkv)*Dh] dequantised Q | K | V
+  const __nv_bfloat16* kpre;    // [P][Hkv][Dh] of this layer
+  const __nv_bfloat16* vtpre;   // [Hkv][Dh][p_pad] of this layer (values transposed)
+  int p_pad;                    // P rounded up to a multiple of 8
+  void* out;                    // [M][H*Dh] codes
   const float* s_out;
   int out_fp8;
   int M, P, H, Hkv;
-  int kc;       // keys per split (multiple of 64)
-  int nsplit;   // splits = cluster size (<= 8)
+  int kc;       // keys per slice (multiple of 64, <= 192)
+  int nsplit;   // slices = cluster size (<= 8)
+  int* err;
 };
-void attn_plan(int M, int P, int* kc, int* nsplit);
+// Slice plan for P + M keys; FM_ERR_SHAPE when they need more than 8 x 192.
+int attn_plan(int M, int P, int* kc, int* nsplit);
 size_t attn_smem_bytes(int kc);
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
 cudaError_t attn_configure();
+// v [L][rows][Hkv][Dh] -> vt[l][g][d][tok_begin + t] (row stride p_pad).
+cudaError_t transpose_v_launch(const __nv_bfloat16* v, __nv_bfloat16* vt, int L, int rows, int Hkv, int p_pad,
+                               int tok_begin, cudaStream_t st);
 
 // ---------------------------------------------------------------- standalone GEMM + consumer
 struct GemmConsumerArgs {

@@ -156,7 +156,10 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
       return st;
     }
   }
-  fm::attn_plan(c->M, c->P, &dv->attn_kc, &dv->attn_nsplit);
+  if (fm::attn_plan(c->M, c->P, &dv->attn_kc, &dv->attn_nsplit) != FM_OK) {
+    *why = "P + M keys exceed the attention plan's 8 slices x 192 keys";
+    return FM_ERR_SHAPE;
+  }
   return FM_OK;
 }
 
@@ -177,7 +180,8 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.w_out = ly.take(static_cast<size_t>(d) * c->A * 2);
   ly.b_out = ly.take(static_cast<size_t>(c->A) * 4);
   ly.gamma_f = ly.take(static_cast<size_t>(d) * 4);
-  ly.kv_bytes = static_cast<size_t>(L) * c->P * c->Hkv * c->Dh * 2;
+  // K [L][P][Hkv][Dh]; V stored transposed [L][Hkv][Dh][P_pad], P_pad = P rounded up to 8
+  ly.kv_bytes = static_cast<size_t>(L) * ((c->P + 7) / 8 * 8) * c->Hkv * c->Dh * 2;
   ly.kcache = ly.take(ly.kv_bytes);
   ly.vcache = ly.take(ly.kv_bytes);
   ly.a_bytes = static_cast<size_t>(M) * c->A * 4;
@@ -323,9 +327,11 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
 
   fm::AttnArgs at;
   at.qkv = reinterpret_cast<const __nv_bfloat16*>(y[0]);
-  const size_t kv_layer = static_cast<size_t>(c.P) * c.Hkv * c.Dh;
-  at.kpre = p->at<__nv_bfloat16>(p->ly.kcache) + l * kv_layer;
-  at.vpre = p->at<__nv_bfloat16>(p->ly.vcache) + l * kv_layer;
+  const int p_pad = (c.P + 7) / 8 * 8;
+  at.kpre = p->at<__nv_bfloat16>(p->ly.kcache) + static_cast<size_t>(l) * c.P * c.Hkv * c.Dh;
+  at.vtpre = p->at<__nv_bfloat16>(p->ly.vcache) + static_cast<size_t>(l) * c.Hkv * c.Dh * p_pad;
+  at.p_pad = p_pad;
+  at.err = err;
   at.out = p->at<void>(p->ly.o);
   at.s_out = p->ascale(l, FM_SITE_ATTN_OUT);
   at.out_fp8 = fp8;
@@ -793,13 +799,12 @@ int refresh_prefix(fm_policy* p, int tok_begin, int tok_end, const uint16_t* k, 
   const size_t row = static_cast<size_t>(c.Hkv) * c.Dh * 2;
   const size_t rows = static_cast<size_t>(tok_end - tok_begin);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const uint16_t* src[2] = {k, v};
-  const size_t dst_off[2] = {p->ly.kcache, p->ly.vcache};
-  for (int i = 0; i < 2; ++i) {
-    uint8_t* dst = p->at<uint8_t>(dst_off[i]) + tok_begin * row;
-    FM_CUDA(p, cudaMemcpy2DAsync(dst, static_cast<size_t>(c.P) * row, src[i], rows * row, rows * row, c.L,
-                                 cudaMemcpyDeviceToDevice, s));
-  }
+  uint8_t* kdst = p->at<uint8_t>(p->ly.kcache) + tok_begin * row;
+  FM_CUDA(p, cudaMemcpy2DAsync(kdst, static_cast<size_t>(c.P) * row, k, rows * row, rows * row, c.L,
+                               cudaMemcpyDeviceToDevice, s));
+  // values are kept transposed, [L][Hkv][Dh][P_pad], the layout attention's P.V operand needs
+  FM_CUDA(p, fm::transpose_v_launch(reinterpret_cast<const __nv_bfloat16*>(v), p->at<__nv_bfloat16>(p->ly.vcache), c.L,
+                                    static_cast<int>(rows), c.Hkv, (c.P + 7) / 8 * 8, tok_begin, s));
   return FM_OK;
 }
 

@@ -211,7 +211,9 @@ int fm_device_status(fm_policy* p, void* stream, int* word);
 
 /* Address and size of one of the policy's named persistent buffers (the
  * execution contract's named buffers), for inspection and for zero-copy input:
- *   "prefix_k", "prefix_v"  bf16 [L][P][Hkv][Dh]
+ *   "prefix_k"              bf16 [L][P][Hkv][Dh]
+ *   "prefix_v"              bf16 [L][Hkv][Dh][P_pad], P_pad = P rounded up to 8 (values
+ *                           kept transposed: the layout attention's P.V operand reads)
  *   "actions"               fp32 [M][A] noise/action state
  *   "x"                     fp32 [M][d] residual stream
  *   "q", "q2"               codes [M][d] (pre-attention / pre-MLP GEMM operand)
