@@ -32,14 +32,13 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;        // 8 warps: two per TMEM lane quarter, splitting each row's keys
 constexpr int kRows = 128;           // stacked query rows per CTA (MMA M)
 constexpr int kDh = 128;             // head dim
 constexpr int kMaxSplit = 8;         // portable cluster size
 constexpr int kMaxKc = 192;          // keys per slice (MMA N of QK^T), multiple of 64
 constexpr int kTile = kRows * 128;   // bytes of one [128 rows][128 B] swizzled block
-constexpr int kLdsO = kDh + 4;       // fp32 row stride of the O staging buffer
-static_assert(kThreads == kDh, "one thread per head-dim row of V^T");
+static_assert(kThreads == 2 * kDh, "two threads per head-dim row of V^T");
 
 struct KParams {
   const __nv_bfloat16* qkv;    // [M][ldq]
@@ -61,6 +60,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
                : "memory");
 }
 
@@ -87,30 +92,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   }
 }
 
-__host__ __device__ inline size_t main_bytes(int kc) {
-  // Q: 2 blocks; K: kc rows x 256 B; V^T and P: kc/64 blocks each
-  return 2 * static_cast<size_t>(kTile) + static_cast<size_t>(kc) * 256 + 2 * static_cast<size_t>(kc / 64) * kTile;
+// Shared-memory plan of one CTA (byte offsets from the 1024-aligned base).
+struct SmemPlan {
+  size_t q, k, vt, pm, recv, stats, part, bar, total;
+};
+__host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit) {
+  SmemPlan s;
+  s.q = 0;
+  s.k = 2 * static_cast<size_t>(kTile);
+  s.vt = s.k + static_cast<size_t>(kc) * 256;
+  s.pm = s.vt + static_cast<size_t>(kc / 64) * kTile;
+  const size_t main_end = s.pm + static_cast<size_t>(kc / 64) * kTile;
+  const int rows_per = (kRows + nsplit - 1) / nsplit;
+  const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * kDh * 4;
+  // the O receive buffer reuses Q and K (dead once every CTA passed the statistics
+  // exchange) when they are large enough, else it follows the operand tiles
+  s.recv = recv_bytes <= s.vt ? 0 : (main_end + 1023) / 1024 * 1024;
+  size_t end = recv_bytes <= s.vt ? main_end : s.recv + recv_bytes;
+  s.stats = (end + 15) / 16 * 16;                            // [kMaxSplit][128] float2
+  s.part = s.stats + static_cast<size_t>(kMaxSplit) * kRows * 8;   // [2][128] float2
+  s.bar = s.part + 2 * kRows * 8;
+  s.total = s.bar + 64;
+  return s;
 }
 
-__host__ __device__ inline size_t staging_bytes(int kc) {
-  const size_t o = static_cast<size_t>(kRows) * kLdsO * 4;   // O staging aliases the operand tiles
-  const size_t m = main_bytes(kc);
-  return ((m > o ? m : o) + 1023) / 1024 * 1024;
-}
-
+template <int KC>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
+  constexpr int kHalf = KC / 2;   // keys of the slice handled by one thread of a row
+  constexpr int kBlk = KC / 64;   // 64-key blocks of the slice
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int kc = p.kc;
-  const int kblk = kc / 64;   // 64-key blocks of the slice
-  uint8_t* sQ = smem;                                         // 2 blocks: dims 0-63, 64-127
-  uint8_t* sK = sQ + 2 * kTile;                               // 2 blocks of [kc rows][128 B]
-  uint8_t* sVt = sK + static_cast<size_t>(kc) * 256;          // kblk blocks of [128 dims][128 B]
-  uint8_t* sP = sVt + static_cast<size_t>(kblk) * kTile;      // kblk blocks of [128 rows][128 B]
-  float* sO = reinterpret_cast<float*>(smem);                 // [128][kLdsO] fp32 after both MMAs
-  float* sML = reinterpret_cast<float*>(smem + staging_bytes(kc));   // [128][2] slice max, sum
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sML + kRows * 2);      // S done, O done
+  const SmemPlan sp = smem_plan(KC, p.nsplit);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + sp.bar);   // S done, O done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  float2* sStats = reinterpret_cast<float2*>(smem + sp.stats);  // [rank][row] (slice max, slice sum)
+  float2* sPart = reinterpret_cast<float2*>(smem + sp.part);    // [half][row]
+  float* recv = reinterpret_cast<float*>(smem + sp.recv);       // [rank][local row][128]
   __shared__ int s_abort;
 
   const int split = blockIdx.x;
@@ -118,10 +135,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int g = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
   const int nkeys = p.P + p.M;
-  const int t0 = split * kc;
-  const int nvalid = min(kc, nkeys - t0);
-  const uint32_t ncols = (kc + kDh) <= 256 ? 256u : 512u;
+  const int t0 = split * KC;
+  const int nvalid = min(KC, nkeys - t0);
+  constexpr uint32_t ncols = (KC + kDh) <= 256 ? 256u : 512u;
+  const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
 
   if (tid == 0) {
     s_abort = 0;
@@ -137,29 +156,30 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive_relaxed();   // paired with the wait before the first remote store
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();   // after TMEM is held: a later GEMM waiting on this grid cannot starve it
 
-  const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVta = smem_u32(sVt), sPa = smem_u32(sP);
+  const uint32_t base = smem_u32(smem);
+  const uint32_t sQa = base + sp.q, sKa = base + sp.k, sVta = base + sp.vt, sPa = base + sp.pm;
 
   // ---- prefix keys and transposed values of this slice (written before this graph ran)
-  for (int idx = tid; idx < kc * 16; idx += kThreads) {
+  for (int idx = tid; idx < KC * 16; idx += kThreads) {
     const int i = idx >> 4, c16 = idx & 15;   // key row, 16-byte chunk of its 256 bytes
     const int t = t0 + i;
-    const uint32_t dst = sKa + (c16 >> 3) * (kc * 128) + swz(i, c16 & 7);
+    const uint32_t dst = sKa + (c16 >> 3) * (KC * 128) + swz(i, c16 & 7);
     if (t < p.P)
       cp_async16(dst, p.kpre + (static_cast<size_t>(t) * p.Hkv + g) * kDh + c16 * 8);
     else if (t >= nkeys)
       st_shared_v4(dst, make_uint4(0, 0, 0, 0));
   }
-  // V^T rows: thread d copies head-dim row d, 8 keys (16 bytes) at a time. The cache
-  // row is padded with zeros from P to P_pad, so a group straddling the end of the
-  // prefix is copied whole; its keys >= P are overwritten with the chunk's values.
-  const int ngrp = kc / 8;   // 8-key groups of the slice
+  // V^T rows: two threads per head-dim row d copy 8 keys (16 bytes) at a time. The
+  // cache row is padded with zeros from P to P_pad, so a group straddling the end of
+  // the prefix is copied whole; its keys >= P are overwritten with the chunk's values.
   {
-    const int d = tid;   // kThreads == kDh
+    const int d = tid & (kDh - 1);
     const __nv_bfloat16* vrow = p.vtpre + (static_cast<size_t>(g) * kDh + d) * p.p_pad;
-    for (int grp = 0; grp < ngrp; ++grp) {
+    for (int grp = tid >> 7; grp < KC / 8; grp += 2) {
       const int t = t0 + grp * 8;
       const uint32_t dst = sVta + (grp >> 3) * kTile + swz(d, grp & 7);
       if (t < p.P)
@@ -183,24 +203,24 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       st_shared_v4(dst, make_uint4(0, 0, 0, 0));
     }
   }
-  const int c_lo = max(t0, p.P), c_hi = min(t0 + kc, nkeys);
-  const int nchunk = c_hi > c_lo ? c_hi - c_lo : 0;   // <= kc
-  const __nv_bfloat16* vstage = reinterpret_cast<const __nv_bfloat16*>(sP);   // [nchunk][128] staging
+  const int c_lo = max(t0, p.P), c_hi = min(t0 + KC, nkeys);
+  const int nchunk = c_hi > c_lo ? c_hi - c_lo : 0;   // <= KC
   for (int idx = tid; idx < nchunk * 16; idx += kThreads) {
     const int t = c_lo + (idx >> 4), c16 = idx & 15;
     const __nv_bfloat16* row = p.qkv + static_cast<size_t>(t - p.P) * p.ldq;
-    cp_async16(sKa + (c16 >> 3) * (kc * 128) + swz(t - t0, c16 & 7), row + (p.H + g) * kDh + c16 * 8);
+    cp_async16(sKa + (c16 >> 3) * (KC * 128) + swz(t - t0, c16 & 7), row + (p.H + g) * kDh + c16 * 8);
+    // the chunk's values are staged row-major in the P tiles, transposed below
     cp_async16(sPa + static_cast<uint32_t>(((t - c_lo) * kDh + c16 * 8) * 2), row + (p.H + p.Hkv + g) * kDh + c16 * 8);
   }
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();   // V^T groups and the staged chunk values are in place
-  // the chunk's own values, transposed shared -> shared into V^T (keys along K)
-  if (nchunk > 0) {
-    const int d = tid;   // kThreads == kDh
-    for (int t = c_lo; t < c_hi; ++t) {
+  if (nchunk > 0) {   // shared -> shared transpose into V^T (keys along K)
+    const int d = tid & (kDh - 1);
+    const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
+    for (int t = c_lo + (tid >> 7); t < c_hi; t += 2) {
       const int key = t - t0, grp = key >> 3;
-      const uint16_t v = reinterpret_cast<const uint16_t*>(vstage)[(t - c_lo) * kDh + d];
+      const uint16_t v = vstage[(t - c_lo) * kDh + d];
       const uint32_t addr = sVta + (grp >> 3) * kTile + swz(d, grp & 7) + (key & 7) * 2;
       asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
     }
@@ -208,16 +228,16 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   fence_async_smem();   // generic-proxy shared-memory writes -> tensor-core reads
   __syncthreads();
 
-  // ---- S = Q K^T into TMEM columns [0, kc)
+  // ---- S = Q K^T into TMEM columns [0, KC)
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = make_idesc(false, kRows, static_cast<uint32_t>(kc));
+    const uint32_t idesc = make_idesc(false, kRows, static_cast<uint32_t>(KC));
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         tc_mma<false>(tmem, sw128_kmajor_desc(sQa + b * kTile + k * 32),
-                      sw128_kmajor_desc(sKa + b * (kc * 128) + k * 32), idesc, (b | k) ? 1u : 0u);
+                      sw128_kmajor_desc(sKa + b * (KC * 128) + k * 32), idesc, (b | k) ? 1u : 0u);
     }
     tc_commit(&bar[0]);
   }
@@ -228,84 +248,80 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   tc_fence_after();
   __syncwarp();
 
-  const int r = warp * 32 + lane;   // this thread's row == its TMEM lane
-  const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int r = quarter * 32 + lane;   // this thread's row == its TMEM lane
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const int c0 = half * kHalf;         // this thread's keys: [c0, c0 + kHalf) of the slice
   const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh));   // log2(e) / sqrt(Dh)
 
-  // ---- pass 1: row max and sum of exp over this slice
-  float mrow = -INFINITY, lrow = 0.f;
-  for (int c = 0; c < kc; c += 32) {
+  // ---- pass 1: this row-half's scores (kept in registers), max and sum of exp
+  float sv[kHalf];
+#pragma unroll
+  for (int c = 0; c < kHalf; c += 32) {
     float v[32];
-    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
-    float mx = -INFINITY;
+    tmem_ld32(t_row + static_cast<uint32_t>(c0 + c), v);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      v[e] = c + e < nvalid ? v[e] * kscale : -INFINITY;
-      mx = fmaxf(mx, v[e]);
-    }
-    const float mnew = fmaxf(mrow, mx);
-    if (mnew == -INFINITY) continue;   // every key of this chunk lies past the slice end
-    float sum = 0.f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) sum += exp2f(v[e] - mnew);
-    lrow = lrow * exp2f(mrow - mnew) + sum;
-    mrow = mnew;
+    for (int e = 0; e < 32; ++e) sv[c + e] = c0 + c + e < nvalid ? v[e] * kscale : -INFINITY;
   }
-  sML[r * 2] = mrow;
-  sML[r * 2 + 1] = lrow;
-
-  // ---- exchange the slice statistics across the cluster: global max and sum per row
-  cluster_sync_all();
+  float mh = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < kHalf; ++e) mh = fmaxf(mh, sv[e]);
+  float lh = 0.f;
+  if (mh > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < kHalf; ++e) lh += exp2f(sv[e] - mh);
+  }
+  sPart[half * kRows + r] = make_float2(mh, lh);
+  __syncthreads();
+  // the slice statistics of row r, pushed to every CTA of the cluster (slot = own rank)
+  cluster_wait();   // every peer has started: its shared memory exists
+  if (half == 0) {
+    const float2 a = sPart[r], b = sPart[kRows + r];
+    const float m = fmaxf(a.x, b.x);
+    const float l = (a.y > 0.f ? a.y * exp2f(a.x - m) : 0.f) + (b.y > 0.f ? b.y * exp2f(b.x - m) : 0.f);
+    const uint32_t rank = cluster_rank();
+    const uint32_t off = smem_u32(sStats + rank * kRows + r);
+    for (int q = 0; q < p.nsplit; ++q) {
+      const uint32_t dst = map_dsmem(off, static_cast<uint32_t>(q));
+      st_dsmem_f32(dst, m);
+      st_dsmem_f32(dst + 4, l);
+    }
+  }
+  cluster_sync_all();   // every slice's statistics have landed
   float gmax = -INFINITY, gsum = 0.f;
-  {
-    const uint32_t ml_local = smem_u32(sML + r * 2);
-    float mq[kMaxSplit], lq[kMaxSplit];
-#pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q) {
-      if (q < p.nsplit) {
-        const uint32_t a = map_dsmem(ml_local, static_cast<uint32_t>(q));
-        mq[q] = ld_dsmem_f32(a);
-        lq[q] = ld_dsmem_f32(a + 4);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q)
-      if (q < p.nsplit) gmax = fmaxf(gmax, mq[q]);
-#pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q)
-      if (q < p.nsplit) gsum += lq[q] * exp2f(mq[q] - gmax);
+  for (int q = 0; q < p.nsplit; ++q) gmax = fmaxf(gmax, sStats[q * kRows + r].x);
+  for (int q = 0; q < p.nsplit; ++q) {
+    const float2 st = sStats[q * kRows + r];
+    gsum += st.y * exp2f(st.x - gmax);
   }
+  const float ginv = 1.0f / gsum;
 
   // ---- pass 2: P = bf16(exp(s - M) / L) into the swizzled A operand of P V
-  const float ginv = 1.0f / gsum;
-  for (int c = 0; c < kc; c += 32) {
-    float v[32];
-    tmem_ld32(t_row + static_cast<uint32_t>(c), v);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = c + e < nvalid ? exp2f(v[e] * kscale - gmax) * ginv : 0.f;
+  for (int ch = 0; ch < kHalf / 8; ++ch) {   // 8-key chunks of 16 bytes
+    const int key = c0 + ch * 8;
+    float pv[8];
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {   // four 8-key chunks of 16 bytes
-      const int key = c + ch * 8;
-      uint4 u;
-      u.x = pack_bf16(v[ch * 8 + 0], v[ch * 8 + 1]);
-      u.y = pack_bf16(v[ch * 8 + 2], v[ch * 8 + 3]);
-      u.z = pack_bf16(v[ch * 8 + 4], v[ch * 8 + 5]);
-      u.w = pack_bf16(v[ch * 8 + 6], v[ch * 8 + 7]);
-      st_shared_v4(sPa + (key >> 6) * kTile + swz(r, (key & 63) >> 3), u);
-    }
+    for (int e = 0; e < 8; ++e) pv[e] = key + e < nvalid ? exp2f(sv[ch * 8 + e] - gmax) * ginv : 0.f;
+    uint4 u;
+    u.x = pack_bf16(pv[0], pv[1]);
+    u.y = pack_bf16(pv[2], pv[3]);
+    u.z = pack_bf16(pv[4], pv[5]);
+    u.w = pack_bf16(pv[6], pv[7]);
+    st_shared_v4(sPa + (key >> 6) * kTile + swz(r, (key & 63) >> 3), u);
   }
   tc_fence_before();
   fence_async_smem();
   __syncthreads();
 
-  // ---- O = P V into TMEM columns [kc, kc + 128)
+  // ---- O = P V into TMEM columns [KC, KC + 128)
   if (tid == 0) {
     tc_fence_after();
     const uint32_t idesc = make_idesc(false, kRows, kDh);
-    for (int b = 0; b < kblk; ++b) {
+#pragma unroll
+    for (int b = 0; b < kBlk; ++b) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc_mma<false>(tmem + static_cast<uint32_t>(kc), sw128_kmajor_desc(sPa + b * kTile + k * 32),
+        tc_mma<false>(tmem + static_cast<uint32_t>(KC), sw128_kmajor_desc(sPa + b * kTile + k * 32),
                       sw128_kmajor_desc(sVta + b * kTile + k * 32), idesc, (b | k) ? 1u : 0u);
     }
     tc_commit(&bar[1]);
@@ -316,46 +332,44 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   }
   tc_fence_after();
   __syncwarp();
-  // this slice's share of O (already normalised by the global sum) to shared memory
-  for (int c = 0; c < kDh; c += 32) {
-    float v[32];
-    tmem_ld32(t_row + static_cast<uint32_t>(kc + c), v);
-#pragma unroll
-    for (int e = 0; e < 32; e += 4)
-      *reinterpret_cast<float4*>(sO + r * kLdsO + c + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-  }
 
-  // ---- sum the slices' shares across the cluster in fixed slice order, quantise.
-  // A thread owns 4 adjacent head-dim columns of one row (32 threads per row, 4 rows
-  // in flight per CTA) and issues the loads of all slices before summing.
-  cluster_sync_all();
+  // ---- this slice's share of O (already normalised by the global sum), pushed to
+  // the rank that finalises row r: rows are split into bands of rows_per
+  {
+    const int R = qt * kRows + r;
+    const int owner = r / rows_per, lr = r - owner * rows_per;
+    const uint32_t rank = cluster_rank();
+    const uint32_t dst = map_dsmem(smem_u32(recv + ((rank * rows_per + lr) * kDh + half * 64)),
+                                   static_cast<uint32_t>(owner));
+#pragma unroll
+    for (int c = 0; c < 64; c += 32) {
+      float v[32];
+      tmem_ld32(t_row + static_cast<uint32_t>(KC + half * 64 + c), v);
+      if (R < p.G * p.M) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          st_dsmem_v4(dst + static_cast<uint32_t>((c + e) * 4), make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
+      }
+    }
+  }
+  cluster_sync_all();   // every share of this CTA's rows has landed
+
+  // ---- sum the slices' shares in fixed slice order, quantise, store
   if (s_abort == 0) {
     const int rank = static_cast<int>(cluster_rank());
-    const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
     const int e4 = lane * 4;
     const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
-    const uint32_t o_local = smem_u32(sO);
-    uint32_t peer[kMaxSplit];
-#pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q) peer[q] = q < p.nsplit ? map_dsmem(o_local, static_cast<uint32_t>(q)) : 0u;
-    const int r_end = min(kRows, (rank + 1) * rows_per);
-    for (int rr = rank * rows_per + warp; rr < r_end; rr += kThreads / 32) {
+    for (int lr = warp; lr < rows_per; lr += kThreads / 32) {
+      const int rr = rank * rows_per + lr;
       const int R = qt * kRows + rr;
-      if (R >= p.G * p.M) break;
-      const uint32_t off = static_cast<uint32_t>((rr * kLdsO + e4) * 4);
-      float4 v[kMaxSplit];
-#pragma unroll
-      for (int q = 0; q < kMaxSplit; ++q)
-        if (q < p.nsplit) v[q] = ld_dsmem_f32x4(peer[q] + off);
+      if (rr >= kRows || R >= p.G * p.M) break;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < kMaxSplit; ++q) {
-        if (q < p.nsplit) {
-          acc.x += v[q].x;
-          acc.y += v[q].y;
-          acc.z += v[q].z;
-          acc.w += v[q].w;
-        }
+      for (int q = 0; q < p.nsplit; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDh + e4);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
       }
       const int hl = R / p.M, m = R % p.M;
       const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e4;
@@ -374,7 +388,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
     }
   }
-  cluster_sync_all();   // peers may still be reading this CTA's share
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -414,9 +427,17 @@ int attn_plan(int M, int P, int* kc, int* nsplit) {
   return FM_OK;
 }
 
-size_t attn_smem_bytes(int kc) { return 1024 + staging_bytes(kc) + kRows * 2 * 4 + 64; }
+size_t attn_smem_bytes(int kc, int nsplit) { return 1024 + smem_plan(kc, nsplit).total; }
 
-cudaError_t attn_configure() { return allow_max_dynamic_smem(reinterpret_cast<const void*>(attn_kernel)); }
+cudaError_t attn_configure() {
+  const void* ks[3] = {reinterpret_cast<const void*>(attn_kernel<64>), reinterpret_cast<const void*>(attn_kernel<128>),
+                       reinterpret_cast<const void*>(attn_kernel<192>)};
+  for (const void* k : ks) {
+    const cudaError_t e = allow_max_dynamic_smem(k);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   KParams p;
@@ -441,7 +462,13 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
                   static_cast<unsigned>(a.Hkv));
   LaunchOpts lo = o;
   lo.cluster = dim3(static_cast<unsigned>(a.nsplit), 1, 1);
-  return launch(attn_kernel, grid, dim3(kThreads), attn_smem_bytes(a.kc), lo, p);
+  const size_t smem = attn_smem_bytes(a.kc, a.nsplit);
+  switch (a.kc) {
+    case 64: return launch(attn_kernel<64>, grid, dim3(kThreads), smem, lo, p);
+    case 128: return launch(attn_kernel<128>, grid, dim3(kThreads), smem, lo, p);
+    case 192: return launch(attn_kernel<192>, grid, dim3(kThreads), smem, lo, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t transpose_v_launch(const __nv_bfloat16* v, __nv_bfloat16* vt, int L, int rows, int Hkv, int p_pad,

@@ -148,7 +148,7 @@ struct AttnArgs {
 };
 // Slice plan for P + M keys; FM_ERR_SHAPE when they need more than 8 x 192.
 int attn_plan(int M, int P, int* kc, int* nsplit);
-size_t attn_smem_bytes(int kc);
+size_t attn_smem_bytes(int kc, int nsplit);
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
 cudaError_t attn_configure();
 // v [L][rows][Hkv][Dh] -> vt[l][g][d][tok_begin + t] (row stride p_pad).
