@@ -389,6 +389,100 @@ def profile_case():
     pol.close()
 
 
+def run_bf16_protocol(args):
+    """Matched 16-bit workload (bf16 weights and activations, M = 63, 18 layers x 10
+    steps, prefix 788): 100 consecutive decisions on one policy with new noise each,
+    the 768 image-token rows of the prefix refreshed before every 5th decision.
+    Reports the mean decision latency without the refresh, the refresh latency, the
+    mean per decision including refreshes, and capsule restore + decision against
+    set_prefix_kv + decision. Every input is resident on the device beforehand."""
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    device = torch.device("cuda", 0)
+    fmad.load()
+    cfg = fm_synth.config("expert_bf16_m63")
+    rows, every, n_dec = 768, 5, 100
+    layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
+    weights = fmad.DeviceWeights(cfg, layers, fm_synth.final_weights(cfg), device=device)
+    del layers
+    pol = fmad.Policy(cfg, weights=weights, device=device)
+    del weights
+    bf = lambda a: torch.from_numpy(a).to(device, torch.bfloat16)
+    kp, vp = fm_synth.prefix_kv(cfg)
+    k_dev, v_dev = bf(kp), bf(vp)
+    pol.set_prefix_kv(k_dev, v_dev)
+    refresh = {d: tuple(bf(a) for a in fm_synth.prefix_kv_rows(cfg, d // every, rows))
+               for d in range(every, n_dec, every)}
+    noise = [torch.from_numpy(fm_synth.noise(cfg, d)).to(device) for d in range(n_dec)]
+    actions = torch.empty_like(noise[0])
+    stream = torch.cuda.current_stream(device)
+    for _ in range(max(3, args.warmup)):
+        pol.decode(noise[0], actions)
+    pol.set_prefix_kv(k_dev, v_dev)
+    torch.cuda.synchronize(device)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = []
+    with ClockSampler(0) as clocks:
+        start = ev()
+        start.record(stream)
+        for d in range(n_dec):
+            r0 = r1 = None
+            if d in refresh:
+                r0, r1 = ev(), ev()
+                r0.record(stream)
+                pol.refresh_prefix(0, rows, *refresh[d])
+                r1.record(stream)
+            d0, d1 = ev(), ev()
+            d0.record(stream)
+            pol.decode(noise[d], actions)
+            d1.record(stream)
+            marks.append((r0, r1, d0, d1))
+        end = ev()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+    if fmad.device_status(pol.handle):
+        raise RuntimeError("device error word set")
+    dec = [d0.elapsed_time(d1) for _, _, d0, d1 in marks]
+    ref = [r0.elapsed_time(r1) for r0, r1, _, _ in marks if r0 is not None]
+    total = start.elapsed_time(end)
+
+    # capsule restore + decision vs re-set prefix + decision (same resulting state)
+    n = fmad.state_size(pol.handle)
+    cap = torch.empty(n, dtype=torch.uint8, device=device)
+    fmad.snapshot_state(pol.handle, cap, n, True)
+    reps = 20
+    t = {}
+    for name in ("restore", "set_prefix"):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(reps):
+            if name == "restore":
+                fmad.restore_state(pol.handle, cap, n, True)
+            else:
+                pol.set_prefix_kv(k_dev, v_dev)
+            pol.decode(noise[0], actions)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        t[name] = e0.elapsed_time(e1) / reps
+    pol.close()
+    peak_gbs, peak_kind = measured_peaks()
+    ab = algorithmic_bytes(cfg)["total"]
+    mean_dec = statistics.fmean(dec)
+    return {"protocol": "bf16 persistent prefix, refresh every 5th decision", "workload": cfg.name,
+            "decisions": n_dec, "unit": "ms",
+            "decision_mean_excl_refresh": round(mean_dec, 4),
+            "decision_p99": round(float(np.percentile(dec, 99)), 4),
+            "refresh_mean": round(statistics.fmean(ref), 4), "refreshes": len(ref),
+            "mean_per_decision_incl_refresh": round(total / n_dec, 4),
+            "restore_plus_decision": round(t["restore"], 4),
+            "set_prefix_plus_decision": round(t["set_prefix"], 4),
+            "state_bytes": n,
+            "decision_hbm": {"algorithmic_bytes": int(ab), "achieved_gbs": round(ab / (mean_dec * 1e-3) / 1e9, 1),
+                             "peak_gbs": peak_gbs, "frac": round(ab / (mean_dec * 1e-3) / 1e9 / peak_gbs, 4),
+                             "peak_kind": peak_kind},
+            "clocks": clocks.summary()}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,7 +493,12 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")
     ap.add_argument("--profile-case", action="store_true",
                     help="run only the small 1-layer, 1-step case for ncu (profiler range on its 2nd decision)")
+    ap.add_argument("--bf16-protocol", action="store_true",
+                    help="run only the matched 16-bit persistence protocol (100 decisions, refresh every 5th)")
     args = ap.parse_args()
+    if args.bf16_protocol:
+        print(json.dumps(run_bf16_protocol(args)), flush=True)
+        return
     if args.profile_case:
         profile_case()
         return

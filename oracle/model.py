@@ -241,7 +241,7 @@ def layer_forward(model: Model, l: int, k: int, x: np.ndarray, q: np.ndarray,
     H, Hkv, Dh, F, af = cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.act_fmt
     sc1, sh1, g1, sc2, sh2, g2 = model.mods[k][0][l]
     w = model.w[l]
-    s = act_scales[l]
+    s = act_scales[l] if af == "fp8" else None   # bf16 operands carry no scale
     sa = lambda i: float(s[i]) if af == "fp8" else 1.0
 
     qkv = gemm(q, sa(SITE_ATTN_IN), w["qkv"])

@@ -1,0 +1,114 @@
+"""Teacher-forced, stage-by-stage check of a recorded decision (fm_decode_trace)
+against the oracle: every kernel's recorded output must equal the oracle's stage
+applied to the GPU's own recorded input. Shared by the FP8 and bf16 decision tests.
+
+Tolerances:
+- fp32 outputs (GEMM partial sums, residual stream, Euler update): 1e-5 * RMS;
+- quantised operands (E4M3 codes or bf16 values): one grid step at the larger
+  magnitude plus abs_tol * RMS, with at most max_frac of the values differing
+  (a value within rounding distance of a tie may round either way);
+- the QKV epilogue's bf16 outputs: within one bf16 rounding of the exact product.
+"""
+import numpy as np
+
+from oracle import model as O
+
+
+def e4m3_ulp(v):
+    """Spacing of the E4M3 grid at |v| (code units): 2^(e-3) for normal values, 2^-9 below 2^-6."""
+    a = np.abs(np.asarray(v, np.float64))
+    _, E = np.frexp(a)
+    return np.ldexp(1.0, np.maximum(E - 1, -6) - 3)
+
+
+def bf16_ulp(v):
+    """Spacing of the bf16 grid at |v|: 8 significant bits, 2^(e-7) for |v| in [2^e, 2^(e+1))."""
+    a = np.abs(np.asarray(v, np.float64))
+    _, E = np.frexp(a)
+    return np.ldexp(1.0, np.maximum(E - 1, -126) - 7)
+
+
+def check_codes(got_values, ref_values, what, fmt="fp8", max_frac=1e-3, abs_tol=1e-3):
+    """Quantised operands agree when they differ by at most one grid step at the larger
+    magnitude plus abs_tol * RMS: a near-tie input rounds either way, and near zero
+    (subnormal steps) a tiny upstream difference can span several steps."""
+    got, ref = np.asarray(got_values, np.float64), np.asarray(ref_values, np.float64)
+    ulp = e4m3_ulp if fmt == "fp8" else bf16_ulp
+    diff = np.abs(got - ref)
+    allow = ulp(np.maximum(np.abs(got), np.abs(ref))) + abs_tol * np.sqrt(np.mean(ref ** 2))
+    bad = diff > allow * (1 + 1e-12)
+    if np.any(bad):
+        i = np.unravel_index(np.argmax(diff - allow), diff.shape)
+        raise AssertionError(f"{what}: {np.sum(bad)} codes beyond tolerance, worst at {i}: "
+                             f"got {got[i]} ref {ref[i]} (allow {allow[i]:.3g})")
+    frac = np.mean(diff > 0)
+    assert frac <= max_frac, f"{what}: {frac:.2e} of codes differ"
+
+
+def check_close(got, ref, what, tol=1e-5):
+    err = np.max(np.abs(np.asarray(got, np.float64) - ref)) / (np.sqrt(np.mean(ref ** 2)) + 1e-30)
+    assert err <= tol, f"{what}: {err:.2e} > {tol:.0e}"
+
+
+def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac=1e-3):
+    """recs[k][l] as parse_trace returns them; scales [L][4] (ignored for bf16)."""
+    fmt = cfg.act_fmt
+    M, H, Dh, F, L, S = cfg.M, cfg.H, cfg.Dh, cfg.F, cfg.L, cfg.S
+    fin = model.final
+    kp, vp = np.asarray(kp, np.float64), np.asarray(vp, np.float64)
+
+    def s_act(l, i):
+        return float(scales[l][i]) if fmt == "fp8" else 1.0
+
+    def dq(l, i, w):   # dequantisation factor fp32(s_a * s_w) the epilogues apply
+        return np.float64(np.float32(s_act(l, i)) * np.float32(w.scale))
+
+    a_prev = np.asarray(noise, np.float64)
+    check_close(recs[0][0]["x_in"], a_prev @ fin["w_in"].T + fin["b_in"], "step head x")
+    for k in range(S):
+        for l in range(L):
+            r = recs[k][l]
+            W = model.w[l]
+            sc1, sh1, g1, sc2, sh2, g2 = model.mods[k][0][l]
+            where = f"step {k} layer {l}"
+            check_codes(r["q"], O.quant_codes(O.ada_norm(r["x_in"], sc1, sh1, cfg.eps), s_act(l, 0), fmt),
+                        where + " pre-attention quantise", fmt)
+            # QKV: the GEMM epilogue emits bf16(sum * dequant); within one bf16 rounding
+            # of the exact dequantised product
+            qkv = r["y_qkv"]
+            exact = (r["q"] @ W["qkv"].codes.T) * dq(l, 0, W["qkv"])
+            assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-5 * np.sqrt(np.mean(exact ** 2))), \
+                where + " QKV GEMM"
+            # the attention stage's input is exactly the recorded bf16 Q | K | V
+            Q = qkv[:, :H * Dh]
+            Kc = qkv[:, H * Dh:(H + cfg.Hkv) * Dh]
+            Vc = qkv[:, (H + cfg.Hkv) * Dh:]
+            Oref = O.attention(Q, Kc, Vc, kp[l], vp[l], H, cfg.Hkv, Dh)
+            # attention rounds its probabilities to bf16: a near-tie probability rounding
+            # either way moves a row of O by up to 2^-9 * P * |V|, so its allowance is 2^-7 * RMS
+            check_codes(r["attn_out"], O.quant_codes(Oref, s_act(l, 1), fmt), where + " attention", fmt,
+                        max_frac=attn_max_frac, abs_tol=2.0 ** -7)
+            yo = r["y_o"].sum(0)
+            check_close(yo, r["attn_out"] @ W["o"].codes.T, where + " O GEMM")
+            check_close(r["x_mid"], r["x_in"] + g1 * yo * dq(l, 1, W["o"]), where + " attention residual")
+            check_codes(r["q2"], O.quant_codes(O.ada_norm(r["x_mid"], sc2, sh2, cfg.eps), s_act(l, 2), fmt),
+                        where + " pre-MLP quantise", fmt)
+            # gate|up GEMM with GeGLU + quantise in its epilogue
+            gu = (r["q2"] @ W["gu"].codes.T) * dq(l, 2, W["gu"])
+            check_codes(r["geglu_out"], O.quant_codes(O.gelu_tanh(gu[:, :F]) * gu[:, F:], s_act(l, 3), fmt),
+                        where + " gate|up GEMM + GeGLU", fmt)
+            yd = r["y_d"].sum(0)
+            check_close(yd, r["geglu_out"] @ W["d"].codes.T, where + " down GEMM")
+            x_res = r["x_mid"] + g2 * yd * dq(l, 3, W["d"])
+            if l < L - 1:
+                check_close(r["x_out"], x_res, where + " MLP residual")
+                continue
+            scf, shf = model.mods[k][1]
+            v = (O.ada_norm(x_res, scf, shf, cfg.eps) * fin["gamma_f"]) @ fin["w_out"].T + fin["b_out"]
+            check_close(r["actions"], a_prev + (-1.0 / S) * v, where + " Euler update")
+            a_prev = r["actions"].astype(np.float64)
+            if k < S - 1:
+                check_close(r["x_out"], a_prev @ fin["w_in"].T + fin["b_in"], where + " next step head")
+            else:
+                check_close(r["x_out"], x_res, where + " MLP residual")
+    return recs[S - 1][L - 1]["actions"]

@@ -22,6 +22,7 @@ from oracle import codecs as C
 from oracle import model as O
 
 from _gpu import GOLDEN, code_step_distance, dev, load_scales, parse_trace, require_gpu
+from _stagewise import check_decision_stages
 
 pytestmark = pytest.mark.gpu
 TOL_FP8 = 2e-2
@@ -119,34 +120,6 @@ def test_decision_fp8_end_to_end_within_oracle_envelope(expert):
     pol.close()
 
 
-def e4m3_ulp(v):
-    """Spacing of the E4M3 grid at |v| (code units): 2^(e-3) for normal values, 2^-9 below 2^-6."""
-    a = np.abs(np.asarray(v, np.float64))
-    _, E = np.frexp(a)
-    return np.ldexp(1.0, np.maximum(E - 1, -6) - 3)
-
-
-def _check_codes(got_values, ref_values, what, max_frac=1e-3, abs_tol=1e-3):
-    """Quantised operands agree when they differ by at most one grid step at the larger
-    magnitude plus abs_tol * RMS: a near-tie input rounds either way, and near zero
-    (subnormal steps of 2^-9) a tiny upstream difference can span several steps."""
-    got, ref = np.asarray(got_values, np.float64), np.asarray(ref_values, np.float64)
-    diff = np.abs(got - ref)
-    allow = e4m3_ulp(np.maximum(np.abs(got), np.abs(ref))) + abs_tol * np.sqrt(np.mean(ref ** 2))
-    bad = diff > allow * (1 + 1e-12)
-    if np.any(bad):
-        i = np.unravel_index(np.argmax(diff - allow), diff.shape)
-        raise AssertionError(f"{what}: {np.sum(bad)} codes beyond tolerance, worst at {i}: "
-                             f"got {got[i]} ref {ref[i]} (allow {allow[i]:.3g})")
-    frac = np.mean(diff > 0)
-    assert frac <= max_frac, f"{what}: {frac:.2e} of codes differ"
-
-
-def _check_close(got, ref, what, tol=1e-5):
-    err = np.max(np.abs(np.asarray(got, np.float64) - ref)) / (np.sqrt(np.mean(ref ** 2)) + 1e-30)
-    assert err <= tol, f"{what}: {err:.2e} > {tol:.0e}"
-
-
 def test_decision_fp8_every_stage_vs_oracle(expert):
     """Teacher-forced parity of every kernel of all 180 layer-steps: each recorded
     output equals the oracle's stage applied to the GPU's own recorded input -
@@ -163,60 +136,8 @@ def test_decision_fp8_every_stage_vs_oracle(expert):
     # the traced (eager) run is bitwise the graph run
     assert torch.equal(act.cpu(), pol.decode(dev(nz, expert.device)).cpu())
     recs = parse_trace(trace.cpu().numpy(), cfg, pol)
-    M, d, H, Dh, F, L, S = cfg.M, cfg.d, cfg.H, cfg.Dh, cfg.F, cfg.L, cfg.S
-    fin = model.final
-    sc = expert.scales
-    kp, vp = expert.kp.astype(np.float64), expert.vp.astype(np.float64)
-    a_prev = nz.astype(np.float64)
-    _check_close(recs[0][0]["x_in"], a_prev @ fin["w_in"].T + fin["b_in"], "step head x")
-    for k in range(S):
-        for l in range(L):
-            r = recs[k][l]
-            W = model.w[l]
-            sc1, sh1, g1, sc2, sh2, g2 = model.mods[k][0][l]
-            where = f"step {k} layer {l}"
-            _check_codes(r["q"], O.quant_codes(O.ada_norm(r["x_in"], sc1, sh1, cfg.eps), sc[l, 0], "fp8"),
-                         where + " pre-attention quantise")
-            # QKV: the GEMM epilogue emits bf16(sum * fp32(s_a * s_w)); within one bf16
-            # rounding of the exact dequantised product
-            qkv = r["y_qkv"]
-            exact = (r["q"] @ W["qkv"].codes.T) * np.float64(np.float32(sc[l, 0]) * np.float32(W["qkv"].scale))
-            assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-5 * np.sqrt(np.mean(exact ** 2))), \
-                where + " QKV GEMM"
-            # the attention stage's input is exactly the recorded bf16 Q | K | V
-            Q = qkv[:, :H * Dh]
-            Kc = qkv[:, H * Dh:(H + cfg.Hkv) * Dh]
-            Vc = qkv[:, (H + cfg.Hkv) * Dh:]
-            Oref = O.attention(Q, Kc, Vc, kp[l], vp[l], H, cfg.Hkv, Dh)
-            # attention rounds its probabilities to bf16: a near-tie probability rounding
-            # either way moves a row of O by up to 2^-9 * P * |V|, so its allowance is 2^-7 * RMS
-            _check_codes(r["attn_out"], O.quant_codes(Oref, sc[l, 1], "fp8"), where + " attention",
-                         abs_tol=2.0 ** -7)
-            yo = r["y_o"].sum(0)
-            _check_close(yo, r["attn_out"] @ W["o"].codes.T, where + " O GEMM")
-            o = yo * np.float64(np.float32(sc[l, 1]) * np.float32(W["o"].scale))
-            _check_close(r["x_mid"], r["x_in"] + g1 * o, where + " attention residual")
-            _check_codes(r["q2"], O.quant_codes(O.ada_norm(r["x_mid"], sc2, sh2, cfg.eps), sc[l, 2], "fp8"),
-                         where + " pre-MLP quantise")
-            # gate|up GEMM with GeGLU + quantise in its epilogue
-            gu = (r["q2"] @ W["gu"].codes.T) * np.float64(np.float32(sc[l, 2]) * np.float32(W["gu"].scale))
-            _check_codes(r["geglu_out"], O.quant_codes(O.gelu_tanh(gu[:, :F]) * gu[:, F:], sc[l, 3], "fp8"),
-                         where + " gate|up GEMM + GeGLU")
-            yd = r["y_d"].sum(0)
-            _check_close(yd, r["geglu_out"] @ W["d"].codes.T, where + " down GEMM")
-            x_res = r["x_mid"] + g2 * yd * np.float64(np.float32(sc[l, 3]) * np.float32(W["d"].scale))
-            if l < L - 1:
-                _check_close(r["x_out"], x_res, where + " MLP residual")
-                continue
-            scf, shf = model.mods[k][1]
-            v = (O.ada_norm(x_res, scf, shf, cfg.eps) * fin["gamma_f"]) @ fin["w_out"].T + fin["b_out"]
-            _check_close(r["actions"], a_prev + (-1.0 / S) * v, where + " Euler update")
-            a_prev = r["actions"].astype(np.float64)
-            if k < S - 1:
-                _check_close(r["x_out"], a_prev @ fin["w_in"].T + fin["b_in"], where + " next step head")
-            else:
-                _check_close(r["x_out"], x_res, where + " MLP residual")
-    np.testing.assert_array_equal(recs[S - 1][L - 1]["actions"], act.cpu().numpy())
+    last = check_decision_stages(cfg, model, recs, nz, expert.kp, expert.vp, expert.scales)
+    np.testing.assert_array_equal(last, act.cpu().numpy())
     pol.close()
 
 
