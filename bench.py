@@ -49,6 +49,13 @@ def algorithmic_bytes(cfg) -> dict:
             "total": total}
 
 
+def algorithmic_flops(cfg) -> dict:
+    """GEMM and attention FLOPs of one decision (2 per multiply-add)."""
+    gemm = 2 * cfg.M * sum(n * k for n, k in cfg.gemm_shapes)
+    attn = 2 * 2 * cfg.M * cfg.H * (cfg.P + cfg.M) * cfg.Dh   # Q K^T and P V
+    return {"gemm": cfg.S * cfg.L * gemm, "attn": cfg.S * cfg.L * attn, "total": cfg.S * cfg.L * (gemm + attn)}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -56,6 +63,17 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_tensor_peak(sustained=False):
+    """Dense bf16 (= f16) tensor peak in TFLOP/s: burst for a kernel timed alone,
+    sustained for a kernel inside a long step."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    return (1700.0 if sustained else 1900.0), "fallback"
 
 
 class ClockSampler:
@@ -117,7 +135,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     fmad.load()
-    cfg = fm_synth.config(WORKLOAD)
+    cfg = fm_synth.config(args.workload)
     layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
     final = fm_synth.final_weights(cfg)
     scales = fm_synth.default_act_scales(cfg)
@@ -181,8 +199,9 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3
 
-    # ---- dominant kernel timed alone: the gate|up skinny GEMM, rotating weight copies
-    gemm = time_dominant_gemm(cfg, pol, device, stream)
+    # ---- dominant kernel timed alone: the gate|up GEMM, rotating weight copies
+    gemm = time_dominant_gemm(cfg, pol, device, stream) if cfg.weight_fmt == "fp8" else \
+        time_dominant_gemm_nvfp4(cfg, device, stream)
 
     # ---- launch-mode variants (PDL off, graph off), same kernels and inputs
     variant_ms = {}
@@ -225,13 +244,13 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3",
+        "dtype": "fp8_e4m3" if cfg.weight_fmt == "fp8" else "nvfp4 weights, fp8_e4m3 activations, f16 MMA",
         "data": "synthetic (seeded N(0,1)/N(0,0.02) weights, prefix KV, noise; no trained weights)",
-        "config": {"workload": WORKLOAD, "layers": cfg.L, "euler_steps": cfg.S, "action_rows": cfg.M,
+        "config": {"workload": cfg.name, "layers": cfg.L, "euler_steps": cfg.S, "action_rows": cfg.M,
                    "d_model": cfg.d, "heads": f"{cfg.H}x{cfg.Dh} (kv {cfg.Hkv})", "prefix_tokens": cfg.P,
                    "mlp": f"GeGLU {cfg.d}->2x{cfg.F}->{cfg.d}", "weights": cfg.weight_fmt,
                    "activations": cfg.act_fmt, "launch": "CUDA graph + PDL",
-                   "l2": "no flush: 2.7 GB of weights streamed per decision >> 129 MB L2",
+                   "l2": f"no flush: {ab['weights'] / 1e9:.1f} GB of weights streamed per decision >> 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "latency_ms": {"median": round(statistics.median(per), 4),
                        "p99": round(float(np.percentile(per, 99)), 4),
@@ -247,8 +266,15 @@ def run_ours(args, rank, world, local_rank):
         "launch_variants_ms": variant_ms,
         "clocks": clocks.summary(),
     }
+    if cfg.weight_fmt == "nvfp4":
+        fl = algorithmic_flops(cfg)
+        tpk, tkind = measured_tensor_peak(sustained=True)
+        tf = fl["total"] / (lat_ms * 1e-3) / 1e12
+        line["decision_tensor"] = {"algorithmic_flops": int(fl["total"]), "achieved_tflops": round(tf, 1),
+                                   "peak_tflops": tpk, "frac": round(tf / tpk, 4),
+                                   "peak_kind": f"{peak_kind_note(tkind)} sustained dense bf16"}
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, samples=1)
+        line["cpu_baseline"] = cpu_baseline(cfg)
     return line
 
 
@@ -305,6 +331,54 @@ def time_dominant_gemm(cfg, pol, device, stream):
             "timing": "back-to-back launches, rotating weights over > 2x L2, CUDA events"}
 
 
+def time_dominant_gemm_nvfp4(cfg, device, stream):
+    """The NVFP4 gate|up GEMM (N = 2F, K = d, M rows, one K slice) launched back to
+    back through the C ABI over rotating packed weights (> 2x L2); tensor-bound at
+    M = 256, so reported against the dense bf16/f16 tensor peak."""
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+
+    N, K, M = 2 * cfg.F, cfg.d, cfg.M
+    nbytes = fmad.fm_packed_weight_bytes(N, K, fmad.FMT_NVFP4)
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    copies = max(4, int(np.ceil(2 * l2 / nbytes)) + 1)
+    rng = np.random.default_rng(0)
+    w = torch.from_numpy((rng.standard_normal((N, K)) * 0.02).astype(np.float32)).to(device)
+    bufs = []
+    scale = torch.empty(1, dtype=torch.float32, device=device)
+    for _ in range(copies):
+        b = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device)
+        ptr = b.data_ptr() + ((-b.data_ptr()) % 1024)
+        fmad.fm_pack_weight(w, None, N, K, fmad.FMT_NVFP4, ptr, scale)
+        bufs.append((b, ptr))
+    del w
+    a = (torch.randn((M, K), device=device) * 4).to(torch.float16)
+    out = torch.empty((1, M, N), dtype=torch.float32, device=device)
+    reps = copies * 8
+    for i in range(copies):
+        fmad.fm_test_skinny_gemm(a, M, K, bufs[i][1], N, fmad.FMT_NVFP4, 1, 1, out, stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        fmad.fm_test_skinny_gemm(a, M, K, bufs[i % copies][1], N, fmad.FMT_NVFP4, 1, 1, out, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    flops = 2 * M * N * K
+    peak, kind = measured_tensor_peak(sustained=False)
+    achieved = flops / (us * 1e-6) / 1e12
+    hbm = (nbytes + M * K * 2 + M * N * 4) / (us * 1e-6) / 1e9
+    hpk, hkind = measured_peaks()
+    return {"kernel": f"nvfp4_gemm_kernel gate|up (N={N}, K={K}, M={M}, split 1)",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind_note(kind)} dense bf16 burst (f16 same rate)",
+            "traffic": None, "algorithmic_flops": int(flops), "avg_launch_us": round(us, 3),
+            "hbm": {"achieved_gbs": round(hbm, 1), "peak_gbs": hpk, "frac": round(hbm / hpk, 4)},
+            "timing": "back-to-back launches, rotating weights over > 2x L2, CUDA events"}
+
+
 def profiled_traffic(name="skinny_gemm_gu_m50.md"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
     only while the kernel source is the one that was profiled (else None)."""
@@ -328,10 +402,10 @@ def peak_kind_note(kind):
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
-def cpu_baseline(cfg, samples: int = 1, steps_per_sample: int = 2):
-    """Time the FP64 oracle as it stands on this host's cores on a bounded sample:
-    `steps_per_sample` Euler steps (each = all 18 layers) of the same workload;
-    scaled to ms per 10-step decision."""
+def cpu_baseline(cfg, samples: int = 1):
+    """Time the FP64 oracle as it stands on this host's cores on a bounded sample of
+    the workload: whole Euler steps (two) of the 18-layer expert, or the first layers
+    of one step for larger decoders; scaled to ms per decision."""
     from oracle import model as O
     layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
     model = O.Model(cfg, layers, fm_synth.final_weights(cfg))
@@ -340,41 +414,52 @@ def cpu_baseline(cfg, samples: int = 1, steps_per_sample: int = 2):
     kp, vp = kp.astype(np.float64), vp.astype(np.float64)
     scales = fm_synth.default_act_scales(cfg)
     a = fm_synth.noise(cfg, 0).astype(np.float64)
+    big = cfg.M * cfg.d > 100_000
+    n_layers = min(cfg.L, 4) if big else cfg.L
+    steps = 1 if big else 2
     times = []
     for _ in range(samples):
         t0 = time.perf_counter()
-        for k in range(steps_per_sample):
-            a = O.euler_step(model, k, a, kp, vp, scales)
-        times.append((time.perf_counter() - t0) / steps_per_sample * cfg.S * 1e3)
+        if big:
+            x = a @ model.final["w_in"].T + model.final["b_in"]
+            for l in range(n_layers):
+                q = O.pre_attn_quant(model, l, 0, x, scales)
+                x = O.layer_forward(model, l, 0, x, q, kp, vp, scales)
+        else:
+            for k in range(steps):
+                a = O.euler_step(model, k, a, kp, vp, scales)
+        dt = time.perf_counter() - t0
+        times.append(dt / (steps * n_layers) * cfg.S * cfg.L * 1e3)
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
         cores = os.cpu_count()
+    what = (f"{n_layers} layers of Euler step 0" if big else f"{steps} Euler steps x {cfg.L} layers")
     return {"value": round(statistics.median(times), 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{steps_per_sample} Euler steps x {cfg.L} layers of {WORKLOAD} (FP64 numpy, "
-                      f"weights prepared outside the timing), scaled x{cfg.S // steps_per_sample} to one decision"}
+            "sample": f"{what} of {cfg.name} (FP64 numpy, weights prepared outside the timing), "
+                      f"scaled to one {cfg.L}-layer x {cfg.S}-step decision"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    cfg = fm_synth.config(WORKLOAD)
-    base = cpu_baseline(cfg, samples=max(1, args.steps), steps_per_sample=1)
+    cfg = fm_synth.config(args.workload)
+    base = cpu_baseline(cfg, samples=max(1, min(args.steps, 3)))
     return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": base["value"], "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers": cfg.L, "euler_steps": cfg.S, "action_rows": cfg.M},
+            "config": {"workload": cfg.name, "layers": cfg.L, "euler_steps": cfg.S, "action_rows": cfg.M},
             "cpu_baseline": base,
             "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def profile_case():
+def profile_case(workload=WORKLOAD):
     """Small ncu target: a 1-layer, 1-step policy of the bench workload (about 18 MiB
     on the device); the second decision runs inside a cudaProfilerStart/Stop range
     (ncu --profile-from-start off)."""
     import torch
     import flow_matching_action_denoise_gb300 as fmad
-    cfg = fm_synth.config(WORKLOAD, L=1, S=1)
+    cfg = fm_synth.config(workload, L=1, S=1)
     pol = fmad.Policy(cfg, [fm_synth.layer_weights(cfg, 0)], fm_synth.final_weights(cfg),
                       act_scales=fm_synth.default_act_scales(cfg))
     kp, vp = fm_synth.prefix_kv(cfg)
@@ -489,6 +574,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["expert_fp8_m50", "wam_nvfp4_m256"], default=WORKLOAD,
+                    help="decoder workload (default: the 18-layer FP8 action expert, M = 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")
     ap.add_argument("--profile-case", action="store_true",
@@ -500,7 +587,7 @@ def main():
         print(json.dumps(run_bf16_protocol(args)), flush=True)
         return
     if args.profile_case:
-        profile_case()
+        profile_case(args.workload)
         return
     if args.warmup < 3:
         args.warmup = 3

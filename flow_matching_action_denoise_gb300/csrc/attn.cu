@@ -58,11 +58,6 @@ __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gmem_s
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w)
@@ -379,7 +374,16 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
         cc.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.y * rs, __NV_SATFINITE, __NV_E4M3));
         cc.z = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.z * rs, __NV_SATFINITE, __NV_E4M3));
         cc.w = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.w * rs, __NV_SATFINITE, __NV_E4M3));
-        *reinterpret_cast<uchar4*>(static_cast<uint8_t*>(p.out) + oidx) = cc;
+        if (p.out_fp8 == kQFp8AsF16) {   // the codes' f16 values (exact)
+          const uint8_t b[4] = {cc.x, cc.y, cc.z, cc.w};
+          uint32_t h[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            h[i] = __half_as_ushort(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b[i]), __NV_E4M3)));
+          *reinterpret_cast<uint2*>(static_cast<__half*>(p.out) + oidx) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        } else {
+          *reinterpret_cast<uchar4*>(static_cast<uint8_t*>(p.out) + oidx) = cc;
+        }
       } else {
         uint2 u;
         u.x = pack_bf16(acc.x, acc.y);

@@ -519,16 +519,24 @@ cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const Ge
 size_t packed_weight_bytes(int N, int K, int fmt) {
   if (fmt == FM_FMT_FP8) return static_cast<size_t>(N) * K;
   if (fmt == FM_FMT_BF16) return static_cast<size_t>(N) * K * 2;
+  if (fmt == FM_FMT_NVFP4) return nvfp4_packed_bytes(N, K);
   return 0;
+}
+
+cudaError_t weight_amax_launch(const float* w, const float* gamma, int N, int K, unsigned* amax, cudaStream_t st) {
+  const cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  amax_fold_kernel<<<1184, 256, 0, st>>>(w, gamma, N, K, amax);
+  return cudaGetLastError();
 }
 
 cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
                         unsigned* amax_scratch, cudaStream_t st, int geglu_interleave) {
   const int threads = 256;
+  if (fmt == FM_FMT_NVFP4) return pack_nvfp4(w, gamma, N, K, packed, scale_out, amax_scratch, st, geglu_interleave);
   if (fmt == FM_FMT_FP8) {
-    cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), st);
+    cudaError_t e = weight_amax_launch(w, gamma, N, K, amax_scratch, st);
     if (e != cudaSuccess) return e;
-    amax_fold_kernel<<<1184, threads, 0, st>>>(w, gamma, N, K, amax_scratch);
     scale_from_amax_kernel<<<1, 1, 0, st>>>(amax_scratch, scale_out);
     const size_t chunks = static_cast<size_t>(N) * K / 16;
     pack_fp8_kernel<<<static_cast<unsigned>((chunks + threads - 1) / threads), threads, 0, st>>>(

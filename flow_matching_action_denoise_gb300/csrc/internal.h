@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -88,6 +89,31 @@ cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const Ge
                         const float* sq = nullptr);
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
+// ---------------------------------------------------------------- NVFP4-weight GEMM
+struct Nvfp4Shape {
+  int M, N, K;
+  int s;           // K-split: partial planes [s][M][N]
+  int n_pad;       // MMA N (M rounded up to 16)
+  int nkb_total;   // 64-element K blocks
+  int nkb_cta;
+  int op_stages;   // decoded-operand pipeline stages
+  size_t smem;
+};
+int nvfp4_plan(int M, int N, int K, int s, Nvfp4Shape* g);
+// Activation tensor map: f16 values of E4M3 codes [M][K], box = 64 elements x n_pad rows.
+bool nvfp4_tmap_act(CUtensorMap* map, const void* a, const Nvfp4Shape& g);
+cudaError_t nvfp4_configure();
+// out: fp32 partial planes [s][M][N]; or out_geglu (s == 1, gate|up packed with
+// interleave): f16 values of E4M3(gelu(g) u * (1/s_q)) [M][N/2], g, u dequantised by fp32(sa * sw).
+cudaError_t nvfp4_gemm_launch(const CUtensorMap& tmA, const void* wpk, const Nvfp4Shape& g, float* out,
+                              __half* out_geglu, const float* sa, const float* sw, const float* sq, int* err,
+                              const LaunchOpts& o);
+size_t nvfp4_packed_bytes(int N, int K);
+cudaError_t pack_nvfp4(const float* w, const float* gamma, int N, int K, void* packed, float* ts_out,
+                       unsigned* amax_scratch, cudaStream_t st, int geglu_interleave);
+// max |w[n][k] * gamma[k]| (fp32 products) as the bits of a non-negative float.
+cudaError_t weight_amax_launch(const float* w, const float* gamma, int N, int K, unsigned* amax, cudaStream_t st);
+
 // Packing
 size_t packed_weight_bytes(int N, int K, int fmt);
 // geglu_interleave: pack a gate|up weight [2F][K] so tile t holds gate rows 64t.. and up rows F+64t..
@@ -95,6 +121,12 @@ cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fm
                         unsigned* amax_scratch, cudaStream_t st, int geglu_interleave = 0);
 
 // ---------------------------------------------------------------- row kernels
+// Storage of a quantised GEMM operand (RowArgs::q_fp8, AttnArgs::out_fp8):
+// 0 = bf16 values, 1 = E4M3 codes, 2 = E4M3 codes stored as their f16 values.
+constexpr int kQFp8AsF16 = 2;
+// y[m][n] = bf16(sum_j planes[j][m][n] * fp32(sa * sw)) for s K-slice planes [s][M][N].
+cudaError_t qkv_finalize_launch(const float* planes, int s, int M, int N, const float* sa, const float* sw,
+                                __nv_bfloat16* out, const LaunchOpts& o);
 struct RowArgs {
   int M, N;
   // residual update from GEMM partials: x += gate * (sum_p parts[p] * fp32(sa*sw) + bias)

@@ -47,6 +47,7 @@ struct Layout {
   size_t total = 0;
   std::vector<size_t> wpk;   // [L*4] packed weights
   size_t wscale, ascale, mod, modf, w_in, b_in, w_out, b_out, gamma_f, kcache, vcache, a, x, q, o, q2, mc;
+  size_t qkvb;   // bf16 Q | K | V the attention reads (== y[0] unless NVFP4 reduces planes separately)
   size_t y[4];
   size_t err, amax, conds;
   size_t kv_bytes, a_bytes, scale_bytes;
@@ -61,9 +62,15 @@ struct Derived {
   int nqkv;
   int act_bytes;
   int fp8;
+  int nvfp4;
+  int q_store;   // quantised operand storage: 0 bf16, 1 E4M3 codes, 2 E4M3 codes as f16 values
   fm::GemmShape gs[4];
+  fm::Nvfp4Shape ns[4];
   int gN[4], gK[4];
   int attn_kc, attn_nsplit;
+  // fp32 partial planes GEMM g writes (its K-slices not reduced in the GEMM itself)
+  int nparts(int g) const { return nvfp4 ? ns[g].s : gs[g].s / gs[g].cs; }
+  int kernels_per_layer() const { return nvfp4 ? 8 : 7; }
 };
 
 int num_sms() {
@@ -106,10 +113,6 @@ int validate(const fm_config* c, std::string* why) {
     *why = "unsupported weight/activation format pair";
     return FM_ERR_INVALID_ARG;
   }
-  if (c->weight_fmt == FM_FMT_NVFP4) {
-    *why = "NVFP4 weights are not implemented in this build";
-    return FM_ERR_UNSUPPORTED;
-  }
   if (c->cond_mode != FM_COND_TIME && c->cond_mode != FM_COND_GIVEN) {
     *why = "bad cond_mode";
     return FM_ERR_INVALID_ARG;
@@ -131,9 +134,40 @@ int validate(const fm_config* c, std::string* why) {
 int derive(const fm_config* c, Derived* dv, std::string* why) {
   dv->nqkv = (c->H + 2 * c->Hkv) * c->Dh;
   dv->fp8 = c->act_fmt == FM_FMT_FP8;
-  dv->act_bytes = dv->fp8 ? 1 : 2;
+  dv->nvfp4 = c->weight_fmt == FM_FMT_NVFP4;
+  dv->q_store = dv->nvfp4 ? fm::kQFp8AsF16 : dv->fp8;
+  dv->act_bytes = dv->q_store == 1 ? 1 : 2;
   const int N[4] = {dv->nqkv, c->d, 2 * c->F, c->d};
   const int K[4] = {c->d, c->H * c->Dh, c->d, c->F};
+  if (dv->nvfp4) {
+    // NVFP4 weights: the GEMMs write fp32 partial planes (QKV's are reduced by a
+    // separate kernel into bf16); the gate|up GEMM applies GeGLU itself, so it keeps
+    // the whole K in one CTA.
+    for (int g = 0; g < 4; ++g) {
+      dv->gN[g] = N[g];
+      dv->gK[g] = K[g];
+      const int nkb = K[g] / 64;
+      int s = c->ksplit[g] > 0 ? c->ksplit[g] : (g == 2 ? 1 : auto_split(N[g] / 128, nkb));
+      if (g == 2 && s != 1) {
+        *why = "with NVFP4 weights the gate|up GEMM cannot be K-split (its epilogue applies GeGLU)";
+        return FM_ERR_SHAPE;
+      }
+      if (fm::nvfp4_plan(c->M, N[g], K[g], s, &dv->ns[g]) != FM_OK) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "NVFP4 GEMM %d: split %d does not divide %d K-blocks (N=%d, K=%d)", g, s, nkb,
+                 N[g], K[g]);
+        *why = buf;
+        return FM_ERR_SHAPE;
+      }
+      memset(&dv->gs[g], 0, sizeof(fm::GemmShape));
+    }
+    if (fm::attn_plan(c->M, c->P, &dv->attn_kc, &dv->attn_nsplit) != FM_OK) {
+      *why = "P + M keys exceed the attention plan's 8 slices x 192 keys";
+      return FM_ERR_SHAPE;
+    }
+    return FM_OK;
+  }
+  memset(dv->ns, 0, sizeof dv->ns);
   for (int g = 0; g < 4; ++g) {
     dv->gN[g] = N[g];
     dv->gK[g] = K[g];
@@ -193,8 +227,9 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.mc = ly.take(static_cast<size_t>(M) * c->F * dv.act_bytes);
   for (int g = 0; g < 4; ++g)
     ly.y[g] = ly.take(g == 2 ? 0 :   // the gate|up GEMM writes the GeGLU output directly
-                      g == 0 ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
-                             : static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4);
+                      (g == 0 && !dv.nvfp4) ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
+                                            : static_cast<size_t>(dv.nparts(g)) * M * dv.gN[g] * 4);
+  ly.qkvb = dv.nvfp4 ? ly.take(static_cast<size_t>(M) * dv.gN[0] * 2) : ly.y[0];
   ly.err = ly.take(64);
   ly.amax = ly.take(64);
   ly.conds = ly.take(static_cast<size_t>(S) * d * sizeof(double));
@@ -303,10 +338,10 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   size_t ybytes[4];
   for (int g = 0; g < 4; ++g) {
     y[g] = p->at<float>(p->ly.y[g]);
-    ybytes[g] = g == 0 ? static_cast<size_t>(c.M) * dv.gN[0] * 2
-                       : static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * c.M * dv.gN[g] * 4;
+    ybytes[g] = g == 0 ? static_cast<size_t>(c.M) * dv.gN[0] * 2 : static_cast<size_t>(dv.nparts(g)) * c.M * dv.gN[g] * 4;
   }
-  const int fp8 = dv.fp8;
+  const int fp8 = dv.q_store;
+  __nv_bfloat16* qkvb = p->at<__nv_bfloat16>(p->ly.qkvb);
   const size_t xbytes = static_cast<size_t>(c.M) * c.d * 4;
   const size_t ab = dv.act_bytes;
   Trace none;
@@ -320,13 +355,22 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   FM_REC(p->at<void>(p->ly.q), static_cast<size_t>(c.M) * c.d * ab);
 
   // QKV: the epilogue dequantises and rounds to bf16, the operand attention reads
-  e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], nullptr, err, o,
-                      reinterpret_cast<__nv_bfloat16*>(y[0]), p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0));
+  // (NVFP4: partial planes, reduced and rounded by a separate kernel)
+  if (dv.nvfp4) {
+    e = fm::nvfp4_gemm_launch(p->tmA[0], p->at<void>(p->ly.wpk[l * 4 + 0]), dv.ns[0], y[0], nullptr, nullptr, nullptr,
+                              nullptr, err, o);
+    if (e != cudaSuccess) return e;
+    e = fm::qkv_finalize_launch(y[0], dv.ns[0].s, c.M, dv.gN[0], p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), qkvb,
+                                o);
+  } else {
+    e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], nullptr, err, o, qkvb, p->ascale(l, FM_SITE_ATTN_IN),
+                        p->wscale(l, 0));
+  }
   if (e != cudaSuccess) return e;
-  FM_REC(y[0], ybytes[0]);
+  FM_REC(qkvb, ybytes[0]);
 
   fm::AttnArgs at;
-  at.qkv = reinterpret_cast<const __nv_bfloat16*>(y[0]);
+  at.qkv = qkvb;
   const int p_pad = (c.P + 7) / 8 * 8;
   at.kpre = p->at<__nv_bfloat16>(p->ly.kcache) + static_cast<size_t>(l) * c.P * c.Hkv * c.Dh;
   at.vtpre = p->at<__nv_bfloat16>(p->ly.vcache) + static_cast<size_t>(l) * c.Hkv * c.Dh * p_pad;
@@ -345,7 +389,9 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   if (e != cudaSuccess) return e;
   FM_REC(p->at<void>(p->ly.o), static_cast<size_t>(c.M) * c.H * c.Dh * ab);
 
-  e = fm::gemm_launch(p->tmW[l * 4 + 1], p->tmA[1], dv.gs[1], y[1], err, o);
+  e = dv.nvfp4 ? fm::nvfp4_gemm_launch(p->tmA[1], p->at<void>(p->ly.wpk[l * 4 + 1]), dv.ns[1], y[1], nullptr, nullptr,
+                                       nullptr, nullptr, err, o)
+               : fm::gemm_launch(p->tmW[l * 4 + 1], p->tmA[1], dv.gs[1], y[1], err, o);
   if (e != cudaSuccess) return e;
   FM_REC(y[1], ybytes[1]);
 
@@ -353,7 +399,7 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   r1.M = c.M;
   r1.N = c.d;
   r1.parts = y[1];
-  r1.nparts = dv.gs[1].s / dv.gs[1].cs;
+  r1.nparts = dv.nparts(1);
   r1.sa = p->ascale(l, FM_SITE_ATTN_OUT);
   r1.sw = p->wscale(l, 1);
   r1.gate = p->mod(k, l, 2);
@@ -371,12 +417,18 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
 
   // gate|up: the epilogue applies GeGLU and quantises, writing the down GEMM's operand
-  e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], nullptr, err, o, nullptr, p->ascale(l, FM_SITE_MLP_IN),
-                      p->wscale(l, 2), p->at<void>(p->ly.mc), fp8, p->ascale(l, FM_SITE_GEGLU));
+  if (dv.nvfp4)
+    e = fm::nvfp4_gemm_launch(p->tmA[2], p->at<void>(p->ly.wpk[l * 4 + 2]), dv.ns[2], nullptr, p->at<__half>(p->ly.mc),
+                              p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->ascale(l, FM_SITE_GEGLU), err, o);
+  else
+    e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], nullptr, err, o, nullptr, p->ascale(l, FM_SITE_MLP_IN),
+                        p->wscale(l, 2), p->at<void>(p->ly.mc), fp8, p->ascale(l, FM_SITE_GEGLU));
   if (e != cudaSuccess) return e;
   FM_REC(p->at<void>(p->ly.mc), static_cast<size_t>(c.M) * c.F * ab);
 
-  e = fm::gemm_launch(p->tmW[l * 4 + 3], p->tmA[3], dv.gs[3], y[3], err, o);
+  e = dv.nvfp4 ? fm::nvfp4_gemm_launch(p->tmA[3], p->at<void>(p->ly.wpk[l * 4 + 3]), dv.ns[3], y[3], nullptr, nullptr,
+                                       nullptr, nullptr, err, o)
+               : fm::gemm_launch(p->tmW[l * 4 + 3], p->tmA[3], dv.gs[3], y[3], err, o);
   if (e != cudaSuccess) return e;
   FM_REC(y[3], ybytes[3]);
 
@@ -384,7 +436,7 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   r2.M = c.M;
   r2.N = c.d;
   r2.parts = y[3];
-  r2.nparts = dv.gs[3].s / dv.gs[3].cs;
+  r2.nparts = dv.nparts(3);
   r2.sa = p->ascale(l, FM_SITE_GEGLU);
   r2.sw = p->wscale(l, 3);
   r2.gate = p->mod(k, l, 5);
@@ -432,7 +484,7 @@ size_t trace_record_bytes(const fm_policy* p) {
   const size_t M = c.M, ab = dv.act_bytes;
   size_t n = 3 * M * c.d * 4 + M * c.d * ab * 2 + M * c.H * c.Dh * ab + M * c.F * ab + p->ly.a_bytes;
   n += M * dv.gN[0] * 2;
-  for (int g = 1; g < 4; g += 2) n += static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4;
+  for (int g = 1; g < 4; g += 2) n += static_cast<size_t>(dv.nparts(g)) * M * dv.gN[g] * 4;
   return n;
 }
 
@@ -452,7 +504,7 @@ cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
   r.shift = p->mod(0, 0, 1);
   r.sq = p->ascale(0, FM_SITE_ATTN_IN);
   r.q = p->at<void>(p->ly.q);
-  r.q_fp8 = p->dv.fp8;
+  r.q_fp8 = p->dv.q_store;
   r.eps = c.rms_eps;
   return fm::row_launch(r, o);
 }
@@ -688,7 +740,8 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
     return false;
   };
 
-  if (!cu(fm::gemm_configure(), "gemm_configure") || !cu(fm::attn_configure(), "attn_configure"))
+  if (!cu(fm::gemm_configure(), "gemm_configure") || !cu(fm::nvfp4_configure(), "nvfp4_configure") ||
+      !cu(fm::attn_configure(), "attn_configure"))
     return bail(FM_ERR_CUDA, why);
 
   // weights: fold gamma, quantise, tile
@@ -742,21 +795,28 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
   if (!cu(cudaStreamSynchronize(s), "create sync")) return bail(FM_ERR_CUDA, why);
 
   // tensor maps (fixed addresses, recorded into the graph by value)
-  p->tmW.resize(static_cast<size_t>(c.L) * 4);
-  for (int l = 0; l < c.L; ++l)
-    for (int g = 0; g < 4; ++g)
-      if (!fm::gemm_tmap_weight(&p->tmW[l * 4 + g], p->at<void>(p->ly.wpk[l * 4 + g]), dv.gs[g]))
-        return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed");
   const size_t act_off[4] = {p->ly.q, p->ly.o, p->ly.q2, p->ly.mc};
-  for (int g = 0; g < 4; ++g)
-    if (!fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.gs[g]))
-      return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
+  if (dv.nvfp4) {   // packed NVFP4 blocks are fetched with plain bulk copies: no weight maps
+    for (int g = 0; g < 4; ++g)
+      if (!fm::nvfp4_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.ns[g]))
+        return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
+  } else {
+    p->tmW.resize(static_cast<size_t>(c.L) * 4);
+    for (int l = 0; l < c.L; ++l)
+      for (int g = 0; g < 4; ++g)
+        if (!fm::gemm_tmap_weight(&p->tmW[l * 4 + g], p->at<void>(p->ly.wpk[l * 4 + g]), dv.gs[g]))
+          return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed");
+    for (int g = 0; g < 4; ++g)
+      if (!fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.gs[g]))
+        return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
+  }
 
   uint64_t h = 1469598103934665603ull;
   h = fnv(h, &c, sizeof c);
   const uintptr_t base = reinterpret_cast<uintptr_t>(p->ws);
   h = fnv(h, &base, sizeof base);
   for (int g = 0; g < 4; ++g) h = fnv(h, &dv.gs[g], sizeof(fm::GemmShape));
+  for (int g = 0; g < 4; ++g) h = fnv(h, &dv.ns[g], sizeof(fm::Nvfp4Shape));
   h = fnv(h, &dv.attn_kc, sizeof(int));
   p->plan_hash = h;
 
@@ -939,7 +999,7 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
   const Derived& dv = p->dv;
   const Layout& ly = p->ly;
   const size_t M = c.M, ab = dv.act_bytes;
-  auto ypart = [&](int g) { return static_cast<size_t>(dv.gs[g].s / dv.gs[g].cs) * M * dv.gN[g] * 4; };
+  auto ypart = [&](int g) { return static_cast<size_t>(dv.nparts(g)) * M * dv.gN[g] * 4; };
   struct Entry {
     const char* n;
     size_t off, bytes;
@@ -952,7 +1012,7 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
       {"q2", ly.q2, M * c.d * ab},
       {"attn_out", ly.o, M * c.H * c.Dh * ab},
       {"geglu_out", ly.mc, M * c.F * ab},
-      {"y_qkv", ly.y[0], M * dv.gN[0] * 2},
+      {"y_qkv", ly.qkvb, M * dv.gN[0] * 2},
       {"y_o", ly.y[1], ypart(1)},
       {"y_d", ly.y[3], ypart(3)},
       {"act_scales", ly.ascale, ly.scale_bytes},
@@ -996,8 +1056,8 @@ int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trac
 
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) {
   if (!p || !per_layer || !per_decision) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
-  *per_layer = 7;
-  *per_decision = 1 + p->cfg.S * p->cfg.L * 7;
+  *per_layer = p->dv.kernels_per_layer();
+  *per_decision = 1 + p->cfg.S * p->cfg.L * p->dv.kernels_per_layer();
   return FM_OK;
 }
 
@@ -1011,7 +1071,8 @@ int fm_test_quant_e4m3(const float* x, int64_t n, float scale, uint8_t* codes, v
 int fm_packed_weight_bytes(int N, int K, int fmt, size_t* bytes) {
   if (!bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "bytes is NULL");
   if (N <= 0 || K <= 0 || N % 128 || K % 128) return fail(nullptr, FM_ERR_SHAPE, "N, K must be multiples of 128");
-  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16 && fmt != FM_FMT_NVFP4)
+    return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
   *bytes = fm::packed_weight_bytes(N, K, fmt);
   return FM_OK;
 }
@@ -1020,7 +1081,8 @@ int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt, vo
                    void* stream) {
   if (!w || !packed || !scale_out) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
   if (N <= 0 || K <= 0 || N % 128 || K % 128) return fail(nullptr, FM_ERR_SHAPE, "N, K must be multiples of 128");
-  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16 && fmt != FM_FMT_NVFP4)
+    return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
   if (reinterpret_cast<uintptr_t>(packed) % kAlign) return fail(nullptr, FM_ERR_ALIGN, "packed not 1024-aligned");
   // The caller's 4-byte scale slot doubles as the amax accumulator: the amax kernel
   // fills it, then one thread reads it and overwrites it with the scale.
@@ -1032,9 +1094,27 @@ int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt, vo
 int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s, int cluster_reduce,
                         float* partials, void* stream) {
   if (!a || !w_packed || !partials) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
-  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16) return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
+  if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16 && fmt != FM_FMT_NVFP4)
+    return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
   if (!aligned16(a) || reinterpret_cast<uintptr_t>(w_packed) % kAlign)
     return fail(nullptr, FM_ERR_ALIGN, "a must be 16-byte and w_packed 1024-byte aligned");
+  if (fmt == FM_FMT_NVFP4) {
+    if (cluster_reduce != 1) return fail(nullptr, FM_ERR_SHAPE, "NVFP4 GEMM writes every slice: cluster_reduce 1");
+    fm::Nvfp4Shape g;
+    if (fm::nvfp4_plan(M, N, K, s, &g) != FM_OK)
+      return fail(nullptr, FM_ERR_SHAPE, "GEMM shape/split precondition violated");
+    CUtensorMap ta;
+    if (!fm::nvfp4_tmap_act(&ta, a, g)) return fail(nullptr, FM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    cudaError_t e = fm::nvfp4_configure();
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "nvfp4_configure");
+    int* err_word = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err_word), fm_standalone_err);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
+    LaunchOpts o;
+    o.stream = static_cast<cudaStream_t>(stream);
+    e = fm::nvfp4_gemm_launch(ta, w_packed, g, partials, nullptr, nullptr, nullptr, nullptr, err_word, o);
+    return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "nvfp4 gemm launch");
+  }
   fm::GemmShape g;
   const int st = fm::gemm_plan(M, N, K, fmt == FM_FMT_FP8, s, cluster_reduce, &g);
   if (st != FM_OK) return fail(nullptr, st, "GEMM shape/split precondition violated");
@@ -1123,7 +1203,7 @@ int fm_test_layer(fm_policy* p, const float* x_in, int layer, int step, float* x
   r.shift = p->mod(step, layer, 1);
   r.sq = p->ascale(layer, FM_SITE_ATTN_IN);
   r.q = p->at<void>(p->ly.q);
-  r.q_fp8 = p->dv.fp8;
+  r.q_fp8 = p->dv.q_store;
   r.eps = p->cfg.rms_eps;
   FM_CUDA(p, fm::row_launch(r, o));
   FM_CUDA(p, enqueue_layer(p, layer, step, false, o));

@@ -43,6 +43,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -86,6 +89,22 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Plain bulk copy of `bytes` contiguous bytes (16-byte aligned both sides, size a
+// multiple of 16) into shared memory, completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -153,6 +172,11 @@ __device__ __forceinline__ uint32_t make_idesc(bool fp8, uint32_t mma_m, uint32_
          | (fmt << 10)             // B format
          | ((mma_n >> 3) << 17)    // N >> 3
          | ((mma_m >> 4) << 24);   // M >> 4
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B (format code 0), fp32 D.
+__device__ __forceinline__ uint32_t make_idesc_f16(uint32_t mma_m, uint32_t mma_n) {
+  return (1u << 4) | ((mma_n >> 3) << 17) | ((mma_m >> 4) << 24);
 }
 
 // Each thread of a warp reads 16 consecutive 32-bit columns of its TMEM lane.

@@ -16,7 +16,10 @@
 // Create-time kernels: timestep embedding and the per-step modulation table.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -46,7 +49,16 @@ __device__ __forceinline__ uint8_t e4m3(float v) {
 }
 
 __device__ __forceinline__ void store_q4(void* q, size_t idx, float4 h, int fp8, float rs) {
-  if (fp8) {
+  if (fp8 == kQFp8AsF16) {   // E4M3 codes stored as their f16 values (exact)
+    const uint8_t c[4] = {e4m3(h.x * rs), e4m3(h.y * rs), e4m3(h.z * rs), e4m3(h.w * rs)};
+    __half v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c[i]), __NV_E4M3));
+    uint2 u;
+    u.x = static_cast<uint32_t>(__half_as_ushort(v[0])) | (static_cast<uint32_t>(__half_as_ushort(v[1])) << 16);
+    u.y = static_cast<uint32_t>(__half_as_ushort(v[2])) | (static_cast<uint32_t>(__half_as_ushort(v[3])) << 16);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(q) + idx) = u;
+  } else if (fp8) {
     uchar4 c;
     c.x = e4m3(h.x * rs);
     c.y = e4m3(h.y * rs);
@@ -261,6 +273,43 @@ __global__ void quant_e4m3_kernel(const float* __restrict__ x, int64_t n, float 
 }
 
 }  // namespace
+
+namespace {
+
+// y[m][n] = bf16(sum_j planes[j][m][n] * fp32(sa * sw)), slices summed in order j = 0..s-1.
+__global__ void __launch_bounds__(256) qkv_finalize_kernel(const float* __restrict__ planes, int s, size_t n4,
+                                                           const float* __restrict__ sa,
+                                                           const float* __restrict__ sw, __nv_bfloat16* out) {
+  pdl_trigger();
+  const float ds = __fmul_rn(*sa, *sw);
+  pdl_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(planes)[i];
+    for (int j = 1; j < s; ++j) {
+      const float4 v = reinterpret_cast<const float4*>(planes + static_cast<size_t>(j) * n4 * 4)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * ds, acc.y * ds);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * ds, acc.w * ds);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(out)[i] = u;
+  }
+}
+
+}  // namespace
+
+cudaError_t qkv_finalize_launch(const float* planes, int s, int M, int N, const float* sa, const float* sw,
+                                __nv_bfloat16* out, const LaunchOpts& o) {
+  const size_t n4 = static_cast<size_t>(M) * N / 4;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n4 + 255) / 256, 1216));
+  return launch(qkv_finalize_kernel, dim3(blocks), dim3(256), 0, o, planes, s, n4, sa, sw, out);
+}
 
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
   const size_t smem = static_cast<size_t>(r.N) * sizeof(float);

@@ -89,7 +89,9 @@ enum {
  *   1 <= M <= 256; 1 <= A <= 256; P >= 0; L, S >= 1;
  *   ksplit[i] (0 = automatic) divides the GEMM's K/128-byte block count.
  * act_fmt must be FP8 or BF16; weight_fmt FP8 requires act_fmt FP8, BF16
- * requires BF16, NVFP4 requires FP8. */
+ * requires BF16, NVFP4 requires FP8. With NVFP4 weights the K-split counts
+ * 64-element blocks, the gate|up GEMM is not split (ksplit[2] 0 or 1), and a
+ * layer runs 8 kernels (the QKV partial planes are reduced by their own kernel). */
 typedef struct fm_config {
   int abi_version;     /* must be FM_ABI_VERSION */
   int L, S, M, d, H, Hkv, Dh, F, P, A;
@@ -223,7 +225,9 @@ int fm_device_status(fm_policy* p, void* stream, int* word);
  *   "y_o", "y_d"            fp32 [parts][M][N] GEMM partial planes
  *   "act_scales", "weight_scales"  fp32 [L][4]
  *   "mod"                   fp32 [S][L][6][d]; "mod_final" fp32 [S][2][d]
- * Codes are one byte (FP8 activations) or bf16. FM_ERR_INVALID_ARG for an unknown name. */
+ * Codes are one byte (FP8 activations), bf16 (BF16), or, with NVFP4 weights, the
+ * E4M3 codes' f16 values (two bytes, exact: the operand format of the NVFP4 GEMM).
+ * FM_ERR_INVALID_ARG for an unknown name. */
 int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* bytes);
 
 /* Bytes of one decision trace (see fm_decode_trace). */
@@ -267,6 +271,12 @@ int fm_packed_weight_bytes(int N, int K, int fmt, size_t* bytes);
 /* Fold gamma (device fp32 [K] or NULL), quantise and tile a weight w (device fp32
  * [N][K]) into `packed` (device, 1024-byte aligned, fm_packed_weight_bytes).
  * scale_out (device fp32 [1]) receives the tensor scale (1.0 for BF16).
+ * NVFP4 (news article "FlashRT-PAI", 4-bit weights): ts = fp32(amax) / 2688;
+ * per 16 consecutive K elements bs = E4M3(amax_block / fp32(6 ts)); elements
+ * e = E2M1_RNE(w' / fp32(bs ts)) (0 where bs ts == 0), w' = fp32(w gamma); all
+ * divisions fp32 round-to-nearest. Layout: blocks (n/128, k/64) of 4608 bytes,
+ * n-tile-major then k-block, each [128 rows][32 bytes] of codes (element 2i in
+ * the low nibble) followed by [128 rows][4] block-scale codes.
  * FP8 tile layout: tile (n/128, k/128) is 128 rows x 128 bytes, rows n, bytes k,
  * tiles ordered n-tile-major then k-block; each tile is stored as TMA writes it
  * with 128-byte swizzle undone, i.e. plain [128][128] bytes (BF16: [128][64]). */
@@ -280,7 +290,9 @@ int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt,
  * cluster_reduce = c (1, 2, 4 or 8, dividing s): the c CTAs of consecutive
  * slices sum their partials in fixed order through distributed shared memory,
  * so partials holds s/c slices [s/c][M][N]. 1 <= M <= 256; N, K multiples of
- * 128; s divides K/128 (FP8) or K/64 (BF16). */
+ * 128; s divides K/128 (FP8) or K/64 (BF16). fmt NVFP4: A holds the f16
+ * values of E4M3 codes [M][K], w_packed NVFP4 from fm_pack_weight, the partials
+ * are sum A * (e * bs) without ts, s divides K/64 and cluster_reduce is 1. */
 int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt,
                         int s, int cluster_reduce, float* partials, void* stream);
 

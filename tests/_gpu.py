@@ -70,7 +70,8 @@ def parse_trace(raw, cfg, pol):
     returned as decoded values (E4M3 codes without their scale, or bf16 values)."""
     M, d = cfg.M, cfg.d
     fp8 = cfg.act_fmt == "fp8"
-    ab = 1 if fp8 else 2
+    f16_codes = cfg.weight_fmt == "nvfp4"   # E4M3 codes stored as their f16 values
+    ab = 1 if fp8 and not f16_codes else 2
 
     def parts(name, n):
         _, nbytes = fmad.named_buffer(pol.handle, name)
@@ -97,6 +98,8 @@ def parse_trace(raw, cfg, pol):
                     r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
                 elif kind == "f":
                     r[name] = chunk.view(np.float32).reshape(shape).astype(np.float64)
+                elif f16_codes:
+                    r[name] = chunk.view(np.float16).astype(np.float64).reshape(shape)
                 elif fp8:
                     r[name] = C.e4m3_decode_code(chunk).reshape(shape)
                 else:

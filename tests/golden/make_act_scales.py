@@ -17,7 +17,7 @@ import fm_synth  # noqa: E402
 from oracle import model as O  # noqa: E402
 
 
-def main(names=("layer_fp8_m10", "expert_fp8_m50")):
+def main(names=("layer_fp8_m10", "expert_fp8_m50", "wam_nvfp4_m256")):
     for name in names:
         cfg = fm_synth.config(name)
         layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
@@ -44,4 +44,4 @@ def main(names=("layer_fp8_m10", "expert_fp8_m50")):
 
 
 if __name__ == "__main__":
-    main(sys.argv[1:] or ("layer_fp8_m10", "expert_fp8_m50"))
+    main(sys.argv[1:] or ("layer_fp8_m10", "expert_fp8_m50", "wam_nvfp4_m256"))
