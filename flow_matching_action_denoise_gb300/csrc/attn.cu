@@ -14,13 +14,15 @@
 // contractions run on tcgen05 tensor cores with bf16 operands in shared memory
 // (K-major, 128-byte swizzle, the layout TMA writes) and fp32 accumulators in
 // TMEM: S = Q K^T (M = 128 rows, N = slice keys, K = 128 head dims), then
-// O = P V (N = 128 head dims, K = slice keys) with V held transposed. Each of the
-// four warps owns 32 rows (its TMEM lane quarter), so the softmax needs no
-// shuffles: pass 1 reads S for the row max and sum, the cluster exchanges them
-// through distributed shared memory so every CTA normalises with the global max
-// and sum, pass 2 forms P = exp(s - M) / L, rounds it to bf16 and writes the
-// swizzled operand. The slices' shares of O are summed across the cluster in
-// fixed slice order and quantised with the static output scale.
+// O = P V (N = 128 head dims, K = slice keys) with V held transposed. Two warps
+// share each TMEM lane quarter (32 rows) and split the slice's keys, so the softmax
+// needs no shuffles: pass 1 reads S, takes each row half's max m_h and keeps
+// exp(s - m_h) in registers with its sum; the cluster exchanges the (max, sum)
+// pairs through distributed shared memory so every CTA normalises with the global
+// max M and sum L; pass 2 forms P = exp(s - m_h) * exp(m_h - M) / L, rounds it to
+// bf16 and writes the swizzled operand. Each slice pushes its share of O into the
+// shared memory of the CTA that finalises those rows, which sums the shares in
+// fixed slice order and quantises with the static output scale.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -260,10 +262,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   float mh = -INFINITY;
 #pragma unroll
   for (int e = 0; e < kHalf; ++e) mh = fmaxf(mh, sv[e]);
+  // sv <- exp(s - m_half): the only exponentials of the row; pass 2 rescales them
   float lh = 0.f;
-  if (mh > -INFINITY) {
 #pragma unroll
-    for (int e = 0; e < kHalf; ++e) lh += exp2f(sv[e] - mh);
+  for (int e = 0; e < kHalf; ++e) {
+    sv[e] = mh > -INFINITY ? exp2f(sv[e] - mh) : 0.f;
+    lh += sv[e];
   }
   sPart[half * kRows + r] = make_float2(mh, lh);
   __syncthreads();
@@ -290,13 +294,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   }
   const float ginv = 1.0f / gsum;
 
-  // ---- pass 2: P = bf16(exp(s - M) / L) into the swizzled A operand of P V
+  // ---- pass 2: P = bf16(exp(s - m_half) * exp(m_half - M) / L) into the swizzled A
+  // operand of P V
+  const float fscale = mh > -INFINITY ? exp2f(mh - gmax) * ginv : 0.f;
 #pragma unroll
   for (int ch = 0; ch < kHalf / 8; ++ch) {   // 8-key chunks of 16 bytes
     const int key = c0 + ch * 8;
     float pv[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) pv[e] = key + e < nvalid ? exp2f(sv[ch * 8 + e] - gmax) * ginv : 0.f;
+    for (int e = 0; e < 8; ++e) pv[e] = key + e < nvalid ? sv[ch * 8 + e] * fscale : 0.f;
     uint4 u;
     u.x = pack_bf16(pv[0], pv[1]);
     u.y = pack_bf16(pv[2], pv[3]);

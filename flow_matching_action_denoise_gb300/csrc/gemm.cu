@@ -8,8 +8,11 @@
 // GB300 mapping ("swap-AB"): the weight tile is the MMA's A operand (M = 128 rows
 // of W, i.e. 128 output columns n), the activations are the MMA's B operand
 // (N = M rounded up to 16), so the tiny row count costs nothing in tensor-core
-// shape and the weights - the only large operand - stream through TMA in
-// 16 KB boxes (128 rows x 128 bytes of K) into a multi-stage shared-memory ring.
+// shape. Each TMA transaction and each barrier round trip costs a fixed ~0.1-0.3 us
+// on this part while the bytes of one transaction are nearly free up to tens of KB,
+// so a pipeline stage moves `chunk` K blocks at once: the weights - the only large
+// operand, packed pre-swizzled so a plain bulk copy lands them in the MMA layout -
+// in one copy of chunk x 16 KB, the activations in one 3-D box of chunk K blocks.
 // One elected thread issues the TMA loads, another issues tcgen05.mma into a
 // TMEM accumulator; four warps read TMEM back. CTAs (n-tile, slice j) of
 // consecutive slices form a thread-block cluster of size cs that sums its
@@ -39,6 +42,7 @@ constexpr size_t kStageCap = 196 * 1024;         // shared-memory budget for the
 constexpr size_t kCtrlBytes = 256;
 
 struct KParams {
+  const uint8_t* wpk;       // packed, pre-swizzled weight tiles [N/128][K blocks][128][128 B]
   float* out;               // fp32 partial planes [s/cs][M][N], or
   __nv_bfloat16* out_bf16;  // when non-null (cs == s): bf16(sum * fp32(sa * sw)) [M][N]
   void* out_geglu;          // when non-null (cs == s, gate|up interleaved): Q(gelu(g) u) [M][N/2]
@@ -48,7 +52,7 @@ struct KParams {
   const float* sw;
   int M, N;
   int nkb_total, nkb_cta;
-  int n_pad, stages, cs;
+  int n_pad, stages, cs, chunk;
   int* err;
 };
 
@@ -61,8 +65,7 @@ __host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 template <bool kFp8, int kCs>
-__global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
-                                                               const __grid_constant__ CUtensorMap tmA,
+__global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
@@ -70,10 +73,13 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   __shared__ int s_issued;
 
   const int stages = p.stages;
+  const int chunk = p.chunk;
   const uint32_t a_tile_bytes = static_cast<uint32_t>(p.n_pad) * kBlockBytes;
+  const uint32_t w_stage_bytes = static_cast<uint32_t>(chunk) * kWTileBytes;
+  const uint32_t a_stage_bytes = static_cast<uint32_t>(chunk) * a_tile_bytes;
   uint8_t* w_tiles = smem;
-  uint8_t* a_tiles = smem + static_cast<size_t>(stages) * kWTileBytes;
-  const size_t main_bytes = static_cast<size_t>(stages) * (kWTileBytes + a_tile_bytes);
+  uint8_t* a_tiles = smem + static_cast<size_t>(stages) * w_stage_bytes;
+  const size_t main_bytes = static_cast<size_t>(stages) * (w_stage_bytes + a_stage_bytes);
   const int rows_per = (p.M + kCs - 1) / kCs;   // output rows each cluster rank finalises
   float* recv = reinterpret_cast<float*>(smem + align_up(main_bytes, 1024));   // [kCs][rows_per][128]
   uint8_t* ctrl = reinterpret_cast<uint8_t*>(recv) +
@@ -98,7 +104,6 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     }
     mbar_init(done, 1);
     fence_mbar_init();
-    tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmA);
   }
   if (warp == 0) {
@@ -117,58 +122,61 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   // wait for this grid must never be able to take the columns this CTA still needs.
   pdl_trigger();
 
-  const int a_elems_per_block = kFp8 ? kBlockBytes : kBlockBytes / 2;
   const int kb0 = j * p.nkb_cta;
+  const int nst = p.nkb_cta / chunk;   // pipeline stages to run (chunk divides nkb_cta)
 
   if (threadIdx.x == 0) {
-    // ---------------- TMA producer
+    // ---------------- producer: per stage one bulk copy of chunk weight tiles (contiguous
+    // in the packed layout) and one 3-D box of chunk activation K blocks
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_a = l2_policy_evict_last();
-    const int wrow0 = (nt * p.nkb_total + kb0) * kTileN;
-    const uint32_t tx = kWTileBytes + a_tile_bytes;
-    for (int i = 0; i < stages; ++i) {
+    const uint8_t* wsrc = p.wpk + (static_cast<size_t>(nt) * p.nkb_total + kb0) * kWTileBytes;
+    const uint32_t tx = w_stage_bytes + a_stage_bytes;
+    const int pre = min(stages, nst);
+    for (int i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], tx);
-      tma_load_2d(w_tiles + static_cast<size_t>(i) * kWTileBytes, &tmW, &full[i], 0, wrow0 + i * kTileN, pol_w);
+      bulk_load(w_tiles + static_cast<size_t>(i) * w_stage_bytes, wsrc + static_cast<size_t>(i) * w_stage_bytes,
+                w_stage_bytes, &full[i], pol_w);
     }
     pdl_wait();   // activations are written by the previous kernel
-    for (int i = 0; i < stages; ++i)
-      tma_load_2d(a_tiles + static_cast<size_t>(i) * a_tile_bytes, &tmA, &full[i], (kb0 + i) * a_elems_per_block,
-                  0, pol_a);
-    int issued = stages;
-    for (int kb = stages; kb < p.nkb_cta; ++kb) {
-      const int slot = kb % stages;
-      const uint32_t use = static_cast<uint32_t>(kb / stages);
+    for (int i = 0; i < pre; ++i)
+      tma_load_3d(a_tiles + static_cast<size_t>(i) * a_stage_bytes, &tmA, &full[i], 0, 0, kb0 + i * chunk, pol_a);
+    int issued = pre;
+    for (int st = stages; st < nst; ++st) {
+      const int slot = st % stages;
+      const uint32_t use = static_cast<uint32_t>(st / stages);
       if (!mbar_wait(&empty[slot], (use - 1) & 1)) {
         atomicOr(p.err, kErrPipelineTimeout);
         s_abort = 1;
         break;
       }
       mbar_arrive_expect_tx(&full[slot], tx);
-      tma_load_2d(w_tiles + static_cast<size_t>(slot) * kWTileBytes, &tmW, &full[slot], 0, wrow0 + kb * kTileN,
-                  pol_w);
-      tma_load_2d(a_tiles + static_cast<size_t>(slot) * a_tile_bytes, &tmA, &full[slot],
-                  (kb0 + kb) * a_elems_per_block, 0, pol_a);
+      bulk_load(w_tiles + static_cast<size_t>(slot) * w_stage_bytes, wsrc + static_cast<size_t>(st) * w_stage_bytes,
+                w_stage_bytes, &full[slot], pol_w);
+      tma_load_3d(a_tiles + static_cast<size_t>(slot) * a_stage_bytes, &tmA, &full[slot], 0, 0, kb0 + st * chunk,
+                  pol_a);
       ++issued;
     }
     s_issued = issued;
   } else if (threadIdx.x == 32) {
     // ---------------- MMA issuer
     const uint32_t idesc = make_idesc(kFp8, kTileN, static_cast<uint32_t>(p.n_pad));
-    for (int kb = 0; kb < p.nkb_cta; ++kb) {
-      const int slot = kb % stages;
-      const uint32_t use = static_cast<uint32_t>(kb / stages);
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % stages;
+      const uint32_t use = static_cast<uint32_t>(st / stages);
       if (!mbar_wait(&full[slot], use & 1)) {
         atomicOr(p.err, kErrPipelineTimeout);
         s_abort = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t wa = smem_u32(w_tiles + static_cast<size_t>(slot) * kWTileBytes);
-      const uint32_t aa = smem_u32(a_tiles + static_cast<size_t>(slot) * a_tile_bytes);
+      for (int c = 0; c < chunk; ++c) {
+        const uint32_t wa = smem_u32(w_tiles + static_cast<size_t>(slot) * w_stage_bytes + c * kWTileBytes);
+        const uint32_t aa = smem_u32(a_tiles + static_cast<size_t>(slot) * a_stage_bytes + c * a_tile_bytes);
 #pragma unroll
-      for (int k = 0; k < kBlockBytes / 32; ++k) {
-        tc_mma<kFp8>(tmem, sw128_kmajor_desc(wa + k * 32), sw128_kmajor_desc(aa + k * 32), idesc,
-                     (kb > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kBlockBytes / 32; ++k)
+          tc_mma<kFp8>(tmem, sw128_kmajor_desc(wa + k * 32), sw128_kmajor_desc(aa + k * 32), idesc,
+                       (st > 0 || c > 0 || k > 0) ? 1u : 0u);
       }
       tc_commit(&empty[slot]);
     }
@@ -346,6 +354,8 @@ __global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __rest
   const int ntile = static_cast<int>(tile / nkb), kb = static_cast<int>(tile % nkb);
   const size_t n = source_row(static_cast<size_t>(ntile) * 128 + r, N, interleave);
   const int k0 = kb * 128 + cb;
+  // stored at the 128-byte-swizzled position of its 16-byte chunk (the MMA layout)
+  const size_t dst = tile * kWTileBytes + r * 128 + (((cb >> 4) ^ (r & 7)) << 4);
   alignas(16) uint8_t codes[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -353,7 +363,7 @@ __global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __rest
     const float v = __fmul_rn(__fmul_rn(w[n * K + k0 + i], g), rs);
     codes[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
   }
-  *reinterpret_cast<uint4*>(out + o) = *reinterpret_cast<const uint4*>(codes);
+  *reinterpret_cast<uint4*>(out + dst) = *reinterpret_cast<const uint4*>(codes);
 }
 
 // BF16: one thread writes 16 bytes (8 values) of a [128][64]-element tile.
@@ -370,13 +380,14 @@ __global__ void pack_bf16_kernel(const float* __restrict__ w, const float* __res
   const int ntile = static_cast<int>(tile / nkb), kb = static_cast<int>(tile % nkb);
   const size_t n = source_row(static_cast<size_t>(ntile) * 128 + r, N, interleave);
   const int k0 = kb * 64 + ce;
+  const size_t dst = tile * (128 * 64) + r * 64 + (((ce >> 3) ^ (r & 7)) << 3);   // swizzled chunk, in elements
   alignas(16) __nv_bfloat16 vals[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float g = gamma ? gamma[k0 + i] : 1.0f;
     vals[i] = __float2bfloat16_rn(__fmul_rn(w[n * K + k0 + i], g));
   }
-  *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(vals);
+  *reinterpret_cast<uint4*>(out + dst) = *reinterpret_cast<const uint4*>(vals);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
@@ -410,6 +421,23 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t i
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_kblocks(CUtensorMap* map, const void* base, int elem_bytes, uint64_t K, uint64_t rows,
+                       uint32_t box_rows, uint32_t blocks) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  if (reinterpret_cast<uintptr_t>(base) % 16 || (K * elem_bytes) % 128) return false;
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t inner = 128 / elem_bytes;
+  cuuint64_t dims[3] = {inner, rows, K / inner};
+  cuuint64_t strides[2] = {K * static_cast<cuuint64_t>(elem_bytes), 128};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), box_rows, blocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
   if (M < 1 || M > 256 || N <= 0 || K <= 0 || N % 128 || K % 128) return FM_ERR_SHAPE;
   const int eb = fp8 ? 1 : 2;
@@ -425,13 +453,27 @@ int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
   g->n_pad = (M + 15) / 16 * 16;
   g->nkb_total = nkb_total;
   g->nkb_cta = nkb_total / s;
-  const size_t stage_bytes = kWTileBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;
+  const size_t block_bytes = kWTileBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;   // one K block
   const int rows_per = (M + cs - 1) / cs;
   const size_t recv_bytes = align_up(static_cast<size_t>(cs) * rows_per * kTileN * sizeof(float), 1024);
-  if (recv_bytes + stage_bytes > kStageCap) return FM_ERR_SHAPE;
-  int st = static_cast<int>((kStageCap - recv_bytes) / stage_bytes);
+  if (recv_bytes + block_bytes > kStageCap) return FM_ERR_SHAPE;
+  // chunk: the largest divisor of nkb_cta up to 4 whose double-buffered ring fits (or a
+  // single stage holding all of the CTA's K blocks)
+  const size_t room = kStageCap - recv_bytes;
+  int chunk = 1;
+  for (int c = std::min(4, g->nkb_cta); c >= 1; --c) {
+    if (g->nkb_cta % c) continue;
+    const int need = std::min(2, g->nkb_cta / c);
+    if (static_cast<size_t>(need) * c * block_bytes <= room) {
+      chunk = c;
+      break;
+    }
+  }
+  g->chunk = chunk;
+  const size_t stage_bytes = static_cast<size_t>(chunk) * block_bytes;
+  int st = static_cast<int>(room / stage_bytes);
   st = std::min(st, kMaxStages);
-  st = std::min(st, g->nkb_cta);
+  st = std::min(st, g->nkb_cta / chunk);
   g->stages = std::max(st, 1);
   const size_t main_bytes = g->stages * stage_bytes;
   g->smem = 1024 + align_up(main_bytes, 1024) + recv_bytes + kCtrlBytes;
@@ -439,15 +481,8 @@ int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
 }
 
 bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g) {
-  const int eb = g.fp8 ? 1 : 2;
-  return make_tmap_2d(map, a, eb, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), kBlockBytes / eb,
-                      static_cast<uint32_t>(g.n_pad));
-}
-
-bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g) {
-  const int eb = g.fp8 ? 1 : 2;
-  const uint64_t rows = static_cast<uint64_t>(g.N / kTileN) * g.nkb_total * kTileN;
-  return make_tmap_2d(map, packed, eb, kBlockBytes / eb, rows, kBlockBytes / eb, kTileN);
+  return make_tmap_kblocks(map, a, g.fp8 ? 1 : 2, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M),
+                           static_cast<uint32_t>(g.n_pad), static_cast<uint32_t>(g.chunk));
 }
 
 cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted) {
@@ -478,12 +513,13 @@ cudaError_t gemm_configure() {
   return cudaSuccess;
 }
 
-cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
+cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw,
                         void* out_geglu, int geglu_fp8, const float* sq) {
   if ((out_bf16 || out_geglu) && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
   if (out_geglu && (!sq || g.N % 128)) return cudaErrorInvalidValue;
   KParams p;
+  p.wpk = static_cast<const uint8_t*>(wpk);
   p.out = out;
   p.out_bf16 = out_bf16;
   p.out_geglu = out_geglu;
@@ -498,20 +534,21 @@ cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const Ge
   p.n_pad = g.n_pad;
   p.stages = g.stages;
   p.cs = g.cs;
+  p.chunk = g.chunk;
   p.err = err;
   LaunchOpts lo = o;
   lo.cluster = dim3(1, static_cast<unsigned>(g.cs), 1);
   const dim3 grid(static_cast<unsigned>(g.N / kTileN), static_cast<unsigned>(g.s), 1);
   const dim3 blk(kThreads);
   switch (g.cs * 2 + (g.fp8 ? 1 : 0)) {
-    case 3: return launch(skinny_gemm_kernel<true, 1>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 5: return launch(skinny_gemm_kernel<true, 2>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 9: return launch(skinny_gemm_kernel<true, 4>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 17: return launch(skinny_gemm_kernel<true, 8>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 2: return launch(skinny_gemm_kernel<false, 1>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 4: return launch(skinny_gemm_kernel<false, 2>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 8: return launch(skinny_gemm_kernel<false, 4>, grid, blk, g.smem, lo, tmW, tmA, p);
-    case 16: return launch(skinny_gemm_kernel<false, 8>, grid, blk, g.smem, lo, tmW, tmA, p);
+    case 3: return launch(skinny_gemm_kernel<true, 1>, grid, blk, g.smem, lo, tmA, p);
+    case 5: return launch(skinny_gemm_kernel<true, 2>, grid, blk, g.smem, lo, tmA, p);
+    case 9: return launch(skinny_gemm_kernel<true, 4>, grid, blk, g.smem, lo, tmA, p);
+    case 17: return launch(skinny_gemm_kernel<true, 8>, grid, blk, g.smem, lo, tmA, p);
+    case 2: return launch(skinny_gemm_kernel<false, 1>, grid, blk, g.smem, lo, tmA, p);
+    case 4: return launch(skinny_gemm_kernel<false, 2>, grid, blk, g.smem, lo, tmA, p);
+    case 8: return launch(skinny_gemm_kernel<false, 4>, grid, blk, g.smem, lo, tmA, p);
+    case 16: return launch(skinny_gemm_kernel<false, 8>, grid, blk, g.smem, lo, tmA, p);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -10,11 +10,13 @@
 // fp32 accumulation: the only rounding is the fp32 accumulation itself, and ts
 // joins the activation scale in the consumer's dequantisation fp32(s_a * ts).
 //
-// Work split (one CTA per 128 weight rows x one K slice, 8 warps):
-//   thread 0    - producer: bulk copies of the packed weight blocks (4.5 KB per
-//                 64 K elements: codes + block scales) into an 8-deep raw ring,
-//                 issued before the programmatic-dependent-launch wait, and TMA
-//                 loads of the f16 activation tiles after it;
+// Work split (one CTA per 128 weight rows x one K slice, 8 warps). A pipeline stage
+// covers `chunk` 64-element K blocks (one transaction each way: TMA transactions
+// and barrier round trips, not bytes, bound the per-SM streaming rate here):
+//   thread 0    - producer: one bulk copy of the stage's packed weight blocks
+//                 (4.5 KB per block: codes + block scales) into a raw ring, issued
+//                 before the programmatic-dependent-launch wait, and one 3-D TMA
+//                 box of the stage's f16 activation K blocks after it;
 //   thread 32   - MMA issuer: 4 x (M=128, N=M_pad, K=16) per 64-element block;
 //   warps 4..7  - decoders: thread r expands weight row r of a block into the
 //                 128-byte-swizzled K-major f16 operand tile;
@@ -39,11 +41,11 @@ constexpr int kTileN = 128;                                   // weight rows per
 constexpr int kKb = 64;                                       // K elements per pipeline block
 constexpr int kCodeBytes = kTileN * kKb / 2;                  // 4096: two E2M1 codes per byte
 constexpr int kRawBytes = kCodeBytes + kTileN * kKb / 16;     // + 512 block scales = 4608
-constexpr int kRawStages = 8;
+constexpr int kMaxRawStages = 8;
 constexpr int kMaxOpStages = 6;
 constexpr int kATileBytes = kTileN * 128;                     // f16 [128][64], one swizzle row per weight row
-constexpr size_t kSmemCap = 200 * 1024;
-constexpr int kNumBars = 2 * kRawStages + 3 * kMaxOpStages + 1;
+constexpr size_t kSmemCap = 222 * 1024;
+constexpr int kNumBars = 2 * kMaxRawStages + 3 * kMaxOpStages + 1;
 
 struct NvParams {
   const uint8_t* wpk;   // packed blocks [N/128][K/64][kRawBytes]
@@ -54,7 +56,7 @@ struct NvParams {
   const float* sq;
   int M, N;
   int nkb_total, nkb_cta;
-  int n_pad, op_stages;
+  int n_pad, op_stages, raw_stages, chunk;
   int* err;
 };
 
@@ -93,15 +95,16 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   __shared__ int s_abort;
   __shared__ int s_raw_issued, s_act_issued;
 
-  const int S = p.op_stages;
-  const uint32_t b_bytes = static_cast<uint32_t>(p.n_pad) * 128;
-  uint8_t* a_tiles = smem;                                          // [S][16 KB] decoded weights
-  uint8_t* b_tiles = smem + static_cast<size_t>(S) * kATileBytes;   // [S][n_pad][128 B] activations
-  uint8_t* raw = b_tiles + static_cast<size_t>(S) * b_bytes;        // [kRawStages][kRawBytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRawBytes);
+  const int S = p.op_stages, R = p.raw_stages, C = p.chunk;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.n_pad) * 128;   // one K block of activations
+  const uint32_t a_stage = C * kATileBytes, b_stage = C * b_bytes, raw_stage = C * kRawBytes;
+  uint8_t* a_tiles = smem;                                     // [S][C][16 KB] decoded weights
+  uint8_t* b_tiles = smem + static_cast<size_t>(S) * a_stage;  // [S][C][n_pad][128 B] activations
+  uint8_t* raw = b_tiles + static_cast<size_t>(S) * b_stage;   // [R][C][kRawBytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + static_cast<size_t>(R) * raw_stage);
   uint64_t* raw_full = bars;
-  uint64_t* raw_empty = raw_full + kRawStages;
-  uint64_t* a_full = raw_empty + kRawStages;
+  uint64_t* raw_empty = raw_full + kMaxRawStages;
+  uint64_t* a_full = raw_empty + kMaxRawStages;
   uint64_t* b_full = a_full + kMaxOpStages;
   uint64_t* op_empty = b_full + kMaxOpStages;
   uint64_t* done = op_empty + kMaxOpStages;
@@ -110,15 +113,15 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int nt = blockIdx.x, j = blockIdx.y;
-  const int nkb = p.nkb_cta;
-  const int kb0 = j * nkb;
+  const int kb0 = j * p.nkb_cta;
+  const int nst = p.nkb_cta / C;   // stages to run
   const uint32_t ncols = pow2_at_least(static_cast<uint32_t>(p.n_pad), 32);
 
   if (tid == 0) {
     s_abort = 0;
     s_raw_issued = 0;
     s_act_issued = 0;
-    for (int i = 0; i < kRawStages; ++i) {
+    for (int i = 0; i < kMaxRawStages; ++i) {
       mbar_init(&raw_full[i], 1);
       mbar_init(&raw_empty[i], 4);   // one arrival per decoder warp
     }
@@ -150,33 +153,35 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_a = l2_policy_evict_last();
     const uint8_t* wsrc = p.wpk + (static_cast<size_t>(nt) * p.nkb_total + kb0) * kRawBytes;
-    const int pre = min(kRawStages, nkb);
+    const int pre = min(R, nst);
     for (int i = 0; i < pre; ++i) {
-      mbar_arrive_expect_tx(&raw_full[i], kRawBytes);
-      bulk_load(raw + i * kRawBytes, wsrc + static_cast<size_t>(i) * kRawBytes, kRawBytes, &raw_full[i], pol_w);
+      mbar_arrive_expect_tx(&raw_full[i], raw_stage);
+      bulk_load(raw + static_cast<size_t>(i) * raw_stage, wsrc + static_cast<size_t>(i) * raw_stage, raw_stage,
+                &raw_full[i], pol_w);
     }
     int raw_issued = pre, act_issued = 0;
     pdl_wait();   // the activations are written by the previous kernel
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int slot = kb % S;
-      if (kb >= S && !mbar_wait(&op_empty[slot], static_cast<uint32_t>((kb / S) - 1) & 1u)) {
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % S;
+      if (st >= S && !mbar_wait(&op_empty[slot], static_cast<uint32_t>((st / S) - 1) & 1u)) {
         atomicOr(p.err, kErrPipelineTimeout);
         s_abort = 1;
         break;
       }
-      mbar_arrive_expect_tx(&b_full[slot], b_bytes);
-      tma_load_2d(b_tiles + static_cast<size_t>(slot) * b_bytes, &tmA, &b_full[slot], (kb0 + kb) * kKb, 0, pol_a);
+      mbar_arrive_expect_tx(&b_full[slot], b_stage);
+      tma_load_3d(b_tiles + static_cast<size_t>(slot) * b_stage, &tmA, &b_full[slot], 0, 0, kb0 + st * C, pol_a);
       ++act_issued;
-      const int nk = kb + kRawStages;   // refill the raw slot block kb occupied
-      if (nk < nkb) {
-        const int r = nk % kRawStages;
-        if (!mbar_wait(&raw_empty[r], static_cast<uint32_t>((nk / kRawStages) - 1) & 1u)) {
+      const int ns = st + R;   // refill the raw slot stage st occupied
+      if (ns < nst) {
+        const int r = ns % R;
+        if (!mbar_wait(&raw_empty[r], static_cast<uint32_t>((ns / R) - 1) & 1u)) {
           atomicOr(p.err, kErrPipelineTimeout);
           s_abort = 1;
           break;
         }
-        mbar_arrive_expect_tx(&raw_full[r], kRawBytes);
-        bulk_load(raw + r * kRawBytes, wsrc + static_cast<size_t>(nk) * kRawBytes, kRawBytes, &raw_full[r], pol_w);
+        mbar_arrive_expect_tx(&raw_full[r], raw_stage);
+        bulk_load(raw + static_cast<size_t>(r) * raw_stage, wsrc + static_cast<size_t>(ns) * raw_stage, raw_stage,
+                  &raw_full[r], pol_w);
         ++raw_issued;
       }
     }
@@ -185,52 +190,60 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   } else if (tid == 32) {
     // ---------------- MMA issuer
     const uint32_t idesc = make_idesc_f16(kTileN, static_cast<uint32_t>(p.n_pad));
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int slot = kb % S;
-      const uint32_t par = static_cast<uint32_t>(kb / S) & 1u;
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % S;
+      const uint32_t par = static_cast<uint32_t>(st / S) & 1u;
       if (!mbar_wait(&a_full[slot], par) || !mbar_wait(&b_full[slot], par)) {
         atomicOr(p.err, kErrPipelineTimeout);
         s_abort = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t aa = smem_u32(a_tiles + static_cast<size_t>(slot) * kATileBytes);
-      const uint32_t ba = smem_u32(b_tiles + static_cast<size_t>(slot) * b_bytes);
+      for (int c = 0; c < C; ++c) {
+        const uint32_t aa = smem_u32(a_tiles + static_cast<size_t>(slot) * a_stage + c * kATileBytes);
+        const uint32_t ba = smem_u32(b_tiles + static_cast<size_t>(slot) * b_stage + c * b_bytes);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc_mma<false>(tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32), idesc,
-                      (kb > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < 4; ++k)
+          tc_mma<false>(tmem, sw128_kmajor_desc(aa + k * 32), sw128_kmajor_desc(ba + k * 32), idesc,
+                        (st > 0 || c > 0 || k > 0) ? 1u : 0u);
+      }
       tc_commit(&op_empty[slot]);
     }
     tc_commit(done);
   } else if (warp >= 4) {
     // ---------------- decoders: thread row expands weight row `row` of each block
     const int row = tid - 128;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int r = kb % kRawStages;
-      if (!mbar_wait(&raw_full[r], static_cast<uint32_t>(kb / kRawStages) & 1u)) {
+    for (int st = 0; st < nst; ++st) {
+      const int r = st % R;
+      if (!mbar_wait(&raw_full[r], static_cast<uint32_t>(st / R) & 1u)) {
         atomicOr(p.err, kErrPipelineTimeout);
         s_abort = 1;
         break;
       }
-      const uint8_t* src = raw + r * kRawBytes;
-      const uint4 c0 = *reinterpret_cast<const uint4*>(src + row * 32);
-      const uint4 c1 = *reinterpret_cast<const uint4*>(src + row * 32 + 16);
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(src + kCodeBytes + row * 4);
+      uint32_t codes[2][8], sc[2];
+      for (int c = 0; c < C; ++c) {
+        const uint8_t* src = raw + static_cast<size_t>(r) * raw_stage + c * kRawBytes;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(src + row * 32);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(src + row * 32 + 16);
+        codes[c][0] = c0.x; codes[c][1] = c0.y; codes[c][2] = c0.z; codes[c][3] = c0.w;
+        codes[c][4] = c1.x; codes[c][5] = c1.y; codes[c][6] = c1.z; codes[c][7] = c1.w;
+        sc[c] = *reinterpret_cast<const uint32_t*>(src + kCodeBytes + row * 4);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&raw_empty[r]);
-      const int slot = kb % S;
-      if (kb >= S && !mbar_wait(&op_empty[slot], static_cast<uint32_t>((kb / S) - 1) & 1u)) {
+      const int slot = st % S;
+      if (st >= S && !mbar_wait(&op_empty[slot], static_cast<uint32_t>((st / S) - 1) & 1u)) {
         atomicOr(p.err, kErrPipelineTimeout);
         s_abort = 1;
         break;
       }
-      const uint32_t dst = smem_u32(a_tiles + static_cast<size_t>(slot) * kATileBytes) + row * 128;
-      const uint32_t codes[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      for (int c = 0; c < C; ++c) {
+        const uint32_t dst = smem_u32(a_tiles + static_cast<size_t>(slot) * a_stage + c * kATileBytes) + row * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {   // chunk c = elements 8c..8c+7, block scale c / 2
-        const __half bs = e4m3_half(static_cast<uint8_t>((sc >> (8 * (c >> 1))) & 0xffu));
-        st_shared_v4(dst + ((c ^ (row & 7)) << 4), decode8(codes[c], __half2(bs, bs)));
+        for (int q = 0; q < 8; ++q) {   // 16-byte chunk q = elements 8q..8q+7, block scale q / 2
+          const __half bs = e4m3_half(static_cast<uint8_t>((sc[c] >> (8 * (q >> 1))) & 0xffu));
+          st_shared_v4(dst + ((q ^ (row & 7)) << 4), decode8(codes[c][q], __half2(bs, bs)));
+        }
       }
       fence_async_smem();   // generic-proxy writes -> tensor-core reads
       __syncwarp();
@@ -281,8 +294,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   // On an abandoned pipeline, let copies already in flight land before the CTA exits.
   if (abort && tid == 0) {
     const int ri = s_raw_issued, ai = s_act_issued;
-    for (int r = 0; r < kRawStages && r < ri; ++r)
-      mbar_wait(&raw_full[r], static_cast<uint32_t>((ri - 1 - r) / kRawStages) & 1u, 100000000ull);
+    for (int r = 0; r < R && r < ri; ++r)
+      mbar_wait(&raw_full[r], static_cast<uint32_t>((ri - 1 - r) / R) & 1u, 100000000ull);
     for (int slot = 0; slot < S && slot < ai; ++slot)
       mbar_wait(&b_full[slot], static_cast<uint32_t>((ai - 1 - slot) / S) & 1u, 100000000ull);
   }
@@ -373,18 +386,30 @@ int nvfp4_plan(int M, int N, int K, int s, Nvfp4Shape* g) {
   g->n_pad = (M + 15) / 16 * 16;
   g->nkb_total = nkb_total;
   g->nkb_cta = nkb_total / s;
-  const size_t stage = kATileBytes + static_cast<size_t>(g->n_pad) * 128;
-  const size_t fixed = static_cast<size_t>(kRawStages) * kRawBytes + align_up(kNumBars * 8 + 8, 256);
-  const int st = static_cast<int>(std::min<size_t>(kMaxOpStages, (kSmemCap - fixed) / stage));
-  if (st < 2) return FM_ERR_SHAPE;
-  g->op_stages = st;
-  g->smem = 1024 + st * stage + fixed;
-  return FM_OK;
+  const size_t ctrl = align_up(kNumBars * 8 + 8, 256);
+  // one K block per stage with the deepest operand ring that fits; two per stage
+  // only if one would not leave room for two stages
+  for (int chunk = 1; chunk <= 2; ++chunk) {
+    if (g->nkb_cta % chunk) continue;
+    const size_t stage = static_cast<size_t>(chunk) * (kATileBytes + static_cast<size_t>(g->n_pad) * 128);
+    const size_t raw_stage = static_cast<size_t>(chunk) * kRawBytes;
+    for (int raw = kMaxRawStages; raw >= 3; --raw) {
+      const size_t fixed = raw * raw_stage + ctrl;
+      if (fixed + 2 * stage > kSmemCap) continue;
+      const int st = static_cast<int>(std::min<size_t>(kMaxOpStages, (kSmemCap - fixed) / stage));
+      g->chunk = chunk;
+      g->raw_stages = raw;
+      g->op_stages = st;
+      g->smem = 1024 + st * stage + fixed;
+      return FM_OK;
+    }
+  }
+  return FM_ERR_SHAPE;
 }
 
 bool nvfp4_tmap_act(CUtensorMap* map, const void* a, const Nvfp4Shape& g) {
-  return make_tmap_2d(map, a, 2, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), kKb,
-                      static_cast<uint32_t>(g.n_pad));
+  return make_tmap_kblocks(map, a, 2, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M),
+                           static_cast<uint32_t>(g.n_pad), static_cast<uint32_t>(g.chunk));
 }
 
 cudaError_t nvfp4_configure() { return allow_max_dynamic_smem(reinterpret_cast<const void*>(nvfp4_gemm_kernel)); }
@@ -407,6 +432,8 @@ cudaError_t nvfp4_gemm_launch(const CUtensorMap& tmA, const void* wpk, const Nvf
   p.nkb_cta = g.nkb_cta;
   p.n_pad = g.n_pad;
   p.op_stages = g.op_stages;
+  p.raw_stages = g.raw_stages;
+  p.chunk = g.chunk;
   p.err = err;
   LaunchOpts lo = o;
   lo.cluster = dim3(1, 1, 1);

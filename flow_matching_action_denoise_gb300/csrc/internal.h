@@ -59,6 +59,11 @@ cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted = nullptr
 // 128-byte swizzle, zero fill out of bounds. Returns false on failure.
 bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t inner, uint64_t outer,
                   uint32_t box_inner, uint32_t box_outer);
+// 3-D view of a row-major [rows][K] array as (128-byte K block inner, rows, K blocks):
+// one box brings `blocks` consecutive K blocks of box_rows rows, laid out in shared
+// memory as [blocks][box_rows][128 B] with the 128-byte swizzle.
+bool make_tmap_kblocks(CUtensorMap* map, const void* base, int elem_bytes, uint64_t K, uint64_t rows,
+                       uint32_t box_rows, uint32_t blocks);
 
 // ---------------------------------------------------------------- skinny GEMM
 struct GemmShape {
@@ -69,21 +74,21 @@ struct GemmShape {
   int n_pad;      // MMA N (M rounded up to 16)
   int nkb_total;  // 128-byte K blocks
   int nkb_cta;    // K blocks per CTA
+  int chunk;      // K blocks per pipeline stage (one weight copy + one activation box)
   int stages;     // pipeline stages in shared memory
   size_t smem;    // dynamic shared memory bytes
 };
 // Fills the derived fields; returns FM_OK or FM_ERR_SHAPE.
 int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g);
-// Activation tensor map: A [M][K], box = 128 bytes x n_pad rows.
+// Activation tensor map: A [M][K] in K blocks of 128 bytes, box = chunk blocks x n_pad rows.
 bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
-// Weight tensor map over the packed tiles of a [N][K] weight.
-bool gemm_tmap_weight(CUtensorMap* map, const void* packed, const GemmShape& g);
 // out: fp32 partial planes [s/cs][M][N]; or, with out_bf16 (requires cs == s), the
 // dequantised product bf16(sum * fp32(*sa * *sw)) as [M][N].
 // out_geglu (requires cs == s and a gate|up weight packed with interleave): the
 // epilogue applies m = gelu_tanh(g) * u to the dequantised sums and writes Q(m, *sq)
 // as [M][N/2] codes (E4M3 bytes if geglu_fp8, else bf16).
-cudaError_t gemm_launch(const CUtensorMap& tmW, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
+// wpk: packed weight tiles (1024-byte aligned, fm_pack_weight layout).
+cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16 = nullptr, const float* sa = nullptr,
                         const float* sw = nullptr, void* out_geglu = nullptr, int geglu_fp8 = 0,
                         const float* sq = nullptr);
@@ -97,6 +102,8 @@ struct Nvfp4Shape {
   int nkb_total;   // 64-element K blocks
   int nkb_cta;
   int op_stages;   // decoded-operand pipeline stages
+  int raw_stages;  // packed-weight ring stages
+  int chunk;       // K blocks per stage
   size_t smem;
 };
 int nvfp4_plan(int M, int N, int K, int s, Nvfp4Shape* g);

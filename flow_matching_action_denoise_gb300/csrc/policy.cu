@@ -265,7 +265,6 @@ struct fm_policy {
   Layout ly;
   uint8_t* ws = nullptr;
   size_t ws_bytes = 0;
-  std::vector<CUtensorMap> tmW;   // [L*4]
   CUtensorMap tmA[4];
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
@@ -363,7 +362,7 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
     e = fm::qkv_finalize_launch(y[0], dv.ns[0].s, c.M, dv.gN[0], p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), qkvb,
                                 o);
   } else {
-    e = fm::gemm_launch(p->tmW[l * 4 + 0], p->tmA[0], dv.gs[0], nullptr, err, o, qkvb, p->ascale(l, FM_SITE_ATTN_IN),
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, qkvb, p->ascale(l, FM_SITE_ATTN_IN),
                         p->wscale(l, 0));
   }
   if (e != cudaSuccess) return e;
@@ -391,7 +390,7 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
 
   e = dv.nvfp4 ? fm::nvfp4_gemm_launch(p->tmA[1], p->at<void>(p->ly.wpk[l * 4 + 1]), dv.ns[1], y[1], nullptr, nullptr,
                                        nullptr, nullptr, err, o)
-               : fm::gemm_launch(p->tmW[l * 4 + 1], p->tmA[1], dv.gs[1], y[1], err, o);
+               : fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 1]), p->tmA[1], dv.gs[1], y[1], err, o);
   if (e != cudaSuccess) return e;
   FM_REC(y[1], ybytes[1]);
 
@@ -421,14 +420,14 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
     e = fm::nvfp4_gemm_launch(p->tmA[2], p->at<void>(p->ly.wpk[l * 4 + 2]), dv.ns[2], nullptr, p->at<__half>(p->ly.mc),
                               p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->ascale(l, FM_SITE_GEGLU), err, o);
   else
-    e = fm::gemm_launch(p->tmW[l * 4 + 2], p->tmA[2], dv.gs[2], nullptr, err, o, nullptr, p->ascale(l, FM_SITE_MLP_IN),
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 2]), p->tmA[2], dv.gs[2], nullptr, err, o, nullptr, p->ascale(l, FM_SITE_MLP_IN),
                         p->wscale(l, 2), p->at<void>(p->ly.mc), fp8, p->ascale(l, FM_SITE_GEGLU));
   if (e != cudaSuccess) return e;
   FM_REC(p->at<void>(p->ly.mc), static_cast<size_t>(c.M) * c.F * ab);
 
   e = dv.nvfp4 ? fm::nvfp4_gemm_launch(p->tmA[3], p->at<void>(p->ly.wpk[l * 4 + 3]), dv.ns[3], y[3], nullptr, nullptr,
                                        nullptr, nullptr, err, o)
-               : fm::gemm_launch(p->tmW[l * 4 + 3], p->tmA[3], dv.gs[3], y[3], err, o);
+               : fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 3]), p->tmA[3], dv.gs[3], y[3], err, o);
   if (e != cudaSuccess) return e;
   FM_REC(y[3], ybytes[3]);
 
@@ -622,8 +621,8 @@ int gemm_consumer_run(const GemmConsumerArgs& a, float* scratch, size_t scratch_
   }
   GemmShape g;
   gemm_plan(a.M, a.N, a.K, a.fmt == FM_FMT_FP8, a.s, cluster_for(a.s), &g);
-  CUtensorMap tw, ta;
-  if (!gemm_tmap_weight(&tw, a.w_packed, g) || !gemm_tmap_act(&ta, a.a, g)) {
+  CUtensorMap ta;
+  if (!gemm_tmap_act(&ta, a.a, g)) {
     *why = "cuTensorMapEncodeTiled failed";
     return FM_ERR_CUDA;
   }
@@ -633,7 +632,7 @@ int gemm_consumer_run(const GemmConsumerArgs& a, float* scratch, size_t scratch_
   }
   LaunchOpts o;
   o.stream = st;
-  if (gemm_launch(tw, ta, g, scratch, err_word, o) != cudaSuccess) {
+  if (gemm_launch(a.w_packed, ta, g, scratch, err_word, o) != cudaSuccess) {
     *why = "GEMM launch failed";
     return FM_ERR_CUDA;
   }
@@ -800,12 +799,7 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
     for (int g = 0; g < 4; ++g)
       if (!fm::nvfp4_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.ns[g]))
         return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
-  } else {
-    p->tmW.resize(static_cast<size_t>(c.L) * 4);
-    for (int l = 0; l < c.L; ++l)
-      for (int g = 0; g < 4; ++g)
-        if (!fm::gemm_tmap_weight(&p->tmW[l * 4 + g], p->at<void>(p->ly.wpk[l * 4 + g]), dv.gs[g]))
-          return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed");
+  } else {   // packed weights are fetched with plain bulk copies
     for (int g = 0; g < 4; ++g)
       if (!fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.gs[g]))
         return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
@@ -1118,8 +1112,8 @@ int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N
   fm::GemmShape g;
   const int st = fm::gemm_plan(M, N, K, fmt == FM_FMT_FP8, s, cluster_reduce, &g);
   if (st != FM_OK) return fail(nullptr, st, "GEMM shape/split precondition violated");
-  CUtensorMap tw, ta;
-  if (!fm::gemm_tmap_weight(&tw, w_packed, g) || !fm::gemm_tmap_act(&ta, a, g))
+  CUtensorMap ta;
+  if (!fm::gemm_tmap_act(&ta, a, g))
     return fail(nullptr, FM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   cudaError_t e = fm::gemm_configure();
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "gemm_configure");
@@ -1128,7 +1122,7 @@ int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
   LaunchOpts o;
   o.stream = static_cast<cudaStream_t>(stream);
-  e = fm::gemm_launch(tw, ta, g, partials, err_word, o);
+  e = fm::gemm_launch(w_packed, ta, g, partials, err_word, o);
   return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "skinny_gemm launch");
 }
 

@@ -278,8 +278,10 @@ int fm_packed_weight_bytes(int N, int K, int fmt, size_t* bytes);
  * n-tile-major then k-block, each [128 rows][32 bytes] of codes (element 2i in
  * the low nibble) followed by [128 rows][4] block-scale codes.
  * FP8 tile layout: tile (n/128, k/128) is 128 rows x 128 bytes, rows n, bytes k,
- * tiles ordered n-tile-major then k-block; each tile is stored as TMA writes it
- * with 128-byte swizzle undone, i.e. plain [128][128] bytes (BF16: [128][64]). */
+ * tiles ordered n-tile-major then k-block; each tile is [128 rows][128 bytes]
+ * (BF16: [128][64] elements) with the 128-byte swizzle applied: the 16-byte
+ * chunk c of row r is stored at chunk position c ^ (r mod 8), the layout the
+ * tensor cores read, so one bulk copy moves consecutive tiles into place. */
 int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt,
                    void* packed, float* scale_out, void* stream);
 

@@ -32,15 +32,31 @@ def aligned_empty(nbytes, device, align=1024):
     return buf, buf.data_ptr() + off
 
 
+def _chunk_perm(rows):
+    """Chunk index (0..7, 16 bytes each) where row r of a 128-byte-row tile stores its
+    chunk c under the 128-byte swizzle: c ^ (r mod 8)."""
+    r = np.arange(rows)[:, None]
+    c = np.arange(8)[None, :]
+    return r, c, c ^ (r % 8)
+
+
 def tile_codes(codes, elems_per_row_block):
-    """[N][K] -> the packed tile order [N/128][K/e][128][e] (e = 128 fp8 or 64 bf16)."""
+    """[N][K] -> the packed tile order [N/128][K/e][128][e] (e = 128 fp8 or 64 bf16), each
+    128-byte row stored with the 128-byte swizzle (the layout the MMA reads)."""
     n, k = codes.shape
     e = elems_per_row_block
-    return codes.reshape(n // 128, 128, k // e, e).transpose(0, 2, 1, 3).copy()
+    t = codes.reshape(n // 128, 128, k // e, e).transpose(0, 2, 1, 3).reshape(n // 128, k // e, 128, 8, e // 8)
+    r, c, sw = _chunk_perm(128)
+    out = np.empty_like(t)
+    out[:, :, r, sw, :] = t[:, :, r, c, :]
+    return out.reshape(n // 128, k // e, 128, e).copy()
 
 
 def untile_codes(packed, n, k, e):
-    return packed.reshape(n // 128, k // e, 128, e).transpose(0, 2, 1, 3).reshape(n, k)
+    t = np.asarray(packed).reshape(n // 128, k // e, 128, 8, e // 8)
+    r, c, sw = _chunk_perm(128)
+    plain = t[:, :, r, sw, :]   # chunk c of row r lives at position c ^ (r mod 8)
+    return plain.reshape(n // 128, k // e, 128, e).transpose(0, 2, 1, 3).reshape(n, k)
 
 
 def e4m3_values_of_bytes(b):
