@@ -52,6 +52,7 @@ class Config:
     seed: int
     cond: str = "time"   # "time": sinusoidal t-embedding; "given": cond vector drawn per step
     eps: float = 1e-6
+    attn_fmt: str = "bf16"   # "bf16" | "fp8": attention operands (Q, K, V, P)
 
     @property
     def n_qkv(self) -> int:
@@ -73,6 +74,10 @@ CONFIGS = {
     "expert_fp8_m50": Config("expert_fp8_m50", L=18, S=10, M=50, d=1024, H=8, Hkv=1, Dh=128,
                              F=4096, P=788, A=32, weight_fmt="fp8", act_fmt="fp8", seed=1),
     # matched 16-bit variant, M=63
+    # the same expert with FP8 attention (E4M3 Q, K, V and probabilities)
+    "expert_fp8attn_m50": Config("expert_fp8attn_m50", L=18, S=10, M=50, d=1024, H=8, Hkv=1, Dh=128,
+                                 F=4096, P=788, A=32, weight_fmt="fp8", act_fmt="fp8", seed=1,
+                                 attn_fmt="fp8"),
     "expert_bf16_m63": Config("expert_bf16_m63", L=18, S=10, M=63, d=1024, H=8, Hkv=1, Dh=128,
                               F=4096, P=788, A=32, weight_fmt="bf16", act_fmt="bf16", seed=3),
     # world-action-model-sized decoder, NVFP4 weights, FP8 activations
@@ -166,14 +171,16 @@ def layer_input(cfg: Config) -> np.ndarray:
 
 
 def default_act_scales(cfg: Config) -> np.ndarray:
-    """A data-independent static activation-scale table [L][4] (fp32).
+    """A data-independent static activation-scale table [L][4] (fp32; [L][7] with FP8 attention).
 
     Quant points per layer: 0 = pre-attention norm output, 1 = attention output,
     2 = pre-MLP norm output, 3 = GeGLU output. Used where no calibrated table is
     supplied; the values are plain constants sized for the distributions above.
     """
-    base = np.array([24.0, 1.0, 24.0, 16.0], np.float32) / np.float32(448.0)
-    return np.tile(base, (cfg.L, 1)).astype(np.float32)
+    base = [24.0, 1.0, 24.0, 16.0]
+    if cfg.attn_fmt == "fp8":   # FP8 attention adds Q, K, V (columns 4-6 of an [L][7] table)
+        base += [8.0, 8.0, 8.0]
+    return np.tile(np.array(base, np.float32) / np.float32(448.0), (cfg.L, 1)).astype(np.float32)
 
 
 def gemm_case(M: int, K: int, N: int, seed: int = 2, integer: bool = False) -> dict:

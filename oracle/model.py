@@ -27,6 +27,10 @@ Readings where the pages are silent (each also listed in the design notes):
   fp32(s_a * s_w); weight scale amax/448 (1 if the matrix is all zero); noise at
   t = 1, t_k = 1 - k/S, Euler step dt = -1/S; adaptive final norm (no gate)
   with gamma_f, then W_out; attention probabilities rounded to bf16 before P.V.
+  FP8 attention mode: Q, K, V (chunk and prefix) quantised with static per-layer
+  scales (fp32 reciprocal multiply, E4M3 RNE with saturation), scores dequantised
+  by fp32(s_q * s_k), probabilities P in [0, 1] stored as E4M3(P * 448) (static
+  scale 1/448), output dequantised by fp32(s_v / 448).
 """
 from __future__ import annotations
 
@@ -38,8 +42,11 @@ from . import codecs as C
 
 F32 = np.float32
 
-# quant points per layer (index into the [L][4] activation-scale table)
+# quant points per layer (index into the [L][4] activation-scale table; the FP8
+# attention mode adds Q, K and V as columns 4-6 of an [L][7] table)
 SITE_ATTN_IN, SITE_ATTN_OUT, SITE_MLP_IN, SITE_GEGLU = 0, 1, 2, 3
+SITE_Q, SITE_K, SITE_V = 4, 5, 6
+P_CODE_SCALE = 448.0   # E4M3 probabilities: code = E4M3(P * 448), value = code / 448
 
 
 # ---------------------------------------------------------------- primitives
@@ -187,6 +194,25 @@ def attention(q, kc, vc, kpre, vpre, H, Hkv, Dh, round_p=True):
     return out
 
 
+def attention_fp8(qc, kc, vc, kpre_c, vpre_c, H, Hkv, Dh, s_q, s_k, s_v):
+    """FP8 attention over [prefix; chunk] keys. All operands are E4M3 code values
+    (without their static scales): qc [M][H*Dh], kc/vc [M][Hkv*Dh], kpre_c/vpre_c
+    [P][Hkv][Dh]. Scores s = (qc . k^T) * fp32(s_q * s_k) / sqrt(Dh); P = softmax(s);
+    P codes = E4M3(P * 448); O = (P codes . v) * fp32(s_v / 448). Returns O [M][H*Dh]."""
+    M = qc.shape[0]
+    ds = np.float64(F32(s_q) * F32(s_k))
+    dv = np.float64(F32(s_v) / F32(P_CODE_SCALE))
+    out = np.empty((M, H * Dh), np.float64)
+    for h in range(H):
+        g = (h * Hkv) // H
+        keys = np.concatenate([kpre_c[:, g, :], kc[:, g * Dh:(g + 1) * Dh]], axis=0)
+        vals = np.concatenate([vpre_c[:, g, :], vc[:, g * Dh:(g + 1) * Dh]], axis=0)
+        sc = (qc[:, h * Dh:(h + 1) * Dh] @ keys.T) * ds / math.sqrt(Dh)
+        pc = C.e4m3(softmax(sc) * P_CODE_SCALE)
+        out[:, h * Dh:(h + 1) * Dh] = (pc @ vals) * dv
+    return out
+
+
 class Model:
     """Prepared weights and the per-step modulation table of one policy."""
 
@@ -246,10 +272,20 @@ def layer_forward(model: Model, l: int, k: int, x: np.ndarray, q: np.ndarray,
 
     qkv = gemm(q, sa(SITE_ATTN_IN), w["qkv"])
     nq, nk = H * Dh, Hkv * Dh
-    Q = C.bf16(qkv[:, :nq])
-    Kc = C.bf16(qkv[:, nq:nq + nk])
-    Vc = C.bf16(qkv[:, nq + nk:])
-    O = attention(Q, Kc, Vc, kpre[l], vpre[l], H, Hkv, Dh)
+    if getattr(cfg, "attn_fmt", "bf16") == "fp8":
+        if amax is not None:
+            amax[l, SITE_Q] = max(amax[l, SITE_Q], np.max(np.abs(qkv[:, :nq])))
+            amax[l, SITE_K] = max(amax[l, SITE_K], np.max(np.abs(qkv[:, nq:nq + nk])), np.max(np.abs(kpre[l])))
+            amax[l, SITE_V] = max(amax[l, SITE_V], np.max(np.abs(qkv[:, nq + nk:])), np.max(np.abs(vpre[l])))
+        s_q, s_k, s_v = sa(SITE_Q), sa(SITE_K), sa(SITE_V)
+        O = attention_fp8(quant_codes(qkv[:, :nq], s_q, "fp8"), quant_codes(qkv[:, nq:nq + nk], s_k, "fp8"),
+                          quant_codes(qkv[:, nq + nk:], s_v, "fp8"), quant_codes(kpre[l], s_k, "fp8"),
+                          quant_codes(vpre[l], s_v, "fp8"), H, Hkv, Dh, s_q, s_k, s_v)
+    else:
+        Q = C.bf16(qkv[:, :nq])
+        Kc = C.bf16(qkv[:, nq:nq + nk])
+        Vc = C.bf16(qkv[:, nq + nk:])
+        O = attention(Q, Kc, Vc, kpre[l], vpre[l], H, Hkv, Dh)
     if amax is not None:
         amax[l, SITE_ATTN_OUT] = max(amax[l, SITE_ATTN_OUT], np.max(np.abs(O)))
     o = gemm(quant_codes(O, sa(SITE_ATTN_OUT), af), sa(SITE_ATTN_OUT), w["o"])
@@ -305,7 +341,7 @@ def calibrate(model: Model, noise, kpre, vpre, provisional_scales) -> np.ndarray
     provisional table), divided by 448 and rounded to fp32; a point whose amax is 0
     keeps its provisional scale."""
     cfg = model.cfg
-    amax = np.zeros((cfg.L, 4), np.float64)
+    amax = np.zeros(np.shape(provisional_scales), np.float64)
     decode(model, noise, kpre, vpre, provisional_scales, amax)
     out = np.asarray(provisional_scales, np.float32).copy()
     nz = amax > 0

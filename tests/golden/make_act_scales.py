@@ -1,4 +1,5 @@
-"""Write the calibrated static activation-scale tables used by the GPU parity tests.
+"""Write the calibrated static activation-scale tables used by the GPU parity tests
+([L][4]; [L][7] for the FP8-attention workload, columns 4-6 = Q, K, V).
 
 Calls only the CPU oracle (oracle.model.calibrate): one calibration decision
 with noise draw 1000 and the workload's prefix, starting from the data-independent
@@ -17,7 +18,7 @@ import fm_synth  # noqa: E402
 from oracle import model as O  # noqa: E402
 
 
-def main(names=("layer_fp8_m10", "expert_fp8_m50", "wam_nvfp4_m256")):
+def main(names=("layer_fp8_m10", "expert_fp8_m50", "expert_fp8attn_m50", "wam_nvfp4_m256")):
     for name in names:
         cfg = fm_synth.config(name)
         layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
@@ -37,11 +38,11 @@ def main(names=("layer_fp8_m10", "expert_fp8_m50", "wam_nvfp4_m256")):
             how = "oracle calibration decision, noise draw 1000"
         path = os.path.join(HERE, f"act_scales_{name}.txt")
         with open(path, "w") as f:
-            f.write(f"# static activation scales [L][4] for {name}: {how}\n")
+            f.write(f"# static activation scales [L][{sc.shape[1]}] for {name}: {how}\n")
             for row in sc:
                 f.write(" ".join(f"{float(v):.9e}" for v in row) + "\n")
         print(path)
 
 
 if __name__ == "__main__":
-    main(sys.argv[1:] or ("layer_fp8_m10", "expert_fp8_m50", "wam_nvfp4_m256"))
+    main(sys.argv[1:] or ("layer_fp8_m10", "expert_fp8_m50", "expert_fp8attn_m50", "wam_nvfp4_m256"))

@@ -387,3 +387,73 @@ def test_brute_force_scalar_step_matches_oracle():
     ref = O.euler_step(model, 1, a0.astype(np.float64), kp, vp, sc)
     brute = _scalar_step(cfg, layers, fin, 1, a0, kp, vp, sc)
     np.testing.assert_allclose(brute, ref, rtol=1e-9, atol=1e-11)
+
+
+# ---------------------------------------------------------------- FP8 attention mode
+
+def _e4m3_grid_values(rng, shape):
+    grid = C.e4m3_decode_code(np.arange(0, 0x70))   # finite positive codes up to 240 and their signs
+    vals = rng.choice(grid, size=shape)
+    return vals * rng.choice([-1.0, 1.0], size=shape)
+
+
+def test_attention_fp8_brute_force_tiny():
+    """Scalar loops over a tiny case (2 query heads sharing 1 KV head, Dh = 4, 3 prefix
+    keys + 2 chunk keys): scores scaled by fp32(s_q s_k)/sqrt(Dh), exact softmax,
+    probabilities coded E4M3(P * 448), output scaled by fp32(s_v / 448)."""
+    rng = np.random.default_rng(11)
+    H, Hkv, Dh, M, P = 2, 1, 4, 2, 3
+    qc = _e4m3_grid_values(rng, (M, H * Dh)) / 64
+    kc = _e4m3_grid_values(rng, (M, Hkv * Dh)) / 64
+    vc = _e4m3_grid_values(rng, (M, Hkv * Dh)) / 64
+    kp = _e4m3_grid_values(rng, (P, Hkv, Dh)) / 64
+    vp = _e4m3_grid_values(rng, (P, Hkv, Dh)) / 64
+    s_q, s_k, s_v = 0.03, 0.05, 0.07
+    got = O.attention_fp8(qc, kc, vc, kp, vp, H, Hkv, Dh, s_q, s_k, s_v)
+    ds = float(np.float32(s_q) * np.float32(s_k))
+    dv = float(np.float32(s_v) / np.float32(448.0))
+    for m in range(M):
+        for h in range(H):
+            keys = [list(kp[j, 0]) for j in range(P)] + [list(kc[j, 0:Dh]) for j in range(M)]
+            vals = [list(vp[j, 0]) for j in range(P)] + [list(vc[j, 0:Dh]) for j in range(M)]
+            sc = []
+            for kk in keys:
+                acc = 0.0
+                for e in range(Dh):
+                    acc += qc[m, h * Dh + e] * kk[e]
+                sc.append(acc * ds / math.sqrt(Dh))
+            mx = max(sc)
+            ex = [math.exp(x - mx) for x in sc]
+            tot = sum(ex)
+            pcode = [float(C.e4m3(np.array([x / tot * 448.0]))[0]) for x in ex]
+            for e in range(Dh):
+                ref = sum(pcode[j] * vals[j][e] for j in range(len(vals))) * dv
+                assert got[m, h * Dh + e] == pytest.approx(ref, rel=1e-12, abs=1e-15)
+
+
+def test_attention_fp8_single_key_returns_scaled_value():
+    """One key: P = 1 is coded exactly (E4M3(448) = 448), so O = v * 448 * (s_v / 448) =
+    v * s_v exactly when s_v / 448 is a power of two (s_v = 1.75: 1.75 / 448 = 2^-8)."""
+    rng = np.random.default_rng(12)
+    Dh = 8
+    qc = _e4m3_grid_values(rng, (1, Dh))
+    kc = _e4m3_grid_values(rng, (1, Dh))
+    vc = _e4m3_grid_values(rng, (1, Dh))
+    empty = np.zeros((0, 1, Dh))
+    out = O.attention_fp8(qc, kc, vc, empty, empty, 1, 1, Dh, 0.5, 0.25, 1.75)
+    np.testing.assert_array_equal(out, vc * 1.75)
+
+
+def test_attention_fp8_uniform_scores():
+    """Equal keys: P = 1/7 for 7 keys, coded E4M3(448 / 7) = 64 exactly, so
+    O = 64 * sum(v) * (1.75 / 448) = sum(v) / 4."""
+    rng = np.random.default_rng(13)
+    Dh = 8
+    k = _e4m3_grid_values(rng, (Dh,))
+    kp = np.tile(k, (6, 1))[:, None, :]
+    kc = k[None, :]
+    vp = _e4m3_grid_values(rng, (6, 1, Dh))
+    vc = _e4m3_grid_values(rng, (1, Dh))
+    qc = _e4m3_grid_values(rng, (1, Dh))
+    out = O.attention_fp8(qc, kc, vc, kp, vp, 1, 1, Dh, 0.125, 0.5, 1.75)
+    np.testing.assert_array_equal(out[0], (vp[:, 0, :].sum(axis=0) + vc[0]) / 4)
