@@ -26,7 +26,7 @@ __all__ = [
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfmad.so")
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
 FLAG_USE_GRAPH, FLAG_USE_PDL = 1, 2
 COND_TIME, COND_GIVEN = 0, 1
@@ -54,7 +54,8 @@ class FmConfig(ctypes.Structure):
                 ("L", ctypes.c_int), ("S", ctypes.c_int), ("M", ctypes.c_int), ("d", ctypes.c_int),
                 ("H", ctypes.c_int), ("Hkv", ctypes.c_int), ("Dh", ctypes.c_int), ("F", ctypes.c_int),
                 ("P", ctypes.c_int), ("A", ctypes.c_int),
-                ("weight_fmt", ctypes.c_int), ("act_fmt", ctypes.c_int), ("cond_mode", ctypes.c_int),
+                ("weight_fmt", ctypes.c_int), ("act_fmt", ctypes.c_int), ("attn_fmt", ctypes.c_int),
+                ("cond_mode", ctypes.c_int),
                 ("rms_eps", ctypes.c_float), ("ksplit", ctypes.c_int * 4), ("flags", ctypes.c_uint)]
 
 
@@ -160,6 +161,7 @@ def make_config(cfg, flags: int = FLAG_USE_GRAPH | FLAG_USE_PDL, ksplit=(0, 0, 0
         setattr(c, k, int(getattr(cfg, k)))
     c.weight_fmt = fmts[cfg.weight_fmt]
     c.act_fmt = fmts[cfg.act_fmt]
+    c.attn_fmt = fmts[getattr(cfg, "attn_fmt", "bf16")]
     c.cond_mode = COND_GIVEN if cfg.cond == "given" else COND_TIME
     c.rms_eps = float(cfg.eps)
     for i, s in enumerate(ksplit):

@@ -27,6 +27,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -44,6 +46,11 @@ static_assert(kThreads == 2 * kDh, "two threads per head-dim row of V^T");
 
 struct KParams {
   const __nv_bfloat16* qkv;    // [M][ldq]
+  const uint8_t* qkv8;         // FP8 attention: E4M3 codes [M][ldq]
+  const uint8_t* kpre8;        // FP8 attention: [P][Hkv][Dh] codes of this layer
+  const uint8_t* vtpre8;       // FP8 attention: [Hkv][Dh][p16] codes (transposed)
+  int p16;
+  const float* s_qkv;          // FP8 attention: static scales of Q, K, V
   int ldq;
   const __nv_bfloat16* kpre;   // [P][Hkv][Dh] of this layer
   const __nv_bfloat16* vtpre;  // [Hkv][Dh][p_pad] of this layer (transposed)
@@ -93,13 +100,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 struct SmemPlan {
   size_t q, k, vt, pm, recv, stats, part, bar, total;
 };
-__host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit) {
+// Operand tiles: Q [128 rows][Dh] (bf16: two 128-byte blocks, E4M3: one); K [kc keys][Dh]
+// likewise; V^T and P in blocks of [128][128 bytes] along the keys (bf16: kc/64 blocks of
+// 64 keys; E4M3: the keys padded to a multiple of 128, one block per 128 keys).
+__host__ __device__ inline int kblocks(int kc, bool fp8) { return fp8 ? (kc + 127) / 128 : kc / 64; }
+__host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8) {
   SmemPlan s;
+  const size_t eb = fp8 ? 1 : 2;
   s.q = 0;
-  s.k = 2 * static_cast<size_t>(kTile);
-  s.vt = s.k + static_cast<size_t>(kc) * 256;
-  s.pm = s.vt + static_cast<size_t>(kc / 64) * kTile;
-  const size_t main_end = s.pm + static_cast<size_t>(kc / 64) * kTile;
+  s.k = eb * static_cast<size_t>(kTile);
+  s.vt = s.k + static_cast<size_t>(kc) * 128 * eb;
+  s.pm = s.vt + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
+  const size_t main_end = s.pm + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
   const int rows_per = (kRows + nsplit - 1) / nsplit;
   const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * kDh * 4;
   // the O receive buffer reuses Q and K (dead once every CTA passed the statistics
@@ -113,13 +125,15 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit) {
   return s;
 }
 
-template <int KC>
+template <int KC, bool kF8>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
-  constexpr int kHalf = KC / 2;   // keys of the slice handled by one thread of a row
-  constexpr int kBlk = KC / 64;   // 64-key blocks of the slice
+  constexpr int kHalf = KC / 2;                 // keys of the slice handled by one thread of a row
+  constexpr int kBlk = kF8 ? (KC + 127) / 128 : KC / 64;   // key blocks of the P V contraction
+  constexpr int kKcp = kF8 ? kBlk * 128 : KC;   // keys of the P V contraction (E4M3: zero padded)
+  constexpr int kRowChunks = kF8 ? 8 : 16;      // 16-byte chunks of one Dh-wide row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemPlan sp = smem_plan(KC, p.nsplit);
+  const SmemPlan sp = smem_plan(KC, p.nsplit, kF8);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + sp.bar);   // S done, O done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
   float2* sStats = reinterpret_cast<float2*>(smem + sp.stats);  // [rank][row] (slice max, slice sum)
@@ -161,19 +175,34 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const uint32_t sQa = base + sp.q, sKa = base + sp.k, sVta = base + sp.vt, sPa = base + sp.pm;
 
   // ---- prefix keys and transposed values of this slice (written before this graph ran)
-  for (int idx = tid; idx < KC * 16; idx += kThreads) {
-    const int i = idx >> 4, c16 = idx & 15;   // key row, 16-byte chunk of its 256 bytes
+  for (int idx = tid; idx < KC * kRowChunks; idx += kThreads) {
+    const int i = idx / kRowChunks, c16 = idx % kRowChunks;   // key row, 16-byte chunk of it
     const int t = t0 + i;
     const uint32_t dst = sKa + (c16 >> 3) * (KC * 128) + swz(i, c16 & 7);
-    if (t < p.P)
-      cp_async16(dst, p.kpre + (static_cast<size_t>(t) * p.Hkv + g) * kDh + c16 * 8);
-    else if (t >= nkeys)
+    if (t < p.P) {
+      if constexpr (kF8)
+        cp_async16(dst, p.kpre8 + (static_cast<size_t>(t) * p.Hkv + g) * kDh + c16 * 16);
+      else
+        cp_async16(dst, p.kpre + (static_cast<size_t>(t) * p.Hkv + g) * kDh + c16 * 8);
+    } else if (t >= nkeys) {
       st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+    }
   }
   // V^T rows: two threads per head-dim row d copy 8 keys (16 bytes) at a time. The
   // cache row is padded with zeros from P to P_pad, so a group straddling the end of
   // the prefix is copied whole; its keys >= P are overwritten with the chunk's values.
-  {
+  if constexpr (kF8) {   // E4M3: 16 keys per 16-byte group; the padding keys [KC, kKcp) are zero
+    const int d = tid & (kDh - 1);
+    const uint8_t* vrow = p.vtpre8 + (static_cast<size_t>(g) * kDh + d) * p.p16;
+    for (int grp = tid >> 7; grp < kKcp / 16; grp += 2) {
+      const int t = t0 + grp * 16;
+      const uint32_t dst = sVta + (grp >> 3) * kTile + swz(d, grp & 7);
+      if (grp * 16 < KC && t < p.P)
+        cp_async16(dst, vrow + t);
+      else
+        st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+    }
+  } else {
     const int d = tid & (kDh - 1);
     const __nv_bfloat16* vrow = p.vtpre + (static_cast<size_t>(g) * kDh + d) * p.p_pad;
     for (int grp = tid >> 7; grp < KC / 8; grp += 2) {
@@ -189,37 +218,57 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   pdl_wait();   // Q, K, V of the chunk are written by the QKV GEMM
 
   // ---- stacked query rows and the chunk's own keys (rows P..P+M-1 of the key axis)
-  for (int idx = tid; idx < kRows * 16; idx += kThreads) {
-    const int r = idx >> 4, c16 = idx & 15;
+  for (int idx = tid; idx < kRows * kRowChunks; idx += kThreads) {
+    const int r = idx / kRowChunks, c16 = idx % kRowChunks;
     const int R = qt * kRows + r;
     const uint32_t dst = sQa + (c16 >> 3) * kTile + swz(r, c16 & 7);
     if (R < p.G * p.M) {
       const int hl = R / p.M, m = R % p.M;
-      cp_async16(dst, p.qkv + static_cast<size_t>(m) * p.ldq + (g * p.G + hl) * kDh + c16 * 8);
+      if constexpr (kF8)
+        cp_async16(dst, p.qkv8 + static_cast<size_t>(m) * p.ldq + (g * p.G + hl) * kDh + c16 * 16);
+      else
+        cp_async16(dst, p.qkv + static_cast<size_t>(m) * p.ldq + (g * p.G + hl) * kDh + c16 * 8);
     } else {
       st_shared_v4(dst, make_uint4(0, 0, 0, 0));
     }
   }
   const int c_lo = max(t0, p.P), c_hi = min(t0 + KC, nkeys);
   const int nchunk = c_hi > c_lo ? c_hi - c_lo : 0;   // <= KC
-  for (int idx = tid; idx < nchunk * 16; idx += kThreads) {
-    const int t = c_lo + (idx >> 4), c16 = idx & 15;
-    const __nv_bfloat16* row = p.qkv + static_cast<size_t>(t - p.P) * p.ldq;
-    cp_async16(sKa + (c16 >> 3) * (KC * 128) + swz(t - t0, c16 & 7), row + (p.H + g) * kDh + c16 * 8);
+  for (int idx = tid; idx < nchunk * kRowChunks; idx += kThreads) {
+    const int t = c_lo + idx / kRowChunks, c16 = idx % kRowChunks;
     // the chunk's values are staged row-major in the P tiles, transposed below
-    cp_async16(sPa + static_cast<uint32_t>(((t - c_lo) * kDh + c16 * 8) * 2), row + (p.H + p.Hkv + g) * kDh + c16 * 8);
+    if constexpr (kF8) {
+      const uint8_t* row = p.qkv8 + static_cast<size_t>(t - p.P) * p.ldq;
+      cp_async16(sKa + swz(t - t0, c16), row + (p.H + g) * kDh + c16 * 16);
+      cp_async16(sPa + static_cast<uint32_t>((t - c_lo) * kDh + c16 * 16), row + (p.H + p.Hkv + g) * kDh + c16 * 16);
+    } else {
+      const __nv_bfloat16* row = p.qkv + static_cast<size_t>(t - p.P) * p.ldq;
+      cp_async16(sKa + (c16 >> 3) * (KC * 128) + swz(t - t0, c16 & 7), row + (p.H + g) * kDh + c16 * 8);
+      cp_async16(sPa + static_cast<uint32_t>(((t - c_lo) * kDh + c16 * 8) * 2),
+                 row + (p.H + p.Hkv + g) * kDh + c16 * 8);
+    }
   }
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();   // V^T groups and the staged chunk values are in place
   if (nchunk > 0) {   // shared -> shared transpose into V^T (keys along K)
     const int d = tid & (kDh - 1);
-    const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
-    for (int t = c_lo + (tid >> 7); t < c_hi; t += 2) {
-      const int key = t - t0, grp = key >> 3;
-      const uint16_t v = vstage[(t - c_lo) * kDh + d];
-      const uint32_t addr = sVta + (grp >> 3) * kTile + swz(d, grp & 7) + (key & 7) * 2;
-      asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+    if constexpr (kF8) {
+      const uint8_t* vstage = smem + sp.pm;
+      for (int t = c_lo + (tid >> 7); t < c_hi; t += 2) {
+        const int key = t - t0;
+        const uint32_t v = vstage[(t - c_lo) * kDh + d];
+        const uint32_t addr = sVta + (key >> 7) * kTile + swz(d, (key & 127) >> 4) + (key & 15);
+        asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+      }
+    } else {
+      const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
+      for (int t = c_lo + (tid >> 7); t < c_hi; t += 2) {
+        const int key = t - t0, grp = key >> 3;
+        const uint16_t v = vstage[(t - c_lo) * kDh + d];
+        const uint32_t addr = sVta + (grp >> 3) * kTile + swz(d, grp & 7) + (key & 7) * 2;
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+      }
     }
   }
   fence_async_smem();   // generic-proxy shared-memory writes -> tensor-core reads
@@ -228,13 +277,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // ---- S = Q K^T into TMEM columns [0, KC)
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = make_idesc(false, kRows, static_cast<uint32_t>(KC));
+    const uint32_t idesc = make_idesc(kF8, kRows, static_cast<uint32_t>(KC));
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < (kF8 ? 1 : 2); ++b) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc_mma<false>(tmem, sw128_kmajor_desc(sQa + b * kTile + k * 32),
-                      sw128_kmajor_desc(sKa + b * (KC * 128) + k * 32), idesc, (b | k) ? 1u : 0u);
+        tc_mma<kF8>(tmem, sw128_kmajor_desc(sQa + b * kTile + k * 32),
+                    sw128_kmajor_desc(sKa + b * (KC * 128) + k * 32), idesc, (b | k) ? 1u : 0u);
     }
     tc_commit(&bar[0]);
   }
@@ -248,7 +297,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int r = quarter * 32 + lane;   // this thread's row == its TMEM lane
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int c0 = half * kHalf;         // this thread's keys: [c0, c0 + kHalf) of the slice
-  const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh));   // log2(e) / sqrt(Dh)
+  // log2(e) / sqrt(Dh), times the E4M3 codes' dequantisation fp32(s_q * s_k)
+  const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh)) *
+                       (kF8 ? __fmul_rn(p.s_qkv[0], p.s_qkv[1]) : 1.0f);
 
   // ---- pass 1: this row-half's scores (kept in registers), max and sum of exp
   float sv[kHalf];
@@ -297,18 +348,43 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // ---- pass 2: P = bf16(exp(s - m_half) * exp(m_half - M) / L) into the swizzled A
   // operand of P V
   const float fscale = mh > -INFINITY ? exp2f(mh - gmax) * ginv : 0.f;
+  if constexpr (kF8) {
+    // E4M3 probabilities with static scale 1/448: code = E4M3(P * 448), 16 keys per chunk
 #pragma unroll
-  for (int ch = 0; ch < kHalf / 8; ++ch) {   // 8-key chunks of 16 bytes
-    const int key = c0 + ch * 8;
-    float pv[8];
+    for (int ch = 0; ch < kHalf / 16; ++ch) {
+      const int key = c0 + ch * 16;
+      uint32_t w[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) pv[e] = key + e < nvalid ? sv[ch * 8 + e] * fscale : 0.f;
-    uint4 u;
-    u.x = pack_bf16(pv[0], pv[1]);
-    u.y = pack_bf16(pv[2], pv[3]);
-    u.z = pack_bf16(pv[4], pv[5]);
-    u.w = pack_bf16(pv[6], pv[7]);
-    st_shared_v4(sPa + (key >> 6) * kTile + swz(r, (key & 63) >> 3), u);
+      for (int q = 0; q < 4; ++q) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kk = ch * 16 + q * 4 + e;
+          const float pv = key + q * 4 + e < nvalid ? sv[kk] * fscale : 0.f;
+          packed |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(pv * 448.0f, __NV_SATFINITE, __NV_E4M3)) << (8 * e);
+        }
+        w[q] = packed;
+      }
+      st_shared_v4(sPa + (key >> 7) * kTile + swz(r, (key & 127) >> 4), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+    for (int j = half; j < (kKcp - KC) / 16; j += 2) {   // the zero-padded keys [KC, kKcp)
+      const int key = KC + j * 16;
+      st_shared_v4(sPa + (key >> 7) * kTile + swz(r, (key & 127) >> 4), make_uint4(0, 0, 0, 0));
+    }
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < kHalf / 8; ++ch) {   // 8-key chunks of 16 bytes
+      const int key = c0 + ch * 8;
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pv[e] = key + e < nvalid ? sv[ch * 8 + e] * fscale : 0.f;
+      uint4 u;
+      u.x = pack_bf16(pv[0], pv[1]);
+      u.y = pack_bf16(pv[2], pv[3]);
+      u.z = pack_bf16(pv[4], pv[5]);
+      u.w = pack_bf16(pv[6], pv[7]);
+      st_shared_v4(sPa + (key >> 6) * kTile + swz(r, (key & 63) >> 3), u);
+    }
   }
   tc_fence_before();
   fence_async_smem();
@@ -317,13 +393,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // ---- O = P V into TMEM columns [KC, KC + 128)
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = make_idesc(false, kRows, kDh);
+    const uint32_t idesc = make_idesc(kF8, kRows, kDh);
 #pragma unroll
     for (int b = 0; b < kBlk; ++b) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc_mma<false>(tmem + static_cast<uint32_t>(KC), sw128_kmajor_desc(sPa + b * kTile + k * 32),
-                      sw128_kmajor_desc(sVta + b * kTile + k * 32), idesc, (b | k) ? 1u : 0u);
+        tc_mma<kF8>(tmem + static_cast<uint32_t>(KC), sw128_kmajor_desc(sPa + b * kTile + k * 32),
+                    sw128_kmajor_desc(sVta + b * kTile + k * 32), idesc, (b | k) ? 1u : 0u);
     }
     tc_commit(&bar[1]);
   }
@@ -360,6 +436,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     const int rank = static_cast<int>(cluster_rank());
     const int e4 = lane * 4;
     const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
+    const float dv = kF8 ? __fdiv_rn(p.s_qkv[2], 448.0f) : 1.0f;   // E4M3 P and V: fp32(s_v / 448)
     for (int lr = warp; lr < rows_per; lr += kThreads / 32) {
       const int rr = rank * rows_per + lr;
       const int R = qt * kRows + rr;
@@ -371,6 +448,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
         acc.y += v.y;
         acc.z += v.z;
         acc.w += v.w;
+      }
+      if constexpr (kF8) {
+        acc.x *= dv;
+        acc.y *= dv;
+        acc.z *= dv;
+        acc.w *= dv;
       }
       const int hl = R / p.M, m = R % p.M;
       const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e4;
@@ -437,11 +520,15 @@ int attn_plan(int M, int P, int* kc, int* nsplit) {
   return FM_OK;
 }
 
-size_t attn_smem_bytes(int kc, int nsplit) { return 1024 + smem_plan(kc, nsplit).total; }
+size_t attn_smem_bytes(int kc, int nsplit, int fp8) { return 1024 + smem_plan(kc, nsplit, fp8 != 0).total; }
 
 cudaError_t attn_configure() {
-  const void* ks[3] = {reinterpret_cast<const void*>(attn_kernel<64>), reinterpret_cast<const void*>(attn_kernel<128>),
-                       reinterpret_cast<const void*>(attn_kernel<192>)};
+  const void* ks[6] = {reinterpret_cast<const void*>(attn_kernel<64, false>),
+                       reinterpret_cast<const void*>(attn_kernel<128, false>),
+                       reinterpret_cast<const void*>(attn_kernel<192, false>),
+                       reinterpret_cast<const void*>(attn_kernel<64, true>),
+                       reinterpret_cast<const void*>(attn_kernel<128, true>),
+                       reinterpret_cast<const void*>(attn_kernel<192, true>)};
   for (const void* k : ks) {
     const cudaError_t e = allow_max_dynamic_smem(k);
     if (e != cudaSuccess) return e;
@@ -452,6 +539,11 @@ cudaError_t attn_configure() {
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   KParams p;
   p.qkv = a.qkv;
+  p.qkv8 = reinterpret_cast<const uint8_t*>(a.qkv);
+  p.kpre8 = a.kpre8;
+  p.vtpre8 = a.vtpre8;
+  p.p16 = a.p16;
+  p.s_qkv = a.s_qkv;
   p.ldq = (a.H + 2 * a.Hkv) * kDh;
   p.kpre = a.kpre;
   p.vtpre = a.vtpre;
@@ -467,18 +559,64 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   p.kc = a.kc;
   p.nsplit = a.nsplit;
   p.err = a.err;
+  if (a.fp8 && (!a.kpre8 || !a.vtpre8 || !a.s_qkv || a.p16 % 16)) return cudaErrorInvalidValue;
   const int rows = p.G * p.M;
   const dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>((rows + kRows - 1) / kRows),
                   static_cast<unsigned>(a.Hkv));
   LaunchOpts lo = o;
   lo.cluster = dim3(static_cast<unsigned>(a.nsplit), 1, 1);
-  const size_t smem = attn_smem_bytes(a.kc, a.nsplit);
-  switch (a.kc) {
-    case 64: return launch(attn_kernel<64>, grid, dim3(kThreads), smem, lo, p);
-    case 128: return launch(attn_kernel<128>, grid, dim3(kThreads), smem, lo, p);
-    case 192: return launch(attn_kernel<192>, grid, dim3(kThreads), smem, lo, p);
+  const size_t smem = attn_smem_bytes(a.kc, a.nsplit, a.fp8);
+  switch (a.kc * 2 + (a.fp8 ? 1 : 0)) {
+    case 128: return launch(attn_kernel<64, false>, grid, dim3(kThreads), smem, lo, p);
+    case 256: return launch(attn_kernel<128, false>, grid, dim3(kThreads), smem, lo, p);
+    case 384: return launch(attn_kernel<192, false>, grid, dim3(kThreads), smem, lo, p);
+    case 129: return launch(attn_kernel<64, true>, grid, dim3(kThreads), smem, lo, p);
+    case 257: return launch(attn_kernel<128, true>, grid, dim3(kThreads), smem, lo, p);
+    case 385: return launch(attn_kernel<192, true>, grid, dim3(kThreads), smem, lo, p);
     default: return cudaErrorInvalidValue;
   }
+}
+
+namespace {
+
+__global__ void prefix_quant_kernel(const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vt,
+                                    uint8_t* __restrict__ k8, uint8_t* __restrict__ v8t,
+                                    const float* __restrict__ ascale, int P, int Hkv, int p_pad, int p16, int b,
+                                    int rows, size_t nk, size_t nv) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < nk + nv;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    if (i < nk) {   // keys: [L][rows][Hkv][Dh] of the range, stored at rows b.. of [L][P][Hkv][Dh]
+      const size_t per_l = static_cast<size_t>(rows) * Hkv * kDh;
+      const int l = static_cast<int>(i / per_l);
+      const size_t rem = i % per_l;
+      const size_t idx = (static_cast<size_t>(l) * P + b) * Hkv * kDh + rem;
+      const float rs = 1.0f / ascale[l * 8 + FM_SITE_K];
+      k8[idx] = static_cast<uint8_t>(
+          __nv_cvt_float_to_fp8(__bfloat162float(kc[idx]) * rs, __NV_SATFINITE, __NV_E4M3));
+    } else {   // values, transposed: [L][Hkv][Dh] rows, tokens b..b+rows-1 of each
+      const size_t j = i - nk;
+      const size_t vrow = j / rows;   // l * Hkv * Dh + g * Dh + d
+      const int t = b + static_cast<int>(j % rows);
+      const int l = static_cast<int>(vrow / (static_cast<size_t>(Hkv) * kDh));
+      const float rs = 1.0f / ascale[l * 8 + FM_SITE_V];
+      v8t[vrow * p16 + t] = static_cast<uint8_t>(
+          __nv_cvt_float_to_fp8(__bfloat162float(vt[vrow * p_pad + t]) * rs, __NV_SATFINITE, __NV_E4M3));
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t prefix_quant_launch(const __nv_bfloat16* kcache, const __nv_bfloat16* vtcache, uint8_t* k8, uint8_t* v8t,
+                                const float* ascale, int L, int P, int Hkv, int p_pad, int p16, int b, int e,
+                                cudaStream_t st) {
+  if (b < 0 || e > P || b >= e) return cudaErrorInvalidValue;
+  const int rows = e - b;
+  const size_t nk = static_cast<size_t>(L) * rows * Hkv * kDh;
+  const size_t nv = static_cast<size_t>(L) * Hkv * kDh * rows;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((nk + nv + 255) / 256, 2368));
+  prefix_quant_kernel<<<blocks, 256, 0, st>>>(kcache, vtcache, k8, v8t, ascale, P, Hkv, p_pad, p16, b, rows, nk, nv);
+  return cudaGetLastError();
 }
 
 cudaError_t transpose_v_launch(const __nv_bfloat16* v, __nv_bfloat16* vt, int L, int rows, int Hkv, int p_pad,

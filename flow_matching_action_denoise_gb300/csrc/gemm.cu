@@ -46,6 +46,9 @@ struct KParams {
   float* out;               // fp32 partial planes [s/cs][M][N], or
   __nv_bfloat16* out_bf16;  // when non-null (cs == s): bf16(sum * fp32(sa * sw)) [M][N]
   void* out_geglu;          // when non-null (cs == s, gate|up interleaved): Q(gelu(g) u) [M][N/2]
+  uint8_t* out_qkv8;        // when non-null (cs == s): E4M3 codes of Q | K | V [M][N] with scales s_qkv[0..2]
+  const float* s_qkv;
+  int nq, nk;
   int geglu_fp8;
   const float* sq;          // static scale of the GeGLU output
   const float* sa;
@@ -116,7 +119,10 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   tc_fence_after();
   if (kCs > 1) cluster_arrive_relaxed();   // paired with the wait before the first remote store
   const uint32_t tmem = *tmem_slot;
-  const float ds = (p.out_bf16 || p.out_geglu) ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
+  const float ds = (p.out_bf16 || p.out_geglu || p.out_qkv8) ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
+  float rs_qkv[3] = {1.0f, 1.0f, 1.0f};
+  if (p.out_qkv8)
+    for (int i = 0; i < 3; ++i) rs_qkv[i] = 1.0f / p.s_qkv[i];
   const float rs_geglu = (p.out_geglu && p.geglu_fp8) ? 1.0f / *p.sq : 1.0f;
   // Dependents may start only once this CTA holds its TMEM: a later GEMM's CTAs that
   // wait for this grid must never be able to take the columns this CTA still needs.
@@ -277,6 +283,16 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
             *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out_geglu) + fidx) = u;
           }
         }
+      } else if (p.out_qkv8) {
+        // the 4 columns share a section (sections are multiples of 128 columns)
+        const int c0 = static_cast<int>(col);
+        const float rs = c0 < p.nq ? rs_qkv[0] : (c0 < p.nq + p.nk ? rs_qkv[1] : rs_qkv[2]);
+        uchar4 cq;
+        cq.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8((acc.x * ds) * rs, __NV_SATFINITE, __NV_E4M3));
+        cq.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8((acc.y * ds) * rs, __NV_SATFINITE, __NV_E4M3));
+        cq.z = static_cast<uint8_t>(__nv_cvt_float_to_fp8((acc.z * ds) * rs, __NV_SATFINITE, __NV_E4M3));
+        cq.w = static_cast<uint8_t>(__nv_cvt_float_to_fp8((acc.w * ds) * rs, __NV_SATFINITE, __NV_E4M3));
+        *reinterpret_cast<uchar4*>(p.out_qkv8 + static_cast<size_t>(m) * p.N + col) = cq;
       } else if (p.out_bf16) {
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * ds, acc.y * ds);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * ds, acc.w * ds);
@@ -515,13 +531,19 @@ cudaError_t gemm_configure() {
 
 cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw,
-                        void* out_geglu, int geglu_fp8, const float* sq) {
-  if ((out_bf16 || out_geglu) && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
+                        void* out_geglu, int geglu_fp8, const float* sq, uint8_t* out_qkv8, const float* s_qkv,
+                        int nq, int nk) {
+  if ((out_bf16 || out_geglu || out_qkv8) && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
+  if (out_qkv8 && (!s_qkv || nq % 128 || nk % 128)) return cudaErrorInvalidValue;
   if (out_geglu && (!sq || g.N % 128)) return cudaErrorInvalidValue;
   KParams p;
   p.wpk = static_cast<const uint8_t*>(wpk);
   p.out = out;
   p.out_bf16 = out_bf16;
+  p.out_qkv8 = out_qkv8;
+  p.s_qkv = s_qkv;
+  p.nq = nq;
+  p.nk = nk;
   p.out_geglu = out_geglu;
   p.geglu_fp8 = geglu_fp8;
   p.sq = sq;

@@ -88,10 +88,13 @@ bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
 // epilogue applies m = gelu_tanh(g) * u to the dequantised sums and writes Q(m, *sq)
 // as [M][N/2] codes (E4M3 bytes if geglu_fp8, else bf16).
 // wpk: packed weight tiles (1024-byte aligned, fm_pack_weight layout).
+// out_qkv8 (requires cs == s): E4M3 codes of the dequantised product with the static
+// scales s_qkv[0..2] for columns [0, nq), [nq, nq + nk), [nq + nk, N) (Q, K, V).
 cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16 = nullptr, const float* sa = nullptr,
                         const float* sw = nullptr, void* out_geglu = nullptr, int geglu_fp8 = 0,
-                        const float* sq = nullptr);
+                        const float* sq = nullptr, uint8_t* out_qkv8 = nullptr, const float* s_qkv = nullptr,
+                        int nq = 0, int nk = 0);
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
 // ---------------------------------------------------------------- NVFP4-weight GEMM
@@ -184,12 +187,24 @@ struct AttnArgs {
   int kc;       // keys per slice (multiple of 64, <= 192)
   int nsplit;   // slices = cluster size (<= 8)
   int* err;
+  // FP8 attention: qkv holds E4M3 codes [M][(H+2Hkv)*Dh] (bytes), the prefix comes
+  // from its E4M3 copies, s_qkv points at the three static scales (Q, K, V)
+  int fp8 = 0;
+  const uint8_t* kpre8 = nullptr;    // [P][Hkv][Dh] of this layer
+  const uint8_t* vtpre8 = nullptr;   // [Hkv][Dh][p16] of this layer
+  int p16 = 0;                       // P rounded up to a multiple of 16
+  const float* s_qkv = nullptr;
 };
 // Slice plan for P + M keys; FM_ERR_SHAPE when they need more than 8 x 192.
 int attn_plan(int M, int P, int* kc, int* nsplit);
-size_t attn_smem_bytes(int kc, int nsplit);
+size_t attn_smem_bytes(int kc, int nsplit, int fp8);
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
 cudaError_t attn_configure();
+// E4M3 copies of prefix rows [b, e) of every layer: k8 = E4M3(k * (1/s_k)), v8t likewise
+// from the transposed bf16 values (row stride p16); s_k, s_v = ascale[l*8 + 5], [l*8 + 6].
+cudaError_t prefix_quant_launch(const __nv_bfloat16* kcache, const __nv_bfloat16* vtcache, uint8_t* k8, uint8_t* v8t,
+                                const float* ascale, int L, int P, int Hkv, int p_pad, int p16, int b, int e,
+                                cudaStream_t st);
 // v [L][rows][Hkv][Dh] -> vt[l][g][d][tok_begin + t] (row stride p_pad).
 cudaError_t transpose_v_launch(const __nv_bfloat16* v, __nv_bfloat16* vt, int L, int rows, int Hkv, int p_pad,
                                int tok_begin, cudaStream_t st);

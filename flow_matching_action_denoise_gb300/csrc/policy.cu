@@ -47,7 +47,10 @@ struct Layout {
   size_t total = 0;
   std::vector<size_t> wpk;   // [L*4] packed weights
   size_t wscale, ascale, mod, modf, w_in, b_in, w_out, b_out, gamma_f, kcache, vcache, a, x, q, o, q2, mc;
-  size_t qkvb;   // bf16 Q | K | V the attention reads (== y[0] unless NVFP4 reduces planes separately)
+  size_t qkvb;   // bf16 Q | K | V the attention reads (== y[0] unless NVFP4 reduces planes separately;
+                 // E4M3 codes with FP8 attention)
+  size_t kcache8, vcache8;   // FP8 attention: E4M3 copies of the prefix cache
+  size_t kv8_bytes, v8_bytes, ascale_bytes;
   size_t y[4];
   size_t err, amax, conds;
   size_t kv_bytes, a_bytes, scale_bytes;
@@ -64,6 +67,7 @@ struct Derived {
   int fp8;
   int nvfp4;
   int q_store;   // quantised operand storage: 0 bf16, 1 E4M3 codes, 2 E4M3 codes as f16 values
+  int attn_fp8;  // attention on E4M3 Q, K, V and probabilities
   fm::GemmShape gs[4];
   fm::Nvfp4Shape ns[4];
   int gN[4], gK[4];
@@ -113,6 +117,14 @@ int validate(const fm_config* c, std::string* why) {
     *why = "unsupported weight/activation format pair";
     return FM_ERR_INVALID_ARG;
   }
+  if (c->attn_fmt != FM_FMT_BF16 && c->attn_fmt != FM_FMT_FP8) {
+    *why = "attn_fmt must be FM_FMT_BF16 or FM_FMT_FP8";
+    return FM_ERR_INVALID_ARG;
+  }
+  if (c->attn_fmt == FM_FMT_FP8 && (c->weight_fmt != FM_FMT_FP8 || c->act_fmt != FM_FMT_FP8)) {
+    *why = "FP8 attention is built for FP8 weights and activations";
+    return FM_ERR_UNSUPPORTED;
+  }
   if (c->cond_mode != FM_COND_TIME && c->cond_mode != FM_COND_GIVEN) {
     *why = "bad cond_mode";
     return FM_ERR_INVALID_ARG;
@@ -136,6 +148,7 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
   dv->fp8 = c->act_fmt == FM_FMT_FP8;
   dv->nvfp4 = c->weight_fmt == FM_FMT_NVFP4;
   dv->q_store = dv->nvfp4 ? fm::kQFp8AsF16 : dv->fp8;
+  dv->attn_fp8 = c->attn_fmt == FM_FMT_FP8;
   dv->act_bytes = dv->q_store == 1 ? 1 : 2;
   const int N[4] = {dv->nqkv, c->d, 2 * c->F, c->d};
   const int K[4] = {c->d, c->H * c->Dh, c->d, c->F};
@@ -205,8 +218,9 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   for (int l = 0; l < L; ++l)
     for (int g = 0; g < 4; ++g) ly.wpk[l * 4 + g] = ly.take(fm::packed_weight_bytes(dv.gN[g], dv.gK[g], wfmt));
   ly.scale_bytes = static_cast<size_t>(L) * 4 * sizeof(float);
+  ly.ascale_bytes = static_cast<size_t>(L) * 8 * sizeof(float);   // [L][8]: FM_SITE_* columns
   ly.wscale = ly.take(ly.scale_bytes);
-  ly.ascale = ly.take(ly.scale_bytes);
+  ly.ascale = ly.take(ly.ascale_bytes);
   ly.mod = ly.take(static_cast<size_t>(S) * L * 6 * d * sizeof(float));
   ly.modf = ly.take(static_cast<size_t>(S) * 2 * d * sizeof(float));
   ly.w_in = ly.take(static_cast<size_t>(d) * c->A * 2);
@@ -230,6 +244,10 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
                       (g == 0 && !dv.nvfp4) ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
                                             : static_cast<size_t>(dv.nparts(g)) * M * dv.gN[g] * 4);
   ly.qkvb = dv.nvfp4 ? ly.take(static_cast<size_t>(M) * dv.gN[0] * 2) : ly.y[0];
+  ly.kv8_bytes = dv.attn_fp8 ? static_cast<size_t>(L) * c->P * c->Hkv * c->Dh : 0;
+  ly.v8_bytes = dv.attn_fp8 ? static_cast<size_t>(L) * c->Hkv * c->Dh * ((c->P + 15) / 16 * 16) : 0;
+  ly.kcache8 = ly.take(ly.kv8_bytes);
+  ly.vcache8 = ly.take(ly.v8_bytes);
   ly.err = ly.take(64);
   ly.amax = ly.take(64);
   ly.conds = ly.take(static_cast<size_t>(S) * d * sizeof(double));
@@ -283,7 +301,7 @@ struct fm_policy {
   }
   float* modf(int k, int i) const { return at<float>(ly.modf) + (static_cast<size_t>(k) * 2 + i) * cfg.d; }
   float* wscale(int l, int g) const { return at<float>(ly.wscale) + l * 4 + g; }
-  float* ascale(int l, int i) const { return at<float>(ly.ascale) + l * 4 + i; }
+  float* ascale(int l, int i) const { return at<float>(ly.ascale) + l * 8 + i; }
   int* errw() const { return at<int>(ly.err); }
 };
 
@@ -310,6 +328,16 @@ int cuda_fail(fm_policy* p, cudaError_t e, const char* where) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
+// The device scale table [L][8] from the caller's [L][4] ([L][7] with FP8 attention).
+std::vector<float> scale_table(const fm_config& c, const Derived& dv, const float* act_scales) {
+  std::vector<float> sc(static_cast<size_t>(c.L) * 8, 1.0f);
+  const int cols = dv.attn_fp8 ? 7 : 4;
+  if (dv.fp8 && act_scales)
+    for (int l = 0; l < c.L; ++l)
+      for (int i = 0; i < cols; ++i) sc[static_cast<size_t>(l) * 8 + i] = act_scales[static_cast<size_t>(l) * cols + i];
+  return sc;
+}
+
 // ---------------------------------------------------------------- tracing
 // Optional recorder: after a kernel, copy the buffer it wrote into the trace.
 struct Trace {
@@ -328,6 +356,16 @@ struct Trace {
 // Kernels of layer l at step k. tail: -1 = next layer's norm (layer (l+1) mod L),
 // otherwise the last layer of a decision step (Euler tail; head of step tail
 // if tail < S).
+// E4M3 copies of prefix rows [b, e) of every layer (FP8 attention), quantised with
+// the layer's static K and V scales.
+cudaError_t requant_prefix(fm_policy* p, int b, int e, cudaStream_t s) {
+  const fm_config& c = p->cfg;
+  return fm::prefix_quant_launch(p->at<__nv_bfloat16>(p->ly.kcache), p->at<__nv_bfloat16>(p->ly.vcache),
+                                 p->at<uint8_t>(p->ly.kcache8), p->at<uint8_t>(p->ly.vcache8),
+                                 p->at<float>(p->ly.ascale), c.L, c.P, c.Hkv, (c.P + 7) / 8 * 8,
+                                 (c.P + 15) / 16 * 16, b, e, s);
+}
+
 cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const LaunchOpts& o, Trace* tr = nullptr) {
   const fm_config& c = p->cfg;
   const Derived& dv = p->dv;
@@ -361,12 +399,16 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
     if (e != cudaSuccess) return e;
     e = fm::qkv_finalize_launch(y[0], dv.ns[0].s, c.M, dv.gN[0], p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), qkvb,
                                 o);
+  } else if (dv.attn_fp8) {   // E4M3 Q | K | V codes with their static scales
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, nullptr,
+                        p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), nullptr, 0, nullptr,
+                        reinterpret_cast<uint8_t*>(qkvb), p->ascale(l, FM_SITE_Q), c.H * c.Dh, c.Hkv * c.Dh);
   } else {
     e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, qkvb, p->ascale(l, FM_SITE_ATTN_IN),
                         p->wscale(l, 0));
   }
   if (e != cudaSuccess) return e;
-  FM_REC(qkvb, ybytes[0]);
+  FM_REC(qkvb, dv.attn_fp8 ? ybytes[0] / 2 : ybytes[0]);
 
   fm::AttnArgs at;
   at.qkv = qkvb;
@@ -384,6 +426,14 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   at.Hkv = c.Hkv;
   at.kc = dv.attn_kc;
   at.nsplit = dv.attn_nsplit;
+  if (dv.attn_fp8) {
+    const int p16 = (c.P + 15) / 16 * 16;
+    at.fp8 = 1;
+    at.kpre8 = p->at<uint8_t>(p->ly.kcache8) + static_cast<size_t>(l) * c.P * c.Hkv * c.Dh;
+    at.vtpre8 = p->at<uint8_t>(p->ly.vcache8) + static_cast<size_t>(l) * c.Hkv * c.Dh * p16;
+    at.p16 = p16;
+    at.s_qkv = p->ascale(l, FM_SITE_Q);
+  }
   e = fm::attn_launch(at, o);
   if (e != cudaSuccess) return e;
   FM_REC(p->at<void>(p->ly.o), static_cast<size_t>(c.M) * c.H * c.Dh * ab);
@@ -482,7 +532,7 @@ size_t trace_record_bytes(const fm_policy* p) {
   const Derived& dv = p->dv;
   const size_t M = c.M, ab = dv.act_bytes;
   size_t n = 3 * M * c.d * 4 + M * c.d * ab * 2 + M * c.H * c.Dh * ab + M * c.F * ab + p->ly.a_bytes;
-  n += M * dv.gN[0] * 2;
+  n += M * dv.gN[0] * (dv.attn_fp8 ? 1 : 2);
   for (int g = 1; g < 4; g += 2) n += static_cast<size_t>(dv.nparts(g)) * M * dv.gN[g] * 4;
   return n;
 }
@@ -782,12 +832,13 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
           "copy gamma_f"))
     return bail(FM_ERR_CUDA, why);
   // activation scales (BF16 activations: 1)
-  std::vector<float> sc(static_cast<size_t>(c.L) * 4, 1.0f);
-  if (dv.fp8) std::copy(act_scales, act_scales + sc.size(), sc.begin());
+  const std::vector<float> sc = scale_table(c, dv, act_scales);
   if (!cu(cudaMemcpyAsync(p->at<void>(p->ly.ascale), sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, s),
           "copy act scales") ||
       !cu(cudaMemsetAsync(p->at<void>(p->ly.kcache), 0, p->ly.kv_bytes, s), "zero kcache") ||
       !cu(cudaMemsetAsync(p->at<void>(p->ly.vcache), 0, p->ly.kv_bytes, s), "zero vcache") ||
+      !cu(cudaMemsetAsync(p->at<void>(p->ly.kcache8), 0, std::max<size_t>(p->ly.kv8_bytes, 1), s), "zero kcache8") ||
+      !cu(cudaMemsetAsync(p->at<void>(p->ly.vcache8), 0, std::max<size_t>(p->ly.v8_bytes, 1), s), "zero vcache8") ||
       !cu(cudaMemsetAsync(p->at<void>(p->ly.a), 0, p->ly.a_bytes, s), "zero a") ||
       !cu(cudaMemsetAsync(p->errw(), 0, 64, s), "zero err"))
     return bail(FM_ERR_CUDA, why);
@@ -834,10 +885,11 @@ int policy_destroy(fm_policy* p) {
 int fm_set_act_scales(fm_policy* p, const float* act_scales, void* stream) {
   if (!p || !act_scales) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
   if (!p->dv.fp8) return FM_OK;
-  FM_CUDA(p, cudaMemcpyAsync(p->at<void>(p->ly.ascale), act_scales, p->ly.scale_bytes, cudaMemcpyHostToDevice,
-                             static_cast<cudaStream_t>(stream)));
-  return cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) == cudaSuccess ? FM_OK
-                                                                                 : fail(p, FM_ERR_CUDA, "sync");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const std::vector<float> sc = scale_table(p->cfg, p->dv, act_scales);
+  FM_CUDA(p, cudaMemcpyAsync(p->at<void>(p->ly.ascale), sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, s));
+  if (p->dv.attn_fp8 && p->cfg.P > 0) FM_CUDA(p, requant_prefix(p, 0, p->cfg.P, s));
+  return cudaStreamSynchronize(s) == cudaSuccess ? FM_OK : fail(p, FM_ERR_CUDA, "sync");
 }
 
 int set_prefix_kv(fm_policy* p, const uint16_t* k, const uint16_t* v, void* stream) {
@@ -859,6 +911,7 @@ int refresh_prefix(fm_policy* p, int tok_begin, int tok_end, const uint16_t* k, 
   // values are kept transposed, [L][Hkv][Dh][P_pad], the layout attention's P.V operand needs
   FM_CUDA(p, fm::transpose_v_launch(reinterpret_cast<const __nv_bfloat16*>(v), p->at<__nv_bfloat16>(p->ly.vcache), c.L,
                                     static_cast<int>(rows), c.Hkv, (c.P + 7) / 8 * 8, tok_begin, s));
+  if (p->dv.attn_fp8) FM_CUDA(p, requant_prefix(p, tok_begin, tok_end, s));
   return FM_OK;
 }
 
@@ -891,7 +944,7 @@ int decode_actions_host(fm_policy* p, const float* noise_host, float* actions_ho
 
 int fm_state_size(const fm_policy* p, size_t* bytes) {
   if (!p || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
-  *bytes = sizeof(CapsuleHeader) + 2 * p->ly.kv_bytes + p->ly.a_bytes + p->ly.scale_bytes;
+  *bytes = sizeof(CapsuleHeader) + 2 * p->ly.kv_bytes + p->ly.a_bytes + p->ly.ascale_bytes;
   return FM_OK;
 }
 
@@ -910,7 +963,7 @@ int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, voi
   h.ws_base = reinterpret_cast<uintptr_t>(p->ws);
   h.kv_bytes = p->ly.kv_bytes;
   h.a_bytes = p->ly.a_bytes;
-  h.scale_bytes = p->ly.scale_bytes;
+  h.scale_bytes = p->ly.ascale_bytes;
   h.L = p->cfg.L;
   h.P = p->cfg.P;
   h.Hkv = p->cfg.Hkv;
@@ -930,7 +983,7 @@ int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, voi
   const size_t regions[4][2] = {{p->ly.kcache, p->ly.kv_bytes},
                                 {p->ly.vcache, p->ly.kv_bytes},
                                 {p->ly.a, p->ly.a_bytes},
-                                {p->ly.ascale, p->ly.scale_bytes}};
+                                {p->ly.ascale, p->ly.ascale_bytes}};
   for (const auto& r : regions) {
     if (r[1]) FM_CUDA(p, cudaMemcpyAsync(d + off, p->at<void>(r[0]), r[1], k, s));
     off += r[1];
@@ -957,7 +1010,7 @@ int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device
   if (h.plan_hash != p->plan_hash) return fail(p, FM_ERR_STATE_MISMATCH, "capsule was made by another plan");
   if (h.ws_base != reinterpret_cast<uintptr_t>(p->ws))
     return fail(p, FM_ERR_STATE_MISMATCH, "capsule is bound to another workspace address");
-  if (h.kv_bytes != p->ly.kv_bytes || h.a_bytes != p->ly.a_bytes || h.scale_bytes != p->ly.scale_bytes ||
+  if (h.kv_bytes != p->ly.kv_bytes || h.a_bytes != p->ly.a_bytes || h.scale_bytes != p->ly.ascale_bytes ||
       h.L != p->cfg.L || h.P != p->cfg.P || h.M != p->cfg.M || h.A != p->cfg.A)
     return fail(p, FM_ERR_STATE_MISMATCH, "capsule shapes differ");
   const uint8_t* sp = static_cast<const uint8_t*>(src);
@@ -966,11 +1019,13 @@ int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device
   const size_t regions[4][2] = {{p->ly.kcache, p->ly.kv_bytes},
                                 {p->ly.vcache, p->ly.kv_bytes},
                                 {p->ly.a, p->ly.a_bytes},
-                                {p->ly.ascale, p->ly.scale_bytes}};
+                                {p->ly.ascale, p->ly.ascale_bytes}};
   for (const auto& r : regions) {
     if (r[1]) FM_CUDA(p, cudaMemcpyAsync(p->at<void>(r[0]), sp + off, r[1], k, s));
     off += r[1];
   }
+  // the E4M3 prefix copy is derived state: re-derive it from the restored cache and scales
+  if (p->dv.attn_fp8 && p->cfg.P > 0) FM_CUDA(p, requant_prefix(p, 0, p->cfg.P, s));
   if (!src_on_device) FM_CUDA(p, cudaStreamSynchronize(s));
   p->decisions = h.decisions;
   return FM_OK;
@@ -1009,7 +1064,9 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
       {"y_qkv", ly.qkvb, M * dv.gN[0] * 2},
       {"y_o", ly.y[1], ypart(1)},
       {"y_d", ly.y[3], ypart(3)},
-      {"act_scales", ly.ascale, ly.scale_bytes},
+      {"act_scales", ly.ascale, ly.ascale_bytes},
+      {"prefix_k8", ly.kcache8, ly.kv8_bytes},
+      {"prefix_v8", ly.vcache8, ly.v8_bytes},
       {"weight_scales", ly.wscale, ly.scale_bytes},
       {"mod", ly.mod, static_cast<size_t>(c.S) * c.L * 6 * c.d * 4},
       {"mod_final", ly.modf, static_cast<size_t>(c.S) * 2 * c.d * 4},

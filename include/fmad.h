@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define FM_ABI_VERSION 1
+#define FM_ABI_VERSION 2
 
 typedef enum fm_status {
   FM_OK = 0,
@@ -76,12 +76,17 @@ enum {
   FM_COND_GIVEN = 1   /* cond of step k = caller-supplied vector (fm_weights.conds) */
 };
 
-/* Activation quant points per layer, the column index of the [L][4] scale table. */
+/* Activation quant points per layer, the column index of the [L][4] scale table
+ * ([L][7] with FP8 attention: columns 4-6 are the static scales of Q, K and V,
+ * the prefix cache's keys and values included). */
 enum {
   FM_SITE_ATTN_IN = 0,   /* pre-attention AdaRMSNorm output (QKV GEMM input) */
   FM_SITE_ATTN_OUT = 1,  /* attention output (O GEMM input) */
   FM_SITE_MLP_IN = 2,    /* pre-MLP AdaRMSNorm output (gate|up GEMM input) */
-  FM_SITE_GEGLU = 3      /* GeGLU output (down GEMM input) */
+  FM_SITE_GEGLU = 3,     /* GeGLU output (down GEMM input) */
+  FM_SITE_Q = 4,         /* FP8 attention: queries */
+  FM_SITE_K = 5,         /* FP8 attention: keys (chunk and prefix) */
+  FM_SITE_V = 6          /* FP8 attention: values (chunk and prefix) */
 };
 
 /* Policy shape and options. Preconditions (FM_ERR_SHAPE otherwise):
@@ -97,6 +102,9 @@ typedef struct fm_config {
   int L, S, M, d, H, Hkv, Dh, F, P, A;
   int weight_fmt;      /* fm_format */
   int act_fmt;         /* fm_format (FP8 or BF16) */
+  int attn_fmt;        /* fm_format of the attention operands: BF16, or FP8 (E4M3 Q, K, V
+                          with static scales and probabilities coded E4M3(P * 448));
+                          FP8 requires FP8 weights and activations */
   int cond_mode;       /* FM_COND_TIME or FM_COND_GIVEN */
   float rms_eps;       /* AdaRMSNorm epsilon */
   int ksplit[4];       /* K-split of the QKV, O, gate|up and down GEMMs; 0 = auto */
@@ -159,7 +167,8 @@ int fm_workspace_size(const fm_config* cfg, size_t* bytes);
  * K-major 128-byte swizzled tiles, precomputes the per-step modulation table
  * (the t-schedule is fixed, so modulation is per-create state), copies the
  * in/out projections, stores the static activation scales (host [L][4] fp32,
- * columns FM_SITE_*; ignored for BF16 activations and may then be NULL) and,
+ * [L][7] with FP8 attention, columns FM_SITE_*; ignored for BF16 activations and
+ * may then be NULL) and,
  * with FM_FLAG_USE_GRAPH, captures the whole decision as one CUDA graph.
  * Synchronises `stream` before returning. The prefix cache starts zeroed.
  * On failure nothing is leaked and *out is NULL. */
@@ -170,11 +179,14 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
  * The caller must not destroy a policy with work in flight on its stream. */
 int policy_destroy(fm_policy* p);
 
-/* Replace the static activation scales (host [L][4] fp32). Stream-ordered copy
- * into the policy's scale buffer; the captured graph reads them from there. */
+/* Replace the static activation scales (host [L][4] fp32, [L][7] with FP8
+ * attention). Stream-ordered copy into the policy's scale buffer; the captured
+ * graph reads them from there. With FP8 attention the prefix cache's E4M3 copy
+ * is re-derived with the new K and V scales. */
 int fm_set_act_scales(fm_policy* p, const float* act_scales, void* stream);
 
-/* Overwrite the whole prefix KV cache: k, v device bf16 [L][P][Hkv][Dh]. */
+/* Overwrite the whole prefix KV cache: k, v device bf16 [L][P][Hkv][Dh]. With
+ * FP8 attention the cache's E4M3 copy (static K and V scales) is derived here. */
 int set_prefix_kv(fm_policy* p, const uint16_t* k, const uint16_t* v, void* stream);
 
 /* Overwrite rows [tok_begin, tok_end) of every layer's prefix K and V (the
@@ -221,9 +233,14 @@ int fm_device_status(fm_policy* p, void* stream, int* word);
  *   "q", "q2"               codes [M][d] (pre-attention / pre-MLP GEMM operand)
  *   "attn_out"              codes [M][H*Dh]
  *   "geglu_out"             codes [M][F]
- *   "y_qkv"                 bf16 [M][(H+2Hkv)*Dh] dequantised Q | K | V
+ *   "y_qkv"                 bf16 [M][(H+2Hkv)*Dh] dequantised Q | K | V (FP8 attention:
+ *                           their E4M3 codes, one byte each, static scales FM_SITE_Q..V)
+ *   "prefix_k8", "prefix_v8"  FP8 attention only: E4M3 copies of the prefix cache,
+ *                           keys [L][P][Hkv][Dh], values transposed [L][Hkv][Dh][P16]
+ *                           (P16 = P rounded up to 16)
  *   "y_o", "y_d"            fp32 [parts][M][N] GEMM partial planes
- *   "act_scales", "weight_scales"  fp32 [L][4]
+ *   "act_scales"            fp32 [L][8] (columns FM_SITE_*, column 7 unused)
+ *   "weight_scales"         fp32 [L][4]
  *   "mod"                   fp32 [S][L][6][d]; "mod_final" fp32 [S][2][d]
  * Codes are one byte (FP8 activations), bf16 (BF16), or, with NVFP4 weights, the
  * E4M3 codes' f16 values (two bytes, exact: the operand format of the NVFP4 GEMM).

@@ -87,6 +87,7 @@ def parse_trace(raw, cfg, pol):
     M, d = cfg.M, cfg.d
     fp8 = cfg.act_fmt == "fp8"
     f16_codes = cfg.weight_fmt == "nvfp4"   # E4M3 codes stored as their f16 values
+    qkv8 = getattr(cfg, "attn_fmt", "bf16") == "fp8"   # Q | K | V as E4M3 codes
     ab = 1 if fp8 and not f16_codes else 2
 
     def parts(name, n):
@@ -107,10 +108,12 @@ def parse_trace(raw, cfg, pol):
             r = {}
             for name, kind, shape in layout:
                 n = int(np.prod(shape))
-                nb = n * (4 if kind == "f" else 2 if kind == "b" else ab)
+                nb = n * (4 if kind == "f" else (1 if qkv8 else 2) if kind == "b" else ab)
                 chunk = raw[off:off + nb]
                 off += nb
-                if kind == "b":
+                if kind == "b" and qkv8:
+                    r[name] = C.e4m3_decode_code(chunk).reshape(shape)
+                elif kind == "b":
                     r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
                 elif kind == "f":
                     r[name] = chunk.view(np.float32).reshape(shape).astype(np.float64)

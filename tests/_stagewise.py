@@ -11,6 +11,7 @@ Tolerances:
 """
 import numpy as np
 
+from oracle import codecs as C
 from oracle import model as O
 
 
@@ -28,14 +29,15 @@ def bf16_ulp(v):
     return np.ldexp(1.0, np.maximum(E - 1, -126) - 7)
 
 
-def check_codes(got_values, ref_values, what, fmt="fp8", max_frac=1e-3, abs_tol=1e-3):
+def check_codes(got_values, ref_values, what, fmt="fp8", max_frac=1e-3, abs_tol=1e-3, extra=0.0):
     """Quantised operands agree when they differ by at most one grid step at the larger
-    magnitude plus abs_tol * RMS: a near-tie input rounds either way, and near zero
-    (subnormal steps) a tiny upstream difference can span several steps."""
+    magnitude plus abs_tol * RMS (plus a per-element `extra`): a near-tie input rounds
+    either way, and near zero (subnormal steps) a tiny upstream difference can span
+    several steps."""
     got, ref = np.asarray(got_values, np.float64), np.asarray(ref_values, np.float64)
     ulp = e4m3_ulp if fmt == "fp8" else bf16_ulp
     diff = np.abs(got - ref)
-    allow = ulp(np.maximum(np.abs(got), np.abs(ref))) + abs_tol * np.sqrt(np.mean(ref ** 2))
+    allow = ulp(np.maximum(np.abs(got), np.abs(ref))) + abs_tol * np.sqrt(np.mean(ref ** 2)) + extra
     bad = diff > allow * (1 + 1e-12)
     if np.any(bad):
         i = np.unravel_index(np.argmax(diff - allow), diff.shape)
@@ -50,9 +52,47 @@ def check_close(got, ref, what, tol=1e-5):
     assert err <= tol, f"{what}: {err:.2e} > {tol:.0e}"
 
 
-def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac=1e-3):
-    """recs[k][l] as parse_trace returns them; scales [L][4] (ignored for bf16)."""
+def prefix_codes(kp, vp, scales):
+    """The E4M3 prefix copy the FP8-attention path keeps: per layer
+    E4M3(fp32(x * fp32(1 / s))) with the layer's K and V scales."""
+    out = []
+    for l in range(kp.shape[0]):
+        rk = np.float64(np.float32(1.0) / np.float32(scales[l][O.SITE_K]))
+        rv = np.float64(np.float32(1.0) / np.float32(scales[l][O.SITE_V]))
+        out.append((C.e4m3(C.fp32(np.asarray(kp[l], np.float64) * rk)),
+                    C.e4m3(C.fp32(np.asarray(vp[l], np.float64) * rv))))
+    return out
+
+
+_E4M3_POS = np.unique(np.abs(C.e4m3_decode_code(np.arange(0, 127))))
+
+
+def fp8_attention_allowance(qc, kc, vc, kpre_c, vpre_c, H, Hkv, Dh, s_q, s_k, s_v, rel=1e-5):
+    """Largest change of O when probability codes whose exact value P * 448 lies within
+    `rel` of an E4M3 rounding boundary round the other way (fp32 softmax on the GPU vs
+    the exact one here): per element, sum over such keys of one code step * |v| *
+    fp32(s_v / 448). Returns [M][H*Dh]."""
+    ds = np.float64(np.float32(s_q) * np.float32(s_k))
+    dv = np.float64(np.float32(s_v) / np.float32(448.0))
+    out = np.zeros((qc.shape[0], H * Dh))
+    for h in range(H):
+        g = (h * Hkv) // H
+        keys = np.concatenate([kpre_c[:, g, :], kc[:, g * Dh:(g + 1) * Dh]], axis=0)
+        vals = np.concatenate([vpre_c[:, g, :], vc[:, g * Dh:(g + 1) * Dh]], axis=0)
+        x = O.softmax((qc[:, h * Dh:(h + 1) * Dh] @ keys.T) * ds / np.sqrt(Dh)) * 448.0
+        hi = np.clip(np.searchsorted(_E4M3_POS, x), 1, _E4M3_POS.size - 1)
+        g0, g1 = _E4M3_POS[hi - 1], _E4M3_POS[hi]
+        near = np.abs(x - (g0 + g1) / 2) <= rel * np.maximum(x, 1e-30)
+        out[:, h * Dh:(h + 1) * Dh] = (near * (g1 - g0)) @ np.abs(vals) * dv
+    return out
+
+
+def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac=1e-3, attn_abs_tol=2.0 ** -7):
+    """recs[k][l] as parse_trace returns them; scales [L][4] ([L][7] with FP8
+    attention; ignored for bf16)."""
     fmt = cfg.act_fmt
+    attn8 = getattr(cfg, "attn_fmt", "bf16") == "fp8"
+    prefix8 = prefix_codes(kp, vp, scales) if attn8 else None
     M, H, Dh, F, L, S = cfg.M, cfg.H, cfg.Dh, cfg.F, cfg.L, cfg.S
     fin = model.final
     kp, vp = np.asarray(kp, np.float64), np.asarray(vp, np.float64)
@@ -73,21 +113,33 @@ def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac
             where = f"step {k} layer {l}"
             check_codes(r["q"], O.quant_codes(O.ada_norm(r["x_in"], sc1, sh1, cfg.eps), s_act(l, 0), fmt),
                         where + " pre-attention quantise", fmt)
-            # QKV: the GEMM epilogue emits bf16(sum * dequant); within one bf16 rounding
-            # of the exact dequantised product
             qkv = r["y_qkv"]
             exact = (r["q"] @ W["qkv"].codes.T) * dq(l, 0, W["qkv"])
-            assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) + 1e-5 * np.sqrt(np.mean(exact ** 2))), \
-                where + " QKV GEMM"
-            # the attention stage's input is exactly the recorded bf16 Q | K | V
-            Q = qkv[:, :H * Dh]
-            Kc = qkv[:, H * Dh:(H + cfg.Hkv) * Dh]
-            Vc = qkv[:, (H + cfg.Hkv) * Dh:]
-            Oref = O.attention(Q, Kc, Vc, kp[l], vp[l], H, cfg.Hkv, Dh)
-            # attention rounds its probabilities to bf16: a near-tie probability rounding
-            # either way moves a row of O by up to 2^-9 * P * |V|, so its allowance is 2^-7 * RMS
+            nq, nk = H * Dh, cfg.Hkv * Dh
+            if attn8:
+                # E4M3 Q | K | V codes with their static scales, from the exact product
+                s3 = [s_act(l, O.SITE_Q), s_act(l, O.SITE_K), s_act(l, O.SITE_V)]
+                for (a, b), sx, nm in zip(((0, nq), (nq, nq + nk), (nq + nk, exact.shape[1])), s3, "QKV"):
+                    check_codes(qkv[:, a:b], O.quant_codes(exact[:, a:b], sx, "fp8"), where + f" QKV GEMM ({nm} codes)")
+                # the attention stage's input is exactly the recorded codes and the prefix copy
+                args = (qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], prefix8[l][0], prefix8[l][1], H,
+                        cfg.Hkv, Dh, *s3)
+                Oref = O.attention_fp8(*args)
+                # probability codes at a rounding boundary may round either way
+                extra = fp8_attention_allowance(*args) / s_act(l, 1)
+            else:
+                extra = 0.0
+                # QKV: the GEMM epilogue emits bf16(sum * dequant); within one bf16 rounding
+                # of the exact dequantised product
+                assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) +
+                              1e-5 * np.sqrt(np.mean(exact ** 2))), where + " QKV GEMM"
+                # the attention stage's input is exactly the recorded bf16 Q | K | V
+                Oref = O.attention(qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], kp[l], vp[l], H, cfg.Hkv, Dh)
+            # attention rounds its probabilities (bf16, or E4M3 with 3 mantissa bits): a
+            # near-tie probability rounding either way moves a row of O by a fraction of
+            # P * |V|, so its allowance is abs_tol * RMS
             check_codes(r["attn_out"], O.quant_codes(Oref, s_act(l, 1), fmt), where + " attention", fmt,
-                        max_frac=attn_max_frac, abs_tol=2.0 ** -7)
+                        max_frac=attn_max_frac, abs_tol=attn_abs_tol, extra=extra)
             yo = r["y_o"].sum(0)
             check_close(yo, r["attn_out"] @ W["o"].codes.T, where + " O GEMM")
             check_close(r["x_mid"], r["x_in"] + g1 * yo * dq(l, 1, W["o"]), where + " attention residual")

@@ -8,7 +8,8 @@ the largest action difference between the oracle and the same oracle whose
 pre-quantisation values are first rounded to fp32 (a perturbation of at most
 2^-24 relative, i.e. what any fp32 implementation of the same arithmetic may
 differ by), relative to RMS(actions). Uses the calibrated scales and noise draw 0.
-Run: python tests/golden/make_fp8_envelope.py
+Run: python tests/golden/make_fp8_envelope.py [workload ...]
+(default: expert_fp8_m50 and expert_fp8attn_m50, the same expert with FP8 attention).
 """
 import os
 import sys
@@ -52,4 +53,5 @@ def main(name="expert_fp8_m50"):
 
 
 if __name__ == "__main__":
-    main()
+    for name in sys.argv[1:] or ("expert_fp8_m50", "expert_fp8attn_m50"):
+        main(name)
