@@ -279,6 +279,33 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+def time_graph(device, launches, replays=5):
+    """Capture `launches` (callables taking a stream) back to back into one CUDA graph,
+    replay it, and return the device time per launch in microseconds (CUDA events on
+    the replay stream): kernel durations without host launch gaps."""
+    import torch
+    s = torch.cuda.Stream(device)
+    for f in launches[:2]:   # one-time setup (function attributes, module load) outside the capture
+        f(s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for f in launches:
+            f(s)
+    g.replay()
+    torch.cuda.synchronize(device)
+    cur = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(replays):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1e3 / (replays * len(launches))
+    del g
+    return us
+
+
 def time_dominant_gemm(cfg, pol, device, stream):
     """Average duration of the gate|up GEMM (the largest weight stream of a layer)
     launched back to back through the C ABI over rotating packed weights (> 2x L2),
@@ -310,17 +337,9 @@ def time_dominant_gemm(cfg, pol, device, stream):
     del w
     a = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device=device)
     out = torch.empty((nparts, M, N), dtype=torch.float32, device=device)
-    reps = copies * 8
-    for i in range(copies):
-        fmad.fm_test_skinny_gemm(a, M, K, bufs[i][1], N, fmad.FMT_FP8, s, cs, out, stream)
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(reps):
-        fmad.fm_test_skinny_gemm(a, M, K, bufs[i % copies][1], N, fmad.FMT_FP8, s, cs, out, stream)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    launches = [lambda st, ptr=ptr: fmad.fm_test_skinny_gemm(a, M, K, ptr, N, fmad.FMT_FP8, s, cs, out, st)
+                for _, ptr in bufs] * 4
+    us = time_graph(device, launches)
     algo = N * K + M * K + nparts * M * N * 4
     peak, kind = measured_peaks()
     achieved = algo / (us * 1e-6) / 1e9
@@ -329,7 +348,7 @@ def time_dominant_gemm(cfg, pol, device, stream):
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind_note(kind),
             "traffic": profiled_traffic(), "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
-            "timing": "back-to-back launches, rotating weights over > 2x L2, CUDA events"}
+            "timing": "CUDA graph of back-to-back launches over rotating weights (> 2x L2), CUDA events"}
 
 
 def time_dominant_gemm_nvfp4(cfg, device, stream):
@@ -356,17 +375,9 @@ def time_dominant_gemm_nvfp4(cfg, device, stream):
     del w
     a = (torch.randn((M, K), device=device) * 4).to(torch.float16)
     out = torch.empty((1, M, N), dtype=torch.float32, device=device)
-    reps = copies * 8
-    for i in range(copies):
-        fmad.fm_test_skinny_gemm(a, M, K, bufs[i][1], N, fmad.FMT_NVFP4, 1, 1, out, stream)
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(reps):
-        fmad.fm_test_skinny_gemm(a, M, K, bufs[i % copies][1], N, fmad.FMT_NVFP4, 1, 1, out, stream)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    launches = [lambda st, ptr=ptr: fmad.fm_test_skinny_gemm(a, M, K, ptr, N, fmad.FMT_NVFP4, 1, 1, out, st)
+                for _, ptr in bufs] * 4
+    us = time_graph(device, launches)
     flops = 2 * M * N * K
     peak, kind = measured_tensor_peak(sustained=False)
     achieved = flops / (us * 1e-6) / 1e12
@@ -377,7 +388,7 @@ def time_dominant_gemm_nvfp4(cfg, device, stream):
             "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind_note(kind)} dense bf16 burst (f16 same rate)",
             "traffic": None, "algorithmic_flops": int(flops), "avg_launch_us": round(us, 3),
             "hbm": {"achieved_gbs": round(hbm, 1), "peak_gbs": hpk, "frac": round(hbm / hpk, 4)},
-            "timing": "back-to-back launches, rotating weights over > 2x L2, CUDA events"}
+            "timing": "CUDA graph of back-to-back launches over rotating weights (> 2x L2), CUDA events"}
 
 
 def profiled_traffic(name="skinny_gemm_gu_m50.md"):
@@ -569,6 +580,120 @@ def run_bf16_protocol(args):
             "clocks": clocks.summary()}
 
 
+def l2_bytes(device):
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    return getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+
+
+def run_layer_protocol(args):
+    """Single decoder layer, one denoise step (M = 10, d = 1024, prefix 64, FP8): R
+    copies of the layer's weights in separate buffers, R * 15 MB >= 2x L2, run as one
+    R-layer, 1-step policy (one CUDA graph with PDL); time per layer = decision time / R
+    (the step head and tail are included, spread over the R layers)."""
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    device = torch.device("cuda", 0)
+    fmad.load()
+    base = fm_synth.config("layer_fp8_m10")
+    layer = fm_synth.layer_weights(base, 0)
+    ab = algorithmic_bytes(base)
+    per_layer = ab["weights"] + ab["kv"] + base.S * 6 * base.d * 4   # weights, prefix KV, the layer's modulation
+    R = int(np.ceil(2 * l2_bytes(device) / per_layer)) + 1
+    cfg = fm_synth.config("layer_fp8_m10", L=R)
+    conds = fm_synth.step_conds(cfg)
+    scales = np.tile(np.loadtxt(os.path.join(ROOT, "tests", "golden", "act_scales_layer_fp8_m10.txt"),
+                                ndmin=2).astype(np.float32), (R, 1))
+    pol = fmad.Policy(cfg, [layer] * R, fm_synth.final_weights(cfg), act_scales=scales, conds=conds, device=device)
+    kp, vp = fm_synth.prefix_kv(cfg)
+    pol.set_prefix_kv(torch.from_numpy(kp).to(device, torch.bfloat16), torch.from_numpy(vp).to(device, torch.bfloat16))
+    noise = torch.from_numpy(fm_synth.noise(cfg, 0)).to(device)
+    actions = torch.empty_like(noise)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(max(3, args.warmup)):
+        pol.decode(noise, actions)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            pol.decode(noise, actions)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+    if fmad.device_status(pol.handle):
+        raise RuntimeError("device error word set")
+    us = e0.elapsed_time(e1) * 1e3 / args.steps / R
+    peak, kind = measured_peaks()
+    gbs = per_layer / (us * 1e-6) / 1e9
+    pol.close()
+    return {"protocol": "single layer, rotating weight copies", "workload": base.name, "copies": R,
+            "bytes_per_layer": int(per_layer), "us_per_layer": round(us, 3), "achieved_gbs": round(gbs, 1),
+            "peak_gbs": peak, "frac": round(gbs / peak, 4), "peak_kind": peak_kind_note(kind),
+            "kernels_per_layer": 7, "steps": args.steps, "clocks": clocks.summary()}
+
+
+def run_gemm_sweep(args):
+    """Skinny GEMM + fused consumer (fm_gemm_consumer: bias + gated residual + AdaRMSNorm
+    + static E4M3 quantise) over M in {1, 10, 50, 63}, K in {1024, 2048, 4096},
+    N in {1024, 4096, 8192, 16384}, K-split s in {1, 2, 4, 8, 16}: back-to-back calls
+    over rotating packed weights (> 2x L2), captured in a CUDA graph, CUDA events.
+    Algorithmic bytes per call:
+    K N (weights) + M K (activations) + 9 M N (x read/write, partial write/read, codes)
+    + 16 N (bias, gate, scale, shift)."""
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    device = torch.device("cuda", 0)
+    fmad.load()
+    stream = torch.cuda.current_stream(device)
+    peak, kind = measured_peaks()
+    l2 = l2_bytes(device)
+    rows = []
+    f32 = lambda n, v=0.1: torch.full((n,), v, dtype=torch.float32, device=device)
+    for K in (1024, 2048, 4096):
+        for N in (1024, 4096, 8192, 16384):
+            nbytes = fmad.fm_packed_weight_bytes(N, K, fmad.FMT_FP8)
+            copies = min(256, int(np.ceil(2 * l2 / nbytes)) + 1)
+            w = (torch.randn(N, K, device=device) * 0.02)
+            pool = torch.empty(copies * (nbytes + 1024), dtype=torch.uint8, device=device)
+            base = pool.data_ptr() + ((-pool.data_ptr()) % 1024)
+            ptrs = [base + i * (nbytes + 1024) for i in range(copies)]
+            s_w = torch.empty(1, dtype=torch.float32, device=device)
+            for ptr in ptrs:
+                fmad.fm_pack_weight(w, None, N, K, fmad.FMT_FP8, ptr, s_w)
+            del w
+            for M in (1, 10, 50, 63):
+                a = torch.randint(0, 0x70, (M, K), dtype=torch.uint8, device=device)
+                x = torch.randn(M, N, device=device)
+                q = torch.empty((M, N), dtype=torch.uint8, device=device)
+                bias, gate, scale, shift = f32(N, 0.01), f32(N, 0.1), f32(N, 0.1), f32(N, 0.0)
+                s_a, s_q = f32(1, 0.02), f32(1, 0.05)
+                for s in (1, 2, 4, 8, 16):
+                    row = {"M": M, "K": K, "N": N, "s": s}
+                    try:
+                        sb = fmad.gemm_consumer_scratch_bytes(M, N, K, fmad.FMT_FP8, s)
+                    except fmad.FmError as e:
+                        row["skipped"] = str(e).split(":")[-1].strip()[:80]
+                        rows.append(row)
+                        continue
+                    scratch = torch.empty(max(sb // 4, 1), dtype=torch.float32, device=device)
+                    launches = [lambda st, ptr=ptr: fmad.fm_gemm_consumer(a, M, K, ptr, N, fmad.FMT_FP8, s, s_a, s_w,
+                                                                          bias, x, gate, scale, shift, 1e-6, s_q, q,
+                                                                          scratch, sb, st)
+                                for ptr in ptrs] * max(1, 24 // copies)
+                    us = time_graph(device, launches, replays=3)
+                    algo = K * N + M * K + 9 * M * N + 16 * N
+                    gbs = algo / (us * 1e-6) / 1e9
+                    row.update({"us": round(us, 3), "algorithmic_bytes": algo, "gbs": round(gbs, 1),
+                                "frac": round(gbs / peak, 4)})
+                    rows.append(row)
+            del pool
+            torch.cuda.empty_cache()
+    done = [r for r in rows if "us" in r]
+    best = max(done, key=lambda r: r["frac"])
+    return {"protocol": "skinny GEMM + fused consumer sweep (FP8)", "points": len(rows), "measured": len(done),
+            "peak_gbs": peak, "peak_kind": peak_kind_note(kind), "best": best, "rows": rows}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -581,11 +706,21 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")
     ap.add_argument("--profile-case", action="store_true",
                     help="run only the small 1-layer, 1-step case for ncu (profiler range on its 2nd decision)")
+    ap.add_argument("--layer-protocol", action="store_true",
+                    help="run only the single-layer protocol (M = 10, rotating weight copies > 2x L2)")
+    ap.add_argument("--gemm-sweep", action="store_true",
+                    help="run only the skinny GEMM + fused consumer sweep (240 points)")
     ap.add_argument("--bf16-protocol", action="store_true",
                     help="run only the matched 16-bit persistence protocol (100 decisions, refresh every 5th)")
     args = ap.parse_args()
     if args.bf16_protocol:
         print(json.dumps(run_bf16_protocol(args)), flush=True)
+        return
+    if args.layer_protocol:
+        print(json.dumps(run_layer_protocol(args)), flush=True)
+        return
+    if args.gemm_sweep:
+        print(json.dumps(run_gemm_sweep(args)), flush=True)
         return
     if args.profile_case:
         profile_case(args.workload)

@@ -522,7 +522,9 @@ int attn_plan(int M, int P, int* kc, int* nsplit) {
 
 size_t attn_smem_bytes(int kc, int nsplit, int fp8) { return 1024 + smem_plan(kc, nsplit, fp8 != 0).total; }
 
-cudaError_t attn_configure() {
+namespace {
+
+cudaError_t attn_configure_impl() {
   const void* ks[6] = {reinterpret_cast<const void*>(attn_kernel<64, false>),
                        reinterpret_cast<const void*>(attn_kernel<128, false>),
                        reinterpret_cast<const void*>(attn_kernel<192, false>),
@@ -535,6 +537,10 @@ cudaError_t attn_configure() {
   }
   return cudaSuccess;
 }
+
+}  // namespace
+
+cudaError_t attn_configure() { return configure_once(2, attn_configure_impl); }
 
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   KParams p;

@@ -25,6 +25,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -513,7 +514,22 @@ cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
 }
 
-cudaError_t gemm_configure() {
+cudaError_t configure_once(int family, cudaError_t (*fn)()) {
+  static std::atomic<uint64_t> done[4];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (family < 0 || family >= 4 || dev >= 64) return fn();
+  const uint64_t bit = 1ull << dev;
+  if (done[family].load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess) done[family].fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+namespace {
+
+cudaError_t gemm_configure_impl() {
   const void* ks[8] = {reinterpret_cast<const void*>(skinny_gemm_kernel<true, 1>),
                        reinterpret_cast<const void*>(skinny_gemm_kernel<true, 2>),
                        reinterpret_cast<const void*>(skinny_gemm_kernel<true, 4>),
@@ -528,6 +544,10 @@ cudaError_t gemm_configure() {
   }
   return cudaSuccess;
 }
+
+}  // namespace
+
+cudaError_t gemm_configure() { return configure_once(0, gemm_configure_impl); }
 
 cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw,

@@ -412,7 +412,9 @@ bool nvfp4_tmap_act(CUtensorMap* map, const void* a, const Nvfp4Shape& g) {
                            static_cast<uint32_t>(g.n_pad), static_cast<uint32_t>(g.chunk));
 }
 
-cudaError_t nvfp4_configure() { return allow_max_dynamic_smem(reinterpret_cast<const void*>(nvfp4_gemm_kernel)); }
+cudaError_t nvfp4_configure() {
+  return configure_once(1, [] { return allow_max_dynamic_smem(reinterpret_cast<const void*>(nvfp4_gemm_kernel)); });
+}
 
 cudaError_t nvfp4_gemm_launch(const CUtensorMap& tmA, const void* wpk, const Nvfp4Shape& g, float* out,
                               __half* out_geglu, const float* sa, const float* sw, const float* sq, int* err,

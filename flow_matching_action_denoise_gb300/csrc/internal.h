@@ -53,6 +53,8 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // Largest dynamic shared memory `kernel` may request on the current device (the
 // opt-in per-block maximum minus the kernel's static shared memory); sets it.
 cudaError_t allow_max_dynamic_smem(const void* kernel, size_t* granted = nullptr);
+// Run a kernel family's one-time attribute setup (family 0..3) once per device.
+cudaError_t configure_once(int family, cudaError_t (*fn)());
 
 // ---------------------------------------------------------------- tensor maps
 // 2-D tensor map over a row-major [outer][inner] array of 1- or 2-byte elements,
