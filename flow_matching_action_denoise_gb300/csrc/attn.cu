@@ -14,9 +14,9 @@
 // contractions run on tcgen05 tensor cores with bf16 operands in shared memory
 // (K-major, 128-byte swizzle, the layout TMA writes) and fp32 accumulators in
 // TMEM: S = Q K^T (M = 128 rows, N = slice keys, K = 128 head dims), then
-// O = P V (N = 128 head dims, K = slice keys) with V held transposed. Two warps
+// O = P V (N = 128 head dims, K = slice keys) with V held transposed. Four warps
 // share each TMEM lane quarter (32 rows) and split the slice's keys, so the softmax
-// needs no shuffles: pass 1 reads S, takes each row half's max m_h and keeps
+// needs no shuffles: pass 1 reads S, takes each row part's max m_h and keeps
 // exp(s - m_h) in registers with its sum; the cluster exchanges the (max, sum)
 // pairs through distributed shared memory so every CTA normalises with the global
 // max M and sum L; pass 2 forms P = exp(s - m_h) * exp(m_h - M) / L, rounds it to
@@ -36,13 +36,14 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 256;        // 8 warps: two per TMEM lane quarter, splitting each row's keys
+constexpr int kThreads = 512;        // 16 warps: four per TMEM lane quarter, splitting each row's keys
+constexpr int kParts = kThreads / 128;   // warps (key parts) per TMEM lane quarter
 constexpr int kRows = 128;           // stacked query rows per CTA (MMA M)
 constexpr int kDh = 128;             // head dim
 constexpr int kMaxSplit = 8;         // portable cluster size
 constexpr int kMaxKc = 192;          // keys per slice (MMA N of QK^T), multiple of 64
 constexpr int kTile = kRows * 128;   // bytes of one [128 rows][128 B] swizzled block
-static_assert(kThreads == 2 * kDh, "two threads per head-dim row of V^T");
+static_assert(kThreads % kDh == 0, "whole threads per head-dim row of V^T");
 
 struct KParams {
   const __nv_bfloat16* qkv;    // [M][ldq]
@@ -84,21 +85,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 32 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  float a[16], b[16];
-  tmem_ld16(taddr, a);
-  tmem_ld16(taddr + 16, b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[i] = a[i];
-    v[16 + i] = b[i];
-  }
-}
-
 // Shared-memory plan of one CTA (byte offsets from the 1024-aligned base).
 struct SmemPlan {
-  size_t q, k, vt, pm, recv, stats, part, bar, total;
+  size_t q, k, vt, pm, stage, recv, stats, part, bar, total;
 };
 // Operand tiles: Q [128 rows][Dh] (bf16: two 128-byte blocks, E4M3: one); K [kc keys][Dh]
 // likewise; V^T and P in blocks of [128][128 bytes] along the keys (bf16: kc/64 blocks of
@@ -114,20 +103,33 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8) {
   const size_t main_end = s.pm + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
   const int rows_per = (kRows + nsplit - 1) / nsplit;
   const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * kDh * 4;
-  // the O receive buffer reuses Q and K (dead once every CTA passed the statistics
-  // exchange) when they are large enough, else it follows the operand tiles
-  s.recv = recv_bytes <= s.vt ? 0 : (main_end + 1023) / 1024 * 1024;
-  size_t end = recv_bytes <= s.vt ? main_end : s.recv + recv_bytes;
+  const size_t stage_bytes = static_cast<size_t>(kRows) * kDh * 4;
+  size_t end = main_end;
+  // this CTA's O share is staged in V^T and P (dead once P V completed) when they are
+  // large enough; the O receive buffer reuses Q and K (dead once every CTA passed the
+  // statistics exchange) when they are large enough; else each follows the tiles
+  if (main_end - s.vt >= stage_bytes) {
+    s.stage = s.vt;
+  } else {
+    s.stage = (end + 1023) / 1024 * 1024;
+    end = s.stage + stage_bytes;
+  }
+  if (recv_bytes <= s.vt) {
+    s.recv = 0;
+  } else {
+    s.recv = (end + 1023) / 1024 * 1024;
+    end = s.recv + recv_bytes;
+  }
   s.stats = (end + 15) / 16 * 16;                            // [kMaxSplit][128] float2
-  s.part = s.stats + static_cast<size_t>(kMaxSplit) * kRows * 8;   // [2][128] float2
-  s.bar = s.part + 2 * kRows * 8;
+  s.part = s.stats + static_cast<size_t>(kMaxSplit) * kRows * 8;   // [kParts][128] float2
+  s.bar = s.part + static_cast<size_t>(kParts) * kRows * 8;
   s.total = s.bar + 64;
   return s;
 }
 
 template <int KC, bool kF8>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
-  constexpr int kHalf = KC / 2;                 // keys of the slice handled by one thread of a row
+  constexpr int kPart = KC / kParts;            // keys of the slice handled by one thread of a row
   constexpr int kBlk = kF8 ? (KC + 127) / 128 : KC / 64;   // key blocks of the P V contraction
   constexpr int kKcp = kF8 ? kBlk * 128 : KC;   // keys of the P V contraction (E4M3: zero padded)
   constexpr int kRowChunks = kF8 ? 8 : 16;      // 16-byte chunks of one Dh-wide row
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + sp.bar);   // S done, O done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
   float2* sStats = reinterpret_cast<float2*>(smem + sp.stats);  // [rank][row] (slice max, slice sum)
-  float2* sPart = reinterpret_cast<float2*>(smem + sp.part);    // [half][row]
+  float2* sPart = reinterpret_cast<float2*>(smem + sp.part);    // [part][row]
   float* recv = reinterpret_cast<float*>(smem + sp.recv);       // [rank][local row][128]
   __shared__ int s_abort;
 
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int g = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
+  const int quarter = warp & 3, part = warp >> 2;
   const int nkeys = p.P + p.M;
   const int t0 = split * KC;
   const int nvalid = min(KC, nkeys - t0);
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   if constexpr (kF8) {   // E4M3: 16 keys per 16-byte group; the padding keys [KC, kKcp) are zero
     const int d = tid & (kDh - 1);
     const uint8_t* vrow = p.vtpre8 + (static_cast<size_t>(g) * kDh + d) * p.p16;
-    for (int grp = tid >> 7; grp < kKcp / 16; grp += 2) {
+    for (int grp = tid >> 7; grp < kKcp / 16; grp += kThreads / kDh) {
       const int t = t0 + grp * 16;
       const uint32_t dst = sVta + (grp >> 3) * kTile + swz(d, grp & 7);
       if (grp * 16 < KC && t < p.P)
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   } else {
     const int d = tid & (kDh - 1);
     const __nv_bfloat16* vrow = p.vtpre + (static_cast<size_t>(g) * kDh + d) * p.p_pad;
-    for (int grp = tid >> 7; grp < KC / 8; grp += 2) {
+    for (int grp = tid >> 7; grp < KC / 8; grp += kThreads / kDh) {
       const int t = t0 + grp * 8;
       const uint32_t dst = sVta + (grp >> 3) * kTile + swz(d, grp & 7);
       if (t < p.P)
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     const int d = tid & (kDh - 1);
     if constexpr (kF8) {
       const uint8_t* vstage = smem + sp.pm;
-      for (int t = c_lo + (tid >> 7); t < c_hi; t += 2) {
+      for (int t = c_lo + (tid >> 7); t < c_hi; t += kThreads / kDh) {
         const int key = t - t0;
         const uint32_t v = vstage[(t - c_lo) * kDh + d];
         const uint32_t addr = sVta + (key >> 7) * kTile + swz(d, (key & 127) >> 4) + (key & 15);
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
     } else {
       const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
-      for (int t = c_lo + (tid >> 7); t < c_hi; t += 2) {
+      for (int t = c_lo + (tid >> 7); t < c_hi; t += kThreads / kDh) {
         const int key = t - t0, grp = key >> 3;
         const uint16_t v = vstage[(t - c_lo) * kDh + d];
         const uint32_t addr = sVta + (grp >> 3) * kTile + swz(d, grp & 7) + (key & 7) * 2;
@@ -296,38 +298,44 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
 
   const int r = quarter * 32 + lane;   // this thread's row == its TMEM lane
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  const int c0 = half * kHalf;         // this thread's keys: [c0, c0 + kHalf) of the slice
+  const int c0 = part * kPart;         // this thread's keys: [c0, c0 + kPart) of the slice
   // log2(e) / sqrt(Dh), times the E4M3 codes' dequantisation fp32(s_q * s_k)
   const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh)) *
                        (kF8 ? __fmul_rn(p.s_qkv[0], p.s_qkv[1]) : 1.0f);
 
-  // ---- pass 1: this row-half's scores (kept in registers), max and sum of exp
-  float sv[kHalf];
+  // ---- pass 1: this row part's scores (kept in registers), max and sum of exp
+  float sv[kPart];
 #pragma unroll
-  for (int c = 0; c < kHalf; c += 32) {
-    float v[32];
-    tmem_ld32(t_row + static_cast<uint32_t>(c0 + c), v);
+  for (int c = 0; c < kPart; c += 16) {
+    float v[16];
+    tmem_ld16(t_row + static_cast<uint32_t>(c0 + c), v);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) sv[c + e] = c0 + c + e < nvalid ? v[e] * kscale : -INFINITY;
+    for (int e = 0; e < 16; ++e) sv[c + e] = c0 + c + e < nvalid ? v[e] * kscale : -INFINITY;
   }
   float mh = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < kHalf; ++e) mh = fmaxf(mh, sv[e]);
-  // sv <- exp(s - m_half): the only exponentials of the row; pass 2 rescales them
+  for (int e = 0; e < kPart; ++e) mh = fmaxf(mh, sv[e]);
+  // sv <- exp(s - m_part): the only exponentials of the row; pass 2 rescales them
   float lh = 0.f;
 #pragma unroll
-  for (int e = 0; e < kHalf; ++e) {
+  for (int e = 0; e < kPart; ++e) {
     sv[e] = mh > -INFINITY ? exp2f(sv[e] - mh) : 0.f;
     lh += sv[e];
   }
-  sPart[half * kRows + r] = make_float2(mh, lh);
+  sPart[part * kRows + r] = make_float2(mh, lh);
   __syncthreads();
   // the slice statistics of row r, pushed to every CTA of the cluster (slot = own rank)
   cluster_wait();   // every peer has started: its shared memory exists
-  if (half == 0) {
-    const float2 a = sPart[r], b = sPart[kRows + r];
-    const float m = fmaxf(a.x, b.x);
-    const float l = (a.y > 0.f ? a.y * exp2f(a.x - m) : 0.f) + (b.y > 0.f ? b.y * exp2f(b.x - m) : 0.f);
+  if (part == 0) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) m = fmaxf(m, sPart[q * kRows + r].x);
+    float l = 0.f;
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) {
+      const float2 st = sPart[q * kRows + r];
+      l += st.y > 0.f ? st.y * exp2f(st.x - m) : 0.f;
+    }
     const uint32_t rank = cluster_rank();
     const uint32_t off = smem_u32(sStats + rank * kRows + r);
     for (int q = 0; q < p.nsplit; ++q) {
@@ -345,13 +353,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   }
   const float ginv = 1.0f / gsum;
 
-  // ---- pass 2: P = bf16(exp(s - m_half) * exp(m_half - M) / L) into the swizzled A
+  // ---- pass 2: P = bf16(exp(s - m_part) * exp(m_part - M) / L) into the swizzled A
   // operand of P V
   const float fscale = mh > -INFINITY ? exp2f(mh - gmax) * ginv : 0.f;
   if constexpr (kF8) {
     // E4M3 probabilities with static scale 1/448: code = E4M3(P * 448), 16 keys per chunk
 #pragma unroll
-    for (int ch = 0; ch < kHalf / 16; ++ch) {
+    for (int ch = 0; ch < kPart / 16; ++ch) {
       const int key = c0 + ch * 16;
       uint32_t w[4];
 #pragma unroll
@@ -367,13 +375,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
       st_shared_v4(sPa + (key >> 7) * kTile + swz(r, (key & 127) >> 4), make_uint4(w[0], w[1], w[2], w[3]));
     }
-    for (int j = half; j < (kKcp - KC) / 16; j += 2) {   // the zero-padded keys [KC, kKcp)
+    for (int j = part; j < (kKcp - KC) / 16; j += kParts) {   // the zero-padded keys [KC, kKcp)
       const int key = KC + j * 16;
       st_shared_v4(sPa + (key >> 7) * kTile + swz(r, (key & 127) >> 4), make_uint4(0, 0, 0, 0));
     }
   } else {
 #pragma unroll
-    for (int ch = 0; ch < kHalf / 8; ++ch) {   // 8-key chunks of 16 bytes
+    for (int ch = 0; ch < kPart / 8; ++ch) {   // 8-key chunks of 16 bytes
       const int key = c0 + ch * 8;
       float pv[8];
 #pragma unroll
@@ -410,23 +418,36 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   tc_fence_after();
   __syncwarp();
 
-  // ---- this slice's share of O (already normalised by the global sum), pushed to
-  // the rank that finalises row r: rows are split into bands of rows_per
+  // ---- this slice's share of O (already normalised by the global sum) goes row by
+  // row to the CTA that finalises it (rows are split into bands of rows_per). TMEM
+  // gives each thread one row, so the share is first staged row-major in shared
+  // memory (16-byte chunks swizzled by row: conflict-free), then each warp pushes
+  // whole 512-byte rows with contiguous remote stores.
   {
-    const int R = qt * kRows + r;
-    const int owner = r / rows_per, lr = r - owner * rows_per;
-    const uint32_t rank = cluster_rank();
-    const uint32_t dst = map_dsmem(smem_u32(recv + ((rank * rows_per + lr) * kDh + half * 64)),
-                                   static_cast<uint32_t>(owner));
+    constexpr int kCols = kDh / kParts;   // O columns read by one thread
+    const uint32_t stage = base + static_cast<uint32_t>(sp.stage);
 #pragma unroll
-    for (int c = 0; c < 64; c += 32) {
-      float v[32];
-      tmem_ld32(t_row + static_cast<uint32_t>(KC + half * 64 + c), v);
-      if (R < p.G * p.M) {
+    for (int c = 0; c < kCols; c += 16) {
+      float v[16];
+      tmem_ld16(t_row + static_cast<uint32_t>(KC + part * kCols + c), v);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          st_dsmem_v4(dst + static_cast<uint32_t>((c + e) * 4), make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]));
+      for (int e = 0; e < 16; e += 4) {
+        const int chunk = (part * kCols + c + e) >> 2;   // 16-byte chunk (0..31) of the row
+        st_shared_v4(stage + r * 512 + ((chunk ^ (r & 7)) << 4),
+                     make_uint4(__float_as_uint(v[e]), __float_as_uint(v[e + 1]), __float_as_uint(v[e + 2]),
+                                __float_as_uint(v[e + 3])));
       }
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t rank = cluster_rank();
+    for (int row = warp; row < kRows; row += kThreads / 32) {
+      if (qt * kRows + row >= p.G * p.M) break;   // padding rows (none after a padding row)
+      const int owner = row / rows_per, lr = row - owner * rows_per;
+      const float4 v = *reinterpret_cast<const float4*>(smem + sp.stage + row * 512 + ((lane ^ (row & 7)) << 4));
+      st_dsmem_v4(map_dsmem(smem_u32(recv + (rank * rows_per + lr) * kDh + lane * 4), static_cast<uint32_t>(owner)),
+                  v);
     }
   }
   cluster_sync_all();   // every share of this CTA's rows has landed

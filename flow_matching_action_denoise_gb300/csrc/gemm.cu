@@ -34,7 +34,7 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // 8 warps: two per TMEM lane quarter in the epilogue
 constexpr int kTileN = 128;                      // weight rows per CTA (MMA M)
 constexpr int kBlockBytes = 128;                 // K bytes per pipeline block (one swizzle row)
 constexpr int kMaxStages = 8;
@@ -204,8 +204,10 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   tc_fence_after();
   __syncthreads();
   const bool abort = s_abort != 0;
-  const int n_local = warp * 32 + lane;   // TMEM lane == weight row within the tile
-  const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  // warps w and w + 4 share TMEM lane quarter w % 4 and take alternate 16-column chunks
+  const int quarter = warp & 3, colset = warp >> 2;
+  const int n_local = quarter * 32 + lane;   // TMEM lane == weight row within the tile
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int rank = kCs > 1 ? static_cast<int>(cluster_rank()) : 0;
   const uint32_t recv_base = smem_u32(recv);
   uint32_t peer[kCs];
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
               static_cast<uint32_t>((rank * rows_per * kTileN + n_local) * 4);
   if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
   __syncwarp();                  // tcgen05.ld is warp-collective
-  for (int c = 0; c < p.n_pad; c += 16) {
+  for (int c = colset * 16; c < p.n_pad; c += 32) {
     float v[16];
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
 #pragma unroll

@@ -169,7 +169,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
         break;
       }
       mbar_arrive_expect_tx(&b_full[slot], b_stage);
-      tma_load_3d(b_tiles + static_cast<size_t>(slot) * b_stage, &tmA, &b_full[slot], 0, 0, kb0 + st * C, pol_a);
+      if (C == 1)   // a plain 2-D box when a stage holds one K block (the 3-D view measured slower)
+        tma_load_2d(b_tiles + static_cast<size_t>(slot) * b_stage, &tmA, &b_full[slot], (kb0 + st) * kKb, 0, pol_a);
+      else
+        tma_load_3d(b_tiles + static_cast<size_t>(slot) * b_stage, &tmA, &b_full[slot], 0, 0, kb0 + st * C, pol_a);
       ++act_issued;
       const int ns = st + R;   // refill the raw slot stage st occupied
       if (ns < nst) {
@@ -408,6 +411,9 @@ int nvfp4_plan(int M, int N, int K, int s, Nvfp4Shape* g) {
 }
 
 bool nvfp4_tmap_act(CUtensorMap* map, const void* a, const Nvfp4Shape& g) {
+  if (g.chunk == 1)
+    return make_tmap_2d(map, a, 2, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M), kKb,
+                        static_cast<uint32_t>(g.n_pad));
   return make_tmap_kblocks(map, a, 2, static_cast<uint64_t>(g.K), static_cast<uint64_t>(g.M),
                            static_cast<uint32_t>(g.n_pad), static_cast<uint32_t>(g.chunk));
 }
