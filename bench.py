@@ -149,6 +149,10 @@ def run_ours(args, rank, world, local_rank):
                                                 flags=fmad.FLAG_USE_GRAPH),
                     "eager_pdl": fmad.Policy(cfg, act_scales=scales, weights=weights, device=device,
                                              flags=fmad.FLAG_USE_PDL)}
+        if cfg.weight_fmt != "nvfp4":   # the other consumer placement: inside the GEMMs
+            variants["graph_pdl_fused_consumers"] = fmad.Policy(
+                cfg, act_scales=scales, weights=weights, device=device,
+                flags=fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | fmad.FLAG_FUSED_CONSUMERS)
     del weights
     torch.cuda.empty_cache()
     kp, vp = fm_synth.prefix_kv(cfg)
@@ -604,7 +608,10 @@ def run_layer_protocol(args):
     conds = fm_synth.step_conds(cfg)
     scales = np.tile(np.loadtxt(os.path.join(ROOT, "tests", "golden", "act_scales_layer_fp8_m10.txt"),
                                 ndmin=2).astype(np.float32), (R, 1))
-    pol = fmad.Policy(cfg, [layer] * R, fm_synth.final_weights(cfg), act_scales=scales, conds=conds, device=device)
+    flags = fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | (fmad.FLAG_FUSED_CONSUMERS if args.fused_consumers else 0)
+    pol = fmad.Policy(cfg, [layer] * R, fm_synth.final_weights(cfg), act_scales=scales, conds=conds, device=device,
+                      flags=flags)
+    kernels_per_layer = fmad.kernel_count(pol.handle)[0]
     kp, vp = fm_synth.prefix_kv(cfg)
     pol.set_prefix_kv(torch.from_numpy(kp).to(device, torch.bfloat16), torch.from_numpy(vp).to(device, torch.bfloat16))
     noise = torch.from_numpy(fm_synth.noise(cfg, 0)).to(device)
@@ -629,7 +636,8 @@ def run_layer_protocol(args):
     return {"protocol": "single layer, rotating weight copies", "workload": base.name, "copies": R,
             "bytes_per_layer": int(per_layer), "us_per_layer": round(us, 3), "achieved_gbs": round(gbs, 1),
             "peak_gbs": peak, "frac": round(gbs / peak, 4), "peak_kind": peak_kind_note(kind),
-            "kernels_per_layer": 7, "steps": args.steps, "clocks": clocks.summary()}
+            "kernels_per_layer": kernels_per_layer, "fused_consumers": bool(args.fused_consumers),
+            "steps": args.steps, "clocks": clocks.summary()}
 
 
 def run_gemm_sweep(args):
@@ -706,6 +714,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")
     ap.add_argument("--profile-case", action="store_true",
                     help="run only the small 1-layer, 1-step case for ncu (profiler range on its 2nd decision)")
+    ap.add_argument("--fused-consumers", action="store_true",
+                    help="with --layer-protocol: run the consumers inside the GEMMs")
     ap.add_argument("--layer-protocol", action="store_true",
                     help="run only the single-layer protocol (M = 10, rotating weight copies > 2x L2)")
     ap.add_argument("--gemm-sweep", action="store_true",

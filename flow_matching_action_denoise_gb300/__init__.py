@@ -19,7 +19,7 @@ __all__ = [
     "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status",
     "kernel_count", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
     "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "named_buffer", "Policy", "DeviceWeights",
-    "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "COND_TIME", "COND_GIVEN",
+    "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "FLAG_FUSED_CONSUMERS", "COND_TIME", "COND_GIVEN",
     "ABI_VERSION", "STATUS",
 ]
 
@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(PKG, "libfmad.so")
 
 ABI_VERSION = 2
 FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
-FLAG_USE_GRAPH, FLAG_USE_PDL = 1, 2
+FLAG_USE_GRAPH, FLAG_USE_PDL, FLAG_FUSED_CONSUMERS = 1, 2, 4
 COND_TIME, COND_GIVEN = 0, 1
 STATUS = {0: "FM_OK", 1: "FM_ERR_INVALID_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_ALIGN",
           4: "FM_ERR_WORKSPACE", 5: "FM_ERR_CUDA", 6: "FM_ERR_STATE_MISMATCH",

@@ -58,6 +58,18 @@ struct KParams {
   int nkb_total, nkb_cta;
   int n_pad, stages, cs, chunk;
   int* err;
+  // kMode 1 (residual epilogue; cs == s): x[m][n] += gate[n] * (sum * fp32(sa * sw)) for the
+  // rows and columns this CTA finalises, and ssq[nt][m] = the tile's sum of x_new^2.
+  // kMode 2 (normalising prologue): the activation operand of the CTA's K range is built
+  // here from x: q = Q(x * rsqrt(sum_t ssq[t][m] / K + eps) * (1 + scale) + shift).
+  float* x;
+  const float* gate;
+  float* ssq;
+  const float* scale;
+  const float* shift;
+  const float* sqa;   // static scale of q (FP8 operands)
+  float eps;
+  void* q_out;        // kMode 2: n-tile 0 also stores its K range of q here
 };
 
 __host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
@@ -68,7 +80,7 @@ __host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-template <bool kFp8, int kCs>
+template <bool kFp8, int kCs, int kMode>
 __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                const KParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -108,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     }
     mbar_init(done, 1);
     fence_mbar_init();
-    tma_prefetch_desc(&tmA);
+    if (kMode != 2) tma_prefetch_desc(&tmA);
   }
   if (warp == 0) {
     __syncwarp();
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   tc_fence_after();
   if (kCs > 1) cluster_arrive_relaxed();   // paired with the wait before the first remote store
   const uint32_t tmem = *tmem_slot;
-  const float ds = (p.out_bf16 || p.out_geglu || p.out_qkv8) ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
+  const float ds = (p.out_bf16 || p.out_geglu || p.out_qkv8 || kMode == 1) ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
   float rs_qkv[3] = {1.0f, 1.0f, 1.0f};
   if (p.out_qkv8)
     for (int i = 0; i < 3; ++i) rs_qkv[i] = 1.0f / p.s_qkv[i];
@@ -132,7 +144,18 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const int kb0 = j * p.nkb_cta;
   const int nst = p.nkb_cta / chunk;   // pipeline stages to run (chunk divides nkb_cta)
 
-  if (threadIdx.x == 0) {
+  if (kMode == 2 && threadIdx.x == 0) {
+    // ---------------- producer: only the weights (the whole K range fits in the stages);
+    // the activation operand is built by all threads below
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint8_t* wsrc = p.wpk + (static_cast<size_t>(nt) * p.nkb_total + kb0) * kWTileBytes;
+    for (int i = 0; i < nst; ++i) {
+      mbar_arrive_expect_tx(&full[i], w_stage_bytes);
+      bulk_load(w_tiles + static_cast<size_t>(i) * w_stage_bytes, wsrc + static_cast<size_t>(i) * w_stage_bytes,
+                w_stage_bytes, &full[i], pol_w);
+    }
+    s_issued = nst;
+  } else if (kMode != 2 && threadIdx.x == 0) {
     // ---------------- producer: per stage one bulk copy of chunk weight tiles (contiguous
     // in the packed layout) and one 3-D box of chunk activation K blocks
     const uint64_t pol_w = l2_policy_evict_first();
@@ -165,7 +188,101 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       ++issued;
     }
     s_issued = issued;
-  } else if (threadIdx.x == 32) {
+  }
+  if constexpr (kMode == 2) {
+    // ---------------- normalising prologue: AdaRMSNorm + static quantise of x into the
+    // swizzled K-major operand tiles of this CTA's K range (blog post, section "Static
+    // quantisation": the input-dependent RMS is computed at run time, gamma folded into W).
+    // Thread t owns 16-byte chunk t % nchunk of every row (t / nchunk + i * rstep).
+    constexpr int kEb = kFp8 ? 1 : 2;
+    constexpr int kPerChunk = 16 / kEb;   // elements per 16-byte chunk
+    const int K = p.nkb_total * (kBlockBytes / kEb);
+    const int k_lo = kb0 * (kBlockBytes / kEb);
+    const int nchunk = p.nkb_cta * (kBlockBytes / 16);
+    const int ci = static_cast<int>(threadIdx.x) % nchunk;
+    const int rstep = kThreads / nchunk;
+    const int k0 = k_lo + ci * kPerChunk;
+    float sc[kPerChunk], sh[kPerChunk];   // per-create constants: fetched before the wait
+#pragma unroll
+    for (int e = 0; e < kPerChunk; e += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(p.scale + k0 + e);
+      const float4 b = *reinterpret_cast<const float4*>(p.shift + k0 + e);
+      sc[e] = 1.f + a.x; sc[e + 1] = 1.f + a.y; sc[e + 2] = 1.f + a.z; sc[e + 3] = 1.f + a.w;
+      sh[e] = b.x; sh[e + 1] = b.y; sh[e + 2] = b.z; sh[e + 3] = b.w;
+    }
+    const float rs = kFp8 ? 1.0f / *p.sqa : 1.0f;
+    __shared__ float s_rr[256];
+    pdl_wait();   // x and its tile sums are written by the previous kernel
+    if (static_cast<int>(threadIdx.x) < p.M) {
+      const int ntile = K / kTileN;
+      float ss = 0.f;
+      int t = 0;
+      for (; t + 4 <= ntile; t += 4) {   // independent loads in flight together
+        const float a = p.ssq[t * p.M + threadIdx.x], b = p.ssq[(t + 1) * p.M + threadIdx.x];
+        const float c = p.ssq[(t + 2) * p.M + threadIdx.x], d = p.ssq[(t + 3) * p.M + threadIdx.x];
+        ss += a;
+        ss += b;
+        ss += c;
+        ss += d;
+      }
+      for (; t < ntile; ++t) ss += p.ssq[t * p.M + threadIdx.x];
+      s_rr[threadIdx.x] = rsqrtf(ss / static_cast<float>(K) + p.eps);
+    }
+    __syncthreads();
+    const int kbl = ci / (kBlockBytes / 16), c16 = ci % (kBlockBytes / 16);   // K block within the range, chunk
+    uint8_t* tile = a_tiles + static_cast<size_t>(kbl / chunk) * a_stage_bytes + (kbl % chunk) * a_tile_bytes;
+    // rows in batches of kBatch, their x loads issued together (the loads are the latency)
+    constexpr int kBatch = kFp8 ? 4 : 8;
+    for (int m0 = static_cast<int>(threadIdx.x) / nchunk; m0 < p.n_pad; m0 += kBatch * rstep) {
+      float4 xv[kBatch][kPerChunk / 4];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int m = m0 + b * rstep;
+        const float* xr = p.x + static_cast<size_t>(m < p.M ? m : 0) * K + k0;
+#pragma unroll
+        for (int e = 0; e < kPerChunk / 4; ++e)
+          xv[b][e] = m < p.M ? *reinterpret_cast<const float4*>(xr + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int m = m0 + b * rstep;
+        if (m >= p.n_pad) break;
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (m < p.M) {
+          const float rr = s_rr[m];
+          float h[kPerChunk];
+#pragma unroll
+          for (int e = 0; e < kPerChunk / 4; ++e) {
+            h[4 * e] = fmaf(xv[b][e].x * rr, sc[4 * e], sh[4 * e]);
+            h[4 * e + 1] = fmaf(xv[b][e].y * rr, sc[4 * e + 1], sh[4 * e + 1]);
+            h[4 * e + 2] = fmaf(xv[b][e].z * rr, sc[4 * e + 2], sh[4 * e + 2]);
+            h[4 * e + 3] = fmaf(xv[b][e].w * rr, sc[4 * e + 3], sh[4 * e + 3]);
+          }
+          uint32_t* w = &u.x;
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              w[q] = static_cast<uint32_t>(__nv_cvt_float_to_fp8(h[4 * q] * rs, __NV_SATFINITE, __NV_E4M3)) |
+                     (static_cast<uint32_t>(__nv_cvt_float_to_fp8(h[4 * q + 1] * rs, __NV_SATFINITE, __NV_E4M3)) << 8) |
+                     (static_cast<uint32_t>(__nv_cvt_float_to_fp8(h[4 * q + 2] * rs, __NV_SATFINITE, __NV_E4M3)) << 16) |
+                     (static_cast<uint32_t>(__nv_cvt_float_to_fp8(h[4 * q + 3] * rs, __NV_SATFINITE, __NV_E4M3)) << 24);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(h[2 * q], h[2 * q + 1]);
+              w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+          }
+          if (nt == 0 && p.q_out)
+            *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.q_out) + (static_cast<size_t>(m) * K + k0) * kEb) = u;
+        }
+        st_shared_v4(smem_u32(tile) + static_cast<uint32_t>(m * 128 + ((c16 ^ (m & 7)) << 4)), u);
+      }
+    }
+    fence_async_smem();   // generic-proxy writes -> tensor-core reads
+    __syncthreads();
+  }
+  if (threadIdx.x == 32) {
     // ---------------- MMA issuer
     const uint32_t idesc = make_idesc(kFp8, kTileN, static_cast<uint32_t>(p.n_pad));
     for (int st = 0; st < nst; ++st) {
@@ -303,6 +420,20 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
         u.x = *reinterpret_cast<const uint32_t*>(&lo);
         u.y = *reinterpret_cast<const uint32_t*>(&hi);
         *reinterpret_cast<uint2*>(p.out_bf16 + static_cast<size_t>(m) * p.N + col) = u;
+      } else if (kMode == 1) {
+        // gated residual on the finished sum, and this tile's share of the row's sum of squares
+        const float4 g = *reinterpret_cast<const float4*>(p.gate + col);
+        float4* xp = reinterpret_cast<float4*>(p.x + static_cast<size_t>(m) * p.N + col);
+        float4 xv = *xp;
+        xv.x = fmaf(g.x, acc.x * ds, xv.x);
+        xv.y = fmaf(g.y, acc.y * ds, xv.y);
+        xv.z = fmaf(g.z, acc.z * ds, xv.z);
+        xv.w = fmaf(g.w, acc.w * ds, xv.w);
+        *xp = xv;
+        float ssq = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+        if (lane == 0) p.ssq[static_cast<size_t>(nt) * p.M + m] = ssq;
       } else {
         *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(part) * p.M + m) * p.N + col) = acc;
       }
@@ -531,20 +662,44 @@ cudaError_t configure_once(int family, cudaError_t (*fn)()) {
 
 namespace {
 
-cudaError_t gemm_configure_impl() {
-  const void* ks[8] = {reinterpret_cast<const void*>(skinny_gemm_kernel<true, 1>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 2>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 4>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 8>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 1>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 2>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 4>),
-                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 8>)};
+template <int kMode>
+cudaError_t configure_mode() {
+  const void* ks[8] = {reinterpret_cast<const void*>(skinny_gemm_kernel<true, 1, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 2, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 4, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 8, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 1, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 2, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 4, kMode>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 8, kMode>)};
   for (const void* k : ks) {
     const cudaError_t e = allow_max_dynamic_smem(k);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t gemm_configure_impl() {
+  cudaError_t e = configure_mode<0>();
+  if (e == cudaSuccess) e = configure_mode<1>();
+  if (e == cudaSuccess) e = configure_mode<2>();
+  return e;
+}
+
+template <int kMode>
+cudaError_t launch_mode(const GemmShape& g, dim3 grid, const LaunchOpts& lo, const CUtensorMap& tmA, const KParams& p) {
+  const dim3 blk(kThreads);
+  switch (g.cs * 2 + (g.fp8 ? 1 : 0)) {
+    case 3: return launch(skinny_gemm_kernel<true, 1, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 5: return launch(skinny_gemm_kernel<true, 2, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 9: return launch(skinny_gemm_kernel<true, 4, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 17: return launch(skinny_gemm_kernel<true, 8, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 2: return launch(skinny_gemm_kernel<false, 1, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 4: return launch(skinny_gemm_kernel<false, 2, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 8: return launch(skinny_gemm_kernel<false, 4, kMode>, grid, blk, g.smem, lo, tmA, p);
+    case 16: return launch(skinny_gemm_kernel<false, 8, kMode>, grid, blk, g.smem, lo, tmA, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -554,7 +709,7 @@ cudaError_t gemm_configure() { return configure_once(0, gemm_configure_impl); }
 cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw,
                         void* out_geglu, int geglu_fp8, const float* sq, uint8_t* out_qkv8, const float* s_qkv,
-                        int nq, int nk) {
+                        int nq, int nk, const GemmFuse* fuse) {
   if ((out_bf16 || out_geglu || out_qkv8) && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
   if (out_qkv8 && (!s_qkv || nq % 128 || nk % 128)) return cudaErrorInvalidValue;
   if (out_geglu && (!sq || g.N % 128)) return cudaErrorInvalidValue;
@@ -580,21 +735,34 @@ cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape
   p.cs = g.cs;
   p.chunk = g.chunk;
   p.err = err;
+  const int mode = fuse ? fuse->mode : 0;
+  p.x = fuse ? fuse->x : nullptr;
+  p.gate = fuse ? fuse->gate : nullptr;
+  p.ssq = fuse ? fuse->ssq : nullptr;
+  p.scale = fuse ? fuse->scale : nullptr;
+  p.shift = fuse ? fuse->shift : nullptr;
+  p.sqa = fuse ? fuse->sqa : nullptr;
+  p.eps = fuse ? fuse->eps : 0.f;
+  p.q_out = fuse ? fuse->q_out : nullptr;
+  if (mode == 1 && (g.cs != g.s || !p.x || !p.gate || !p.ssq || !sa || !sw || out_bf16 || out_geglu || out_qkv8))
+    return cudaErrorInvalidValue;
+  if (mode == 2 && (!gemm_mode2_ok(g) || !p.x || !p.ssq || !p.scale || !p.shift || (g.fp8 && !p.sqa)))
+    return cudaErrorInvalidValue;
+  if (mode == 0 && !out && !out_bf16 && !out_geglu && !out_qkv8) return cudaErrorInvalidValue;
   LaunchOpts lo = o;
   lo.cluster = dim3(1, static_cast<unsigned>(g.cs), 1);
   const dim3 grid(static_cast<unsigned>(g.N / kTileN), static_cast<unsigned>(g.s), 1);
-  const dim3 blk(kThreads);
-  switch (g.cs * 2 + (g.fp8 ? 1 : 0)) {
-    case 3: return launch(skinny_gemm_kernel<true, 1>, grid, blk, g.smem, lo, tmA, p);
-    case 5: return launch(skinny_gemm_kernel<true, 2>, grid, blk, g.smem, lo, tmA, p);
-    case 9: return launch(skinny_gemm_kernel<true, 4>, grid, blk, g.smem, lo, tmA, p);
-    case 17: return launch(skinny_gemm_kernel<true, 8>, grid, blk, g.smem, lo, tmA, p);
-    case 2: return launch(skinny_gemm_kernel<false, 1>, grid, blk, g.smem, lo, tmA, p);
-    case 4: return launch(skinny_gemm_kernel<false, 2>, grid, blk, g.smem, lo, tmA, p);
-    case 8: return launch(skinny_gemm_kernel<false, 4>, grid, blk, g.smem, lo, tmA, p);
-    case 16: return launch(skinny_gemm_kernel<false, 8>, grid, blk, g.smem, lo, tmA, p);
+  switch (mode) {
+    case 0: return launch_mode<0>(g, grid, lo, tmA, p);
+    case 1: return launch_mode<1>(g, grid, lo, tmA, p);
+    case 2: return launch_mode<2>(g, grid, lo, tmA, p);
     default: return cudaErrorInvalidValue;
   }
+}
+
+bool gemm_mode2_ok(const GemmShape& g) {
+  const int nchunk = g.nkb_cta * (kBlockBytes / 16);
+  return g.nkb_cta / g.chunk <= g.stages && nchunk <= kThreads && kThreads % nchunk == 0 && g.M <= 256;
 }
 
 size_t packed_weight_bytes(int N, int K, int fmt) {

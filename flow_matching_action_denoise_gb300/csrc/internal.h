@@ -90,13 +90,32 @@ bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
 // epilogue applies m = gelu_tanh(g) * u to the dequantised sums and writes Q(m, *sq)
 // as [M][N/2] codes (E4M3 bytes if geglu_fp8, else bf16).
 // wpk: packed weight tiles (1024-byte aligned, fm_pack_weight layout).
+// Row work fused into a skinny GEMM. mode 1 (epilogue, requires cs == s): the gated
+// residual x[m][n] += gate[n] * (sum * fp32(sa * sw)) on the finished sums, and
+// ssq[n / 128][m] = that 128-column tile's sum of the new x^2 (no partial planes).
+// mode 2 (prologue, the whole K range in the stages: gemm_mode2_ok): the activation
+// operand is built from x [M][K] instead of loaded: Q(x * rsqrt(sum_t ssq[t][m] / K +
+// eps) * (1 + scale) + shift), E4M3 with 1/sqa or bf16; the first n-tile's CTAs also
+// store their K range of it in q_out [M][K].
+struct GemmFuse {
+  int mode = 0;
+  float* x = nullptr;
+  const float* gate = nullptr;
+  float* ssq = nullptr;
+  const float* scale = nullptr;
+  const float* shift = nullptr;
+  const float* sqa = nullptr;
+  float eps = 0.f;
+  void* q_out = nullptr;
+};
+bool gemm_mode2_ok(const GemmShape& g);
 // out_qkv8 (requires cs == s): E4M3 codes of the dequantised product with the static
 // scales s_qkv[0..2] for columns [0, nq), [nq, nq + nk), [nq + nk, N) (Q, K, V).
 cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16 = nullptr, const float* sa = nullptr,
                         const float* sw = nullptr, void* out_geglu = nullptr, int geglu_fp8 = 0,
                         const float* sq = nullptr, uint8_t* out_qkv8 = nullptr, const float* s_qkv = nullptr,
-                        int nq = 0, int nk = 0);
+                        int nq = 0, int nk = 0, const GemmFuse* fuse = nullptr);
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
 // ---------------------------------------------------------------- NVFP4-weight GEMM
@@ -172,6 +191,10 @@ struct RowArgs {
   void* q;
   int q_fp8;
   float eps;
+  // per-tile sums of squares for a following normalising GEMM prologue: the row's sum
+  // of x^2 (after the head, if any) into ssq[0][m], zeros into ssq[1..ssq_tiles-1][m]
+  float* ssq;
+  int ssq_tiles;
 };
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o);
 

@@ -51,6 +51,7 @@ struct Layout {
                  // E4M3 codes with FP8 attention)
   size_t kcache8, vcache8;   // FP8 attention: E4M3 copies of the prefix cache
   size_t kv8_bytes, v8_bytes, ascale_bytes;
+  size_t ssq;   // [d/128][M] per-tile sums of squares of x (consumers inside the GEMMs)
   size_t y[4];
   size_t err, amax, conds;
   size_t kv_bytes, a_bytes, scale_bytes;
@@ -68,13 +69,17 @@ struct Derived {
   int nvfp4;
   int q_store;   // quantised operand storage: 0 bf16, 1 E4M3 codes, 2 E4M3 codes as f16 values
   int attn_fp8;  // attention on E4M3 Q, K, V and probabilities
+  // FP8/BF16: the consumers run inside the GEMMs - the O and down GEMM epilogues apply
+  // the gated residual and emit per-tile sums of squares, the QKV and gate|up GEMMs
+  // build their normalised, quantised operand in a prologue (5 kernels per layer)
+  int rowfuse;
   fm::GemmShape gs[4];
   fm::Nvfp4Shape ns[4];
   int gN[4], gK[4];
   int attn_kc, attn_nsplit;
   // fp32 partial planes GEMM g writes (its K-slices not reduced in the GEMM itself)
-  int nparts(int g) const { return nvfp4 ? ns[g].s : gs[g].s / gs[g].cs; }
-  int kernels_per_layer() const { return nvfp4 ? 8 : 7; }
+  int nparts(int g) const { return nvfp4 ? ns[g].s : (rowfuse && (g == 1 || g == 3)) ? 0 : gs[g].s / gs[g].cs; }
+  int kernels_per_layer() const { return nvfp4 ? 8 : rowfuse ? 5 : 7; }
 };
 
 int num_sms() {
@@ -149,6 +154,7 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
   dv->nvfp4 = c->weight_fmt == FM_FMT_NVFP4;
   dv->q_store = dv->nvfp4 ? fm::kQFp8AsF16 : dv->fp8;
   dv->attn_fp8 = c->attn_fmt == FM_FMT_FP8;
+  dv->rowfuse = 0;
   dv->act_bytes = dv->q_store == 1 ? 1 : 2;
   const int N[4] = {dv->nqkv, c->d, 2 * c->F, c->d};
   const int K[4] = {c->d, c->H * c->Dh, c->d, c->F};
@@ -207,6 +213,33 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
     *why = "P + M keys exceed the attention plan's 8 slices x 192 keys";
     return FM_ERR_SHAPE;
   }
+  // Consumers inside the GEMMs: the O and down GEMMs must finish every K slice in one
+  // cluster (split = cluster <= 8) and the QKV and gate|up GEMMs must hold their whole
+  // K range in shared memory; automatic splits are adjusted to get there.
+  if (c->flags & FM_FLAG_FUSED_CONSUMERS) {
+    fm::GemmShape cand[4] = {dv->gs[0], dv->gs[1], dv->gs[2], dv->gs[3]};
+    bool ok = true;
+    for (int g = 0; g < 4 && ok; ++g) {
+      const int nkb = K[g] * dv->act_bytes / 128;
+      int s = cand[g].s;
+      if (g == 1 || g == 3) {
+        if (c->ksplit[g] <= 0)
+          while (s > 8 || (s & (s - 1)) || nkb % s) --s;
+        ok = s == cluster_for(s) && s <= 8 &&
+             fm::gemm_plan(c->M, N[g], K[g], dv->fp8, s, cluster_for(s), &cand[g]) == FM_OK;
+      } else {
+        while (!fm::gemm_mode2_ok(cand[g]) && c->ksplit[g] <= 0 && s * 2 <= 8 && nkb % (s * 2) == 0) {
+          s *= 2;
+          if (fm::gemm_plan(c->M, N[g], K[g], dv->fp8, s, cluster_for(s), &cand[g]) != FM_OK) break;
+        }
+        ok = fm::gemm_mode2_ok(cand[g]);
+      }
+    }
+    if (ok) {
+      for (int g = 0; g < 4; ++g) dv->gs[g] = cand[g];
+      dv->rowfuse = 1;
+    }
+  }
   return FM_OK;
 }
 
@@ -249,6 +282,7 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.kcache8 = ly.take(ly.kv8_bytes);
   ly.vcache8 = ly.take(ly.v8_bytes);
   ly.err = ly.take(64);
+  ly.ssq = ly.take(static_cast<size_t>(c->d / 128) * M * sizeof(float));
   ly.amax = ly.take(64);
   ly.conds = ly.take(static_cast<size_t>(S) * d * sizeof(double));
   return ly;
@@ -389,7 +423,19 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
     if (e != cudaSuccess) return e;        \
   } while (0)
   FM_REC(p->at<void>(p->ly.x), xbytes);
-  FM_REC(p->at<void>(p->ly.q), static_cast<size_t>(c.M) * c.d * ab);
+  if (!dv.rowfuse) FM_REC(p->at<void>(p->ly.q), static_cast<size_t>(c.M) * c.d * ab);
+  float* ssq = p->at<float>(p->ly.ssq);
+  // consumers inside the GEMMs: the QKV GEMM normalises and quantises x itself
+  fm::GemmFuse fq;
+  fq.mode = 2;
+  fq.x = p->at<float>(p->ly.x);
+  fq.ssq = ssq;
+  fq.scale = p->mod(k, l, 0);
+  fq.shift = p->mod(k, l, 1);
+  fq.sqa = p->ascale(l, FM_SITE_ATTN_IN);
+  fq.eps = c.rms_eps;
+  fq.q_out = p->at<void>(p->ly.q);
+  const fm::GemmFuse* fqp = dv.rowfuse ? &fq : nullptr;
 
   // QKV: the epilogue dequantises and rounds to bf16, the operand attention reads
   // (NVFP4: partial planes, reduced and rounded by a separate kernel)
@@ -402,12 +448,14 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   } else if (dv.attn_fp8) {   // E4M3 Q | K | V codes with their static scales
     e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, nullptr,
                         p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), nullptr, 0, nullptr,
-                        reinterpret_cast<uint8_t*>(qkvb), p->ascale(l, FM_SITE_Q), c.H * c.Dh, c.Hkv * c.Dh);
+                        reinterpret_cast<uint8_t*>(qkvb), p->ascale(l, FM_SITE_Q), c.H * c.Dh, c.Hkv * c.Dh, fqp);
   } else {
-    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, qkvb, p->ascale(l, FM_SITE_ATTN_IN),
-                        p->wscale(l, 0));
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, qkvb,
+                        p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), nullptr, 0, nullptr, nullptr, nullptr, 0, 0,
+                        fqp);
   }
   if (e != cudaSuccess) return e;
+  if (dv.rowfuse) FM_REC(p->at<void>(p->ly.q), static_cast<size_t>(c.M) * c.d * ab);
   FM_REC(qkvb, dv.attn_fp8 ? ybytes[0] / 2 : ybytes[0]);
 
   fm::AttnArgs at;
@@ -438,9 +486,21 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   if (e != cudaSuccess) return e;
   FM_REC(p->at<void>(p->ly.o), static_cast<size_t>(c.M) * c.H * c.Dh * ab);
 
-  e = dv.nvfp4 ? fm::nvfp4_gemm_launch(p->tmA[1], p->at<void>(p->ly.wpk[l * 4 + 1]), dv.ns[1], y[1], nullptr, nullptr,
-                                       nullptr, nullptr, err, o)
-               : fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 1]), p->tmA[1], dv.gs[1], y[1], err, o);
+  // consumers inside the GEMMs: the O GEMM applies the gated residual itself
+  fm::GemmFuse fo;
+  fo.mode = 1;
+  fo.x = p->at<float>(p->ly.x);
+  fo.gate = p->mod(k, l, 2);
+  fo.ssq = ssq;
+  if (dv.nvfp4)
+    e = fm::nvfp4_gemm_launch(p->tmA[1], p->at<void>(p->ly.wpk[l * 4 + 1]), dv.ns[1], y[1], nullptr, nullptr, nullptr,
+                              nullptr, err, o);
+  else if (dv.rowfuse)
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 1]), p->tmA[1], dv.gs[1], nullptr, err, o, nullptr,
+                        p->ascale(l, FM_SITE_ATTN_OUT), p->wscale(l, 1), nullptr, 0, nullptr, nullptr, nullptr, 0, 0,
+                        &fo);
+  else
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 1]), p->tmA[1], dv.gs[1], y[1], err, o);
   if (e != cudaSuccess) return e;
   FM_REC(y[1], ybytes[1]);
 
@@ -460,24 +520,41 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   r1.q = p->at<void>(p->ly.q2);
   r1.q_fp8 = fp8;
   r1.eps = c.rms_eps;
-  e = fm::row_launch(r1, o);
-  if (e != cudaSuccess) return e;
+  if (!dv.rowfuse) {
+    e = fm::row_launch(r1, o);
+    if (e != cudaSuccess) return e;
+  }
   FM_REC(p->at<void>(p->ly.x), xbytes);
-  FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
+  if (!dv.rowfuse) FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
+  fm::GemmFuse fg = fq;   // the gate|up GEMM normalises and quantises with the pre-MLP norm
+  fg.scale = p->mod(k, l, 3);
+  fg.shift = p->mod(k, l, 4);
+  fg.sqa = p->ascale(l, FM_SITE_MLP_IN);
+  fg.q_out = p->at<void>(p->ly.q2);
 
   // gate|up: the epilogue applies GeGLU and quantises, writing the down GEMM's operand
   if (dv.nvfp4)
     e = fm::nvfp4_gemm_launch(p->tmA[2], p->at<void>(p->ly.wpk[l * 4 + 2]), dv.ns[2], nullptr, p->at<__half>(p->ly.mc),
                               p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->ascale(l, FM_SITE_GEGLU), err, o);
   else
-    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 2]), p->tmA[2], dv.gs[2], nullptr, err, o, nullptr, p->ascale(l, FM_SITE_MLP_IN),
-                        p->wscale(l, 2), p->at<void>(p->ly.mc), fp8, p->ascale(l, FM_SITE_GEGLU));
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 2]), p->tmA[2], dv.gs[2], nullptr, err, o, nullptr,
+                        p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->at<void>(p->ly.mc), fp8,
+                        p->ascale(l, FM_SITE_GEGLU), nullptr, nullptr, 0, 0, dv.rowfuse ? &fg : nullptr);
   if (e != cudaSuccess) return e;
+  if (dv.rowfuse) FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
   FM_REC(p->at<void>(p->ly.mc), static_cast<size_t>(c.M) * c.F * ab);
 
-  e = dv.nvfp4 ? fm::nvfp4_gemm_launch(p->tmA[3], p->at<void>(p->ly.wpk[l * 4 + 3]), dv.ns[3], y[3], nullptr, nullptr,
-                                       nullptr, nullptr, err, o)
-               : fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 3]), p->tmA[3], dv.gs[3], y[3], err, o);
+  fm::GemmFuse fd = fo;   // the down GEMM applies the MLP's gated residual itself
+  fd.gate = p->mod(k, l, 5);
+  if (dv.nvfp4)
+    e = fm::nvfp4_gemm_launch(p->tmA[3], p->at<void>(p->ly.wpk[l * 4 + 3]), dv.ns[3], y[3], nullptr, nullptr, nullptr,
+                              nullptr, err, o);
+  else if (dv.rowfuse)
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 3]), p->tmA[3], dv.gs[3], nullptr, err, o, nullptr,
+                        p->ascale(l, FM_SITE_GEGLU), p->wscale(l, 3), nullptr, 0, nullptr, nullptr, nullptr, 0, 0,
+                        &fd);
+  else
+    e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 3]), p->tmA[3], dv.gs[3], y[3], err, o);
   if (e != cudaSuccess) return e;
   FM_REC(y[3], ybytes[3]);
 
@@ -519,8 +596,18 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
       r2.sq = p->ascale(0, FM_SITE_ATTN_IN);
     }
   }
-  e = fm::row_launch(r2, o);
-  if (e != cudaSuccess) return e;
+  if (dv.rowfuse) {
+    // the down GEMM already applied the residual; a step boundary still needs the
+    // Euler tail (and the next step's head, whose x the next QKV GEMM normalises)
+    r2.parts = nullptr;
+    r2.do_quant = 0;
+    r2.ssq = ssq;
+    r2.ssq_tiles = c.d / 128;
+  }
+  if (!dv.rowfuse || step_end) {
+    e = fm::row_launch(r2, o);
+    if (e != cudaSuccess) return e;
+  }
   FM_REC(p->at<void>(p->ly.x), xbytes);
   FM_REC(p->at<void>(p->ly.a), p->ly.a_bytes);
 #undef FM_REC
@@ -555,6 +642,11 @@ cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
   r.q = p->at<void>(p->ly.q);
   r.q_fp8 = p->dv.q_store;
   r.eps = c.rms_eps;
+  if (p->dv.rowfuse) {   // the first QKV GEMM normalises x itself: hand it the row sums
+    r.do_quant = 0;
+    r.ssq = p->at<float>(p->ly.ssq);
+    r.ssq_tiles = c.d / 128;
+  }
   return fm::row_launch(r, o);
 }
 
@@ -862,6 +954,7 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
   h = fnv(h, &base, sizeof base);
   for (int g = 0; g < 4; ++g) h = fnv(h, &dv.gs[g], sizeof(fm::GemmShape));
   for (int g = 0; g < 4; ++g) h = fnv(h, &dv.ns[g], sizeof(fm::Nvfp4Shape));
+  h = fnv(h, &dv.rowfuse, sizeof(int));
   h = fnv(h, &dv.attn_kc, sizeof(int));
   p->plan_hash = h;
 
@@ -1108,7 +1201,7 @@ int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trac
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) {
   if (!p || !per_layer || !per_decision) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
   *per_layer = p->dv.kernels_per_layer();
-  *per_decision = 1 + p->cfg.S * p->cfg.L * p->dv.kernels_per_layer();
+  *per_decision = 1 + p->cfg.S * p->cfg.L * p->dv.kernels_per_layer() + (p->dv.rowfuse ? p->cfg.S : 0);
   return FM_OK;
 }
 
@@ -1256,8 +1349,28 @@ int fm_test_layer(fm_policy* p, const float* x_in, int layer, int step, float* x
   r.q = p->at<void>(p->ly.q);
   r.q_fp8 = p->dv.q_store;
   r.eps = p->cfg.rms_eps;
+  if (p->dv.rowfuse) {   // the QKV GEMM normalises x itself: hand it the row sums instead
+    r.do_quant = 0;
+    r.ssq = p->at<float>(p->ly.ssq);
+    r.ssq_tiles = p->cfg.d / 128;
+  }
   FM_CUDA(p, fm::row_launch(r, o));
   FM_CUDA(p, enqueue_layer(p, layer, step, false, o));
+  if (p->dv.rowfuse) {   // the next layer's pre-attention operand, as a separate consumer computes it
+    fm::RowArgs n = {};
+    const int ln = (layer + 1) % p->cfg.L;
+    n.M = p->cfg.M;
+    n.N = p->cfg.d;
+    n.x = p->at<float>(p->ly.x);
+    n.do_quant = 1;
+    n.scale = p->mod(step, ln, 0);
+    n.shift = p->mod(step, ln, 1);
+    n.sq = p->ascale(ln, FM_SITE_ATTN_IN);
+    n.q = p->at<void>(p->ly.q);
+    n.q_fp8 = p->dv.q_store;
+    n.eps = p->cfg.rms_eps;
+    FM_CUDA(p, fm::row_launch(n, o));
+  }
   const size_t xb = static_cast<size_t>(p->cfg.M) * p->cfg.d * 4;
   FM_CUDA(p, cudaMemcpyAsync(x_out, p->at<void>(p->ly.x), xb, cudaMemcpyDeviceToDevice, s));
   FM_CUDA(p, cudaMemcpyAsync(q_out, p->at<void>(p->ly.q), static_cast<size_t>(p->cfg.M) * p->cfg.d * p->dv.act_bytes,

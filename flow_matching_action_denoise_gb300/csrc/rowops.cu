@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
 
   // ---- residual update (skipped when the step head recomputes x from the actions)
   float ss = 0.f;
-  const bool load_x = r.parts || r.x_src || !r.do_head;
+  const bool load_x = r.parts || r.x_src || !r.do_head || r.do_tail;
   for (int c = tid; load_x && c < n4; c += kRowThreads) {
     float4 x = *reinterpret_cast<const float4*>(xin + c * 4);
     if (r.parts) {
@@ -208,6 +208,12 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
       *reinterpret_cast<float4*>(xrow + c * 4) = x;
       ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
     }
+  }
+
+  // ---- the row's sum of squares for a normalising GEMM prologue
+  if (r.ssq) {
+    const float tot = block_sum(ss, red);
+    if (tid < r.ssq_tiles) r.ssq[static_cast<size_t>(tid) * r.M + m] = tid == 0 ? tot : 0.f;
   }
 
   // ---- AdaRMSNorm + static-scale quantisation into the next GEMM's operand

@@ -68,7 +68,16 @@ typedef enum fm_format {
 
 enum {
   FM_FLAG_USE_GRAPH = 1u,  /* replay the whole decision as one CUDA graph */
-  FM_FLAG_USE_PDL = 2u     /* launch every kernel with Programmatic Dependent Launch */
+  FM_FLAG_USE_PDL = 2u,    /* launch every kernel with Programmatic Dependent Launch */
+  /* FP8/BF16: run the consumers inside the GEMMs (5 kernels per layer instead of 7): the
+   * O and down GEMM epilogues apply the gated residual and emit per-tile sums of squares
+   * of x, the QKV and gate|up GEMMs normalise and quantise x in a prologue. Off by
+   * default: every CTA of those GEMMs re-reads the fp32 x of its K range, which at M = 50
+   * costs more than the two kernel boundaries it removes. Taken only where the shapes
+   * allow it (the O and down GEMMs reduce every K slice in one cluster of <= 8, the QKV
+   * and gate|up GEMMs hold their K range in one stage); otherwise, and for NVFP4, the
+   * flag is ignored: fm_kernel_count reports the placement in use. */
+  FM_FLAG_FUSED_CONSUMERS = 4u
 };
 
 enum {

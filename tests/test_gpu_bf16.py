@@ -62,8 +62,8 @@ class Bf16Expert:
             k[:, :IMAGE_ROWS], v[:, :IMAGE_ROWS] = self.refresh_rows(version)
         return k, v
 
-    def policy(self, decision=0):
-        p = fmad.Policy(self.cfg, weights=self.weights)
+    def policy(self, decision=0, flags=fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL):
+        p = fmad.Policy(self.cfg, weights=self.weights, flags=flags)
         k, v = self.prefix_at(decision)
         p.set_prefix_kv(dev(k, self.device, torch.bfloat16), dev(v, self.device, torch.bfloat16))
         return p
@@ -93,6 +93,7 @@ def run(bf16):
     torch.cuda.synchronize()
     assert fmad.device_status(pol.handle) == 0
     per_layer, per_decision = fmad.kernel_count(pol.handle)
+    # QKV, attention, O, residual + norm, gate|up (+ GeGLU), down, residual + norm
     assert (per_layer, per_decision) == (7, 1 + 18 * 10 * 7)
     pol.close()
     return out
@@ -112,20 +113,24 @@ def test_decision_bf16_vs_oracle(bf16, run, decision):
     assert err <= 2 * envelope(decision), (decision, err, envelope(decision))
 
 
-def test_decision_bf16_every_stage_vs_oracle(bf16, run):
+@pytest.mark.parametrize("fused", [False, True])
+def test_decision_bf16_every_stage_vs_oracle(bf16, run, fused):
     """Teacher-forced parity of every kernel of all 180 layer-steps of decision 5
     (just after a refresh): fp32 outputs within 1e-5 * RMS, bf16 operands within one
     bf16 step. Attention outputs are accumulated from bf16-rounded probabilities over
-    838 keys, so up to 1% of them may sit one bf16 step apart."""
+    838 keys, so up to 1% of them may sit one bf16 step apart. Both consumer
+    placements (own kernels, inside the GEMMs)."""
     cfg = bf16.cfg
-    pol = bf16.policy(5)
+    pol = bf16.policy(5, fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | (fmad.FLAG_FUSED_CONSUMERS if fused else 0))
+    assert fmad.kernel_count(pol.handle)[0] == (5 if fused else 7)
     nbytes = fmad.trace_size(pol.handle)
     trace = torch.empty(nbytes, dtype=torch.uint8, device=bf16.device)
     nz = fm_synth.noise(cfg, 5)
     act = torch.empty((cfg.M, cfg.A), dtype=torch.float32, device=bf16.device)
     fmad.decode_trace(pol.handle, dev(nz, bf16.device), act, trace, nbytes)
     assert fmad.device_status(pol.handle) == 0
-    assert torch.equal(act.cpu(), run[5])
+    if not fused:
+        assert torch.equal(act.cpu(), run[5])
     recs = parse_trace(trace.cpu().numpy(), cfg, pol)
     k, v = bf16.prefix_at(5)
     last = check_decision_stages(cfg, bf16.oracle(), recs, nz, k, v, None, attn_max_frac=1e-2)

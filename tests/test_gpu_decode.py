@@ -35,7 +35,8 @@ def device():
 
 # ---------------------------------------------------------------- single layer (M = 10)
 
-def test_single_layer_vs_oracle(device):
+@pytest.mark.parametrize("fused", [False, True])
+def test_single_layer_vs_oracle(device, fused):
     cfg = fm_synth.config("layer_fp8_m10")
     layers = [fm_synth.layer_weights(cfg, 0)]
     final = fm_synth.final_weights(cfg)
@@ -46,7 +47,8 @@ def test_single_layer_vs_oracle(device):
     model = O.Model(cfg, layers, final, conds)
     x_ref, q_ref, _ = O.single_layer(model, x, kp, vp, scales)
 
-    pol = fmad.Policy(cfg, layers, final, act_scales=scales, conds=conds)
+    flags = fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | (fmad.FLAG_FUSED_CONSUMERS if fused else 0)
+    pol = fmad.Policy(cfg, layers, final, act_scales=scales, conds=conds, flags=flags)
     pol.set_prefix_kv(dev(kp, device, torch.bfloat16), dev(vp, device, torch.bfloat16))
     xin = dev(x, device)
     xout = torch.empty_like(xin)
@@ -60,7 +62,7 @@ def test_single_layer_vs_oracle(device):
     dist = code_step_distance(q.cpu().numpy(), C.e4m3_encode_code(q_ref))
     assert np.max(dist) <= 1 and np.mean(dist > 0) <= 1e-2
     per_layer, per_decision = fmad.kernel_count(pol.handle)
-    assert per_layer == 7 and per_decision == 1 + 7
+    assert (per_layer, per_decision) == ((5, 1 + 5 + 1) if fused else (7, 1 + 7))
     pol.close()
 
 
@@ -105,28 +107,32 @@ def test_decision_fp8_end_to_end_within_oracle_envelope(expert):
     by `env` (tests/golden/make_fp8_envelope.py) when only its pre-quantisation values
     are rounded to fp32. The GPU must stay within twice that envelope; the
     stage-by-stage test below pins every kernel tightly."""
-    pol = expert.policy()
     nz = fm_synth.noise(expert.cfg, 0)
-    act = pol.decode(dev(nz, expert.device))
-    torch.cuda.synchronize()
-    assert fmad.device_status(pol.handle) == 0
-    got = act.cpu().numpy().astype(np.float64)
     ref = O.decode(expert.oracle(), nz, expert.kp, expert.vp, expert.scales)
     env = float(np.loadtxt(os.path.join(GOLDEN, "fp8_envelope_expert_fp8_m50.txt")))
-    err = np.max(np.abs(got - ref)) / np.sqrt(np.mean(ref ** 2))
-    assert err <= 2 * env, (err, env)
-    per_layer, per_decision = fmad.kernel_count(pol.handle)
-    assert (per_layer, per_decision) == (7, 1 + 18 * 10 * 7)
-    pol.close()
+    base = fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL
+    # consumers as their own kernels (default) and inside the GEMMs (5 kernels per layer
+    # plus one step-boundary kernel per step)
+    for flags, counts in [(base, (7, 1 + 18 * 10 * 7)), (base | fmad.FLAG_FUSED_CONSUMERS, (5, 1 + 18 * 10 * 5 + 10))]:
+        pol = expert.policy(flags)
+        act = pol.decode(dev(nz, expert.device))
+        torch.cuda.synchronize()
+        assert fmad.device_status(pol.handle) == 0
+        got = act.cpu().numpy().astype(np.float64)
+        err = np.max(np.abs(got - ref)) / np.sqrt(np.mean(ref ** 2))
+        assert err <= 2 * env, (flags, err, env)
+        assert fmad.kernel_count(pol.handle) == counts
+        pol.close()
 
 
-def test_decision_fp8_every_stage_vs_oracle(expert):
+@pytest.mark.parametrize("fused", [False, True])
+def test_decision_fp8_every_stage_vs_oracle(expert, fused):
     """Teacher-forced parity of every kernel of all 180 layer-steps: each recorded
     output equals the oracle's stage applied to the GPU's own recorded input -
     fp32 outputs within 1e-5 * RMS, quantised codes within one E4M3 step with at
     most 0.1% near-tie differences."""
     cfg, model = expert.cfg, expert.oracle()
-    pol = expert.policy()
+    pol = expert.policy(fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | (fmad.FLAG_FUSED_CONSUMERS if fused else 0))
     nbytes = fmad.trace_size(pol.handle)
     trace = torch.empty(nbytes, dtype=torch.uint8, device=expert.device)
     nz = fm_synth.noise(cfg, 0)
