@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   // kernel: fetch them before waiting for it.
   const float ds = r.parts ? __fmul_rn(*r.sa, *r.sw) : 0.f;
   const float rs_q = (r.do_quant && r.q_fp8) ? 1.0f / *r.sq : 1.0f;
-  constexpr int kPre = 2;   // column groups per thread kept in registers (N <= 2048)
+  constexpr int kPre = 2;   // column groups per thread kept in registers (N <= 2048); the
+                            // selects below name both explicitly (static register indices)
   float4 gate_v[kPre], scale_v[kPre], shift_v[kPre];
 #pragma unroll
   for (int u = 0; u < kPre; ++u) {
@@ -116,17 +117,29 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
     float4 x = *reinterpret_cast<const float4*>(xin + c * 4);
     if (r.parts) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p = 0; p < r.nparts; ++p) {
-        const float4 v = *reinterpret_cast<const float4*>(r.parts + p * plane + static_cast<size_t>(m) * N + c * 4);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+      // planes in groups of four, each group's loads issued together (slots past the
+      // last plane re-read the group's first and are dropped); summed in plane order
+      for (int p0 = 0; p0 < r.nparts; p0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int p = p0 + j < r.nparts ? p0 + j : p0;
+          v[j] = *reinterpret_cast<const float4*>(r.parts + p * plane + static_cast<size_t>(m) * N + c * 4);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (p0 + j < r.nparts) {
+            acc.x += v[j].x;
+            acc.y += v[j].y;
+            acc.z += v[j].z;
+            acc.w += v[j].w;
+          }
+        }
       }
       float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
       if (r.bias) b = *reinterpret_cast<const float4*>(r.bias + c * 4);
       const int u = (c - tid) / kRowThreads;
-      const float4 gt = u < kPre ? gate_v[u] : *reinterpret_cast<const float4*>(r.gate + c * 4);
+      const float4 gt = u == 0 ? gate_v[0] : u == 1 ? gate_v[1] : *reinterpret_cast<const float4*>(r.gate + c * 4);
       x.x = fmaf(gt.x, fmaf(acc.x, ds, b.x), x.x);
       x.y = fmaf(gt.y, fmaf(acc.y, ds, b.y), x.y);
       x.z = fmaf(gt.z, fmaf(acc.z, ds, b.z), x.z);
@@ -153,17 +166,20 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
       hf[1] = fmaf(x.y * rr, 1.f + sc.y, sh.y) * gf.y;
       hf[2] = fmaf(x.z * rr, 1.f + sc.z, sh.z) * gf.z;
       hf[3] = fmaf(x.w * rr, 1.f + sc.w, sh.w) * gf.w;
+      // all A weight loads first (rows past A re-read row 0 and are dropped): loads
+      // under a per-row branch would each wait for the previous one's FMAs
+      uint2 wv[kMaxA];
+#pragma unroll
+      for (int a = 0; a < kMaxA; ++a)
+        wv[a] = *reinterpret_cast<const uint2*>(r.w_out + static_cast<size_t>(a < r.A ? a : 0) * N + c * 4);
 #pragma unroll
       for (int a = 0; a < kMaxA; ++a) {
-        if (a < r.A) {
-          const uint2 wv = *reinterpret_cast<const uint2*>(r.w_out + static_cast<size_t>(a) * N + c * 4);
-          const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wv.x);
-          const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wv.y);
-          acc[a] = fmaf(hf[0], __low2float(w01), acc[a]);
-          acc[a] = fmaf(hf[1], __high2float(w01), acc[a]);
-          acc[a] = fmaf(hf[2], __low2float(w23), acc[a]);
-          acc[a] = fmaf(hf[3], __high2float(w23), acc[a]);
-        }
+        const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wv[a].x);
+        const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wv[a].y);
+        acc[a] = fmaf(hf[0], __low2float(w01), acc[a]);
+        acc[a] = fmaf(hf[1], __high2float(w01), acc[a]);
+        acc[a] = fmaf(hf[2], __low2float(w23), acc[a]);
+        acc[a] = fmaf(hf[3], __high2float(w23), acc[a]);
       }
     }
     const int warp = tid >> 5, lane = tid & 31;
@@ -195,13 +211,38 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
     ss = 0.f;
     for (int c = tid; c < n4; c += kRowThreads) {
       float xv[4];
+      if ((r.A & 7) == 0) {
+        // the four rows' weights as 16-byte loads, all issued before the FMA chains
+        // (blocks past A re-read block 0 and are dropped)
+        uint4 wv[4][kMaxA / 8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int n = c * 4 + i;
-        const __nv_bfloat16* wrow = r.w_in + static_cast<size_t>(n) * r.A;
-        float acc = 0.f;
-        for (int a = 0; a < r.A; ++a) acc = fmaf(sa_vec[a], __bfloat162float(wrow[a]), acc);
-        xv[i] = acc + r.b_in[n];
+        for (int i = 0; i < 4; ++i) {
+          const uint4* wrow = reinterpret_cast<const uint4*>(r.w_in + static_cast<size_t>(c * 4 + i) * r.A);
+#pragma unroll
+          for (int j = 0; j < kMaxA / 8; ++j) wv[i][j] = wrow[j < r.A / 8 ? j : 0];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxA / 8; ++j) {
+            if (j < r.A / 8) {
+              const __nv_bfloat16* w8 = reinterpret_cast<const __nv_bfloat16*>(&wv[i][j]);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc = fmaf(sa_vec[j * 8 + e], __bfloat162float(w8[e]), acc);
+            }
+          }
+          xv[i] = acc + r.b_in[c * 4 + i];
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int n = c * 4 + i;
+          const __nv_bfloat16* wrow = r.w_in + static_cast<size_t>(n) * r.A;
+          float acc = 0.f;
+          for (int a = 0; a < r.A; ++a) acc = fmaf(sa_vec[a], __bfloat162float(wrow[a]), acc);
+          xv[i] = acc + r.b_in[n];
+        }
       }
       const float4 x = make_float4(xv[0], xv[1], xv[2], xv[3]);
       *reinterpret_cast<float4*>(xs + c * 4) = x;
@@ -223,8 +264,8 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
     for (int c = tid; c < n4; c += kRowThreads) {
       const float4 x = *reinterpret_cast<const float4*>(xs + c * 4);
       const int u = (c - tid) / kRowThreads;
-      const float4 sc = u < kPre ? scale_v[u] : *reinterpret_cast<const float4*>(r.scale + c * 4);
-      const float4 sh = u < kPre ? shift_v[u] : *reinterpret_cast<const float4*>(r.shift + c * 4);
+      const float4 sc = u == 0 ? scale_v[0] : u == 1 ? scale_v[1] : *reinterpret_cast<const float4*>(r.scale + c * 4);
+      const float4 sh = u == 0 ? shift_v[0] : u == 1 ? shift_v[1] : *reinterpret_cast<const float4*>(r.shift + c * 4);
       float4 h;
       h.x = fmaf(x.x * rr, 1.f + sc.x, sh.x);
       h.y = fmaf(x.y * rr, 1.f + sc.y, sh.y);

@@ -76,7 +76,7 @@ enum {
    * costs more than the two kernel boundaries it removes. Taken only where the shapes
    * allow it (the O and down GEMMs reduce every K slice in one cluster of <= 8, the QKV
    * and gate|up GEMMs hold their K range in one stage); otherwise, and for NVFP4, the
-   * flag is ignored: fm_kernel_count reports the placement in use. */
+   * flag is ignored: fm_test_kernel_count reports the placement in use. */
   FM_FLAG_FUSED_CONSUMERS = 4u
 };
 
