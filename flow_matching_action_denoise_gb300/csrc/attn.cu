@@ -154,6 +154,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int nvalid = min(KC, nkeys - t0);
   constexpr uint32_t ncols = (KC + kDh) <= 256 ? 256u : 512u;
   const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
+  // static scales (set through the host API, never by a kernel of the decision):
+  // fetched at the start, off the critical path
+  // log2(e) / sqrt(Dh), times the E4M3 codes' dequantisation fp32(s_q * s_k)
+  const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh)) *
+                       (kF8 ? __fmul_rn(p.s_qkv[0], p.s_qkv[1]) : 1.0f);
+  const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
+  const float dv = kF8 ? __fdiv_rn(p.s_qkv[2], 448.0f) : 1.0f;   // E4M3 P and V: fp32(s_v / 448)
 
   if (tid == 0) {
     s_abort = 0;
@@ -299,9 +306,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int r = quarter * 32 + lane;   // this thread's row == its TMEM lane
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int c0 = part * kPart;         // this thread's keys: [c0, c0 + kPart) of the slice
-  // log2(e) / sqrt(Dh), times the E4M3 codes' dequantisation fp32(s_q * s_k)
-  const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh)) *
-                       (kF8 ? __fmul_rn(p.s_qkv[0], p.s_qkv[1]) : 1.0f);
 
   // ---- pass 1: this row part's scores (kept in registers), max and sum of exp
   float sv[kPart];
@@ -456,8 +460,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   if (s_abort == 0) {
     const int rank = static_cast<int>(cluster_rank());
     const int e4 = lane * 4;
-    const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
-    const float dv = kF8 ? __fdiv_rn(p.s_qkv[2], 448.0f) : 1.0f;   // E4M3 P and V: fp32(s_v / 448)
     for (int lr = warp; lr < rows_per; lr += kThreads / 32) {
       const int rr = rank * rows_per + lr;
       const int R = qt * kRows + rr;
