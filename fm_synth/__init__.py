@@ -53,6 +53,7 @@ class Config:
     cond: str = "time"   # "time": sinusoidal t-embedding; "given": cond vector drawn per step
     eps: float = 1e-6
     attn_fmt: str = "bf16"   # "bf16" | "fp8": attention operands (Q, K, V, P)
+    warm_t: float = 0.0      # flow time of the one-step warm start (0: none)
 
     @property
     def n_qkv(self) -> int:

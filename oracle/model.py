@@ -233,7 +233,10 @@ class Model:
             self.mod_w.append((np.asarray(lw["w_mod"], np.float64), np.asarray(lw["b_mod"], np.float64)))
         self.final = {k: np.asarray(v, np.float64) for k, v in final.items()} if final else None
         self.conds = None if conds is None else np.asarray(conds, np.float64)
-        self.mods = [self._step_mods(k) for k in range(cfg.S)]
+        self.mods = [self._mods_for_cond(self.cond(k)) for k in range(cfg.S)]
+        # the one-step warm start's modulation (flow time warm_t) is row S
+        if getattr(cfg, "warm_t", 0.0) > 0:
+            self.mods.append(self.mods_at(warm_time(cfg)))
 
     def cond(self, k: int) -> np.ndarray:
         cfg = self.cfg
@@ -241,11 +244,14 @@ class Model:
             return self.conds[k]
         return time_embedding(1.0 - k / cfg.S, cfg.d)
 
-    def _step_mods(self, k: int):
-        """Modulation of step k: per layer [scale1, shift1, gate1, scale2, shift2, gate2]
-        (each [d], fp32-rounded) and the final [scale_f, shift_f]."""
+    def mods_at(self, t: float):
+        """Modulation at an arbitrary flow time t (time-conditioned models only)."""
+        return self._mods_for_cond(time_embedding(t, self.cfg.d))
+
+    def _mods_for_cond(self, c: np.ndarray):
+        """Modulation for a cond vector: per layer [scale1, shift1, gate1, scale2, shift2,
+        gate2] (each [d], fp32-rounded) and the final [scale_f, shift_f]."""
         d = self.cfg.d
-        c = self.cond(k)
         per_layer = []
         for wm, bm in self.mod_w:
             m = C.fp32(c @ wm.T + bm)
@@ -312,8 +318,9 @@ def pre_attn_quant(model: Model, l: int, k: int, x, act_scales, amax=None):
     return quant_codes(h, s, cfg.act_fmt)
 
 
-def euler_step(model: Model, k: int, a: np.ndarray, kpre, vpre, act_scales, amax=None):
-    """One flow-matching Euler step: a <- a + dt * v(a, t_k), dt = -1/S."""
+def euler_step(model: Model, k: int, a: np.ndarray, kpre, vpre, act_scales, amax=None, dt=None):
+    """One flow-matching Euler step: a <- a + dt * v(a, t_k) with step k's modulation,
+    dt = -1/S unless given."""
     cfg, fin = model.cfg, model.final
     x = np.asarray(a, np.float64) @ fin["w_in"].T + fin["b_in"]
     for l in range(cfg.L):
@@ -322,7 +329,7 @@ def euler_step(model: Model, k: int, a: np.ndarray, kpre, vpre, act_scales, amax
     scf, shf = model.mods[k][1]
     hf = ada_norm(x, scf, shf, cfg.eps) * fin["gamma_f"]
     v = hf @ fin["w_out"].T + fin["b_out"]
-    return a + (-1.0 / cfg.S) * v
+    return a + ((-1.0 / cfg.S) if dt is None else dt) * v
 
 
 def decode(model: Model, noise, kpre, vpre, act_scales, amax=None) -> np.ndarray:
@@ -333,6 +340,40 @@ def decode(model: Model, noise, kpre, vpre, act_scales, amax=None) -> np.ndarray
     for k in range(model.cfg.S):
         a = euler_step(model, k, a, kpre, vpre, act_scales, amax)
     return a
+
+
+def warm_time(cfg) -> float:
+    """The warm start's flow time as the library holds it (an fp32 config field)."""
+    return float(np.float32(cfg.warm_t))
+
+
+def warm_start_input(prev, executed: int, tau: float, noise) -> np.ndarray:
+    """One-step warm start (blog post, section "Few-step denoise brings the error back
+    into consecutive decisions"): the previous chunk moved forward by the number of
+    actions already executed, its tail padded with its last action, then mixed with
+    fresh noise at flow time tau: a_tau = tau * noise + (1 - tau) * shifted."""
+    prev = np.asarray(prev, np.float64)
+    M = prev.shape[0]
+    shifted = prev[np.minimum(np.arange(M) + executed, M - 1)]
+    return tau * np.asarray(noise, np.float64) + (1.0 - tau) * shifted
+
+
+def decode_warm(model: Model, noise, prev, executed: int, kpre, vpre, act_scales, tau=None,
+                amax=None) -> np.ndarray:
+    """The warm-start decision: one Euler step from a_tau (warm_start_input) at flow
+    time tau to t = 0, i.e. dt = -tau, with the modulation at t = tau. tau defaults
+    to the config's warm_t (fp32)."""
+    kpre = np.asarray(kpre, np.float64)
+    vpre = np.asarray(vpre, np.float64)
+    given = tau is not None
+    if not given:
+        tau = warm_time(model.cfg)
+    model.mods.append(model.mods_at(tau) if given else model.mods[model.cfg.S])
+    try:
+        a = warm_start_input(prev, executed, tau, noise)
+        return euler_step(model, len(model.mods) - 1, a, kpre, vpre, act_scales, amax, dt=-tau)
+    finally:
+        model.mods.pop()
 
 
 def calibrate(model: Model, noise, kpre, vpre, provisional_scales) -> np.ndarray:
