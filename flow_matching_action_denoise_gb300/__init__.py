@@ -17,7 +17,7 @@ __all__ = [
     "FmError", "lib", "load", "FmConfig", "make_config", "workspace_size", "policy_create",
     "policy_destroy", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
     "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status",
-    "kernel_count", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
+    "kernel_count", "philox_noise", "decode_actions_seeded", "last_timing", "decode_warm", "episode_reset", "FmTiming", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
     "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "named_buffer", "Policy", "DeviceWeights",
     "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "FLAG_FUSED_CONSUMERS", "COND_TIME", "COND_GIVEN",
     "ABI_VERSION", "STATUS",
@@ -26,7 +26,7 @@ __all__ = [
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfmad.so")
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
 FLAG_USE_GRAPH, FLAG_USE_PDL, FLAG_FUSED_CONSUMERS = 1, 2, 4
 COND_TIME, COND_GIVEN = 0, 1
@@ -40,6 +40,7 @@ EXPORTS = [
     "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight", "fm_test_skinny_gemm",
     "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
     "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer", "fm_gemm_consumer_noalloc",
+    "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
 ]
 
 
@@ -56,7 +57,13 @@ class FmConfig(ctypes.Structure):
                 ("P", ctypes.c_int), ("A", ctypes.c_int),
                 ("weight_fmt", ctypes.c_int), ("act_fmt", ctypes.c_int), ("attn_fmt", ctypes.c_int),
                 ("cond_mode", ctypes.c_int),
-                ("rms_eps", ctypes.c_float), ("ksplit", ctypes.c_int * 4), ("flags", ctypes.c_uint)]
+                ("rms_eps", ctypes.c_float), ("ksplit", ctypes.c_int * 4), ("flags", ctypes.c_uint),
+                ("warm_t", ctypes.c_float)]
+
+
+class FmTiming(ctypes.Structure):
+    _fields_ = [("host_submit_ns", ctypes.c_uint64), ("device_start_ns", ctypes.c_uint64),
+                ("device_end_ns", ctypes.c_uint64)]
 
 
 class FmLayerWeights(ctypes.Structure):
@@ -114,6 +121,11 @@ def load() -> ctypes.CDLL:
         "fm_gemm_consumer_noalloc": (i, [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
                                          vp]),
         "fm_decode_trace": (i, [vp, vp, vp, vp, sz, vp]),
+        "fm_philox_noise": (i, [vp, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
+        "fm_decode_actions_seeded": (i, [vp, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
+        "fm_last_timing": (i, [vp, ctypes.POINTER(FmTiming), vp]),
+        "fm_decode_warm": (i, [vp, vp, i, vp, vp]),
+        "fm_episode_reset": (i, [vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -167,6 +179,7 @@ def make_config(cfg, flags: int = FLAG_USE_GRAPH | FLAG_USE_PDL, ksplit=(0, 0, 0
     for i, s in enumerate(ksplit):
         c.ksplit[i] = int(s)
     c.flags = int(flags)
+    c.warm_t = float(getattr(cfg, "warm_t", 0.0))
     return c
 
 
@@ -215,6 +228,37 @@ def decode_actions_host(p: int, noise_host, actions_host, stream=None):
     """noise_host / actions_host: pinned (or pageable) CPU float32 tensors."""
     _check(load().decode_actions_host(p, _ptr(noise_host), _ptr(actions_host), _stream(stream)),
            "decode_actions_host", p)
+
+
+def philox_noise(out, seed: int, counter: int, raw_words=None, stream=None):
+    """Fill the device float32 tensor `out` with the decision noise of stream
+    (seed, counter); raw_words: None or a device int32/uint32 tensor of
+    ceil(n/4)*4 words receiving the Philox output words."""
+    _check(load().fm_philox_noise(_ptr(out), out.numel(), seed & (2 ** 64 - 1), counter & (2 ** 64 - 1),
+                                  _ptr(raw_words), _stream(stream)), "fm_philox_noise")
+
+
+def decode_actions_seeded(p: int, seed: int, counter: int, actions, stream=None):
+    _check(load().fm_decode_actions_seeded(p, seed & (2 ** 64 - 1), counter & (2 ** 64 - 1), _ptr(actions),
+                                           _stream(stream)), "fm_decode_actions_seeded", p)
+
+
+def decode_warm(p: int, noise, executed: int, actions, stream=None):
+    _check(load().fm_decode_warm(p, _ptr(noise), int(executed), _ptr(actions), _stream(stream)), "fm_decode_warm", p)
+
+
+def episode_reset(p: int):
+    _check(load().fm_episode_reset(p), "fm_episode_reset", p)
+
+
+def last_timing(p: int, stream=None) -> dict:
+    """Timestamps of the last decision: host submit (steady clock, ns) and the GPU
+    globaltimer at its first kernel's start and last kernel's end; t_infer_ns is
+    their difference."""
+    t = FmTiming()
+    _check(load().fm_last_timing(p, ctypes.byref(t), _stream(stream)), "fm_last_timing", p)
+    return {"host_submit_ns": t.host_submit_ns, "device_start_ns": t.device_start_ns,
+            "device_end_ns": t.device_end_ns, "t_infer_ns": t.device_end_ns - t.device_start_ns}
 
 
 def state_size(p: int) -> int:
@@ -411,6 +455,27 @@ class Policy:
             actions = self.torch.empty_like(noise)
         decode_actions(self.handle, noise, actions, stream)
         return actions
+
+    def decode_seeded(self, seed: int, counter: int, actions=None, stream=None):
+        """One decision from device-generated noise (seed, counter)."""
+        if actions is None:
+            actions = self.torch.empty((self.cfg.M, self.cfg.A), dtype=self.torch.float32, device=self.device)
+        decode_actions_seeded(self.handle, seed, counter, actions, stream)
+        return actions
+
+    def last_timing(self, stream=None) -> dict:
+        return last_timing(self.handle, stream)
+
+    def decode_warm(self, noise, executed: int, actions=None, stream=None):
+        """One-step warm start from the previous chunk (the full decision at an
+        episode's start)."""
+        if actions is None:
+            actions = self.torch.empty_like(noise)
+        decode_warm(self.handle, noise, executed, actions, stream)
+        return actions
+
+    def episode_reset(self):
+        episode_reset(self.handle)
 
     def close(self):
         if getattr(self, "handle", None):

@@ -195,8 +195,18 @@ struct RowArgs {
   // of x^2 (after the head, if any) into ssq[0][m], zeros into ssq[1..ssq_tiles-1][m]
   float* ssq;
   int ssq_tiles;
+  // decision timestamps (globaltimer ns): stamp_kind 1 = CTA 0 writes stamp[0] at its
+  // start and clears stamp[1]; 2 = every CTA raises stamp[1] to its end time
+  unsigned long long* stamp;
+  int stamp_kind;
 };
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o);
+// Decision noise: out[i] (i < n) from Philox4x32-10 block i / 4 with counter
+// (i / 4, 0, counter_lo, counter_hi) and key (seed_lo, seed_hi); words (w0, w1) give
+// elements 4b, 4b+1 and (w2, w3) give 4b+2, 4b+3 by Box-Muller (in double, rounded to
+// float). raw != nullptr also stores the four words of every block.
+cudaError_t philox_noise_launch(float* out, int64_t n, uint64_t seed, uint64_t counter, uint32_t* raw,
+                                cudaStream_t st);
 
 
 
@@ -262,7 +272,12 @@ int gemm_consumer_run(const GemmConsumerArgs& g, float* scratch, size_t scratch_
 int record_error(int status, const char* why);
 
 // ---------------------------------------------------------------- create-time kernels
-cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, cudaStream_t st);
+// conds [S + (warm_t > 0)][d]: rows k < S for t_k = 1 - k/S (or the given vectors),
+// row S for t = warm_t when warm_t > 0
+cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, float warm_t, cudaStream_t st);
+// One-step warm start input: a[m][j] = tau * noise[m][j] + (1 - tau) * prev[min(m + e, M - 1)][j]
+cudaError_t warm_mix_launch(float* a, const float* prev, const float* noise, int M, int A, int e, float tau,
+                            cudaStream_t st);
 cudaError_t modtable_launch(const double* conds, int S, int d, const __nv_bfloat16* w_mod, const float* b_mod,
                             int nout, float* out, size_t out_step_stride, cudaStream_t st);
 cudaError_t quant_e4m3_launch(const float* x, int64_t n, float scale, uint8_t* codes, cudaStream_t st);

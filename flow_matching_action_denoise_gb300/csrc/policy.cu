@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -52,6 +53,8 @@ struct Layout {
   size_t kcache8, vcache8;   // FP8 attention: E4M3 copies of the prefix cache
   size_t kv8_bytes, v8_bytes, ascale_bytes;
   size_t ssq;   // [d/128][M] per-tile sums of squares of x (consumers inside the GEMMs)
+  size_t stamps;   // [2] u64: globaltimer ns at the decision's first kernel start, last kernel end
+  size_t prev;     // [M][A] fp32: the previous chunk, shifted by a warm start
   size_t y[4];
   size_t err, amax, conds;
   size_t kv_bytes, a_bytes, scale_bytes;
@@ -143,6 +146,10 @@ int validate(const fm_config* c, std::string* why) {
   }
   if (!(c->rms_eps > 0.f)) {
     *why = "rms_eps must be positive";
+    return FM_ERR_INVALID_ARG;
+  }
+  if (!(c->warm_t >= 0.f && c->warm_t <= 1.f) || (c->warm_t > 0.f && c->cond_mode != FM_COND_TIME)) {
+    *why = "warm_t must lie in [0, 1], and a warm start needs time conditioning";
     return FM_ERR_INVALID_ARG;
   }
   return FM_OK;
@@ -254,8 +261,9 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.ascale_bytes = static_cast<size_t>(L) * 8 * sizeof(float);   // [L][8]: FM_SITE_* columns
   ly.wscale = ly.take(ly.scale_bytes);
   ly.ascale = ly.take(ly.ascale_bytes);
-  ly.mod = ly.take(static_cast<size_t>(S) * L * 6 * d * sizeof(float));
-  ly.modf = ly.take(static_cast<size_t>(S) * 2 * d * sizeof(float));
+  const int rows = S + (c->warm_t > 0.f ? 1 : 0);   // row S: the warm start's flow time
+  ly.mod = ly.take(static_cast<size_t>(rows) * L * 6 * d * sizeof(float));
+  ly.modf = ly.take(static_cast<size_t>(rows) * 2 * d * sizeof(float));
   ly.w_in = ly.take(static_cast<size_t>(d) * c->A * 2);
   ly.b_in = ly.take(static_cast<size_t>(d) * 4);
   ly.w_out = ly.take(static_cast<size_t>(d) * c->A * 2);
@@ -284,7 +292,9 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.err = ly.take(64);
   ly.ssq = ly.take(static_cast<size_t>(c->d / 128) * M * sizeof(float));
   ly.amax = ly.take(64);
-  ly.conds = ly.take(static_cast<size_t>(S) * d * sizeof(double));
+  ly.stamps = ly.take(64);
+  ly.conds = ly.take(static_cast<size_t>(rows) * d * sizeof(double));
+  ly.prev = ly.take(ly.a_bytes);   // the chunk a warm start shifts
   return ly;
 }
 
@@ -321,8 +331,12 @@ struct fm_policy {
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  cudaGraph_t warm_graph = nullptr;     // the one-step warm start (cfg.warm_t > 0)
+  cudaGraphExec_t warm_exec = nullptr;
+  bool have_prev = false;               // the noise/action buffer holds a decided chunk
   uint64_t plan_hash = 0;
   uint64_t decisions = 0;
+  uint64_t host_submit_ns = 0;   // steady clock when the last decision was enqueued
   std::string err;
   CapsuleHeader hdr;   // staging for device-side snapshots (must outlive the async copy)
 
@@ -585,7 +599,12 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
     r2.b_out = p->at<float>(p->ly.b_out);
     r2.a = p->at<float>(p->ly.a);
     r2.A = c.A;
-    r2.dt = -1.0f / static_cast<float>(c.S);
+    // step k < S of the schedule, or the warm start's single step (k == S) from warm_t
+    r2.dt = k < c.S ? -1.0f / static_cast<float>(c.S) : -c.warm_t;
+    if (k + 1 >= c.S) {   // the decision's last kernel
+      r2.stamp = p->at<unsigned long long>(p->ly.stamps);
+      r2.stamp_kind = 2;
+    }
     if (k + 1 < c.S) {
       r2.do_head = 1;
       r2.w_in = p->at<__nv_bfloat16>(p->ly.w_in);
@@ -624,7 +643,7 @@ size_t trace_record_bytes(const fm_policy* p) {
   return n;
 }
 
-cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
+cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o, int k0 = 0) {
   const fm_config& c = p->cfg;
   fm::RowArgs r = {};
   r.M = c.M;
@@ -636,12 +655,14 @@ cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o) {
   r.w_in = p->at<__nv_bfloat16>(p->ly.w_in);
   r.b_in = p->at<float>(p->ly.b_in);
   r.do_quant = 1;
-  r.scale = p->mod(0, 0, 0);
-  r.shift = p->mod(0, 0, 1);
+  r.scale = p->mod(k0, 0, 0);
+  r.shift = p->mod(k0, 0, 1);
   r.sq = p->ascale(0, FM_SITE_ATTN_IN);
   r.q = p->at<void>(p->ly.q);
   r.q_fp8 = p->dv.q_store;
   r.eps = c.rms_eps;
+  r.stamp = p->at<unsigned long long>(p->ly.stamps);
+  r.stamp_kind = 1;
   if (p->dv.rowfuse) {   // the first QKV GEMM normalises x itself: hand it the row sums
     r.do_quant = 0;
     r.ssq = p->at<float>(p->ly.ssq);
@@ -664,26 +685,52 @@ cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st, Trace* tr = nullptr)
   return cudaGetLastError();
 }
 
-int build_graph(fm_policy* p) {
-  FM_CUDA(p, cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking));
+// The warm start's single step: the head and all layers with modulation row S; the
+// last layer's tail steps by dt = -warm_t.
+cudaError_t enqueue_warm(fm_policy* p, cudaStream_t st) {
+  LaunchOpts o;
+  o.stream = st;
+  o.pdl = (p->cfg.flags & FM_FLAG_USE_PDL) != 0;
+  cudaError_t e = enqueue_head(p, o, p->cfg.S);
+  if (e != cudaSuccess) return e;
+  for (int l = 0; l < p->cfg.L; ++l) {
+    e = enqueue_layer(p, l, p->cfg.S, l == p->cfg.L - 1, o, nullptr);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+int capture(fm_policy* p, cudaError_t (*enq)(fm_policy*, cudaStream_t), cudaGraph_t* graph, cudaGraphExec_t* exec,
+            const char* what) {
   FM_CUDA(p, cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeThreadLocal));
-  cudaError_t e = enqueue_decision(p, p->cap_stream);
+  cudaError_t e = enq(p, p->cap_stream);
   cudaGraph_t g = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(p->cap_stream, &g);
   if (e != cudaSuccess) {
     if (g) cudaGraphDestroy(g);
-    return cuda_fail(p, e, "capturing the decision");
+    return cuda_fail(p, e, what);
   }
   if (e2 != cudaSuccess) return cuda_fail(p, e2, "cudaStreamEndCapture");
-  p->graph = g;
-  FM_CUDA(p, cudaGraphInstantiate(&p->exec, p->graph, 0));
+  *graph = g;
+  FM_CUDA(p, cudaGraphInstantiate(exec, g, 0));
   return FM_OK;
+}
+
+cudaError_t enqueue_full(fm_policy* p, cudaStream_t st) { return enqueue_decision(p, st); }
+
+int build_graph(fm_policy* p) {
+  FM_CUDA(p, cudaStreamCreateWithFlags(&p->cap_stream, cudaStreamNonBlocking));
+  int st = capture(p, enqueue_full, &p->graph, &p->exec, "capturing the decision");
+  if (st != FM_OK || !(p->cfg.warm_t > 0.f)) return st;
+  return capture(p, enqueue_warm, &p->warm_graph, &p->warm_exec, "capturing the warm start");
 }
 
 void release(fm_policy* p) {
   if (!p) return;
   if (p->exec) cudaGraphExecDestroy(p->exec);
   if (p->graph) cudaGraphDestroy(p->graph);
+  if (p->warm_exec) cudaGraphExecDestroy(p->warm_exec);
+  if (p->warm_graph) cudaGraphDestroy(p->warm_graph);
   if (p->cap_stream) cudaStreamDestroy(p->cap_stream);
   delete p;
 }
@@ -900,17 +947,18 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
   }
   // modulation table (the t-schedule is fixed: per-create state)
   double* conds = p->at<double>(p->ly.conds);
-  if (!cu(fm::cond_embed_launch(conds, c.S, c.d, c.cond_mode == FM_COND_GIVEN ? w->conds : nullptr, s),
+  const int mod_rows = c.S + (c.warm_t > 0.f ? 1 : 0);
+  if (!cu(fm::cond_embed_launch(conds, c.S, c.d, c.cond_mode == FM_COND_GIVEN ? w->conds : nullptr, c.warm_t, s),
           "cond_embed"))
     return bail(FM_ERR_CUDA, why);
   for (int l = 0; l < c.L; ++l) {
     const fm_layer_weights& lw = w->layers[l];
-    if (!cu(fm::modtable_launch(conds, c.S, c.d, reinterpret_cast<const __nv_bfloat16*>(lw.w_mod), lw.b_mod, 6 * c.d,
+    if (!cu(fm::modtable_launch(conds, mod_rows, c.d, reinterpret_cast<const __nv_bfloat16*>(lw.w_mod), lw.b_mod, 6 * c.d,
                                 p->mod(0, l, 0), static_cast<size_t>(c.L) * 6 * c.d, s),
             "modtable"))
       return bail(FM_ERR_CUDA, why);
   }
-  if (!cu(fm::modtable_launch(conds, c.S, c.d, reinterpret_cast<const __nv_bfloat16*>(w->w_mod_f), w->b_mod_f,
+  if (!cu(fm::modtable_launch(conds, mod_rows, c.d, reinterpret_cast<const __nv_bfloat16*>(w->w_mod_f), w->b_mod_f,
                               2 * c.d, p->modf(0, 0), static_cast<size_t>(2) * c.d, s),
           "modtable_final"))
     return bail(FM_ERR_CUDA, why);
@@ -1008,10 +1056,17 @@ int refresh_prefix(fm_policy* p, int tok_begin, int tok_end, const uint16_t* k, 
   return FM_OK;
 }
 
+uint64_t steady_ns() {
+  return static_cast<uint64_t>(std::chrono::duration_cast<std::chrono::nanoseconds>(
+                                   std::chrono::steady_clock::now().time_since_epoch())
+                                   .count());
+}
+
 int decode_actions(fm_policy* p, const float* noise, float* actions, void* stream) {
   if (!p || !actions) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* a = p->at<float>(p->ly.a);
+  p->host_submit_ns = steady_ns();
   if (noise && noise != a) FM_CUDA(p, cudaMemcpyAsync(a, noise, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
   if (p->exec) {
     FM_CUDA(p, cudaGraphLaunch(p->exec, s));
@@ -1020,6 +1075,62 @@ int decode_actions(fm_policy* p, const float* noise, float* actions, void* strea
   }
   if (actions != a) FM_CUDA(p, cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
   ++p->decisions;
+  p->have_prev = true;
+  return FM_OK;
+}
+
+int fm_decode_warm(fm_policy* p, const float* noise, int executed, float* actions, void* stream) {
+  if (!p || !noise || !actions) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  const fm_config& c = p->cfg;
+  if (!(c.warm_t > 0.f)) return fail(p, FM_ERR_UNSUPPORTED, "the policy was created with warm_t = 0");
+  if (executed < 0 || executed > c.M) return fail(p, FM_ERR_INVALID_ARG, "executed must lie in [0, M]");
+  if (!p->have_prev) return decode_actions(p, noise, actions, stream);   // episode start: all S steps
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->at<float>(p->ly.a);
+  float* prev = p->at<float>(p->ly.prev);
+  p->host_submit_ns = steady_ns();
+  FM_CUDA(p, cudaMemcpyAsync(prev, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  FM_CUDA(p, fm::warm_mix_launch(a, prev, noise, c.M, c.A, executed, c.warm_t, s));
+  if (p->warm_exec) {
+    FM_CUDA(p, cudaGraphLaunch(p->warm_exec, s));
+  } else {
+    FM_CUDA(p, enqueue_warm(p, s));
+  }
+  if (actions != a) FM_CUDA(p, cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  ++p->decisions;
+  return FM_OK;
+}
+
+int fm_episode_reset(fm_policy* p) {
+  if (!p) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL policy");
+  p->have_prev = false;
+  return FM_OK;
+}
+
+int fm_decode_actions_seeded(fm_policy* p, uint64_t seed, uint64_t counter, float* actions, void* stream) {
+  if (!p || !actions) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->at<float>(p->ly.a);
+  FM_CUDA(p, fm::philox_noise_launch(a, static_cast<int64_t>(p->cfg.M) * p->cfg.A, seed, counter, nullptr, s));
+  return decode_actions(p, nullptr, actions, stream);
+}
+
+int fm_philox_noise(float* out, int64_t n, uint64_t seed, uint64_t counter, uint32_t* raw_words, void* stream) {
+  if (!out || n < 0) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL output or negative size");
+  const cudaError_t e = fm::philox_noise_launch(out, n, seed, counter, raw_words, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(nullptr, FM_ERR_CUDA, cudaGetErrorString(e));
+  return FM_OK;
+}
+
+int fm_last_timing(fm_policy* p, fm_timing* t, void* stream) {
+  if (!p || !t) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long st[2] = {0, 0};
+  FM_CUDA(p, cudaMemcpyAsync(st, p->at<void>(p->ly.stamps), sizeof st, cudaMemcpyDeviceToHost, s));
+  FM_CUDA(p, cudaStreamSynchronize(s));
+  t->host_submit_ns = p->host_submit_ns;
+  t->device_start_ns = st[0];
+  t->device_end_ns = st[1];
   return FM_OK;
 }
 
@@ -1121,6 +1232,7 @@ int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device
   if (p->dv.attn_fp8 && p->cfg.P > 0) FM_CUDA(p, requant_prefix(p, 0, p->cfg.P, s));
   if (!src_on_device) FM_CUDA(p, cudaStreamSynchronize(s));
   p->decisions = h.decisions;
+  p->have_prev = h.decisions > 0;   // the restored noise/action buffer holds a decided chunk
   return FM_OK;
 }
 
@@ -1193,6 +1305,7 @@ int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trac
   tr.st = s;
   FM_CUDA(p, enqueue_decision(p, s, &tr));
   if (actions != a) FM_CUDA(p, cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  p->have_prev = true;
   FM_CUDA(p, cudaStreamSynchronize(s));
   if (tr.off != need) return fail(p, FM_ERR_INVALID_ARG, "internal: trace size mismatch");
   return FM_OK;

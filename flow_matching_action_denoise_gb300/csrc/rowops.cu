@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   const int tid = threadIdx.x;
   const int N = r.N;
   const int n4 = N / 4;
+  if (r.stamp_kind == 1 && m == 0 && tid == 0) {   // the decision's first kernel starts
+    r.stamp[0] = global_ns();
+    r.stamp[1] = 0ull;
+  }
   pdl_trigger();
   // Per-create constants (scales, modulation rows) do not depend on the previous
   // kernel: fetch them before waiting for it.
@@ -274,22 +278,73 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
       store_q4(r.q, static_cast<size_t>(m) * N + c * 4, h, r.q_fp8, rs);
     }
   }
+  if (r.stamp_kind == 2) {   // the decision's last kernel: latest CTA end
+    __syncthreads();
+    if (tid == 0) atomicMax(r.stamp + 1, global_ns());
+  }
+}
+
+// ---------------------------------------------------------------- decision noise
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC'11, section 3.2): per round (hi0, lo0) = M0 * x0, (hi1, lo1) = M1 * x2,
+// x <- (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0); the key is bumped by the Weyl
+// constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint32_t hi0 = __umulhi(kM0, x.x), lo0 = kM0 * x.x;
+    const uint32_t hi1 = __umulhi(kM1, x.z), lo1 = kM1 * x.z;
+    x = make_uint4(hi1 ^ x.y ^ k0, lo1, hi0 ^ x.w ^ k1, lo0);
+  }
+  return x;
+}
+
+// Box-Muller (Box and Muller, 1958) on two words: u = (w + 1/2) / 2^32 in (0, 1).
+__device__ __forceinline__ float2 box_muller(uint32_t wa, uint32_t wb) {
+  const double ua = (static_cast<double>(wa) + 0.5) * 0x1p-32;
+  const double ub = (static_cast<double>(wb) + 0.5) * 0x1p-32;
+  const double rad = sqrt(-2.0 * log(ua));
+  double sn, cs;
+  sincospi(2.0 * ub, &sn, &cs);
+  return make_float2(static_cast<float>(rad * cs), static_cast<float>(rad * sn));
+}
+
+__global__ void philox_noise_kernel(float* __restrict__ out, int64_t n, uint32_t k0, uint32_t k1, uint32_t c_lo,
+                                    uint32_t c_hi, uint32_t* __restrict__ raw) {
+  const int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (b * 4 >= n) return;
+  const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(b), static_cast<uint32_t>(b >> 32), c_lo, c_hi),
+                                k0, k1);
+  if (raw) reinterpret_cast<uint4*>(raw)[b] = w;
+  const float2 z01 = box_muller(w.x, w.y), z23 = box_muller(w.z, w.w);
+  const float z[4] = {z01.x, z01.y, z23.x, z23.y};
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (b * 4 + j < n) out[b * 4 + j] = z[j];
 }
 
 // ---------------------------------------------------------------- create-time kernels
 
 // cond[k][i]: the given vector, or the sinusoidal embedding of t_k = 1 - k/S
-// ([sin(2 pi t / p_i), cos(2 pi t / p_i)], p_i geometric from 4e-3 to 4), in double.
-__global__ void cond_embed_kernel(double* conds, int S, int d, const float* given) {
+// ([sin(2 pi t / p_i), cos(2 pi t / p_i)], p_i geometric from 4e-3 to 4), in double;
+// row S (rows = S + 1) is the embedding of the warm start's t = warm_t.
+__global__ void cond_embed_kernel(double* conds, int S, int rows, int d, const float* given, float warm_t) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= S * d) return;
+  if (idx >= rows * d) return;
   if (given) {
     conds[idx] = static_cast<double>(given[idx]);
     return;
   }
   const int k = idx / d, i = idx % d, half = d / 2;
   const int f = i < half ? i : i - half;
-  const double t = 1.0 - static_cast<double>(k) / S;
+  const double t = k < S ? 1.0 - static_cast<double>(k) / S : static_cast<double>(warm_t);
   const double period = 4e-3 * pow(4.0 / 4e-3, static_cast<double>(f) / (half - 1));
   const double arg = 2.0 * 3.14159265358979323846 * t / period;
   conds[idx] = i < half ? sin(arg) : cos(arg);
@@ -310,6 +365,15 @@ __global__ void modtable_kernel(const double* __restrict__ conds, int S, int d, 
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) out[k * step_stride + j] = static_cast<float>(acc + static_cast<double>(b[j]));
   }
+}
+
+__global__ void warm_mix_kernel(float* __restrict__ a, const float* __restrict__ prev, const float* __restrict__ noise,
+                                int M, int A, int e, float tau) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= M * A) return;
+  const int m = idx / A, j = idx % A;
+  const int src = min(m + e, M - 1);
+  a[idx] = fmaf(tau, noise[idx], (1.0f - tau) * prev[src * A + j]);
 }
 
 __global__ void quant_e4m3_kernel(const float* __restrict__ x, int64_t n, float scale, uint8_t* __restrict__ codes) {
@@ -367,9 +431,27 @@ cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
   return launch(row_kernel, dim3(static_cast<unsigned>(r.M)), dim3(kRowThreads), smem, o, r);
 }
 
-cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, cudaStream_t st) {
-  const int n = S * d;
-  cond_embed_kernel<<<(n + 255) / 256, 256, 0, st>>>(conds, S, d, given);
+cudaError_t philox_noise_launch(float* out, int64_t n, uint64_t seed, uint64_t counter, uint32_t* raw,
+                                cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n + 3) / 4;
+  philox_noise_kernel<<<static_cast<unsigned>((blocks + 127) / 128), 128, 0, st>>>(
+      out, n, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), static_cast<uint32_t>(counter),
+      static_cast<uint32_t>(counter >> 32), raw);
+  return cudaGetLastError();
+}
+
+cudaError_t cond_embed_launch(double* conds, int S, int d, const float* given, float warm_t, cudaStream_t st) {
+  const int rows = S + (warm_t > 0.f ? 1 : 0);
+  const int n = rows * d;
+  cond_embed_kernel<<<(n + 255) / 256, 256, 0, st>>>(conds, S, rows, d, given, warm_t);
+  return cudaGetLastError();
+}
+
+cudaError_t warm_mix_launch(float* a, const float* prev, const float* noise, int M, int A, int e, float tau,
+                            cudaStream_t st) {
+  const int n = M * A;
+  warm_mix_kernel<<<(n + 255) / 256, 256, 0, st>>>(a, prev, noise, M, A, e, tau);
   return cudaGetLastError();
 }
 

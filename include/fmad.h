@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define FM_ABI_VERSION 2
+#define FM_ABI_VERSION 3
 
 typedef enum fm_status {
   FM_OK = 0,
@@ -100,7 +100,8 @@ enum {
 
 /* Policy shape and options. Preconditions (FM_ERR_SHAPE otherwise):
  *   d, F and H*Dh multiples of 128; Dh == 128; H a multiple of Hkv;
- *   1 <= M <= 256; 1 <= A <= 256; P >= 0; L, S >= 1;
+ *   1 <= M <= 256; 1 <= A <= 32; P >= 0; L, S >= 1; 0 <= warm_t <= 1 (warm_t > 0
+ *   requires FM_COND_TIME);
  *   ksplit[i] (0 = automatic) divides the GEMM's K/128-byte block count.
  * act_fmt must be FP8 or BF16; weight_fmt FP8 requires act_fmt FP8, BF16
  * requires BF16, NVFP4 requires FP8. With NVFP4 weights the K-split counts
@@ -118,6 +119,7 @@ typedef struct fm_config {
   float rms_eps;       /* AdaRMSNorm epsilon */
   int ksplit[4];       /* K-split of the QKV, O, gate|up and down GEMMs; 0 = auto */
   unsigned flags;      /* FM_FLAG_* */
+  float warm_t;        /* flow time of the one-step warm start (fm_decode_warm); 0 = none */
 } fm_config;
 
 /* One layer's raw parameters (device pointers, read only during policy_create).
@@ -213,6 +215,51 @@ int decode_actions(fm_policy* p, const float* noise, float* actions, void* strea
 /* Same as decode_actions with HOST buffers (pinned recommended): copies the
  * noise in, decodes, copies the actions out, then synchronises the stream. */
 int decode_actions_host(fm_policy* p, const float* noise_host, float* actions_host, void* stream);
+
+/* Decision noise on the device (no host noise input): element i of the [n]
+ * fp32 output comes from Philox4x32-10 (Salmon et al., "Parallel random numbers:
+ * as easy as 1, 2, 3", SC'11) block b = i / 4 with counter words
+ * (b, 0, counter & 0xffffffff, counter >> 32) and key (seed & 0xffffffff,
+ * seed >> 32); words (w0, w1) give elements 4b and 4b+1, (w2, w3) give 4b+2 and
+ * 4b+3, by Box-Muller: u = (w + 1/2) / 2^32, z = sqrt(-2 ln u_a) * (cos, sin)
+ * (2 pi u_b), evaluated in double and rounded to float. Distinct (seed, counter)
+ * pairs give independent streams; the same pair gives the same noise.
+ * out: device fp32 [n]; raw_words: NULL or device u32 [ceil(n/4)][4] receiving the
+ * Philox words (for tests). Asynchronous. */
+int fm_philox_noise(float* out, int64_t n, uint64_t seed, uint64_t counter, uint32_t* raw_words, void* stream);
+
+/* decode_actions whose noise is fm_philox_noise(M * A, seed, counter), generated
+ * on the device into the policy's noise/action buffer. actions: device fp32 [M][A].
+ * Asynchronous. */
+int fm_decode_actions_seeded(fm_policy* p, uint64_t seed, uint64_t counter, float* actions, void* stream);
+
+/* One-step warm start (blog post, section "Few-step denoise brings the error back
+ * into consecutive decisions"): the previous decision's chunk (the policy's
+ * noise/action buffer) is moved forward by `executed` actions, its tail padded
+ * with its last action, mixed with the new noise at flow time tau = cfg.warm_t,
+ * a_tau = tau * noise + (1 - tau) * shifted, and one Euler step of dt = -tau with
+ * the modulation at t = tau gives the actions. The previous chunk is kept from the
+ * last decision of any kind; fm_episode_reset clears it, and a warm decode without
+ * one runs the full S-step decision instead. noise: device fp32 [M][A];
+ * 0 <= executed <= M; actions: device fp32 [M][A]. FM_ERR_UNSUPPORTED when
+ * cfg.warm_t is 0. Asynchronous. */
+int fm_decode_warm(fm_policy* p, const float* noise, int executed, float* actions, void* stream);
+
+/* Start of an episode: the next fm_decode_warm runs the full decision. */
+int fm_episode_reset(fm_policy* p);
+
+/* Timestamps of the last decision (blog post, section on the observation age
+ * A_k = t_apply,k - t_capture, measured with timestamps rather than summed stage
+ * estimates). host_submit_ns: steady-clock time the decision was enqueued;
+ * device_start_ns / device_end_ns: GPU globaltimer at the start of the decision's
+ * first kernel and at the end of its last kernel, so T_infer = end - start (the two
+ * clocks are not comparable with each other). Synchronises `stream`. */
+typedef struct fm_timing {
+  uint64_t host_submit_ns;
+  uint64_t device_start_ns;
+  uint64_t device_end_ns;
+} fm_timing;
+int fm_last_timing(fm_policy* p, fm_timing* t, void* stream);
 
 /* Bytes of an execution-state capsule (header + prefix K/V + noise/action
  * buffer + activation scales + counters). */

@@ -89,3 +89,29 @@ def test_policy_free_exports_validate(lib):
     assert lib.fm_test_skinny_gemm(1024, 300, 1024, 1024, 1024, fmad.FMT_FP8, 1, 1, 1024, None) == 2
     assert lib.fm_test_skinny_gemm(1032, 10, 1024, 1024, 1024, fmad.FMT_FP8, 1, 1, 1024, None) == 3
     assert lib.fm_test_quant_e4m3(1024, 16, ctypes.c_float(0.0), 1024, None) == 1
+
+
+def test_warm_start_config_validation(lib):
+    base = fmad.make_config(fm_synth.config("expert_fp8_m50"))
+    warm = fmad.make_config(fm_synth.config("expert_fp8_m50", warm_t=0.5))
+    # the warm start adds one modulation row: [L][6][d] + [2][d] fp32 and its [d] double cond
+    extra = fmad.workspace_size(warm) - fmad.workspace_size(base)
+    row = 18 * 6 * 1024 * 4 + 2 * 1024 * 4 + 1024 * 8
+    assert row <= extra < row + 3 * 1024
+    for t in (-0.1, 1.5, float("nan")):
+        bad = fmad.make_config(fm_synth.config("expert_fp8_m50", warm_t=t))
+        with pytest.raises(fmad.FmError) as e:
+            fmad.workspace_size(bad)
+        assert e.value.status == 1
+    given = fmad.make_config(fm_synth.config("layer_fp8_m10", warm_t=0.5))   # cond given per step
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(given)
+    assert e.value.status == 1
+
+
+def test_noise_and_warm_entry_points_validate_without_a_gpu(lib):
+    assert lib.fm_philox_noise(None, 16, 1, 2, None, None) == 1
+    assert lib.fm_decode_warm(None, None, 0, None, None) == 1
+    assert lib.fm_episode_reset(None) == 1
+    assert lib.fm_last_timing(None, None, None) == 1
+    assert lib.fm_decode_actions_seeded(None, 1, 2, None, None) == 1
