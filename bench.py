@@ -142,6 +142,8 @@ def run_ours(args, rank, world, local_rank):
     weights = fmad.DeviceWeights(cfg, layers, final, device=device)
     del layers
     pol = fmad.Policy(cfg, act_scales=scales, weights=weights, device=device)
+    # the one-step warm start needs its flow time in the plan: a policy of its own
+    weights_for_warm = weights if cfg.weight_fmt != "nvfp4" else None
     # launch-mode variants of the same policy (same kernels): graph without PDL, no graph
     variants = {}
     if not args.no_variants:
@@ -154,7 +156,6 @@ def run_ours(args, rank, world, local_rank):
                 cfg, act_scales=scales, weights=weights, device=device,
                 flags=fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | fmad.FLAG_FUSED_CONSUMERS)
     del weights
-    torch.cuda.empty_cache()
     kp, vp = fm_synth.prefix_kv(cfg)
     k_dev = torch.from_numpy(kp).to(device, torch.bfloat16)
     v_dev = torch.from_numpy(vp).to(device, torch.bfloat16)
@@ -165,6 +166,7 @@ def run_ours(args, rank, world, local_rank):
     actions = torch.empty_like(noise)
     stream = torch.cuda.current_stream(device)
     per_layer, per_decision = fmad.kernel_count(pol.handle)
+    pol_ws_bytes = pol.ws_bytes
 
     def barrier():
         if world > 1:
@@ -202,6 +204,36 @@ def run_ours(args, rank, world, local_rank):
         fmad.decode_actions_host(pol.handle, h_noise, h_act)
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3
+
+    # ---- the same policy's other entry points: device-generated noise (Philox) with the
+    # decision's own timestamps, and a session of the policy (shared weights, own state)
+    for _ in range(2):
+        fmad.decode_actions_seeded(pol.handle, 1234, 0, actions)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_infer = []
+    e0.record(stream)
+    for i in range(args.steps):
+        fmad.decode_actions_seeded(pol.handle, 1234, i, actions)
+        if i < 3:
+            t_infer.append(fmad.last_timing(pol.handle)["t_infer_ns"] * 1e-6)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    seeded_ms = e0.elapsed_time(e1) / args.steps
+    sess = pol.session()
+    sess.set_prefix_kv(k_dev, v_dev)
+    for _ in range(2):
+        sess.decode(noise, actions)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(args.steps):
+        sess.decode(noise, actions)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    session_ms = e0.elapsed_time(e1) / args.steps
+    session_bytes = sess.ws_bytes
+    sess.close()
+    warm = time_warm_start(cfg, weights_for_warm, scales, k_dev, v_dev, noise, device, stream, args)
 
     # ---- dominant kernel timed alone: the gate|up GEMM, rotating weight copies
     gemm = time_dominant_gemm(cfg, pol, device, stream) if cfg.weight_fmt == "fp8" else \
@@ -270,6 +302,14 @@ def run_ours(args, rank, world, local_rank):
         "kernels_per_layer": per_layer,
         "launch_variants_ms": variant_ms,
         "clocks": clocks.summary(),
+        "entry_points_ms": {
+            "decode_actions_seeded": round(seeded_ms, 4),
+            "t_infer_device": [round(t, 4) for t in t_infer],
+            "session_decision": round(session_ms, 4),
+            "session_workspace_mb": round(session_bytes / 2 ** 20, 1),
+            "policy_workspace_mb": round(pol_ws_bytes / 2 ** 20, 1),
+            **warm,
+        },
     }
     if cfg.weight_fmt == "nvfp4":
         fl = algorithmic_flops(cfg)
@@ -281,6 +321,35 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
     return line
+
+
+def time_warm_start(cfg, weights, scales, k_dev, v_dev, noise, device, stream, args):
+    """The one-step warm start (warm_t = 0.5, 3 actions executed) against the full
+    decision, on a policy created with that flow time (CUDA events)."""
+    import dataclasses
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    if weights is None:
+        return {}
+    wcfg = dataclasses.replace(cfg, warm_t=0.5)
+    pol = fmad.Policy(wcfg, act_scales=scales, weights=weights, device=device)
+    pol.set_prefix_kv(k_dev, v_dev)
+    out = torch.empty_like(noise)
+    pol.decode(noise, out)
+    for _ in range(3):
+        pol.decode_warm(noise, 3, out)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        pol.decode_warm(noise, 3, out)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / args.steps
+    if fmad.device_status(pol.handle):
+        raise RuntimeError("device error word set (warm start)")
+    pol.close()
+    return {"decode_warm_one_step": round(ms, 4), "warm_t": 0.5}
 
 
 def time_graph(device, launches, replays=5):

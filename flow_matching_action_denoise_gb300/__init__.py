@@ -17,7 +17,8 @@ __all__ = [
     "FmError", "lib", "load", "FmConfig", "make_config", "workspace_size", "policy_create",
     "policy_destroy", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
     "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status",
-    "kernel_count", "philox_noise", "decode_actions_seeded", "last_timing", "decode_warm", "episode_reset", "FmTiming", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
+    "kernel_count", "philox_noise", "decode_actions_seeded", "last_timing", "decode_warm", "episode_reset", "Session",
+    "session_workspace_size", "session_create", "session_fork", "FmTiming", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
     "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "named_buffer", "Policy", "DeviceWeights",
     "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "FLAG_FUSED_CONSUMERS", "COND_TIME", "COND_GIVEN",
     "ABI_VERSION", "STATUS",
@@ -41,6 +42,7 @@ EXPORTS = [
     "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
     "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer", "fm_gemm_consumer_noalloc",
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
+    "fm_session_workspace_size", "fm_session_create", "fm_session_fork",
 ]
 
 
@@ -126,6 +128,9 @@ def load() -> ctypes.CDLL:
         "fm_last_timing": (i, [vp, ctypes.POINTER(FmTiming), vp]),
         "fm_decode_warm": (i, [vp, vp, i, vp, vp]),
         "fm_episode_reset": (i, [vp]),
+        "fm_session_workspace_size": (i, [vp, ctypes.POINTER(sz)]),
+        "fm_session_create": (i, [vp, vp, sz, vp, ctypes.POINTER(vp)]),
+        "fm_session_fork": (i, [vp, vp, sz, i, vp, sz, vp, ctypes.POINTER(vp)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -228,6 +233,27 @@ def decode_actions_host(p: int, noise_host, actions_host, stream=None):
     """noise_host / actions_host: pinned (or pageable) CPU float32 tensors."""
     _check(load().decode_actions_host(p, _ptr(noise_host), _ptr(actions_host), _stream(stream)),
            "decode_actions_host", p)
+
+
+def session_workspace_size(base: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_session_workspace_size(base, ctypes.byref(n)), "fm_session_workspace_size", base)
+    return n.value
+
+
+def session_create(base: int, workspace: int, ws_bytes: int, stream=None) -> int:
+    out = ctypes.c_void_p()
+    _check(load().fm_session_create(base, workspace, ws_bytes, _stream(stream), ctypes.byref(out)),
+           "fm_session_create")
+    return out.value
+
+
+def session_fork(base: int, capsule, nbytes: int, capsule_on_device: bool, workspace: int, ws_bytes: int,
+                 stream=None) -> int:
+    out = ctypes.c_void_p()
+    _check(load().fm_session_fork(base, _ptr(capsule), nbytes, int(capsule_on_device), workspace, ws_bytes,
+                                  _stream(stream), ctypes.byref(out)), "fm_session_fork")
+    return out.value
 
 
 def philox_noise(out, seed: int, counter: int, raw_words=None, stream=None):
@@ -437,10 +463,15 @@ class Policy:
         refresh_prefix(self.handle, b, e, k, v, stream)
 
     def buffer(self, name: str, dtype=None, shape=None):
-        """Zero-copy torch view of a named persistent buffer inside the workspace."""
+        """Zero-copy torch view of a named persistent buffer (a session's shared
+        buffers live in its base policy's workspace)."""
         ptr, n = named_buffer(self.handle, name)
-        off = ptr - self.workspace.data_ptr()
-        view = self.workspace[off:off + n]
+        space = self.workspace
+        base = getattr(self, "base", None)
+        if base is not None and not (space.data_ptr() <= ptr < space.data_ptr() + space.numel()):
+            space = base.workspace
+        off = ptr - space.data_ptr()
+        view = space[off:off + n]
         if dtype is not None:
             view = view.view(dtype)
         if shape is not None:
@@ -477,6 +508,14 @@ class Policy:
     def episode_reset(self):
         episode_reset(self.handle)
 
+    def session(self, stream=None) -> "Session":
+        """A new session sharing this policy's weights, with its own state."""
+        return Session(self, stream=stream)
+
+    def fork(self, capsule, capsule_on_device: bool = True, stream=None) -> "Session":
+        """A new session started from a capsule of this policy (or of a session of it)."""
+        return Session(self, capsule, capsule_on_device, stream)
+
     def close(self):
         if getattr(self, "handle", None):
             policy_destroy(self.handle)
@@ -487,3 +526,25 @@ class Policy:
             self.close()
         except Exception:
             pass
+
+
+class Session(Policy):
+    """A session of a base Policy: shares the base's plan and read-only buffers,
+    owns its state (prefix cache, scales, action buffer, activations) in its own
+    workspace. Holds a reference to the base, which must outlive it."""
+
+    def __init__(self, base: Policy, capsule=None, capsule_on_device: bool = True, stream=None):
+        torch = base.torch
+        self.torch = torch
+        self.cfg = base.cfg
+        self.fmcfg = base.fmcfg
+        self.device = base.device
+        self.base = base
+        self.ws_bytes = session_workspace_size(base.handle)
+        self.workspace = torch.empty(self.ws_bytes + 1024, dtype=torch.uint8, device=self.device)
+        self.ws_ptr = self.workspace.data_ptr() + (-self.workspace.data_ptr()) % 1024
+        if capsule is None:
+            self.handle = session_create(base.handle, self.ws_ptr, self.ws_bytes, stream)
+        else:
+            self.handle = session_fork(base.handle, capsule, capsule.numel() * capsule.element_size(),
+                                       capsule_on_device, self.ws_ptr, self.ws_bytes, stream)

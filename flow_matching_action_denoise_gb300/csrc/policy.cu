@@ -46,6 +46,9 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
   size_t total = 0;
+  // [0, shared_end): read-only after create (packed weights, scales, modulation, the
+  // in/out projections), shared by the policy's sessions; the rest is per-session state
+  size_t shared_end = 0;
   std::vector<size_t> wpk;   // [L*4] packed weights
   size_t wscale, ascale, mod, modf, w_in, b_in, w_out, b_out, gamma_f, kcache, vcache, a, x, q, o, q2, mc;
   size_t qkvb;   // bf16 Q | K | V the attention reads (== y[0] unless NVFP4 reduces planes separately;
@@ -260,7 +263,6 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.scale_bytes = static_cast<size_t>(L) * 4 * sizeof(float);
   ly.ascale_bytes = static_cast<size_t>(L) * 8 * sizeof(float);   // [L][8]: FM_SITE_* columns
   ly.wscale = ly.take(ly.scale_bytes);
-  ly.ascale = ly.take(ly.ascale_bytes);
   const int rows = S + (c->warm_t > 0.f ? 1 : 0);   // row S: the warm start's flow time
   ly.mod = ly.take(static_cast<size_t>(rows) * L * 6 * d * sizeof(float));
   ly.modf = ly.take(static_cast<size_t>(rows) * 2 * d * sizeof(float));
@@ -269,6 +271,11 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.w_out = ly.take(static_cast<size_t>(d) * c->A * 2);
   ly.b_out = ly.take(static_cast<size_t>(c->A) * 4);
   ly.gamma_f = ly.take(static_cast<size_t>(d) * 4);
+  ly.conds = ly.take(static_cast<size_t>(rows) * d * sizeof(double));
+  ly.amax = ly.take(64);
+  ly.shared_end = ly.total;
+  // ---- per-session state
+  ly.ascale = ly.take(ly.ascale_bytes);
   // K [L][P][Hkv][Dh]; V stored transposed [L][Hkv][Dh][P_pad], P_pad = P rounded up to 8
   ly.kv_bytes = static_cast<size_t>(L) * ((c->P + 7) / 8 * 8) * c->Hkv * c->Dh * 2;
   ly.kcache = ly.take(ly.kv_bytes);
@@ -291,9 +298,7 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
   ly.vcache8 = ly.take(ly.v8_bytes);
   ly.err = ly.take(64);
   ly.ssq = ly.take(static_cast<size_t>(c->d / 128) * M * sizeof(float));
-  ly.amax = ly.take(64);
   ly.stamps = ly.take(64);
-  ly.conds = ly.take(static_cast<size_t>(rows) * d * sizeof(double));
   ly.prev = ly.take(ly.a_bytes);   // the chunk a warm start shifts
   return ly;
 }
@@ -325,8 +330,12 @@ struct fm_policy {
   fm_config cfg;
   Derived dv;
   Layout ly;
-  uint8_t* ws = nullptr;
+  uint8_t* ws = nullptr;       // this policy's (or session's) workspace: capsules bind to it
   size_t ws_bytes = 0;
+  uint8_t* shared = nullptr;   // layout offsets [0, shared_end): the base policy's workspace
+  uint8_t* state = nullptr;    // layout offsets [shared_end, total)
+  fm_policy* base = nullptr;   // a session's base policy (shares its weights)
+  int sessions = 0;            // live sessions of this base policy
   CUtensorMap tmA[4];
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
@@ -342,7 +351,7 @@ struct fm_policy {
 
   template <typename T>
   T* at(size_t off) const {
-    return reinterpret_cast<T*>(ws + off);
+    return reinterpret_cast<T*>(off < ly.shared_end ? shared + off : state + (off - ly.shared_end));
   }
   float* mod(int k, int l, int i) const {
     return at<float>(ly.mod) + ((static_cast<size_t>(k) * cfg.L + l) * 6 + i) * cfg.d;
@@ -735,6 +744,18 @@ void release(fm_policy* p) {
   delete p;
 }
 
+// Tensor maps of the GEMM activation operands (fixed addresses, recorded into the
+// graph by value); packed weights are fetched with plain bulk copies.
+bool build_tmaps(fm_policy* p) {
+  const size_t act_off[4] = {p->ly.q, p->ly.o, p->ly.q2, p->ly.mc};
+  for (int g = 0; g < 4; ++g) {
+    const bool ok = p->dv.nvfp4 ? fm::nvfp4_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), p->dv.ns[g])
+                                : fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), p->dv.gs[g]);
+    if (!ok) return false;
+  }
+  return true;
+}
+
 int check_ptrs(const fm_weights* w, int L, bool given, std::string* why) {
   if (!w || !w->layers || !w->w_in || !w->b_in || !w->w_out || !w->b_out || !w->gamma_f || !w->w_mod_f ||
       !w->b_mod_f || (given && !w->conds)) {
@@ -914,6 +935,8 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
   }
   p->ws = static_cast<uint8_t*>(workspace);
   p->ws_bytes = ws_bytes;
+  p->shared = p->ws;
+  p->state = p->ws + p->ly.shared_end;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const fm_config& c = p->cfg;
   const Derived& dv = p->dv;
@@ -984,17 +1007,7 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
     return bail(FM_ERR_CUDA, why);
   if (!cu(cudaStreamSynchronize(s), "create sync")) return bail(FM_ERR_CUDA, why);
 
-  // tensor maps (fixed addresses, recorded into the graph by value)
-  const size_t act_off[4] = {p->ly.q, p->ly.o, p->ly.q2, p->ly.mc};
-  if (dv.nvfp4) {   // packed NVFP4 blocks are fetched with plain bulk copies: no weight maps
-    for (int g = 0; g < 4; ++g)
-      if (!fm::nvfp4_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.ns[g]))
-        return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
-  } else {   // packed weights are fetched with plain bulk copies
-    for (int g = 0; g < 4; ++g)
-      if (!fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), dv.gs[g]))
-        return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
-  }
+  if (!build_tmaps(p)) return bail(FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
 
   uint64_t h = 1469598103934665603ull;
   h = fnv(h, &c, sizeof c);
@@ -1019,7 +1032,67 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
 
 int policy_destroy(fm_policy* p) {
   if (!p) return fail(nullptr, FM_ERR_INVALID_ARG, "policy is NULL");
+  if (p->sessions > 0) return fail(p, FM_ERR_INVALID_ARG, "the policy still has live sessions");
+  if (p->base) --p->base->sessions;
   release(p);
+  return FM_OK;
+}
+
+int fm_session_workspace_size(const fm_policy* base, size_t* bytes) {
+  if (!base || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  *bytes = base->ly.total - base->ly.shared_end;
+  return FM_OK;
+}
+
+int fm_session_create(fm_policy* base, void* workspace, size_t ws_bytes, void* stream, fm_policy** out) {
+  if (!out) return fail(nullptr, FM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!base || !workspace) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  if (base->base) base = base->base;   // a session of a session shares the same weights
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return fail(nullptr, FM_ERR_ALIGN, "workspace not 1024-aligned");
+  const size_t need = base->ly.total - base->ly.shared_end;
+  if (ws_bytes < need) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "session workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return fail(nullptr, FM_ERR_WORKSPACE, buf);
+  }
+  fm_policy* p = new (std::nothrow) fm_policy();
+  if (!p) return fail(nullptr, FM_ERR_INVALID_ARG, "out of host memory");
+  p->cfg = base->cfg;
+  p->dv = base->dv;
+  p->ly = base->ly;
+  p->ws = static_cast<uint8_t*>(workspace);
+  p->ws_bytes = ws_bytes;
+  p->shared = base->shared;
+  p->state = p->ws;
+  p->plan_hash = base->plan_hash;   // the same plan: capsules move between its sessions by fork
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // fresh state: empty prefix cache, zero action buffer and error word; the base's
+  // current activation scales
+  cudaError_t e = cudaMemsetAsync(p->state, 0, need, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(p->at<void>(p->ly.ascale), base->at<void>(base->ly.ascale), p->ly.ascale_bytes,
+                        cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    release(p);
+    return fail(nullptr, FM_ERR_CUDA, std::string("session state init: ") + cudaGetErrorString(e));
+  }
+  if (!build_tmaps(p)) {
+    release(p);
+    return fail(nullptr, FM_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed");
+  }
+  if (p->cfg.flags & FM_FLAG_USE_GRAPH) {
+    const int st = build_graph(p);
+    if (st != FM_OK) {
+      const std::string why = p->err;
+      release(p);
+      return fail(nullptr, st, why);
+    }
+  }
+  p->base = base;
+  ++base->sessions;
+  *out = p;
   return FM_OK;
 }
 
@@ -1196,7 +1269,31 @@ int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, voi
   return FM_OK;
 }
 
+static int restore_impl(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream, bool bound);
+
 int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream) {
+  return restore_impl(p, src, bytes, src_on_device, stream, true);
+}
+
+int fm_session_fork(fm_policy* base, const void* capsule, size_t bytes, int capsule_on_device, void* workspace,
+                    size_t ws_bytes, void* stream, fm_policy** out) {
+  if (!out) return fail(nullptr, FM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!base || !capsule) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  fm_policy* p = nullptr;
+  int st = fm_session_create(base, workspace, ws_bytes, stream, &p);
+  if (st != FM_OK) return st;
+  st = restore_impl(p, capsule, bytes, capsule_on_device, stream, false);
+  if (st != FM_OK) {
+    const std::string why = p->err;
+    policy_destroy(p);
+    return fail(nullptr, st, why);
+  }
+  *out = p;
+  return FM_OK;
+}
+
+static int restore_impl(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream, bool bound) {
   if (!p || !src) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
   size_t need = 0;
   fm_state_size(p, &need);
@@ -1212,7 +1309,7 @@ int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device
   if (h.magic != kCapsuleMagic || h.abi != FM_ABI_VERSION || h.header_bytes != sizeof h)
     return fail(p, FM_ERR_STATE_MISMATCH, "not a capsule of this library version");
   if (h.plan_hash != p->plan_hash) return fail(p, FM_ERR_STATE_MISMATCH, "capsule was made by another plan");
-  if (h.ws_base != reinterpret_cast<uintptr_t>(p->ws))
+  if (bound && h.ws_base != reinterpret_cast<uintptr_t>(p->ws))
     return fail(p, FM_ERR_STATE_MISMATCH, "capsule is bound to another workspace address");
   if (h.kv_bytes != p->ly.kv_bytes || h.a_bytes != p->ly.a_bytes || h.scale_bytes != p->ly.ascale_bytes ||
       h.L != p->cfg.L || h.P != p->cfg.P || h.M != p->cfg.M || h.A != p->cfg.A)
@@ -1278,7 +1375,7 @@ int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* by
   };
   for (const Entry& e : table) {
     if (std::strcmp(e.n, name) == 0) {
-      *ptr = p->ws + e.off;
+      *ptr = p->at<uint8_t>(e.off);
       *bytes = e.bytes;
       return FM_OK;
     }

@@ -186,8 +186,9 @@ int fm_workspace_size(const fm_config* cfg, size_t* bytes);
 int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_scales,
                   void* workspace, size_t ws_bytes, void* stream, fm_policy** out);
 
-/* Release the host-side policy (graph, plan). Does not touch the workspace.
- * The caller must not destroy a policy with work in flight on its stream. */
+/* Release the host-side policy or session (graphs, plan). Does not touch the
+ * workspace. The caller must not destroy a policy with work in flight on its
+ * stream; a base policy with live sessions is not destroyed (FM_ERR_INVALID_ARG). */
 int policy_destroy(fm_policy* p);
 
 /* Replace the static activation scales (host [L][4] fp32, [L][7] with FP8
@@ -273,6 +274,28 @@ int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, voi
  * workspace address and shapes); otherwise FM_ERR_STATE_MISMATCH and nothing is
  * written. Capsules are in-process only, bound to the plan and device addresses. */
 int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream);
+
+/* Sessions (paper, "execution-state capsules" for snapshot, restore and fork of the
+ * persistent state): several policies that share one plan and its read-only buffers
+ * (packed weights, weight scales, modulation tables, in/out projections) while each
+ * owns its state (prefix K/V cache and its E4M3 copy, activation scales,
+ * noise/action buffer, activations, error word) in its own workspace.
+ *
+ * fm_session_workspace_size: bytes of a session's workspace (1024-aligned device
+ * memory owned by the caller) for sessions of `base`.
+ * fm_session_create: a new session of `base` (or of base's own base, if `base` is a
+ * session) with an empty prefix cache, a zero action buffer and base's current
+ * activation scales; it has its own CUDA graphs and runs independently of, and
+ * concurrently with, the base and other sessions on other streams.
+ * fm_session_fork: a session started from a capsule made by snapshot_state of
+ * `base` or of any session of it: the one way a capsule moves to another workspace
+ * (restore_state stays bound to the capsule's own workspace address).
+ * policy_destroy of a base with live sessions fails with FM_ERR_INVALID_ARG and
+ * destroys nothing: destroy the sessions first. */
+int fm_session_workspace_size(const fm_policy* base, size_t* bytes);
+int fm_session_create(fm_policy* base, void* workspace, size_t ws_bytes, void* stream, fm_policy** out);
+int fm_session_fork(fm_policy* base, const void* capsule, size_t bytes, int capsule_on_device, void* workspace,
+                    size_t ws_bytes, void* stream, fm_policy** out);
 
 /* Synchronise `stream`, read and clear the device error word. Returns FM_OK, or
  * FM_ERR_DEVICE with *word = the bits a kernel set when it abandoned a bounded

@@ -115,3 +115,12 @@ def test_noise_and_warm_entry_points_validate_without_a_gpu(lib):
     assert lib.fm_episode_reset(None) == 1
     assert lib.fm_last_timing(None, None, None) == 1
     assert lib.fm_decode_actions_seeded(None, 1, 2, None, None) == 1
+
+
+def test_session_entry_points_validate_without_a_gpu(lib):
+    n = ctypes.c_size_t()
+    assert lib.fm_session_workspace_size(None, ctypes.byref(n)) == 1
+    out = ctypes.c_void_p(1)
+    assert lib.fm_session_create(None, 1024, 1 << 20, None, ctypes.byref(out)) == 1 and out.value is None
+    assert lib.fm_session_fork(None, None, 0, 1, 1024, 1 << 20, None, ctypes.byref(out)) == 1
+    assert lib.policy_destroy(None) == 1
