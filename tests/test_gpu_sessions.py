@@ -62,10 +62,8 @@ def test_fork_continues_from_the_capsule_then_diverges(base):
     b = f.decode(None, torch.empty((base.cfg.M, base.cfg.A), device=base.device))
     torch.cuda.synchronize()
     assert torch.equal(a, b)
-    # a capsule of the base does not restore into the fork's workspace
-    with pytest.raises(fmad.FmError) as e:
-        fmad.restore_state(f.handle, cap, n, True)
-    assert e.value.status == 6
+    # a capsule of the base does not restore into the fork's workspace (STATE_MISMATCH)
+    assert fmad.restore_state(f.handle, cap, n, True) == 6
     # the base's prefix refresh stays in the base
     kr, vr = fm_synth.prefix_kv_rows(base.cfg, 4, 768)
     base.refresh_prefix(0, 768, dev(kr, base.device, torch.bfloat16), dev(vr, base.device, torch.bfloat16))
