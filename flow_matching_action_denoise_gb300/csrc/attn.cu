@@ -68,11 +68,6 @@ __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gmem_s
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w)
-               : "memory");
-}
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a [rows][128 B] block with
 // the 128-byte swizzle (the block base is 1024-byte aligned).
@@ -136,8 +131,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const SmemPlan sp = smem_plan(KC, p.nsplit, kF8);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + sp.bar);   // S done, O done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  // S done, O done, every slice's statistics received, this CTA's O band received
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + sp.bar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
   float2* sStats = reinterpret_cast<float2*>(smem + sp.stats);  // [rank][row] (slice max, slice sum)
   float2* sPart = reinterpret_cast<float2*>(smem + sp.part);    // [part][row]
   float* recv = reinterpret_cast<float*>(smem + sp.recv);       // [rank][local row][128]
@@ -154,6 +150,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int nvalid = min(KC, nkeys - t0);
   constexpr uint32_t ncols = (KC + kDh) <= 256 ? 256u : 512u;
   const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
+  const int tile_rows = min(kRows, p.G * p.M - qt * kRows);   // real (head, row) rows of the tile
+  // rows [lo, hi) of the band finalised by cluster rank o (empty past the real rows)
+  auto band = [&](int o, int& lo, int& hi) {
+    lo = o * rows_per;
+    hi = min(min(kRows, lo + rows_per), tile_rows);
+    if (hi < lo) hi = lo;
+  };
   // static scales (set through the host API, never by a kernel of the decision):
   // fetched at the start, off the critical path
   // log2(e) / sqrt(Dh), times the E4M3 codes' dequantisation fp32(s_q * s_k)
@@ -166,7 +169,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     s_abort = 0;
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
+    mbar_init(&bar[3], 1);
     fence_mbar_init();
+    // every slice pushes (max, sum) of all 128 rows; this CTA's band of O arrives from
+    // every slice by bulk copies
+    mbar_arrive_expect_tx(&bar[2], static_cast<uint32_t>(p.nsplit * kRows * 8));
+    int lo, hi;
+    band(static_cast<int>(cluster_rank()), lo, hi);
+    mbar_arrive_expect_tx(&bar[3], static_cast<uint32_t>(p.nsplit * (hi - lo) * kDh * 4));
   }
   if (warp == 0) {
     __syncwarp();
@@ -342,13 +353,16 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     }
     const uint32_t rank = cluster_rank();
     const uint32_t off = smem_u32(sStats + rank * kRows + r);
-    for (int q = 0; q < p.nsplit; ++q) {
-      const uint32_t dst = map_dsmem(off, static_cast<uint32_t>(q));
-      st_dsmem_f32(dst, m);
-      st_dsmem_f32(dst + 4, l);
-    }
+    const uint32_t mb = smem_u32(&bar[2]);
+    for (int q = 0; q < p.nsplit; ++q)
+      st_async_v2(map_dsmem(off, static_cast<uint32_t>(q)), m, l, map_dsmem(mb, static_cast<uint32_t>(q)));
   }
-  cluster_sync_all();   // every slice's statistics have landed
+  // Every slice's statistics have landed. Each peer sent them after its S = Q K^T
+  // completed, so from here on its Q and K tiles are dead and may receive O shares.
+  if (!mbar_wait(&bar[2], 0)) {
+    atomicOr(p.err, kErrPipelineTimeout);
+    s_abort = 1;
+  }
   float gmax = -INFINITY, gsum = 0.f;
   for (int q = 0; q < p.nsplit; ++q) gmax = fmaxf(gmax, sStats[q * kRows + r].x);
   for (int q = 0; q < p.nsplit; ++q) {
@@ -422,11 +436,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   tc_fence_after();
   __syncwarp();
 
-  // ---- this slice's share of O (already normalised by the global sum) goes row by
-  // row to the CTA that finalises it (rows are split into bands of rows_per). TMEM
+  // ---- this slice's share of O (already normalised by the global sum) goes band by
+  // band to the CTA that finalises it (rows are split into bands of rows_per). TMEM
   // gives each thread one row, so the share is first staged row-major in shared
-  // memory (16-byte chunks swizzled by row: conflict-free), then each warp pushes
-  // whole 512-byte rows with contiguous remote stores.
+  // memory (16-byte chunks swizzled by row: conflict-free); then one bulk copy per
+  // band moves the band's rows into the owner's receive slot for this rank, counted
+  // on the owner's mbarrier.
   {
     constexpr int kCols = kDh / kParts;   // O columns read by one thread
     const uint32_t stage = base + static_cast<uint32_t>(sp.stage);
@@ -442,19 +457,28 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
                                 __float_as_uint(v[e + 3])));
       }
     }
-  }
-  __syncthreads();
-  {
-    const uint32_t rank = cluster_rank();
-    for (int row = warp; row < kRows; row += kThreads / 32) {
-      if (qt * kRows + row >= p.G * p.M) break;   // padding rows (none after a padding row)
-      const int owner = row / rows_per, lr = row - owner * rows_per;
-      const float4 v = *reinterpret_cast<const float4*>(smem + sp.stage + row * 512 + ((lane ^ (row & 7)) << 4));
-      st_dsmem_v4(map_dsmem(smem_u32(recv + (rank * rows_per + lr) * kDh + lane * 4), static_cast<uint32_t>(owner)),
-                  v);
+    fence_async_smem();   // the staged rows -> the bulk copies' reads
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t rank = cluster_rank();
+      const uint32_t slot = smem_u32(recv + static_cast<size_t>(rank) * rows_per * kDh);
+      for (int o = 0; o < p.nsplit; ++o) {
+        int lo, hi;
+        band(o, lo, hi);
+        if (hi > lo)
+          bulk_copy_to_peer(map_dsmem(slot, static_cast<uint32_t>(o)), stage + static_cast<uint32_t>(lo * 512),
+                            static_cast<uint32_t>((hi - lo) * 512), map_dsmem(smem_u32(&bar[3]), static_cast<uint32_t>(o)));
+      }
     }
   }
-  cluster_sync_all();   // every share of this CTA's rows has landed
+  if (!mbar_wait(&bar[3], 0)) {   // every slice's share of this CTA's band has landed
+    atomicOr(p.err, kErrPipelineTimeout);
+    s_abort = 1;
+  }
+  // Once every owner has its band, no bulk copy still reads this CTA's stage: each
+  // CTA arrives here and waits before exit (lifetime only; the data is ordered by
+  // the mbarriers).
+  cluster_arrive_relaxed();
 
   // ---- sum the slices' shares in fixed slice order, quantise, store
   if (s_abort == 0) {
@@ -465,8 +489,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       const int R = qt * kRows + rr;
       if (rr >= kRows || R >= p.G * p.M) break;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int sw = (lane ^ (rr & 7)) << 2;   // the staged row's swizzled chunk
       for (int q = 0; q < p.nsplit; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDh + e4);
+        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDh + sw);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -504,6 +529,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
     }
   }
+  cluster_wait();   // every owner has its band: no copy still reads this CTA
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

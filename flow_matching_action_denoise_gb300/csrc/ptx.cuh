@@ -213,6 +213,21 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Bulk copy (TMA engine) from this CTA's shared memory to the shared memory of a CTA
+// of the cluster; `dst` and `mbar` are shared::cluster addresses in the destination
+// CTA, whose mbarrier receives the byte count. Addresses and size: multiples of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "r"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+// Asynchronous 8-byte store into a CTA of the cluster, counted on that CTA's mbarrier
+// (shared::cluster addresses).
+__device__ __forceinline__ void st_async_v2(uint32_t dst, float a, float b, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(dst), "f"(a), "f"(b), "r"(mbar)
+               : "memory");
+}
 __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
