@@ -14,7 +14,11 @@
 // contractions run on tcgen05 tensor cores with bf16 operands in shared memory
 // (K-major, 128-byte swizzle, the layout TMA writes) and fp32 accumulators in
 // TMEM: S = Q K^T (M = 128 rows, N = slice keys, K = 128 head dims), then
-// O = P V (N = 128 head dims, K = slice keys) with V held transposed. Four warps
+// O = P V (N = 64 head dims, K = slice keys) with V held transposed: the two halves
+// of the head dims of O are two CTAs that compute the same S and softmax, so each
+// stages, exchanges and sums half the O bytes (the exchange is bound by distributed
+// shared memory bandwidth, the duplicated S and exponentials by nothing: they run
+// on otherwise idle SMs). Four warps
 // share each TMEM lane quarter (32 rows) and split the slice's keys, so the softmax
 // needs no shuffles: pass 1 reads S, takes each row part's max m_h and keeps
 // exp(s - m_h) in registers with its sum; the cluster exchanges the (max, sum)
@@ -43,6 +47,8 @@ constexpr int kDh = 128;             // head dim
 constexpr int kMaxSplit = 8;         // portable cluster size
 constexpr int kMaxKc = 192;          // keys per slice (MMA N of QK^T), multiple of 64
 constexpr int kTile = kRows * 128;   // bytes of one [128 rows][128 B] swizzled block
+constexpr int kDv = kDh / 2;         // head dims of O per CTA (the P V contraction's N)
+constexpr int kTileV = kDv * 128;    // bytes of one [kDv rows][128 B] block of V^T
 static_assert(kThreads % kDh == 0, "whole threads per head-dim row of V^T");
 
 struct KParams {
@@ -85,8 +91,9 @@ struct SmemPlan {
   size_t q, k, vt, pm, stage, recv, stats, part, bar, total;
 };
 // Operand tiles: Q [128 rows][Dh] (bf16: two 128-byte blocks, E4M3: one); K [kc keys][Dh]
-// likewise; V^T and P in blocks of [128][128 bytes] along the keys (bf16: kc/64 blocks of
-// 64 keys; E4M3: the keys padded to a multiple of 128, one block per 128 keys).
+// likewise; P in blocks of [128 rows][128 bytes] and this CTA's half of V^T in blocks of
+// [kDv rows][128 bytes] along the keys (bf16: kc/64 blocks of 64 keys; E4M3: the keys
+// padded to a multiple of 128, one block per 128 keys).
 __host__ __device__ inline int kblocks(int kc, bool fp8) { return fp8 ? (kc + 127) / 128 : kc / 64; }
 __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8) {
   SmemPlan s;
@@ -94,11 +101,11 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8) {
   s.q = 0;
   s.k = eb * static_cast<size_t>(kTile);
   s.vt = s.k + static_cast<size_t>(kc) * 128 * eb;
-  s.pm = s.vt + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
+  s.pm = s.vt + static_cast<size_t>(kblocks(kc, fp8)) * kTileV;
   const size_t main_end = s.pm + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
   const int rows_per = (kRows + nsplit - 1) / nsplit;
-  const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * kDh * 4;
-  const size_t stage_bytes = static_cast<size_t>(kRows) * kDh * 4;
+  const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * kDv * 4;
+  const size_t stage_bytes = static_cast<size_t>(kRows) * kDv * 4;
   size_t end = main_end;
   // this CTA's O share is staged in V^T and P (dead once P V completed) when they are
   // large enough; the O receive buffer reuses Q and K (dead once every CTA passed the
@@ -141,14 +148,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
 
   const int split = blockIdx.x;
   const int qt = blockIdx.y;
-  const int g = blockIdx.z;
+  const int g = blockIdx.z >> 1;          // KV head
+  const int d0 = (blockIdx.z & 1) * kDv;  // this CTA's head dims of O: [d0, d0 + kDv)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, part = warp >> 2;
   const int nkeys = p.P + p.M;
   const int t0 = split * KC;
   const int nvalid = min(KC, nkeys - t0);
-  constexpr uint32_t ncols = (KC + kDh) <= 256 ? 256u : 512u;
+  constexpr uint32_t ncols = (KC + kDv) <= 256 ? 256u : 512u;
   const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
   const int tile_rows = min(kRows, p.G * p.M - qt * kRows);   // real (head, row) rows of the tile
   // rows [lo, hi) of the band finalised by cluster rank o (empty past the real rows)
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     mbar_arrive_expect_tx(&bar[2], static_cast<uint32_t>(p.nsplit * kRows * 8));
     int lo, hi;
     band(static_cast<int>(cluster_rank()), lo, hi);
-    mbar_arrive_expect_tx(&bar[3], static_cast<uint32_t>(p.nsplit * (hi - lo) * kDh * 4));
+    mbar_arrive_expect_tx(&bar[3], static_cast<uint32_t>(p.nsplit * (hi - lo) * kDv * 4));
   }
   if (warp == 0) {
     __syncwarp();
@@ -208,26 +216,26 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       st_shared_v4(dst, make_uint4(0, 0, 0, 0));
     }
   }
-  // V^T rows: two threads per head-dim row d copy 8 keys (16 bytes) at a time. The
+  // V^T rows of this CTA's head dims: eight threads per row copy 16 bytes at a time. The
   // cache row is padded with zeros from P to P_pad, so a group straddling the end of
   // the prefix is copied whole; its keys >= P are overwritten with the chunk's values.
   if constexpr (kF8) {   // E4M3: 16 keys per 16-byte group; the padding keys [KC, kKcp) are zero
-    const int d = tid & (kDh - 1);
-    const uint8_t* vrow = p.vtpre8 + (static_cast<size_t>(g) * kDh + d) * p.p16;
-    for (int grp = tid >> 7; grp < kKcp / 16; grp += kThreads / kDh) {
+    const int d = tid & (kDv - 1);
+    const uint8_t* vrow = p.vtpre8 + (static_cast<size_t>(g) * kDh + d0 + d) * p.p16;
+    for (int grp = tid / kDv; grp < kKcp / 16; grp += kThreads / kDv) {
       const int t = t0 + grp * 16;
-      const uint32_t dst = sVta + (grp >> 3) * kTile + swz(d, grp & 7);
+      const uint32_t dst = sVta + (grp >> 3) * kTileV + swz(d, grp & 7);
       if (grp * 16 < KC && t < p.P)
         cp_async16(dst, vrow + t);
       else
         st_shared_v4(dst, make_uint4(0, 0, 0, 0));
     }
   } else {
-    const int d = tid & (kDh - 1);
-    const __nv_bfloat16* vrow = p.vtpre + (static_cast<size_t>(g) * kDh + d) * p.p_pad;
-    for (int grp = tid >> 7; grp < KC / 8; grp += kThreads / kDh) {
+    const int d = tid & (kDv - 1);
+    const __nv_bfloat16* vrow = p.vtpre + (static_cast<size_t>(g) * kDh + d0 + d) * p.p_pad;
+    for (int grp = tid / kDv; grp < KC / 8; grp += kThreads / kDv) {
       const int t = t0 + grp * 8;
-      const uint32_t dst = sVta + (grp >> 3) * kTile + swz(d, grp & 7);
+      const uint32_t dst = sVta + (grp >> 3) * kTileV + swz(d, grp & 7);
       if (t < p.P)
         cp_async16(dst, vrow + t);
       else
@@ -271,22 +279,22 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();   // V^T groups and the staged chunk values are in place
-  if (nchunk > 0) {   // shared -> shared transpose into V^T (keys along K)
-    const int d = tid & (kDh - 1);
+  if (nchunk > 0) {   // shared -> shared transpose into V^T (keys along K), this CTA's dims
+    const int d = tid & (kDv - 1);
     if constexpr (kF8) {
       const uint8_t* vstage = smem + sp.pm;
-      for (int t = c_lo + (tid >> 7); t < c_hi; t += kThreads / kDh) {
+      for (int t = c_lo + tid / kDv; t < c_hi; t += kThreads / kDv) {
         const int key = t - t0;
-        const uint32_t v = vstage[(t - c_lo) * kDh + d];
-        const uint32_t addr = sVta + (key >> 7) * kTile + swz(d, (key & 127) >> 4) + (key & 15);
+        const uint32_t v = vstage[(t - c_lo) * kDh + d0 + d];
+        const uint32_t addr = sVta + (key >> 7) * kTileV + swz(d, (key & 127) >> 4) + (key & 15);
         asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
       }
     } else {
       const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
-      for (int t = c_lo + (tid >> 7); t < c_hi; t += kThreads / kDh) {
+      for (int t = c_lo + tid / kDv; t < c_hi; t += kThreads / kDv) {
         const int key = t - t0, grp = key >> 3;
-        const uint16_t v = vstage[(t - c_lo) * kDh + d];
-        const uint32_t addr = sVta + (grp >> 3) * kTile + swz(d, grp & 7) + (key & 7) * 2;
+        const uint16_t v = vstage[(t - c_lo) * kDh + d0 + d];
+        const uint32_t addr = sVta + (grp >> 3) * kTileV + swz(d, grp & 7) + (key & 7) * 2;
         asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
       }
     }
@@ -416,16 +424,16 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   fence_async_smem();
   __syncthreads();
 
-  // ---- O = P V into TMEM columns [KC, KC + 128)
+  // ---- O = P V into TMEM columns [KC, KC + kDv): this CTA's head dims
   if (tid == 0) {
     tc_fence_after();
-    const uint32_t idesc = make_idesc(kF8, kRows, kDh);
+    const uint32_t idesc = make_idesc(kF8, kRows, kDv);
 #pragma unroll
     for (int b = 0; b < kBlk; ++b) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         tc_mma<kF8>(tmem + static_cast<uint32_t>(KC), sw128_kmajor_desc(sPa + b * kTile + k * 32),
-                    sw128_kmajor_desc(sVta + b * kTile + k * 32), idesc, (b | k) ? 1u : 0u);
+                    sw128_kmajor_desc(sVta + b * kTileV + k * 32), idesc, (b | k) ? 1u : 0u);
     }
     tc_commit(&bar[1]);
   }
@@ -443,7 +451,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // band moves the band's rows into the owner's receive slot for this rank, counted
   // on the owner's mbarrier.
   {
-    constexpr int kCols = kDh / kParts;   // O columns read by one thread
+    constexpr int kCols = kDv / kParts;   // O columns read by one thread
+    constexpr int kRowBytes = kDv * 4;    // one staged row of this CTA's O share
     const uint32_t stage = base + static_cast<uint32_t>(sp.stage);
 #pragma unroll
     for (int c = 0; c < kCols; c += 16) {
@@ -451,8 +460,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       tmem_ld16(t_row + static_cast<uint32_t>(KC + part * kCols + c), v);
 #pragma unroll
       for (int e = 0; e < 16; e += 4) {
-        const int chunk = (part * kCols + c + e) >> 2;   // 16-byte chunk (0..31) of the row
-        st_shared_v4(stage + r * 512 + ((chunk ^ (r & 7)) << 4),
+        const int chunk = (part * kCols + c + e) >> 2;   // 16-byte chunk (0..kDv/4-1) of the row
+        st_shared_v4(stage + r * kRowBytes + ((chunk ^ (r & 7)) << 4),
                      make_uint4(__float_as_uint(v[e]), __float_as_uint(v[e + 1]), __float_as_uint(v[e + 2]),
                                 __float_as_uint(v[e + 3])));
       }
@@ -461,13 +470,14 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     __syncthreads();
     if (tid == 0) {
       const uint32_t rank = cluster_rank();
-      const uint32_t slot = smem_u32(recv + static_cast<size_t>(rank) * rows_per * kDh);
+      const uint32_t slot = smem_u32(recv + static_cast<size_t>(rank) * rows_per * kDv);
       for (int o = 0; o < p.nsplit; ++o) {
         int lo, hi;
         band(o, lo, hi);
         if (hi > lo)
-          bulk_copy_to_peer(map_dsmem(slot, static_cast<uint32_t>(o)), stage + static_cast<uint32_t>(lo * 512),
-                            static_cast<uint32_t>((hi - lo) * 512), map_dsmem(smem_u32(&bar[3]), static_cast<uint32_t>(o)));
+          bulk_copy_to_peer(map_dsmem(slot, static_cast<uint32_t>(o)), stage + static_cast<uint32_t>(lo * kRowBytes),
+                            static_cast<uint32_t>((hi - lo) * kRowBytes),
+                            map_dsmem(smem_u32(&bar[3]), static_cast<uint32_t>(o)));
       }
     }
   }
@@ -483,15 +493,17 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // ---- sum the slices' shares in fixed slice order, quantise, store
   if (s_abort == 0) {
     const int rank = static_cast<int>(cluster_rank());
-    const int e4 = lane * 4;
-    for (int lr = warp; lr < rows_per; lr += kThreads / 32) {
+    // a half warp per row: 16 lanes x 4 of this CTA's kDv head dims
+    const int l16 = lane & 15;
+    const int e4 = l16 * 4;
+    for (int lr = warp * 2 + (lane >> 4); lr < rows_per; lr += kThreads / 16) {
       const int rr = rank * rows_per + lr;
       const int R = qt * kRows + rr;
       if (rr >= kRows || R >= p.G * p.M) break;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int sw = (lane ^ (rr & 7)) << 2;   // the staged row's swizzled chunk
+      const int sw = (l16 ^ (rr & 7)) << 2;   // the staged row's swizzled chunk
       for (int q = 0; q < p.nsplit; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDh + sw);
+        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDv + sw);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -504,7 +516,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
         acc.w *= dv;
       }
       const int hl = R / p.M, m = R % p.M;
-      const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + e4;
+      const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + d0 + e4;
       if (p.out_fp8) {
         uchar4 cc;
         cc.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.x * rs, __NV_SATFINITE, __NV_E4M3));
@@ -616,8 +628,9 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   p.err = a.err;
   if (a.fp8 && (!a.kpre8 || !a.vtpre8 || !a.s_qkv || a.p16 % 16)) return cudaErrorInvalidValue;
   const int rows = p.G * p.M;
+  // z: KV head x the two halves of the head dims of O
   const dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>((rows + kRows - 1) / kRows),
-                  static_cast<unsigned>(a.Hkv));
+                  static_cast<unsigned>(a.Hkv * 2));
   LaunchOpts lo = o;
   lo.cluster = dim3(static_cast<unsigned>(a.nsplit), 1, 1);
   const size_t smem = attn_smem_bytes(a.kc, a.nsplit, a.fp8);
