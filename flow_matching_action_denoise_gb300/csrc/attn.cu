@@ -371,13 +371,22 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
-  float gmax = -INFINITY, gsum = 0.f;
-  for (int q = 0; q < p.nsplit; ++q) gmax = fmaxf(gmax, sStats[q * kRows + r].x);
-  for (int q = 0; q < p.nsplit; ++q) {
-    const float2 st = sStats[q * kRows + r];
-    gsum += st.y * exp2f(st.x - gmax);
+  // the row's global max and 1 / sum, once per row (the part-0 thread), in slice order
+  if (part == 0) {
+    float2 st[kMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q) st[q] = q < p.nsplit ? sStats[q * kRows + r] : make_float2(-INFINITY, 0.f);
+    float gm = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q) gm = fmaxf(gm, st[q].x);
+    float gs = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q)
+      if (q < p.nsplit) gs += st[q].y * exp2f(st[q].x - gm);
+    sPart[r] = make_float2(gm, 1.0f / gs);
   }
-  const float ginv = 1.0f / gsum;
+  __syncthreads();
+  const float gmax = sPart[r].x, ginv = sPart[r].y;
 
   // ---- pass 2: P = bf16(exp(s - m_part) * exp(m_part - M) / L) into the swizzled A
   // operand of P V
