@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* recvd = done + 1;   // the partial rows this CTA finalises have arrived from every rank
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -119,7 +120,13 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       mbar_init(&empty[i], 1);
     }
     mbar_init(done, 1);
+    mbar_init(recvd, 1);
     fence_mbar_init();
+    if (kCs > 1) {   // every rank sends 128 fp32 columns of each row m = rank (mod kCs), m < M
+      const int rk = static_cast<int>(cluster_rank());
+      const int owned = rk < p.M ? (p.M - 1 - rk) / kCs + 1 : 0;
+      mbar_arrive_expect_tx(recvd, static_cast<uint32_t>(kCs * owned * kTileN * 4));
+    }
     if (kMode != 2) tma_prefetch_desc(&tmA);
   }
   if (warp == 0) {
@@ -327,11 +334,13 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int rank = kCs > 1 ? static_cast<int>(cluster_rank()) : 0;
   const uint32_t recv_base = smem_u32(recv);
-  uint32_t peer[kCs];
+  uint32_t peer[kCs], peer_bar[kCs];
 #pragma unroll
-  for (int q = 0; q < kCs; ++q)
+  for (int q = 0; q < kCs; ++q) {
     peer[q] = (kCs > 1 ? map_dsmem(recv_base, static_cast<uint32_t>(q)) : recv_base) +
               static_cast<uint32_t>((rank * rows_per * kTileN + n_local) * 4);
+    peer_bar[q] = kCs > 1 ? map_dsmem(smem_u32(recvd), static_cast<uint32_t>(q)) : 0u;
+  }
   if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
   __syncwarp();                  // tcgen05.ld is warp-collective
   for (int c = colset * 16; c < p.n_pad; c += 32) {
@@ -343,16 +352,20 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
         // owner (c + i) % kCs == i % kCs since kCs divides 16; local row (c + i) / kCs
         const uint32_t addr = peer[i % kCs] + static_cast<uint32_t>(((c + i) / kCs) * kTileN * 4);
         if (kCs > 1)
-          st_dsmem_f32(addr, v[i]);
+          st_async_f32(addr, v[i], peer_bar[i % kCs]);   // counted on the owner's mbarrier
         else
           asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v[i]) : "memory");
       }
     }
   }
-  if (kCs > 1)
-    cluster_sync_all();   // all pushes into this CTA's receive buffer have landed
-  else
+  if (kCs > 1) {
+    // every rank's partial rows for this CTA have landed (no cluster-wide release barrier);
+    // the relaxed arrive, waited before exit, keeps this CTA alive while peers store into it
+    if (!mbar_wait(recvd, 0)) atomicOr(p.err, kErrPipelineTimeout);
+    cluster_arrive_relaxed();
+  } else {
     __syncthreads();
+  }
   if (!abort) {
     const int part = j / kCs;
     const int c4 = lane * 4;
@@ -448,6 +461,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       mbar_wait(&full[slot], last_use & 1, 100000000ull);
     }
   }
+  if (kCs > 1) cluster_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -221,6 +221,13 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
                ::"r"(dst), "r"(src), "r"(bytes), "r"(mbar)
                : "memory");
 }
+// Asynchronous 4-byte store into a CTA of the cluster, counted on that CTA's mbarrier
+// (shared::cluster addresses).
+__device__ __forceinline__ void st_async_f32(uint32_t dst, float a, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(dst), "f"(a),
+               "r"(mbar)
+               : "memory");
+}
 // Asynchronous 8-byte store into a CTA of the cluster, counted on that CTA's mbarrier
 // (shared::cluster addresses).
 __device__ __forceinline__ void st_async_v2(uint32_t dst, float a, float b, uint32_t mbar) {
