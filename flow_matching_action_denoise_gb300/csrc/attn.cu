@@ -47,8 +47,6 @@ constexpr int kDh = 128;             // head dim
 constexpr int kMaxSplit = 8;         // portable cluster size
 constexpr int kMaxKc = 192;          // keys per slice (MMA N of QK^T), multiple of 64
 constexpr int kTile = kRows * 128;   // bytes of one [128 rows][128 B] swizzled block
-constexpr int kDv = kDh / 2;         // head dims of O per CTA (the P V contraction's N)
-constexpr int kTileV = kDv * 128;    // bytes of one [kDv rows][128 B] block of V^T
 static_assert(kThreads % kDh == 0, "whole threads per head-dim row of V^T");
 
 struct KParams {
@@ -91,21 +89,21 @@ struct SmemPlan {
   size_t q, k, vt, pm, stage, recv, stats, part, bar, total;
 };
 // Operand tiles: Q [128 rows][Dh] (bf16: two 128-byte blocks, E4M3: one); K [kc keys][Dh]
-// likewise; P in blocks of [128 rows][128 bytes] and this CTA's half of V^T in blocks of
-// [kDv rows][128 bytes] along the keys (bf16: kc/64 blocks of 64 keys; E4M3: the keys
-// padded to a multiple of 128, one block per 128 keys).
+// likewise; P in blocks of [128 rows][128 bytes] and this CTA's dv head dims of V^T in
+// blocks of [dv rows][128 bytes] along the keys (bf16: kc/64 blocks of 64 keys; E4M3: the
+// keys padded to a multiple of 128, one block per 128 keys).
 __host__ __device__ inline int kblocks(int kc, bool fp8) { return fp8 ? (kc + 127) / 128 : kc / 64; }
-__host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8) {
+__host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8, int dv) {
   SmemPlan s;
   const size_t eb = fp8 ? 1 : 2;
   s.q = 0;
   s.k = eb * static_cast<size_t>(kTile);
   s.vt = s.k + static_cast<size_t>(kc) * 128 * eb;
-  s.pm = s.vt + static_cast<size_t>(kblocks(kc, fp8)) * kTileV;
+  s.pm = s.vt + static_cast<size_t>(kblocks(kc, fp8)) * dv * 128;
   const size_t main_end = s.pm + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
   const int rows_per = (kRows + nsplit - 1) / nsplit;
-  const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * kDv * 4;
-  const size_t stage_bytes = static_cast<size_t>(kRows) * kDv * 4;
+  const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * dv * 4;
+  const size_t stage_bytes = static_cast<size_t>(kRows) * dv * 4;
   size_t end = main_end;
   // this CTA's O share is staged in V^T and P (dead once P V completed) when they are
   // large enough; the O receive buffer reuses Q and K (dead once every CTA passed the
@@ -129,15 +127,20 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8) {
   return s;
 }
 
-template <int KC, bool kF8>
+// kDv: head dims of O per CTA (the P V contraction's N): kDh, or kDh / 2 when the two
+// halves run as two CTAs that repeat S and the softmax (small grids, where the O
+// exchange through distributed shared memory dominates)
+template <int KC, bool kF8, int kDv>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
+  constexpr int kTileV = kDv * 128;   // bytes of one [kDv rows][128 B] block of V^T
+  constexpr int kDsplit = kDh / kDv;
   constexpr int kPart = KC / kParts;            // keys of the slice handled by one thread of a row
   constexpr int kBlk = kF8 ? (KC + 127) / 128 : KC / 64;   // key blocks of the P V contraction
   constexpr int kKcp = kF8 ? kBlk * 128 : KC;   // keys of the P V contraction (E4M3: zero padded)
   constexpr int kRowChunks = kF8 ? 8 : 16;      // 16-byte chunks of one Dh-wide row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemPlan sp = smem_plan(KC, p.nsplit, kF8);
+  const SmemPlan sp = smem_plan(KC, p.nsplit, kF8, kDv);
   // S done, O done, every slice's statistics received, this CTA's O band received
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + sp.bar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
@@ -148,8 +151,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
 
   const int split = blockIdx.x;
   const int qt = blockIdx.y;
-  const int g = blockIdx.z >> 1;          // KV head
-  const int d0 = (blockIdx.z & 1) * kDv;  // this CTA's head dims of O: [d0, d0 + kDv)
+  const int g = blockIdx.z / kDsplit;              // KV head
+  const int d0 = (blockIdx.z % kDsplit) * kDv;     // this CTA's head dims of O: [d0, d0 + kDv)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, part = warp >> 2;
@@ -502,10 +505,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // ---- sum the slices' shares in fixed slice order, quantise, store
   if (s_abort == 0) {
     const int rank = static_cast<int>(cluster_rank());
-    // a half warp per row: 16 lanes x 4 of this CTA's kDv head dims
-    const int l16 = lane & 15;
+    // kDv / 4 lanes per row, 4 head dims each
+    constexpr int kLanesRow = kDv / 4;
+    constexpr int kRowsWarp = 32 / kLanesRow;
+    const int l16 = lane % kLanesRow;
     const int e4 = l16 * 4;
-    for (int lr = warp * 2 + (lane >> 4); lr < rows_per; lr += kThreads / 16) {
+    for (int lr = warp * kRowsWarp + lane / kLanesRow; lr < rows_per; lr += (kThreads / 32) * kRowsWarp) {
       const int rr = rank * rows_per + lr;
       const int R = qt * kRows + rr;
       if (rr >= kRows || R >= p.G * p.M) break;
@@ -590,17 +595,25 @@ int attn_plan(int M, int P, int* kc, int* nsplit) {
   return FM_OK;
 }
 
-size_t attn_smem_bytes(int kc, int nsplit, int fp8) { return 1024 + smem_plan(kc, nsplit, fp8 != 0).total; }
+size_t attn_smem_bytes(int kc, int nsplit, int fp8, int dv) {
+  return 1024 + smem_plan(kc, nsplit, fp8 != 0, dv).total;
+}
 
 namespace {
 
 cudaError_t attn_configure_impl() {
-  const void* ks[6] = {reinterpret_cast<const void*>(attn_kernel<64, false>),
-                       reinterpret_cast<const void*>(attn_kernel<128, false>),
-                       reinterpret_cast<const void*>(attn_kernel<192, false>),
-                       reinterpret_cast<const void*>(attn_kernel<64, true>),
-                       reinterpret_cast<const void*>(attn_kernel<128, true>),
-                       reinterpret_cast<const void*>(attn_kernel<192, true>)};
+  const void* ks[12] = {reinterpret_cast<const void*>(attn_kernel<64, false, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<128, false, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<192, false, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<64, true, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<128, true, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<192, true, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<64, false, kDh / 2>),
+                        reinterpret_cast<const void*>(attn_kernel<128, false, kDh / 2>),
+                        reinterpret_cast<const void*>(attn_kernel<192, false, kDh / 2>),
+                        reinterpret_cast<const void*>(attn_kernel<64, true, kDh / 2>),
+                        reinterpret_cast<const void*>(attn_kernel<128, true, kDh / 2>),
+                        reinterpret_cast<const void*>(attn_kernel<192, true, kDh / 2>)};
   for (const void* k : ks) {
     const cudaError_t e = allow_max_dynamic_smem(k);
     if (e != cudaSuccess) return e;
@@ -637,19 +650,36 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   p.err = a.err;
   if (a.fp8 && (!a.kpre8 || !a.vtpre8 || !a.s_qkv || a.p16 % 16)) return cudaErrorInvalidValue;
   const int rows = p.G * p.M;
-  // z: KV head x the two halves of the head dims of O
-  const dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>((rows + kRows - 1) / kRows),
-                  static_cast<unsigned>(a.Hkv * 2));
+  const int tiles = (rows + kRows - 1) / kRows;
+  // The two halves of O's head dims become two CTAs (repeating S and the softmax) while
+  // the doubled grid still fits in one wave on half the SMs; larger grids keep one CTA.
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      sms = 148;
+  }
+  const bool dsplit = 4 * a.nsplit * tiles * a.Hkv <= sms;
+  // z: KV head x (with the split) the two halves of the head dims of O
+  const dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>(tiles),
+                  static_cast<unsigned>(a.Hkv * (dsplit ? 2 : 1)));
   LaunchOpts lo = o;
   lo.cluster = dim3(static_cast<unsigned>(a.nsplit), 1, 1);
-  const size_t smem = attn_smem_bytes(a.kc, a.nsplit, a.fp8);
-  switch (a.kc * 2 + (a.fp8 ? 1 : 0)) {
-    case 128: return launch(attn_kernel<64, false>, grid, dim3(kThreads), smem, lo, p);
-    case 256: return launch(attn_kernel<128, false>, grid, dim3(kThreads), smem, lo, p);
-    case 384: return launch(attn_kernel<192, false>, grid, dim3(kThreads), smem, lo, p);
-    case 129: return launch(attn_kernel<64, true>, grid, dim3(kThreads), smem, lo, p);
-    case 257: return launch(attn_kernel<128, true>, grid, dim3(kThreads), smem, lo, p);
-    case 385: return launch(attn_kernel<192, true>, grid, dim3(kThreads), smem, lo, p);
+  const size_t smem = attn_smem_bytes(a.kc, a.nsplit, a.fp8, dsplit ? kDh / 2 : kDh);
+  switch ((a.kc * 2 + (a.fp8 ? 1 : 0)) * 2 + (dsplit ? 1 : 0)) {
+    case 256: return launch(attn_kernel<64, false, kDh>, grid, dim3(kThreads), smem, lo, p);
+    case 512: return launch(attn_kernel<128, false, kDh>, grid, dim3(kThreads), smem, lo, p);
+    case 768: return launch(attn_kernel<192, false, kDh>, grid, dim3(kThreads), smem, lo, p);
+    case 258: return launch(attn_kernel<64, true, kDh>, grid, dim3(kThreads), smem, lo, p);
+    case 514: return launch(attn_kernel<128, true, kDh>, grid, dim3(kThreads), smem, lo, p);
+    case 770: return launch(attn_kernel<192, true, kDh>, grid, dim3(kThreads), smem, lo, p);
+    case 257: return launch(attn_kernel<64, false, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
+    case 513: return launch(attn_kernel<128, false, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
+    case 769: return launch(attn_kernel<192, false, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
+    case 259: return launch(attn_kernel<64, true, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
+    case 515: return launch(attn_kernel<128, true, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
+    case 771: return launch(attn_kernel<192, true, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
     default: return cudaErrorInvalidValue;
   }
 }

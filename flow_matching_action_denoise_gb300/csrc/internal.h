@@ -232,7 +232,7 @@ struct AttnArgs {
 };
 // Slice plan for P + M keys; FM_ERR_SHAPE when they need more than 8 x 192.
 int attn_plan(int M, int P, int* kc, int* nsplit);
-size_t attn_smem_bytes(int kc, int nsplit, int fp8);
+size_t attn_smem_bytes(int kc, int nsplit, int fp8, int dv);   // dv: head dims of O per CTA
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
 cudaError_t attn_configure();
 // E4M3 copies of prefix rows [b, e) of every layer: k8 = E4M3(k * (1/s_k)), v8t likewise
