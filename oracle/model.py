@@ -67,16 +67,39 @@ def recip32(s) -> np.float64:
     return np.float64(F32(1.0) / F32(s))
 
 
+def quant_nvfp4_act(h: np.ndarray, ts: float):
+    """NVFP4 activation operand for a four-bit (W4A4) GEMM (news article "FlashRT-PAI",
+    sections "It optimises the relay" and the four-bit pi0.5 results): the tensor scale
+    ts is static (calibrated like the FP8 scales, amax / (448 * 6)); the block scales
+    are the activation's own, one per 16 consecutive K elements of a row:
+    bs = E4M3_RNE_sat(fp32(amax_b / fp32(6 ts))), e = E2M1_RNE_sat(fp32(h / fp32(bs ts))),
+    0 where bs ts = 0. Returns (e * bs as values [M][K], bs [M][K/16])."""
+    h = np.asarray(h, np.float64)
+    m, k = h.shape
+    blocks = h.reshape(m, k // 16, 16)
+    amax_b = np.max(np.abs(blocks), axis=-1)
+    six_ts = np.float64(F32(6.0) * F32(ts))
+    bs = C.e4m3(C.fp32(amax_b / six_ts))
+    denom = C.fp32(bs * np.float64(F32(ts)))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.where(denom[..., None] > 0,
+                     C.e2m1(C.fp32(blocks / np.where(denom > 0, denom, 1.0)[..., None])), 0.0)
+    return (e * bs[..., None]).reshape(m, k), bs
+
+
 def quant_codes(h: np.ndarray, s: float, fmt: str) -> np.ndarray:
     """Static-scale activation quantisation; returns the operand codes as values.
 
     fp8: code = E4M3_RNE_sat(h * fp32(1/s)); the GEMM later multiplies by s.
     bf16: code = bf16_RNE(h) (no scale).
+    nvfp4: e * bs of quant_nvfp4_act with tensor scale s; the GEMM multiplies by s.
     """
     if fmt == "fp8":
         return C.e4m3(np.asarray(h, np.float64) * recip32(s))
     if fmt == "bf16":
         return C.bf16(h)
+    if fmt == "nvfp4":
+        return quant_nvfp4_act(h, s)[0]
     raise ValueError(fmt)
 
 
@@ -273,8 +296,8 @@ def layer_forward(model: Model, l: int, k: int, x: np.ndarray, q: np.ndarray,
     H, Hkv, Dh, F, af = cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.act_fmt
     sc1, sh1, g1, sc2, sh2, g2 = model.mods[k][0][l]
     w = model.w[l]
-    s = act_scales[l] if af == "fp8" else None   # bf16 operands carry no scale
-    sa = lambda i: float(s[i]) if af == "fp8" else 1.0
+    s = act_scales[l] if af in ("fp8", "nvfp4") else None   # bf16 operands carry no scale
+    sa = lambda i: float(s[i]) if af in ("fp8", "nvfp4") else 1.0
 
     qkv = gemm(q, sa(SITE_ATTN_IN), w["qkv"])
     nq, nk = H * Dh, Hkv * Dh
@@ -314,7 +337,7 @@ def pre_attn_quant(model: Model, l: int, k: int, x, act_scales, amax=None):
     h = ada_norm(x, sc1, sh1, cfg.eps)
     if amax is not None:
         amax[l, SITE_ATTN_IN] = max(amax[l, SITE_ATTN_IN], np.max(np.abs(h)))
-    s = float(act_scales[l][SITE_ATTN_IN]) if cfg.act_fmt == "fp8" else 1.0
+    s = float(act_scales[l][SITE_ATTN_IN]) if cfg.act_fmt in ("fp8", "nvfp4") else 1.0
     return quant_codes(h, s, cfg.act_fmt)
 
 
@@ -386,7 +409,9 @@ def calibrate(model: Model, noise, kpre, vpre, provisional_scales) -> np.ndarray
     decode(model, noise, kpre, vpre, provisional_scales, amax)
     out = np.asarray(provisional_scales, np.float32).copy()
     nz = amax > 0
-    out[nz] = (amax[nz].astype(np.float32) / F32(448.0)).astype(np.float32)
+    # E4M3: amax / 448; NVFP4 activations: the tensor scale amax / (448 * 6)
+    div = F32(2688.0) if cfg.act_fmt == "nvfp4" else F32(448.0)
+    out[nz] = (amax[nz].astype(np.float32) / div).astype(np.float32)
     return out
 
 
