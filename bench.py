@@ -255,11 +255,7 @@ def run_ours(args, rank, world, local_rank):
         vpol.close()
 
     # ---- max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = t.tolist()
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], device)
     pol.close()
     if rank != 0:
         return None
@@ -267,7 +263,7 @@ def run_ours(args, rank, world, local_rank):
     peak_gbs, peak_kind = measured_peaks()
     ab = algorithmic_bytes(cfg)
     lat_ms = total_ms / args.steps
-    value = total_ms / (args.steps * world)
+    value = aggregate_ms_per_decision(total_ms, args.steps, world)
     achieved_gbs = ab["total"] / (lat_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -523,6 +519,24 @@ def cpu_baseline(cfg, samples: int = 1):
     return {"value": round(statistics.median(times), 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{what} of {cfg.name} (FP64 numpy, weights prepared outside the timing), "
                       f"scaled to one {cfg.L}-layer x {cfg.S}-step decision"}
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (every rank calls it; one rank returns
+    its own): the slowest replica sets the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_ms_per_decision(total_ms: float, steps: int, world: int) -> float:
+    """Whole-job figure for N replicas that each ran `steps` decisions in (the max of)
+    total_ms: time per decision of the job."""
+    return total_ms / (steps * world)
 
 
 def run_reference(args, rank, world):
