@@ -42,7 +42,7 @@ EXPORTS = [
     "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
     "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer", "fm_gemm_consumer_noalloc",
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
-    "fm_session_workspace_size", "fm_session_create", "fm_session_fork",
+    "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes",
 ]
 
 
@@ -129,6 +129,7 @@ def load() -> ctypes.CDLL:
         "fm_decode_warm": (i, [vp, vp, i, vp, vp]),
         "fm_episode_reset": (i, [vp]),
         "fm_session_workspace_size": (i, [vp, ctypes.POINTER(sz)]),
+        "fm_abi_sizes": (i, [ctypes.POINTER(sz)] * 4),
         "fm_session_create": (i, [vp, vp, sz, vp, ctypes.POINTER(vp)]),
         "fm_session_fork": (i, [vp, vp, sz, i, vp, sz, vp, ctypes.POINTER(vp)]),
     }

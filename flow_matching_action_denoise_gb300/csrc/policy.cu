@@ -892,6 +892,14 @@ const char* fm_status_string(int s) {
 
 const char* fm_last_error(const fm_policy* p) { return p ? p->err.c_str() : g_last_error.c_str(); }
 
+int fm_abi_sizes(size_t* config, size_t* weights, size_t* layer_weights, size_t* timing) {
+  if (config) *config = sizeof(fm_config);
+  if (weights) *weights = sizeof(fm_weights);
+  if (layer_weights) *layer_weights = sizeof(fm_layer_weights);
+  if (timing) *timing = sizeof(fm_timing);
+  return FM_OK;
+}
+
 int fm_workspace_size(const fm_config* cfg, size_t* bytes) {
   std::string why;
   int st = validate(cfg, &why);

@@ -171,6 +171,11 @@ const char* fm_last_error(const fm_policy* p);
 /* Bytes of device workspace a policy with this config needs (host call). */
 int fm_workspace_size(const fm_config* cfg, size_t* bytes);
 
+/* sizeof of the ABI structs as this library was compiled (fm_config, fm_weights,
+ * fm_layer_weights, fm_timing), for bindings to check their mirrors. Any pointer may
+ * be NULL. Never fails. */
+int fm_abi_sizes(size_t* config, size_t* weights, size_t* layer_weights, size_t* timing);
+
 /* Build a policy in a caller-owned workspace (device, 1024-byte aligned,
  * >= fm_workspace_size bytes). Folds gamma into the GEMM weights, computes each
  * weight's static scale (amax/448 for FP8; amax/(448*6) tensor scale plus E4M3

@@ -124,3 +124,13 @@ def test_session_entry_points_validate_without_a_gpu(lib):
     assert lib.fm_session_create(None, 1024, 1 << 20, None, ctypes.byref(out)) == 1 and out.value is None
     assert lib.fm_session_fork(None, None, 0, 1, 1024, 1 << 20, None, ctypes.byref(out)) == 1
     assert lib.policy_destroy(None) == 1
+
+
+def test_binding_struct_mirrors_match_the_library(lib):
+    sizes = [ctypes.c_size_t() for _ in range(4)]
+    assert lib.fm_abi_sizes(*[ctypes.byref(s) for s in sizes]) == 0
+    cfg, w, lw, t = (s.value for s in sizes)
+    assert cfg == ctypes.sizeof(fmad.FmConfig)
+    assert w == ctypes.sizeof(fmad.FmWeights)
+    assert lw == ctypes.sizeof(fmad.FmLayerWeights)
+    assert t == ctypes.sizeof(fmad.FmTiming)
