@@ -134,3 +134,13 @@ def test_binding_struct_mirrors_match_the_library(lib):
     assert w == ctypes.sizeof(fmad.FmWeights)
     assert lw == ctypes.sizeof(fmad.FmLayerWeights)
     assert t == ctypes.sizeof(fmad.FmTiming)
+
+
+def test_attention_plan_limits_are_validated(lib):
+    # keys = P + M must fit 8 key slices of at most 192 keys
+    ok = fmad.make_config(fm_synth.config("expert_fp8_m50", P=1536 - 50))
+    assert fmad.workspace_size(ok) > 0
+    bad = fmad.make_config(fm_synth.config("expert_fp8_m50", P=1536 - 49))
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(bad)
+    assert e.value.status == 2 and "attention plan" in str(e.value)
