@@ -1,6 +1,7 @@
 """The stage-by-stage checker the GPU parity tests use (tests/_stagewise.py),
-exercised on CPU: records produced by the oracle itself in the trace's layout
-pass, and records from an implementation with a plausible mistake (gate and up
+exercised on CPU for FP8 and BF16 decisions: records produced by the oracle
+itself in the trace's layout pass, and records from an implementation with a
+plausible mistake (gate and up
 swapped, a dropped residual gate, the Euler sign, the next layer's modulation in
 the pre-MLP norm, K and V swapped in the QKV output, a wrong dequantisation
 scale) each fail it."""
@@ -14,14 +15,14 @@ from oracle import model as O
 from _stagewise import check_decision_stages
 
 
-def tiny():
+def tiny(fmt="fp8"):
     cfg = fm_synth.Config(name="tiny_stages", L=2, S=2, M=3, d=32, H=2, Hkv=1, Dh=16, F=64, P=4, A=4,
-                          weight_fmt="fp8", act_fmt="fp8", seed=21)
+                          weight_fmt=fmt, act_fmt=fmt, seed=21)
     layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
     model = O.Model(cfg, layers, fm_synth.final_weights(cfg))
     kp, vp = fm_synth.prefix_kv(cfg)
     nz = fm_synth.noise(cfg, 0)
-    sc = O.calibrate(model, nz, kp, vp, np.full((cfg.L, 4), 0.05, np.float32))
+    sc = O.calibrate(model, nz, kp, vp, np.full((cfg.L, 4), 0.05, np.float32)) if fmt == "fp8" else None
     return cfg, model, kp, vp, nz, sc
 
 
@@ -29,9 +30,11 @@ def records(cfg, model, kp, vp, nz, sc, mistake=None):
     """What a decision's trace holds, computed by the oracle's stages (optionally
     with one planted mistake)."""
     M, H, Dh, F, L, S, d = cfg.M, cfg.H, cfg.Dh, cfg.F, cfg.L, cfg.S, cfg.d
+    fmt = cfg.act_fmt
+    s_act = lambda l, i: float(sc[l][i]) if fmt == "fp8" else 1.0
     fin = model.final
     nq, nk = H * Dh, cfg.Hkv * Dh
-    dq = lambda l, i, w: np.float64(np.float32(sc[l][i]) * np.float32(w.scale)) * (
+    dq = lambda l, i, w: np.float64(np.float32(s_act(l, i)) * np.float32(w.scale)) * (
         2.0 if mistake == "dequant" and i == 1 else 1.0)
     kp64, vp64 = np.asarray(kp, np.float64), np.asarray(vp, np.float64)
     a = np.asarray(nz, np.float64)
@@ -45,21 +48,21 @@ def records(cfg, model, kp, vp, nz, sc, mistake=None):
             if mistake == "next_layer_mod":
                 sc2, sh2 = model.mods[k][0][(l + 1) % L][3], model.mods[k][0][(l + 1) % L][4]
             r["x_in"] = x
-            r["q"] = O.quant_codes(O.ada_norm(x, sc1, sh1, cfg.eps), sc[l][0], "fp8")
+            r["q"] = O.quant_codes(O.ada_norm(x, sc1, sh1, cfg.eps), s_act(l, 0), fmt)
             qkv = C.bf16((r["q"] @ W["qkv"].codes.T) * dq(l, 0, W["qkv"]))
             if mistake == "kv_swapped":
                 qkv = np.concatenate([qkv[:, :nq], qkv[:, nq + nk:], qkv[:, nq:nq + nk]], axis=1)
             r["y_qkv"] = qkv
             att = O.attention(qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], kp64[l], vp64[l], H, cfg.Hkv, Dh)
-            r["attn_out"] = O.quant_codes(att, sc[l][1], "fp8")
+            r["attn_out"] = O.quant_codes(att, s_act(l, 1), fmt)
             yo = r["attn_out"] @ W["o"].codes.T
             r["y_o"] = np.zeros((0, M, d))
             x_mid = x + (1.0 if mistake == "dropped_gate" else g1) * yo * dq(l, 1, W["o"])
             r["x_mid"] = x_mid
-            r["q2"] = O.quant_codes(O.ada_norm(x_mid, sc2, sh2, cfg.eps), sc[l][2], "fp8")
+            r["q2"] = O.quant_codes(O.ada_norm(x_mid, sc2, sh2, cfg.eps), s_act(l, 2), fmt)
             gu = (r["q2"] @ W["gu"].codes.T) * dq(l, 2, W["gu"])
             g, u = (gu[:, F:], gu[:, :F]) if mistake == "gate_up_swapped" else (gu[:, :F], gu[:, F:])
-            r["geglu_out"] = O.quant_codes(O.gelu_tanh(g) * u, sc[l][3], "fp8")
+            r["geglu_out"] = O.quant_codes(O.gelu_tanh(g) * u, s_act(l, 3), fmt)
             r["y_d"] = np.zeros((0, M, d))
             x = x_mid + g2 * (r["geglu_out"] @ W["d"].codes.T) * dq(l, 3, W["d"])
             if l == L - 1:
@@ -74,9 +77,9 @@ def records(cfg, model, kp, vp, nz, sc, mistake=None):
     return recs
 
 
-@pytest.fixture(scope="module")
-def case():
-    return tiny()
+@pytest.fixture(scope="module", params=["fp8", "bf16"])
+def case(request):
+    return tiny(request.param)
 
 
 def test_oracle_records_pass(case):
