@@ -16,7 +16,7 @@ import numpy as np
 __all__ = [
     "FmError", "lib", "load", "FmConfig", "make_config", "workspace_size", "policy_create",
     "policy_destroy", "set_prefix_kv", "refresh_prefix", "decode_actions", "decode_actions_host",
-    "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status",
+    "state_size", "snapshot_state", "restore_state", "fm_set_act_scales", "device_status", "standalone_status",
     "kernel_count", "philox_noise", "decode_actions_seeded", "last_timing", "decode_warm", "episode_reset", "Session",
     "session_workspace_size", "session_create", "session_fork", "FmTiming", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
     "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "named_buffer", "Policy", "DeviceWeights",
@@ -42,7 +42,7 @@ EXPORTS = [
     "fm_test_consumer", "fm_test_layer", "fm_named_buffer", "fm_trace_size", "fm_decode_trace",
     "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer", "fm_gemm_consumer_noalloc",
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
-    "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes",
+    "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes", "fm_standalone_status",
 ]
 
 
@@ -108,6 +108,7 @@ def load() -> ctypes.CDLL:
         "snapshot_state": (i, [vp, vp, sz, i, vp]),
         "restore_state": (i, [vp, vp, sz, i, vp]),
         "fm_device_status": (i, [vp, vp, ctypes.POINTER(i)]),
+        "fm_standalone_status": (i, [vp, ctypes.POINTER(i)]),
         "fm_test_kernel_count": (i, [vp, ctypes.POINTER(i), ctypes.POINTER(i)]),
         "fm_test_quant_e4m3": (i, [vp, ctypes.c_int64, ctypes.c_float, vp, vp]),
         "fm_packed_weight_bytes": (i, [i, i, i, ctypes.POINTER(sz)]),
@@ -311,6 +312,17 @@ def device_status(p: int, stream=None) -> int:
     st = load().fm_device_status(p, _stream(stream), ctypes.byref(w))
     if st not in (0, 7):
         _check(st, "fm_device_status", p)
+    return w.value
+
+
+def standalone_status(stream=None) -> int:
+    """Read and clear the error word of the policy-free building blocks (fm_test_skinny_gemm,
+    fm_gemm_consumer, fm_gemm_consumer_noalloc) after synchronising the stream; 0 = no
+    kernel of theirs abandoned a bounded wait."""
+    w = ctypes.c_int()
+    st = load().fm_standalone_status(_stream(stream), ctypes.byref(w))
+    if st not in (0, 7):
+        _check(st, "fm_standalone_status")
     return w.value
 
 

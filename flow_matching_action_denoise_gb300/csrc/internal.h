@@ -267,6 +267,10 @@ int gemm_consumer_scratch_bytes(int M, int N, int K, int fmt, int s, size_t* byt
 int gemm_consumer_run(const GemmConsumerArgs& g, float* scratch, size_t scratch_bytes, int* err_word,
                       cudaStream_t st, const char** why);
 
+// Device address of fm_gemm_consumer_noalloc's error word on device `dev` (nullptr
+// before that entry point's first call there).
+int* noalloc_error_word(int dev);
+
 // Record `why` as the thread's last policy-free error (what fm_last_error(NULL)
 // reports) and return `status`.
 int record_error(int status, const char* why);

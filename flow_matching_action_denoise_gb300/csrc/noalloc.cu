@@ -36,6 +36,18 @@ int* g_err_addr[kMaxDevices] = {};
 
 }  // namespace
 
+namespace fm {
+
+// The device address of this file's error word on device `dev`, or nullptr when no
+// call has set it up there yet (then no launch of this entry point could have set it).
+int* noalloc_error_word(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  return g_err_addr[dev];
+}
+
+}  // namespace fm
+
 extern "C" int fm_gemm_consumer_noalloc(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s,
                                         const float* s_a, const float* s_w, const float* bias, float* x,
                                         const float* gate, const float* scale, const float* shift, float eps,

@@ -1352,6 +1352,25 @@ int fm_device_status(fm_policy* p, void* stream, int* word) {
   return w ? fail(p, FM_ERR_DEVICE, "a kernel abandoned a bounded wait") : FM_OK;
 }
 
+int fm_standalone_status(void* stream, int* word) {
+  if (!word) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  int* words[2] = {nullptr, nullptr};
+  FM_CUDA(nullptr, cudaGetDevice(&dev));
+  FM_CUDA(nullptr, cudaGetSymbolAddress(reinterpret_cast<void**>(&words[0]), fm_standalone_err));
+  words[1] = fm::noalloc_error_word(dev);
+  int got[2] = {0, 0};
+  for (int i = 0; i < 2; ++i) {
+    if (!words[i]) continue;
+    FM_CUDA(nullptr, cudaMemcpyAsync(&got[i], words[i], sizeof(int), cudaMemcpyDeviceToHost, s));
+    FM_CUDA(nullptr, cudaMemsetAsync(words[i], 0, sizeof(int), s));
+  }
+  FM_CUDA(nullptr, cudaStreamSynchronize(s));
+  *word = got[0] | got[1];
+  return *word ? fail(nullptr, FM_ERR_DEVICE, "a standalone kernel abandoned a bounded wait") : FM_OK;
+}
+
 int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* bytes) {
   if (!p || !name || !ptr || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
   const fm_config& c = p->cfg;

@@ -307,6 +307,14 @@ int fm_session_fork(fm_policy* base, const void* capsule, size_t bytes, int caps
  * wait (1 = TMA/MMA pipeline wait expired). */
 int fm_device_status(fm_policy* p, void* stream, int* word);
 
+/* Error word of the policy-free building blocks (fm_test_skinny_gemm, fm_gemm_consumer,
+ * fm_gemm_consumer_noalloc): synchronise `stream`, read and clear the bits their kernels
+ * set when they abandoned a bounded wait on the current device. Returns FM_OK, or
+ * FM_ERR_DEVICE with *word = the bits (1 = TMA/MMA pipeline wait expired); the outputs of
+ * the calls since the previous check are then not to be trusted. Those entry points are
+ * asynchronous, so they cannot report this themselves. */
+int fm_standalone_status(void* stream, int* word);
+
 /* Address and size of one of the policy's named persistent buffers (the
  * execution contract's named buffers), for inspection and for zero-copy input:
  *   "prefix_k"              bf16 [L][P][Hkv][Dh]

@@ -96,6 +96,7 @@ def run_gemm(device, a_bytes_or_bf16, M, K, packed_host, N, fmt, s, cs):
     out = torch.full((nparts, M, N), float("nan"), dtype=torch.float32, device=device)
     fmad.fm_test_skinny_gemm(a, M, K, ptr, N, fmt, s, cs, out)
     torch.cuda.synchronize()
+    assert fmad.standalone_status() == 0, "a GEMM pipeline wait expired"
     return out.cpu().numpy().astype(np.float64)
 
 
@@ -226,6 +227,7 @@ def run_gemm_consumer(device, inp, M, K, N, fmt, s, entry="scratch"):
     else:
         fmad.fm_gemm_consumer_noalloc(*args)
     torch.cuda.synchronize()
+    assert fmad.standalone_status() == 0, "a GEMM pipeline wait expired"
     return x.cpu().numpy().astype(np.float64), q
 
 

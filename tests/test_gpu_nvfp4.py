@@ -70,6 +70,7 @@ def run_nvfp4_gemm(device, a_values, w_ptr, M, K, N, s):
     out = torch.full((s, M, N), float("nan"), dtype=torch.float32, device=device)
     fmad.fm_test_skinny_gemm(a, M, K, w_ptr, N, fmad.FMT_NVFP4, s, 1, out)
     torch.cuda.synchronize()
+    assert fmad.standalone_status() == 0, "a GEMM pipeline wait expired"
     return out.cpu().numpy().astype(np.float64)
 
 

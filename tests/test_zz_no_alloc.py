@@ -45,6 +45,26 @@ def test_noalloc_matches_scratch_entry_on_consecutive_calls():
         check_gemm_consumer_outputs(x_na, q_na, x_oracle, q_oracle, fmt)
 
 
+def test_noalloc_allocates_nothing_after_its_first_call():
+    """Once the first call on this device has looked the built-in array up, a call
+    changes neither torch's allocator state nor the device's free memory."""
+    device = require_gpu()
+    M, K, N, s, fmt = 50, 1024, 8192, 2, fmad.FMT_FP8
+    inp, _, _ = gemm_consumer_case(device, M, K, N, fmt, seed=31)
+    x = inp["x0"].clone()
+    q = torch.empty((M, N), dtype=torch.uint8, device=device)
+    args = (inp["a"], M, K, inp["w"][1], N, fmt, s, inp["s_a"], inp["s_w"], inp["bias"], x, inp["gate"],
+            inp["scale"], inp["shift"], 1e-6, inp["s_q"], q)
+    fmad.fm_gemm_consumer_noalloc(*args)   # first call: symbol lookup, kernel modules loaded
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(device), torch.cuda.mem_get_info(device)[0]
+    fmad.fm_gemm_consumer_noalloc(*args)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(device) == alloc0
+    assert torch.cuda.mem_get_info(device)[0] == free0
+    assert fmad.standalone_status() == 0
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     device = require_gpu()
     M, K, N, s = 256, 1024, 16384, 1   # 256 x 16384 x 4 bytes = 16 MiB of partials
