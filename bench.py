@@ -235,9 +235,13 @@ def run_ours(args, rank, world, local_rank):
     sess.close()
     warm = time_warm_start(cfg, weights_for_warm, scales, k_dev, v_dev, noise, device, stream, args)
 
-    # ---- dominant kernel timed alone: the gate|up GEMM, rotating weight copies
-    gemm = time_dominant_gemm(cfg, pol, device, stream) if cfg.weight_fmt == "fp8" else \
-        time_dominant_gemm_nvfp4(cfg, device, stream)
+    # ---- dominant kernel timed alone: the gate|up GEMM, rotating weight copies; the
+    # decision's own variant (GeGLU + E4M3 epilogue) and the fp32-plane building block
+    if cfg.weight_fmt == "fp8":
+        gemm = time_decision_gemm(cfg, scales, device)
+        gemm_planes = time_dominant_gemm(cfg, pol, device, stream)
+    else:
+        gemm, gemm_planes = time_dominant_gemm_nvfp4(cfg, device, stream), None
 
     # ---- launch-mode variants (PDL off, graph off), same kernels and inputs
     variant_ms = {}
@@ -294,6 +298,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_ms / args.steps, 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(h_noise.numel() * 4), "d2h_bytes_per_step": int(h_act.numel() * 4)},
         "roofline": gemm,
+        **({"roofline_planes_variant": gemm_planes} if gemm_planes else {}),
         "gpu_launches": int(per_decision * args.steps),
         "kernels_per_layer": per_layer,
         "launch_variants_ms": variant_ms,
@@ -375,10 +380,49 @@ def time_graph(device, launches, replays=5):
     return us
 
 
+def time_decision_gemm(cfg, scales, device, index=4):
+    """The gate|up GEMM exactly as the decision launches it (GeGLU + E4M3 epilogue,
+    the decision's split and cluster; kernel `index` of a layer-step), launched back to
+    back through fm_test_launch_kernel over the layers of a policy whose packed weights
+    rotate through more than 2x L2, timed with CUDA events on the replay stream.
+    Algorithmic bytes per launch: weights N K + activations M K + GeGLU codes M N / 2."""
+    import dataclasses
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+
+    N, K, M = 2 * cfg.F, cfg.d, cfg.M
+    l2 = l2_bytes(device)
+    R = int(np.ceil(2 * l2 / (N * K))) + 1
+    rcfg = dataclasses.replace(cfg, L=R, S=1)
+    layer = fm_synth.layer_weights(rcfg, 0)
+    pol = fmad.Policy(rcfg, [layer] * R, fm_synth.final_weights(rcfg), act_scales=np.tile(scales[:1], (R, 1)),
+                      device=device)
+    kp, vp = fm_synth.prefix_kv(dataclasses.replace(rcfg, L=1))
+    pol.set_prefix_kv(torch.from_numpy(np.repeat(kp, R, 0)).to(device, torch.bfloat16),
+                      torch.from_numpy(np.repeat(vp, R, 0)).to(device, torch.bfloat16))
+    noise = torch.from_numpy(fm_synth.noise(rcfg, 0)).to(device)
+    pol.decode(noise)   # fills every buffer the kernel reads
+    torch.cuda.synchronize(device)
+    launches = [lambda st, l=l: fmad.launch_kernel(pol.handle, l, 0, index, st) for l in range(R)] * 2
+    us = time_graph(device, launches)
+    if fmad.device_status(pol.handle):
+        raise RuntimeError("device error word set (decision GEMM timing)")
+    pol.close()
+    algo = N * K + M * K + M * (N // 2)
+    peak, kind = measured_peaks()
+    achieved = algo / (us * 1e-6) / 1e9
+    return {"kernel": f"skinny_gemm_kernel<fp8> gate|up + GeGLU epilogue as in the decision (N={N}, K={K}, M={M})",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": peak_kind_note(kind),
+            "traffic": profiled_traffic(), "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
+            "timing": f"CUDA graph of back-to-back launches over {R} layers' weights (> 2x L2), CUDA events"}
+
+
 def time_dominant_gemm(cfg, pol, device, stream):
-    """Average duration of the gate|up GEMM (the largest weight stream of a layer)
-    launched back to back through the C ABI over rotating packed weights (> 2x L2),
-    timed with CUDA events on the launching stream."""
+    """Average duration of the gate|up GEMM (the largest weight stream of a layer) as the
+    building block fm_test_skinny_gemm (fp32 partial planes), launched back to back through
+    the C ABI over rotating packed weights (> 2x L2), timed with CUDA events on the
+    launching stream."""
     import torch
     import flow_matching_action_denoise_gb300 as fmad
 
@@ -416,7 +460,7 @@ def time_dominant_gemm(cfg, pol, device, stream):
                       f"split {s}, cluster {cs})",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind_note(kind),
-            "traffic": profiled_traffic(), "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
+            "traffic": None, "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
             "timing": "CUDA graph of back-to-back launches over rotating weights (> 2x L2), CUDA events"}
 
 
@@ -483,42 +527,83 @@ def peak_kind_note(kind):
 
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
-def cpu_baseline(cfg, samples: int = 1):
-    """Time the FP64 oracle as it stands on this host's cores on a bounded sample of
-    the workload: whole Euler steps (two) of the 18-layer expert, or the first layers
-    of one step for larger decoders; scaled to ms per decision."""
-    from oracle import model as O
-    layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
-    model = O.Model(cfg, layers, fm_synth.final_weights(cfg))
-    del layers
-    kp, vp = fm_synth.prefix_kv(cfg)
-    kp, vp = kp.astype(np.float64), vp.astype(np.float64)
-    scales = fm_synth.default_act_scales(cfg)
-    a = fm_synth.noise(cfg, 0).astype(np.float64)
-    big = cfg.M * cfg.d > 100_000
-    n_layers = min(cfg.L, 4) if big else cfg.L
-    steps = 1 if big else 2
-    times = []
-    for _ in range(samples):
-        t0 = time.perf_counter()
-        if big:
-            x = a @ model.final["w_in"].T + model.final["b_in"]
-            for l in range(n_layers):
-                q = O.pre_attn_quant(model, l, 0, x, scales)
-                x = O.layer_forward(model, l, 0, x, q, kp, vp, scales)
-        else:
-            for k in range(steps):
-                a = O.euler_step(model, k, a, kp, vp, scales)
-        dt = time.perf_counter() - t0
-        times.append(dt / (steps * n_layers) * cfg.S * cfg.L * 1e3)
+def host_cores() -> dict:
     try:
-        cores = len(os.sched_getaffinity(0))
+        aff = len(os.sched_getaffinity(0))
     except AttributeError:
-        cores = os.cpu_count()
+        aff = os.cpu_count()
+    return {"affinity": aff, "os_cpu_count": os.cpu_count()}
+
+
+def oracle_layer_steps_ms(cfg, n_layers: int, n_steps: int) -> float:
+    """Time the FP64 oracle as it stands on n_steps Euler steps through the first
+    n_layers layers of `cfg` (weights prepared outside the timing), in ms per
+    layer-step."""
+    from oracle import model as O
+    import dataclasses
+    sub = dataclasses.replace(cfg, L=n_layers)
+    layers = [fm_synth.layer_weights(sub, l) for l in range(n_layers)]
+    conds = fm_synth.step_conds(sub) if sub.cond == "given" else None
+    model = O.Model(sub, layers, fm_synth.final_weights(sub), conds)
+    del layers
+    kp, vp = fm_synth.prefix_kv(sub)
+    kp, vp = kp.astype(np.float64), vp.astype(np.float64)
+    scales = fm_synth.default_act_scales(sub)
+    a = fm_synth.noise(sub, 0).astype(np.float64)
+    t0 = time.perf_counter()
+    for k in range(n_steps):
+        a = O.euler_step(model, k, a, kp, vp, scales)
+    return (time.perf_counter() - t0) * 1e3 / (n_layers * n_steps)
+
+
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                  "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1"}
+
+
+def oracle_one_thread_ms(workload: str) -> float | None:
+    """The same single-layer oracle timing in a fresh process whose BLAS runs one thread."""
+    code = ("import sys; sys.path.insert(0, %r); import bench, fm_synth; "
+            "print(bench.oracle_layer_steps_ms(fm_synth.config(%r), 1, 1))" % (ROOT, workload))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
+                           env={**os.environ, **ONE_THREAD_ENV})
+        return float(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def cpu_baseline(cfg, samples: int = 1):
+    """Time the FP64 oracle as it stands on this host's cores (BLAS threads = numpy's
+    default, all cores) on a bounded sample of the workload: two Euler steps of all 18
+    layers of the expert (the first layers of one step for larger decoders), scaled to
+    ms per decision. Also one bounded oracle timing per other workload (each scaled to
+    its own decision) and the single-layer workload with one BLAS thread."""
+    big = cfg.M * cfg.d > 100_000
+    n_layers = min(cfg.L, 2) if big else cfg.L
+    steps = 1 if big else 2
+    times = [oracle_layer_steps_ms(cfg, n_layers, steps) * cfg.S * cfg.L for _ in range(samples)]
     what = (f"{n_layers} layers of Euler step 0" if big else f"{steps} Euler steps x {cfg.L} layers")
-    return {"value": round(statistics.median(times), 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{what} of {cfg.name} (FP64 numpy, weights prepared outside the timing), "
-                      f"scaled to one {cfg.L}-layer x {cfg.S}-step decision"}
+    out = {"value": round(statistics.median(times), 1), "unit": UNIT, "cores": host_cores()["affinity"],
+           "kind": "oracle",
+           "sample": f"{what} of {cfg.name} (FP64 numpy, weights prepared outside the timing), "
+                     f"scaled to one {cfg.L}-layer x {cfg.S}-step decision",
+           "sampled_layer_steps": n_layers * steps, "scaled_to_layer_steps": cfg.L * cfg.S,
+           "host": host_cores(), "blas_threads": "numpy default (all cores)"}
+    per = {}
+    l0 = fm_synth.config("layer_fp8_m10")
+    per["layer_fp8_m10"] = {"ms_per_decision": round(oracle_layer_steps_ms(l0, 1, 1), 2),
+                            "sample": "the whole 1-layer x 1-step decision"}
+    one = oracle_one_thread_ms("layer_fp8_m10")
+    per["layer_fp8_m10_one_thread"] = {"ms_per_decision": None if one is None else round(one, 2),
+                                       "sample": "the whole 1-layer x 1-step decision, BLAS limited to 1 thread"}
+    for name, nl in (("expert_bf16_m63", 2), ("wam_nvfp4_m256", 1)):
+        if name == cfg.name:
+            continue
+        c = fm_synth.config(name)
+        per[name] = {"ms_per_decision": round(oracle_layer_steps_ms(c, nl, 1) * c.L * c.S, 1),
+                     "sample": f"{nl} layer(s) x 1 Euler step, scaled to {c.L} x {c.S}"}
+    out["per_workload"] = per
+    return out
 
 
 def max_over_ranks(values, device):
@@ -540,16 +625,45 @@ def aggregate_ms_per_decision(total_ms: float, steps: int, world: int) -> float:
 
 
 def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each of the K timed steps (after W warm-up
+    steps) is one Euler step through all layers of the workload - a bounded sample, one
+    S-th of a decision - and the reported value is the median step scaled by S to ms
+    per decision. Rank 0 only."""
     if rank != 0:
         return None
+    from oracle import model as O
     cfg = fm_synth.config(args.workload)
-    base = cpu_baseline(cfg, samples=max(1, min(args.steps, 3)))
-    return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": base["value"], "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+    big = cfg.M * cfg.d > 100_000
+    n_layers = min(cfg.L, 2) if big else cfg.L
+    import dataclasses
+    sub = dataclasses.replace(cfg, L=n_layers)
+    layers = [fm_synth.layer_weights(sub, l) for l in range(n_layers)]
+    model = O.Model(sub, layers, fm_synth.final_weights(sub))
+    del layers
+    kp, vp = fm_synth.prefix_kv(sub)
+    kp, vp = kp.astype(np.float64), vp.astype(np.float64)
+    scales = fm_synth.default_act_scales(sub)
+    a = fm_synth.noise(sub, 0).astype(np.float64)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        O.euler_step(model, i % cfg.S, a, kp, vp, scales)
+        if i >= args.warmup:
+            times.append((time.perf_counter() - t0) * 1e3)
+    step_ms = statistics.median(times)
+    scale = cfg.S * cfg.L / n_layers
+    value = step_ms * scale
+    cores = host_cores()
+    sample = (f"one Euler step x {n_layers} of {cfg.L} layers of {cfg.name} per timed step (FP64 numpy, BLAS "
+              f"on all cores, weights prepared outside the timing); value = median step x {scale:g}")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 2),
+            "step": f"one Euler step through {n_layers} layers (1/{scale:g} of a decision)",
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "layers": cfg.L, "euler_steps": cfg.S, "action_rows": cfg.M},
-            "cpu_baseline": base,
-            "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores["affinity"], "kind": "oracle",
+                             "sample": sample, "host": cores},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def profile_case(workload=WORKLOAD):

@@ -43,6 +43,7 @@ EXPORTS = [
     "fm_gemm_consumer_scratch_bytes", "fm_gemm_consumer", "fm_gemm_consumer_noalloc",
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
     "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes", "fm_standalone_status",
+    "fm_warm_trace_size", "fm_decode_warm_trace", "fm_test_launch_kernel", "fm_decode_timeline",
 ]
 
 
@@ -124,6 +125,10 @@ def load() -> ctypes.CDLL:
         "fm_gemm_consumer_noalloc": (i, [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
                                          vp]),
         "fm_decode_trace": (i, [vp, vp, vp, vp, sz, vp]),
+        "fm_warm_trace_size": (i, [vp, ctypes.POINTER(sz)]),
+        "fm_test_launch_kernel": (i, [vp, i, i, i, vp]),
+        "fm_decode_timeline": (i, [vp, vp, vp, vp, sz, vp]),
+        "fm_decode_warm_trace": (i, [vp, vp, i, vp, vp, sz, vp]),
         "fm_philox_noise": (i, [vp, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
         "fm_decode_actions_seeded": (i, [vp, ctypes.c_uint64, ctypes.c_uint64, vp, vp]),
         "fm_last_timing": (i, [vp, ctypes.POINTER(FmTiming), vp]),
@@ -342,6 +347,41 @@ def trace_size(p: int) -> int:
 def decode_trace(p: int, noise, actions, trace, nbytes: int, stream=None):
     _check(load().fm_decode_trace(p, _ptr(noise), _ptr(actions), _ptr(trace), nbytes, _stream(stream)),
            "fm_decode_trace", p)
+
+
+def warm_trace_size(p: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_warm_trace_size(p, ctypes.byref(n)), "fm_warm_trace_size", p)
+    return n.value
+
+
+def decode_warm_trace(p: int, noise, executed: int, actions, trace, nbytes: int, stream=None):
+    _check(load().fm_decode_warm_trace(p, _ptr(noise), int(executed), _ptr(actions), _ptr(trace), nbytes,
+                                       _stream(stream)), "fm_decode_warm_trace", p)
+
+
+def launch_kernel(p: int, layer: int, step: int, index: int, stream=None):
+    """Launch one kernel of a layer-step exactly as the decision does (no PDL)."""
+    _check(load().fm_test_launch_kernel(p, layer, step, index, _stream(stream)), "fm_test_launch_kernel", p)
+
+
+def decode_timeline(p: int, noise, actions, buf, nbytes: int, stream=None):
+    """One decision whose kernels record per-CTA timestamps into buf (see the header)."""
+    _check(load().fm_decode_timeline(p, _ptr(noise), _ptr(actions), _ptr(buf), nbytes, _stream(stream)),
+           "fm_decode_timeline", p)
+
+
+def parse_timeline(raw) -> list:
+    """Records of a timeline buffer (numpy uint8) as dicts: kind, grid, block, sm, t[7]."""
+    count, cap = (int(v) for v in raw[:8].view(np.uint32))
+    recs = raw[64:64 + 64 * min(count, cap)].view(np.uint64).reshape(-1, 8)
+    out = []
+    for r in recs:
+        w = int(r[0])
+        out.append({"kind": w & 0xff, "grid": ((w >> 8) & 0xfff, (w >> 20) & 0xfff),
+                    "block": ((w >> 32) & 0xfff, (w >> 44) & 0xfff), "sm": (w >> 56) & 0xff,
+                    "t": [int(x) for x in r[1:]]})
+    return out
 
 
 def kernel_count(p: int):

@@ -65,6 +65,9 @@ struct KParams {
   int out_fp8;
   int M, P, H, Hkv, G, kc, nsplit;
   int* err;
+  // diagnostic timeline (nullptr = off): entry, after the PDL wait, S = Q K^T complete,
+  // every slice's statistics received, O = P V complete, this CTA's O band received, exit
+  unsigned long long* tl;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gmem_src) {
@@ -156,6 +159,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, part = warp >> 2;
+  const bool tl_on = p.tl != nullptr && tid == 0;
+  __shared__ uint64_t tt[7];   // timeline stamps (thread 0)
+  if (tl_on)
+    for (int i = 0; i < 7; ++i) tt[i] = 0;
+  if (tl_on) tt[0] = global_ns();
   const int nkeys = p.P + p.M;
   const int t0 = split * KC;
   const int nvalid = min(KC, nkeys - t0);
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   }
   cp_async_commit();
   pdl_wait();   // Q, K, V of the chunk are written by the QKV GEMM
+  if (tl_on) tt[1] = global_ns();
 
   // ---- stacked query rows and the chunk's own keys (rows P..P+M-1 of the key axis)
   for (int idx = tid; idx < kRows * kRowChunks; idx += kThreads) {
@@ -322,6 +331,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
+  if (tl_on) tt[2] = global_ns();
   tc_fence_after();
   __syncwarp();
 
@@ -374,6 +384,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
+  if (tl_on) tt[3] = global_ns();
   // the row's global max and 1 / sum, once per row (the part-0 thread), in slice order
   if (part == 0) {
     float2 st[kMaxSplit];
@@ -453,6 +464,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
+  if (tl_on) tt[4] = global_ns();
   tc_fence_after();
   __syncwarp();
 
@@ -497,6 +509,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
+  if (tl_on) tt[5] = global_ns();
   // Once every owner has its band, no bulk copy still reads this CTA's stage: each
   // CTA arrives here and waits before exit (lifetime only; the data is ordered by
   // the mbarriers).
@@ -558,6 +571,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   cluster_wait();   // every owner has its band: no copy still reads this CTA
   tc_fence_before();
   __syncthreads();
+  if (tl_on) {
+    tt[6] = global_ns();
+    tl_record(p.tl, kTlAttn, gridDim.y * gridDim.z, blockIdx.y * gridDim.z + blockIdx.z, tt);
+  }
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -648,6 +665,7 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   p.kc = a.kc;
   p.nsplit = a.nsplit;
   p.err = a.err;
+  p.tl = o.tl;
   if (a.fp8 && (!a.kpre8 || !a.vtpre8 || !a.s_qkv || a.p16 % 16)) return cudaErrorInvalidValue;
   const int rows = p.G * p.M;
   const int tiles = (rows + kRows - 1) / kRows;

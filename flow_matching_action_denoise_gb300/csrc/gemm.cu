@@ -70,6 +70,9 @@ struct KParams {
   const float* sqa;   // static scale of q (FP8 operands)
   float eps;
   void* q_out;        // kMode 2: n-tile 0 also stores its K range of q here
+  // diagnostic timeline (nullptr = off): entry, activations requested (after the PDL
+  // wait), MMAs complete, split-K rows received, outputs written, exit
+  unsigned long long* tl;
 };
 
 __host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
@@ -111,6 +114,11 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const int nt = blockIdx.x;
   const int j = blockIdx.y;
   const uint32_t ncols = pow2_at_least(static_cast<uint32_t>(p.n_pad), 32);
+  const bool tl_on = p.tl != nullptr && threadIdx.x == 0;
+  __shared__ uint64_t tt[7];   // timeline stamps (thread 0)
+  if (tl_on)
+    for (int i = 0; i < 7; ++i) tt[i] = 0;
+  if (tl_on) tt[0] = global_ns();
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -176,6 +184,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
                 w_stage_bytes, &full[i], pol_w);
     }
     pdl_wait();   // activations are written by the previous kernel
+    if (tl_on) tt[1] = global_ns();
     for (int i = 0; i < pre; ++i)
       tma_load_3d(a_tiles + static_cast<size_t>(i) * a_stage_bytes, &tmA, &full[i], 0, 0, kb0 + i * chunk, pol_a);
     int issued = pre;
@@ -220,6 +229,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     const float rs = kFp8 ? 1.0f / *p.sqa : 1.0f;
     __shared__ float s_rr[256];
     pdl_wait();   // x and its tile sums are written by the previous kernel
+    if (tl_on) tt[1] = global_ns();
     if (static_cast<int>(threadIdx.x) < p.M) {
       const int ntile = K / kTileN;
       float ss = 0.f;
@@ -325,6 +335,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
+  if (tl_on) tt[2] = global_ns();
   tc_fence_after();
   __syncthreads();
   const bool abort = s_abort != 0;
@@ -366,6 +377,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   } else {
     __syncthreads();
   }
+  if (tl_on) tt[3] = global_ns();
   if (!abort) {
     const int part = j / kCs;
     const int c4 = lane * 4;
@@ -453,6 +465,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     }
   }
 
+  if (tl_on) tt[4] = global_ns();
   // On an abandoned pipeline, let copies already in flight land before the CTA exits.
   if (abort && threadIdx.x == 0) {
     const int issued = s_issued;
@@ -464,6 +477,10 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   if (kCs > 1) cluster_wait();
   tc_fence_before();
   __syncthreads();
+  if (tl_on) {
+    tt[5] = global_ns();
+    tl_record(p.tl, kTlGemm, gridDim.y, blockIdx.y, tt);
+  }
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -758,6 +775,7 @@ cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape
   p.sqa = fuse ? fuse->sqa : nullptr;
   p.eps = fuse ? fuse->eps : 0.f;
   p.q_out = fuse ? fuse->q_out : nullptr;
+  p.tl = o.tl;
   if (mode == 1 && (g.cs != g.s || !p.x || !p.gate || !p.ssq || !sa || !sw || out_bf16 || out_geglu || out_qkv8))
     return cudaErrorInvalidValue;
   if (mode == 2 && (!gemm_mode2_ok(g) || !p.x || !p.ssq || !p.scale || !p.shift || (g.fp8 && !p.sqa)))

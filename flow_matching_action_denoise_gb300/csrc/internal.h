@@ -21,11 +21,21 @@ struct LaunchOpts {
   cudaStream_t stream = nullptr;
   bool pdl = false;      // Programmatic Dependent Launch attribute
   dim3 cluster{1, 1, 1};
+  // Selective launch (standalone timing of one kernel of a sequence): when seq is set,
+  // each launch takes the next index from *seq and only index `only` is issued.
+  int* seq = nullptr;
+  int only = -1;
+  // Diagnostic timeline buffer (see tl_record in ptx.cuh); nullptr = off.
+  unsigned long long* tl = nullptr;
 };
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchOpts& o,
                           Args&&... args) {
+  if (o.seq) {
+    const int idx = (*o.seq)++;
+    if (o.only >= 0 && idx != o.only) return cudaSuccess;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -199,6 +209,7 @@ struct RowArgs {
   // start and clears stamp[1]; 2 = every CTA raises stamp[1] to its end time
   unsigned long long* stamp;
   int stamp_kind;
+  unsigned long long* tl;   // diagnostic timeline (set from LaunchOpts by row_launch)
 };
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o);
 // Decision noise: out[i] (i < n) from Philox4x32-10 block i / 4 with counter

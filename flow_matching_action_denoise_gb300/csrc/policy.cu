@@ -680,10 +680,11 @@ cudaError_t enqueue_head(fm_policy* p, const LaunchOpts& o, int k0 = 0) {
   return fm::row_launch(r, o);
 }
 
-cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st, Trace* tr = nullptr) {
+cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st, Trace* tr = nullptr, unsigned long long* tl = nullptr) {
   LaunchOpts o;
   o.stream = st;
   o.pdl = (p->cfg.flags & FM_FLAG_USE_PDL) != 0;
+  o.tl = tl;
   cudaError_t e = enqueue_head(p, o);
   if (e != cudaSuccess) return e;
   for (int k = 0; k < p->cfg.S; ++k)
@@ -696,18 +697,20 @@ cudaError_t enqueue_decision(fm_policy* p, cudaStream_t st, Trace* tr = nullptr)
 
 // The warm start's single step: the head and all layers with modulation row S; the
 // last layer's tail steps by dt = -warm_t.
-cudaError_t enqueue_warm(fm_policy* p, cudaStream_t st) {
+cudaError_t enqueue_warm_traced(fm_policy* p, cudaStream_t st, Trace* tr) {
   LaunchOpts o;
   o.stream = st;
   o.pdl = (p->cfg.flags & FM_FLAG_USE_PDL) != 0;
   cudaError_t e = enqueue_head(p, o, p->cfg.S);
   if (e != cudaSuccess) return e;
   for (int l = 0; l < p->cfg.L; ++l) {
-    e = enqueue_layer(p, l, p->cfg.S, l == p->cfg.L - 1, o, nullptr);
+    e = enqueue_layer(p, l, p->cfg.S, l == p->cfg.L - 1, o, tr);
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
+
+cudaError_t enqueue_warm(fm_policy* p, cudaStream_t st) { return enqueue_warm_traced(p, st, nullptr); }
 
 int capture(fm_policy* p, cudaError_t (*enq)(fm_policy*, cudaStream_t), cudaGraph_t* graph, cudaGraphExec_t* exec,
             const char* what) {
@@ -1432,6 +1435,97 @@ int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trac
   p->have_prev = true;
   FM_CUDA(p, cudaStreamSynchronize(s));
   if (tr.off != need) return fail(p, FM_ERR_INVALID_ARG, "internal: trace size mismatch");
+  return FM_OK;
+}
+
+int fm_warm_trace_size(const fm_policy* p, size_t* bytes) {
+  if (!p || !bytes) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  *bytes = p->ly.a_bytes + trace_record_bytes(p) * p->cfg.L;
+  return FM_OK;
+}
+
+int fm_decode_warm_trace(fm_policy* p, const float* noise, int executed, float* actions, void* trace, size_t bytes,
+                         void* stream) {
+  if (!p || !noise || !actions || !trace) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  const fm_config& c = p->cfg;
+  if (!(c.warm_t > 0.f)) return fail(p, FM_ERR_UNSUPPORTED, "the policy was created with warm_t = 0");
+  if (executed < 0 || executed > c.M) return fail(p, FM_ERR_INVALID_ARG, "executed must lie in [0, M]");
+  if (!p->have_prev) return fail(p, FM_ERR_INVALID_ARG, "no previous chunk to warm-start from");
+  size_t need = 0;
+  fm_warm_trace_size(p, &need);
+  if (bytes < need) return fail(p, FM_ERR_WORKSPACE, "trace buffer too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* a = p->at<float>(p->ly.a);
+  float* prev = p->at<float>(p->ly.prev);
+  FM_CUDA(p, cudaMemcpyAsync(prev, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  FM_CUDA(p, fm::warm_mix_launch(a, prev, noise, c.M, c.A, executed, c.warm_t, s));
+  Trace tr;
+  tr.base = static_cast<uint8_t*>(trace);
+  tr.st = s;
+  FM_CUDA(p, tr.rec(a, p->ly.a_bytes));   // a_tau, the input of the single Euler step
+  FM_CUDA(p, enqueue_warm_traced(p, s, &tr));
+  if (actions != a) FM_CUDA(p, cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s));
+  ++p->decisions;
+  FM_CUDA(p, cudaStreamSynchronize(s));
+  if (tr.off != need) return fail(p, FM_ERR_INVALID_ARG, "internal: trace size mismatch");
+  return FM_OK;
+}
+
+int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* stream) {
+  if (!p) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL policy");
+  const fm_config& c = p->cfg;
+  if (layer < 0 || layer >= c.L || step < 0 || step >= c.S || index < 0 || index >= p->dv.kernels_per_layer())
+    return fail(p, FM_ERR_INVALID_ARG, "layer, step or kernel index out of range");
+  LaunchOpts o;
+  o.stream = static_cast<cudaStream_t>(stream);
+  int seq = 0;
+  o.seq = &seq;
+  o.only = index;
+  FM_CUDA(p, enqueue_layer(p, layer, step, layer == c.L - 1, o));
+  if (seq <= index) return fail(p, FM_ERR_INVALID_ARG, "kernel index beyond this layer-step's launches");
+  return FM_OK;
+}
+
+int fm_decode_timeline(fm_policy* p, const float* noise, float* actions, void* buf, size_t bytes, void* stream) {
+  if (!p || !noise || !actions || !buf) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
+  if (bytes < 128 || reinterpret_cast<uintptr_t>(buf) % 16) return fail(p, FM_ERR_WORKSPACE, "buffer too small or unaligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long* tl = static_cast<unsigned long long*>(buf);
+  const unsigned hdr[2] = {0u, static_cast<unsigned>(std::min<size_t>((bytes - 64) / 64, 0xffffffffu))};
+  float* a = p->at<float>(p->ly.a);
+  // the same plan as decode_actions, captured with the timeline buffer in its kernels'
+  // parameters (a graph when the policy replays one, else launched one by one)
+  cudaGraph_t g = nullptr;
+  cudaGraphExec_t ge = nullptr;
+  const bool use_graph = (p->cfg.flags & FM_FLAG_USE_GRAPH) != 0;
+  if (use_graph) {
+    FM_CUDA(p, cudaStreamBeginCapture(p->cap_stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = enqueue_decision(p, p->cap_stream, nullptr, tl);
+    cudaError_t e2 = cudaStreamEndCapture(p->cap_stream, &g);
+    if (e != cudaSuccess || e2 != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return cuda_fail(p, e != cudaSuccess ? e : e2, "capturing the timeline decision");
+    }
+    e = cudaGraphInstantiate(&ge, g, 0);
+    if (e == cudaSuccess) e = cudaGraphUpload(ge, s);
+    if (e != cudaSuccess) {
+      cudaGraphDestroy(g);
+      return cuda_fail(p, e, "instantiating the timeline decision");
+    }
+  }
+  cudaError_t e = cudaSuccess;
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {   // the first pass warms up
+    e = cudaMemcpyAsync(tl, hdr, sizeof hdr, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && noise != a) e = cudaMemcpyAsync(a, noise, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = use_graph ? cudaGraphLaunch(ge, s) : enqueue_decision(p, s, nullptr, tl);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e == cudaSuccess && actions != a) e = cudaMemcpyAsync(actions, a, p->ly.a_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (ge) cudaGraphExecDestroy(ge);
+  if (g) cudaGraphDestroy(g);
+  if (e != cudaSuccess) return cuda_fail(p, e, "timeline decision");
+  p->have_prev = true;
   return FM_OK;
 }
 

@@ -265,4 +265,32 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
   return v;
 }
 
+// ---------------------------------------------------------------- timeline (diagnostics)
+// When a kernel is given a timeline buffer, thread 0 of each CTA appends one 64-byte
+// record: word 0 identifies the CTA (kind | gridDim.x << 8 | grid rows << 20 |
+// blockIdx.x << 32 | block row << 44 | SM id << 56), words 1-7 are %globaltimer stamps
+// (ns) at points the kernel defines (0 = not reached). Buffer: u32 count, u32 capacity,
+// 56 bytes of padding, then the records; records past the capacity are dropped.
+enum TlKind : uint32_t { kTlGemm = 1, kTlAttn = 2, kTlRow = 3, kTlNvfp4 = 4 };
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void tl_record(unsigned long long* tl, uint32_t kind, uint32_t grid_rows, uint32_t row,
+                                          const uint64_t* t) {
+  unsigned* hdr = reinterpret_cast<unsigned*>(tl);
+  const unsigned idx = atomicAdd(hdr, 1u);
+  if (idx >= hdr[1]) return;
+  unsigned long long* rec = tl + 8 + static_cast<size_t>(idx) * 8;
+  rec[0] = static_cast<unsigned long long>(kind) | (static_cast<unsigned long long>(gridDim.x & 0xfff) << 8) |
+           (static_cast<unsigned long long>(grid_rows & 0xfff) << 20) |
+           (static_cast<unsigned long long>(blockIdx.x & 0xfff) << 32) |
+           (static_cast<unsigned long long>(row & 0xfff) << 44) | (static_cast<unsigned long long>(sm_id() & 0xff) << 56);
+#pragma unroll
+  for (int i = 0; i < 7; ++i) rec[1 + i] = t[i];
+}
+
 }  // namespace fm

@@ -85,6 +85,11 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   const int tid = threadIdx.x;
   const int N = r.N;
   const int n4 = N / 4;
+  const bool tl_on = r.tl != nullptr && tid == 0;   // diagnostic timeline: entry, after the wait, exit
+  __shared__ uint64_t tt[7];   // timeline stamps (thread 0)
+  if (tl_on)
+    for (int i = 0; i < 7; ++i) tt[i] = 0;
+  if (tl_on) tt[0] = global_ns();
   if (r.stamp_kind == 1 && m == 0 && tid == 0) {   // the decision's first kernel starts
     r.stamp[0] = global_ns();
     r.stamp[1] = 0ull;
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
     }
   }
   pdl_wait();
+  if (tl_on) tt[1] = global_ns();
 
   float* xrow = r.x + static_cast<size_t>(m) * N;
   const float* xin = r.x_src ? r.x_src + static_cast<size_t>(m) * N : xrow;
@@ -282,6 +288,10 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
     __syncthreads();
     if (tid == 0) atomicMax(r.stamp + 1, global_ns());
   }
+  if (tl_on) {
+    tt[2] = global_ns();
+    tl_record(r.tl, kTlRow, 1, 0, tt);
+  }
 }
 
 // ---------------------------------------------------------------- decision noise
@@ -428,7 +438,9 @@ cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
     cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(row_kernel));
     if (e != cudaSuccess) return e;
   }
-  return launch(row_kernel, dim3(static_cast<unsigned>(r.M)), dim3(kRowThreads), smem, o, r);
+  RowArgs ra = r;
+  ra.tl = o.tl;
+  return launch(row_kernel, dim3(static_cast<unsigned>(r.M)), dim3(kRowThreads), smem, o, ra);
 }
 
 cudaError_t philox_noise_launch(float* out, int64_t n, uint64_t seed, uint64_t counter, uint32_t* raw,

@@ -363,8 +363,40 @@ int fm_trace_size(const fm_policy* p, size_t* bytes);
  * Codes are one byte (FP8) or bf16 (BF16 activations). Synchronous. */
 int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trace, size_t bytes, void* stream);
 
+/* The warm start of fm_decode_warm (same arguments, launched one by one, no graph),
+ * recording into `trace` (device, >= fm_warm_trace_size bytes) first the mixed input of
+ * the single Euler step, a_tau = tau * noise + (1 - tau) * shifted as fp32 [M][A], then
+ * one fm_decode_trace record per layer of that step (the last record's actions are the
+ * decision's). Needs a previous chunk (FM_ERR_INVALID_ARG after fm_episode_reset or
+ * before the first decision). Synchronous. */
+int fm_warm_trace_size(const fm_policy* p, size_t* bytes);
+int fm_decode_warm_trace(fm_policy* p, const float* noise, int executed, float* actions, void* trace,
+                         size_t bytes, void* stream);
+
+/* One decision (as decode_actions: the same kernels, launch configuration and graph)
+ * whose kernels also record a timeline into `buf` (device, 16-byte aligned): u32
+ * record count, u32 capacity, 56 bytes of padding, then one 64-byte record per CTA of
+ * every kernel: u64 id = kind (1 skinny GEMM, 2 attention, 3 row kernel, 4 NVFP4 GEMM)
+ * | gridDim.x << 8 | grid rows << 20 | blockIdx.x << 32 | block row << 44 | SM << 56,
+ * then seven u64 %globaltimer stamps in ns (0 = not recorded): GEMM - entry, after the
+ * programmatic-dependent-launch wait, MMAs complete, split-K rows received, outputs
+ * written, exit; attention - entry, after the wait, S = Q K^T complete, statistics
+ * received, O = P V complete, O band received, exit; row kernel - entry, after the
+ * wait, exit. Records past the capacity (bytes - 64) / 64 are dropped. Runs the
+ * decision twice (the first warms the new graph up) and synchronises; a diagnostic,
+ * not the timed path. */
+int fm_decode_timeline(fm_policy* p, const float* noise, float* actions, void* buf, size_t bytes, void* stream);
+
 /* Kernel launches per decoder layer and per decision of the captured plan. */
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
+
+/* Launch only kernel `index` (0 .. per_layer - 1, in the decision's order: FP8/BF16
+ * QKV GEMM, attention, O GEMM, consumer, gate|up GEMM + GeGLU, down GEMM, consumer or
+ * step boundary) of layer `layer` at Euler step `step`, with exactly the arguments and
+ * launch configuration the decision uses, without Programmatic Dependent Launch, on the
+ * policy's current buffers: for timing one kernel on its own (the buffers hold the last
+ * decision's data). It updates the policy's state as that kernel does. Asynchronous. */
+int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Building blocks, exported for tests and standalone use (same conventions).

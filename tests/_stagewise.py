@@ -98,9 +98,12 @@ def fp8_attention_allowance(qc, kc, vc, kpre_c, vpre_c, H, Hkv, Dh, s_q, s_k, s_
     return out
 
 
-def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac=1e-3, attn_abs_tol=2.0 ** -7):
+def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac=1e-3, attn_abs_tol=2.0 ** -7,
+                          mod_rows=None, dt=None):
     """recs[k][l] as parse_trace returns them; scales [L][4] ([L][7] with FP8
-    attention; ignored for bf16)."""
+    attention; ignored for bf16). mod_rows: the modulation row of each recorded step
+    (default 0 .. S-1); dt: the Euler step (default -1/S). The one-step warm start
+    is mod_rows=[S], dt=-warm_t from its mixed input a_tau as `noise`."""
     fmt = cfg.act_fmt
     attn8 = getattr(cfg, "attn_fmt", "bf16") == "fp8"
     prefix8 = prefix_codes(kp, vp, scales) if attn8 else None
@@ -114,11 +117,13 @@ def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac
     def dq(l, i, w):   # dequantisation factor fp32(s_a * s_w) the epilogues apply
         return np.float64(np.float32(s_act(l, i)) * np.float32(w.scale))
 
+    rows = list(range(S)) if mod_rows is None else list(mod_rows)
+    dt = -1.0 / S if dt is None else dt
     a_prev = np.asarray(noise, np.float64)
     check_close(recs[0][0]["x_in"], a_prev @ fin["w_in"].T + fin["b_in"], "step head x")
-    for k in range(S):
+    for i, k in enumerate(rows):
         for l in range(L):
-            r = recs[k][l]
+            r = recs[i][l]
             W = model.w[l]
             sc1, sh1, g1, sc2, sh2, g2 = model.mods[k][0][l]
             where = f"step {k} layer {l}"
@@ -173,10 +178,10 @@ def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac
                 continue
             scf, shf = model.mods[k][1]
             v = (O.ada_norm(x_res, scf, shf, cfg.eps) * fin["gamma_f"]) @ fin["w_out"].T + fin["b_out"]
-            check_close(r["actions"], a_prev + (-1.0 / S) * v, where + " Euler update")
+            check_close(r["actions"], a_prev + dt * v, where + " Euler update")
             a_prev = r["actions"].astype(np.float64)
-            if k < S - 1:
+            if i < len(rows) - 1:
                 check_close(r["x_out"], a_prev @ fin["w_in"].T + fin["b_in"], where + " next step head")
             else:
                 check_close(r["x_out"], x_res, where + " MLP residual")
-    return recs[S - 1][L - 1]["actions"]
+    return recs[len(rows) - 1][L - 1]["actions"]

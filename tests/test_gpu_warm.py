@@ -6,6 +6,10 @@
   runs the full S-step decision, bitwise equal to decode_actions;
 - warm_t = 0.5, 3 actions executed: within twice the oracle's own FP8 envelope of
   the oracle's warm decision from the GPU's previous chunk (teacher forced);
+- teacher forced stage by stage (fm_decode_warm_trace), for 0, 3 and M executed
+  actions: the mixed input a_tau (shift, pad with the last action, mix with the
+  noise) equals the oracle's within fp32 rounding, and every kernel of the single
+  Euler step matches the oracle's stage applied to its recorded input;
 - the warm decision takes a fraction of the full decision's time.
 """
 import dataclasses
@@ -19,7 +23,8 @@ import fm_synth
 import flow_matching_action_denoise_gb300 as fmad
 from oracle import model as O
 
-from _gpu import GOLDEN, dev, load_scales, require_gpu
+from _gpu import GOLDEN, dev, load_scales, parse_trace, require_gpu
+from _stagewise import check_decision_stages
 
 pytestmark = pytest.mark.gpu
 
@@ -109,3 +114,33 @@ def test_warm_decision_is_one_step_of_time(ex):
     full, warm = e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3])
     assert warm < 0.25 * full, (warm, full)
     p.close()
+
+
+@pytest.mark.parametrize("executed", [0, 3, 50])
+def test_warm_start_teacher_forced(ex, executed):
+    cfg = dataclasses.replace(ex.cfg, warm_t=0.5)
+    p = ex.policy(warm_t=0.5)
+    prev = p.decode(ex.noise(0)).cpu().numpy().astype(np.float64)
+    nz = fm_synth.noise(cfg, 1)
+    nbytes = fmad.warm_trace_size(p.handle)
+    trace = torch.empty(nbytes, dtype=torch.uint8, device=ex.device)
+    actions = torch.empty((cfg.M, cfg.A), dtype=torch.float32, device=ex.device)
+    fmad.decode_warm_trace(p.handle, dev(nz, ex.device), executed, actions, trace, nbytes)
+    assert fmad.device_status(p.handle) == 0
+    raw = trace.cpu().numpy()
+    got = actions.cpu().numpy()
+    ab = cfg.M * cfg.A * 4
+    recs = parse_trace(raw[ab:], dataclasses.replace(cfg, S=1), p)
+    p.close()
+    a_tau = raw[:ab].view(np.float32).reshape(cfg.M, cfg.A).astype(np.float64)
+    tau = O.warm_time(cfg)
+    want = O.warm_start_input(prev, executed, tau, nz)
+    shifted = prev[np.minimum(np.arange(cfg.M) + executed, cfg.M - 1)]
+    # one fp32 product and one fp32 fused multiply-add
+    allow = 2.0 ** -23 * (tau * np.abs(nz) + (1.0 - tau) * np.abs(shifted))
+    assert np.all(np.abs(a_tau - want) <= allow)
+    if executed == cfg.M:   # every row is the last action, mixed with its own noise row
+        assert np.allclose(a_tau - tau * nz, (1.0 - tau) * prev[-1], rtol=0, atol=1e-6)
+    model = O.Model(cfg, ex.layers, ex.final)
+    last = check_decision_stages(cfg, model, recs, a_tau, ex.kp, ex.vp, ex.scales, mod_rows=[cfg.S], dt=-tau)
+    np.testing.assert_array_equal(got, last.astype(np.float32))
