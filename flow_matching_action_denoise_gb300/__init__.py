@@ -372,9 +372,9 @@ def decode_timeline(p: int, noise, actions, buf, nbytes: int, stream=None):
 
 
 def parse_timeline(raw) -> list:
-    """Records of a timeline buffer (numpy uint8) as dicts: kind, grid, block, sm, t[7]."""
+    """Records of a timeline buffer (numpy uint8) as dicts: kind, grid, block, sm, t[15]."""
     count, cap = (int(v) for v in raw[:8].view(np.uint32))
-    recs = raw[64:64 + 64 * min(count, cap)].view(np.uint64).reshape(-1, 8)
+    recs = raw[64:64 + 128 * min(count, cap)].view(np.uint64).reshape(-1, 16)
     out = []
     for r in recs:
         w = int(r[0])

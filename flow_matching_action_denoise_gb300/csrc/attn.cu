@@ -65,8 +65,10 @@ struct KParams {
   int out_fp8;
   int M, P, H, Hkv, G, kc, nsplit;
   int* err;
-  // diagnostic timeline (nullptr = off): entry, after the PDL wait, S = Q K^T complete,
-  // every slice's statistics received, O = P V complete, this CTA's O band received, exit
+  // diagnostic timeline (nullptr = off): entry, after the PDL wait, operands loaded, chunk
+  // values transposed, S = Q K^T complete, pass 1 done, cluster peers started, statistics
+  // sent, every slice's statistics received, P written, O = P V complete, O band copies
+  // issued, this CTA's O band received, band summed and stored, exit
   unsigned long long* tl;
 };
 
@@ -160,9 +162,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, part = warp >> 2;
   const bool tl_on = p.tl != nullptr && tid == 0;
-  __shared__ uint64_t tt[7];   // timeline stamps (thread 0)
+  __shared__ uint64_t tt[kTlStamps];   // timeline stamps (thread 0)
   if (tl_on)
-    for (int i = 0; i < 7; ++i) tt[i] = 0;
+    for (int i = 0; i < kTlStamps; ++i) tt[i] = 0;
   if (tl_on) tt[0] = global_ns();
   const int nkeys = p.P + p.M;
   const int t0 = split * KC;
@@ -291,6 +293,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();   // V^T groups and the staged chunk values are in place
+  if (tl_on) tt[2] = global_ns();
   if (nchunk > 0) {   // shared -> shared transpose into V^T (keys along K), this CTA's dims
     const int d = tid & (kDv - 1);
     if constexpr (kF8) {
@@ -313,6 +316,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   }
   fence_async_smem();   // generic-proxy shared-memory writes -> tensor-core reads
   __syncthreads();
+  if (tl_on) tt[3] = global_ns();
 
   // ---- S = Q K^T into TMEM columns [0, KC)
   if (tid == 0) {
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
-  if (tl_on) tt[2] = global_ns();
+  if (tl_on) tt[4] = global_ns();
   tc_fence_after();
   __syncwarp();
 
@@ -342,7 +346,14 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // ---- pass 1: this row part's scores (kept in registers), max and sum of exp
   float sv[kPart];
 #pragma unroll
-  for (int c = 0; c < kPart; c += 16) {
+  for (int c = 0; c + 32 <= kPart; c += 32) {   // 32 columns per TMEM load
+    float v[32];
+    tmem_ld32(t_row + static_cast<uint32_t>(c0 + c), v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) sv[c + e] = c0 + c + e < nvalid ? v[e] * kscale : -INFINITY;
+  }
+  if constexpr (kPart % 32 != 0) {
+    constexpr int c = kPart - 16;
     float v[16];
     tmem_ld16(t_row + static_cast<uint32_t>(c0 + c), v);
 #pragma unroll
@@ -355,13 +366,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   float lh = 0.f;
 #pragma unroll
   for (int e = 0; e < kPart; ++e) {
-    sv[e] = mh > -INFINITY ? exp2f(sv[e] - mh) : 0.f;
+    sv[e] = mh > -INFINITY ? ex2_approx(sv[e] - mh) : 0.f;
     lh += sv[e];
   }
   sPart[part * kRows + r] = make_float2(mh, lh);
+  if (tl_on) tt[5] = global_ns();
   __syncthreads();
   // the slice statistics of row r, pushed to every CTA of the cluster (slot = own rank)
   cluster_wait();   // every peer has started: its shared memory exists
+  if (tl_on) tt[6] = global_ns();
   if (part == 0) {
     float m = -INFINITY;
 #pragma unroll
@@ -377,6 +390,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     const uint32_t mb = smem_u32(&bar[2]);
     for (int q = 0; q < p.nsplit; ++q)
       st_async_v2(map_dsmem(off, static_cast<uint32_t>(q)), m, l, map_dsmem(mb, static_cast<uint32_t>(q)));
+    if (tl_on) tt[7] = global_ns();
   }
   // Every slice's statistics have landed. Each peer sent them after its S = Q K^T
   // completed, so from here on its Q and K tiles are dead and may receive O shares.
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
-  if (tl_on) tt[3] = global_ns();
+  if (tl_on) tt[8] = global_ns();
   // the row's global max and 1 / sum, once per row (the part-0 thread), in slice order
   if (part == 0) {
     float2 st[kMaxSplit];
@@ -446,6 +460,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   tc_fence_before();
   fence_async_smem();
   __syncthreads();
+  if (tl_on) tt[9] = global_ns();
 
   // ---- O = P V into TMEM columns [KC, KC + kDv): this CTA's head dims
   if (tid == 0) {
@@ -464,7 +479,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
-  if (tl_on) tt[4] = global_ns();
+  if (tl_on) tt[10] = global_ns();
   tc_fence_after();
   __syncwarp();
 
@@ -503,13 +518,14 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
                             static_cast<uint32_t>((hi - lo) * kRowBytes),
                             map_dsmem(smem_u32(&bar[3]), static_cast<uint32_t>(o)));
       }
+      if (tl_on) tt[11] = global_ns();
     }
   }
   if (!mbar_wait(&bar[3], 0)) {   // every slice's share of this CTA's band has landed
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
-  if (tl_on) tt[5] = global_ns();
+  if (tl_on) tt[12] = global_ns();
   // Once every owner has its band, no bulk copy still reads this CTA's stage: each
   // CTA arrives here and waits before exit (lifetime only; the data is ordered by
   // the mbarriers).
@@ -568,11 +584,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
     }
   }
+  if (tl_on) tt[13] = global_ns();
   cluster_wait();   // every owner has its band: no copy still reads this CTA
   tc_fence_before();
   __syncthreads();
   if (tl_on) {
-    tt[6] = global_ns();
+    tt[14] = global_ns();
     tl_record(p.tl, kTlAttn, gridDim.y * gridDim.z, blockIdx.y * gridDim.z + blockIdx.z, tt);
   }
   if (warp == 0) {

@@ -71,7 +71,7 @@ struct KParams {
   float eps;
   void* q_out;        // kMode 2: n-tile 0 also stores its K range of q here
   // diagnostic timeline (nullptr = off): entry, activations requested (after the PDL
-  // wait), MMAs complete, split-K rows received, outputs written, exit
+  // wait), MMAs complete, partial rows pushed, split-K rows received, outputs written, exit
   unsigned long long* tl;
 };
 
@@ -115,9 +115,9 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const int j = blockIdx.y;
   const uint32_t ncols = pow2_at_least(static_cast<uint32_t>(p.n_pad), 32);
   const bool tl_on = p.tl != nullptr && threadIdx.x == 0;
-  __shared__ uint64_t tt[7];   // timeline stamps (thread 0)
+  __shared__ uint64_t tt[kTlStamps];   // timeline stamps (thread 0)
   if (tl_on)
-    for (int i = 0; i < 7; ++i) tt[i] = 0;
+    for (int i = 0; i < kTlStamps; ++i) tt[i] = 0;
   if (tl_on) tt[0] = global_ns();
 
   if (threadIdx.x == 0) {
@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       }
     }
   }
+  if (tl_on) tt[3] = global_ns();
   if (kCs > 1) {
     // every rank's partial rows for this CTA have landed (no cluster-wide release barrier);
     // the relaxed arrive, waited before exit, keeps this CTA alive while peers store into it
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   } else {
     __syncthreads();
   }
-  if (tl_on) tt[3] = global_ns();
+  if (tl_on) tt[4] = global_ns();
   if (!abort) {
     const int part = j / kCs;
     const int c4 = lane * 4;
@@ -395,38 +396,24 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
         acc.w += v.w;
       }
       if (p.out_geglu) {
-        // lanes 0-15 hold gate columns 4L..4L+3 of this tile's 64 GeGLU columns, lanes
-        // 16-31 the matching up columns: m = gelu_tanh(g) * u, quantised
-        float4 up;
-        up.x = __shfl_xor_sync(0xffffffffu, acc.x, 16);
-        up.y = __shfl_xor_sync(0xffffffffu, acc.y, 16);
-        up.z = __shfl_xor_sync(0xffffffffu, acc.z, 16);
-        up.w = __shfl_xor_sync(0xffffffffu, acc.w, 16);
-        if (lane < 16) {
-          const float gv[4] = {acc.x * ds, acc.y * ds, acc.z * ds, acc.w * ds};
-          const float uv[4] = {up.x * ds, up.y * ds, up.z * ds, up.w * ds};
-          float mv[4];
+        // the four columns are (gate, up) of GeGLU columns 2L and 2L+1 of this tile's 64:
+        // m = gelu_tanh(g) * u, quantised
+        float mv[2];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x = gv[e];
-            mv[e] = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * uv[e];
-          }
-          const size_t fidx = static_cast<size_t>(m) * (p.N / 2) + static_cast<size_t>(nt) * 64 + c4;
-          if (p.geglu_fp8) {
-            uchar4 c;
-            c.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[0] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
-            c.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[1] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
-            c.z = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[2] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
-            c.w = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[3] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
-            *reinterpret_cast<uchar4*>(static_cast<uint8_t*>(p.out_geglu) + fidx) = c;
-          } else {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(mv[0], mv[1]);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(mv[2], mv[3]);
-            uint2 u;
-            u.x = *reinterpret_cast<const uint32_t*>(&lo);
-            u.y = *reinterpret_cast<const uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out_geglu) + fidx) = u;
-          }
+        for (int e = 0; e < 2; ++e) {
+          const float x = (e ? acc.z : acc.x) * ds;
+          const float u = (e ? acc.w : acc.y) * ds;
+          mv[e] = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * u;
+        }
+        const size_t fidx = static_cast<size_t>(m) * (p.N / 2) + static_cast<size_t>(nt) * 64 + 2 * lane;
+        if (p.geglu_fp8) {
+          uchar2 c;
+          c.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[0] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
+          c.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[1] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
+          *reinterpret_cast<uchar2*>(static_cast<uint8_t*>(p.out_geglu) + fidx) = c;
+        } else {
+          const __nv_bfloat162 b = __floats2bfloat162_rn(mv[0], mv[1]);
+          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out_geglu) + fidx) = b;
         }
       } else if (p.out_qkv8) {
         // the 4 columns share a section (sections are multiples of 128 columns)
@@ -465,7 +452,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     }
   }
 
-  if (tl_on) tt[4] = global_ns();
+  if (tl_on) tt[5] = global_ns();
   // On an abandoned pipeline, let copies already in flight land before the CTA exits.
   if (abort && threadIdx.x == 0) {
     const int issued = s_issued;
@@ -478,7 +465,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   if (tl_on) {
-    tt[5] = global_ns();
+    tt[6] = global_ns();
     tl_record(p.tl, kTlGemm, gridDim.y, blockIdx.y, tt);
   }
   if (warp == 0) {
@@ -512,13 +499,14 @@ __global__ void scale_from_amax_kernel(const unsigned* __restrict__ amax, float*
 __global__ void set_one_kernel(float* p) { *p = 1.0f; }
 
 // FP8: one thread writes 16 bytes (16 codes) of a [128][128]-byte tile.
-// Packed row n of a gate|up weight with interleave: tile t = n / 128 holds gate rows
-// 64t..64t+63 then the matching up rows F+64t..F+64t+63 (F = N/2), so one output tile
-// carries both halves of 64 GeGLU columns.
+// Packed row n of a gate|up weight with interleave: tile t = n / 128 holds, for GeGLU
+// columns j = 64t .. 64t+63, gate row j at tile row 2(j - 64t) and the matching up row
+// F + j at tile row 2(j - 64t) + 1 (F = N/2), so one output tile carries both halves of
+// 64 GeGLU columns and each (gate, up) pair sits in adjacent accumulator columns.
 __device__ __forceinline__ size_t source_row(size_t n, int N, int interleave) {
   if (!interleave) return n;
   const size_t t = n / 128, r = n % 128;
-  return r < 64 ? t * 64 + r : static_cast<size_t>(N / 2) + t * 64 + (r - 64);
+  return (r & 1 ? static_cast<size_t>(N / 2) : 0) + t * 64 + r / 2;
 }
 
 __global__ void pack_fp8_kernel(const float* __restrict__ w, const float* __restrict__ gamma, int N, int K,

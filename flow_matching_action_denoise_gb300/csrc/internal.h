@@ -157,7 +157,8 @@ cudaError_t weight_amax_launch(const float* w, const float* gamma, int N, int K,
 
 // Packing
 size_t packed_weight_bytes(int N, int K, int fmt);
-// geglu_interleave: pack a gate|up weight [2F][K] so tile t holds gate rows 64t.. and up rows F+64t..
+// geglu_interleave: pack a gate|up weight [2F][K] so tile t holds, in alternate rows, gate row 64t+i and
+// up row F+64t+i (i = 0..63)
 cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fmt, void* packed, float* scale_out,
                         unsigned* amax_scratch, cudaStream_t st, int geglu_interleave = 0);
 

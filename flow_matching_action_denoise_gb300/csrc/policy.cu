@@ -1488,10 +1488,10 @@ int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* st
 
 int fm_decode_timeline(fm_policy* p, const float* noise, float* actions, void* buf, size_t bytes, void* stream) {
   if (!p || !noise || !actions || !buf) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
-  if (bytes < 128 || reinterpret_cast<uintptr_t>(buf) % 16) return fail(p, FM_ERR_WORKSPACE, "buffer too small or unaligned");
+  if (bytes < 192 || reinterpret_cast<uintptr_t>(buf) % 16) return fail(p, FM_ERR_WORKSPACE, "buffer too small or unaligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned long long* tl = static_cast<unsigned long long*>(buf);
-  const unsigned hdr[2] = {0u, static_cast<unsigned>(std::min<size_t>((bytes - 64) / 64, 0xffffffffu))};
+  const unsigned hdr[2] = {0u, static_cast<unsigned>(std::min<size_t>((bytes - 64) / 128, 0xffffffffu))};
   float* a = p->at<float>(p->ly.a);
   // the same plan as decode_actions, captured with the timeline buffer in its kernels'
   // parameters (a graph when the policy replays one, else launched one by one)

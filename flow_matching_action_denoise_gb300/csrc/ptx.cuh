@@ -203,6 +203,31 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Each thread of a warp reads 32 consecutive 32-bit columns of its TMEM lane (one load,
+// one wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x by the MUFU instruction (approximate, denormal results flushed to zero); the
+// attention's probabilities are rounded to bf16 or E4M3 afterwards.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -266,11 +291,12 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------- timeline (diagnostics)
-// When a kernel is given a timeline buffer, thread 0 of each CTA appends one 64-byte
+// When a kernel is given a timeline buffer, thread 0 of each CTA appends one 128-byte
 // record: word 0 identifies the CTA (kind | gridDim.x << 8 | grid rows << 20 |
-// blockIdx.x << 32 | block row << 44 | SM id << 56), words 1-7 are %globaltimer stamps
+// blockIdx.x << 32 | block row << 44 | SM id << 56), words 1-15 are %globaltimer stamps
 // (ns) at points the kernel defines (0 = not reached). Buffer: u32 count, u32 capacity,
 // 56 bytes of padding, then the records; records past the capacity are dropped.
+constexpr int kTlStamps = 15;
 enum TlKind : uint32_t { kTlGemm = 1, kTlAttn = 2, kTlRow = 3, kTlNvfp4 = 4 };
 
 __device__ __forceinline__ uint32_t sm_id() {
@@ -284,13 +310,13 @@ __device__ __forceinline__ void tl_record(unsigned long long* tl, uint32_t kind,
   unsigned* hdr = reinterpret_cast<unsigned*>(tl);
   const unsigned idx = atomicAdd(hdr, 1u);
   if (idx >= hdr[1]) return;
-  unsigned long long* rec = tl + 8 + static_cast<size_t>(idx) * 8;
+  unsigned long long* rec = tl + 8 + static_cast<size_t>(idx) * 16;
   rec[0] = static_cast<unsigned long long>(kind) | (static_cast<unsigned long long>(gridDim.x & 0xfff) << 8) |
            (static_cast<unsigned long long>(grid_rows & 0xfff) << 20) |
            (static_cast<unsigned long long>(blockIdx.x & 0xfff) << 32) |
            (static_cast<unsigned long long>(row & 0xfff) << 44) | (static_cast<unsigned long long>(sm_id() & 0xff) << 56);
 #pragma unroll
-  for (int i = 0; i < 7; ++i) rec[1 + i] = t[i];
+  for (int i = 0; i < kTlStamps; ++i) rec[1 + i] = t[i];
 }
 
 }  // namespace fm

@@ -86,9 +86,9 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   const int N = r.N;
   const int n4 = N / 4;
   const bool tl_on = r.tl != nullptr && tid == 0;   // diagnostic timeline: entry, after the wait, exit
-  __shared__ uint64_t tt[7];   // timeline stamps (thread 0)
+  __shared__ uint64_t tt[kTlStamps];   // timeline stamps (thread 0)
   if (tl_on)
-    for (int i = 0; i < 7; ++i) tt[i] = 0;
+    for (int i = 0; i < kTlStamps; ++i) tt[i] = 0;
   if (tl_on) tt[0] = global_ns();
   if (r.stamp_kind == 1 && m == 0 && tid == 0) {   // the decision's first kernel starts
     r.stamp[0] = global_ns();

@@ -375,14 +375,16 @@ int fm_decode_warm_trace(fm_policy* p, const float* noise, int executed, float* 
 
 /* One decision (as decode_actions: the same kernels, launch configuration and graph)
  * whose kernels also record a timeline into `buf` (device, 16-byte aligned): u32
- * record count, u32 capacity, 56 bytes of padding, then one 64-byte record per CTA of
+ * record count, u32 capacity, 56 bytes of padding, then one 128-byte record per CTA of
  * every kernel: u64 id = kind (1 skinny GEMM, 2 attention, 3 row kernel, 4 NVFP4 GEMM)
  * | gridDim.x << 8 | grid rows << 20 | blockIdx.x << 32 | block row << 44 | SM << 56,
- * then seven u64 %globaltimer stamps in ns (0 = not recorded): GEMM - entry, after the
- * programmatic-dependent-launch wait, MMAs complete, split-K rows received, outputs
- * written, exit; attention - entry, after the wait, S = Q K^T complete, statistics
- * received, O = P V complete, O band received, exit; row kernel - entry, after the
- * wait, exit. Records past the capacity (bytes - 64) / 64 are dropped. Runs the
+ * then fifteen u64 %globaltimer stamps in ns (0 = not recorded): GEMM - entry, after
+ * the programmatic-dependent-launch wait, MMAs complete, partial rows pushed, split-K
+ * rows received, outputs written, exit; attention - entry, after the wait, operands
+ * loaded, chunk values transposed, S = Q K^T complete, pass 1 done, cluster peers
+ * started, statistics sent, statistics received, P written, O = P V complete, O band
+ * copies issued, O band received, band stored, exit; row kernel - entry, after the
+ * wait, exit. Records past the capacity (bytes - 64) / 128 are dropped. Runs the
  * decision twice (the first warms the new graph up) and synchronises; a diagnostic,
  * not the timed path. */
 int fm_decode_timeline(fm_policy* p, const float* noise, float* actions, void* buf, size_t bytes, void* stream);
