@@ -281,7 +281,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": ("fp8_e4m3" + (" (attention too)" if cfg.attn_fmt == "fp8" else "")) if cfg.weight_fmt == "fp8"
-        else "nvfp4 weights, fp8_e4m3 activations, f16 MMA",
+        else f"nvfp4 weights, {'nvfp4' if cfg.act_fmt == 'nvfp4' else 'fp8_e4m3'} activations, f16 MMA",
         "data": "synthetic (seeded N(0,1)/N(0,0.02) weights, prefix KV, noise; no trained weights)",
         "config": {"workload": cfg.name, "layers": cfg.L, "euler_steps": cfg.S, "action_rows": cfg.M,
                    "d_model": cfg.d, "heads": f"{cfg.H}x{cfg.Dh} (kv {cfg.Hkv})", "prefix_tokens": cfg.P,
@@ -905,7 +905,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["expert_fp8_m50", "expert_fp8attn_m50", "wam_nvfp4_m256"], default=WORKLOAD,
+    ap.add_argument("--workload", choices=["expert_fp8_m50", "expert_fp8attn_m50", "wam_nvfp4_m256", "wam_w4a4_m256"],
+                    default=WORKLOAD,
                     help="decoder workload (default: the 18-layer FP8 action expert, M = 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the PDL-off / graph-off timings")

@@ -35,6 +35,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace fm {
 
@@ -183,7 +184,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   // log2(e) / sqrt(Dh), times the E4M3 codes' dequantisation fp32(s_q * s_k)
   const float kscale = 1.4426950408889634f * rsqrtf(static_cast<float>(kDh)) *
                        (kF8 ? __fmul_rn(p.s_qkv[0], p.s_qkv[1]) : 1.0f);
-  const float rs = p.out_fp8 ? 1.0f / *p.s_out : 1.0f;
+  // E4M3 output: the reciprocal of its static scale; four-bit output: the tensor scale
+  const float rs = p.out_fp8 ? (p.out_fp8 == kQNvfp4AsF16 ? *p.s_out : 1.0f / *p.s_out) : 1.0f;
   const float dv = kF8 ? __fdiv_rn(p.s_qkv[2], 448.0f) : 1.0f;   // E4M3 P and V: fp32(s_v / 448)
 
   if (tid == 0) {
@@ -560,7 +562,21 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       }
       const int hl = R / p.M, m = R % p.M;
       const size_t oidx = static_cast<size_t>(m) * (p.H * kDh) + (g * p.G + hl) * kDh + d0 + e4;
-      if (p.out_fp8) {
+      if (p.out_fp8 == kQNvfp4AsF16) {
+        // four-bit output: a 16-dim block is four consecutive lanes of this row (the row's
+        // lanes run the loop together: mask them)
+        const unsigned rmask = kLanesRow == 32 ? 0xffffffffu : (0xffffu << (lane & 16));
+        float a = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
+        a = fmaxf(a, __shfl_xor_sync(rmask, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(rmask, a, 2));
+        float den;
+        const float bs = nvfp4_block(a, rs, &den);
+        const __half2 lo = nvfp4_pair(acc.x, acc.y, bs, den), hi = nvfp4_pair(acc.z, acc.w, bs, den);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(p.out) + oidx) = u;
+      } else if (p.out_fp8) {
         uchar4 cc;
         cc.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.x * rs, __NV_SATFINITE, __NV_E4M3));
         cc.y = static_cast<uint8_t>(__nv_cvt_float_to_fp8(acc.y * rs, __NV_SATFINITE, __NV_E4M3));

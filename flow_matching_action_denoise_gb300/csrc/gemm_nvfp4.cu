@@ -31,6 +31,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace fm {
 
@@ -54,10 +55,14 @@ struct NvParams {
   const float* sa;
   const float* sw;
   const float* sq;
+  int geglu_nvfp4;      // out_geglu holds four-bit activation values e * bs (tensor scale *sq)
   int M, N;
   int nkb_total, nkb_cta;
   int n_pad, op_stages, raw_stages, chunk;
   int* err;
+  // diagnostic timeline (nullptr = off): entry, after the PDL wait, MMAs complete,
+  // outputs written, exit
+  unsigned long long* tl;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -116,6 +121,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   const int kb0 = j * p.nkb_cta;
   const int nst = p.nkb_cta / C;   // stages to run
   const uint32_t ncols = pow2_at_least(static_cast<uint32_t>(p.n_pad), 32);
+  const bool tl_on = p.tl != nullptr && tid == 0;
+  __shared__ uint64_t tt[kTlStamps];   // timeline stamps (thread 0)
+  if (tl_on)
+    for (int i = 0; i < kTlStamps; ++i) tt[i] = 0;
+  if (tl_on) tt[0] = global_ns();
 
   if (tid == 0) {
     s_abort = 0;
@@ -145,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
   const bool geglu = p.out_geglu != nullptr;
   const float ds = geglu ? __fmul_rn(*p.sa, *p.sw) : 1.0f;
-  const float rs = geglu ? 1.0f / *p.sq : 1.0f;
+  const float rs = geglu ? (p.geglu_nvfp4 ? *p.sq : 1.0f / *p.sq) : 1.0f;   // four-bit: ts itself
   pdl_trigger();   // after TMEM is held (see the FP8 GEMM)
 
   if (tid == 0) {
@@ -161,6 +171,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     }
     int raw_issued = pre, act_issued = 0;
     pdl_wait();   // the activations are written by the previous kernel
+    if (tl_on) tt[1] = global_ns();
     for (int st = 0; st < nst; ++st) {
       const int slot = st % S;
       if (st >= S && !mbar_wait(&op_empty[slot], static_cast<uint32_t>((st / S) - 1) & 1u)) {
@@ -261,6 +272,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     atomicOr(p.err, kErrPipelineTimeout);
     s_abort = 1;
   }
+  if (tl_on) tt[2] = global_ns();
   tc_fence_after();
   __syncthreads();
   const bool abort = s_abort != 0;
@@ -279,9 +291,21 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
       for (int i = 0; i < 16; ++i) {
         const float up = __shfl_xor_sync(0xffffffffu, v[i], 16);
         const int m = c + i;
-        if (lane < 16 && m < p.M) {
-          const float x = v[i] * ds, u = up * ds;
-          const float mv = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * u;
+        const float x = v[i] * ds, u = up * ds;
+        const float mv = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * u;
+        if (p.geglu_nvfp4) {
+          // lanes 0-15 hold one 16-column block of this row: its amax by shuffles within
+          // the half-warp (lanes 16-31 carry up values and are not stored)
+          float a = fabsf(mv);
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+          a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+          float den;
+          const float bs = nvfp4_block(a, rs, &den);
+          if (lane < 16 && m < p.M)
+            p.out_geglu[static_cast<size_t>(m) * (p.N / 2) + col] = __low2half(nvfp4_pair(mv, 0.f, bs, den));
+        } else if (lane < 16 && m < p.M) {
           const uint8_t code = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv * rs, __NV_SATFINITE, __NV_E4M3));
           p.out_geglu[static_cast<size_t>(m) * (p.N / 2) + col] = e4m3_half(code);
         }
@@ -294,6 +318,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     }
   }
 
+  if (tl_on) tt[3] = global_ns();
   // On an abandoned pipeline, let copies already in flight land before the CTA exits.
   if (abort && tid == 0) {
     const int ri = s_raw_issued, ai = s_act_issued;
@@ -304,6 +329,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
+  if (tl_on) {
+    tt[4] = global_ns();
+    tl_record(p.tl, kTlNvfp4, gridDim.y, blockIdx.y, tt);
+  }
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -424,7 +453,7 @@ cudaError_t nvfp4_configure() {
 
 cudaError_t nvfp4_gemm_launch(const CUtensorMap& tmA, const void* wpk, const Nvfp4Shape& g, float* out,
                               __half* out_geglu, const float* sa, const float* sw, const float* sq, int* err,
-                              const LaunchOpts& o) {
+                              const LaunchOpts& o, int geglu_nvfp4) {
   if (out_geglu && (g.s != 1 || !sa || !sw || !sq)) return cudaErrorInvalidValue;
   if (!out_geglu && !out) return cudaErrorInvalidValue;
   NvParams p;
@@ -434,6 +463,8 @@ cudaError_t nvfp4_gemm_launch(const CUtensorMap& tmA, const void* wpk, const Nvf
   p.sa = sa;
   p.sw = sw;
   p.sq = sq;
+  p.geglu_nvfp4 = geglu_nvfp4;
+  p.tl = o.tl;
   p.M = g.M;
   p.N = g.N;
   p.nkb_total = g.nkb_total;

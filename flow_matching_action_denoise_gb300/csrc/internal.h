@@ -145,10 +145,11 @@ int nvfp4_plan(int M, int N, int K, int s, Nvfp4Shape* g);
 bool nvfp4_tmap_act(CUtensorMap* map, const void* a, const Nvfp4Shape& g);
 cudaError_t nvfp4_configure();
 // out: fp32 partial planes [s][M][N]; or out_geglu (s == 1, gate|up packed with
-// interleave): f16 values of E4M3(gelu(g) u * (1/s_q)) [M][N/2], g, u dequantised by fp32(sa * sw).
+// interleave): f16 values of E4M3(gelu(g) u * (1/s_q)) [M][N/2], g, u dequantised by fp32(sa * sw);
+// with geglu_nvfp4 instead the four-bit activation values e * bs of gelu(g) u with tensor scale s_q.
 cudaError_t nvfp4_gemm_launch(const CUtensorMap& tmA, const void* wpk, const Nvfp4Shape& g, float* out,
                               __half* out_geglu, const float* sa, const float* sw, const float* sq, int* err,
-                              const LaunchOpts& o);
+                              const LaunchOpts& o, int geglu_nvfp4 = 0);
 size_t nvfp4_packed_bytes(int N, int K);
 cudaError_t pack_nvfp4(const float* w, const float* gamma, int N, int K, void* packed, float* ts_out,
                        unsigned* amax_scratch, cudaStream_t st, int geglu_interleave);
@@ -164,8 +165,10 @@ cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fm
 
 // ---------------------------------------------------------------- row kernels
 // Storage of a quantised GEMM operand (RowArgs::q_fp8, AttnArgs::out_fp8):
-// 0 = bf16 values, 1 = E4M3 codes, 2 = E4M3 codes stored as their f16 values.
+// 0 = bf16 values, 1 = E4M3 codes, 2 = E4M3 codes stored as their f16 values,
+// 3 = four-bit (NVFP4) activations stored as the f16 values e * bs (quant.cuh).
 constexpr int kQFp8AsF16 = 2;
+constexpr int kQNvfp4AsF16 = 3;
 // y[m][n] = bf16(sum_j planes[j][m][n] * fp32(sa * sw)) for s K-slice planes [s][M][N].
 cudaError_t qkv_finalize_launch(const float* planes, int s, int M, int N, const float* sa, const float* sw,
                                 __nv_bfloat16* out, const LaunchOpts& o);

@@ -73,7 +73,9 @@ struct Derived {
   int act_bytes;
   int fp8;
   int nvfp4;
-  int q_store;   // quantised operand storage: 0 bf16, 1 E4M3 codes, 2 E4M3 codes as f16 values
+  int q_store;   // quantised operand storage: 0 bf16, 1 E4M3 codes, 2 E4M3 codes as f16 values,
+                 // 3 four-bit activation values e * bs as f16
+  int act4;      // four-bit (NVFP4) activations: block scales from the activation, static tensor scale
   int attn_fp8;  // attention on E4M3 Q, K, V and probabilities
   // FP8/BF16: the consumers run inside the GEMMs - the O and down GEMM epilogues apply
   // the gated residual and emit per-tile sums of squares, the QKV and gate|up GEMMs
@@ -123,7 +125,7 @@ int validate(const fm_config* c, std::string* why) {
   }
   const bool fmt_ok = (c->weight_fmt == FM_FMT_FP8 && c->act_fmt == FM_FMT_FP8) ||
                       (c->weight_fmt == FM_FMT_BF16 && c->act_fmt == FM_FMT_BF16) ||
-                      (c->weight_fmt == FM_FMT_NVFP4 && c->act_fmt == FM_FMT_FP8);
+                      (c->weight_fmt == FM_FMT_NVFP4 && (c->act_fmt == FM_FMT_FP8 || c->act_fmt == FM_FMT_NVFP4));
   if (!fmt_ok) {
     *why = "unsupported weight/activation format pair";
     return FM_ERR_INVALID_ARG;
@@ -162,7 +164,8 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
   dv->nqkv = (c->H + 2 * c->Hkv) * c->Dh;
   dv->fp8 = c->act_fmt == FM_FMT_FP8;
   dv->nvfp4 = c->weight_fmt == FM_FMT_NVFP4;
-  dv->q_store = dv->nvfp4 ? fm::kQFp8AsF16 : dv->fp8;
+  dv->act4 = c->act_fmt == FM_FMT_NVFP4;
+  dv->q_store = dv->nvfp4 ? (dv->act4 ? fm::kQNvfp4AsF16 : fm::kQFp8AsF16) : dv->fp8;
   dv->attn_fp8 = c->attn_fmt == FM_FMT_FP8;
   dv->rowfuse = 0;
   dv->act_bytes = dv->q_store == 1 ? 1 : 2;
@@ -389,7 +392,7 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15)
 std::vector<float> scale_table(const fm_config& c, const Derived& dv, const float* act_scales) {
   std::vector<float> sc(static_cast<size_t>(c.L) * 8, 1.0f);
   const int cols = dv.attn_fp8 ? 7 : 4;
-  if (dv.fp8 && act_scales)
+  if ((dv.fp8 || dv.act4) && act_scales)
     for (int l = 0; l < c.L; ++l)
       for (int i = 0; i < cols; ++i) sc[static_cast<size_t>(l) * 8 + i] = act_scales[static_cast<size_t>(l) * cols + i];
   return sc;
@@ -558,7 +561,8 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   // gate|up: the epilogue applies GeGLU and quantises, writing the down GEMM's operand
   if (dv.nvfp4)
     e = fm::nvfp4_gemm_launch(p->tmA[2], p->at<void>(p->ly.wpk[l * 4 + 2]), dv.ns[2], nullptr, p->at<__half>(p->ly.mc),
-                              p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->ascale(l, FM_SITE_GEGLU), err, o);
+                              p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->ascale(l, FM_SITE_GEGLU), err, o,
+                              dv.act4);
   else
     e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 2]), p->tmA[2], dv.gs[2], nullptr, err, o, nullptr,
                         p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->at<void>(p->ly.mc), fp8,
@@ -924,8 +928,8 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
   if (st != FM_OK) return fail(nullptr, st, why);
   st = check_ptrs(w, cfg->L, cfg->cond_mode == FM_COND_GIVEN, &why);
   if (st != FM_OK) return fail(nullptr, st, why);
-  if (cfg->act_fmt == FM_FMT_FP8 && !act_scales)
-    return fail(nullptr, FM_ERR_INVALID_ARG, "FP8 activations need an activation-scale table");
+  if ((cfg->act_fmt == FM_FMT_FP8 || cfg->act_fmt == FM_FMT_NVFP4) && !act_scales)
+    return fail(nullptr, FM_ERR_INVALID_ARG, "FP8 and four-bit activations need an activation-scale table");
   if (!workspace) return fail(nullptr, FM_ERR_INVALID_ARG, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return fail(nullptr, FM_ERR_ALIGN, "workspace not 1024-aligned");
 
@@ -1109,7 +1113,7 @@ int fm_session_create(fm_policy* base, void* workspace, size_t ws_bytes, void* s
 
 int fm_set_act_scales(fm_policy* p, const float* act_scales, void* stream) {
   if (!p || !act_scales) return fail(p, FM_ERR_INVALID_ARG, "NULL argument");
-  if (!p->dv.fp8) return FM_OK;
+  if (!p->dv.fp8 && !p->dv.act4) return FM_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const std::vector<float> sc = scale_table(p->cfg, p->dv, act_scales);
   FM_CUDA(p, cudaMemcpyAsync(p->at<void>(p->ly.ascale), sc.data(), sc.size() * 4, cudaMemcpyHostToDevice, s));

@@ -23,6 +23,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace fm {
 
@@ -98,7 +99,8 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
   // Per-create constants (scales, modulation rows) do not depend on the previous
   // kernel: fetch them before waiting for it.
   const float ds = r.parts ? __fmul_rn(*r.sa, *r.sw) : 0.f;
-  const float rs_q = (r.do_quant && r.q_fp8) ? 1.0f / *r.sq : 1.0f;
+  // E4M3: the reciprocal of the static scale; four-bit: the tensor scale itself
+  const float rs_q = (r.do_quant && r.q_fp8) ? (r.q_fp8 == kQNvfp4AsF16 ? *r.sq : 1.0f / *r.sq) : 1.0f;
   constexpr int kPre = 2;   // column groups per thread kept in registers (N <= 2048); the
                             // selects below name both explicitly (static register indices)
   float4 gate_v[kPre], scale_v[kPre], shift_v[kPre];
@@ -281,7 +283,22 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(const RowArgs r) {
       h.y = fmaf(x.y * rr, 1.f + sc.y, sh.y);
       h.z = fmaf(x.z * rr, 1.f + sc.z, sh.z);
       h.w = fmaf(x.w * rr, 1.f + sc.w, sh.w);
-      store_q4(r.q, static_cast<size_t>(m) * N + c * 4, h, r.q_fp8, rs);
+      if (r.q_fp8 == kQNvfp4AsF16) {
+        // a 16-element block is four consecutive threads' columns (c = tid + 256 u): their
+        // amax by two shuffles; every lane of the warp takes part (N is a multiple of 128)
+        float a = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        float den;
+        const float bs = nvfp4_block(a, rs, &den);
+        const __half2 lo = nvfp4_pair(h.x, h.y, bs, den), hi = nvfp4_pair(h.z, h.w, bs, den);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(r.q) + static_cast<size_t>(m) * N + c * 4) = u;
+      } else {
+        store_q4(r.q, static_cast<size_t>(m) * N + c * 4, h, r.q_fp8, rs);
+      }
     }
   }
   if (r.stamp_kind == 2) {   // the decision's last kernel: latest CTA end

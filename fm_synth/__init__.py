@@ -84,6 +84,9 @@ CONFIGS = {
     # world-action-model-sized decoder, NVFP4 weights, FP8 activations
     "wam_nvfp4_m256": Config("wam_nvfp4_m256", L=28, S=10, M=256, d=2048, H=16, Hkv=2, Dh=128,
                              F=8192, P=1024, A=32, weight_fmt="nvfp4", act_fmt="fp8", seed=4),
+    # the same decoder with four-bit activations too (W4A4: NVFP4 weights and activations)
+    "wam_w4a4_m256": Config("wam_w4a4_m256", L=28, S=10, M=256, d=2048, H=16, Hkv=2, Dh=128,
+                            F=8192, P=1024, A=32, weight_fmt="nvfp4", act_fmt="nvfp4", seed=4),
 }
 
 
@@ -181,7 +184,9 @@ def default_act_scales(cfg: Config) -> np.ndarray:
     base = [24.0, 1.0, 24.0, 16.0]
     if cfg.attn_fmt == "fp8":   # FP8 attention adds Q, K, V (columns 4-6 of an [L][7] table)
         base += [8.0, 8.0, 8.0]
-    return np.tile(np.array(base, np.float32) / np.float32(448.0), (cfg.L, 1)).astype(np.float32)
+    # E4M3 codes: amax / 448; four-bit activations: the tensor scale amax / (448 * 6)
+    div = np.float32(2688.0) if cfg.act_fmt == "nvfp4" else np.float32(448.0)
+    return np.tile(np.array(base, np.float32) / div, (cfg.L, 1)).astype(np.float32)
 
 
 def gemm_case(M: int, K: int, N: int, seed: int = 2, integer: bool = False) -> dict:

@@ -63,7 +63,9 @@ typedef enum fm_status {
 typedef enum fm_format {
   FM_FMT_BF16 = 0,   /* bf16 operands, no quantisation */
   FM_FMT_FP8 = 1,    /* E4M3 codes with a static per-tensor scale */
-  FM_FMT_NVFP4 = 2   /* weights only: E2M1 + E4M3 scale per 16 along K + fp32 tensor scale */
+  FM_FMT_NVFP4 = 2   /* E2M1 + E4M3 scale per 16 along K + fp32 tensor scale (weights: all three
+                        fixed at create; activations: static tensor scale, block scales taken
+                        from the activation at run time) */
 } fm_format;
 
 enum {
@@ -103,15 +105,16 @@ enum {
  *   1 <= M <= 256; 1 <= A <= 32; P >= 0; L, S >= 1; 0 <= warm_t <= 1 (warm_t > 0
  *   requires FM_COND_TIME);
  *   ksplit[i] (0 = automatic) divides the GEMM's K/128-byte block count.
- * act_fmt must be FP8 or BF16; weight_fmt FP8 requires act_fmt FP8, BF16
- * requires BF16, NVFP4 requires FP8. With NVFP4 weights the K-split counts
+ * weight_fmt FP8 requires act_fmt FP8, BF16 requires BF16, NVFP4 takes FP8 or NVFP4
+ * (four-bit weights and activations: the activation scale table then holds each quant
+ * point's static tensor scale, amax / (448 * 6)). With NVFP4 weights the K-split counts
  * 64-element blocks, the gate|up GEMM is not split (ksplit[2] 0 or 1), and a
  * layer runs 8 kernels (the QKV partial planes are reduced by their own kernel). */
 typedef struct fm_config {
   int abi_version;     /* must be FM_ABI_VERSION */
   int L, S, M, d, H, Hkv, Dh, F, P, A;
   int weight_fmt;      /* fm_format */
-  int act_fmt;         /* fm_format (FP8 or BF16) */
+  int act_fmt;         /* fm_format (FP8, BF16, or NVFP4 with NVFP4 weights) */
   int attn_fmt;        /* fm_format of the attention operands: BF16, or FP8 (E4M3 Q, K, V
                           with static scales and probabilities coded E4M3(P * 448));
                           FP8 requires FP8 weights and activations */
@@ -335,7 +338,8 @@ int fm_standalone_status(void* stream, int* word);
  *   "weight_scales"         fp32 [L][4]
  *   "mod"                   fp32 [S][L][6][d]; "mod_final" fp32 [S][2][d]
  * Codes are one byte (FP8 activations), bf16 (BF16), or, with NVFP4 weights, the
- * E4M3 codes' f16 values (two bytes, exact: the operand format of the NVFP4 GEMM).
+ * E4M3 codes' f16 values (two bytes, exact: the operand format of the NVFP4 GEMM) or,
+ * with NVFP4 activations, the f16 values e * bs of the four-bit codes (exact).
  * FM_ERR_INVALID_ARG for an unknown name. */
 int fm_named_buffer(const fm_policy* p, const char* name, void** ptr, size_t* bytes);
 
@@ -360,7 +364,8 @@ int fm_trace_size(const fm_policy* p, size_t* bytes);
  *                             a step that is not the last, the next step's x
  *                             (after the Euler update and input projection)
  *   actions fp32 [M][A]       the noise/action state after this layer-step
- * Codes are one byte (FP8) or bf16 (BF16 activations). Synchronous. */
+ * Codes are one byte (FP8), bf16 (BF16 activations), or f16 values with NVFP4 weights
+ * (E4M3 code values, or e * bs with NVFP4 activations). Synchronous. */
 int fm_decode_trace(fm_policy* p, const float* noise, float* actions, void* trace, size_t bytes, void* stream);
 
 /* The warm start of fm_decode_warm (same arguments, launched one by one, no graph),

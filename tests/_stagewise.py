@@ -29,15 +29,35 @@ def bf16_ulp(v):
     return np.ldexp(1.0, np.maximum(E - 1, -126) - 7)
 
 
+def nvfp4_step(got, ref):
+    """One grid step of four-bit activation values e * bs (E2M1 e, E4M3 block scale bs
+    per 16 consecutive elements of the last axis) at the larger of the two magnitudes:
+    every block's largest code is 6 (the block scale is amax / 6, rounded), so bs is the
+    block's largest magnitude / 6; the E2M1 step is 0.5, 1 or 2 for |e| below 2, 4, 6.
+    The larger of the two block scales covers a block whose scale rounded differently."""
+    g, r = np.abs(got), np.abs(ref)
+    shp = g.shape
+    gb, rb = g.reshape(-1, 16), r.reshape(-1, 16)
+    bs = np.maximum(gb.max(axis=1), rb.max(axis=1))[:, None] / 6.0
+    v = np.maximum(gb, rb)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.where(bs > 0, v / np.where(bs > 0, bs, 1.0), 0.0)
+    step = np.where(e < 2, 0.5, np.where(e < 4, 1.0, 2.0)) * bs
+    return step.reshape(shp)
+
+
 def check_codes(got_values, ref_values, what, fmt="fp8", max_frac=1e-3, abs_tol=1e-3, extra=0.0):
     """Quantised operands agree when they differ by at most one grid step at the larger
     magnitude plus abs_tol * RMS (plus a per-element `extra`): a near-tie input rounds
     either way, and near zero (subnormal steps) a tiny upstream difference can span
     several steps."""
     got, ref = np.asarray(got_values, np.float64), np.asarray(ref_values, np.float64)
-    ulp = e4m3_ulp if fmt == "fp8" else bf16_ulp
     diff = np.abs(got - ref)
-    allow = ulp(np.maximum(np.abs(got), np.abs(ref))) + abs_tol * np.sqrt(np.mean(ref ** 2)) + extra
+    if fmt == "nvfp4":
+        step = nvfp4_step(got, ref)
+    else:
+        step = (e4m3_ulp if fmt == "fp8" else bf16_ulp)(np.maximum(np.abs(got), np.abs(ref)))
+    allow = step + abs_tol * np.sqrt(np.mean(ref ** 2)) + extra
     bad = diff > allow * (1 + 1e-12)
     if np.any(bad):
         i = np.unravel_index(np.argmax(diff - allow), diff.shape)
@@ -112,7 +132,7 @@ def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac
     kp, vp = np.asarray(kp, np.float64), np.asarray(vp, np.float64)
 
     def s_act(l, i):
-        return float(scales[l][i]) if fmt == "fp8" else 1.0
+        return float(scales[l][i]) if fmt in ("fp8", "nvfp4") else 1.0
 
     def dq(l, i, w):   # dequantisation factor fp32(s_a * s_w) the epilogues apply
         return np.float64(np.float32(s_act(l, i)) * np.float32(w.scale))

@@ -1,5 +1,6 @@
 """The stage-by-stage checker the GPU parity tests use (tests/_stagewise.py),
-exercised on CPU for FP8, BF16 and FP8-attention decisions: records produced by the oracle
+exercised on CPU for FP8, BF16, FP8-attention and four-bit (W4A4: NVFP4 weights and
+activations) decisions: records produced by the oracle
 itself in the trace's layout pass, and records from an implementation with a
 plausible mistake (gate and up
 swapped, a dropped residual gate, the Euler sign, the next layer's modulation in
@@ -18,14 +19,16 @@ from _stagewise import check_decision_stages, prefix_codes
 def tiny(fmt="fp8"):
     attn8 = fmt == "fp8attn"
     fmt = "fp8" if attn8 else fmt
+    wfmt, afmt = ("nvfp4", "nvfp4") if fmt == "w4a4" else (fmt, fmt)
     cfg = fm_synth.Config(name="tiny_stages", L=2, S=2, M=3, d=32, H=2, Hkv=1, Dh=16, F=64, P=4, A=4,
-                          weight_fmt=fmt, act_fmt=fmt, seed=21, attn_fmt="fp8" if attn8 else "bf16")
+                          weight_fmt=wfmt, act_fmt=afmt, seed=21, attn_fmt="fp8" if attn8 else "bf16")
     layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
     model = O.Model(cfg, layers, fm_synth.final_weights(cfg))
     kp, vp = fm_synth.prefix_kv(cfg)
     nz = fm_synth.noise(cfg, 0)
     cols = 7 if attn8 else 4
-    sc = O.calibrate(model, nz, kp, vp, np.full((cfg.L, cols), 0.05, np.float32)) if fmt == "fp8" else None
+    sc = (O.calibrate(model, nz, kp, vp, np.full((cfg.L, cols), 0.05, np.float32))
+          if afmt in ("fp8", "nvfp4") else None)
     return cfg, model, kp, vp, nz, sc
 
 
@@ -36,7 +39,7 @@ def records(cfg, model, kp, vp, nz, sc, mistake=None):
     fmt = cfg.act_fmt
     attn8 = cfg.attn_fmt == "fp8"
     prefix8 = prefix_codes(kp, vp, sc) if attn8 else None
-    s_act = lambda l, i: float(sc[l][i]) if fmt == "fp8" else 1.0
+    s_act = lambda l, i: float(sc[l][i]) if fmt in ("fp8", "nvfp4") else 1.0
     fin = model.final
     nq, nk = H * Dh, cfg.Hkv * Dh
     dq = lambda l, i, w: np.float64(np.float32(s_act(l, i)) * np.float32(w.scale)) * (
@@ -53,7 +56,8 @@ def records(cfg, model, kp, vp, nz, sc, mistake=None):
             if mistake == "next_layer_mod":
                 sc2, sh2 = model.mods[k][0][(l + 1) % L][3], model.mods[k][0][(l + 1) % L][4]
             r["x_in"] = x
-            r["q"] = O.quant_codes(O.ada_norm(x, sc1, sh1, cfg.eps), s_act(l, 0), fmt)
+            r["q"] = O.quant_codes(O.ada_norm(x, sc1, sh1, cfg.eps), s_act(l, 0),
+                                   "fp8" if mistake == "act_e4m3" else fmt)
             exact = (r["q"] @ W["qkv"].codes.T) * dq(l, 0, W["qkv"])
             if attn8:   # E4M3 Q | K | V codes with their static scales; attention on codes
                 s3 = [s_act(l, O.SITE_Q), s_act(l, O.SITE_K), s_act(l, O.SITE_V)]
@@ -94,7 +98,7 @@ def records(cfg, model, kp, vp, nz, sc, mistake=None):
     return recs
 
 
-@pytest.fixture(scope="module", params=["fp8", "bf16", "fp8attn"])
+@pytest.fixture(scope="module", params=["fp8", "bf16", "fp8attn", "w4a4"])
 def case(request):
     return tiny(request.param)
 
@@ -114,6 +118,13 @@ def test_planted_mistake_fails(case, mistake):
     cfg, model, kp, vp, nz, sc = case
     with pytest.raises(AssertionError):
         check_decision_stages(cfg, model, records(cfg, model, kp, vp, nz, sc, mistake), nz, kp, vp, sc)
+
+
+def test_w4a4_planted_e4m3_activations_fail():
+    """Four-bit activations quantised as E4M3 codes instead (the wrong operand format)."""
+    cfg, model, kp, vp, nz, sc = tiny("w4a4")
+    with pytest.raises(AssertionError):
+        check_decision_stages(cfg, model, records(cfg, model, kp, vp, nz, sc, "act_e4m3"), nz, kp, vp, sc)
 
 
 def test_fp8_attention_planted_scale_fails():
