@@ -401,8 +401,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     s_abort = 1;
   }
   if (tl_on) tt[8] = global_ns();
-  // the row's global max and 1 / sum, once per row (the part-0 thread), in slice order
-  if (part == 0) {
+  // the row's global max and 1 / sum in slice order, by every thread of the row (the
+  // same operations in the same order in each, so no hand-off through shared memory)
+  float gmax, ginv;
+  {
     float2 st[kMaxSplit];
 #pragma unroll
     for (int q = 0; q < kMaxSplit; ++q) st[q] = q < p.nsplit ? sStats[q * kRows + r] : make_float2(-INFINITY, 0.f);
@@ -413,10 +415,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
 #pragma unroll
     for (int q = 0; q < kMaxSplit; ++q)
       if (q < p.nsplit) gs += st[q].y * exp2f(st[q].x - gm);
-    sPart[r] = make_float2(gm, 1.0f / gs);
+    gmax = gm;
+    ginv = 1.0f / gs;
   }
-  __syncthreads();
-  const float gmax = sPart[r].x, ginv = sPart[r].y;
 
   // ---- pass 2: P = bf16(exp(s - m_part) * exp(m_part - M) / L) into the swizzled A
   // operand of P V
@@ -547,12 +548,23 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
       if (rr >= kRows || R >= p.G * p.M) break;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       const int sw = (l16 ^ (rr & 7)) << 2;   // the staged row's swizzled chunk
-      for (int q = 0; q < p.nsplit; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDv + sw);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+      // slots in groups of four whose loads are issued together, summed in slot order
+      for (int q0 = 0; q0 < p.nsplit; q0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int q = q0 + j < p.nsplit ? q0 + j : q0;
+          v[j] = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kDv + sw);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (q0 + j < p.nsplit) {
+            acc.x += v[j].x;
+            acc.y += v[j].y;
+            acc.z += v[j].z;
+            acc.w += v[j].w;
+          }
+        }
       }
       if constexpr (kF8) {
         acc.x *= dv;
