@@ -837,6 +837,80 @@ def run_layer_protocol(args):
             "steps": args.steps, "clocks": clocks.summary()}
 
 
+def run_timeline(args):
+    """Where a decision's time goes: one decision replayed as the same CUDA graph with a
+    per-CTA timeline (fm_decode_timeline), summarised per kernel position in a
+    layer-step: the hand-off (the previous kernel's last CTA exit -> this kernel's last
+    programmatic-dependent-launch wait return), the kernel's own time after that wait,
+    and the median of each recorded stamp after the wait (us), averaged over every
+    layer-step but the first two."""
+    import collections
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    device = torch.device("cuda", 0)
+    fmad.load()
+    cfg = fm_synth.config(args.workload, S=args.timeline_steps) if args.timeline_steps else fm_synth.config(args.workload)
+    layers = [fm_synth.layer_weights(cfg, l) for l in range(cfg.L)]
+    scales = fm_synth.default_act_scales(cfg) if cfg.act_fmt in ("fp8", "nvfp4") else None
+    pol = fmad.Policy(cfg, layers, fm_synth.final_weights(cfg), act_scales=scales, device=device)
+    del layers
+    kp, vp = fm_synth.prefix_kv(cfg)
+    pol.set_prefix_kv(torch.from_numpy(kp).to(device, torch.bfloat16), torch.from_numpy(vp).to(device, torch.bfloat16))
+    noise = torch.from_numpy(fm_synth.noise(cfg, 0)).to(device)
+    act = torch.empty_like(noise)
+    for _ in range(max(3, args.warmup)):
+        pol.decode(noise, act)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        pol.decode(noise, act)
+    e1.record()
+    torch.cuda.synchronize(device)
+    plain_ms = e0.elapsed_time(e1) / args.steps
+    nrec = 2 * (1 + cfg.L * cfg.S * 8) * 256
+    buf = torch.zeros(64 + 128 * nrec, dtype=torch.uint8, device=device)
+    fmad.decode_timeline(pol.handle, noise, act, buf, buf.numel())
+    if fmad.device_status(pol.handle):
+        raise RuntimeError("device error word set (timeline)")
+    pol.close()
+    recs = fmad.parse_timeline(buf.cpu().numpy())
+    by = collections.defaultdict(list)
+    for r in recs:
+        by[(r["kind"], r["grid"])].append(r)
+    inst = []
+    for sig, rs in by.items():
+        n = sig[1][0] * sig[1][1]
+        rs.sort(key=lambda r: r["t"][0])
+        inst += [(sig, rs[i:i + n]) for i in range(0, len(rs), n)]
+    inst.sort(key=lambda x: min(r["t"][0] for r in x[1]))
+    kinds = {1: "gemm", 2: "attention", 3: "row", 4: "nvfp4_gemm"}
+    kpl = (len(inst) - 1) // (cfg.L * cfg.S)
+    per = collections.defaultdict(list)
+    prev_exit = None
+    for i, (sig, rs) in enumerate(inst):
+        wait = max(r["t"][1] for r in rs)
+        ex = max(max(r["t"]) for r in rs)
+        stamps = [float(np.median([r["t"][j] - wait for r in rs if r["t"][j]])) / 1e3
+                  if any(r["t"][j] for r in rs) else None for j in range(2, 15)]
+        if i >= 1 and (i - 1) // kpl >= 2:
+            per[((i - 1) % kpl, f"{kinds[sig[0]]} grid {sig[1][0]}x{sig[1][1]}")].append(
+                ((wait - prev_exit) / 1e3, (ex - wait) / 1e3, stamps))
+        prev_exit = ex
+    rows = []
+    for (pos, name), v in sorted(per.items()):
+        st = [round(float(np.mean([s[j] for _, _, s in v])), 2) if v[0][2][j] is not None else None for j in range(13)]
+        rows.append({"position": pos, "kernel": name, "handoff_us": round(float(np.mean([a for a, _, _ in v])), 2),
+                     "own_us": round(float(np.mean([b for _, b, _ in v])), 2),
+                     "stamps_after_wait_us": [x for x in st if x is not None]})
+    t0 = min(r["t"][0] for r in recs)
+    t1 = max(max(r["t"]) for r in recs)
+    return {"protocol": "in-graph kernel timeline (fm_decode_timeline)", "workload": cfg.name, "layers": cfg.L,
+            "euler_steps": cfg.S, "decision_ms": round(plain_ms, 4), "timeline_decision_ms": round((t1 - t0) / 1e6, 4),
+            "kernels_per_layer_recorded": kpl,
+            "per_layer_step_us": round(sum(r["handoff_us"] + r["own_us"] for r in rows), 2), "kernels": rows}
+
+
 def run_gemm_sweep(args):
     """Skinny GEMM + fused consumer (fm_gemm_consumer: bias + gated residual + AdaRMSNorm
     + static E4M3 quantise) over M in {1, 10, 50, 63}, K in {1024, 2048, 4096},
@@ -905,7 +979,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["expert_fp8_m50", "expert_fp8attn_m50", "wam_nvfp4_m256", "wam_w4a4_m256"],
+    ap.add_argument("--workload", choices=["expert_fp8_m50", "expert_fp8attn_m50", "wam_nvfp4_m256", "wam_w4a4_m256",
+                                           "expert_bf16_m63"],
                     default=WORKLOAD,
                     help="decoder workload (default: the 18-layer FP8 action expert, M = 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -918,11 +993,18 @@ def main():
                     help="run only the single-layer protocol (M = 10, rotating weight copies > 2x L2)")
     ap.add_argument("--gemm-sweep", action="store_true",
                     help="run only the skinny GEMM + fused consumer sweep (240 points)")
+    ap.add_argument("--timeline", action="store_true",
+                    help="run only the in-graph kernel timeline of one decision of --workload")
+    ap.add_argument("--timeline-steps", type=int, default=0,
+                    help="with --timeline: Euler steps of the timed policy (0 = the workload's)")
     ap.add_argument("--bf16-protocol", action="store_true",
                     help="run only the matched 16-bit persistence protocol (100 decisions, refresh every 5th)")
     args = ap.parse_args()
     if args.bf16_protocol:
         print(json.dumps(run_bf16_protocol(args)), flush=True)
+        return
+    if args.timeline:
+        print(json.dumps(run_timeline(args)), flush=True)
         return
     if args.layer_protocol:
         print(json.dumps(run_layer_protocol(args)), flush=True)
@@ -933,6 +1015,8 @@ def main():
     if args.profile_case:
         profile_case(args.workload)
         return
+    if args.workload == "expert_bf16_m63":
+        raise SystemExit("expert_bf16_m63 is measured by --bf16-protocol (and profiled with --profile-case)")
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

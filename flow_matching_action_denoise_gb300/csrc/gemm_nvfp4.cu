@@ -285,17 +285,21 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
     if (abort) continue;
     if (geglu) {
-      // lanes 0-15 of a warp hold gate columns, lanes 16-31 the matching up columns
+      // lanes 0-15 of a warp hold gate columns, lanes 16-31 the matching up columns, for 16
+      // rows (the accumulator columns c .. c + 15)
       const size_t col = static_cast<size_t>(nt) * 64 + quarter * 16 + (lane & 15);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float up = __shfl_xor_sync(0xffffffffu, v[i], 16);
-        const int m = c + i;
-        const float x = v[i] * ds, u = up * ds;
+      for (int i = 0; i < 8; ++i) {
+        // lanes 0-15 finish row c + i and lanes 16-31 row c + i + 8: each half passes the
+        // other the value it lacks (the up value of row c + i, the gate value of row c + i + 8)
+        const bool lo = lane < 16;
+        const float got = __shfl_xor_sync(0xffffffffu, lo ? v[i + 8] : v[i], 16);
+        const int m = c + i + (lo ? 0 : 8);
+        const float x = (lo ? v[i] : got) * ds, u = (lo ? got : v[i + 8]) * ds;
         const float mv = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * u;
         if (p.geglu_nvfp4) {
-          // lanes 0-15 hold one 16-column block of this row: its amax by shuffles within
-          // the half-warp (lanes 16-31 carry up values and are not stored)
+          // each half-warp holds one 16-column block of its row: its amax by shuffles
+          // within the half
           float a = fabsf(mv);
           a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
           a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
@@ -303,9 +307,9 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
           a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
           float den;
           const float bs = nvfp4_block(a, rs, &den);
-          if (lane < 16 && m < p.M)
-            p.out_geglu[static_cast<size_t>(m) * (p.N / 2) + col] = __low2half(nvfp4_pair(mv, 0.f, bs, den));
-        } else if (lane < 16 && m < p.M) {
+          if (m < p.M)
+            p.out_geglu[static_cast<size_t>(m) * (p.N / 2) + col] = nvfp4_one(mv, bs, den);
+        } else if (m < p.M) {
           const uint8_t code = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv * rs, __NV_SATFINITE, __NV_E4M3));
           p.out_geglu[static_cast<size_t>(m) * (p.N / 2) + col] = e4m3_half(code);
         }

@@ -39,4 +39,13 @@ __device__ __forceinline__ __half2 nvfp4_pair(float a, float b, float bs, float 
   return __hmul2(__half2(r), __half2(hb, hb));
 }
 
+// f16 value e * bs of one element of a block.
+__device__ __forceinline__ __half nvfp4_one(float a, float bs, float den) {
+  if (!(den > 0.f)) return __float2half_rn(0.f);
+  const __nv_fp4x2_storage_t e =
+      __nv_cvt_float2_to_fp4x2(make_float2(__fdiv_rn(a, den), 0.f), __NV_E2M1, cudaRoundNearest);
+  const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2(e, __NV_E2M1);
+  return __hmul(__low2half(__half2(r)), __float2half_rn(bs));
+}
+
 }  // namespace fm
