@@ -44,6 +44,7 @@ EXPORTS = [
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
     "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes", "fm_standalone_status",
     "fm_warm_trace_size", "fm_decode_warm_trace", "fm_test_launch_kernel", "fm_decode_timeline",
+    "fm_test_skinny_gemm_tile",
 ]
 
 
@@ -115,6 +116,7 @@ def load() -> ctypes.CDLL:
         "fm_packed_weight_bytes": (i, [i, i, i, ctypes.POINTER(sz)]),
         "fm_pack_weight": (i, [vp, vp, i, i, i, vp, vp, vp]),
         "fm_test_skinny_gemm": (i, [vp, i, i, vp, i, i, i, i, vp, vp]),
+        "fm_test_skinny_gemm_tile": (i, [vp, i, i, vp, i, i, i, i, i, vp, vp]),
         "fm_test_consumer": (i, [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, i, vp]),
         "fm_test_layer": (i, [vp, vp, i, i, vp, vp, vp]),
         "fm_named_buffer": (i, [vp, ctypes.c_char_p, ctypes.POINTER(vp), ctypes.POINTER(sz)]),
@@ -410,6 +412,12 @@ def fm_test_skinny_gemm(a, M: int, K: int, w_packed, N: int, fmt: int, s: int, c
                         partials, stream=None):
     _check(load().fm_test_skinny_gemm(_ptr(a), M, K, _ptr(w_packed), N, fmt, s, cluster_reduce,
                                       _ptr(partials), _stream(stream)), "fm_test_skinny_gemm")
+
+
+def fm_test_skinny_gemm_tile(a, M: int, K: int, w_packed, N: int, fmt: int, s: int, cluster_reduce: int,
+                             tile_rows: int, partials, stream=None):
+    _check(load().fm_test_skinny_gemm_tile(_ptr(a), M, K, _ptr(w_packed), N, fmt, s, cluster_reduce, tile_rows,
+                                           _ptr(partials), _stream(stream)), "fm_test_skinny_gemm_tile")
 
 
 def fm_test_consumer(partials, nparts: int, M: int, N: int, s_a, s_w, bias, x, gate, scale, shift,

@@ -83,9 +83,15 @@ __host__ __device__ inline uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-template <bool kFp8, int kCs, int kMode>
+// kTm: weight rows per CTA, the MMA's M: 128, or 64 (the first or second half of a packed
+// 128-row tile; plain placement only), which halves the partial bytes each CTA of a
+// K-split cluster pushes to its peers. With M = 64 the accumulator's row r sits in TMEM
+// lane 32 (r / 16) + r % 16: lanes 0-15 of each warp's lane quarter.
+template <bool kFp8, int kCs, int kMode, int kTm = kTileN>
 __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                const KParams p) {
+  static_assert(kTm == kTileN || (kTm == kTileN / 2 && kMode == 0), "64-row tiles: plain placement only");
+  constexpr uint32_t kTmBytes = kTm * kBlockBytes;   // one K block of this CTA's weight rows
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
   __shared__ int s_abort;
@@ -94,15 +100,15 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const int stages = p.stages;
   const int chunk = p.chunk;
   const uint32_t a_tile_bytes = static_cast<uint32_t>(p.n_pad) * kBlockBytes;
-  const uint32_t w_stage_bytes = static_cast<uint32_t>(chunk) * kWTileBytes;
+  const uint32_t w_stage_bytes = static_cast<uint32_t>(chunk) * kTmBytes;
   const uint32_t a_stage_bytes = static_cast<uint32_t>(chunk) * a_tile_bytes;
   uint8_t* w_tiles = smem;
   uint8_t* a_tiles = smem + static_cast<size_t>(stages) * w_stage_bytes;
   const size_t main_bytes = static_cast<size_t>(stages) * (w_stage_bytes + a_stage_bytes);
   const int rows_per = (p.M + kCs - 1) / kCs;   // output rows each cluster rank finalises
-  float* recv = reinterpret_cast<float*>(smem + align_up(main_bytes, 1024));   // [kCs][rows_per][128]
+  float* recv = reinterpret_cast<float*>(smem + align_up(main_bytes, 1024));   // [kCs][rows_per][kTm]
   uint8_t* ctrl = reinterpret_cast<uint8_t*>(recv) +
-                  align_up(static_cast<size_t>(kCs) * rows_per * kTileN * sizeof(float), 1024);
+                  align_up(static_cast<size_t>(kCs) * rows_per * kTm * sizeof(float), 1024);
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     if (kCs > 1) {   // every rank sends 128 fp32 columns of each row m = rank (mod kCs), m < M
       const int rk = static_cast<int>(cluster_rank());
       const int owned = rk < p.M ? (p.M - 1 - rk) / kCs + 1 : 0;
-      mbar_arrive_expect_tx(recvd, static_cast<uint32_t>(kCs * owned * kTileN * 4));
+      mbar_arrive_expect_tx(recvd, static_cast<uint32_t>(kCs * owned * kTm * 4));
     }
     if (kMode != 2) tma_prefetch_desc(&tmA);
   }
@@ -175,13 +181,26 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     // in the packed layout) and one 3-D box of chunk activation K blocks
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_a = l2_policy_evict_last();
-    const uint8_t* wsrc = p.wpk + (static_cast<size_t>(nt) * p.nkb_total + kb0) * kWTileBytes;
+    // packed tiles are 128 rows: a 64-row CTA takes half nt % 2 of tile nt / 2, one
+    // 8 KB copy per K block (the halves of consecutive blocks are 16 KB apart)
+    const int tile = kTm == kTileN ? nt : nt / 2;
+    const uint8_t* wsrc = p.wpk + (static_cast<size_t>(tile) * p.nkb_total + kb0) * kWTileBytes +
+                          (kTm == kTileN ? 0 : static_cast<size_t>(nt % 2) * kTmBytes);
+    auto load_w = [&](int slot, int st) {
+      if constexpr (kTm == kTileN) {
+        bulk_load(w_tiles + static_cast<size_t>(slot) * w_stage_bytes, wsrc + static_cast<size_t>(st) * w_stage_bytes,
+                  w_stage_bytes, &full[slot], pol_w);
+      } else {
+        for (int c = 0; c < chunk; ++c)
+          bulk_load(w_tiles + static_cast<size_t>(slot) * w_stage_bytes + c * kTmBytes,
+                    wsrc + static_cast<size_t>(st * chunk + c) * kWTileBytes, kTmBytes, &full[slot], pol_w);
+      }
+    };
     const uint32_t tx = w_stage_bytes + a_stage_bytes;
     const int pre = min(stages, nst);
     for (int i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], tx);
-      bulk_load(w_tiles + static_cast<size_t>(i) * w_stage_bytes, wsrc + static_cast<size_t>(i) * w_stage_bytes,
-                w_stage_bytes, &full[i], pol_w);
+      load_w(i, i);
     }
     pdl_wait();   // activations are written by the previous kernel
     if (tl_on) tt[1] = global_ns();
@@ -197,8 +216,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
         break;
       }
       mbar_arrive_expect_tx(&full[slot], tx);
-      bulk_load(w_tiles + static_cast<size_t>(slot) * w_stage_bytes, wsrc + static_cast<size_t>(st) * w_stage_bytes,
-                w_stage_bytes, &full[slot], pol_w);
+      load_w(slot, st);
       tma_load_3d(a_tiles + static_cast<size_t>(slot) * a_stage_bytes, &tmA, &full[slot], 0, 0, kb0 + st * chunk,
                   pol_a);
       ++issued;
@@ -301,7 +319,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   }
   if (threadIdx.x == 32) {
     // ---------------- MMA issuer
-    const uint32_t idesc = make_idesc(kFp8, kTileN, static_cast<uint32_t>(p.n_pad));
+    const uint32_t idesc = make_idesc(kFp8, kTm, static_cast<uint32_t>(p.n_pad));
     for (int st = 0; st < nst; ++st) {
       const int slot = st % stages;
       const uint32_t use = static_cast<uint32_t>(st / stages);
@@ -312,7 +330,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       }
       tc_fence_after();
       for (int c = 0; c < chunk; ++c) {
-        const uint32_t wa = smem_u32(w_tiles + static_cast<size_t>(slot) * w_stage_bytes + c * kWTileBytes);
+        const uint32_t wa = smem_u32(w_tiles + static_cast<size_t>(slot) * w_stage_bytes + c * kTmBytes);
         const uint32_t aa = smem_u32(a_tiles + static_cast<size_t>(slot) * a_stage_bytes + c * a_tile_bytes);
 #pragma unroll
         for (int k = 0; k < kBlockBytes / 32; ++k)
@@ -341,7 +359,9 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const bool abort = s_abort != 0;
   // warps w and w + 4 share TMEM lane quarter w % 4 and take alternate 16-column chunks
   const int quarter = warp & 3, colset = warp >> 2;
-  const int n_local = quarter * 32 + lane;   // TMEM lane == weight row within the tile
+  // TMEM lane == weight row within the tile (64-row tiles: lanes 0-15 of each quarter)
+  const int n_local = kTm == kTileN ? quarter * 32 + lane : quarter * 16 + (lane & 15);
+  const bool lane_has_row = kTm == kTileN || lane < 16;
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int rank = kCs > 1 ? static_cast<int>(cluster_rank()) : 0;
   const uint32_t recv_base = smem_u32(recv);
@@ -349,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
 #pragma unroll
   for (int q = 0; q < kCs; ++q) {
     peer[q] = (kCs > 1 ? map_dsmem(recv_base, static_cast<uint32_t>(q)) : recv_base) +
-              static_cast<uint32_t>((rank * rows_per * kTileN + n_local) * 4);
+              static_cast<uint32_t>((rank * rows_per * kTm + n_local) * 4);
     peer_bar[q] = kCs > 1 ? map_dsmem(smem_u32(recvd), static_cast<uint32_t>(q)) : 0u;
   }
   if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
@@ -359,9 +379,9 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      if (c + i < p.M) {
+      if (c + i < p.M && lane_has_row) {
         // owner (c + i) % kCs == i % kCs since kCs divides 16; local row (c + i) / kCs
-        const uint32_t addr = peer[i % kCs] + static_cast<uint32_t>(((c + i) / kCs) * kTileN * 4);
+        const uint32_t addr = peer[i % kCs] + static_cast<uint32_t>(((c + i) / kCs) * kTm * 4);
         if (kCs > 1)
           st_async_f32(addr, v[i], peer_bar[i % kCs]);   // counted on the owner's mbarrier
         else
@@ -381,15 +401,17 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   if (tl_on) tt[4] = global_ns();
   if (!abort) {
     const int part = j / kCs;
-    const int c4 = lane * 4;
-    const size_t col = static_cast<size_t>(nt) * kTileN + c4;
-    for (int lr = warp; lr < rows_per; lr += kThreads / 32) {
+    // kTm / 4 lanes per row, four columns each (64-row tiles: two rows per warp)
+    constexpr int kLanesRow = kTm / 4;
+    const int c4 = (lane % kLanesRow) * 4;
+    const size_t col = static_cast<size_t>(nt) * kTm + c4;
+    for (int lr = warp * (32 / kLanesRow) + lane / kLanesRow; lr < rows_per; lr += kThreads / kLanesRow) {
       const int m = lr * kCs + rank;
       if (m >= p.M) break;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < kCs; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kTileN + c4);
+        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kTm + c4);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -405,7 +427,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
           const float u = (e ? acc.w : acc.y) * ds;
           mv[e] = 0.5f * x * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x))) * u;
         }
-        const size_t fidx = static_cast<size_t>(m) * (p.N / 2) + static_cast<size_t>(nt) * 64 + 2 * lane;
+        const size_t fidx = static_cast<size_t>(m) * (p.N / 2) + static_cast<size_t>(nt) * (kTm / 2) + c4 / 2;
         if (p.geglu_fp8) {
           uchar2 c;
           c.x = static_cast<uint8_t>(__nv_cvt_float_to_fp8(mv[0] * rs_geglu, __NV_SATFINITE, __NV_E4M3));
@@ -607,8 +629,9 @@ bool make_tmap_kblocks(CUtensorMap* map, const void* base, int elem_bytes, uint6
   return r == CUDA_SUCCESS;
 }
 
-int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
+int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g, int tile) {
   if (M < 1 || M > 256 || N <= 0 || K <= 0 || N % 128 || K % 128) return FM_ERR_SHAPE;
+  if (tile != kTileN && tile != kTileN / 2) return FM_ERR_SHAPE;
   const int eb = fp8 ? 1 : 2;
   const int nkb_total = K * eb / kBlockBytes;
   if (s < 1 || nkb_total % s) return FM_ERR_SHAPE;
@@ -622,9 +645,11 @@ int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g) {
   g->n_pad = (M + 15) / 16 * 16;
   g->nkb_total = nkb_total;
   g->nkb_cta = nkb_total / s;
-  const size_t block_bytes = kWTileBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;   // one K block
+  g->tile = tile;
+  const size_t block_bytes =
+      static_cast<size_t>(tile) * kBlockBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;   // one K block
   const int rows_per = (M + cs - 1) / cs;
-  const size_t recv_bytes = align_up(static_cast<size_t>(cs) * rows_per * kTileN * sizeof(float), 1024);
+  const size_t recv_bytes = align_up(static_cast<size_t>(cs) * rows_per * tile * sizeof(float), 1024);
   if (recv_bytes + block_bytes > kStageCap) return FM_ERR_SHAPE;
   // chunk: the largest divisor of nkb_cta up to 4 whose double-buffered ring fits (or a
   // single stage holding all of the CTA's K blocks)
@@ -698,11 +723,45 @@ cudaError_t configure_mode() {
   return cudaSuccess;
 }
 
+cudaError_t configure_half_tiles() {
+  const void* ks[8] = {reinterpret_cast<const void*>(skinny_gemm_kernel<true, 1, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 2, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 4, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<true, 8, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 1, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 2, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 4, 0, kTileN / 2>),
+                       reinterpret_cast<const void*>(skinny_gemm_kernel<false, 8, 0, kTileN / 2>)};
+  for (const void* k : ks) {
+    const cudaError_t e = allow_max_dynamic_smem(k);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t gemm_configure_impl() {
   cudaError_t e = configure_mode<0>();
   if (e == cudaSuccess) e = configure_mode<1>();
   if (e == cudaSuccess) e = configure_mode<2>();
+  if (e == cudaSuccess) e = configure_half_tiles();
   return e;
+}
+
+cudaError_t launch_half_tiles(const GemmShape& g, dim3 grid, const LaunchOpts& lo, const CUtensorMap& tmA,
+                              const KParams& p) {
+  const dim3 blk(kThreads);
+  constexpr int kH = kTileN / 2;
+  switch (g.cs * 2 + (g.fp8 ? 1 : 0)) {
+    case 3: return launch(skinny_gemm_kernel<true, 1, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 5: return launch(skinny_gemm_kernel<true, 2, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 9: return launch(skinny_gemm_kernel<true, 4, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 17: return launch(skinny_gemm_kernel<true, 8, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 2: return launch(skinny_gemm_kernel<false, 1, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 4: return launch(skinny_gemm_kernel<false, 2, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 8: return launch(skinny_gemm_kernel<false, 4, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    case 16: return launch(skinny_gemm_kernel<false, 8, 0, kH>, grid, blk, g.smem, lo, tmA, p);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int kMode>
@@ -771,7 +830,11 @@ cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape
   if (mode == 0 && !out && !out_bf16 && !out_geglu && !out_qkv8) return cudaErrorInvalidValue;
   LaunchOpts lo = o;
   lo.cluster = dim3(1, static_cast<unsigned>(g.cs), 1);
-  const dim3 grid(static_cast<unsigned>(g.N / kTileN), static_cast<unsigned>(g.s), 1);
+  const dim3 grid(static_cast<unsigned>(g.N / g.tile), static_cast<unsigned>(g.s), 1);
+  if (g.tile != kTileN) {
+    if (mode != 0) return cudaErrorInvalidValue;
+    return launch_half_tiles(g, grid, lo, tmA, p);
+  }
   switch (mode) {
     case 0: return launch_mode<0>(g, grid, lo, tmA, p);
     case 1: return launch_mode<1>(g, grid, lo, tmA, p);

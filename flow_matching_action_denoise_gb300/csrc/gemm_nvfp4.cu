@@ -18,10 +18,12 @@
 //                 before the programmatic-dependent-launch wait, and one 3-D TMA
 //                 box of the stage's f16 activation K blocks after it;
 //   thread 32   - MMA issuer: 4 x (M=128, N=M_pad, K=16) per 64-element block;
-//   warps 4..7  - decoders: thread r expands weight row r of a block into the
-//                 128-byte-swizzled K-major f16 operand tile;
+//   warps 4..11 - decoders: two threads per weight row, each expanding half of the
+//                 row's 64 elements of a block into the 128-byte-swizzled K-major
+//                 f16 operand tile (eight warps: the expansion, not the tensor pipe,
+//                 bounds these GEMMs);
 //   all warps   - epilogue: TMEM -> fp32 partial planes, or (single K slice,
-//                 gate|up weight) GeGLU + static E4M3 quantisation.
+//                 gate|up weight) GeGLU + static E4M3 (or four-bit) quantisation.
 
 #include <cuda_fp16.h>
 #include <cuda_fp4.h>
@@ -37,7 +39,9 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                                 // 12 warps: roles, 8 decoders, epilogue
+constexpr int kDecoders = kThreads - 128;                     // warps 4-11 expand the weight codes
+constexpr int kDecoderWarps = kDecoders / 32;
 constexpr int kTileN = 128;                                   // weight rows per CTA (MMA M)
 constexpr int kKb = 64;                                       // K elements per pipeline block
 constexpr int kCodeBytes = kTileN * kKb / 2;                  // 4096: two E2M1 codes per byte
@@ -133,10 +137,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     s_act_issued = 0;
     for (int i = 0; i < kMaxRawStages; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], 4);   // one arrival per decoder warp
+      mbar_init(&raw_empty[i], kDecoderWarps);   // one arrival per decoder warp
     }
     for (int i = 0; i < kMaxOpStages; ++i) {
-      mbar_init(&a_full[i], 4);
+      mbar_init(&a_full[i], kDecoderWarps);
       mbar_init(&b_full[i], 1);
       mbar_init(&op_empty[i], 1);
     }
@@ -225,8 +229,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     }
     tc_commit(done);
   } else if (warp >= 4) {
-    // ---------------- decoders: thread row expands weight row `row` of each block
-    const int row = tid - 128;
+    // ---------------- decoders: threads row and row + 128 expand the two halves (chunks
+    // 0-3 and 4-7, elements 0-31 and 32-63) of weight row `row` of each block
+    const int row = (tid - 128) & 127;
+    const int half = (tid - 128) >> 7;
     for (int st = 0; st < nst; ++st) {
       const int r = st % R;
       if (!mbar_wait(&raw_full[r], static_cast<uint32_t>(st / R) & 1u)) {
@@ -234,13 +240,13 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
         s_abort = 1;
         break;
       }
-      uint32_t codes[2][8], sc[2];
-      for (int c = 0; c < C; ++c) {
+      uint32_t codes[2][4], sc[2];   // C <= 2: unrolled, so they stay in registers
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (c >= C) break;
         const uint8_t* src = raw + static_cast<size_t>(r) * raw_stage + c * kRawBytes;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(src + row * 32);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(src + row * 32 + 16);
+        const uint4 c0 = *reinterpret_cast<const uint4*>(src + row * 32 + half * 16);
         codes[c][0] = c0.x; codes[c][1] = c0.y; codes[c][2] = c0.z; codes[c][3] = c0.w;
-        codes[c][4] = c1.x; codes[c][5] = c1.y; codes[c][6] = c1.z; codes[c][7] = c1.w;
         sc[c] = *reinterpret_cast<const uint32_t*>(src + kCodeBytes + row * 4);
       }
       __syncwarp();
@@ -251,12 +257,15 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
         s_abort = 1;
         break;
       }
-      for (int c = 0; c < C; ++c) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (c >= C) break;
         const uint32_t dst = smem_u32(a_tiles + static_cast<size_t>(slot) * a_stage + c * kATileBytes) + row * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {   // 16-byte chunk q = elements 8q..8q+7, block scale q / 2
+        for (int i = 0; i < 4; ++i) {   // 16-byte chunk q = elements 8q..8q+7, block scale q / 2
+          const int q = half * 4 + i;
           const __half bs = e4m3_half(static_cast<uint8_t>((sc[c] >> (8 * (q >> 1))) & 0xffu));
-          st_shared_v4(dst + ((q ^ (row & 7)) << 4), decode8(codes[c][q], __half2(bs, bs)));
+          st_shared_v4(dst + ((q ^ (row & 7)) << 4), decode8(codes[c][i], __half2(bs, bs)));
         }
       }
       fence_async_smem();   // generic-proxy writes -> tensor-core reads
@@ -265,8 +274,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     }
   }
 
-  // ---------------- epilogue: warps w and w + 4 share TMEM lane quarter w % 4 and
-  // take alternate 16-column chunks (activation rows)
+  // ---------------- epilogue: warps w, w + 4 and w + 8 share TMEM lane quarter w % 4 and
+  // take every third 16-column chunk (activation rows)
   pdl_wait();   // the output buffers may still be read by earlier kernels until then
   if (!mbar_wait(done, 0)) {
     atomicOr(p.err, kErrPipelineTimeout);
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int n_local = quarter * 32 + lane;   // TMEM lane == weight row == output column in the tile
   __syncwarp();
-  for (int c = colset * 16; c < p.n_pad; c += 32) {
+  for (int c = colset * 16; c < p.n_pad; c += 16 * (kThreads / 128)) {
     float v[16];
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
     if (abort) continue;

@@ -88,10 +88,11 @@ struct GemmShape {
   int nkb_cta;    // K blocks per CTA
   int chunk;      // K blocks per pipeline stage (one weight copy + one activation box)
   int stages;     // pipeline stages in shared memory
+  int tile;       // weight rows per CTA (MMA M): 128, or 64 (plain placement only)
   size_t smem;    // dynamic shared memory bytes
 };
 // Fills the derived fields; returns FM_OK or FM_ERR_SHAPE.
-int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g);
+int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g, int tile = 128);
 // Activation tensor map: A [M][K] in K blocks of 128 bytes, box = chunk blocks x n_pad rows.
 bool gemm_tmap_act(CUtensorMap* map, const void* a, const GemmShape& g);
 // out: fp32 partial planes [s/cs][M][N]; or, with out_bf16 (requires cs == s), the

@@ -253,6 +253,17 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
       dv->rowfuse = 1;
     }
   }
+  // The gate|up GEMM (N = 2F, the largest) in 64-row weight tiles when the doubled grid
+  // still fits in one wave at two CTAs per SM: half the split-K partial bytes per CTA
+  // (measured: expert_fp8_m50 5.74 -> 5.71 ms; with bf16 operands the CTAs need more
+  // than half an SM's shared memory and it is not taken).
+  if (!dv->rowfuse) {   // (the consumers-inside-GEMMs placement keeps 128-row tiles)
+    fm::GemmShape g64;
+    const fm::GemmShape& g2 = dv->gs[2];
+    if (fm::gemm_plan(c->M, N[2], K[2], dv->fp8, g2.s, g2.cs, &g64, 64) == FM_OK && g64.smem <= 113 * 1024 &&
+        (N[2] / 64) * g2.s <= 2 * num_sms())
+      dv->gs[2] = g64;
+  }
   return FM_OK;
 }
 
@@ -1570,15 +1581,24 @@ int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt, vo
   return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "pack_weight");
 }
 
+int fm_test_skinny_gemm_tile(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s,
+                             int cluster_reduce, int tile_rows, float* partials, void* stream);
+
 int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s, int cluster_reduce,
                         float* partials, void* stream) {
+  return fm_test_skinny_gemm_tile(a, M, K, w_packed, N, fmt, s, cluster_reduce, 128, partials, stream);
+}
+
+int fm_test_skinny_gemm_tile(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s,
+                             int cluster_reduce, int tile_rows, float* partials, void* stream) {
   if (!a || !w_packed || !partials) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
   if (fmt != FM_FMT_FP8 && fmt != FM_FMT_BF16 && fmt != FM_FMT_NVFP4)
     return fail(nullptr, FM_ERR_UNSUPPORTED, "format");
   if (!aligned16(a) || reinterpret_cast<uintptr_t>(w_packed) % kAlign)
     return fail(nullptr, FM_ERR_ALIGN, "a must be 16-byte and w_packed 1024-byte aligned");
   if (fmt == FM_FMT_NVFP4) {
-    if (cluster_reduce != 1) return fail(nullptr, FM_ERR_SHAPE, "NVFP4 GEMM writes every slice: cluster_reduce 1");
+    if (cluster_reduce != 1 || tile_rows != 128)
+      return fail(nullptr, FM_ERR_SHAPE, "NVFP4 GEMM writes every slice of 128-row tiles: cluster_reduce 1, tile 128");
     fm::Nvfp4Shape g;
     if (fm::nvfp4_plan(M, N, K, s, &g) != FM_OK)
       return fail(nullptr, FM_ERR_SHAPE, "GEMM shape/split precondition violated");
@@ -1595,7 +1615,7 @@ int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N
     return e == cudaSuccess ? FM_OK : cuda_fail(nullptr, e, "nvfp4 gemm launch");
   }
   fm::GemmShape g;
-  const int st = fm::gemm_plan(M, N, K, fmt == FM_FMT_FP8, s, cluster_reduce, &g);
+  const int st = fm::gemm_plan(M, N, K, fmt == FM_FMT_FP8, s, cluster_reduce, &g, tile_rows);
   if (st != FM_OK) return fail(nullptr, st, "GEMM shape/split precondition violated");
   CUtensorMap ta;
   if (!fm::gemm_tmap_act(&ta, a, g))

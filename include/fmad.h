@@ -446,6 +446,12 @@ int fm_pack_weight(const float* w, const float* gamma, int N, int K, int fmt,
 int fm_test_skinny_gemm(const void* a, int M, int K, const void* w_packed, int N, int fmt,
                         int s, int cluster_reduce, float* partials, void* stream);
 
+/* fm_test_skinny_gemm with the weight rows per CTA (the MMA's M) chosen: tile_rows 128,
+ * or 64 (each CTA takes one half of a packed 128-row tile; FP8 and BF16 only). The
+ * partials are the same sums. */
+int fm_test_skinny_gemm_tile(const void* a, int M, int K, const void* w_packed, int N, int fmt, int s,
+                             int cluster_reduce, int tile_rows, float* partials, void* stream);
+
 /* Bytes of scratch fm_gemm_consumer needs for its fp32 split-K partial planes. */
 int fm_gemm_consumer_scratch_bytes(int M, int N, int K, int fmt, int s, size_t* bytes);
 

@@ -85,8 +85,9 @@ def test_pack_bf16_bit_exact(device):
 
 # ---------------------------------------------------------------- skinny GEMM
 
-def run_gemm(device, a_bytes_or_bf16, M, K, packed_host, N, fmt, s, cs):
-    """a: host uint8 [M][K] codes (fp8) or uint16 bf16 bits; packed_host: tiled bytes/bits."""
+def run_gemm(device, a_bytes_or_bf16, M, K, packed_host, N, fmt, s, cs, tile=128):
+    """a: host uint8 [M][K] codes (fp8) or uint16 bf16 bits; packed_host: tiled bytes/bits;
+    tile: weight rows per CTA (128, or 64: half of a packed tile)."""
     a = dev(a_bytes_or_bf16, device)
     raw = np.ascontiguousarray(packed_host).view(np.uint8).reshape(-1)
     buf, ptr = aligned_empty(raw.size, device)
@@ -94,17 +95,22 @@ def run_gemm(device, a_bytes_or_bf16, M, K, packed_host, N, fmt, s, cs):
     buf[off:off + raw.size].copy_(torch.from_numpy(raw).to(device))
     nparts = s // cs
     out = torch.full((nparts, M, N), float("nan"), dtype=torch.float32, device=device)
-    fmad.fm_test_skinny_gemm(a, M, K, ptr, N, fmt, s, cs, out)
+    if tile == 128:
+        fmad.fm_test_skinny_gemm(a, M, K, ptr, N, fmt, s, cs, out)
+    else:
+        fmad.fm_test_skinny_gemm_tile(a, M, K, ptr, N, fmt, s, cs, tile, out)
     torch.cuda.synchronize()
     assert fmad.standalone_status() == 0, "a GEMM pipeline wait expired"
     return out.cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("tile", [128, 64])
 @pytest.mark.parametrize("M,K,N", [(1, 1024, 1024), (10, 1024, 1280), (50, 4096, 1024), (63, 2048, 4096),
                                    (256, 1024, 1024)])
-def test_skinny_gemm_integer_split_invariance_bit_exact(device, M, K, N):
+def test_skinny_gemm_integer_split_invariance_bit_exact(device, M, K, N, tile):
     """Integer A, W in [-3, 3] (exact E4M3 codes, scale 1): every partial and every fp32
-    sum is exact, so each K-split and cluster size must give the exact product."""
+    sum is exact, so each K-split and cluster size must give the exact product, with
+    128-row tiles and with 64-row tiles (each CTA half of a packed tile)."""
     case = fm_synth.gemm_case(M, K, N, integer=True)
     a, w = case["a"].astype(np.float64), case["w"].astype(np.float64)
     a_codes = C.e4m3_encode_code(a)
@@ -117,7 +123,7 @@ def test_skinny_gemm_integer_split_invariance_bit_exact(device, M, K, N):
         for cs in [1, 2, 4, 8]:
             if s % cs:
                 continue
-            parts = run_gemm(device, a_codes, M, K, packed, N, fmad.FMT_FP8, s, cs)
+            parts = run_gemm(device, a_codes, M, K, packed, N, fmad.FMT_FP8, s, cs, tile)
             ref = O.gemm_ksplit(a, O.PreparedWeight(w, 1.0, "fp8"), s)
             ref = ref.reshape(s // cs, cs, M, N).sum(axis=1)
             np.testing.assert_array_equal(parts, ref, err_msg=f"s={s} cs={cs}")
@@ -139,14 +145,15 @@ def test_skinny_gemm_fp8_random_vs_oracle(device, M, K, N, s, cs):
     assert np.max(np.abs(got - ref)) <= 1e-5 * rms
 
 
+@pytest.mark.parametrize("tile", [128, 64])
 @pytest.mark.parametrize("M,K,N,s,cs", [(63, 1024, 1280, 4, 4), (10, 4096, 1024, 8, 8), (16, 1024, 2048, 1, 1)])
-def test_skinny_gemm_bf16_vs_oracle(device, M, K, N, s, cs):
+def test_skinny_gemm_bf16_vs_oracle(device, M, K, N, s, cs, tile):
     case = fm_synth.gemm_case(M, K, N, seed=11)
     a = C.bf16(case["a"])
     pw = O.prep_weight(case["w"], None, "bf16")
     a_bits = torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).view(torch.uint16).numpy()
     w_bits = torch.from_numpy(pw.codes.astype(np.float32)).to(torch.bfloat16).view(torch.uint16).numpy()
-    parts = run_gemm(device, a_bits, M, K, tile_codes(w_bits, 64), N, fmad.FMT_BF16, s, cs)
+    parts = run_gemm(device, a_bits, M, K, tile_codes(w_bits, 64), N, fmad.FMT_BF16, s, cs, tile)
     ref = a @ pw.codes.T
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.max(np.abs(parts.sum(axis=0) - ref)) <= 1e-5 * rms
