@@ -155,6 +155,9 @@ def run_ours(args, rank, world, local_rank):
             variants["graph_pdl_fused_consumers"] = fmad.Policy(
                 cfg, act_scales=scales, weights=weights, device=device,
                 flags=fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | fmad.FLAG_FUSED_CONSUMERS)
+            variants["graph_pdl_o_consumer_in_gemm"] = fmad.Policy(
+                cfg, act_scales=scales, weights=weights, device=device,
+                flags=fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | fmad.FLAG_O_CONSUMER_IN_GEMM)
     del weights
     kp, vp = fm_synth.prefix_kv(cfg)
     k_dev = torch.from_numpy(kp).to(device, torch.bfloat16)
@@ -380,7 +383,7 @@ def time_graph(device, launches, replays=5):
     return us
 
 
-def time_decision_gemm(cfg, scales, device, index=4):
+def time_decision_gemm(cfg, scales, device, index=None):
     """The gate|up GEMM exactly as the decision launches it (GeGLU + E4M3 epilogue,
     the decision's split and cluster; kernel `index` of a layer-step), launched back to
     back through fm_test_launch_kernel over the layers of a policy whose packed weights
@@ -403,6 +406,8 @@ def time_decision_gemm(cfg, scales, device, index=4):
     noise = torch.from_numpy(fm_synth.noise(rcfg, 0)).to(device)
     pol.decode(noise)   # fills every buffer the kernel reads
     torch.cuda.synchronize(device)
+    if index is None:   # the gate|up GEMM's position in a layer-step: after the O GEMM's consumer
+        index = 4 if fmad.kernel_count(pol.handle)[0] == 7 else 3
     launches = [lambda st, l=l: fmad.launch_kernel(pol.handle, l, 0, index, st) for l in range(R)] * 2
     us = time_graph(device, launches)
     if fmad.device_status(pol.handle):

@@ -20,7 +20,8 @@ __all__ = [
     "kernel_count", "philox_noise", "decode_actions_seeded", "last_timing", "decode_warm", "episode_reset", "Session",
     "session_workspace_size", "session_create", "session_fork", "FmTiming", "fm_test_quant_e4m3", "fm_packed_weight_bytes", "fm_pack_weight",
     "fm_test_skinny_gemm", "fm_test_consumer", "fm_test_layer", "named_buffer", "Policy", "DeviceWeights",
-    "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "FLAG_FUSED_CONSUMERS", "COND_TIME", "COND_GIVEN",
+    "FMT_BF16", "FMT_FP8", "FMT_NVFP4", "FLAG_USE_GRAPH", "FLAG_USE_PDL", "FLAG_FUSED_CONSUMERS",
+    "FLAG_O_CONSUMER_IN_GEMM", "COND_TIME", "COND_GIVEN",
     "ABI_VERSION", "STATUS",
 ]
 
@@ -29,7 +30,7 @@ LIB_PATH = os.path.join(PKG, "libfmad.so")
 
 ABI_VERSION = 3
 FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
-FLAG_USE_GRAPH, FLAG_USE_PDL, FLAG_FUSED_CONSUMERS = 1, 2, 4
+FLAG_USE_GRAPH, FLAG_USE_PDL, FLAG_FUSED_CONSUMERS, FLAG_O_CONSUMER_IN_GEMM = 1, 2, 4, 8
 COND_TIME, COND_GIVEN = 0, 1
 STATUS = {0: "FM_OK", 1: "FM_ERR_INVALID_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_ALIGN",
           4: "FM_ERR_WORKSPACE", 5: "FM_ERR_CUDA", 6: "FM_ERR_STATE_MISMATCH",

@@ -129,6 +129,25 @@ cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape
                         int nq = 0, int nk = 0, const GemmFuse* fuse = nullptr);
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
+// ---------------------------------------------------------------- O GEMM + consumer
+// The O projection with its consumer in the epilogue (ofuse.cu): one cluster spans the
+// N / 128 <= 8 column tiles, each CTA the whole K of its 128 weight rows (E4M3 operands).
+struct OConsumerShape {
+  int M, N, K;
+  int n_pad;   // MMA N (M rounded up to 16, <= 64)
+  int nkb;     // 128-byte K blocks (all resident)
+  int chunk;   // K blocks per TMA transaction
+  size_t smem;
+};
+int o_consumer_plan(int M, int N, int K, OConsumerShape* g);
+// Activation tensor map: A [M][K] E4M3 in K blocks, box = chunk blocks x n_pad rows.
+bool o_consumer_tmap(CUtensorMap* map, const void* a, const OConsumerShape& g);
+cudaError_t o_consumer_configure();
+// x <- x + gate * (A W^T) * fp32(sa * sw); q = E4M3(AdaRMSNorm(x; scale, shift) * (1 / sq))
+cudaError_t o_consumer_launch(const CUtensorMap& tmA, const void* wpk, const OConsumerShape& g, const float* sa,
+                              const float* sw, const float* gate, float* x, const float* scale, const float* shift,
+                              const float* sq, float eps, uint8_t* q, int* err, const LaunchOpts& o);
+
 // ---------------------------------------------------------------- NVFP4-weight GEMM
 struct Nvfp4Shape {
   int M, N, K;

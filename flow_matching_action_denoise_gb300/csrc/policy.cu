@@ -81,13 +81,19 @@ struct Derived {
   // the gated residual and emit per-tile sums of squares, the QKV and gate|up GEMMs
   // build their normalised, quantised operand in a prologue (5 kernels per layer)
   int rowfuse;
+  // FM_FLAG_O_CONSUMER_IN_GEMM (FP8, d <= 1024, H * Dh <= 1024, M <= 64): the O GEMM and
+  // its consumer in one kernel (ofuse.cu), 6 kernels per layer
+  int ofuse;
+  fm::OConsumerShape os;
   fm::GemmShape gs[4];
   fm::Nvfp4Shape ns[4];
   int gN[4], gK[4];
   int attn_kc, attn_nsplit;
   // fp32 partial planes GEMM g writes (its K-slices not reduced in the GEMM itself)
-  int nparts(int g) const { return nvfp4 ? ns[g].s : (rowfuse && (g == 1 || g == 3)) ? 0 : gs[g].s / gs[g].cs; }
-  int kernels_per_layer() const { return nvfp4 ? 8 : rowfuse ? 5 : 7; }
+  int nparts(int g) const {
+    return nvfp4 ? ns[g].s : ((rowfuse && (g == 1 || g == 3)) || (ofuse && g == 1)) ? 0 : gs[g].s / gs[g].cs;
+  }
+  int kernels_per_layer() const { return nvfp4 ? 8 : rowfuse ? 5 : ofuse ? 6 : 7; }
 };
 
 int num_sms() {
@@ -168,6 +174,7 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
   dv->q_store = dv->nvfp4 ? (dv->act4 ? fm::kQNvfp4AsF16 : fm::kQFp8AsF16) : dv->fp8;
   dv->attn_fp8 = c->attn_fmt == FM_FMT_FP8;
   dv->rowfuse = 0;
+  dv->ofuse = 0;
   dv->act_bytes = dv->q_store == 1 ? 1 : 2;
   const int N[4] = {dv->nqkv, c->d, 2 * c->F, c->d};
   const int K[4] = {c->d, c->H * c->Dh, c->d, c->F};
@@ -257,6 +264,9 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
   // still fits in one wave at two CTAs per SM: half the split-K partial bytes per CTA
   // (measured: expert_fp8_m50 5.74 -> 5.71 ms; with bf16 operands the CTAs need more
   // than half an SM's shared memory and it is not taken).
+  if (!dv->rowfuse && dv->fp8 && (c->flags & FM_FLAG_O_CONSUMER_IN_GEMM) &&
+      fm::o_consumer_plan(c->M, N[1], K[1], &dv->os) == FM_OK)
+    dv->ofuse = 1;
   if (!dv->rowfuse) {   // (the consumers-inside-GEMMs placement keeps 128-row tiles)
     fm::GemmShape g64;
     const fm::GemmShape& g2 = dv->gs[2];
@@ -351,6 +361,7 @@ struct fm_policy {
   fm_policy* base = nullptr;   // a session's base policy (shares its weights)
   int sessions = 0;            // live sessions of this base policy
   CUtensorMap tmA[4];
+  CUtensorMap tmO;   // the attention output as the fused O GEMM + consumer reads it
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -532,6 +543,11 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   if (dv.nvfp4)
     e = fm::nvfp4_gemm_launch(p->tmA[1], p->at<void>(p->ly.wpk[l * 4 + 1]), dv.ns[1], y[1], nullptr, nullptr, nullptr,
                               nullptr, err, o);
+  else if (dv.ofuse)   // the O GEMM with its consumer: x and the pre-MLP operand q2 (no row kernel)
+    e = fm::o_consumer_launch(p->tmO, p->at<void>(p->ly.wpk[l * 4 + 1]), dv.os, p->ascale(l, FM_SITE_ATTN_OUT),
+                              p->wscale(l, 1), p->mod(k, l, 2), p->at<float>(p->ly.x), p->mod(k, l, 3),
+                              p->mod(k, l, 4), p->ascale(l, FM_SITE_MLP_IN), c.rms_eps, p->at<uint8_t>(p->ly.q2), err,
+                              o);
   else if (dv.rowfuse)
     e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 1]), p->tmA[1], dv.gs[1], nullptr, err, o, nullptr,
                         p->ascale(l, FM_SITE_ATTN_OUT), p->wscale(l, 1), nullptr, 0, nullptr, nullptr, nullptr, 0, 0,
@@ -557,7 +573,7 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   r1.q = p->at<void>(p->ly.q2);
   r1.q_fp8 = fp8;
   r1.eps = c.rms_eps;
-  if (!dv.rowfuse) {
+  if (!dv.rowfuse && !dv.ofuse) {
     e = fm::row_launch(r1, o);
     if (e != cudaSuccess) return e;
   }
@@ -771,6 +787,7 @@ bool build_tmaps(fm_policy* p) {
                                 : fm::gemm_tmap_act(&p->tmA[g], p->at<void>(act_off[g]), p->dv.gs[g]);
     if (!ok) return false;
   }
+  if (p->dv.ofuse && !fm::o_consumer_tmap(&p->tmO, p->at<void>(p->ly.o), p->dv.os)) return false;
   return true;
 }
 
@@ -978,7 +995,7 @@ int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_sc
   };
 
   if (!cu(fm::gemm_configure(), "gemm_configure") || !cu(fm::nvfp4_configure(), "nvfp4_configure") ||
-      !cu(fm::attn_configure(), "attn_configure"))
+      !cu(fm::attn_configure(), "attn_configure") || !cu(fm::o_consumer_configure(), "o_consumer_configure"))
     return bail(FM_ERR_CUDA, why);
 
   // weights: fold gamma, quantise, tile

@@ -79,7 +79,15 @@ enum {
    * allow it (the O and down GEMMs reduce every K slice in one cluster of <= 8, the QKV
    * and gate|up GEMMs hold their K range in one stage); otherwise, and for NVFP4, the
    * flag is ignored: fm_test_kernel_count reports the placement in use. */
-  FM_FLAG_FUSED_CONSUMERS = 4u
+  FM_FLAG_FUSED_CONSUMERS = 4u,
+  /* FP8 weights and activations, d <= 1024, H * Dh <= 1024, M <= 64: run the O projection
+   * and its consumer (gated residual + pre-MLP AdaRMSNorm + quantise) as one kernel whose
+   * thread-block cluster spans every column tile, each CTA over the whole K, so each row's
+   * norm is finished inside it (6 kernels per layer). Off by default: eight CTAs carry the
+   * whole projection and the cluster's row statistics, which at M = 50 takes longer than
+   * the row kernel and hand-off it removes (expert_fp8_m50: 6.26 ms against 5.80 ms).
+   * Ignored where the shapes do not allow it; fm_test_kernel_count reports the placement. */
+  FM_FLAG_O_CONSUMER_IN_GEMM = 8u
 };
 
 enum {

@@ -35,8 +35,11 @@ def device():
 
 # ---------------------------------------------------------------- single layer (M = 10)
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_single_layer_vs_oracle(device, fused):
+PLACEMENTS = {"separate": 0, "fused": fmad.FLAG_FUSED_CONSUMERS, "o_fused": fmad.FLAG_O_CONSUMER_IN_GEMM}
+
+
+@pytest.mark.parametrize("placement", list(PLACEMENTS))
+def test_single_layer_vs_oracle(device, placement):
     cfg = fm_synth.config("layer_fp8_m10")
     layers = [fm_synth.layer_weights(cfg, 0)]
     final = fm_synth.final_weights(cfg)
@@ -47,7 +50,7 @@ def test_single_layer_vs_oracle(device, fused):
     model = O.Model(cfg, layers, final, conds)
     x_ref, q_ref, _ = O.single_layer(model, x, kp, vp, scales)
 
-    flags = fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | (fmad.FLAG_FUSED_CONSUMERS if fused else 0)
+    flags = fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | PLACEMENTS[placement]
     pol = fmad.Policy(cfg, layers, final, act_scales=scales, conds=conds, flags=flags)
     pol.set_prefix_kv(dev(kp, device, torch.bfloat16), dev(vp, device, torch.bfloat16))
     xin = dev(x, device)
@@ -62,7 +65,8 @@ def test_single_layer_vs_oracle(device, fused):
     dist = code_step_distance(q.cpu().numpy(), C.e4m3_encode_code(q_ref))
     assert np.max(dist) <= 1 and np.mean(dist > 0) <= 1e-2
     per_layer, per_decision = fmad.kernel_count(pol.handle)
-    assert (per_layer, per_decision) == ((5, 1 + 5 + 1) if fused else (7, 1 + 7))
+    assert (per_layer, per_decision) == {"o_fused": (6, 1 + 6), "fused": (5, 1 + 5 + 1),
+                                         "separate": (7, 1 + 7)}[placement]
     pol.close()
 
 
@@ -111,9 +115,11 @@ def test_decision_fp8_end_to_end_within_oracle_envelope(expert):
     ref = O.decode(expert.oracle(), nz, expert.kp, expert.vp, expert.scales)
     env = float(np.loadtxt(os.path.join(GOLDEN, "fp8_envelope_expert_fp8_m50.txt")))
     base = fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL
-    # consumers as their own kernels (default) and inside the GEMMs (5 kernels per layer
+    # every consumer as its own kernel (default, 7 kernels per layer), the O GEMM's
+    # consumer in its epilogue (6), and the consumers inside the GEMMs (5 kernels per layer
     # plus one step-boundary kernel per step)
-    for flags, counts in [(base, (7, 1 + 18 * 10 * 7)), (base | fmad.FLAG_FUSED_CONSUMERS, (5, 1 + 18 * 10 * 5 + 10))]:
+    for flags, counts in [(base, (7, 1 + 18 * 10 * 7)), (base | fmad.FLAG_O_CONSUMER_IN_GEMM, (6, 1 + 18 * 10 * 6)),
+                          (base | fmad.FLAG_FUSED_CONSUMERS, (5, 1 + 18 * 10 * 5 + 10))]:
         pol = expert.policy(flags)
         act = pol.decode(dev(nz, expert.device))
         torch.cuda.synchronize()
@@ -125,14 +131,14 @@ def test_decision_fp8_end_to_end_within_oracle_envelope(expert):
         pol.close()
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_decision_fp8_every_stage_vs_oracle(expert, fused):
+@pytest.mark.parametrize("placement", list(PLACEMENTS))
+def test_decision_fp8_every_stage_vs_oracle(expert, placement):
     """Teacher-forced parity of every kernel of all 180 layer-steps: each recorded
     output equals the oracle's stage applied to the GPU's own recorded input -
     fp32 outputs within 1e-5 * RMS, quantised codes within one E4M3 step with at
     most 0.1% near-tie differences."""
     cfg, model = expert.cfg, expert.oracle()
-    pol = expert.policy(fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | (fmad.FLAG_FUSED_CONSUMERS if fused else 0))
+    pol = expert.policy(fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL | PLACEMENTS[placement])
     nbytes = fmad.trace_size(pol.handle)
     trace = torch.empty(nbytes, dtype=torch.uint8, device=expert.device)
     nz = fm_synth.noise(cfg, 0)
