@@ -344,10 +344,10 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
 
   // ---------------- epilogue. Output row m belongs to cluster rank m mod cs, as its
   // local row m / cs. Each CTA pushes its fp32 partial of every row into the
-  // owner's receive buffer (slot = its own rank) with remote shared-memory
-  // stores; after one cluster barrier each owner sums its rows over the cs slots
-  // in slice order and writes them with 16-byte stores. With cs == 1 the push is
-  // a local shared-memory store.
+  // owner's receive buffer (slot = its own rank) with 16-byte remote shared-memory
+  // stores counted on the owner's mbarrier; each owner then sums its rows over the
+  // cs slots in slice order and writes them with 16-byte stores. With cs == 1 the
+  // push is a local shared-memory store.
   pdl_wait();
   if (!mbar_wait(done, 0)) {
     atomicOr(p.err, kErrPipelineTimeout);
@@ -365,27 +365,38 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const int rank = kCs > 1 ? static_cast<int>(cluster_rank()) : 0;
   const uint32_t recv_base = smem_u32(recv);
-  uint32_t peer[kCs], peer_bar[kCs];
-#pragma unroll
-  for (int q = 0; q < kCs; ++q) {
-    peer[q] = (kCs > 1 ? map_dsmem(recv_base, static_cast<uint32_t>(q)) : recv_base) +
-              static_cast<uint32_t>((rank * rows_per * kTm + n_local) * 4);
-    peer_bar[q] = kCs > 1 ? map_dsmem(smem_u32(recvd), static_cast<uint32_t>(q)) : 0u;
-  }
   if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
-  __syncwarp();                  // tcgen05.ld is warp-collective
+  __syncwarp();                  // tcgen05.ld and the shuffles are warp-collective
+  // Partial rows leave as 16-byte stores: each aligned group of four lanes (four
+  // consecutive weight rows n0..n0+3) transposes its 4 x 4 blocks, after which lane t4
+  // holds columns n0..n0+3 of activation row c + 4b + t4. That row's owner,
+  // (4b + t4) mod cs (c is a multiple of 16 and cs divides 16), is fixed per lane and b.
+  // (One remote store per warp costs about the same whatever its width, so four
+  // columns per lane take a quarter of the scalar stores' time.)
+  const int t4 = lane & 3;
+  const int n0 = n_local - t4;
+  uint32_t dst_b[4], bar_b[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t q = static_cast<uint32_t>((4 * b + t4) % kCs);
+    dst_b[b] = (kCs > 1 ? map_dsmem(recv_base, q) : recv_base) +
+               static_cast<uint32_t>((rank * rows_per * kTm + n0) * 4);
+    bar_b[b] = kCs > 1 ? map_dsmem(smem_u32(recvd), q) : 0u;
+  }
   for (int c = colset * 16; c < p.n_pad; c += 32) {
     float v[16];
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (c + i < p.M && lane_has_row) {
-        // owner (c + i) % kCs == i % kCs since kCs divides 16; local row (c + i) / kCs
-        const uint32_t addr = peer[i % kCs] + static_cast<uint32_t>(((c + i) / kCs) * kTm * 4);
-        if (kCs > 1)
-          st_async_f32(addr, v[i], peer_bar[i % kCs]);   // counted on the owner's mbarrier
+    for (int b = 0; b < 4; ++b) {
+      transpose4x4(v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3], t4);
+      const int r = c + 4 * b + t4;   // activation row; the owner's local row is r / cs
+      if (r < p.M && lane_has_row) {
+        const uint32_t addr = dst_b[b] + static_cast<uint32_t>((r / kCs) * kTm * 4);
+        if (kCs > 1)   // counted on the owner's mbarrier
+          st_async_v4(addr, v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3], bar_b[b]);
         else
-          asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v[i]) : "memory");
+          st_shared_v4(addr, make_uint4(__float_as_uint(v[4 * b]), __float_as_uint(v[4 * b + 1]),
+                                        __float_as_uint(v[4 * b + 2]), __float_as_uint(v[4 * b + 3])));
       }
     }
   }

@@ -253,6 +253,42 @@ __device__ __forceinline__ void st_async_f32(uint32_t dst, float a, uint32_t mba
                "r"(mbar)
                : "memory");
 }
+// Asynchronous 16-byte store into a CTA of the cluster, counted on that CTA's mbarrier
+// (shared::cluster addresses; dst 16-byte aligned).
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(dst), "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar)
+               : "memory");
+}
+// Transpose of a 4 x 4 block held by the four lanes of an aligned lane group: lane t
+// holds row t on entry and column t on exit. Two butterfly exchanges: the off-diagonal
+// 2 x 2 blocks swap between lanes t and t ^ 2, then each 2 x 2 block transposes between
+// lanes t and t ^ 1. Every lane of the warp must execute it.
+__device__ __forceinline__ void transpose4x4(float& x0, float& x1, float& x2, float& x3, int t) {
+  const bool hi = (t & 2) != 0;
+  float a = hi ? x0 : x2, b = hi ? x1 : x3;
+  a = __shfl_xor_sync(0xffffffffu, a, 2);
+  b = __shfl_xor_sync(0xffffffffu, b, 2);
+  if (hi) {
+    x0 = a;
+    x1 = b;
+  } else {
+    x2 = a;
+    x3 = b;
+  }
+  const bool odd = (t & 1) != 0;
+  a = odd ? x0 : x1;
+  b = odd ? x2 : x3;
+  a = __shfl_xor_sync(0xffffffffu, a, 1);
+  b = __shfl_xor_sync(0xffffffffu, b, 1);
+  if (odd) {
+    x0 = a;
+    x2 = b;
+  } else {
+    x1 = a;
+    x3 = b;
+  }
+}
 // Asynchronous 8-byte store into a CTA of the cluster, counted on that CTA's mbarrier
 // (shared::cluster addresses).
 __device__ __forceinline__ void st_async_v2(uint32_t dst, float a, float b, uint32_t mbar) {

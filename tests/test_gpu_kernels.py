@@ -106,11 +106,12 @@ def run_gemm(device, a_bytes_or_bf16, M, K, packed_host, N, fmt, s, cs, tile=128
 
 @pytest.mark.parametrize("tile", [128, 64])
 @pytest.mark.parametrize("M,K,N", [(1, 1024, 1024), (10, 1024, 1280), (50, 4096, 1024), (63, 2048, 4096),
-                                   (256, 1024, 1024)])
+                                   (100, 1024, 1024), (256, 1024, 1024)])
 def test_skinny_gemm_integer_split_invariance_bit_exact(device, M, K, N, tile):
     """Integer A, W in [-3, 3] (exact E4M3 codes, scale 1): every partial and every fp32
     sum is exact, so each K-split and cluster size must give the exact product, with
-    128-row tiles and with 64-row tiles (each CTA half of a packed tile)."""
+    128-row tiles and with 64-row tiles (each CTA half of a packed tile), for MMA N
+    (the activation rows rounded up to 16) from 16 to 256."""
     case = fm_synth.gemm_case(M, K, N, integer=True)
     a, w = case["a"].astype(np.float64), case["w"].astype(np.float64)
     a_codes = C.e4m3_encode_code(a)
