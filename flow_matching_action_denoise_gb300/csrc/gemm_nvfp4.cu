@@ -10,7 +10,7 @@
 // fp32 accumulation: the only rounding is the fp32 accumulation itself, and ts
 // joins the activation scale in the consumer's dequantisation fp32(s_a * ts).
 //
-// Work split (one CTA per 128 weight rows x one K slice, 8 warps). A pipeline stage
+// Work split (one CTA per 128 weight rows x one K slice, 12 warps). A pipeline stage
 // covers `chunk` 64-element K blocks (one transaction each way: TMA transactions
 // and barrier round trips, not bytes, bound the per-SM streaming rate here):
 //   thread 0    - producer: one bulk copy of the stage's packed weight blocks
