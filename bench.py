@@ -842,6 +842,39 @@ def run_layer_protocol(args):
             "steps": args.steps, "clocks": clocks.summary()}
 
 
+def run_handoff_protocol(args):
+    """What a stage boundary costs by itself: (a) a CUDA graph of dependent empty kernels
+    (programmatic dependent launch, as the decision launches its kernels, and plain
+    stream order), microseconds per kernel; (b) grid-wide barriers inside one cooperative
+    launch (release/acquire at gpu scope, and fences around relaxed atomics), the median
+    over CTAs of nanoseconds per round. Both at 1 CTA, at the decision's typical grid
+    sizes and at one and two CTAs per SM."""
+    import torch
+    import flow_matching_action_denoise_gb300 as fmad
+    device = torch.device("cuda", 0)
+    fmad.load()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    scratch = torch.zeros(4, dtype=torch.int32, device=device)
+    grids = [1, 64, sms, 2 * sms]
+    chain, barrier = [], []
+    with ClockSampler(0) as clocks:
+        for ctas in grids:
+            for pdl in (True, False):
+                us = fmad.pdl_chain(ctas, 256, 1000, 10, pdl, scratch)
+                chain.append({"ctas": ctas, "threads": 256, "pdl": pdl, "us_per_kernel": round(us, 3)})
+        for ctas in grids:
+            for mode, name in ((0, "release/acquire"), (1, "fences + relaxed atomics")):
+                out = torch.zeros(2 * ctas, dtype=torch.int64, device=device)
+                rounds = 2000
+                if fmad.grid_barrier(ctas, 256, rounds, mode, 10 ** 9, scratch, out) != 0:
+                    raise RuntimeError("grid barrier wait ran out")
+                o = out.cpu().numpy().reshape(ctas, 2)
+                barrier.append({"ctas": ctas, "threads": 256, "ordering": name,
+                                "ns_per_round": round(float(np.median(o[:, 0] / o[:, 1])), 1)})
+    return {"protocol": "stage hand-off cost", "kernels_per_graph": 1000, "barrier_rounds": 2000,
+            "pdl_chain": chain, "grid_barrier": barrier, "clocks": clocks.summary()}
+
+
 def run_timeline(args):
     """Where a decision's time goes: one decision replayed as the same CUDA graph with a
     per-CTA timeline (fm_decode_timeline), summarised per kernel position in a
@@ -998,6 +1031,8 @@ def main():
                     help="run only the single-layer protocol (M = 10, rotating weight copies > 2x L2)")
     ap.add_argument("--gemm-sweep", action="store_true",
                     help="run only the skinny GEMM + fused consumer sweep (240 points)")
+    ap.add_argument("--handoff-protocol", action="store_true",
+                    help="cost of a kernel boundary (PDL graph chain) and of an in-kernel grid barrier")
     ap.add_argument("--timeline", action="store_true",
                     help="run only the in-graph kernel timeline of one decision of --workload")
     ap.add_argument("--timeline-steps", type=int, default=0,
@@ -1010,6 +1045,9 @@ def main():
         return
     if args.timeline:
         print(json.dumps(run_timeline(args)), flush=True)
+        return
+    if args.handoff_protocol:
+        print(json.dumps(run_handoff_protocol(args)), flush=True)
         return
     if args.layer_protocol:
         print(json.dumps(run_layer_protocol(args)), flush=True)

@@ -45,7 +45,7 @@ EXPORTS = [
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
     "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes", "fm_standalone_status",
     "fm_warm_trace_size", "fm_decode_warm_trace", "fm_test_launch_kernel", "fm_decode_timeline",
-    "fm_test_skinny_gemm_tile",
+    "fm_test_skinny_gemm_tile", "fm_test_pdl_chain", "fm_test_grid_barrier",
 ]
 
 
@@ -141,6 +141,8 @@ def load() -> ctypes.CDLL:
         "fm_abi_sizes": (i, [ctypes.POINTER(sz)] * 4),
         "fm_session_create": (i, [vp, vp, sz, vp, ctypes.POINTER(vp)]),
         "fm_session_fork": (i, [vp, vp, sz, i, vp, sz, vp, ctypes.POINTER(vp)]),
+        "fm_test_pdl_chain": (i, [i, i, i, i, i, vp, ctypes.POINTER(ctypes.c_float)]),
+        "fm_test_grid_barrier": (i, [i, i, i, i, ctypes.c_ulonglong, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -361,6 +363,28 @@ def warm_trace_size(p: int) -> int:
 def decode_warm_trace(p: int, noise, executed: int, actions, trace, nbytes: int, stream=None):
     _check(load().fm_decode_warm_trace(p, _ptr(noise), int(executed), _ptr(actions), _ptr(trace), nbytes,
                                        _stream(stream)), "fm_decode_warm_trace", p)
+
+
+def pdl_chain(ctas: int, threads: int, kernels: int, reps: int, pdl: bool, scratch) -> float:
+    """Microseconds per kernel of a CUDA graph of `kernels` dependent empty kernels
+    (programmatic dependent launch when pdl, else plain stream order). Synchronous;
+    scratch: a device tensor of >= 4 bytes."""
+    us = ctypes.c_float()
+    _check(load().fm_test_pdl_chain(int(ctas), int(threads), int(kernels), int(reps), int(bool(pdl)), _ptr(scratch),
+                                    ctypes.byref(us)), "fm_test_pdl_chain")
+    return us.value
+
+
+def grid_barrier(ctas: int, threads: int, rounds: int, mode: int, budget_ns: int, scratch, out, stream=None) -> int:
+    """One cooperative launch running `rounds` grid-wide barriers (mode 0 release/acquire,
+    1 fences around relaxed atomics, 2 a CTA that never arrives). Synchronous. out:
+    device int64 [ctas][2] (ns over the completed rounds, rounds completed). Returns the
+    status: 0, or 7 (FM_ERR_DEVICE) when a bounded wait ran out; raises on others."""
+    st = load().fm_test_grid_barrier(int(ctas), int(threads), int(rounds), int(mode), int(budget_ns), _ptr(scratch),
+                                     _ptr(out), _stream(stream))
+    if st not in (0, 7):
+        _check(st, "fm_test_grid_barrier")
+    return st
 
 
 def launch_kernel(p: int, layer: int, step: int, index: int, stream=None):

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfmad.so")
-SOURCES = ["gemm.cu", "gemm_nvfp4.cu", "attn.cu", "rowops.cu", "ofuse.cu", "policy.cu", "noalloc.cu"]
+SOURCES = ["gemm.cu", "gemm_nvfp4.cu", "attn.cu", "rowops.cu", "ofuse.cu", "policy.cu", "noalloc.cu", "handoff.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -413,6 +413,35 @@ int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
  * decision's data). It updates the policy's state as that kernel does. Asynchronous. */
 int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* stream);
 
+/* Hand-off diagnostics (no counterpart in the pages: they measure the kernel
+ * boundaries the decision is made of). Both are synchronous.
+ *
+ * fm_test_pdl_chain: a CUDA graph of `kernels` (1..4096) dependent launches of an
+ * empty kernel of `ctas` x `threads` (threads a multiple of 32, <= 1024), each
+ * launched with programmatic dependent launch when pdl != 0 (it signals its
+ * dependents at entry, then waits for its predecessor), else in plain stream order;
+ * the graph is run once, then `reps` (1..1000) times between two events.
+ * *us_per_kernel = elapsed / (reps * kernels). scratch: device, >= 4 bytes (a
+ * counter the kernels update). The graph, its stream and events are created and
+ * destroyed inside the call. Errors: FM_ERR_INVALID_ARG (NULL), FM_ERR_SHAPE (a
+ * count out of range), FM_ERR_CUDA.
+ *
+ * fm_test_grid_barrier: one cooperative launch of `ctas` x `threads` that runs
+ * `rounds` (1..10^6) grid-wide barriers on an arrive counter in global memory.
+ * mode 0: each CTA arrives by a release reduction and polls with acquire loads (gpu
+ * scope); mode 1: a full fence, a relaxed atomic add, volatile polls, a full fence
+ * after; mode 2: as 0 but CTA 0 never arrives, so every wait runs out (the failure
+ * path). Each wait is bounded by budget_ns (1 us .. 10 s); one that runs out sets an
+ * error word that releases every other waiter. scratch: device, 16-byte aligned,
+ * >= 8 bytes (counter and error word, zeroed by the call). out: device u64
+ * [ctas][2]: CTA b's time over its completed rounds (ns) and that round count.
+ * Errors: FM_ERR_INVALID_ARG, FM_ERR_SHAPE (also when the CTAs cannot all be resident
+ * at once), FM_ERR_ALIGN, FM_ERR_UNSUPPORTED (no cooperative launch), FM_ERR_CUDA,
+ * FM_ERR_DEVICE (a barrier wait ran out: always so in mode 2). */
+int fm_test_pdl_chain(int ctas, int threads, int kernels, int reps, int pdl, void* scratch, float* us_per_kernel);
+int fm_test_grid_barrier(int ctas, int threads, int rounds, int mode, unsigned long long budget_ns, void* scratch,
+                         unsigned long long* out, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Building blocks, exported for tests and standalone use (same conventions).
  * ------------------------------------------------------------------------- */
