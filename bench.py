@@ -845,7 +845,8 @@ def run_layer_protocol(args):
 def run_handoff_protocol(args):
     """What a stage boundary costs by itself: (a) a CUDA graph of dependent empty kernels
     (programmatic dependent launch, as the decision launches its kernels, and plain
-    stream order), microseconds per kernel; (b) grid-wide barriers inside one cooperative
+    stream order; also in thread-block clusters and with every thread storing 16 words
+    after its wait), microseconds per kernel; (b) grid-wide barriers inside one cooperative
     launch (release/acquire at gpu scope, and fences around relaxed atomics), the median
     over CTAs of nanoseconds per round. Both at 1 CTA, at the decision's typical grid
     sizes and at one and two CTAs per SM."""
@@ -854,14 +855,21 @@ def run_handoff_protocol(args):
     device = torch.device("cuda", 0)
     fmad.load()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    scratch = torch.zeros(4, dtype=torch.int32, device=device)
     grids = [1, 64, sms, 2 * sms]
+    writes_max = 16
+    scratch = torch.zeros(1 + 2 * sms * 256 * writes_max, dtype=torch.int32, device=device)
     chain, barrier = [], []
     with ClockSampler(0) as clocks:
         for ctas in grids:
             for pdl in (True, False):
                 us = fmad.pdl_chain(ctas, 256, 1000, 10, pdl, scratch)
-                chain.append({"ctas": ctas, "threads": 256, "pdl": pdl, "us_per_kernel": round(us, 3)})
+                chain.append({"ctas": ctas, "threads": 256, "pdl": pdl, "cluster": 1, "writes": 0,
+                              "us_per_kernel": round(us, 3)})
+        for cluster in (1, 2, 8):   # the decision's kernels run in clusters and store their outputs
+            for writes in (0, writes_max):
+                us = fmad.pdl_chain(64, 256, 1000, 10, True, scratch, cluster, writes)
+                chain.append({"ctas": 64, "threads": 256, "pdl": True, "cluster": cluster, "writes": writes,
+                              "us_per_kernel": round(us, 3)})
         for ctas in grids:
             for mode, name in ((0, "release/acquire"), (1, "fences + relaxed atomics")):
                 out = torch.zeros(2 * ctas, dtype=torch.int64, device=device)

@@ -141,7 +141,7 @@ def load() -> ctypes.CDLL:
         "fm_abi_sizes": (i, [ctypes.POINTER(sz)] * 4),
         "fm_session_create": (i, [vp, vp, sz, vp, ctypes.POINTER(vp)]),
         "fm_session_fork": (i, [vp, vp, sz, i, vp, sz, vp, ctypes.POINTER(vp)]),
-        "fm_test_pdl_chain": (i, [i, i, i, i, i, vp, ctypes.POINTER(ctypes.c_float)]),
+        "fm_test_pdl_chain": (i, [i, i, i, i, i, i, i, vp, sz, ctypes.POINTER(ctypes.c_float)]),
         "fm_test_grid_barrier": (i, [i, i, i, i, ctypes.c_ulonglong, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -365,13 +365,16 @@ def decode_warm_trace(p: int, noise, executed: int, actions, trace, nbytes: int,
                                        _stream(stream)), "fm_decode_warm_trace", p)
 
 
-def pdl_chain(ctas: int, threads: int, kernels: int, reps: int, pdl: bool, scratch) -> float:
-    """Microseconds per kernel of a CUDA graph of `kernels` dependent empty kernels
-    (programmatic dependent launch when pdl, else plain stream order). Synchronous;
-    scratch: a device tensor of >= 4 bytes."""
+def pdl_chain(ctas: int, threads: int, kernels: int, reps: int, pdl: bool, scratch, cluster: int = 1,
+              writes: int = 0) -> float:
+    """Microseconds per kernel of a CUDA graph of `kernels` dependent nearly empty kernels
+    (programmatic dependent launch when pdl, else plain stream order), in clusters of
+    `cluster` CTAs, each thread storing `writes` words after its wait. Synchronous;
+    scratch: a device tensor of >= 4 * (1 + ctas * threads * writes) bytes."""
     us = ctypes.c_float()
-    _check(load().fm_test_pdl_chain(int(ctas), int(threads), int(kernels), int(reps), int(bool(pdl)), _ptr(scratch),
-                                    ctypes.byref(us)), "fm_test_pdl_chain")
+    nbytes = scratch.numel() * scratch.element_size()
+    _check(load().fm_test_pdl_chain(int(ctas), int(threads), int(kernels), int(reps), int(bool(pdl)), int(cluster),
+                                    int(writes), _ptr(scratch), nbytes, ctypes.byref(us)), "fm_test_pdl_chain")
     return us.value
 
 

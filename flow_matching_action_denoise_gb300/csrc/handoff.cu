@@ -2,9 +2,10 @@
 // the next (the decision pays seven such boundaries per layer-step).
 //
 //  * fm_test_pdl_chain: a kernel boundary under programmatic dependent launch inside a
-//    CUDA graph, as the decision launches its kernels: a graph of `kernels` empty
-//    dependent kernels (each signals its dependents at entry, then waits for its
-//    predecessor), timed per kernel.
+//    CUDA graph, as the decision launches its kernels: a graph of `kernels` nearly
+//    empty dependent kernels (each signals its dependents at entry, then waits for its
+//    predecessor), optionally launched as thread-block clusters and with stores to
+//    make visible at completion, timed per kernel.
 //  * fm_test_grid_barrier: a grid-wide barrier inside one cooperatively launched
 //    kernel (every CTA co-resident by construction): rounds of an arrive counter in
 //    global memory, ordered either by release/acquire at gpu scope or by full fences
@@ -82,11 +83,16 @@ __global__ void grid_barrier_kernel(unsigned* words, int rounds, int mode, unsig
 
 // One link of the dependent chain: lets its dependent launch at entry, then waits for
 // its predecessor's completion (programmatic dependent launch; plain stream order
-// without the launch attribute). CTA 0 leaves one store so the kernel is not empty.
-__global__ void chain_kernel(int* sink) {
+// without the launch attribute). CTA 0 counts the link in sink[0]; with writes > 0
+// every thread then stores `writes` words (coalesced) into sink[1 + ...], the
+// memory a grid's completion has to make visible.
+__global__ void chain_kernel(int* sink, int writes) {
   pdl_trigger();
   pdl_wait();
   if (blockIdx.x == 0 && threadIdx.x == 0) sink[0] += 1;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int w = 0; w < writes; ++w) sink[1 + w * stride + t] = w;
 }
 
 }  // namespace
@@ -122,12 +128,15 @@ extern "C" int fm_test_grid_barrier(int ctas, int threads, int rounds, int mode,
   return err ? fm::record_error(FM_ERR_DEVICE, "fm_test_grid_barrier: a barrier wait ran out") : FM_OK;
 }
 
-extern "C" int fm_test_pdl_chain(int ctas, int threads, int kernels, int reps, int pdl, void* scratch,
-                                 float* us_per_kernel) {
+extern "C" int fm_test_pdl_chain(int ctas, int threads, int kernels, int reps, int pdl, int cluster, int writes,
+                                 void* scratch, size_t scratch_bytes, float* us_per_kernel) {
   if (!scratch || !us_per_kernel) return fm::record_error(FM_ERR_INVALID_ARG, "fm_test_pdl_chain: NULL argument");
   if (ctas < 1 || ctas > 65535 || threads < 32 || threads > 1024 || threads % 32 || kernels < 1 || kernels > 4096 ||
-      reps < 1 || reps > 1000)
+      reps < 1 || reps > 1000 || cluster < 1 || cluster > 8 || (cluster & (cluster - 1)) || ctas % cluster ||
+      writes < 0 || writes > 64)
     return fm::record_error(FM_ERR_SHAPE, "fm_test_pdl_chain: argument out of range");
+  if (scratch_bytes < 4 * (1 + static_cast<size_t>(ctas) * threads * writes))
+    return fm::record_error(FM_ERR_WORKSPACE, "fm_test_pdl_chain: scratch smaller than 4 * (1 + ctas * threads * writes)");
   cudaStream_t s = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -142,9 +151,10 @@ extern "C" int fm_test_pdl_chain(int ctas, int threads, int kernels, int reps, i
     fm::LaunchOpts lo;
     lo.stream = s;
     lo.pdl = pdl != 0;
+    lo.cluster = dim3(static_cast<unsigned>(cluster), 1, 1);
     cudaError_t le = cudaSuccess;
     for (int i = 0; i < kernels && le == cudaSuccess; ++i)
-      le = fm::launch(fm::chain_kernel, dim3(ctas), dim3(threads), 0, lo, static_cast<int*>(scratch));
+      le = fm::launch(fm::chain_kernel, dim3(ctas), dim3(threads), 0, lo, static_cast<int*>(scratch), writes);
     const cudaError_t ce = cudaStreamEndCapture(s, &graph);
     if (le != cudaSuccess || ce != cudaSuccess) why = "fm_test_pdl_chain: capture failed";
   }

@@ -416,15 +416,18 @@ int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* st
 /* Hand-off diagnostics (no counterpart in the pages: they measure the kernel
  * boundaries the decision is made of). Both are synchronous.
  *
- * fm_test_pdl_chain: a CUDA graph of `kernels` (1..4096) dependent launches of an
- * empty kernel of `ctas` x `threads` (threads a multiple of 32, <= 1024), each
+ * fm_test_pdl_chain: a CUDA graph of `kernels` (1..4096) dependent launches of a
+ * nearly empty kernel of `ctas` x `threads` (threads a multiple of 32, <= 1024) in
+ * thread-block clusters of `cluster` CTAs (1, 2, 4 or 8; dividing ctas), each
  * launched with programmatic dependent launch when pdl != 0 (it signals its
  * dependents at entry, then waits for its predecessor), else in plain stream order;
- * the graph is run once, then `reps` (1..1000) times between two events.
- * *us_per_kernel = elapsed / (reps * kernels). scratch: device, >= 4 bytes (a
- * counter the kernels update). The graph, its stream and events are created and
- * destroyed inside the call. Errors: FM_ERR_INVALID_ARG (NULL), FM_ERR_SHAPE (a
- * count out of range), FM_ERR_CUDA.
+ * after the wait every thread stores `writes` (0..64) 4-byte words. The graph is run
+ * once, then `reps` (1..1000) times between two events; *us_per_kernel = elapsed /
+ * (reps * kernels). scratch: device, scratch_bytes >= 4 * (1 + ctas * threads *
+ * writes) (a counter the kernels update, then the stored words). The graph, its
+ * stream and events are created and destroyed inside the call. Errors:
+ * FM_ERR_INVALID_ARG (NULL), FM_ERR_SHAPE (a count out of range), FM_ERR_WORKSPACE
+ * (scratch too small), FM_ERR_CUDA.
  *
  * fm_test_grid_barrier: one cooperative launch of `ctas` x `threads` that runs
  * `rounds` (1..10^6) grid-wide barriers on an arrive counter in global memory.
@@ -438,7 +441,8 @@ int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* st
  * Errors: FM_ERR_INVALID_ARG, FM_ERR_SHAPE (also when the CTAs cannot all be resident
  * at once), FM_ERR_ALIGN, FM_ERR_UNSUPPORTED (no cooperative launch), FM_ERR_CUDA,
  * FM_ERR_DEVICE (a barrier wait ran out: always so in mode 2). */
-int fm_test_pdl_chain(int ctas, int threads, int kernels, int reps, int pdl, void* scratch, float* us_per_kernel);
+int fm_test_pdl_chain(int ctas, int threads, int kernels, int reps, int pdl, int cluster, int writes, void* scratch,
+                      size_t scratch_bytes, float* us_per_kernel);
 int fm_test_grid_barrier(int ctas, int threads, int rounds, int mode, unsigned long long budget_ns, void* scratch,
                          unsigned long long* out, void* stream);
 

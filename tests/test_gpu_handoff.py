@@ -15,9 +15,11 @@ import flow_matching_action_denoise_gb300 as fmad
 def test_host_argument_checks():
     L = fmad.load()
     us = ctypes.c_float()
-    assert L.fm_test_pdl_chain(1, 32, 0, 1, 1, 16, ctypes.byref(us)) == 2            # FM_ERR_SHAPE
-    assert L.fm_test_pdl_chain(1, 32, 1, 1, 1, None, ctypes.byref(us)) == 1          # FM_ERR_INVALID_ARG
-    assert L.fm_test_pdl_chain(1, 48, 1, 1, 1, 16, ctypes.byref(us)) == 2            # threads not a multiple of 32
+    assert L.fm_test_pdl_chain(1, 32, 0, 1, 1, 1, 0, 16, 4, ctypes.byref(us)) == 2     # FM_ERR_SHAPE
+    assert L.fm_test_pdl_chain(1, 32, 1, 1, 1, 1, 0, None, 4, ctypes.byref(us)) == 1   # FM_ERR_INVALID_ARG
+    assert L.fm_test_pdl_chain(1, 48, 1, 1, 1, 1, 0, 16, 4, ctypes.byref(us)) == 2     # threads not a multiple of 32
+    assert L.fm_test_pdl_chain(6, 32, 1, 1, 1, 4, 0, 16, 4, ctypes.byref(us)) == 2     # cluster does not divide ctas
+    assert L.fm_test_pdl_chain(8, 32, 1, 1, 1, 8, 2, 16, 64, ctypes.byref(us)) == 4    # FM_ERR_WORKSPACE
     assert L.fm_test_grid_barrier(1, 32, 1, 0, 10 ** 6, None, 16, None) == 1
     assert L.fm_test_grid_barrier(1, 32, 1, 3, 10 ** 6, 16, 16, None) == 2          # mode
     assert L.fm_test_grid_barrier(1, 32, 1, 0, 10, 16, 16, None) == 2               # budget below 1 us
@@ -69,10 +71,13 @@ def test_grid_barrier_rejects_more_ctas_than_fit():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("pdl", [True, False])
-def test_pdl_chain_times_positive(pdl):
+@pytest.mark.parametrize("pdl,cluster,writes", [(True, 1, 0), (False, 1, 0), (True, 8, 4)])
+def test_pdl_chain_times_positive(pdl, cluster, writes):
     import torch
-    scratch = torch.zeros(4, dtype=torch.int32, device="cuda")
-    us = fmad.pdl_chain(64, 128, 100, 3, pdl, scratch)
+    scratch = torch.zeros(1 + 64 * 128 * writes, dtype=torch.int32, device="cuda")
+    us = fmad.pdl_chain(64, 128, 100, 3, pdl, scratch, cluster, writes)
     assert np.isfinite(us) and 0.0 < us < 1000.0
     assert int(scratch[0].item()) == 100 * 4    # the warm-up run and three timed runs
+    if writes:
+        w = scratch[1:].cpu().numpy().reshape(writes, 64 * 128)
+        assert np.all(w == np.arange(writes)[:, None])
