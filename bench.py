@@ -385,9 +385,13 @@ def time_graph(device, launches, replays=5):
 
 def time_decision_gemm(cfg, scales, device, index=None):
     """The gate|up GEMM exactly as the decision launches it (GeGLU + E4M3 epilogue,
-    the decision's split and cluster; kernel `index` of a layer-step), launched back to
-    back through fm_test_launch_kernel over the layers of a policy whose packed weights
-    rotate through more than 2x L2, timed with CUDA events on the replay stream.
+    the decision's split and cluster; kernel `index` of a layer-step; programmatic
+    dependent launch), launched back to back through fm_test_launch_kernel over the
+    layers of a policy whose packed weights rotate through more than 2x L2, timed with
+    CUDA events on the replay stream: the average launch duration is the graph's time
+    over its launches, so a launch's weight copies may overlap its predecessor's tail
+    as they do in the decision. The same without programmatic dependent launch (each
+    launch starts after the previous one has finished) is reported as `no_pdl`.
     Algorithmic bytes per launch: weights N K + activations M K + GeGLU codes M N / 2."""
     import dataclasses
     import torch
@@ -398,29 +402,40 @@ def time_decision_gemm(cfg, scales, device, index=None):
     R = int(np.ceil(2 * l2 / (N * K))) + 1
     rcfg = dataclasses.replace(cfg, L=R, S=1)
     layer = fm_synth.layer_weights(rcfg, 0)
-    pol = fmad.Policy(rcfg, [layer] * R, fm_synth.final_weights(rcfg), act_scales=np.tile(scales[:1], (R, 1)),
-                      device=device)
     kp, vp = fm_synth.prefix_kv(dataclasses.replace(rcfg, L=1))
-    pol.set_prefix_kv(torch.from_numpy(np.repeat(kp, R, 0)).to(device, torch.bfloat16),
-                      torch.from_numpy(np.repeat(vp, R, 0)).to(device, torch.bfloat16))
-    noise = torch.from_numpy(fm_synth.noise(rcfg, 0)).to(device)
-    pol.decode(noise)   # fills every buffer the kernel reads
-    torch.cuda.synchronize(device)
-    if index is None:   # the gate|up GEMM's position in a layer-step: after the O GEMM's consumer
-        index = 4 if fmad.kernel_count(pol.handle)[0] == 7 else 3
-    launches = [lambda st, l=l: fmad.launch_kernel(pol.handle, l, 0, index, st) for l in range(R)] * 2
-    us = time_graph(device, launches)
-    if fmad.device_status(pol.handle):
-        raise RuntimeError("device error word set (decision GEMM timing)")
-    pol.close()
     algo = N * K + M * K + M * (N // 2)
+
+    def timed(flags):
+        nonlocal index
+        pol = fmad.Policy(rcfg, [layer] * R, fm_synth.final_weights(rcfg), act_scales=np.tile(scales[:1], (R, 1)),
+                          device=device, flags=flags)
+        pol.set_prefix_kv(torch.from_numpy(np.repeat(kp, R, 0)).to(device, torch.bfloat16),
+                          torch.from_numpy(np.repeat(vp, R, 0)).to(device, torch.bfloat16))
+        noise = torch.from_numpy(fm_synth.noise(rcfg, 0)).to(device)
+        pol.decode(noise)   # fills every buffer the kernel reads
+        torch.cuda.synchronize(device)
+        if index is None:   # the gate|up GEMM's position in a layer-step: after the O GEMM's consumer
+            index = 4 if fmad.kernel_count(pol.handle)[0] == 7 else 3
+        launches = [lambda st, l=l: fmad.launch_kernel(pol.handle, l, 0, index, st) for l in range(R)] * 2
+        us = time_graph(device, launches)
+        if fmad.device_status(pol.handle):
+            raise RuntimeError("device error word set (decision GEMM timing)")
+        pol.close()
+        return us
+
+    us = timed(fmad.FLAG_USE_GRAPH | fmad.FLAG_USE_PDL)
+    us_plain = timed(fmad.FLAG_USE_GRAPH)
     peak, kind = measured_peaks()
     achieved = algo / (us * 1e-6) / 1e9
+    achieved_plain = algo / (us_plain * 1e-6) / 1e9
     return {"kernel": f"skinny_gemm_kernel<fp8> gate|up + GeGLU epilogue as in the decision (N={N}, K={K}, M={M})",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind_note(kind),
             "traffic": profiled_traffic(), "algorithmic_bytes": int(algo), "avg_launch_us": round(us, 3),
-            "timing": f"CUDA graph of back-to-back launches over {R} layers' weights (> 2x L2), CUDA events"}
+            "timing": f"CUDA graph of back-to-back launches with programmatic dependent launch, as in the "
+                      f"decision, over {R} layers' weights (> 2x L2); graph time / launches, CUDA events",
+            "no_pdl": {"avg_launch_us": round(us_plain, 3), "achieved": round(achieved_plain, 1),
+                       "frac": round(achieved_plain / peak, 4)}}
 
 
 def time_dominant_gemm(cfg, pol, device, stream):

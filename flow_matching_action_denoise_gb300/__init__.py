@@ -391,7 +391,8 @@ def grid_barrier(ctas: int, threads: int, rounds: int, mode: int, budget_ns: int
 
 
 def launch_kernel(p: int, layer: int, step: int, index: int, stream=None):
-    """Launch one kernel of a layer-step exactly as the decision does (no PDL)."""
+    """Launch one kernel of a layer-step exactly as the decision does (with programmatic
+    dependent launch when the policy's flags hold FLAG_USE_PDL)."""
     _check(load().fm_test_launch_kernel(p, layer, step, index, _stream(stream)), "fm_test_launch_kernel", p)
 
 

@@ -1510,6 +1510,7 @@ int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* st
     return fail(p, FM_ERR_INVALID_ARG, "layer, step or kernel index out of range");
   LaunchOpts o;
   o.stream = static_cast<cudaStream_t>(stream);
+  o.pdl = (c.flags & FM_FLAG_USE_PDL) != 0;   // as the decision launches it
   int seq = 0;
   o.seq = &seq;
   o.only = index;

@@ -408,8 +408,9 @@ int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
 /* Launch only kernel `index` (0 .. per_layer - 1, in the decision's order: FP8/BF16
  * QKV GEMM, attention, O GEMM, consumer, gate|up GEMM + GeGLU, down GEMM, consumer or
  * step boundary) of layer `layer` at Euler step `step`, with exactly the arguments and
- * launch configuration the decision uses, without Programmatic Dependent Launch, on the
- * policy's current buffers: for timing one kernel on its own (the buffers hold the last
+ * launch configuration the decision uses (Programmatic Dependent Launch when the
+ * policy's flags hold FM_FLAG_USE_PDL, as in the decision), on the policy's current
+ * buffers: for timing one kernel on its own or back to back (the buffers hold the last
  * decision's data). It updates the policy's state as that kernel does. Asynchronous. */
 int fm_test_launch_kernel(fm_policy* p, int layer, int step, int index, void* stream);
 
