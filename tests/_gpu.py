@@ -81,9 +81,9 @@ def load_scales(name):
     return np.loadtxt(path, dtype=np.float32, ndmin=2)
 
 
-def parse_trace(raw, cfg, pol):
-    """Split an fm_decode_trace buffer into records[k][l] of numpy arrays; codes are
-    returned as decoded values (E4M3 codes without their scale, or bf16 values)."""
+def _trace_fields(cfg, pol):
+    """The fields of one trace record (one layer-step) in order: (name, kind, shape,
+    bytes); kind f = fp32, b = the QKV output, c = activation codes."""
     M, d = cfg.M, cfg.d
     fp8 = cfg.act_fmt == "fp8"
     f16_codes = cfg.weight_fmt == "nvfp4"   # E4M3 codes stored as their f16 values
@@ -100,30 +100,56 @@ def parse_trace(raw, cfg, pol):
               ("x_mid", "f", (M, d)), ("q2", "c", (M, d)),
               ("geglu_out", "c", (M, cfg.F)),
               ("y_d", "f", (parts("y_d", d), M, d)), ("x_out", "f", (M, d)), ("actions", "f", (M, cfg.A))]
-    off = 0
-    recs = []
-    for k in range(cfg.S):
-        row = []
-        for l in range(cfg.L):
-            r = {}
-            for name, kind, shape in layout:
-                n = int(np.prod(shape))
-                nb = n * (4 if kind == "f" else (1 if qkv8 else 2) if kind == "b" else ab)
-                chunk = raw[off:off + nb]
-                off += nb
-                if kind == "b" and qkv8:
-                    r[name] = C.e4m3_decode_code(chunk).reshape(shape)
-                elif kind == "b":
-                    r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
-                elif kind == "f":
-                    r[name] = chunk.view(np.float32).reshape(shape).astype(np.float64)
-                elif f16_codes:
-                    r[name] = chunk.view(np.float16).astype(np.float64).reshape(shape)
-                elif fp8:
-                    r[name] = C.e4m3_decode_code(chunk).reshape(shape)
-                else:
-                    r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
-            row.append(r)
-        recs.append(row)
-    assert off == raw.size, (off, raw.size)
-    return recs
+    out = []
+    for name, kind, shape in layout:
+        n = int(np.prod(shape))
+        out.append((name, kind, shape, n * (4 if kind == "f" else (1 if qkv8 else 2) if kind == "b" else ab)))
+    return out
+
+
+def _decode_record(raw, cfg, fields):
+    fp8 = cfg.act_fmt == "fp8"
+    f16_codes = cfg.weight_fmt == "nvfp4"
+    qkv8 = getattr(cfg, "attn_fmt", "bf16") == "fp8"
+    r, off = {}, 0
+    for name, kind, shape, nb in fields:
+        chunk = raw[off:off + nb]
+        off += nb
+        if kind == "b" and qkv8:
+            r[name] = C.e4m3_decode_code(chunk).reshape(shape)
+        elif kind == "b":
+            r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
+        elif kind == "f":
+            r[name] = chunk.view(np.float32).reshape(shape).astype(np.float64)
+        elif f16_codes:
+            r[name] = chunk.view(np.float16).astype(np.float64).reshape(shape)
+        elif fp8:
+            r[name] = C.e4m3_decode_code(chunk).reshape(shape)
+        else:
+            r[name] = C.bf16_decode_bits(chunk.view(np.uint16)).reshape(shape)
+    assert off == raw.size
+    return r
+
+
+def parse_trace(raw, cfg, pol):
+    """Split an fm_decode_trace buffer into records[k][l] of numpy arrays; codes are
+    returned as decoded values (E4M3 codes without their scale, or bf16 values)."""
+    fields = _trace_fields(cfg, pol)
+    rec = sum(f[3] for f in fields)
+    assert raw.size == rec * cfg.S * cfg.L, (raw.size, rec * cfg.S * cfg.L)
+    return [[_decode_record(raw[(k * cfg.L + l) * rec:(k * cfg.L + l + 1) * rec], cfg, fields)
+             for l in range(cfg.L)] for k in range(cfg.S)]
+
+
+def read_trace_records(trace, cfg, pol, wanted):
+    """{(k, l): record} for the layer-steps in `wanted`, copying only those records out
+    of the device trace buffer (a uint8 tensor): the records are laid out layer-step by
+    layer-step, step-major, each of the same size."""
+    fields = _trace_fields(cfg, pol)
+    rec = sum(f[3] for f in fields)
+    assert trace.numel() >= rec * cfg.S * cfg.L
+    out = {}
+    for k, l in wanted:
+        i = k * cfg.L + l
+        out[(k, l)] = _decode_record(trace[i * rec:(i + 1) * rec].cpu().numpy(), cfg, fields)
+    return out

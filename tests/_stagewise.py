@@ -118,25 +118,96 @@ def fp8_attention_allowance(qc, kc, vc, kpre_c, vpre_c, H, Hkv, Dh, s_q, s_k, s_
     return out
 
 
+def check_layer_stages(cfg, W, mods, r, sl, kp_l, vp_l, prefix8_l, where, attn_max_frac=1e-3,
+                       attn_abs_tol=2.0 ** -7):
+    """Teacher-forced checks of one layer-step's record r: every stage recomputed by the
+    oracle from the record's own inputs. W: the layer's prepared weights; mods: its
+    (sc1, sh1, g1, sc2, sh2, g2) at this step; sl: its activation scales ([4], or [7]
+    with FP8 attention; ignored for bf16); kp_l, vp_l: its prefix rows; prefix8_l: their
+    E4M3 codes (FP8 attention only). Returns (inc, x_res): the MLP branch's increment
+    and x_mid + inc, which the caller checks against the layer-step's output."""
+    fmt = cfg.act_fmt
+    attn8 = getattr(cfg, "attn_fmt", "bf16") == "fp8"
+    H, Dh, F = cfg.H, cfg.Dh, cfg.F
+
+    def s_act(i):
+        return float(sl[i]) if fmt in ("fp8", "nvfp4") else 1.0
+
+    def dq(i, w):   # dequantisation factor fp32(s_a * s_w) the epilogues apply
+        return np.float64(np.float32(s_act(i)) * np.float32(w.scale))
+
+    sc1, sh1, g1, sc2, sh2, g2 = mods
+    check_codes(r["q"], O.quant_codes(O.ada_norm(r["x_in"], sc1, sh1, cfg.eps), s_act(0), fmt),
+                where + " pre-attention quantise", fmt)
+    qkv = r["y_qkv"]
+    exact = (r["q"] @ W["qkv"].codes.T) * dq(0, W["qkv"])
+    nq, nk = H * Dh, cfg.Hkv * Dh
+    if attn8:
+        # E4M3 Q | K | V codes with their static scales, from the exact product
+        s3 = [s_act(O.SITE_Q), s_act(O.SITE_K), s_act(O.SITE_V)]
+        for (a, b), sx, nm in zip(((0, nq), (nq, nq + nk), (nq + nk, exact.shape[1])), s3, "QKV"):
+            check_codes(qkv[:, a:b], O.quant_codes(exact[:, a:b], sx, "fp8"), where + f" QKV GEMM ({nm} codes)")
+        # the attention stage's input is exactly the recorded codes and the prefix copy
+        args = (qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], prefix8_l[0], prefix8_l[1], H, cfg.Hkv, Dh, *s3)
+        Oref = O.attention_fp8(*args)
+        # probability codes at a rounding boundary may round either way
+        extra = fp8_attention_allowance(*args) / s_act(1)
+    else:
+        extra = 0.0
+        # QKV: the GEMM epilogue emits bf16(sum * dequant); within one bf16 rounding
+        # of the exact dequantised product
+        assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) +
+                      1e-5 * np.sqrt(np.mean(exact ** 2))), where + " QKV GEMM"
+        # the attention stage's input is exactly the recorded bf16 Q | K | V
+        Oref = O.attention(qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], kp_l, vp_l, H, cfg.Hkv, Dh)
+    # attention rounds its probabilities (bf16, or E4M3 with 3 mantissa bits): a
+    # near-tie probability rounding either way moves a row of O by a fraction of
+    # P * |V|, so its allowance is abs_tol * RMS
+    check_codes(r["attn_out"], O.quant_codes(Oref, s_act(1), fmt), where + " attention", fmt,
+                max_frac=attn_max_frac, abs_tol=attn_abs_tol, extra=extra)
+    # the O GEMM: its partial planes when recorded, then the gated residual (the
+    # increment is compared, so the tolerance is relative to the branch itself)
+    yo_ref = r["attn_out"] @ W["o"].codes.T
+    if r["y_o"].shape[0]:
+        check_close(r["y_o"].sum(0), yo_ref, where + " O GEMM")
+    check_increment(r["x_mid"], r["x_in"], g1 * yo_ref * dq(1, W["o"]), where + " O GEMM + attention residual")
+    check_codes(r["q2"], O.quant_codes(O.ada_norm(r["x_mid"], sc2, sh2, cfg.eps), s_act(2), fmt),
+                where + " pre-MLP quantise", fmt)
+    # gate|up GEMM with GeGLU + quantise in its epilogue
+    gu = (r["q2"] @ W["gu"].codes.T) * dq(2, W["gu"])
+    check_codes(r["geglu_out"], O.quant_codes(O.gelu_tanh(gu[:, :F]) * gu[:, F:], s_act(3), fmt),
+                where + " gate|up GEMM + GeGLU", fmt)
+    yd_ref = r["geglu_out"] @ W["d"].codes.T
+    if r["y_d"].shape[0]:
+        check_close(r["y_d"].sum(0), yd_ref, where + " down GEMM")
+    inc = g2 * yd_ref * dq(3, W["d"])
+    return inc, r["x_mid"] + inc
+
+
+def check_step_end(model, k, r, x_res, a_prev, dt, next_head, where):
+    """The last layer of step k: the final AdaRMSNorm, W_out and the Euler update from
+    a_prev, then the next step's head (next_head) or the residual itself."""
+    fin = model.final
+    scf, shf = model.mods[k][1]
+    v = (O.ada_norm(x_res, scf, shf, model.cfg.eps) * fin["gamma_f"]) @ fin["w_out"].T + fin["b_out"]
+    check_close(r["actions"], a_prev + dt * v, where + " Euler update")
+    if next_head:
+        check_close(r["x_out"], r["actions"].astype(np.float64) @ fin["w_in"].T + fin["b_in"], where + " next step head")
+    else:
+        check_close(r["x_out"], x_res, where + " MLP residual")
+
+
 def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac=1e-3, attn_abs_tol=2.0 ** -7,
                           mod_rows=None, dt=None):
     """recs[k][l] as parse_trace returns them; scales [L][4] ([L][7] with FP8
     attention; ignored for bf16). mod_rows: the modulation row of each recorded step
     (default 0 .. S-1); dt: the Euler step (default -1/S). The one-step warm start
     is mod_rows=[S], dt=-warm_t from its mixed input a_tau as `noise`."""
-    fmt = cfg.act_fmt
     attn8 = getattr(cfg, "attn_fmt", "bf16") == "fp8"
     prefix8 = prefix_codes(kp, vp, scales) if attn8 else None
-    M, H, Dh, F, L, S = cfg.M, cfg.H, cfg.Dh, cfg.F, cfg.L, cfg.S
+    L, S = cfg.L, cfg.S
     fin = model.final
     kp, vp = np.asarray(kp, np.float64), np.asarray(vp, np.float64)
-
-    def s_act(l, i):
-        return float(scales[l][i]) if fmt in ("fp8", "nvfp4") else 1.0
-
-    def dq(l, i, w):   # dequantisation factor fp32(s_a * s_w) the epilogues apply
-        return np.float64(np.float32(s_act(l, i)) * np.float32(w.scale))
-
     rows = list(range(S)) if mod_rows is None else list(mod_rows)
     dt = -1.0 / S if dt is None else dt
     a_prev = np.asarray(noise, np.float64)
@@ -144,64 +215,13 @@ def check_decision_stages(cfg, model, recs, noise, kp, vp, scales, attn_max_frac
     for i, k in enumerate(rows):
         for l in range(L):
             r = recs[i][l]
-            W = model.w[l]
-            sc1, sh1, g1, sc2, sh2, g2 = model.mods[k][0][l]
             where = f"step {k} layer {l}"
-            check_codes(r["q"], O.quant_codes(O.ada_norm(r["x_in"], sc1, sh1, cfg.eps), s_act(l, 0), fmt),
-                        where + " pre-attention quantise", fmt)
-            qkv = r["y_qkv"]
-            exact = (r["q"] @ W["qkv"].codes.T) * dq(l, 0, W["qkv"])
-            nq, nk = H * Dh, cfg.Hkv * Dh
-            if attn8:
-                # E4M3 Q | K | V codes with their static scales, from the exact product
-                s3 = [s_act(l, O.SITE_Q), s_act(l, O.SITE_K), s_act(l, O.SITE_V)]
-                for (a, b), sx, nm in zip(((0, nq), (nq, nq + nk), (nq + nk, exact.shape[1])), s3, "QKV"):
-                    check_codes(qkv[:, a:b], O.quant_codes(exact[:, a:b], sx, "fp8"), where + f" QKV GEMM ({nm} codes)")
-                # the attention stage's input is exactly the recorded codes and the prefix copy
-                args = (qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], prefix8[l][0], prefix8[l][1], H,
-                        cfg.Hkv, Dh, *s3)
-                Oref = O.attention_fp8(*args)
-                # probability codes at a rounding boundary may round either way
-                extra = fp8_attention_allowance(*args) / s_act(l, 1)
-            else:
-                extra = 0.0
-                # QKV: the GEMM epilogue emits bf16(sum * dequant); within one bf16 rounding
-                # of the exact dequantised product
-                assert np.all(np.abs(qkv - exact) <= 2.0 ** -8 * np.abs(exact) +
-                              1e-5 * np.sqrt(np.mean(exact ** 2))), where + " QKV GEMM"
-                # the attention stage's input is exactly the recorded bf16 Q | K | V
-                Oref = O.attention(qkv[:, :nq], qkv[:, nq:nq + nk], qkv[:, nq + nk:], kp[l], vp[l], H, cfg.Hkv, Dh)
-            # attention rounds its probabilities (bf16, or E4M3 with 3 mantissa bits): a
-            # near-tie probability rounding either way moves a row of O by a fraction of
-            # P * |V|, so its allowance is abs_tol * RMS
-            check_codes(r["attn_out"], O.quant_codes(Oref, s_act(l, 1), fmt), where + " attention", fmt,
-                        max_frac=attn_max_frac, abs_tol=attn_abs_tol, extra=extra)
-            # the O GEMM: its partial planes when recorded, then the gated residual (the
-            # increment is compared, so the tolerance is relative to the branch itself)
-            yo_ref = r["attn_out"] @ W["o"].codes.T
-            if r["y_o"].shape[0]:
-                check_close(r["y_o"].sum(0), yo_ref, where + " O GEMM")
-            check_increment(r["x_mid"], r["x_in"], g1 * yo_ref * dq(l, 1, W["o"]), where + " O GEMM + attention residual")
-            check_codes(r["q2"], O.quant_codes(O.ada_norm(r["x_mid"], sc2, sh2, cfg.eps), s_act(l, 2), fmt),
-                        where + " pre-MLP quantise", fmt)
-            # gate|up GEMM with GeGLU + quantise in its epilogue
-            gu = (r["q2"] @ W["gu"].codes.T) * dq(l, 2, W["gu"])
-            check_codes(r["geglu_out"], O.quant_codes(O.gelu_tanh(gu[:, :F]) * gu[:, F:], s_act(l, 3), fmt),
-                        where + " gate|up GEMM + GeGLU", fmt)
-            yd_ref = r["geglu_out"] @ W["d"].codes.T
-            if r["y_d"].shape[0]:
-                check_close(r["y_d"].sum(0), yd_ref, where + " down GEMM")
-            inc = g2 * yd_ref * dq(l, 3, W["d"])
-            x_res = r["x_mid"] + inc
+            inc, x_res = check_layer_stages(cfg, model.w[l], model.mods[k][0][l], r,
+                                            scales[l] if scales is not None else None, kp[l], vp[l],
+                                            prefix8[l] if attn8 else None, where, attn_max_frac, attn_abs_tol)
             if l < L - 1:
                 check_increment(r["x_out"], r["x_mid"], inc, where + " down GEMM + MLP residual")
                 continue
-            scf, shf = model.mods[k][1]
-            v = (O.ada_norm(x_res, scf, shf, cfg.eps) * fin["gamma_f"]) @ fin["w_out"].T + fin["b_out"]
-            check_close(r["actions"], a_prev + dt * v, where + " Euler update")
+            check_step_end(model, k, r, x_res, a_prev, dt, i < len(rows) - 1, where)
             a_prev = r["actions"].astype(np.float64)
-            if i < len(rows) - 1:
-                check_close(r["x_out"], a_prev @ fin["w_in"].T + fin["b_in"], where + " next step head")
-            else:
-                check_close(r["x_out"], x_res, where + " MLP residual")
     return recs[len(rows) - 1][L - 1]["actions"]
