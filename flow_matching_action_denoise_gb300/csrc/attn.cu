@@ -296,24 +296,36 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   cp_async_wait_all();
   __syncthreads();   // V^T groups and the staged chunk values are in place
   if (tl_on) tt[2] = global_ns();
-  if (nchunk > 0) {   // shared -> shared transpose into V^T (keys along K), this CTA's dims
-    const int d = tid & (kDv - 1);
-    if constexpr (kF8) {
-      const uint8_t* vstage = smem + sp.pm;
-      for (int t = c_lo + tid / kDv; t < c_hi; t += kThreads / kDv) {
-        const int key = t - t0;
-        const uint32_t v = vstage[(t - c_lo) * kDh + d0 + d];
-        const uint32_t addr = sVta + (key >> 7) * kTileV + swz(d, (key & 127) >> 4) + (key & 15);
-        asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+  if (nchunk > 0) {
+    // shared -> shared transpose of the chunk's values into V^T (keys along K), this
+    // CTA's dims: one thread per (16-byte V^T group holding chunk keys, head dim), the
+    // group's current bytes (prefix keys, zeros) merged with the chunk keys it holds,
+    // gathered from the row-major staging (consecutive threads take consecutive dims),
+    // and written back by one 16-byte store
+    constexpr int kPer = kF8 ? 16 : 8;   // keys per 16-byte group
+    const int g_lo = (c_lo - t0) / kPer, g_hi = (c_hi - 1 - t0) / kPer;
+    for (int idx = tid; idx < (g_hi - g_lo + 1) * kDv; idx += kThreads) {
+      const int d = idx % kDv, G = g_lo + idx / kDv;
+      uint4* grp = reinterpret_cast<uint4*>(smem + sp.vt + (G >> 3) * kTileV + swz(d, G & 7));
+      uint4 u = *grp;
+      if constexpr (kF8) {
+        uint8_t* e8 = reinterpret_cast<uint8_t*>(&u);
+        const uint8_t* vstage = smem + sp.pm;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int t = t0 + G * 16 + e;
+          if (t >= c_lo && t < c_hi) e8[e] = vstage[(t - c_lo) * kDh + d0 + d];
+        }
+      } else {
+        uint16_t* e16 = reinterpret_cast<uint16_t*>(&u);
+        const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int t = t0 + G * 8 + e;
+          if (t >= c_lo && t < c_hi) e16[e] = vstage[(t - c_lo) * kDh + d0 + d];
+        }
       }
-    } else {
-      const uint16_t* vstage = reinterpret_cast<const uint16_t*>(smem + sp.pm);
-      for (int t = c_lo + tid / kDv; t < c_hi; t += kThreads / kDv) {
-        const int key = t - t0, grp = key >> 3;
-        const uint16_t v = vstage[(t - c_lo) * kDh + d0 + d];
-        const uint32_t addr = sVta + (grp >> 3) * kTileV + swz(d, grp & 7) + (key & 7) * 2;
-        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-      }
+      *grp = u;
     }
   }
   fence_async_smem();   // generic-proxy shared-memory writes -> tensor-core reads
