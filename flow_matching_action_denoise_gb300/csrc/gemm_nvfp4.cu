@@ -21,7 +21,7 @@
 //   warps 4..11 - decoders: two threads per weight row, each expanding half of the
 //                 row's 64 elements of a block into the 128-byte-swizzled K-major
 //                 f16 operand tile (eight warps: the expansion, not the tensor pipe,
-//                 bounds these GEMMs);
+//                 bounds these GEMMs; the code also takes four threads per row);
 //   all warps   - epilogue: TMEM -> fp32 partial planes, or (single K slice,
 //                 gate|up weight) GeGLU + static E4M3 (or four-bit) quantisation.
 
@@ -42,6 +42,9 @@ namespace {
 constexpr int kThreads = 384;                                 // 12 warps: roles, 8 decoders, epilogue
 constexpr int kDecoders = kThreads - 128;                     // warps 4-11 expand the weight codes
 constexpr int kDecoderWarps = kDecoders / 32;
+constexpr int kRowParts = kDecoders / 128;                    // decoder threads per weight row
+constexpr int kChunksPer = 8 / kRowParts;                     // 8-element chunks of a block row per thread
+static_assert(kRowParts == 2 || kRowParts == 4, "two or four decoder threads per weight row");
 constexpr int kTileN = 128;                                   // weight rows per CTA (MMA M)
 constexpr int kKb = 64;                                       // K elements per pipeline block
 constexpr int kCodeBytes = kTileN * kKb / 2;                  // 4096: two E2M1 codes per byte
@@ -229,10 +232,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
     }
     tc_commit(done);
   } else if (warp >= 4) {
-    // ---------------- decoders: threads row and row + 128 expand the two halves (chunks
-    // 0-3 and 4-7, elements 0-31 and 32-63) of weight row `row` of each block
+    // ---------------- decoders: kRowParts threads per weight row `row` of each block,
+    // thread `part` expanding chunks part * kChunksPer .. + kChunksPer - 1 (elements
+    // 8 per chunk) of that row
     const int row = (tid - 128) & 127;
-    const int half = (tid - 128) >> 7;
+    const int part = (tid - 128) >> 7;
     for (int st = 0; st < nst; ++st) {
       const int r = st % R;
       if (!mbar_wait(&raw_full[r], static_cast<uint32_t>(st / R) & 1u)) {
@@ -240,13 +244,18 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
         s_abort = 1;
         break;
       }
-      uint32_t codes[2][4], sc[2];   // C <= 2: unrolled, so they stay in registers
+      uint32_t codes[2][kChunksPer], sc[2];   // C <= 2: unrolled, so they stay in registers
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (c >= C) break;
         const uint8_t* src = raw + static_cast<size_t>(r) * raw_stage + c * kRawBytes;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(src + row * 32 + half * 16);
-        codes[c][0] = c0.x; codes[c][1] = c0.y; codes[c][2] = c0.z; codes[c][3] = c0.w;
+        if constexpr (kChunksPer == 4) {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(src + row * 32 + part * 16);
+          codes[c][0] = c0.x; codes[c][1] = c0.y; codes[c][2] = c0.z; codes[c][3] = c0.w;
+        } else {
+          const uint2 c0 = *reinterpret_cast<const uint2*>(src + row * 32 + part * 8);
+          codes[c][0] = c0.x; codes[c][1] = c0.y;
+        }
         sc[c] = *reinterpret_cast<const uint32_t*>(src + kCodeBytes + row * 4);
       }
       __syncwarp();
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemm_kernel(const __grid_const
         if (c >= C) break;
         const uint32_t dst = smem_u32(a_tiles + static_cast<size_t>(slot) * a_stage + c * kATileBytes) + row * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // 16-byte chunk q = elements 8q..8q+7, block scale q / 2
-          const int q = half * 4 + i;
+        for (int i = 0; i < kChunksPer; ++i) {   // 16-byte chunk q = elements 8q..8q+7, block scale q / 2
+          const int q = part * kChunksPer + i;
           const __half bs = e4m3_half(static_cast<uint8_t>((sc[c] >> (8 * (q >> 1))) & 0xffu));
           st_shared_v4(dst + ((q ^ (row & 7)) << 4), decode8(codes[c][i], __half2(bs, bs)));
         }
