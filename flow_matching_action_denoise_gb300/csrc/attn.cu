@@ -99,6 +99,34 @@ struct SmemPlan {
 // blocks of [dv rows][128 bytes] along the keys (bf16: kc/64 blocks of 64 keys; E4M3: the
 // keys padded to a multiple of 128, one block per 128 keys).
 __host__ __device__ inline int kblocks(int kc, bool fp8) { return fp8 ? (kc + 127) / 128 : kc / 64; }
+// Each thread of a warp writes its TMEM lane's N (4..28, a multiple of 4) consecutive
+// 32-bit columns from r, in stores of 16, 8 and 4 columns (warp-collective).
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N % 4 == 0 && N >= 4 && N <= 28, "4 to 28 columns, a multiple of 4");
+  constexpr int o8 = N >= 16 ? 16 : 0;
+  constexpr int o4 = o8 + (N - o8 >= 8 ? 8 : 0);
+  static_assert(N - o4 == 0 || N - o4 == 4, "columns left for the last store");
+  if constexpr (N >= 16) {
+    uint32_t a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = r[i];
+    tmem_st16(taddr, a);
+  }
+  if constexpr (N - o8 >= 8) {
+    uint32_t a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = r[o8 + i];
+    tmem_st8(taddr + o8, a);
+  }
+  if constexpr (N - o4 == 4) {
+    uint32_t a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = r[o4 + i];
+    tmem_st4(taddr + o4, a);
+  }
+}
+
 __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8, int dv) {
   SmemPlan s;
   const size_t eb = fp8 ? 1 : 2;
@@ -170,7 +198,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
   const int nkeys = p.P + p.M;
   const int t0 = split * KC;
   const int nvalid = min(KC, nkeys - t0);
-  constexpr uint32_t ncols = (KC + kDv) <= 256 ? 256u : 512u;
+  // TMEM columns: S = Q K^T [0, KC), O [KC, KC + kDv), P from kPcol0 (the A operand of
+  // P V: two bf16 or four E4M3 probabilities of a row per 32-bit column)
+  constexpr int kPcol0 = KC + kDv;
+  constexpr int kPcols = kF8 ? kKcp / 4 : KC / 2;
+  static_assert(kPcol0 + kPcols <= 512, "S, O and P must fit in tensor memory");
+  constexpr uint32_t ncols = (kPcol0 + kPcols) <= 256 ? 256u : 512u;
   const int rows_per = (kRows + p.nsplit - 1) / p.nsplit;
   const int tile_rows = min(kRows, p.G * p.M - qt * kRows);   // real (head, row) rows of the tile
   // rows [lo, hi) of the band finalised by cluster rank o (empty past the real rows)
@@ -431,49 +464,41 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     ginv = 1.0f / gs;
   }
 
-  // ---- pass 2: P = bf16(exp(s - m_part) * exp(m_part - M) / L) into the swizzled A
-  // operand of P V
+  // ---- pass 2: P = bf16(exp(s - m_part) * exp(m_part - M) / L) into tensor memory,
+  // each thread its row's keys [c0, c0 + kPart): the A operand of P V
   const float fscale = mh > -INFINITY ? exp2f(mh - gmax) * ginv : 0.f;
-  if constexpr (kF8) {
-    // E4M3 probabilities with static scale 1/448: code = E4M3(P * 448), 16 keys per chunk
+  {
+    constexpr int kPc = kF8 ? kPart / 4 : kPart / 2;   // this thread's P columns
+    uint32_t pw[kPc];
+    if constexpr (kF8) {
+      // E4M3 probabilities with static scale 1/448: code = E4M3(P * 448), four keys per column
 #pragma unroll
-    for (int ch = 0; ch < kPart / 16; ++ch) {
-      const int key = c0 + ch * 16;
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int c = 0; c < kPc; ++c) {
         uint32_t packed = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int kk = ch * 16 + q * 4 + e;
-          const float pv = key + q * 4 + e < nvalid ? sv[kk] * fscale : 0.f;
+          const int kk = 4 * c + e;
+          const float pv = c0 + kk < nvalid ? sv[kk] * fscale : 0.f;
           packed |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(pv * 448.0f, __NV_SATFINITE, __NV_E4M3)) << (8 * e);
         }
-        w[q] = packed;
+        pw[c] = packed;
       }
-      st_shared_v4(sPa + (key >> 7) * kTile + swz(r, (key & 127) >> 4), make_uint4(w[0], w[1], w[2], w[3]));
-    }
-    for (int j = part; j < (kKcp - KC) / 16; j += kParts) {   // the zero-padded keys [KC, kKcp)
-      const int key = KC + j * 16;
-      st_shared_v4(sPa + (key >> 7) * kTile + swz(r, (key & 127) >> 4), make_uint4(0, 0, 0, 0));
-    }
-  } else {
+    } else {
 #pragma unroll
-    for (int ch = 0; ch < kPart / 8; ++ch) {   // 8-key chunks of 16 bytes
-      const int key = c0 + ch * 8;
-      float pv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) pv[e] = key + e < nvalid ? sv[ch * 8 + e] * fscale : 0.f;
-      uint4 u;
-      u.x = pack_bf16(pv[0], pv[1]);
-      u.y = pack_bf16(pv[2], pv[3]);
-      u.z = pack_bf16(pv[4], pv[5]);
-      u.w = pack_bf16(pv[6], pv[7]);
-      st_shared_v4(sPa + (key >> 6) * kTile + swz(r, (key & 63) >> 3), u);
+      for (int c = 0; c < kPc; ++c) {
+        const int kk = 2 * c;
+        pw[c] = pack_bf16(c0 + kk < nvalid ? sv[kk] * fscale : 0.f, c0 + kk + 1 < nvalid ? sv[kk + 1] * fscale : 0.f);
+      }
     }
+    tmem_st_cols<kPc>(t_row + static_cast<uint32_t>(kPcol0 + c0 / (kF8 ? 4 : 2)), pw);
+    if constexpr (kF8) {   // the zero-padded keys [KC, kKcp): four columns per 16 keys
+      const uint32_t zero[4] = {0u, 0u, 0u, 0u};
+      for (int j = part; j < (kKcp - KC) / 16; j += kParts)
+        tmem_st4(t_row + static_cast<uint32_t>(kPcol0 + (KC + j * 16) / 4), zero);
+    }
+    tmem_wait_st();
   }
   tc_fence_before();
-  fence_async_smem();
   __syncthreads();
   if (tl_on) tt[9] = global_ns();
 
@@ -485,8 +510,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     for (int b = 0; b < kBlk; ++b) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc_mma<kF8>(tmem + static_cast<uint32_t>(KC), sw128_kmajor_desc(sPa + b * kTile + k * 32),
-                    sw128_kmajor_desc(sVta + b * kTileV + k * 32), idesc, (b | k) ? 1u : 0u);
+        tc_mma_ts<kF8>(tmem + static_cast<uint32_t>(KC), tmem + static_cast<uint32_t>(kPcol0 + b * 32 + k * 8),
+                       sw128_kmajor_desc(sVta + b * kTileV + k * 32), idesc, (b | k) ? 1u : 0u);
     }
     tc_commit(&bar[1]);
   }
