@@ -41,14 +41,16 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 512;        // 16 warps: four per TMEM lane quarter, splitting each row's keys
-constexpr int kParts = kThreads / 128;   // warps (key parts) per TMEM lane quarter
 constexpr int kRows = 128;           // stacked query rows per CTA (MMA M)
 constexpr int kDh = 128;             // head dim
 constexpr int kMaxSplit = 8;         // portable cluster size
-constexpr int kMaxKc = 192;          // keys per slice (MMA N of QK^T), multiple of 64
+constexpr int kMaxKc = 192;          // keys per slice (MMA N of QK^T), multiple of 64, by default
+constexpr int kWideKc = 256;         // the wide slice (bf16, all head dims): fewer slices per cluster
 constexpr int kTile = kRows * 128;   // bytes of one [128 rows][128 B] swizzled block
-static_assert(kThreads % kDh == 0, "whole threads per head-dim row of V^T");
+// Threads of a CTA: warps split each row's keys, four (eight for the wide slice) per
+// TMEM lane quarter, so that every thread keeps at most 48 scores in registers.
+__host__ __device__ constexpr int attn_threads(int kc) { return kc == kWideKc ? 1024 : 512; }
+static_assert(attn_threads(64) % kDh == 0 && attn_threads(kWideKc) % kDh == 0, "whole threads per head-dim row");
 
 struct KParams {
   const __nv_bfloat16* qkv;    // [M][ldq]
@@ -65,6 +67,8 @@ struct KParams {
   const float* s_out;
   int out_fp8;
   int M, P, H, Hkv, G, kc, nsplit;
+  const __nv_bfloat16* vtc;    // the chunk's values transposed [Hkv][Dh][m_pad], or nullptr
+  int m_pad;
   int* err;
   // diagnostic timeline (nullptr = off): entry, after the PDL wait, operands loaded, chunk
   // values transposed, S = Q K^T complete, pass 1 done, cluster peers started, statistics
@@ -134,7 +138,9 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8, int 
   s.k = eb * static_cast<size_t>(kTile);
   s.vt = s.k + static_cast<size_t>(kc) * 128 * eb;
   s.pm = s.vt + static_cast<size_t>(kblocks(kc, fp8)) * dv * 128;
-  const size_t main_end = s.pm + static_cast<size_t>(kblocks(kc, fp8)) * kTile;
+  // the chunk's value rows are staged after V^T before their transpose (the wide slice
+  // gathers them from global memory instead: no room)
+  const size_t main_end = s.pm + (kc == kWideKc ? 0 : static_cast<size_t>(kblocks(kc, fp8)) * kTile);
   const int rows_per = (kRows + nsplit - 1) / nsplit;
   const size_t recv_bytes = static_cast<size_t>(nsplit) * rows_per * dv * 4;
   const size_t stage_bytes = static_cast<size_t>(kRows) * dv * 4;
@@ -155,8 +161,8 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8, int 
     end = s.recv + recv_bytes;
   }
   s.stats = (end + 15) / 16 * 16;                            // [kMaxSplit][128] float2
-  s.part = s.stats + static_cast<size_t>(kMaxSplit) * kRows * 8;   // [kParts][128] float2
-  s.bar = s.part + static_cast<size_t>(kParts) * kRows * 8;
+  s.part = s.stats + static_cast<size_t>(kMaxSplit) * kRows * 8;   // [parts][128] float2
+  s.bar = s.part + static_cast<size_t>(attn_threads(kc) / 128) * kRows * 8;
   s.total = s.bar + 64;
   return s;
 }
@@ -165,7 +171,11 @@ __host__ __device__ inline SmemPlan smem_plan(int kc, int nsplit, bool fp8, int 
 // halves run as two CTAs that repeat S and the softmax (small grids, where the O
 // exchange through distributed shared memory dominates)
 template <int KC, bool kF8, int kDv>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
+__global__ void __launch_bounds__(attn_threads(KC)) attn_kernel(const KParams p) {
+  constexpr int kThreads = attn_threads(KC);
+  constexpr int kParts = kThreads / 128;        // warps (key parts) per TMEM lane quarter
+  constexpr bool kStageV = KC != kWideKc;       // chunk values staged in shared memory (else gathered)
+  static_assert(KC != kWideKc || (!kF8 && kDv == kDh), "the wide slice: bf16, all head dims");
   constexpr int kTileV = kDv * 128;   // bytes of one [kDv rows][128 B] block of V^T
   constexpr int kDsplit = kDh / kDv;
   constexpr int kPart = KC / kParts;            // keys of the slice handled by one thread of a row
@@ -321,8 +331,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     } else {
       const __nv_bfloat16* row = p.qkv + static_cast<size_t>(t - p.P) * p.ldq;
       cp_async16(sKa + (c16 >> 3) * (KC * 128) + swz(t - t0, c16 & 7), row + (p.H + g) * kDh + c16 * 8);
-      cp_async16(sPa + static_cast<uint32_t>(((t - c_lo) * kDh + c16 * 8) * 2),
-                 row + (p.H + p.Hkv + g) * kDh + c16 * 8);
+      if constexpr (kStageV)
+        cp_async16(sPa + static_cast<uint32_t>(((t - c_lo) * kDh + c16 * 8) * 2),
+                   row + (p.H + p.Hkv + g) * kDh + c16 * 8);
     }
   }
   cp_async_commit();
@@ -337,7 +348,72 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const KParams p) {
     // and written back by one 16-byte store
     constexpr int kPer = kF8 ? 16 : 8;   // keys per 16-byte group
     const int g_lo = (c_lo - t0) / kPer, g_hi = (c_hi - 1 - t0) / kPer;
-    for (int idx = tid; idx < (g_hi - g_lo + 1) * kDv; idx += kThreads) {
+    if constexpr (!kStageV) {
+      if (p.vtc) {
+        // wide slice with the chunk's values already transposed: whole aligned groups of
+        // 8 keys by 16-byte asynchronous copies, a straddling group merged key by key;
+        // consecutive threads take consecutive groups of one dim (contiguous sources)
+        const int ngrp = g_hi - g_lo + 1;
+        for (int idx = tid; idx < ngrp * kDv; idx += kThreads) {
+          const int d = idx / ngrp, G = g_lo + idx % ngrp;
+          const int t = t0 + G * 8;
+          const __nv_bfloat16* vrow = p.vtc + static_cast<size_t>(g * kDh + d0 + d) * p.m_pad;
+          const size_t off = static_cast<size_t>(sp.vt) + (G >> 3) * kTileV + swz(d, G & 7);
+          if (t >= c_lo && t + 8 <= c_hi && (t - p.P) % 8 == 0) {
+            cp_async16(base + static_cast<uint32_t>(off), vrow + (t - p.P));
+          } else {
+            uint4* grp = reinterpret_cast<uint4*>(smem + off);
+            uint4 u = *grp;
+            uint16_t* e16 = reinterpret_cast<uint16_t*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (t + e >= c_lo && t + e < c_hi)
+                e16[e] = reinterpret_cast<const uint16_t*>(vrow)[t + e - p.P];
+            *grp = u;
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+      }
+    }
+    if constexpr (!kStageV) if (!p.vtc) {
+      // wide slice: every (group, dim) task of this thread loads its keys' values from
+      // the QKV output first (all loads in flight together, two values per register),
+      // then merges them into the groups
+      constexpr int kTasks = (KC / 8) * kDv / kThreads;
+      const int ntask = (g_hi - g_lo + 1) * kDv;
+      const uint16_t* vbase = reinterpret_cast<const uint16_t*>(p.qkv) + (p.H + p.Hkv + g) * kDh + d0;
+      uint32_t w[kTasks][4];
+#pragma unroll
+      for (int i = 0; i < kTasks; ++i) {
+        const int idx = tid + i * kThreads;
+        const int d = idx % kDv, G = g_lo + idx / kDv;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int t = t0 + G * 8 + e;
+          const uint32_t lo = idx < ntask && t >= c_lo && t < c_hi ? vbase[static_cast<size_t>(t - p.P) * p.ldq + d] : 0u;
+          const uint32_t hi =
+              idx < ntask && t + 1 >= c_lo && t + 1 < c_hi ? vbase[static_cast<size_t>(t + 1 - p.P) * p.ldq + d] : 0u;
+          w[i][e / 2] = lo | (hi << 16);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kTasks; ++i) {
+        const int idx = tid + i * kThreads;
+        if (idx >= ntask) break;
+        const int d = idx % kDv, G = g_lo + idx / kDv;
+        uint4* grp = reinterpret_cast<uint4*>(smem + sp.vt + (G >> 3) * kTileV + swz(d, G & 7));
+        uint4 u = *grp;
+        uint16_t* e16 = reinterpret_cast<uint16_t*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int t = t0 + G * 8 + e;
+          if (t >= c_lo && t < c_hi) e16[e] = static_cast<uint16_t>(w[i][e / 2] >> (16 * (e & 1)));
+        }
+        *grp = u;
+      }
+    }
+    for (int idx = tid; kStageV && idx < (g_hi - g_lo + 1) * kDv; idx += kThreads) {
       const int d = idx % kDv, G = g_lo + idx / kDv;
       uint4* grp = reinterpret_cast<uint4*>(smem + sp.vt + (G >> 3) * kTileV + swz(d, G & 7));
       uint4 u = *grp;
@@ -700,8 +776,74 @@ size_t attn_smem_bytes(int kc, int nsplit, int fp8, int dv) {
 
 namespace {
 
+const void* attn_kernel_for(int kc, bool fp8, int dv) {
+  const bool half = dv == kDh / 2;
+  switch ((kc * 2 + (fp8 ? 1 : 0)) * 2 + (half ? 1 : 0)) {
+    case 256: return reinterpret_cast<const void*>(attn_kernel<64, false, kDh>);
+    case 512: return reinterpret_cast<const void*>(attn_kernel<128, false, kDh>);
+    case 768: return reinterpret_cast<const void*>(attn_kernel<192, false, kDh>);
+    case 1024: return reinterpret_cast<const void*>(attn_kernel<kWideKc, false, kDh>);
+    case 258: return reinterpret_cast<const void*>(attn_kernel<64, true, kDh>);
+    case 514: return reinterpret_cast<const void*>(attn_kernel<128, true, kDh>);
+    case 770: return reinterpret_cast<const void*>(attn_kernel<192, true, kDh>);
+    case 257: return reinterpret_cast<const void*>(attn_kernel<64, false, kDh / 2>);
+    case 513: return reinterpret_cast<const void*>(attn_kernel<128, false, kDh / 2>);
+    case 769: return reinterpret_cast<const void*>(attn_kernel<192, false, kDh / 2>);
+    case 259: return reinterpret_cast<const void*>(attn_kernel<64, true, kDh / 2>);
+    case 515: return reinterpret_cast<const void*>(attn_kernel<128, true, kDh / 2>);
+    case 771: return reinterpret_cast<const void*>(attn_kernel<192, true, kDh / 2>);
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+int attn_clusters_per_wave(int kc, int nsplit, int fp8, int dv) {
+  const void* k = attn_kernel_for(kc, fp8 != 0, dv);
+  if (!k || nsplit < 1 || nsplit > kMaxSplit || attn_configure() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nsplit), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(attn_threads(kc)), 1, 1);
+  cfg.dynamicSmemBytes = attn_smem_bytes(kc, nsplit, fp8, dv);
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = static_cast<unsigned>(nsplit);
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    cudaGetLastError();   // a failed query is not an error of the caller's next call
+    return 0;
+  }
+  return n;
+}
+
+int attn_plan_launch(int M, int P, int G, int Hkv, int fp8, int sms, int* kc, int* nsplit) {
+  const int st = attn_plan(M, P, kc, nsplit);
+  if (st != FM_OK || fp8) return st;
+  const int tiles = (G * M + kRows - 1) / kRows;
+  if (4 * *nsplit * tiles * Hkv <= sms) return FM_OK;   // the small grids (head dims split in two)
+  const int keys = P + M;
+  const int ns_w = (keys + kWideKc - 1) / kWideKc;
+  if (ns_w > kMaxSplit) return FM_OK;
+  // the wide slice when its clusters (fewer CTAs each) need fewer waves of the GPU
+  const int per0 = attn_clusters_per_wave(*kc, *nsplit, 0, kDh), per1 = attn_clusters_per_wave(kWideKc, ns_w, 0, kDh);
+  if (per0 <= 0 || per1 <= 0) return FM_OK;
+  const int clusters = tiles * Hkv;
+  if ((clusters + per1 - 1) / per1 < (clusters + per0 - 1) / per0) {
+    *kc = kWideKc;
+    *nsplit = ns_w;
+  }
+  return FM_OK;
+}
+
+namespace {
+
 cudaError_t attn_configure_impl() {
-  const void* ks[12] = {reinterpret_cast<const void*>(attn_kernel<64, false, kDh>),
+  const void* ks[13] = {reinterpret_cast<const void*>(attn_kernel<kWideKc, false, kDh>),
+                        reinterpret_cast<const void*>(attn_kernel<64, false, kDh>),
                         reinterpret_cast<const void*>(attn_kernel<128, false, kDh>),
                         reinterpret_cast<const void*>(attn_kernel<192, false, kDh>),
                         reinterpret_cast<const void*>(attn_kernel<64, true, kDh>),
@@ -746,6 +888,9 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
   p.G = a.H / a.Hkv;
   p.kc = a.kc;
   p.nsplit = a.nsplit;
+  p.vtc = a.vtc;
+  p.m_pad = a.m_pad;
+  if (a.vtc && (a.m_pad < a.M || a.m_pad % 8)) return cudaErrorInvalidValue;
   p.err = a.err;
   p.tl = o.tl;
   if (a.fp8 && (!a.kpre8 || !a.vtpre8 || !a.s_qkv || a.p16 % 16)) return cudaErrorInvalidValue;
@@ -760,26 +905,28 @@ cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o) {
                                                   cudaSuccess)
       sms = 148;
   }
-  const bool dsplit = 4 * a.nsplit * tiles * a.Hkv <= sms;
+  const bool dsplit = a.kc != kWideKc && 4 * a.nsplit * tiles * a.Hkv <= sms;
   // z: KV head x (with the split) the two halves of the head dims of O
   const dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>(tiles),
                   static_cast<unsigned>(a.Hkv * (dsplit ? 2 : 1)));
   LaunchOpts lo = o;
   lo.cluster = dim3(static_cast<unsigned>(a.nsplit), 1, 1);
   const size_t smem = attn_smem_bytes(a.kc, a.nsplit, a.fp8, dsplit ? kDh / 2 : kDh);
+  const dim3 blk(static_cast<unsigned>(attn_threads(a.kc)));
   switch ((a.kc * 2 + (a.fp8 ? 1 : 0)) * 2 + (dsplit ? 1 : 0)) {
-    case 256: return launch(attn_kernel<64, false, kDh>, grid, dim3(kThreads), smem, lo, p);
-    case 512: return launch(attn_kernel<128, false, kDh>, grid, dim3(kThreads), smem, lo, p);
-    case 768: return launch(attn_kernel<192, false, kDh>, grid, dim3(kThreads), smem, lo, p);
-    case 258: return launch(attn_kernel<64, true, kDh>, grid, dim3(kThreads), smem, lo, p);
-    case 514: return launch(attn_kernel<128, true, kDh>, grid, dim3(kThreads), smem, lo, p);
-    case 770: return launch(attn_kernel<192, true, kDh>, grid, dim3(kThreads), smem, lo, p);
-    case 257: return launch(attn_kernel<64, false, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
-    case 513: return launch(attn_kernel<128, false, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
-    case 769: return launch(attn_kernel<192, false, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
-    case 259: return launch(attn_kernel<64, true, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
-    case 515: return launch(attn_kernel<128, true, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
-    case 771: return launch(attn_kernel<192, true, kDh / 2>, grid, dim3(kThreads), smem, lo, p);
+    case 256: return launch(attn_kernel<64, false, kDh>, grid, blk, smem, lo, p);
+    case 512: return launch(attn_kernel<128, false, kDh>, grid, blk, smem, lo, p);
+    case 768: return launch(attn_kernel<192, false, kDh>, grid, blk, smem, lo, p);
+    case 1024: return launch(attn_kernel<kWideKc, false, kDh>, grid, blk, smem, lo, p);
+    case 258: return launch(attn_kernel<64, true, kDh>, grid, blk, smem, lo, p);
+    case 514: return launch(attn_kernel<128, true, kDh>, grid, blk, smem, lo, p);
+    case 770: return launch(attn_kernel<192, true, kDh>, grid, blk, smem, lo, p);
+    case 257: return launch(attn_kernel<64, false, kDh / 2>, grid, blk, smem, lo, p);
+    case 513: return launch(attn_kernel<128, false, kDh / 2>, grid, blk, smem, lo, p);
+    case 769: return launch(attn_kernel<192, false, kDh / 2>, grid, blk, smem, lo, p);
+    case 259: return launch(attn_kernel<64, true, kDh / 2>, grid, blk, smem, lo, p);
+    case 515: return launch(attn_kernel<128, true, kDh / 2>, grid, blk, smem, lo, p);
+    case 771: return launch(attn_kernel<192, true, kDh / 2>, grid, blk, smem, lo, p);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -190,8 +190,10 @@ cudaError_t pack_weight(const float* w, const float* gamma, int N, int K, int fm
 constexpr int kQFp8AsF16 = 2;
 constexpr int kQNvfp4AsF16 = 3;
 // y[m][n] = bf16(sum_j planes[j][m][n] * fp32(sa * sw)) for s K-slice planes [s][M][N].
+// With vt (nullable) the columns n >= nv0 (the values V) are also written transposed:
+// vt[(n - nv0) * m_pad + m] (m_pad: M rounded up to 8), the chunk's V^T attention reads.
 cudaError_t qkv_finalize_launch(const float* planes, int s, int M, int N, const float* sa, const float* sw,
-                                __nv_bfloat16* out, const LaunchOpts& o);
+                                __nv_bfloat16* out, __nv_bfloat16* vt, int nv0, int m_pad, const LaunchOpts& o);
 struct RowArgs {
   int M, N;
   // residual update from GEMM partials: x += gate * (sum_p parts[p] * fp32(sa*sw) + bias)
@@ -264,9 +266,20 @@ struct AttnArgs {
   const uint8_t* vtpre8 = nullptr;   // [Hkv][Dh][p16] of this layer
   int p16 = 0;                       // P rounded up to a multiple of 16
   const float* s_qkv = nullptr;
+  // the chunk's values transposed [Hkv][Dh][m_pad] (bf16 attention; nullable: the wide
+  // slice then gathers them from qkv)
+  const __nv_bfloat16* vtc = nullptr;
+  int m_pad = 0;
 };
 // Slice plan for P + M keys; FM_ERR_SHAPE when they need more than 8 x 192.
 int attn_plan(int M, int P, int* kc, int* nsplit);
+// attn_plan, then (bf16 attention on grids too large for the split head dims) the wide
+// slice of 256 keys when its clusters need fewer waves of the GPU (device occupancy
+// query; without a device the default plan). G: query heads per KV head.
+int attn_plan_launch(int M, int P, int G, int Hkv, int fp8, int sms, int* kc, int* nsplit);
+// Clusters of the attention kernel for (kc, nsplit, fp8, dv) resident at once; 0 when
+// the query fails.
+int attn_clusters_per_wave(int kc, int nsplit, int fp8, int dv);
 size_t attn_smem_bytes(int kc, int nsplit, int fp8, int dv);   // dv: head dims of O per CTA
 cudaError_t attn_launch(const AttnArgs& a, const LaunchOpts& o);
 cudaError_t attn_configure();

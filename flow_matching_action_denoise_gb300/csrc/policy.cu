@@ -51,6 +51,7 @@ struct Layout {
   size_t shared_end = 0;
   std::vector<size_t> wpk;   // [L*4] packed weights
   size_t wscale, ascale, mod, modf, w_in, b_in, w_out, b_out, gamma_f, kcache, vcache, a, x, q, o, q2, mc;
+  size_t vtc;    // NVFP4: the chunk's values transposed [Hkv][Dh][M rounded up to 8] (bf16)
   size_t qkvb;   // bf16 Q | K | V the attention reads (== y[0] unless NVFP4 reduces planes separately;
                  // E4M3 codes with FP8 attention)
   size_t kcache8, vcache8;   // FP8 attention: E4M3 copies of the prefix cache
@@ -200,7 +201,8 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
       }
       memset(&dv->gs[g], 0, sizeof(fm::GemmShape));
     }
-    if (fm::attn_plan(c->M, c->P, &dv->attn_kc, &dv->attn_nsplit) != FM_OK) {
+    if (fm::attn_plan_launch(c->M, c->P, c->H / c->Hkv, c->Hkv, dv->attn_fp8, num_sms(), &dv->attn_kc,
+                             &dv->attn_nsplit) != FM_OK) {
       *why = "P + M keys exceed the attention plan's 8 slices x 192 keys";
       return FM_ERR_SHAPE;
     }
@@ -229,7 +231,8 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
       return st;
     }
   }
-  if (fm::attn_plan(c->M, c->P, &dv->attn_kc, &dv->attn_nsplit) != FM_OK) {
+  if (fm::attn_plan_launch(c->M, c->P, c->H / c->Hkv, c->Hkv, dv->attn_fp8, num_sms(), &dv->attn_kc,
+                           &dv->attn_nsplit) != FM_OK) {
     *why = "P + M keys exceed the attention plan's 8 slices x 192 keys";
     return FM_ERR_SHAPE;
   }
@@ -316,6 +319,7 @@ Layout make_layout(const fm_config* c, const Derived& dv) {
                       (g == 0 && !dv.nvfp4) ? static_cast<size_t>(M) * dv.gN[0] * 2   // dequantised bf16 Q|K|V
                                             : static_cast<size_t>(dv.nparts(g)) * M * dv.gN[g] * 4);
   ly.qkvb = dv.nvfp4 ? ly.take(static_cast<size_t>(M) * dv.gN[0] * 2) : ly.y[0];
+  ly.vtc = dv.nvfp4 ? ly.take(static_cast<size_t>(c->Hkv) * c->Dh * ((M + 7) / 8 * 8) * 2) : 0;
   ly.kv8_bytes = dv.attn_fp8 ? static_cast<size_t>(L) * c->P * c->Hkv * c->Dh : 0;
   ly.v8_bytes = dv.attn_fp8 ? static_cast<size_t>(L) * c->Hkv * c->Dh * ((c->P + 15) / 16 * 16) : 0;
   ly.kcache8 = ly.take(ly.kv8_bytes);
@@ -492,7 +496,7 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
                               nullptr, err, o);
     if (e != cudaSuccess) return e;
     e = fm::qkv_finalize_launch(y[0], dv.ns[0].s, c.M, dv.gN[0], p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), qkvb,
-                                o);
+                                p->at<__nv_bfloat16>(p->ly.vtc), (c.H + c.Hkv) * c.Dh, (c.M + 7) / 8 * 8, o);
   } else if (dv.attn_fp8) {   // E4M3 Q | K | V codes with their static scales
     e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 0]), p->tmA[0], dv.gs[0], nullptr, err, o, nullptr,
                         p->ascale(l, FM_SITE_ATTN_IN), p->wscale(l, 0), nullptr, 0, nullptr,
@@ -522,6 +526,10 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
   at.Hkv = c.Hkv;
   at.kc = dv.attn_kc;
   at.nsplit = dv.attn_nsplit;
+  if (dv.nvfp4) {
+    at.vtc = p->at<__nv_bfloat16>(p->ly.vtc);
+    at.m_pad = (c.M + 7) / 8 * 8;
+  }
   if (dv.attn_fp8) {
     const int p16 = (c.P + 15) / 16 * 16;
     at.fp8 = 1;

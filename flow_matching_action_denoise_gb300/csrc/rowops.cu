@@ -414,10 +414,12 @@ __global__ void quant_e4m3_kernel(const float* __restrict__ x, int64_t n, float 
 
 namespace {
 
-// y[m][n] = bf16(sum_j planes[j][m][n] * fp32(sa * sw)), slices summed in order j = 0..s-1.
+// y[m][n] = bf16(sum_j planes[j][m][n] * fp32(sa * sw)), slices summed in order j = 0..s-1;
+// with vt, columns n >= nv0 also go to vt[(n - nv0) * m_pad + m].
 __global__ void __launch_bounds__(256) qkv_finalize_kernel(const float* __restrict__ planes, int s, size_t n4,
                                                            const float* __restrict__ sa,
-                                                           const float* __restrict__ sw, __nv_bfloat16* out) {
+                                                           const float* __restrict__ sw, __nv_bfloat16* out,
+                                                           __nv_bfloat16* vt, int N, int nv0, int m_pad) {
   pdl_trigger();
   const float ds = __fmul_rn(*sa, *sw);
   pdl_wait();
@@ -437,16 +439,26 @@ __global__ void __launch_bounds__(256) qkv_finalize_kernel(const float* __restri
     u.x = *reinterpret_cast<const uint32_t*>(&lo);
     u.y = *reinterpret_cast<const uint32_t*>(&hi);
     reinterpret_cast<uint2*>(out)[i] = u;
+    const int n = static_cast<int>((i * 4) % static_cast<size_t>(N));
+    if (vt && n >= nv0) {   // N and nv0 are multiples of 4: the quad lies in the V columns
+      const size_t m = (i * 4) / static_cast<size_t>(N);
+      __nv_bfloat16* col = vt + static_cast<size_t>(n - nv0) * m_pad + m;
+      col[0] = __low2bfloat16(lo);
+      col[m_pad] = __high2bfloat16(lo);
+      col[2 * static_cast<size_t>(m_pad)] = __low2bfloat16(hi);
+      col[3 * static_cast<size_t>(m_pad)] = __high2bfloat16(hi);
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t qkv_finalize_launch(const float* planes, int s, int M, int N, const float* sa, const float* sw,
-                                __nv_bfloat16* out, const LaunchOpts& o) {
+                                __nv_bfloat16* out, __nv_bfloat16* vt, int nv0, int m_pad, const LaunchOpts& o) {
+  if (N % 4 || (vt && (nv0 % 4 || nv0 < 0 || nv0 > N || m_pad < M))) return cudaErrorInvalidValue;
   const size_t n4 = static_cast<size_t>(M) * N / 4;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n4 + 255) / 256, 1216));
-  return launch(qkv_finalize_kernel, dim3(blocks), dim3(256), 0, o, planes, s, n4, sa, sw, out);
+  return launch(qkv_finalize_kernel, dim3(blocks), dim3(256), 0, o, planes, s, n4, sa, sw, out, vt, N, nv0, m_pad);
 }
 
 cudaError_t row_launch(const RowArgs& r, const LaunchOpts& o) {
