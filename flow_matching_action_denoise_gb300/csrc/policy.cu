@@ -115,6 +115,19 @@ int auto_split(int tiles, int nkb) {
   return nkb;
 }
 
+// auto_split for a GEMM whose CTAs take a whole SM (the NVFP4 kernel's shared memory):
+// the grid is kept to one wave, the largest such split when auto_split's would spill
+// over (measured: the W4A8 QKV GEMM at split 8, 160 CTAs, took two waves, 13.7 us per
+// layer-step; at split 4, 80 CTAs, 9.4 us).
+int auto_split_one_wave(int tiles, int nkb) {
+  int s = auto_split(tiles, nkb);
+  while (s > 1 && tiles * s > num_sms()) {
+    --s;
+    while (s > 1 && nkb % s) --s;
+  }
+  return s;
+}
+
 int cluster_for(int s) {
   int c = 8;
   while (c > 1 && s % c) c >>= 1;
@@ -187,7 +200,7 @@ int derive(const fm_config* c, Derived* dv, std::string* why) {
       dv->gN[g] = N[g];
       dv->gK[g] = K[g];
       const int nkb = K[g] / 64;
-      int s = c->ksplit[g] > 0 ? c->ksplit[g] : (g == 2 ? 1 : auto_split(N[g] / 128, nkb));
+      int s = c->ksplit[g] > 0 ? c->ksplit[g] : (g == 2 ? 1 : auto_split_one_wave(N[g] / 128, nkb));
       if (g == 2 && s != 1) {
         *why = "with NVFP4 weights the gate|up GEMM cannot be K-split (its epilogue applies GeGLU)";
         return FM_ERR_SHAPE;
