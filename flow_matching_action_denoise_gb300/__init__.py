@@ -45,7 +45,7 @@ EXPORTS = [
     "fm_philox_noise", "fm_decode_actions_seeded", "fm_last_timing", "fm_decode_warm", "fm_episode_reset",
     "fm_session_workspace_size", "fm_session_create", "fm_session_fork", "fm_abi_sizes", "fm_standalone_status",
     "fm_warm_trace_size", "fm_decode_warm_trace", "fm_test_launch_kernel", "fm_decode_timeline",
-    "fm_test_skinny_gemm_tile", "fm_test_pdl_chain", "fm_test_grid_barrier",
+    "fm_test_skinny_gemm_tile", "fm_test_pdl_chain", "fm_test_grid_barrier", "fm_test_attn_plan",
 ]
 
 
@@ -143,6 +143,7 @@ def load() -> ctypes.CDLL:
         "fm_session_fork": (i, [vp, vp, sz, i, vp, sz, vp, ctypes.POINTER(vp)]),
         "fm_test_pdl_chain": (i, [i, i, i, i, i, i, i, vp, sz, ctypes.POINTER(ctypes.c_float)]),
         "fm_test_grid_barrier": (i, [i, i, i, i, ctypes.c_ulonglong, vp, vp, vp]),
+        "fm_test_attn_plan": (i, [vp, ctypes.POINTER(i), ctypes.POINTER(i)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -418,6 +419,13 @@ def parse_timeline(raw) -> list:
 def kernel_count(p: int):
     a, b = ctypes.c_int(), ctypes.c_int()
     _check(load().fm_test_kernel_count(p, ctypes.byref(a), ctypes.byref(b)), "fm_test_kernel_count", p)
+    return a.value, b.value
+
+
+def attn_plan(p: int):
+    """(keys per slice, slices) of the policy's attention."""
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(load().fm_test_attn_plan(p, ctypes.byref(a), ctypes.byref(b)), "fm_test_attn_plan", p)
     return a.value, b.value
 
 

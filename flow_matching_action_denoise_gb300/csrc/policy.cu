@@ -1590,6 +1590,13 @@ int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision) 
   return FM_OK;
 }
 
+int fm_test_attn_plan(const fm_policy* p, int* keys_per_slice, int* slices) {
+  if (!p || !keys_per_slice || !slices) return fail(nullptr, FM_ERR_INVALID_ARG, "NULL argument");
+  *keys_per_slice = p->dv.attn_kc;
+  *slices = p->dv.attn_nsplit;
+  return FM_OK;
+}
+
 int fm_test_quant_e4m3(const float* x, int64_t n, float scale, uint8_t* codes, void* stream) {
   if (!x || !codes || n < 0) return fail(nullptr, FM_ERR_INVALID_ARG, "bad argument");
   if (!(scale > 0.f)) return fail(nullptr, FM_ERR_INVALID_ARG, "scale must be positive");

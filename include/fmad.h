@@ -405,6 +405,10 @@ int fm_decode_timeline(fm_policy* p, const float* noise, float* actions, void* b
 /* Kernel launches per decoder layer and per decision of the captured plan. */
 int fm_test_kernel_count(const fm_policy* p, int* per_layer, int* per_decision);
 
+/* The attention plan of the policy: keys per slice (one CTA's share of the P + M keys;
+ * 64, 128, 192, or 256 for the wide slice) and slices (the cluster size). */
+int fm_test_attn_plan(const fm_policy* p, int* keys_per_slice, int* slices);
+
 /* Launch only kernel `index` (0 .. per_layer - 1, in the decision's order: FP8/BF16
  * QKV GEMM, attention, O GEMM, consumer, gate|up GEMM + GeGLU, down GEMM, consumer or
  * step boundary) of layer `layer` at Euler step `step`, with exactly the arguments and

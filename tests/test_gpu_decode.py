@@ -128,6 +128,8 @@ def test_decision_fp8_end_to_end_within_oracle_envelope(expert):
         err = np.max(np.abs(got - ref)) / np.sqrt(np.mean(ref ** 2))
         assert err <= 2 * env, (flags, err, env)
         assert fmad.kernel_count(pol.handle) == counts
+        # 838 keys in 7 slices of 128 (the small grid splits O's head dims; no wide slice)
+        assert fmad.attn_plan(pol.handle) == (128, 7)
         pol.close()
 
 

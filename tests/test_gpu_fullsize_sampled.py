@@ -42,6 +42,9 @@ def test_full_decision_sampled_layer_steps(name):
     pol = fmad.Policy(cfg, act_scales=scales, weights=weights)
     pol.set_prefix_kv(dev(kp, device, torch.bfloat16), dev(vp, device, torch.bfloat16))
     assert fmad.kernel_count(pol.handle) == (8, 1 + L * S * 8)
+    # 16 row tiles x 2 KV heads of 1280 keys: 7-CTA clusters take three waves of 152
+    # SMs, the wide slice's 5-CTA clusters two
+    assert fmad.attn_plan(pol.handle) == (256, 5)
     nbytes = fmad.trace_size(pol.handle)
     trace = torch.empty(nbytes, dtype=torch.uint8, device=device)
     nz = fm_synth.noise(cfg, 0)
