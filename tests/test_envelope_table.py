@@ -1,9 +1,9 @@
 """The oracle's envelope tables (tests/golden/envelope_table_*.txt, written by
 make_envelope_table.py from the oracle alone) are present and well formed, and the
-end-to-end bound selection of test_gpu_northstar.py picks at least one depth (CPU)."""
+end-to-end bound selection of test_gpu_end_to_end_bounds.py picks at least one depth (CPU)."""
 import numpy as np
 
-from test_gpu_northstar import BOUNDS, envelope_table, resolvable_depths
+from test_gpu_end_to_end_bounds import BOUNDS, envelope_table, resolvable_depths
 
 
 def test_tables_cover_every_depth_and_grow_with_it():

@@ -50,7 +50,7 @@ CASES = [(name, L, S) for name in BOUNDS for L, S in resolvable_depths(name)]
 
 
 @pytest.mark.parametrize("name,L,S", CASES)
-def test_decision_within_north_star_bound(name, L, S):
+def test_decision_within_end_to_end_bound(name, L, S):
     device = require_gpu()
     base = fm_synth.config(name)
     cfg = dataclasses.replace(base, L=L, S=S)
