@@ -57,7 +57,7 @@ typedef enum fm_status {
   FM_ERR_CUDA = 5,            /* a CUDA runtime call failed; see fm_last_error() */
   FM_ERR_STATE_MISMATCH = 6,  /* capsule from another plan, policy or address */
   FM_ERR_DEVICE = 7,          /* a kernel gave up a bounded wait and set the error word */
-  FM_ERR_UNSUPPORTED = 8      /* valid request this build does not implement */
+  FM_ERR_UNSUPPORTED = 8      /* valid request this library does not implement */
 } fm_status;
 
 typedef enum fm_format {
