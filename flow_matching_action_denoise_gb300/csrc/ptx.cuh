@@ -272,9 +272,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // ---------------------------------------------------------------- clusters
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Split cluster barrier: arrive early (relaxed: orders nothing), wait later. Used
 // to know every peer CTA has started before writing into its shared memory.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -339,9 +336,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t dst, float a, float b, uint
                ::"r"(dst), "f"(a), "f"(b), "r"(mbar)
                : "memory");
 }
-__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -352,21 +346,6 @@ __device__ __forceinline__ uint32_t map_dsmem(uint32_t saddr, uint32_t rank) {
   uint32_t out;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(rank));
   return out;
-}
-// Distributed-shared-memory loads. Volatile keeps them after the cluster barrier
-// (volatile asm statements are not reordered among themselves); no memory clobber,
-// so a caller that issues several loads before using any gets them in flight together.
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
 }
 
 // ---------------------------------------------------------------- timeline (diagnostics)
