@@ -57,6 +57,8 @@ struct KParams {
   int M, N;
   int nkb_total, nkb_cta;
   int n_pad, stages, cs, chunk;
+  const uint8_t* pf;   // a range to prefetch into L2 (each CTA its share), or nullptr
+  size_t pf_bytes;
   int* err;
   // kMode 1 (residual epilogue; cs == s): x[m][n] += gate[n] * (sum * fp32(sa * sw)) for the
   // rows and columns this CTA finalises, and ssq[nt][m] = the tile's sum of x_new^2.
@@ -87,6 +89,17 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 // 128-row tile; plain placement only), which halves the partial bytes each CTA of a
 // K-split cluster pushes to its peers. With M = 64 the accumulator's row r sits in TMEM
 // lane 32 (r / 16) + r % 16: lanes 0-15 of each warp's lane quarter.
+// This CTA's share of the L2 prefetch range (16-byte units; a grid-wide split).
+__device__ __forceinline__ void l2_prefetch_share(const KParams& p) {
+  if (!p.pf) return;
+  const size_t nct = static_cast<size_t>(gridDim.x) * gridDim.y;
+  const size_t cta = static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+  const size_t share = ((p.pf_bytes / 16 + nct - 1) / nct) * 16;
+  const size_t lo = cta * share, hi = lo + share < p.pf_bytes ? lo + share : p.pf_bytes;
+  for (size_t a = lo; a < hi; a += 65536)
+    l2_prefetch_bulk(p.pf + a, static_cast<uint32_t>(hi - a < 65536 ? hi - a : 65536));
+}
+
 template <bool kFp8, int kCs, int kMode, int kTm = kTileN>
 __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                const KParams p) {
@@ -175,6 +188,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       bulk_load(w_tiles + static_cast<size_t>(i) * w_stage_bytes, wsrc + static_cast<size_t>(i) * w_stage_bytes,
                 w_stage_bytes, &full[i], pol_w);
     }
+    l2_prefetch_share(p);   // after this CTA's own weights
     s_issued = nst;
   } else if (kMode != 2 && threadIdx.x == 0) {
     // ---------------- producer: per stage one bulk copy of chunk weight tiles (contiguous
@@ -202,6 +216,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
       mbar_arrive_expect_tx(&full[i], tx);
       load_w(i, i);
     }
+    l2_prefetch_share(p);   // after this CTA's own weights
     pdl_wait();   // activations are written by the previous kernel
     if (tl_on) tt[1] = global_ns();
     for (int i = 0; i < pre; ++i)
@@ -798,7 +813,10 @@ cudaError_t gemm_configure() { return configure_once(0, gemm_configure_impl); }
 cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape& g, float* out, int* err,
                         const LaunchOpts& o, __nv_bfloat16* out_bf16, const float* sa, const float* sw,
                         void* out_geglu, int geglu_fp8, const float* sq, uint8_t* out_qkv8, const float* s_qkv,
-                        int nq, int nk, const GemmFuse* fuse) {
+                        int nq, int nk, const GemmFuse* fuse, const void* l2_prefetch,
+                        size_t l2_prefetch_bytes) {
+  if (l2_prefetch && (reinterpret_cast<uintptr_t>(l2_prefetch) % 16 || l2_prefetch_bytes % 16))
+    return cudaErrorInvalidValue;
   if ((out_bf16 || out_geglu || out_qkv8) && (g.cs != g.s || !sa || !sw)) return cudaErrorInvalidValue;
   if (out_qkv8 && (!s_qkv || nq % 128 || nk % 128)) return cudaErrorInvalidValue;
   if (out_geglu && (!sq || g.N % 128)) return cudaErrorInvalidValue;
@@ -823,6 +841,8 @@ cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape
   p.stages = g.stages;
   p.cs = g.cs;
   p.chunk = g.chunk;
+  p.pf = static_cast<const uint8_t*>(l2_prefetch);
+  p.pf_bytes = l2_prefetch ? l2_prefetch_bytes : 0;
   p.err = err;
   const int mode = fuse ? fuse->mode : 0;
   p.x = fuse ? fuse->x : nullptr;

@@ -126,7 +126,11 @@ cudaError_t gemm_launch(const void* wpk, const CUtensorMap& tmA, const GemmShape
                         const LaunchOpts& o, __nv_bfloat16* out_bf16 = nullptr, const float* sa = nullptr,
                         const float* sw = nullptr, void* out_geglu = nullptr, int geglu_fp8 = 0,
                         const float* sq = nullptr, uint8_t* out_qkv8 = nullptr, const float* s_qkv = nullptr,
-                        int nq = 0, int nk = 0, const GemmFuse* fuse = nullptr);
+                        int nq = 0, int nk = 0, const GemmFuse* fuse = nullptr,
+                        const void* l2_prefetch = nullptr, size_t l2_prefetch_bytes = 0);
+// l2_prefetch (16-byte aligned, bytes a multiple of 16): a range the kernel's CTAs
+// prefetch into L2 once their own weight copies are issued, each its share (the next
+// GEMM's weights, for CTAs of that GEMM that cannot be resident early).
 cudaError_t gemm_configure();   // one-time function attributes (shared memory, clusters)
 
 // ---------------------------------------------------------------- O GEMM + consumer

@@ -612,9 +612,15 @@ cudaError_t enqueue_layer(fm_policy* p, int l, int k, bool step_end, const Launc
                               p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->ascale(l, FM_SITE_GEGLU), err, o,
                               dv.act4);
   else
+    // the gate|up GEMM's CTAs (two per SM) leave no room for most of the down GEMM's,
+    // which then start late: with BF16 weights they find theirs in L2, prefetched here
+    // after each CTA's own weight copies (FP8 down weights are half the bytes and come
+    // in time without it; there the prefetch only adds traffic)
     e = fm::gemm_launch(p->at<void>(p->ly.wpk[l * 4 + 2]), p->tmA[2], dv.gs[2], nullptr, err, o, nullptr,
                         p->ascale(l, FM_SITE_MLP_IN), p->wscale(l, 2), p->at<void>(p->ly.mc), fp8,
-                        p->ascale(l, FM_SITE_GEGLU), nullptr, nullptr, 0, 0, dv.rowfuse ? &fg : nullptr);
+                        p->ascale(l, FM_SITE_GEGLU), nullptr, nullptr, 0, 0, dv.rowfuse ? &fg : nullptr,
+                        c.weight_fmt == FM_FMT_BF16 ? p->at<void>(p->ly.wpk[l * 4 + 3]) : nullptr,
+                        c.weight_fmt == FM_FMT_BF16 ? fm::packed_weight_bytes(dv.gN[3], dv.gK[3], c.weight_fmt) : 0);
   if (e != cudaSuccess) return e;
   if (dv.rowfuse) FM_REC(p->at<void>(p->ly.q2), static_cast<size_t>(c.M) * c.d * ab);
   FM_REC(p->at<void>(p->ly.mc), static_cast<size_t>(c.M) * c.F * ab);
