@@ -144,3 +144,37 @@ def test_attention_plan_limits_are_validated(lib):
     with pytest.raises(fmad.FmError) as e:
         fmad.workspace_size(bad)
     assert e.value.status == 2 and "attention plan" in str(e.value)
+
+
+def test_handoff_diagnostics_validate_without_a_gpu(lib):
+    # host addresses stand in for device buffers: every call below is rejected before
+    # any CUDA call, and the alignment case needs a pointer that is not 16-byte aligned
+    buf = ctypes.create_string_buffer(4096 + 16)
+    base = (ctypes.addressof(buf) + 15) // 16 * 16
+    out = ctypes.c_ulonglong()
+    us = ctypes.c_float()
+    gb = lib.fm_test_grid_barrier
+    assert gb(4, 128, 10, 0, 10**6, None, ctypes.byref(out), None) == 1          # NULL scratch
+    assert gb(4, 128, 10, 0, 10**6, base, None, None) == 1                       # NULL result
+    assert gb(0, 128, 10, 0, 10**6, base, ctypes.byref(out), None) == 2          # no CTAs
+    assert gb(4, 100, 10, 0, 10**6, base, ctypes.byref(out), None) == 2          # threads not a warp multiple
+    assert gb(4, 128, 10, 3, 10**6, base, ctypes.byref(out), None) == 2          # unknown mode
+    assert gb(4, 128, 10, 0, 10, base, ctypes.byref(out), None) == 2             # wait budget under 1 us
+    assert gb(4, 128, 10, 0, 10**6, base + 4, ctypes.byref(out), None) == 3      # scratch misaligned
+    pc = lib.fm_test_pdl_chain
+    assert pc(8, 128, 4, 2, 1, 1, 0, None, 4096, ctypes.byref(us)) == 1          # NULL scratch
+    assert pc(8, 128, 4, 2, 1, 1, 0, base, 4096, None) == 1                      # NULL result
+    assert pc(8, 128, 4, 2, 1, 3, 0, base, 4096, ctypes.byref(us)) == 2          # cluster not a power of two
+    assert pc(6, 128, 4, 2, 1, 4, 0, base, 4096, ctypes.byref(us)) == 2          # CTAs not whole clusters
+    assert pc(8, 128, 0, 2, 1, 1, 0, base, 4096, ctypes.byref(us)) == 2          # no kernels
+    assert pc(8, 128, 4, 2, 1, 1, 65, base, 4096, ctypes.byref(us)) == 2         # too many writes per thread
+    # 8 CTAs x 128 threads x 1 write needs 4 * (1 + 1024) bytes
+    assert pc(8, 128, 4, 2, 1, 1, 1, base, 4 * 1025 - 1, ctypes.byref(us)) == 4
+
+
+def test_policy_diagnostics_reject_a_null_policy(lib):
+    a, b = ctypes.c_int(-1), ctypes.c_int(-1)
+    assert lib.fm_test_attn_plan(None, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert (a.value, b.value) == (-1, -1)   # outputs untouched on error
+    assert lib.fm_test_launch_kernel(None, 0, 0, 0, None) == 1
+    assert lib.fm_standalone_status(None, None) == 1
