@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(attn_threads(KC)) attn_kernel(const KParams p)
 #pragma unroll
     for (int q = 0; q < kParts; ++q) {
       const float2 st = sPart[q * kRows + r];
-      l += st.y > 0.f ? st.y * exp2f(st.x - m) : 0.f;
+      l += st.y > 0.f ? st.y * ex2_approx(st.x - m) : 0.f;
     }
     const uint32_t rank = cluster_rank();
     const uint32_t off = smem_u32(sStats + rank * kRows + r);
@@ -523,7 +523,10 @@ __global__ void __launch_bounds__(attn_threads(KC)) attn_kernel(const KParams p)
   }
   if (tl_on) tt[8] = global_ns();
   // the row's global max and 1 / sum in slice order, by every thread of the row (the
-  // same operations in the same order in each, so no hand-off through shared memory)
+  // same operations in the same order in each, so no hand-off through shared memory);
+  // its rescaling exponentials, like pass 1's, by the approximate 2^x: they only feed
+  // probabilities rounded to bf16 or E4M3 (the accurate exp2f kept this phase 0.2 us
+  // longer per layer-step)
   float gmax, ginv;
   {
     float2 st[kMaxSplit];
@@ -535,14 +538,14 @@ __global__ void __launch_bounds__(attn_threads(KC)) attn_kernel(const KParams p)
     float gs = 0.f;
 #pragma unroll
     for (int q = 0; q < kMaxSplit; ++q)
-      if (q < p.nsplit) gs += st[q].y * exp2f(st[q].x - gm);
+      if (q < p.nsplit) gs += st[q].y * ex2_approx(st[q].x - gm);
     gmax = gm;
     ginv = 1.0f / gs;
   }
 
   // ---- pass 2: P = bf16(exp(s - m_part) * exp(m_part - M) / L) into tensor memory,
   // each thread its row's keys [c0, c0 + kPart): the A operand of P V
-  const float fscale = mh > -INFINITY ? exp2f(mh - gmax) * ginv : 0.f;
+  const float fscale = mh > -INFINITY ? ex2_approx(mh - gmax) * ginv : 0.f;
   {
     constexpr int kPc = kF8 ? kPart / 4 : kPart / 2;   // this thread's P columns
     uint32_t pw[kPc];
@@ -604,7 +607,8 @@ __global__ void __launch_bounds__(attn_threads(KC)) attn_kernel(const KParams p)
   // gives each thread one row, so the share is first staged row-major in shared
   // memory (16-byte chunks swizzled by row: conflict-free); then one bulk copy per
   // band moves the band's rows into the owner's receive slot for this rank, counted
-  // on the owner's mbarrier.
+  // on the owner's mbarrier (one lane per band issues its copy: a single thread
+  // issuing them in turn took twice as long).
   {
     constexpr int kCols = kDv / kParts;   // O columns read by one thread
     constexpr int kRowBytes = kDv * 4;    // one staged row of this CTA's O share
@@ -623,19 +627,18 @@ __global__ void __launch_bounds__(attn_threads(KC)) attn_kernel(const KParams p)
     }
     fence_async_smem();   // the staged rows -> the bulk copies' reads
     __syncthreads();
-    if (tid == 0) {
-      const uint32_t rank = cluster_rank();
-      const uint32_t slot = smem_u32(recv + static_cast<size_t>(rank) * rows_per * kDv);
-      for (int o = 0; o < p.nsplit; ++o) {
-        int lo, hi;
-        band(o, lo, hi);
-        if (hi > lo)
-          bulk_copy_to_peer(map_dsmem(slot, static_cast<uint32_t>(o)), stage + static_cast<uint32_t>(lo * kRowBytes),
-                            static_cast<uint32_t>((hi - lo) * kRowBytes),
-                            map_dsmem(smem_u32(&bar[3]), static_cast<uint32_t>(o)));
-      }
-      if (tl_on) tt[11] = global_ns();
+    static_assert(kThreads / 32 >= kMaxSplit, "a warp for every band");
+    if (lane == 0 && warp < p.nsplit) {   // band o's copy issued by warp o (in parallel)
+      const int o = warp;
+      const uint32_t slot = smem_u32(recv + static_cast<size_t>(cluster_rank()) * rows_per * kDv);
+      int lo, hi;
+      band(o, lo, hi);
+      if (hi > lo)
+        bulk_copy_to_peer(map_dsmem(slot, static_cast<uint32_t>(o)), stage + static_cast<uint32_t>(lo * kRowBytes),
+                          static_cast<uint32_t>((hi - lo) * kRowBytes),
+                          map_dsmem(smem_u32(&bar[3]), static_cast<uint32_t>(o)));
     }
+    if (tl_on) tt[11] = global_ns();
   }
   if (!mbar_wait(&bar[3], 0)) {   // every slice's share of this CTA's band has landed
     atomicOr(p.err, kErrPipelineTimeout);
