@@ -100,6 +100,14 @@ __device__ __forceinline__ void l2_prefetch_share(const KParams& p) {
     l2_prefetch_bulk(p.pf + a, static_cast<uint32_t>(hi - a < 65536 ? hi - a : 65536));
 }
 
+// Output rows are finalised in four-row groups: cluster rank o owns the groups
+// g = o (mod cs) of the M rows (as its local group g / cs), so a lane's four
+// consecutive accumulator columns (activation rows 4g..4g+3 of its weight row) go to
+// one owner in one 16-byte store, and consecutive groups to different owners. The
+// receive buffer is [slot][owned group][weight row][4 rows]: the 32 lanes of a warp
+// (consecutive weight rows, one group) fill 512 contiguous bytes of one owner.
+__host__ __device__ inline int owner_groups(int M, int cs) { return ((M + 3) / 4 + cs - 1) / cs; }
+
 template <bool kFp8, int kCs, int kMode, int kTm = kTileN>
 __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                const KParams p) {
@@ -109,6 +117,9 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
   __shared__ int s_abort;
   __shared__ int s_issued;
+  // placement with the consumer inside (kMode 1): per owned row, the sums of squares of
+  // the tile's four 32-row slabs (at most 256 rows per rank)
+  __shared__ float s_ssq[kMode == 1 ? 4 : 1][kMode == 1 ? 256 : 1];
 
   const int stages = p.stages;
   const int chunk = p.chunk;
@@ -118,10 +129,11 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   uint8_t* w_tiles = smem;
   uint8_t* a_tiles = smem + static_cast<size_t>(stages) * w_stage_bytes;
   const size_t main_bytes = static_cast<size_t>(stages) * (w_stage_bytes + a_stage_bytes);
-  const int rows_per = (p.M + kCs - 1) / kCs;   // output rows each cluster rank finalises
-  float* recv = reinterpret_cast<float*>(smem + align_up(main_bytes, 1024));   // [kCs][rows_per][kTm]
+  const int groups = (p.M + 3) / 4;              // four-row groups holding a real row
+  const int g_per = owner_groups(p.M, kCs);      // groups each cluster rank finalises
+  float* recv = reinterpret_cast<float*>(smem + align_up(main_bytes, 1024));   // [kCs][g_per][kTm][4]
   uint8_t* ctrl = reinterpret_cast<uint8_t*>(recv) +
-                  align_up(static_cast<size_t>(kCs) * rows_per * kTm * sizeof(float), 1024);
+                  align_up(static_cast<size_t>(kCs) * g_per * kTm * 4 * sizeof(float), 1024);
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
@@ -149,10 +161,10 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     mbar_init(done, 1);
     mbar_init(recvd, 1);
     fence_mbar_init();
-    if (kCs > 1) {   // every rank sends 128 fp32 columns of each row m = rank (mod kCs), m < M
+    if (kCs > 1) {   // every rank sends each of its kTm weight rows' 16 bytes of every owned group
       const int rk = static_cast<int>(cluster_rank());
-      const int owned = rk < p.M ? (p.M - 1 - rk) / kCs + 1 : 0;
-      mbar_arrive_expect_tx(recvd, static_cast<uint32_t>(kCs * owned * kTm * 4));
+      const int owned = rk < groups ? (groups - 1 - rk) / kCs + 1 : 0;
+      mbar_arrive_expect_tx(recvd, static_cast<uint32_t>(kCs * owned * kTm * 16));
     }
     if (kMode != 2) tma_prefetch_desc(&tmA);
   }
@@ -357,12 +369,13 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
     tc_commit(done);
   }
 
-  // ---------------- epilogue. Output row m belongs to cluster rank m mod cs, as its
-  // local row m / cs. Each CTA pushes its fp32 partial of every row into the
-  // owner's receive buffer (slot = its own rank) with 16-byte remote shared-memory
-  // stores counted on the owner's mbarrier; each owner then sums its rows over the
-  // cs slots in slice order and writes them with 16-byte stores. With cs == 1 the
-  // push is a local shared-memory store.
+  // ---------------- epilogue. Each CTA pushes its fp32 partials into the owners'
+  // receive buffers (slot = its own rank): a lane holds one weight row's accumulator
+  // columns, i.e. consecutive activation rows, so each group of four goes out as one
+  // 16-byte remote shared-memory store counted on the owner's mbarrier. Each owner
+  // then sums its groups over the cs slots in slice order, turns each 4 x 4 block
+  // (four weight rows of four activation rows) around by lane shuffles and writes
+  // its rows with 16-byte stores. With cs == 1 the push is a local store.
   pdl_wait();
   if (!mbar_wait(done, 0)) {
     atomicOr(p.err, kErrPipelineTimeout);
@@ -382,33 +395,19 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const uint32_t recv_base = smem_u32(recv);
   if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
   __syncwarp();                  // tcgen05.ld and the shuffles are warp-collective
-  // Partial rows leave as 16-byte stores: each aligned group of four lanes (four
-  // consecutive weight rows n0..n0+3) transposes its 4 x 4 blocks, after which lane t4
-  // holds columns n0..n0+3 of activation row c + 4b + t4. That row's owner,
-  // (4b + t4) mod cs (c is a multiple of 16 and cs divides 16), is fixed per lane and b.
-  // (One remote store per warp costs about the same whatever its width, so four
-  // columns per lane take a quarter of the scalar stores' time.)
-  const int t4 = lane & 3;
-  const int n0 = n_local - t4;
-  uint32_t dst_b[4], bar_b[4];
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint32_t q = static_cast<uint32_t>((4 * b + t4) % kCs);
-    dst_b[b] = (kCs > 1 ? map_dsmem(recv_base, q) : recv_base) +
-               static_cast<uint32_t>((rank * rows_per * kTm + n0) * 4);
-    bar_b[b] = kCs > 1 ? map_dsmem(smem_u32(recvd), q) : 0u;
-  }
+  const uint32_t recvd_addr = smem_u32(recvd);
   for (int c = colset * 16; c < p.n_pad; c += 32) {
     float v[16];
     tmem_ld16(t_row + static_cast<uint32_t>(c), v);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      transpose4x4(v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3], t4);
-      const int r = c + 4 * b + t4;   // activation row; the owner's local row is r / cs
-      if (r < p.M && lane_has_row) {
-        const uint32_t addr = dst_b[b] + static_cast<uint32_t>((r / kCs) * kTm * 4);
+      const int g = (c >> 2) + b;   // activation rows 4g..4g+3 (rows past M hold zeros)
+      if (g < groups && lane_has_row) {
+        const int o = g % kCs, lg = g / kCs;   // owner rank and its local group
+        const uint32_t addr = recv_base + static_cast<uint32_t>((((rank * g_per + lg) * kTm) + n_local) * 16);
         if (kCs > 1)   // counted on the owner's mbarrier
-          st_async_v4(addr, v[4 * b], v[4 * b + 1], v[4 * b + 2], v[4 * b + 3], bar_b[b]);
+          st_async_v4(map_dsmem(addr, static_cast<uint32_t>(o)), v[4 * b], v[4 * b + 1], v[4 * b + 2],
+                      v[4 * b + 3], map_dsmem(recvd_addr, static_cast<uint32_t>(o)));
         else
           st_shared_v4(addr, make_uint4(__float_as_uint(v[4 * b]), __float_as_uint(v[4 * b + 1]),
                                         __float_as_uint(v[4 * b + 2]), __float_as_uint(v[4 * b + 3])));
@@ -427,22 +426,53 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   if (tl_on) tt[4] = global_ns();
   if (!abort) {
     const int part = j / kCs;
-    // kTm / 4 lanes per row, four columns each (64-row tiles: two rows per warp)
-    constexpr int kLanesRow = kTm / 4;
-    const int c4 = (lane % kLanesRow) * 4;
-    const size_t col = static_cast<size_t>(nt) * kTm + c4;
-    for (int lr = warp * (32 / kLanesRow) + lane / kLanesRow; lr < rows_per; lr += kThreads / kLanesRow) {
-      const int m = lr * kCs + rank;
-      if (m >= p.M) break;
+    const int owned = rank < groups ? (groups - 1 - rank) / kCs + 1 : 0;
+    const bool residual = kMode == 1 && !p.out_geglu && !p.out_qkv8 && !p.out_bf16;
+    // thread <-> (weight row n of the tile, owned group lg); kTm * owned is a multiple of
+    // 64, so every warp runs the same number of trips (the shuffles need all lanes)
+    for (int idx = threadIdx.x; idx < kTm * owned; idx += kThreads) {
+      const int n = idx % kTm, lg = idx / kTm;
+      const float* src = recv + (lg * kTm + n) * 4;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < kCs; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(recv + (q * rows_per + lr) * kTm + c4);
+      for (int q = 0; q < kCs; ++q) {   // slices in order
+        const float4 v = *reinterpret_cast<const float4*>(src + q * g_per * kTm * 4);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
         acc.w += v.w;
       }
+      // lanes 4k..4k+3 hold weight rows n0..n0+3 of the same four activation rows; after
+      // the transpose lane t4 holds activation row 4g + t4, columns n0..n0+3
+      const int t4 = n & 3;
+      transpose4x4(acc.x, acc.y, acc.z, acc.w, t4);
+      const int m = 4 * (lg * kCs + rank) + t4;
+      const int c4 = n - t4;
+      const size_t col = static_cast<size_t>(nt) * kTm + c4;
+      if constexpr (kMode == 1) {
+        if (residual) {
+          // gated residual on the finished sum, and this warp's share of the row's sum
+          // of squares (lanes t4, t4 + 4, ..., t4 + 28: its 32 weight rows)
+          float ssq = 0.f;
+          if (m < p.M) {
+            const float4 g = *reinterpret_cast<const float4*>(p.gate + col);
+            float4* xp = reinterpret_cast<float4*>(p.x + static_cast<size_t>(m) * p.N + col);
+            float4 xv = *xp;
+            xv.x = fmaf(g.x, acc.x * ds, xv.x);
+            xv.y = fmaf(g.y, acc.y * ds, xv.y);
+            xv.z = fmaf(g.z, acc.z * ds, xv.z);
+            xv.w = fmaf(g.w, acc.w * ds, xv.w);
+            *xp = xv;
+            ssq = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
+          }
+          ssq += __shfl_xor_sync(0xffffffffu, ssq, 4);
+          ssq += __shfl_xor_sync(0xffffffffu, ssq, 8);
+          ssq += __shfl_xor_sync(0xffffffffu, ssq, 16);
+          if (lane < 4) s_ssq[n >> 5][4 * lg + t4] = ssq;
+          continue;
+        }
+      }
+      if (m >= p.M) continue;
       if (p.out_geglu) {
         // the four columns are (gate, up) of GeGLU columns 2L and 2L+1 of this tile's 64:
         // m = gelu_tanh(g) * u, quantised
@@ -480,22 +510,18 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
         u.x = *reinterpret_cast<const uint32_t*>(&lo);
         u.y = *reinterpret_cast<const uint32_t*>(&hi);
         *reinterpret_cast<uint2*>(p.out_bf16 + static_cast<size_t>(m) * p.N + col) = u;
-      } else if (kMode == 1) {
-        // gated residual on the finished sum, and this tile's share of the row's sum of squares
-        const float4 g = *reinterpret_cast<const float4*>(p.gate + col);
-        float4* xp = reinterpret_cast<float4*>(p.x + static_cast<size_t>(m) * p.N + col);
-        float4 xv = *xp;
-        xv.x = fmaf(g.x, acc.x * ds, xv.x);
-        xv.y = fmaf(g.y, acc.y * ds, xv.y);
-        xv.z = fmaf(g.z, acc.z * ds, xv.z);
-        xv.w = fmaf(g.w, acc.w * ds, xv.w);
-        *xp = xv;
-        float ssq = xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-        if (lane == 0) p.ssq[static_cast<size_t>(nt) * p.M + m] = ssq;
       } else {
         *reinterpret_cast<float4*>(p.out + (static_cast<size_t>(part) * p.M + m) * p.N + col) = acc;
+      }
+    }
+    if constexpr (kMode == 1) {
+      if (residual) {   // the row's sum of squares over the tile: its four 32-row slabs in order
+        __syncthreads();
+        for (int lr = threadIdx.x; lr < 4 * owned; lr += kThreads) {
+          const int m = 4 * ((lr >> 2) * kCs + rank) + (lr & 3);
+          if (m < p.M)
+            p.ssq[static_cast<size_t>(nt) * p.M + m] = ((s_ssq[0][lr] + s_ssq[1][lr]) + s_ssq[2][lr]) + s_ssq[3][lr];
+        }
       }
     }
   }
@@ -674,8 +700,8 @@ int gemm_plan(int M, int N, int K, int fp8, int s, int cs, GemmShape* g, int til
   g->tile = tile;
   const size_t block_bytes =
       static_cast<size_t>(tile) * kBlockBytes + static_cast<size_t>(g->n_pad) * kBlockBytes;   // one K block
-  const int rows_per = (M + cs - 1) / cs;
-  const size_t recv_bytes = align_up(static_cast<size_t>(cs) * rows_per * tile * sizeof(float), 1024);
+  const size_t recv_bytes =
+      align_up(static_cast<size_t>(cs) * owner_groups(M, cs) * tile * 4 * sizeof(float), 1024);
   if (recv_bytes + block_bytes > kStageCap) return FM_ERR_SHAPE;
   // chunk: the largest divisor of nkb_cta up to 4 whose double-buffered ring fits (or a
   // single stage holding all of the CTA's K blocks)
