@@ -16,6 +16,7 @@ method) on this host's cores, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -47,6 +48,13 @@ def algorithmic_bytes(cfg) -> dict:
     total = cfg.S * cfg.L * (w_layer + kv_layer) + mod + io
     return {"weights": cfg.S * cfg.L * w_layer, "kv": cfg.S * cfg.L * kv_layer, "mod": mod, "io": io,
             "total": total}
+
+
+def layer_bytes(cfg) -> int:
+    """Bytes one layer-step must move at least once: its packed weights, its prefix
+    K/V and its own modulation rows (the single-layer protocol's unit)."""
+    ab = algorithmic_bytes(dataclasses.replace(cfg, L=1, S=1))
+    return int(ab["weights"] + ab["kv"] + 6 * cfg.d * 4)
 
 
 def algorithmic_flops(cfg) -> dict:
@@ -330,7 +338,6 @@ def run_ours(args, rank, world, local_rank):
 def time_warm_start(cfg, weights, scales, k_dev, v_dev, noise, device, stream, args):
     """The one-step warm start (warm_t = 0.5, 3 actions executed) against the full
     decision, on a policy created with that flow time (CUDA events)."""
-    import dataclasses
     import torch
     import flow_matching_action_denoise_gb300 as fmad
     if weights is None:
@@ -393,7 +400,6 @@ def time_decision_gemm(cfg, scales, device, index=None):
     as they do in the decision. The same without programmatic dependent launch (each
     launch starts after the previous one has finished) is reported as `no_pdl`.
     Algorithmic bytes per launch: weights N K + activations M K + GeGLU codes M N / 2."""
-    import dataclasses
     import torch
     import flow_matching_action_denoise_gb300 as fmad
 
@@ -560,7 +566,6 @@ def oracle_layer_steps_ms(cfg, n_layers: int, n_steps: int) -> float:
     n_layers layers of `cfg` (weights prepared outside the timing), in ms per
     layer-step."""
     from oracle import model as O
-    import dataclasses
     sub = dataclasses.replace(cfg, L=n_layers)
     layers = [fm_synth.layer_weights(sub, l) for l in range(n_layers)]
     conds = fm_synth.step_conds(sub) if sub.cond == "given" else None
@@ -655,7 +660,6 @@ def run_reference(args, rank, world):
     cfg = fm_synth.config(args.workload)
     big = cfg.M * cfg.d > 100_000
     n_layers = min(cfg.L, 2) if big else cfg.L
-    import dataclasses
     sub = dataclasses.replace(cfg, L=n_layers)
     layers = [fm_synth.layer_weights(sub, l) for l in range(n_layers)]
     model = O.Model(sub, layers, fm_synth.final_weights(sub))
@@ -818,8 +822,7 @@ def run_layer_protocol(args):
     fmad.load()
     base = fm_synth.config("layer_fp8_m10")
     layer = fm_synth.layer_weights(base, 0)
-    ab = algorithmic_bytes(base)
-    per_layer = ab["weights"] + ab["kv"] + base.S * 6 * base.d * 4   # weights, prefix KV, the layer's modulation
+    per_layer = layer_bytes(base)
     R = int(np.ceil(2 * l2_bytes(device) / per_layer)) + 1
     cfg = fm_synth.config("layer_fp8_m10", L=R)
     conds = fm_synth.step_conds(cfg)
