@@ -198,13 +198,18 @@ int fm_abi_sizes(size_t* config, size_t* weights, size_t* layer_weights, size_t*
  * may then be NULL) and,
  * with FM_FLAG_USE_GRAPH, captures the whole decision as one CUDA graph.
  * Synchronises `stream` before returning. The prefix cache starts zeroed.
- * On failure nothing is leaked and *out is NULL. */
+ * On failure nothing is leaked and *out is NULL.
+ * Source: blog post "Embodied inference acceleration", sections "CUDA Graph vs graph
+ * simplification" (gamma fold, graph replay) and "Static quantisation" (static
+ * scales); news article "FlashRT-PAI", section "It optimises the relay" (the plan
+ * and its named persistent buffers). */
 int policy_create(const fm_config* cfg, const fm_weights* w, const float* act_scales,
                   void* workspace, size_t ws_bytes, void* stream, fm_policy** out);
 
 /* Release the host-side policy or session (graphs, plan). Does not touch the
  * workspace. The caller must not destroy a policy with work in flight on its
- * stream; a base policy with live sessions is not destroyed (FM_ERR_INVALID_ARG). */
+ * stream; a base policy with live sessions is not destroyed (FM_ERR_INVALID_ARG).
+ * Source: news article "FlashRT-PAI", section "It optimises the relay". */
 int policy_destroy(fm_policy* p);
 
 /* Replace the static activation scales (host [L][4] fp32, [L][7] with FP8
@@ -214,19 +219,26 @@ int policy_destroy(fm_policy* p);
 int fm_set_act_scales(fm_policy* p, const float* act_scales, void* stream);
 
 /* Overwrite the whole prefix KV cache: k, v device bf16 [L][P][Hkv][Dh]. With
- * FP8 attention the cache's E4M3 copy (static K and V scales) is derived here. */
+ * FP8 attention the cache's E4M3 copy (static K and V scales) is derived here.
+ * Source: news article "FlashRT-PAI", section "It optimises the relay" (the prefix
+ * state reused across decisions). */
 int set_prefix_kv(fm_policy* p, const uint16_t* k, const uint16_t* v, void* stream);
 
 /* Overwrite rows [tok_begin, tok_end) of every layer's prefix K and V (the
  * image-dependent part after a new observation); other rows persist.
- * k, v: device bf16 [L][tok_end - tok_begin][Hkv][Dh]. 0 <= begin < end <= P. */
+ * k, v: device bf16 [L][tok_end - tok_begin][Hkv][Dh]. 0 <= begin < end <= P.
+ * Source: news article "FlashRT-PAI", section "It optimises the relay" (selective
+ * refresh of the image-dependent state). */
 int refresh_prefix(fm_policy* p, int tok_begin, int tok_end, const uint16_t* k,
                    const uint16_t* v, void* stream);
 
 /* One decision: S Euler steps from the noise (t = 1) to the action chunk (t = 0).
  * noise: device fp32 [M][A], or NULL to start from the policy's noise/action
  * buffer as it stands (e.g. after restore_state). actions: device fp32 [M][A]
- * (may equal noise). Asynchronous. */
+ * (may equal noise). Asynchronous.
+ * Source: blog post "Embodied inference acceleration", section "Static
+ * quantisation" (18 layers x 10 denoise steps); news article "FlashRT-PAI", section
+ * "It optimises the relay" (one graph, Programmatic Dependent Launch). */
 int decode_actions(fm_policy* p, const float* noise, float* actions, void* stream);
 
 /* Same as decode_actions with HOST buffers (pinned recommended): copies the
@@ -283,12 +295,16 @@ int fm_last_timing(fm_policy* p, fm_timing* t, void* stream);
 int fm_state_size(const fm_policy* p, size_t* bytes);
 
 /* Copy the policy's persistent state into dst (host if dst_on_device == 0, else
- * device), stream-ordered; host copies synchronise the stream. */
+ * device), stream-ordered; host copies synchronise the stream.
+ * Source: news article "FlashRT-PAI", section "It optimises the relay"
+ * (execution-state capsules). */
 int snapshot_state(fm_policy* p, void* dst, size_t bytes, int dst_on_device, void* stream);
 
 /* Restore a capsule made by snapshot_state of THIS policy (same plan hash,
  * workspace address and shapes); otherwise FM_ERR_STATE_MISMATCH and nothing is
- * written. Capsules are in-process only, bound to the plan and device addresses. */
+ * written. Capsules are in-process only, bound to the plan and device addresses.
+ * Source: news article "FlashRT-PAI", section "It optimises the relay" (capsules
+ * bound to the plan and device addresses). */
 int restore_state(fm_policy* p, const void* src, size_t bytes, int src_on_device, void* stream);
 
 /* Sessions (paper, "execution-state capsules" for snapshot, restore and fork of the
