@@ -14,10 +14,10 @@
 // operand, packed pre-swizzled so a plain bulk copy lands them in the MMA layout -
 // in one copy of chunk x 16 KB, the activations in one 3-D box of chunk K blocks.
 // One elected thread issues the TMA loads, another issues tcgen05.mma into a
-// TMEM accumulator; four warps read TMEM back. CTAs (n-tile, slice j) of
-// consecutive slices form a thread-block cluster of size cs that sums its
-// partials in fixed slice order through distributed shared memory, so only
-// s/cs partial planes go to global memory (deterministic, no atomics).
+// TMEM accumulator; eight warps (two per TMEM lane quarter) read it back. CTAs
+// (n-tile, slice j) of consecutive slices form a thread-block cluster of size cs
+// that sums its partials in fixed slice order through distributed shared memory,
+// so only s/cs partial planes go to global memory (deterministic, no atomics).
 // Weight loads are issued before the programmatic-dependent-launch wait: they do
 // not depend on the previous kernel, so they overlap its tail.
 
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads) skinny_gemm_kernel(const __grid_cons
   const int rank = kCs > 1 ? static_cast<int>(cluster_rank()) : 0;
   const uint32_t recv_base = smem_u32(recv);
   if (kCs > 1) cluster_wait();   // every peer has started: its receive buffer exists
-  __syncwarp();                  // tcgen05.ld and the shuffles are warp-collective
+  __syncwarp();                  // tcgen05.ld is warp-collective
   const uint32_t recvd_addr = smem_u32(recvd);
   for (int c = colset * 16; c < p.n_pad; c += 32) {
     float v[16];
