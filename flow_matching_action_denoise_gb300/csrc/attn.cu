@@ -11,22 +11,23 @@
 // Work layout. The G = H/Hkv query heads sharing a KV head are stacked into rows
 // r = h_local * M + m. A CTA owns a tile of 128 stacked rows and one contiguous
 // slice of the keys; the slices of a row tile form a thread-block cluster. Both
-// contractions run on tcgen05 tensor cores with bf16 operands in shared memory
-// (K-major, 128-byte swizzle, the layout TMA writes) and fp32 accumulators in
-// TMEM: S = Q K^T (M = 128 rows, N = slice keys, K = 128 head dims), then
-// O = P V (N = 64 head dims, K = slice keys) with V held transposed: the two halves
-// of the head dims of O are two CTAs that compute the same S and softmax, so each
-// stages, exchanges and sums half the O bytes (the exchange is bound by distributed
-// shared memory bandwidth, the duplicated S and exponentials by nothing: they run
-// on otherwise idle SMs). Four warps
-// share each TMEM lane quarter (32 rows) and split the slice's keys, so the softmax
-// needs no shuffles: pass 1 reads S, takes each row part's max m_h and keeps
-// exp(s - m_h) in registers with its sum; the cluster exchanges the (max, sum)
-// pairs through distributed shared memory so every CTA normalises with the global
-// max M and sum L; pass 2 forms P = exp(s - m_h) * exp(m_h - M) / L, rounds it to
-// bf16 and writes the swizzled operand. Each slice pushes its share of O into the
-// shared memory of the CTA that finalises those rows, which sums the shares in
-// fixed slice order and quantises with the static output scale.
+// contractions run on tcgen05 tensor cores with fp32 accumulators in TMEM:
+// S = Q K^T (M = 128 rows, N = slice keys, K = 128 head dims) from bf16 (or E4M3)
+// operands in shared memory (K-major, 128-byte swizzle, the layout TMA writes),
+// then O = P V (N = head dims of O, K = slice keys) with P read from tensor memory
+// and V held transposed in shared memory. On small grids the two halves of the
+// head dims of O are two CTAs that compute the same S and softmax, so each
+// exchanges and sums half the O bytes (the duplicated S and exponentials run on
+// otherwise idle SMs). Four warps (eight in the 256-key wide slice) share each
+// TMEM lane quarter (32 rows) and split the slice's keys, so the softmax needs no
+// shuffles: pass 1 reads S, takes each row part's max m_h and keeps exp(s - m_h)
+// in registers with its sum; the cluster exchanges the (max, sum) pairs through
+// distributed shared memory so every CTA normalises with the global max M and
+// sum L; pass 2 forms P = exp(s - m_h) * exp(m_h - M) / L, rounds it to bf16 (or
+// E4M3) and writes it into tensor memory. Each slice pushes its share of O
+// (staged, then one bulk copy per band) into the shared memory of the CTA that
+// finalises those rows, which sums the shares in fixed slice order and quantises
+// with the static output scale.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
