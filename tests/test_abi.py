@@ -178,3 +178,46 @@ def test_policy_diagnostics_reject_a_null_policy(lib):
     assert (a.value, b.value) == (-1, -1)   # outputs untouched on error
     assert lib.fm_test_launch_kernel(None, 0, 0, 0, None) == 1
     assert lib.fm_standalone_status(None, None) == 1
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("act_fmt", fmad.FMT_BF16, 1),      # FP8 weights with bf16 activations: no such pair
+    ("attn_fmt", fmad.FMT_NVFP4, 1),    # attention runs in bf16 or E4M3 only
+    ("cond_mode", 7, 1),
+    ("Dh", 64, 2),                      # the kernels are built for 128-dim heads
+    ("Hkv", 3, 2),                      # 8 query heads do not share 3 KV heads evenly
+    ("d", 1000, 2),                     # not a multiple of 128
+    ("F", 4100, 2),
+    ("A", 33, 2),
+    ("M", 0, 2),
+    ("rms_eps", 0.0, 1),
+])
+def test_config_preconditions(lib, field, value, status):
+    cfg = fmad.make_config(fm_synth.config("expert_fp8_m50"))
+    setattr(cfg, field, value)
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(cfg)
+    assert e.value.status == status
+
+
+def test_unsupported_mode_combinations_and_splits(lib):
+    # E4M3 attention is built for FP8 weights and activations only
+    cfg = fmad.make_config(fm_synth.config("expert_bf16_m63"))
+    cfg.attn_fmt = fmad.FMT_FP8
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(cfg)
+    assert e.value.status == 8
+    # the QKV and gate|up GEMMs reduce every K slice inside one cluster (at most 8)
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(fmad.make_config(fm_synth.config("expert_fp8_m50"), ksplit=(16, 0, 0, 0)))
+    assert e.value.status == 2 and "1, 2, 4 or 8" in str(e.value)
+    # a split must divide the K blocks: the down GEMM's K = 4096 holds 32 FP8 blocks
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(fmad.make_config(fm_synth.config("expert_fp8_m50"), ksplit=(0, 0, 0, 5)))
+    assert e.value.status == 2
+    # with NVFP4 weights the gate|up GEMM applies GeGLU itself and keeps its whole K
+    with pytest.raises(fmad.FmError) as e:
+        fmad.workspace_size(fmad.make_config(fm_synth.config("wam_nvfp4_m256"), ksplit=(0, 0, 2, 0)))
+    assert e.value.status == 2 and "GeGLU" in str(e.value)
+    # the accepted splits still size a workspace
+    assert fmad.workspace_size(fmad.make_config(fm_synth.config("expert_fp8_m50"), ksplit=(4, 4, 2, 8))) > 0
